@@ -1,0 +1,238 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify, the batched verify step of greedy
+ * (lossless) speculative decoding with an MTP / NextN draft head, for GB300
+ * (sm_103a).
+ *
+ * One verify step, for B branches with k draft tokens each (R = B*(k+1) rows,
+ * row r = b*(k+1)+j sits at position p = pos[b]+j):
+ *
+ *   spec_kv_append      write the k+1 new K/V rows of every branch in place
+ *   spec_verify_attn    causal GQA attention of the R rows over their pages
+ *   spec_lmhead_argmax  logits = hidden . W^T with a fused per-row argmax
+ *   spec_accept         greedy chain acceptance
+ *   spec_mtp_input      the draft head's input  fc([rmsnorm(E[tok]), rmsnorm(h)])
+ *
+ * The method follows the span-02 page `engine/crates/model/src/spec.rs`
+ * (module documentation and `Spec::body_inner`): draft chain, ONE batched
+ * verify forward of B(k+1) rows with the KV appended in place at pos..pos+k,
+ * greedy acceptance, and rollback by advancing `pos` only.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer named as "device" is a device pointer owned by the caller;
+ *    the library never allocates, frees or retains one past the call.
+ *    `spec_kv_desc` itself is a HOST struct that is read during the call only.
+ *  - Every call is asynchronous and ordered on `stream` (a cudaStream_t; 0 is
+ *    the legacy default stream). No call synchronises the device or the host.
+ *  - Return value: SPEC_OK (0) or a negative SPEC_ERR_* code. Host-side
+ *    argument errors are found before any launch, in which case nothing was
+ *    enqueued. `spec_strerror` names a code. The library never prints and
+ *    never aborts.
+ *  - Device-side errors (a bad page id, a position the page table does not
+ *    cover, a token id outside the vocabulary, a d2t entry outside the target
+ *    vocabulary, a bounded wait that gave up) are reported through an
+ *    optional `dev_err` device word: the kernel ORs a SPEC_DEVERR_* bit into
+ *    it with an atomic and skips the offending write. It never traps. The
+ *    caller zeroes the word and reads it at its own synchronisation point.
+ *  - bf16 means IEEE bfloat16 stored as 2 bytes; all matrices are row-major.
+ *
+ * KV pool layout (one of each for K and V):
+ *    pool[num_pages][n_kv_heads][page_size][head_dim]
+ *  so that one (page, kv head) block of page_size*head_dim elements is one
+ *  contiguous run. Element type: bf16 (kv_dtype 0) or FP8 E4M3 codes
+ *  (kv_dtype 1, one byte each) with fp32 dequantisation scales
+ *  scale[num_pages][n_kv_heads]; value = decode(code) * scale.
+ *  The page table is int32 [B][max_pages]; position p of branch b lives in
+ *  page page_table[b*max_pages + p/page_size], slot p % page_size
+ *  (span-02 spec.rs, `SpecReq`: "its KV slot is page pages[pos/16]").
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so that the header needs no CUDA include. */
+typedef struct CUstream_st *spec_stream_t;
+
+/* ---- status codes --------------------------------------------------------------- */
+#define SPEC_OK               0
+#define SPEC_ERR_NULL        -1  /* a required pointer is NULL                           */
+#define SPEC_ERR_ARG         -2  /* a size or count is out of range                      */
+#define SPEC_ERR_UNSUPPORTED -3  /* valid but not implemented (e.g. head_dim 96)         */
+#define SPEC_ERR_WORKSPACE   -4  /* workspace pointer NULL or smaller than required     */
+#define SPEC_ERR_CUDA        -5  /* a CUDA runtime call failed (launch, attribute, ...)  */
+#define SPEC_ERR_ALIGN       -6  /* a pointer or row stride breaks a 16-byte alignment  */
+
+/* ---- device error bits (OR-ed into *dev_err) ------------------------------------- */
+#define SPEC_DEVERR_PAGE     1   /* page id outside [0, num_pages)                      */
+#define SPEC_DEVERR_COVER    2   /* position p with p/page_size >= max_pages            */
+#define SPEC_DEVERR_TOKEN    4   /* token id outside [0, V)                             */
+#define SPEC_DEVERR_D2T      8   /* d2t entry outside [0, d2t_limit)                    */
+#define SPEC_DEVERR_POS      16  /* pos[b] < 0, or pos[b]+k+1 > max_pos                 */
+#define SPEC_DEVERR_TIMEOUT  32  /* a bounded pipeline wait gave up (results invalid)   */
+
+/* ---- limits ------------------------------------------------------------------------ */
+#define SPEC_KMAX            15  /* k <= 15: at most 16 verify rows per branch          */
+#define SPEC_KV_BF16         0
+#define SPEC_KV_FP8_E4M3     1
+
+/* Paged KV pool shared by all branches (span-02 spec.rs, module documentation: the
+ * branches verify "over the branches' own pages" of the scheduler's SHARED pool). */
+typedef struct {
+    void *k_pool;              /* device, [num_pages][n_kv_heads][page_size][head_dim]   */
+    void *v_pool;              /* device, same layout                                    */
+    const float *k_scale;      /* device, [num_pages][n_kv_heads] fp32; FP8 only else NULL */
+    const float *v_scale;      /* device, same                                           */
+    const int32_t *page_table; /* device, [B][max_pages] page ids (unused entries: -1)    */
+    int32_t num_pages;         /* pages in the pool                                      */
+    int32_t max_pages;         /* page-table row width                                   */
+    int32_t page_size;         /* slots per page: a power of two, 1..1024                */
+    int32_t n_kv_heads;        /* Hkv >= 1                                                */
+    int32_t head_dim;          /* d in {64, 128, 256}                                     */
+    int32_t kv_dtype;          /* SPEC_KV_BF16 or SPEC_KV_FP8_E4M3                         */
+} spec_kv_desc;
+
+/* Name of a status code (static string, never NULL). */
+const char *spec_strerror(int status);
+
+/* Library ABI version (major*100 + minor). */
+int spec_version(void);
+
+/* ---- a1: KV append ----------------------------------------------------------------
+ * Writes, for every branch b and j = 0..k, the new K/V row of verify row
+ * r = b*(k+1)+j into position p = pos[b]+j of branch b's pages.
+ * Source: span-02 spec.rs, module documentation ("KV appended in place at
+ * pos..pos+k"); memra-engine spec.rs, `full_attn_verify` (append of the T
+ * verify tokens before the attention).
+ *   pos     device int32 [B]: position of each branch's first verify row, i.e.
+ *           the number of committed tokens already in the pool.
+ *   k_new,
+ *   v_new   device bf16 [B*(k+1)][n_kv_heads][head_dim], 16-byte aligned.
+ * bf16 pools: a bit copy. FP8 pools: code = e4m3_rn_satfinite(float(x) / scale)
+ * with an IEEE fp32 division and the page's (page, kv head) scale.
+ * Host errors: NULL pointers, B < 1, k outside [0, SPEC_KMAX], bad descriptor.
+ * Device errors: SPEC_DEVERR_PAGE, SPEC_DEVERR_COVER, SPEC_DEVERR_POS (pos < 0);
+ * the offending row is skipped. dev_err may be NULL (errors then go unreported). */
+int spec_kv_append(const spec_kv_desc *kv, const int32_t *pos, int B, int k,
+                   const void *k_new, const void *v_new, int32_t *dev_err,
+                   spec_stream_t stream);
+
+/* General form of the append: n_rows rows, row i goes to branch row_branch[i]
+ * (a page-table row) at position row_pos[i]. Used to fill a context (prefill
+ * writes its KV the same way) and by spec_kv_append.
+ *   row_branch, row_pos  device int32 [n_rows]
+ *   k_rows, v_rows       device bf16 [n_rows][n_kv_heads][head_dim]
+ * Errors as spec_kv_append. n_rows == 0 is a no-op. */
+int spec_kv_write_rows(const spec_kv_desc *kv, const int32_t *row_branch,
+                       const int32_t *row_pos, int n_rows, const void *k_rows,
+                       const void *v_rows, int32_t *dev_err, spec_stream_t stream);
+
+/* ---- a2: verify attention ---------------------------------------------------------
+ * For every row r = b*(k+1)+j (position p = pos[b]+j) and q head h (kv head
+ * g = h / (n_q_heads / n_kv_heads)):
+ *     out[r][h] = sum_{t=0..p} softmax_t(scale * q[r][h] . K_t) * V_t
+ * over branch b's keys 0..p inclusive (kv_hi = the row's position), never a
+ * slot beyond p. Sources: span-02 spec.rs, module documentation ("never
+ * attended: kv_hi = position"); memra-engine spec.rs, `full_attn_verify`
+ * ("query row r attends to keys [0..base_len+r+1)"); DSSD-dev fast.py,
+ * `_attention` (per-row exact key path).
+ * Split-KV: keys are cut into fixed 1024-position splits, independent of B, k
+ * and context, so a row's output is byte-identical whatever batch it is
+ * verified in (memra-engine spec.rs, `MtpScratch`: fixed split geometry).
+ *   q       device bf16 [B*(k+1)][n_q_heads][head_dim]
+ *   out     device bf16 [B*(k+1)][n_q_heads][head_dim]
+ *   scale   softmax scale (normally 1/sqrt(head_dim))
+ *   max_pos host bound: pos[b]+k+1 <= max_pos for every b (sizes the grid and
+ *           the workspace; rows beyond it are a device error SPEC_DEVERR_POS).
+ *   ws      device workspace of spec_verify_attn_workspace(...) bytes, 256-byte
+ *           aligned, contents need not be initialised.
+ * Host errors: NULL, B < 1, k out of range, n_q_heads % n_kv_heads != 0,
+ * head_dim not 64/128/256, max_pos < k+1, workspace too small.
+ * Device errors: as spec_kv_append (the row's output is then left unwritten). */
+size_t spec_verify_attn_workspace(const spec_kv_desc *kv, int B, int k, int n_q_heads,
+                                  int max_pos);
+int spec_verify_attn(const spec_kv_desc *kv, const int32_t *pos, int B, int k,
+                     int n_q_heads, const void *q, float scale, void *out,
+                     void *ws, size_t ws_bytes, int max_pos, int32_t *dev_err,
+                     spec_stream_t stream);
+
+/* ---- a3: LM head with fused argmax ------------------------------------------------
+ *   logit[m][v] = sum_h hidden[m][h] * W[v][h]   (fp32 accumulation)
+ *   ids[m]      = the lowest v attaining max_v logit[m][v]; with d2t, d2t[that v]
+ * The logits never reach global memory. W is streamed once per call for all
+ * M rows. Sources: span-02 spec.rs, `Spec::body_inner` (`lm_head_argmax`) and
+ * `greedy_logprob` (first maximum wins); flashrt-structures whole_step.py,
+ * `generate_speculative` (argmax of the fp32 logits).
+ *   hidden  device bf16 [M][H];  W  device bf16 [V][H];  16-byte aligned, H % 8 == 0
+ *   d2t     device int32 [V] or NULL: trimmed draft vocabulary -> target id
+ *           (oxinfer qwen_mtp.rs, module documentation of the trimmed head)
+ *   d2t_limit  target vocabulary size; a d2t entry outside [0, d2t_limit) is
+ *           SPEC_DEVERR_D2T and that row's id is written as -1.
+ *   ids     device int32 [M];  max_logit  device fp32 [M] or NULL
+ *   ws      device workspace of spec_lmhead_workspace(M, V, H) bytes. Its first
+ *           256 bytes must be ZERO before the first call; every call leaves
+ *           them zero again, so a workspace is zeroed once, not per call.
+ *           Calls that share one workspace must not overlap on the GPU.
+ * Limits: 1 <= M <= 256, V >= 1, H >= 8.  */
+size_t spec_lmhead_workspace(int M, int V, int H);
+int spec_lmhead_argmax(const void *hidden, const void *W, int M, int V, int H,
+                       const int32_t *d2t, int d2t_limit, int32_t *ids, float *max_logit,
+                       void *ws, size_t ws_bytes, int32_t *dev_err, spec_stream_t stream);
+
+/* Test hook: the same kernel, K order and accumulators as spec_lmhead_argmax, which
+ * also stores the fp32 logits [M][V] (row-invariance checks). Same workspace rules. */
+int spec_lmhead_logits(const void *hidden, const void *W, int M, int V, int H,
+                       float *logits, int32_t *ids, void *ws, size_t ws_bytes,
+                       spec_stream_t stream);
+
+/* ---- a4: greedy chain acceptance --------------------------------------------------
+ * Per branch b, with target ids g_j = ids[b*(k+1)+j]:
+ *   a = the largest a <= k with drafts[b][i] == g_i for every i < a
+ *   emitted = drafts[b][0..a) followed by the bonus token g_a;  n = a+1
+ *   new pos = pos[b] + a + 1 (rollback is the position advance alone)
+ * Sources: span-02 spec.rs, module documentation ("a token is emitted only if it
+ * equals the target's argmax at the verify row before it"); DSSD-dev fast.py,
+ * `generate_spec` (accept loop then correction/bonus token); flashrt-structures
+ * whole_step.py, `generate_speculative` (device-side prefix match).
+ *   drafts      device int32 [B][k]  (may be NULL when k == 0)
+ *   ids         device int32 [B*(k+1)]
+ *   pos         device int32 [B]
+ *   out_tokens  device int32 [B][k+1]: the n emitted tokens, then -1
+ *   out_n, out_accepted, out_pos, out_next   device int32 [B] (out_next = bonus)
+ *   hidden, H, h_out   optional (all three or none): h_out[b][:] =
+ *       hidden[b*(k+1)+a][:], bf16 [B][H], the target hidden state of the row that
+ *       produced the bonus token -- the next draft step's h (span-02 spec.rs,
+ *       `Spec::body_inner`, `spec_accept` writing h0).
+ * Host errors: NULL, B < 1, k out of range. */
+int spec_accept(const int32_t *drafts, const int32_t *ids, const int32_t *pos, int B,
+                int k, int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted,
+                int32_t *out_pos, int32_t *out_next, const void *hidden, int H,
+                void *h_out, spec_stream_t stream);
+
+/* ---- a5: MTP draft-head input -----------------------------------------------------
+ *   c[m]  = [ rmsnorm(E[tok[m]]; g_emb) ; rmsnorm(h[m]; g_hid) ]  rounded to bf16
+ *   x[m]  = W_fc . c[m]   (fp32 accumulation, stored as bf16)
+ *   rmsnorm(y; g)_i = y_i / sqrt(mean_j y_j^2 + eps) * g_i   (fp32)
+ * Source: oxinfer qwen_mtp.rs, module documentation (x = fc([rmsnorm_emb(embed
+ * (x_{i+1})), rmsnorm_hidden(h_i)]), fc: [H, 2H], embedding first).
+ *   tok    device int32 [M];  E  device bf16 [V][H];  h  device bf16 [M][H]
+ *   g_emb, g_hid  device fp32 [H];  W_fc  device bf16 [H][2H];  x_out  device bf16 [M][H]
+ *   ws     device workspace of spec_mtp_input_workspace(M, H) bytes; its first 256
+ *          bytes follow the same zero rule as spec_lmhead_workspace.
+ * Limits: 1 <= M <= 256, H % 64 == 0. Device error SPEC_DEVERR_TOKEN for tok[m]
+ * outside [0, V) (that row's c is written as zeros). */
+size_t spec_mtp_input_workspace(int M, int H);
+int spec_mtp_input(const int32_t *tok, const void *E, const void *h, const float *g_emb,
+                   const float *g_hid, float eps, const void *W_fc, int M, int H, int V,
+                   void *x_out, void *ws, size_t ws_bytes, int32_t *dev_err,
+                   spec_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

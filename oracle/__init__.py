@@ -1,0 +1,233 @@
+"""CPU oracle of the batched verify step -- test infrastructure only.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+import this package; the product path (the CUDA library and its binding) never does.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, straight loops). This module
+builds it with gcc and marshals numpy arrays through ctypes; it adds no arithmetic.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from pathlib import Path
+
+import numpy as np
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "oracle.c"
+_LIB = _HERE / "liboracle.so"
+
+ERR_PAGE, ERR_COVER, ERR_TOKEN, ERR_D2T, ERR_POS = 1, 2, 4, 8, 16
+
+
+def build(force: bool = False) -> Path:
+    """Compile oracle.c into liboracle.so (OpenMP when the compiler has it)."""
+    if _LIB.exists() and not force and _LIB.stat().st_mtime >= _SRC.stat().st_mtime:
+        return _LIB
+    tmp = _LIB.with_suffix(f".{os.getpid()}.tmp")
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fno-fast-math",
+            "-ffp-contract=off", str(_SRC), "-o", str(tmp), "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Kv(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("kv_dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(str(build()))
+        _lib.orc_bf16_to_double.restype = ctypes.c_double
+        _lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+        _lib.orc_double_to_bf16.restype = ctypes.c_uint16
+        _lib.orc_double_to_bf16.argtypes = [ctypes.c_double]
+        _lib.orc_e4m3_decode.restype = ctypes.c_double
+        _lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        _lib.orc_e4m3_encode.restype = ctypes.c_uint8
+        _lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        _lib.orc_threads.restype = ctypes.c_int
+        _lib.orc_verify_attn.argtypes = [ctypes.POINTER(_Kv)] + [ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                                                  ctypes.c_int, ctypes.c_void_p, ctypes.c_double,
+                                                                  ctypes.c_void_p]
+        _lib.orc_verify_attn_items.argtypes = [ctypes.POINTER(_Kv), ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_void_p, ctypes.c_double, ctypes.c_void_p,
+                                               ctypes.c_int, ctypes.c_void_p]
+        _lib.orc_kv_write_rows.argtypes = [ctypes.POINTER(_Kv), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                           ctypes.c_void_p, ctypes.c_void_p]
+        _lib.orc_kv_append.argtypes = [ctypes.POINTER(_Kv), ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_void_p, ctypes.c_void_p]
+        _lib.orc_lmhead_argmax.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                           ctypes.c_void_p, ctypes.c_void_p]
+        _lib.orc_lmhead_logits.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_void_p]
+        _lib.orc_accept.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 5
+        _lib.orc_mtp_input.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_double, ctypes.c_void_p, ctypes.c_int,
+                                                               ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                                               ctypes.c_void_p]
+    return _lib
+
+
+def threads() -> int:
+    return int(lib().orc_threads())
+
+
+def set_threads(n: int) -> None:
+    lib().orc_set_threads(int(n))
+
+
+def _p(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---- number formats -------------------------------------------------------------------
+
+def bf16_to_double(bits: int) -> float:
+    return float(lib().orc_bf16_to_double(int(bits) & 0xFFFF))
+
+
+def double_to_bf16(x: float) -> int:
+    return int(lib().orc_double_to_bf16(float(x)))
+
+
+def e4m3_decode(code: int) -> float:
+    return float(lib().orc_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(lib().orc_e4m3_encode(float(np.float32(x))))
+
+
+# ---- KV pool ----------------------------------------------------------------------------
+
+class KvPool:
+    """Host copy of a paged pool with the library's layout
+    [num_pages][Hkv][page_size][d] (uint16 bf16 bits or uint8 E4M3 codes)."""
+
+    def __init__(self, k_pool, v_pool, page_table, page_size, k_scale=None, v_scale=None):
+        self.k_pool = np.ascontiguousarray(k_pool)
+        self.v_pool = np.ascontiguousarray(v_pool)
+        assert self.k_pool.shape == self.v_pool.shape and self.k_pool.ndim == 4
+        self.kv_dtype = 0 if self.k_pool.dtype == np.uint16 else 1
+        assert self.kv_dtype == 0 or self.k_pool.dtype == np.uint8
+        self.page_table = _c(page_table, np.int32)
+        self.k_scale = None if k_scale is None else _c(k_scale, np.float32)
+        self.v_scale = None if v_scale is None else _c(v_scale, np.float32)
+        self.num_pages, self.n_kv_heads, ps, self.head_dim = self.k_pool.shape
+        assert ps == page_size
+        self.page_size = page_size
+        self.max_pages = self.page_table.shape[1]
+
+    def _struct(self) -> _Kv:
+        return _Kv(_p(self.k_pool), _p(self.v_pool), _p(self.k_scale), _p(self.v_scale),
+                   _p(self.page_table), self.num_pages, self.max_pages, self.page_size,
+                   self.n_kv_heads, self.head_dim, self.kv_dtype)
+
+
+def kv_write_rows(kv: KvPool, row_branch, row_pos, k_rows, v_rows) -> int:
+    rb, rp = _c(row_branch, np.int32), _c(row_pos, np.int32)
+    kr, vr = _c(k_rows, np.uint16), _c(v_rows, np.uint16)
+    s = kv._struct()
+    return int(lib().orc_kv_write_rows(ctypes.byref(s), _p(rb), _p(rp), len(rb), _p(kr), _p(vr)))
+
+
+def kv_append(kv: KvPool, pos, B: int, k: int, k_new, v_new) -> int:
+    pos = _c(pos, np.int32)
+    kn, vn = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    s = kv._struct()
+    return int(lib().orc_kv_append(ctypes.byref(s), _p(pos), B, k, _p(kn), _p(vn)))
+
+
+def verify_attn(kv: KvPool, pos, B: int, k: int, n_q_heads: int, q, scale: float):
+    """fp64 outputs [B*(k+1)][Hq][d] and the error bits."""
+    pos, q = _c(pos, np.int32), _c(q, np.uint16)
+    R = B * (k + 1)
+    out = np.empty((R, n_q_heads, kv.head_dim), dtype=np.float64)
+    s = kv._struct()
+    err = lib().orc_verify_attn(ctypes.byref(s), _p(pos), B, k, n_q_heads, _p(q), float(scale), _p(out))
+    return out, int(err)
+
+
+def verify_attn_items(kv: KvPool, pos, B: int, k: int, n_q_heads: int, q, scale: float, items):
+    """fp64 outputs [len(items)][d] for items = r * Hq + h."""
+    pos, q, items = _c(pos, np.int32), _c(q, np.uint16), _c(items, np.int32)
+    out = np.empty((len(items), kv.head_dim), dtype=np.float64)
+    s = kv._struct()
+    err = lib().orc_verify_attn_items(ctypes.byref(s), _p(pos), B, k, n_q_heads, _p(q), float(scale),
+                                      _p(items), len(items), _p(out))
+    return out, int(err)
+
+
+# ---- LM head ----------------------------------------------------------------------------
+
+def lmhead_argmax(hidden, W, d2t=None, d2t_limit: int = 0):
+    """ids int32 [M], fp64 max logit [M], fp64 top-2 gap [M], error bits."""
+    hidden, W = _c(hidden, np.uint16), _c(W, np.uint16)
+    M, H = hidden.shape
+    V = W.shape[0]
+    assert W.shape[1] == H
+    d2t = None if d2t is None else _c(d2t, np.int32)
+    ids = np.empty(M, np.int32)
+    mx = np.empty(M, np.float64)
+    gap = np.empty(M, np.float64)
+    err = lib().orc_lmhead_argmax(_p(hidden), _p(W), M, V, H, _p(d2t), int(d2t_limit), _p(ids), _p(mx), _p(gap))
+    return ids, mx, gap, int(err)
+
+
+def lmhead_logits(hidden, W):
+    hidden, W = _c(hidden, np.uint16), _c(W, np.uint16)
+    M, H = hidden.shape
+    V = W.shape[0]
+    out = np.empty((M, V), np.float64)
+    lib().orc_lmhead_logits(_p(hidden), _p(W), M, V, H, _p(out))
+    return out
+
+
+# ---- accept -----------------------------------------------------------------------------
+
+def accept(drafts, ids, pos, B: int, k: int):
+    drafts = _c(np.asarray(drafts).reshape(B, k) if k > 0 else np.zeros((B, 1)), np.int32)
+    ids, pos = _c(ids, np.int32), _c(pos, np.int32)
+    tokens = np.empty((B, k + 1), np.int32)
+    n, a, npos, nxt = (np.empty(B, np.int32) for _ in range(4))
+    lib().orc_accept(_p(drafts), _p(ids), _p(pos), B, k, _p(tokens), _p(n), _p(a), _p(npos), _p(nxt))
+    return tokens, n, a, npos, nxt
+
+
+# ---- MTP input ----------------------------------------------------------------------------
+
+def mtp_input(tok, E, h, g_emb, g_hid, eps: float, W_fc):
+    """bf16 concat [M][2H] (uint16 bits), fp64 x [M][H], error bits."""
+    tok = _c(tok, np.int32)
+    E, h, W_fc = _c(E, np.uint16), _c(h, np.uint16), _c(W_fc, np.uint16)
+    g_emb, g_hid = _c(g_emb, np.float32), _c(g_hid, np.float32)
+    M, H = h.shape
+    V = E.shape[0]
+    concat = np.empty((M, 2 * H), np.uint16)
+    x = np.empty((M, H), np.float64)
+    err = lib().orc_mtp_input(_p(tok), _p(E), _p(h), _p(g_emb), _p(g_hid), float(eps), _p(W_fc),
+                              M, H, V, _p(concat), _p(x))
+    return concat, x, int(err)

@@ -1,0 +1,476 @@
+/*
+ * oracle.c -- plain, slow CPU reference of the batched speculative-decoding verify
+ * step. TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the CPU-baseline
+ * leg of the benchmark call it; the product path never does.
+ *
+ * Everything is computed in fp64 with straight loops in the order the definitions
+ * are written, so that each function can be checked against its source by eye.
+ * Nothing here is shared with the CUDA library: no header, helper or table.
+ * The only parallelism is an OpenMP loop over independent (row, head) items, which
+ * changes no arithmetic.
+ *
+ * Sources (web pages; function or section named on each):
+ *  - span-02 `engine/crates/model/src/spec.rs`: module documentation (verify of B
+ *    branches with KV appended in place at pos..pos+k, emit only on equality with
+ *    the argmax of the row before, rollback = advancing pos, kv_hi = position),
+ *    `SpecReq` (page of position p is pages[p / page_size]), `greedy_logprob`
+ *    (first maximum wins), `Spec::body_inner` (step order).
+ *  - memra-engine 0.70.0 `src/spec.rs`, `full_attn_verify`: row r attends keys
+ *    [0, base_len + r + 1).
+ *  - DSSD-dev `dssd/fast.py`, `_attention` (CPU reference: SDPA per row over its exact
+ *    key list, GQA by consecutive grouping) and `generate_spec` (accept loop, then the
+ *    correction / bonus token target[len(committed)]).
+ *  - oxinfer 0.0.5 `src/qwen_mtp.rs`: module documentation (x = fc([rmsnorm_emb(embed
+ *    (x_{i+1})), rmsnorm_hidden(h_i)]), fc [H, 2H], embedding first) and
+ *    `speculative_accept` (greedy case: accept iff the draft is the argmax).
+ *  - OCP 8-bit floating point specification, E4M3 (bias 7, max 448, no infinities,
+ *    S.1111.111 is NaN, subnormals m * 2^-9): the FP8 page format.
+ *
+ * Readings where the pages are silent (all listed in the design notes):
+ *  - pos[b] is the position of the branch's first verify row = committed tokens.
+ *  - KV page layout [num_pages][Hkv][page_size][d]; q head h uses kv head h / G.
+ *  - FP8: code = e4m3(float(x) / scale) with IEEE fp32 division, round to nearest
+ *    even, saturating to +-448 (satfinite); value = decode(code) * scale.
+ *  - The argmax decision is taken on the fp32-rounded logit (the pages' argmax runs
+ *    on fp32 logits, flashrt-structures whole_step.py `generate_speculative`).
+ *  - MTP concat halves are rounded to bf16 before fc; x is rounded to bf16.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_ERR_PAGE 1
+#define ORC_ERR_COVER 2
+#define ORC_ERR_TOKEN 4
+#define ORC_ERR_D2T 8
+#define ORC_ERR_POS 16
+
+int orc_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void orc_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/* ------------------------------------------------------------------------------------
+ * Number formats
+ * ---------------------------------------------------------------------------------- */
+
+/* bfloat16 -> double: the 16 bits are the top half of an IEEE binary32. */
+double orc_bf16_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* double -> bfloat16, round to nearest, ties to even, written from the definition:
+ * find the two neighbouring bf16 values and pick the nearer (even one on a tie).
+ * NaN -> canonical quiet NaN 0x7FC0; overflow rounds to +-inf as IEEE does. */
+uint16_t orc_double_to_bf16(double x) {
+    if (isnan(x)) return 0x7FC0;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7F80;
+    /* bf16: 8 exponent bits (bias 127), 7 stored mantissa bits. */
+    int e;
+    frexp(a, &e);              /* a = f * 2^e, f in [0.5, 1) -> unbiased exponent e-1 */
+    int ue = e - 1;
+    if (ue < -126) ue = -126;  /* subnormal range shares the quantum of 2^-126 */
+    double quantum = ldexp(1.0, ue - 7);
+    double lo = floor(a / quantum) * quantum;  /* exact: a/quantum is a power-of-two scaling */
+    double hi = lo + quantum;
+    double r;
+    if (a - lo < hi - a) r = lo;
+    else if (a - lo > hi - a) r = hi;
+    else r = (fmod(lo / quantum, 2.0) == 0.0) ? lo : hi;
+    if (r >= ldexp(1.0, 128)) return sign | 0x7F80;
+    float f = (float)r;        /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(sign | ((u >> 16) & 0x7FFF));
+}
+
+/* E4M3 code -> value (OCP FP8: sign, 4 exponent bits with bias 7, 3 mantissa bits;
+ * exponent 0 is subnormal m/8 * 2^-6; S.1111.111 is NaN; no infinities). */
+double orc_e4m3_decode(uint8_t c) {
+    int s = (c >> 7) & 1, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* fp32 value -> E4M3 code, round to nearest even, saturating to the largest finite
+ * magnitude 448 (the "satfinite" behaviour); NaN -> 0x7F. Written as a search over
+ * the 127 non-negative finite codes, which are increasing in value: the nearest one
+ * wins, a tie goes to the even code (mantissa LSB 0). */
+uint8_t orc_e4m3_encode(float xf) {
+    double x = (double)xf;
+    if (isnan(x)) return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs(x);
+    if (a >= 448.0) return sign | 0x7E;
+    int best = 0;
+    for (int c = 1; c <= 0x7E; ++c) {
+        double vc = orc_e4m3_decode((uint8_t)c);
+        if (vc <= a) best = c;
+        else break;
+    }
+    /* best = largest code with value <= a; compare with its successor */
+    double lo = orc_e4m3_decode((uint8_t)best);
+    if (lo == a || best == 0x7E) return sign | (uint8_t)best;
+    double hi = orc_e4m3_decode((uint8_t)(best + 1));
+    int pick;
+    if (a - lo < hi - a) pick = best;
+    else if (a - lo > hi - a) pick = best + 1;
+    else pick = (best % 2 == 0) ? best : best + 1;
+    return sign | (uint8_t)pick;
+}
+
+/* ------------------------------------------------------------------------------------
+ * Paged KV pool
+ * ---------------------------------------------------------------------------------- */
+
+typedef struct {
+    void *k_pool, *v_pool;            /* uint16 bf16 bits or uint8 E4M3 codes */
+    const float *k_scale, *v_scale;   /* [num_pages][Hkv] (FP8 only) */
+    const int32_t *page_table;        /* [B][max_pages] */
+    int32_t num_pages, max_pages, page_size, n_kv_heads, head_dim, kv_dtype;
+} orc_kv;
+
+static size_t pool_index(const orc_kv *kv, int page, int g, int slot) {
+    return (((size_t)page * kv->n_kv_heads + g) * kv->page_size + slot) * kv->head_dim;
+}
+
+/* Resolve position p of page-table row b to (page, slot). Returns an error bit or 0. */
+static int locate(const orc_kv *kv, int b, int p, int *page, int *slot) {
+    if (p < 0) return ORC_ERR_POS;
+    int pi = p / kv->page_size;
+    if (pi >= kv->max_pages) return ORC_ERR_COVER;
+    int pg = kv->page_table[(size_t)b * kv->max_pages + pi];
+    if (pg < 0 || pg >= kv->num_pages) return ORC_ERR_PAGE;
+    *page = pg;
+    *slot = p % kv->page_size;
+    return 0;
+}
+
+/* Write n_rows K/V rows; row i goes to page-table row row_branch[i] at position
+ * row_pos[i] (span-02 spec.rs, `SpecReq`: "its KV slot is page pages[pos / 16]").
+ * bf16 pool: bit copy. FP8 pool: code = e4m3(float(x) / scale[page][g]).
+ * Returns the OR of the error bits of skipped rows. */
+int orc_kv_write_rows(const orc_kv *kv, const int32_t *row_branch, const int32_t *row_pos,
+                      int n_rows, const uint16_t *k_rows, const uint16_t *v_rows) {
+    int err = 0;
+    const int Hkv = kv->n_kv_heads, d = kv->head_dim;
+    for (int i = 0; i < n_rows; ++i) {
+        int page, slot;
+        int e = locate(kv, row_branch[i], row_pos[i], &page, &slot);
+        if (e) { err |= e; continue; }
+        for (int g = 0; g < Hkv; ++g) {
+            const uint16_t *ks = k_rows + ((size_t)i * Hkv + g) * d;
+            const uint16_t *vs = v_rows + ((size_t)i * Hkv + g) * d;
+            size_t dst = pool_index(kv, page, g, slot);
+            if (kv->kv_dtype == 0) {
+                memcpy((uint16_t *)kv->k_pool + dst, ks, (size_t)d * 2);
+                memcpy((uint16_t *)kv->v_pool + dst, vs, (size_t)d * 2);
+            } else {
+                float sk = kv->k_scale[(size_t)page * Hkv + g];
+                float sv = kv->v_scale[(size_t)page * Hkv + g];
+                for (int c = 0; c < d; ++c) {
+                    float xk = (float)orc_bf16_to_double(ks[c]);
+                    float xv = (float)orc_bf16_to_double(vs[c]);
+                    ((uint8_t *)kv->k_pool)[dst + c] = orc_e4m3_encode(xk / sk);
+                    ((uint8_t *)kv->v_pool)[dst + c] = orc_e4m3_encode(xv / sv);
+                }
+            }
+        }
+    }
+    return err;
+}
+
+/* The verify-step append: branch b's k+1 new rows go to positions pos[b]..pos[b]+k
+ * (span-02 spec.rs, module documentation). Row r = b*(k+1)+j. */
+int orc_kv_append(const orc_kv *kv, const int32_t *pos, int B, int k,
+                  const uint16_t *k_new, const uint16_t *v_new) {
+    int R = B * (k + 1);
+    int32_t *rb = (int32_t *)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1));
+    int32_t *rp = (int32_t *)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1));
+    for (int b = 0; b < B; ++b)
+        for (int j = 0; j <= k; ++j) {
+            rb[b * (k + 1) + j] = b;
+            rp[b * (k + 1) + j] = pos[b] + j;
+        }
+    int err = orc_kv_write_rows(kv, rb, rp, R, k_new, v_new);
+    free(rb);
+    free(rp);
+    return err;
+}
+
+/* Value of element c of (page, kv head g, slot) in the K (which=0) or V (1) pool. */
+static double kv_value(const orc_kv *kv, int which, int page, int g, int slot, int c) {
+    size_t i = pool_index(kv, page, g, slot) + c;
+    if (kv->kv_dtype == 0) {
+        const uint16_t *pool = (const uint16_t *)(which ? kv->v_pool : kv->k_pool);
+        return orc_bf16_to_double(pool[i]);
+    }
+    const uint8_t *pool = (const uint8_t *)(which ? kv->v_pool : kv->k_pool);
+    const float *sc = which ? kv->v_scale : kv->k_scale;
+    return orc_e4m3_decode(pool[i]) * (double)sc[(size_t)page * kv->n_kv_heads + g];
+}
+
+/* ------------------------------------------------------------------------------------
+ * Verify attention
+ * ---------------------------------------------------------------------------------- */
+
+/* One output vector: row r of branch b at position p, q head h.
+ *   s_t = scale * sum_c q[c] * K_t[c],  t = 0..p   (keys of branch b, kv head h/G)
+ *   o   = sum_t exp(s_t - max s) V_t / sum_t exp(s_t - max s)
+ * memra-engine spec.rs `full_attn_verify`: row r sees keys [0, base_len + r + 1);
+ * span-02 spec.rs: kv_hi = position. Returns an error bit or 0. */
+static int attn_one(const orc_kv *kv, int b, int p, int g, const uint16_t *q, double scale,
+                    double *o, double *s /* scratch [p+1] */) {
+    const int d = kv->head_dim;
+    double mx = -INFINITY;
+    for (int t = 0; t <= p; ++t) {
+        int page, slot;
+        int e = locate(kv, b, t, &page, &slot);
+        if (e) return e;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += orc_bf16_to_double(q[c]) * kv_value(kv, 0, page, g, slot, c);
+        s[t] = scale * dot;
+        if (s[t] > mx) mx = s[t];
+    }
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    double den = 0.0;
+    for (int t = 0; t <= p; ++t) {
+        int page, slot;
+        locate(kv, b, t, &page, &slot);
+        double w = exp(s[t] - mx);
+        den += w;
+        for (int c = 0; c < d; ++c) o[c] += w * kv_value(kv, 1, page, g, slot, c);
+    }
+    for (int c = 0; c < d; ++c) o[c] /= den;
+    return 0;
+}
+
+/* All R = B*(k+1) rows x Hq heads. q bf16 [R][Hq][d]; out fp64 [R][Hq][d].
+ * Row r = b*(k+1)+j sits at position pos[b]+j. Rows whose key path hits a bad page
+ * are left as NaN and reported. */
+int orc_verify_attn(const orc_kv *kv, const int32_t *pos, int B, int k, int n_q_heads,
+                    const uint16_t *q, double scale, double *out) {
+    const int d = kv->head_dim, Hq = n_q_heads, G = n_q_heads / kv->n_kv_heads;
+    const int R = B * (k + 1);
+    int err = 0;
+    int maxp = 0;
+    for (int b = 0; b < B; ++b)
+        if (pos[b] + k + 1 > maxp) maxp = pos[b] + k + 1;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int item = 0; item < R * Hq; ++item) {
+        int r = item / Hq, h = item % Hq, b = r / (k + 1), j = r % (k + 1);
+        double *s = (double *)malloc(sizeof(double) * (size_t)(maxp + 1));
+        double *o = out + ((size_t)r * Hq + h) * d;
+        int e = (pos[b] < 0) ? ORC_ERR_POS
+                             : attn_one(kv, b, pos[b] + j, h / G, q + ((size_t)r * Hq + h) * d, scale, o, s);
+        if (e) {
+            for (int c = 0; c < d; ++c) o[c] = NAN;
+            err |= e;
+        }
+        free(s);
+    }
+    return err;
+}
+
+/* A chosen subset of (row, head) outputs, for full-size checks:
+ * items[i] = r * Hq + h; out fp64 [n_items][d]. */
+int orc_verify_attn_items(const orc_kv *kv, const int32_t *pos, int B, int k, int n_q_heads,
+                          const uint16_t *q, double scale, const int32_t *items, int n_items,
+                          double *out) {
+    const int d = kv->head_dim, Hq = n_q_heads, G = n_q_heads / kv->n_kv_heads;
+    int err = 0;
+    int maxp = 0;
+    for (int b = 0; b < B; ++b)
+        if (pos[b] + k + 1 > maxp) maxp = pos[b] + k + 1;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int i = 0; i < n_items; ++i) {
+        int r = items[i] / Hq, h = items[i] % Hq, b = r / (k + 1), j = r % (k + 1);
+        double *s = (double *)malloc(sizeof(double) * (size_t)(maxp + 1));
+        double *o = out + (size_t)i * d;
+        int e = attn_one(kv, b, pos[b] + j, h / G, q + ((size_t)r * Hq + h) * d, scale, o, s);
+        if (e) {
+            for (int c = 0; c < d; ++c) o[c] = NAN;
+            err |= e;
+        }
+        free(s);
+    }
+    (void)B;
+    return err;
+}
+
+/* ------------------------------------------------------------------------------------
+ * LM head with argmax
+ * ---------------------------------------------------------------------------------- */
+
+/* Row m: logit[v] = sum_h hidden[m][h] * W[v][h] in fp64 (every bf16 x bf16 product is
+ * exact in fp64); the decision is taken on the fp32-rounded logits: the id is the
+ * first v whose logit is strictly greater than every earlier one (span-02 spec.rs,
+ * `greedy_logprob`: first maximum). With d2t the id becomes d2t[id] (oxinfer
+ * qwen_mtp.rs, trimmed draft head). Also returns the fp64 max logit and the fp64 gap
+ * between the winner and the best other logit (the margin). */
+static void lmhead_row(const uint16_t *hidden_row, const uint16_t *W, int V, int H,
+                       int32_t *id, double *max_logit, double *gap) {
+    int best = -1;
+    float bestf = 0.0f;
+    double best64 = 0.0, second64 = -INFINITY;
+    double *hd = (double *)malloc(sizeof(double) * (size_t)H);
+    for (int c = 0; c < H; ++c) hd[c] = orc_bf16_to_double(hidden_row[c]);
+    for (int v = 0; v < V; ++v) {
+        const uint16_t *w = W + (size_t)v * H;
+        double acc = 0.0;
+        for (int c = 0; c < H; ++c) acc += hd[c] * orc_bf16_to_double(w[c]);
+        float f = (float)acc;
+        if (best < 0 || f > bestf) {
+            if (best >= 0 && best64 > second64) second64 = best64;
+            best = v;
+            bestf = f;
+            best64 = acc;
+        } else if (acc > second64) {
+            second64 = acc;
+        }
+    }
+    free(hd);
+    *id = best;
+    if (max_logit) *max_logit = best64;
+    if (gap) *gap = best64 - second64;
+}
+
+int orc_lmhead_argmax(const uint16_t *hidden, const uint16_t *W, int M, int V, int H,
+                      const int32_t *d2t, int d2t_limit, int32_t *ids, double *max_logit,
+                      double *gap) {
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int m = 0; m < M; ++m) {
+        int32_t id;
+        lmhead_row(hidden + (size_t)m * H, W, V, H, &id, max_logit ? &max_logit[m] : 0,
+                   gap ? &gap[m] : 0);
+        if (d2t) {
+            int32_t t = d2t[id];
+            if (t < 0 || t >= d2t_limit) {
+                err |= ORC_ERR_D2T;
+                t = -1;
+            }
+            id = t;
+        }
+        ids[m] = id;
+    }
+    return err;
+}
+
+/* Plain logits, fp64 [M][V] (for row-invariance and tolerance checks on small sizes). */
+void orc_lmhead_logits(const uint16_t *hidden, const uint16_t *W, int M, int V, int H,
+                       double *logits) {
+#pragma omp parallel for schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int v = 0; v < V; ++v) {
+            double acc = 0.0;
+            for (int c = 0; c < H; ++c)
+                acc += orc_bf16_to_double(hidden[(size_t)m * H + c]) * orc_bf16_to_double(W[(size_t)v * H + c]);
+            logits[(size_t)m * V + v] = acc;
+        }
+}
+
+/* ------------------------------------------------------------------------------------
+ * Greedy chain acceptance
+ * ---------------------------------------------------------------------------------- */
+
+/* DSSD-dev fast.py `generate_spec`: walk the drafts, stop at the first one that differs
+ * from the target token of its row, then append target[len(committed)] (correction or
+ * bonus). span-02 spec.rs: the draft at verify row j+1 is compared with the argmax of
+ * verify row j; new position = pos + accepted + 1. */
+void orc_accept(const int32_t *drafts, const int32_t *ids, const int32_t *pos, int B, int k,
+                int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted, int32_t *out_pos,
+                int32_t *out_next) {
+    for (int b = 0; b < B; ++b) {
+        const int32_t *target = ids + (size_t)b * (k + 1);
+        int32_t *emit = out_tokens + (size_t)b * (k + 1);
+        int n = 0;
+        for (int i = 0; i < k; ++i) {
+            int32_t d = drafts[(size_t)b * k + i];
+            if (d != target[i]) break;
+            emit[n++] = d;
+        }
+        int a = n;
+        emit[n++] = target[a];
+        for (int j = n; j <= k; ++j) emit[j] = -1;
+        out_n[b] = n;
+        out_accepted[b] = a;
+        out_pos[b] = pos[b] + a + 1;
+        out_next[b] = target[a];
+    }
+}
+
+/* ------------------------------------------------------------------------------------
+ * MTP draft-head input
+ * ---------------------------------------------------------------------------------- */
+
+/* oxinfer qwen_mtp.rs, module documentation:
+ *   x = fc([rmsnorm_emb(embed(x_{i+1})), rmsnorm_hidden(h_i)])   fc: [H, 2H]
+ * rmsnorm(y; g)_i = y_i / sqrt(mean(y^2) + eps) * g_i (fp64 here). The two halves are
+ * rounded to bf16 (the concat is a bf16 activation), fc sums in fp64.
+ * concat_out bf16 [M][2H]; x_out fp64 [M][H]. A token outside [0, V) gives a zero
+ * embedding half and an error bit. */
+int orc_mtp_input(const int32_t *tok, const uint16_t *E, const uint16_t *h, const float *g_emb,
+                  const float *g_hid, double eps, const uint16_t *W_fc, int M, int H, int V,
+                  uint16_t *concat_out, double *x_out) {
+    int err = 0;
+    for (int m = 0; m < M; ++m) {
+        uint16_t *c = concat_out + (size_t)m * 2 * H;
+        int t = tok[m];
+        if (t < 0 || t >= V) {
+            err |= ORC_ERR_TOKEN;
+            for (int i = 0; i < H; ++i) c[i] = 0;
+        } else {
+            const uint16_t *e = E + (size_t)t * H;
+            double ss = 0.0;
+            for (int i = 0; i < H; ++i) {
+                double y = orc_bf16_to_double(e[i]);
+                ss += y * y;
+            }
+            double inv = 1.0 / sqrt(ss / H + eps);
+            for (int i = 0; i < H; ++i) c[i] = orc_double_to_bf16(orc_bf16_to_double(e[i]) * inv * (double)g_emb[i]);
+        }
+        const uint16_t *hr = h + (size_t)m * H;
+        double ss = 0.0;
+        for (int i = 0; i < H; ++i) {
+            double y = orc_bf16_to_double(hr[i]);
+            ss += y * y;
+        }
+        double inv = 1.0 / sqrt(ss / H + eps);
+        for (int i = 0; i < H; ++i) c[H + i] = orc_double_to_bf16(orc_bf16_to_double(hr[i]) * inv * (double)g_hid[i]);
+    }
+#pragma omp parallel for schedule(static)
+    for (int item = 0; item < M * H; ++item) {
+        int m = item / H, o = item % H;
+        const uint16_t *c = concat_out + (size_t)m * 2 * H;
+        const uint16_t *w = W_fc + (size_t)o * 2 * H;
+        double acc = 0.0;
+        for (int i = 0; i < 2 * H; ++i) acc += orc_bf16_to_double(w[i]) * orc_bf16_to_double(c[i]);
+        x_out[item] = acc;
+    }
+    return err;
+}
