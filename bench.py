@@ -1,0 +1,425 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched verify step (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-all]
+
+A step = one pass of the whole hot path on one batch of synthetic input:
+KV append -> verify attention -> LM head + argmax -> chain acceptance -> the next
+draft step's MTP input, on one stream (captured in a CUDA graph).
+The headline workload is the single-stream MTP verify (B=1, k=4, H=2048, 16/2 heads,
+d=256, ctx 4096, P=64, V=151936). The other workloads are reported under "all_configs".
+
+--impl reference times the CPU oracle (the plain fp64 reference) on the same workload,
+one bounded sample per step, on this host's cores.
+Under torchrun (N > 1) every rank runs an independent replica (weak scaling; the path
+has no exchange step), and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------------
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _setup_workload(cid: int, dev: str):
+    """Inputs of workload `cid` drawn on the device, KV context written by the library."""
+    import torch
+    from greedy_speculative_decode_spec_gb300.step import PagedKv, VerifyStep
+    from greedy_speculative_decode_spec_gb300.workloads import (CONFIGS, DRAFT_CONFIG, algorithmic_kv_bytes,
+                                                                config4_verify, draft_inputs, make_lm_head,
+                                                                verify_inputs)
+    draft = None
+    if cid == 4:
+        dc = DRAFT_CONFIG
+        cfg = config4_verify(dc)
+        W = make_lm_head(cfg.V, cfg.H, cfg.seed + 7, dev)
+        draft = draft_inputs(dc, device=dev, E=W)
+        vi = verify_inputs(cfg, device=dev, W=W)
+    else:
+        cfg = CONFIGS[cid]
+        vi = verify_inputs(cfg, device=dev)
+    c = vi.cfg
+    kv = PagedKv(vi.num_pages, c.Hkv, c.P, c.d, vi.page_table.to(dev), fp8=c.kv_dtype == "fp8",
+                 k_scale=vi.k_scale, v_scale=vi.v_scale, device=dev)
+    kv.write_rows(vi.ctx_branch.to(dev), vi.ctx_pos.to(dev), vi.ctx_k.to(dev), vi.ctx_v.to(dev))
+    del vi.ctx_k, vi.ctx_v
+    # the next draft step's MTP input (tied embedding table = LM head weight)
+    g = torch.Generator(device=dev)
+    g.manual_seed(c.seed + 11)
+    mtp = dict(E=vi.W, g_emb=(0.5 + torch.rand(c.H, generator=g, device=dev)).float(),
+               g_hid=(0.5 + torch.rand(c.H, generator=g, device=dev)).float(), eps=1e-6,
+               W_fc=(0.02 * torch.randn((c.H, 2 * c.H), generator=g, device=dev)).to(torch.bfloat16))
+    step = VerifyStep(kv, c.B, c.k, c.Hq, vi.W, vi.max_pos, mtp=mtp, device=dev)
+    inputs = dict(pos=vi.pos.to(dev), q=vi.q, k_new=vi.k_new, v_new=vi.v_new, hidden=vi.hidden, drafts=vi.drafts.to(dev))
+    kv_bytes = algorithmic_kv_bytes(c, vi.pos.tolist())
+    w_bytes = c.V * c.H * 2
+    return dict(cfg=c, vi=vi, kv=kv, step=step, inputs=inputs, draft=draft, kv_bytes=kv_bytes, w_bytes=w_bytes)
+
+
+class DraftStage:
+    """Workload 4's draft side: MTP input for M rows, then the trimmed draft head + d2t."""
+
+    def __init__(self, draft, dev):
+        import torch
+        from greedy_speculative_decode_spec_gb300 import _binding as bnd
+        self.bnd, self.d = bnd, draft
+        M, H = draft.h.shape
+        self.x = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        self.ids = torch.empty(M, dtype=torch.int32, device=dev)
+        self.mtp_ws = torch.zeros(bnd.spec_mtp_input_workspace(M, H), dtype=torch.uint8, device=dev)
+        self.head_ws = torch.zeros(bnd.spec_lmhead_workspace(M, draft.W_draft.shape[0], H), dtype=torch.uint8,
+                                   device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run(self):
+        d, b = self.d, self.bnd
+        b.spec_mtp_input(d.tok, d.E, d.h, d.g_emb, d.g_hid, d.cfg.eps, d.W_fc, self.x, self.mtp_ws, self.err)
+        b.spec_lmhead_argmax(self.x, d.W_draft, self.ids, self.head_ws, d2t=d.d2t, d2t_limit=d.E.shape[0],
+                             dev_err=self.err)
+
+
+def _time_region(fn, steps, flush, stream):
+    """CUDA-event time of each call of fn (L2 flushed before each, outside the events)."""
+    import torch
+    evs = []
+    for _ in range(steps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from greedy_speculative_decode_spec_gb300 import _binding as bnd
+    from greedy_speculative_decode_spec_gb300 import build as pkg_build
+
+    world, rank, local = _dist()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    pkg_build.build()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    hbm_peak, peak_kind = _peaks()
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def measure(cid, steps, warmup, with_e2e=False):
+        w = _setup_workload(cid, dev)
+        step, inp, c = w["step"], w["inputs"], w["cfg"]
+        ds = DraftStage(w["draft"], dev) if w["draft"] is not None else None
+
+        def one():
+            if ds is not None:
+                ds.run()
+            step.run(inp["pos"], inp["q"], inp["k_new"], inp["v_new"], inp["hidden"], inp["drafts"])
+
+        for _ in range(2):
+            one()
+        torch.cuda.synchronize()
+        assert int(step.out.dev_err.item()) == 0, "device error during the step"
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one()
+        torch.cuda.synchronize()
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        sampler = ClockSampler(local) if cid == args.config else None
+        if sampler:
+            sampler.start()
+        t_steps = _time_region(graph.replay, steps, flush, stream)
+        torch.cuda.synchronize()
+        clocks = sampler.stop() if sampler else None
+        if world > 1:
+            dist.barrier()
+        # per-kernel times of the two bandwidth kernels (same stream, same flush)
+        o, kv = step.out, step.kv
+        t_attn = _time_region(lambda: bnd.spec_verify_attn(kv.desc, inp["pos"], c.B, c.k, c.Hq, inp["q"], step.scale,
+                                                           o.attn, step.attn_ws, step.max_pos, o.dev_err),
+                              steps, flush, stream)
+        t_head = _time_region(lambda: bnd.spec_lmhead_argmax(inp["hidden"], step.W, o.ids, step.head_ws,
+                                                             max_logit=o.max_logit, dev_err=o.dev_err),
+                              steps, flush, stream)
+        res = dict(cfg=c, ms=statistics.median(t_steps), ms_mean=statistics.mean(t_steps), t_attn=statistics.median(t_attn),
+                   t_head=statistics.median(t_head), kv_bytes=w["kv_bytes"], w_bytes=w["w_bytes"], clocks=clocks,
+                   launches=step.launches_per_step + (4 if ds is not None else 0))
+        if with_e2e:
+            res["e2e"] = measure_e2e(step, inp, steps, flush)
+        del w, step, graph
+        torch.cuda.empty_cache()
+        return res
+
+    def measure_e2e(step, inp, steps, flush):
+        """Host buffers in, host results out, copies inside the timed region."""
+        names_in = ["pos", "q", "k_new", "v_new", "hidden", "drafts"]
+        host = {n: inp[n].cpu().pin_memory() for n in names_in}
+        dev_in = {n: torch.empty_like(inp[n]) for n in names_in}
+        o = step.out
+        outs = [o.tokens, o.n, o.accepted, o.new_pos, o.next_tok]
+        host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+        def one():
+            for n in names_in:
+                dev_in[n].copy_(host[n], non_blocking=True)
+            step.run(dev_in["pos"], dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["hidden"], dev_in["drafts"])
+            for h, t in zip(host_out, outs):
+                h.copy_(t, non_blocking=True)
+
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        ts = _time_region(one, steps, flush, stream)
+        return dict(ms=statistics.median(ts), h2d=h2d, d2h=d2h)
+
+    main = measure(args.config, args.steps, args.warmup, with_e2e=True)
+    c = main["cfg"]
+    rows = c.B * (c.k + 1)
+    ms_max = main["ms"]
+    if world > 1:
+        t = torch.tensor([ms_max], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = world * rows / (ms_max * 1e-3)
+    head_gbs = main["w_bytes"] / (main["t_head"] * 1e-3) / 1e9
+    attn_gbs = main["kv_bytes"] / (main["t_attn"] * 1e-3) / 1e9
+    others = {}
+    if args.all and rank == 0:
+        for cid in (0, 2, 3, 4):
+            if cid == args.config:
+                continue
+            r = measure(cid, max(5, min(args.steps, 20)), max(3, args.warmup))
+            rc = r["cfg"]
+            R = rc.B * (rc.k + 1)
+            others[str(cid)] = {
+                "workload": rc.name, "us_per_step": round(r["ms"] * 1e3, 2), "rows_per_s": round(R / (r["ms"] * 1e-3), 1),
+                "attn_us": round(r["t_attn"] * 1e3, 2), "attn_gbs": round(r["kv_bytes"] / (r["t_attn"] * 1e-3) / 1e9, 1),
+                "attn_frac": round(r["kv_bytes"] / (r["t_attn"] * 1e-3) / 1e9 / hbm_peak, 4),
+                "lmhead_us": round(r["t_head"] * 1e3, 2), "lmhead_gbs": round(r["w_bytes"] / (r["t_head"] * 1e-3) / 1e9, 1),
+                "lmhead_frac": round(r["w_bytes"] / (r["t_head"] * 1e-3) / 1e9 / hbm_peak, 4),
+                "kv_bytes": r["kv_bytes"], "w_bytes": r["w_bytes"]}
+    if rank != 0:
+        return
+    e2e = main["e2e"]
+    line = {
+        "metric": "verified rows/s (B*(k+1) rows per verify step); us per verify step; HBM GB/s of the LM head",
+        "value": round(value, 1), "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4), "us_per_step": round(ms_max * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init weights)",
+        "config": {"workload": c.name, "B": c.B, "k": c.k, "rows": rows, "H": c.H, "q_heads": c.Hq, "kv_heads": c.Hkv,
+                   "head_dim": c.d, "context": list(c.ctx), "page_size": c.P, "vocab": c.V, "kv_dtype": c.kv_dtype,
+                   "parallelism": f"replicas x{world}", "graph": "CUDA graph per step",
+                   "l2": "flushed before every timed step (256 MiB write)"},
+        "roofline": {"bound": "hbm", "kernel": "spec_lmhead_argmax", "achieved": round(head_gbs, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(head_gbs / hbm_peak, 4),
+                     "peak_kind": peak_kind, "algorithmic_bytes": main["w_bytes"], "kernel_us": round(main["t_head"] * 1e3, 2),
+                     "traffic": None},
+        "attention": {"kernel": "spec_verify_attn", "achieved": round(attn_gbs, 1), "unit": "GB/s",
+                      "frac": round(attn_gbs / hbm_peak, 4), "kernel_us": round(main["t_attn"] * 1e3, 2),
+                      "algorithmic_bytes": main["kv_bytes"]},
+        "e2e": {"value": round(rows / (e2e["ms"] * 1e-3), 1), "unit": "rows/s", "ms_per_step": round(e2e["ms"], 4),
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+        "gpu_launches": main["launches"] * args.steps,
+        "clocks": main["clocks"],
+        "all_configs": others,
+    }
+    if world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(args.config, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+# ---- the oracle on the host cores ------------------------------------------------------------
+
+def _oracle_sample(cid: int):
+    """A bounded sample of workload `cid` for the oracle: one verify row (b=0, j=k) through
+    append, attention over all q heads, the full-vocabulary LM head and acceptance."""
+    import numpy as np
+    import oracle as orc
+    from greedy_speculative_decode_spec_gb300.workloads import CONFIGS, bits, scaled, verify_inputs
+    cfg = CONFIGS[cid]
+    # one branch only (the oracle's input is the same workload restricted to branch 0)
+    one = scaled(cfg, B=1, ctx=(cfg.ctx[0],) if cfg.ctx else (cfg.ctx_range[1],), ctx_range=(), num_pages=0,
+                 near_tie=0)
+    vi = verify_inputs(one)
+    c = vi.cfg
+    fp8 = c.kv_dtype == "fp8"
+    shape = vi.pool_shape
+    kp = np.full(shape, 0x7F if fp8 else 0x7FC0, np.uint8 if fp8 else np.uint16)
+    okv = orc.KvPool(kp, kp.copy(), vi.page_table.numpy(), c.P,
+                     None if vi.k_scale is None else vi.k_scale.numpy(), None if vi.v_scale is None else vi.v_scale.numpy())
+    assert orc.kv_write_rows(okv, vi.ctx_branch.numpy(), vi.ctx_pos.numpy(), bits(vi.ctx_k), bits(vi.ctx_v)) == 0
+    hid = bits(vi.hidden)
+    W = bits(vi.W)
+    q = bits(vi.q)
+    kn, vn = bits(vi.k_new), bits(vi.v_new)
+    items = np.arange(c.k * c.Hq, (c.k + 1) * c.Hq, dtype=np.int32)   # row k, every head
+
+    def run():
+        orc.kv_append(okv, vi.pos.numpy(), 1, c.k, kn, vn)
+        orc.verify_attn_items(okv, vi.pos.numpy(), 1, c.k, c.Hq, q, 1.0 / math.sqrt(c.d), items)
+        ids, _, _, _ = orc.lmhead_argmax(hid[c.k:c.k + 1], W)
+        orc.accept(vi.drafts.numpy(), np.concatenate([vi.planted.numpy()[:c.k], ids]), vi.pos.numpy(), 1, c.k)
+    desc = (f"1 verify row of {c.name} (b=0, j=k): KV append, attention over {c.Hq} q heads and "
+            f"{int(vi.pos[0]) + c.k + 1} keys, LM head over V={c.V} x H={c.H}, acceptance")
+    return run, desc
+
+
+def cpu_baseline(cid: int, budget_s: float = 20.0):
+    import oracle as orc
+    orc.build()
+    run, desc = _oracle_sample(cid)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        run()
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or n >= 50:
+            break
+    return {"value": round(n / dt, 4), "unit": "rows/s", "cores": orc.threads(), "kind": "oracle",
+            "sample": f"{n} x {desc}", "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    import oracle as orc
+    from greedy_speculative_decode_spec_gb300.workloads import CONFIGS
+    orc.build()
+    c = CONFIGS[args.config]
+    run, desc = _oracle_sample(args.config)
+    for _ in range(args.warmup):
+        run()
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        ts.append(time.perf_counter() - t0)
+    sec = statistics.median(ts)
+    value = 1.0 / sec  # one verify row per sample
+    line = {"impl": "reference", "metric": "verified rows/s (B*(k+1) rows per verify step); us per verify step; "
+            "HBM GB/s of the LM head", "value": round(value, 4), "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": {"workload": c.name, "B": c.B, "k": c.k, "rows_per_sample": 1},
+            "cpu_baseline": {"value": round(value, 4), "unit": "rows/s", "cores": orc.threads(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3])
+    ap.add_argument("--no-all", dest="all", action="store_false")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

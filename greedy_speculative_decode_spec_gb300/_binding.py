@@ -1,0 +1,210 @@
+"""Thin ctypes binding of libspecverify (include/spec_verify.h).
+
+Argument marshalling only: every function here passes device pointers, sizes and the
+current CUDA stream to the C ABI entry point of the same name and raises `SpecError`
+on a non-zero status. There is no fallback: if the library is missing or a tensor is
+not on a CUDA device, the call fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libspecverify.so"
+
+SPEC_OK = 0
+STATUS = {-1: "SPEC_ERR_NULL", -2: "SPEC_ERR_ARG", -3: "SPEC_ERR_UNSUPPORTED", -4: "SPEC_ERR_WORKSPACE",
+          -5: "SPEC_ERR_CUDA", -6: "SPEC_ERR_ALIGN"}
+DEVERR_PAGE, DEVERR_COVER, DEVERR_TOKEN, DEVERR_D2T, DEVERR_POS, DEVERR_TIMEOUT = 1, 2, 4, 8, 16, 32
+KMAX = 15
+KV_BF16, KV_FP8_E4M3 = 0, 1
+
+EXPORTS = ("spec_strerror", "spec_version", "spec_kv_append", "spec_kv_write_rows",
+           "spec_verify_attn_workspace", "spec_verify_attn", "spec_lmhead_workspace",
+           "spec_lmhead_argmax", "spec_lmhead_logits", "spec_accept", "spec_mtp_input_workspace",
+           "spec_mtp_input")
+
+
+class SpecError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)} ({strerror(status)})")
+
+
+class spec_kv_desc(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("page_table", ctypes.c_void_p),
+                ("num_pages", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("kv_dtype", ctypes.c_int32)]
+
+
+_lib = None
+_vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_KVP = ctypes.POINTER(spec_kv_desc)
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        if not LIB_PATH.exists():
+            raise RuntimeError(f"{LIB_PATH} is not built: run `python -m greedy_speculative_decode_spec_gb300.build` "
+                               "(or __graft_entry__.build()) first")
+        L = ctypes.CDLL(str(LIB_PATH))
+        L.spec_strerror.restype = ctypes.c_char_p
+        L.spec_strerror.argtypes = [_i32]
+        L.spec_version.restype = _i32
+        L.spec_kv_append.argtypes = [_KVP, _vp, _i32, _i32, _vp, _vp, _vp, _vp]
+        L.spec_kv_write_rows.argtypes = [_KVP, _vp, _vp, _i32, _vp, _vp, _vp, _vp]
+        L.spec_verify_attn_workspace.restype = _sz
+        L.spec_verify_attn_workspace.argtypes = [_KVP, _i32, _i32, _i32, _i32]
+        L.spec_verify_attn.argtypes = [_KVP, _vp, _i32, _i32, _i32, _vp, _f32, _vp, _vp, _sz, _i32, _vp, _vp]
+        L.spec_lmhead_workspace.restype = _sz
+        L.spec_lmhead_workspace.argtypes = [_i32, _i32, _i32]
+        L.spec_lmhead_argmax.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _sz, _vp, _vp]
+        L.spec_lmhead_logits.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]
+        L.spec_accept.argtypes = [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp]
+        L.spec_mtp_input_workspace.restype = _sz
+        L.spec_mtp_input_workspace.argtypes = [_i32, _i32]
+        L.spec_mtp_input.argtypes = [_vp, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp, _vp]
+        _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().spec_strerror(int(status)).decode()
+
+
+def version() -> int:
+    return int(lib().spec_version())
+
+
+def _ptr(t, name: str, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device (no CPU path exists)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(fn: str, st: int):
+    if st != SPEC_OK:
+        raise SpecError(fn, st)
+
+
+def make_kv_desc(k_pool, v_pool, page_table, page_size: int, k_scale=None, v_scale=None) -> spec_kv_desc:
+    """Descriptor of a pool [num_pages][Hkv][page_size][d] (bf16, or uint8 E4M3 codes + scales)."""
+    num_pages, hkv, ps, d = k_pool.shape
+    if ps != page_size or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("pool shapes do not match the page size")
+    fp8 = k_pool.dtype == torch.uint8
+    return spec_kv_desc(_ptr(k_pool, "k_pool"), _ptr(v_pool, "v_pool"),
+                        _ptr(k_scale, "k_scale", torch.float32), _ptr(v_scale, "v_scale", torch.float32),
+                        _ptr(page_table, "page_table", torch.int32), num_pages, page_table.shape[1], page_size, hkv,
+                        d, KV_FP8_E4M3 if fp8 else KV_BF16)
+
+
+# ---- entry points (same names as the C ABI) -----------------------------------------------
+
+def spec_kv_append(kv: spec_kv_desc, pos, B: int, k: int, k_new, v_new, dev_err=None, stream=None):
+    _check("spec_kv_append", lib().spec_kv_append(ctypes.byref(kv), _ptr(pos, "pos", torch.int32), B, k,
+                                                  _ptr(k_new, "k_new", torch.bfloat16),
+                                                  _ptr(v_new, "v_new", torch.bfloat16),
+                                                  _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
+
+
+def spec_kv_write_rows(kv: spec_kv_desc, row_branch, row_pos, k_rows, v_rows, dev_err=None, stream=None):
+    n = int(row_pos.shape[0])
+    _check("spec_kv_write_rows", lib().spec_kv_write_rows(ctypes.byref(kv), _ptr(row_branch, "row_branch", torch.int32),
+                                                          _ptr(row_pos, "row_pos", torch.int32), n,
+                                                          _ptr(k_rows, "k_rows", torch.bfloat16),
+                                                          _ptr(v_rows, "v_rows", torch.bfloat16),
+                                                          _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
+
+
+def spec_verify_attn_workspace(kv: spec_kv_desc, B: int, k: int, n_q_heads: int, max_pos: int) -> int:
+    return int(lib().spec_verify_attn_workspace(ctypes.byref(kv), B, k, n_q_heads, max_pos))
+
+
+def spec_verify_attn(kv: spec_kv_desc, pos, B: int, k: int, n_q_heads: int, q, scale: float, out, ws,
+                     max_pos: int, dev_err=None, stream=None):
+    _check("spec_verify_attn", lib().spec_verify_attn(ctypes.byref(kv), _ptr(pos, "pos", torch.int32), B, k, n_q_heads,
+                                                      _ptr(q, "q", torch.bfloat16), float(scale),
+                                                      _ptr(out, "out", torch.bfloat16), _ptr(ws, "ws"),
+                                                      ws.numel() * ws.element_size(), int(max_pos),
+                                                      _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
+
+
+def spec_lmhead_workspace(M: int, V: int, H: int) -> int:
+    return int(lib().spec_lmhead_workspace(M, V, H))
+
+
+def spec_lmhead_argmax(hidden, W, ids, ws, d2t=None, d2t_limit: int = 0, max_logit=None, dev_err=None,
+                       stream=None):
+    M, H = hidden.shape
+    V = W.shape[0]
+    _check("spec_lmhead_argmax", lib().spec_lmhead_argmax(_ptr(hidden, "hidden", torch.bfloat16),
+                                                          _ptr(W, "W", torch.bfloat16), M, V, H,
+                                                          _ptr(d2t, "d2t", torch.int32), int(d2t_limit),
+                                                          _ptr(ids, "ids", torch.int32),
+                                                          _ptr(max_logit, "max_logit", torch.float32),
+                                                          _ptr(ws, "ws"), ws.numel() * ws.element_size(),
+                                                          _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
+
+
+def spec_lmhead_logits(hidden, W, logits, ids, ws, stream=None):
+    M, H = hidden.shape
+    V = W.shape[0]
+    _check("spec_lmhead_logits", lib().spec_lmhead_logits(_ptr(hidden, "hidden", torch.bfloat16),
+                                                          _ptr(W, "W", torch.bfloat16), M, V, H,
+                                                          _ptr(logits, "logits", torch.float32),
+                                                          _ptr(ids, "ids", torch.int32), _ptr(ws, "ws"),
+                                                          ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def spec_accept(drafts, ids, pos, B: int, k: int, out_tokens, out_n, out_accepted, out_pos, out_next,
+                hidden=None, h_out=None, stream=None):
+    H = int(hidden.shape[-1]) if hidden is not None else 0
+    _check("spec_accept", lib().spec_accept(_ptr(drafts, "drafts", torch.int32) if k > 0 else None,
+                                            _ptr(ids, "ids", torch.int32), _ptr(pos, "pos", torch.int32), B, k,
+                                            _ptr(out_tokens, "out_tokens", torch.int32),
+                                            _ptr(out_n, "out_n", torch.int32),
+                                            _ptr(out_accepted, "out_accepted", torch.int32),
+                                            _ptr(out_pos, "out_pos", torch.int32),
+                                            _ptr(out_next, "out_next", torch.int32),
+                                            _ptr(hidden, "hidden", torch.bfloat16), H,
+                                            _ptr(h_out, "h_out", torch.bfloat16), _stream(stream)))
+
+
+def spec_mtp_input_workspace(M: int, H: int) -> int:
+    return int(lib().spec_mtp_input_workspace(M, H))
+
+
+def spec_mtp_input(tok, E, h, g_emb, g_hid, eps: float, W_fc, x_out, ws, dev_err=None, stream=None):
+    M, H = h.shape
+    V = E.shape[0]
+    _check("spec_mtp_input", lib().spec_mtp_input(_ptr(tok, "tok", torch.int32), _ptr(E, "E", torch.bfloat16),
+                                                  _ptr(h, "h", torch.bfloat16), _ptr(g_emb, "g_emb", torch.float32),
+                                                  _ptr(g_hid, "g_hid", torch.float32), float(eps),
+                                                  _ptr(W_fc, "W_fc", torch.bfloat16), M, H, V,
+                                                  _ptr(x_out, "x_out", torch.bfloat16), _ptr(ws, "ws"),
+                                                  ws.numel() * ws.element_size(),
+                                                  _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))

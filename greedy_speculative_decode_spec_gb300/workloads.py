@@ -190,10 +190,12 @@ def make_lm_head(V: int, H: int, seed: int, device="cpu") -> torch.Tensor:
 
 
 def verify_inputs(cfg: VerifyConfig, device="cpu", W: torch.Tensor | None = None,
-                  planted: torch.Tensor | None = None) -> VerifyInputs:
+                  drafts: torch.Tensor | None = None) -> VerifyInputs:
     """All inputs of one verify step of `cfg`, drawn from cfg.seed on `device`.
-    `W` reuses an LM-head weight (tied embeddings); `planted` fixes the target ids
-    (drafts then follow the acceptance schedule against them)."""
+    `W` reuses an LM-head weight (tied embeddings). `drafts` [B][k] fixes the draft
+    tokens (e.g. a draft head's output): the target of row (b, j < k) is then planted on
+    drafts[b][j] with the acceptance probability of depth j, else on another id."""
+    planted = None
     g = _gen(cfg.seed, device)
     B, k, P = cfg.B, cfg.k, cfg.P
     if cfg.ctx:
@@ -251,6 +253,13 @@ def verify_inputs(cfg: VerifyConfig, device="cpu", W: torch.Tensor | None = None
     if W is None:
         W = make_lm_head(cfg.V, cfg.H, cfg.seed + 7, device)
     tie_pairs = None
+    if drafts is not None:
+        drafts = drafts.to(device=device, dtype=torch.int64).view(B, k)
+        p = torch.tensor(cfg.accept_p[:k], dtype=torch.float32, device=device).expand(B, k)
+        hit = torch.rand((B, k), generator=g, device=device) < p
+        tgt = torch.where(hit, drafts, _uniform_other(drafts, cfg.V, g, device))
+        bonus = _randint(0, cfg.V, (B, 1), g, device)
+        planted = torch.cat([tgt, bonus], dim=1).reshape(-1)
     if planted is None:
         if cfg.near_tie:
             pairs = torch.randperm(cfg.V, generator=g, device=device)[:2 * cfg.near_tie].view(cfg.near_tie, 2)
@@ -271,7 +280,9 @@ def verify_inputs(cfg: VerifyConfig, device="cpu", W: torch.Tensor | None = None
     hidden = planted_hidden(W, planted, g, device)
     # drafts: draft j of branch b is compared with the target of row b*(k+1)+j
     tgt = planted.view(B, k + 1)[:, :k]
-    if k > 0:
+    if drafts is not None:
+        pass
+    elif k > 0:
         p = torch.tensor(cfg.accept_p[:k], dtype=torch.float32, device=device).expand(B, k)
         hit = torch.rand((B, k), generator=g, device=device) < p
         drafts = torch.where(hit, tgt, _uniform_other(tgt, cfg.V, g, device))

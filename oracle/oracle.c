@@ -117,24 +117,25 @@ double orc_e4m3_decode(uint8_t c) {
 }
 
 /* fp32 value -> E4M3 code, round to nearest even, saturating to the largest finite
- * magnitude 448 (the "satfinite" behaviour); NaN -> 0x7F. Written as a search over
- * the 127 non-negative finite codes, which are increasing in value: the nearest one
- * wins, a tie goes to the even code (mantissa LSB 0). */
+ * magnitude 448 (the "satfinite" behaviour); NaN -> 0x7F. Written as a search over the
+ * 127 non-negative finite codes, whose values increase with the code: find the largest
+ * code whose value is <= |x| (binary search), then the nearer of it and its successor
+ * wins, a tie going to the even code (mantissa LSB 0). */
 uint8_t orc_e4m3_encode(float xf) {
     double x = (double)xf;
     if (isnan(x)) return 0x7F;
     uint8_t sign = signbit(x) ? 0x80 : 0;
     double a = fabs(x);
     if (a >= 448.0) return sign | 0x7E;
-    int best = 0;
-    for (int c = 1; c <= 0x7E; ++c) {
-        double vc = orc_e4m3_decode((uint8_t)c);
-        if (vc <= a) best = c;
-        else break;
+    int lo_c = 0, hi_c = 0x7E;          /* invariant: value(lo_c) <= a < value(hi_c) */
+    while (hi_c - lo_c > 1) {
+        int mid = (lo_c + hi_c) / 2;
+        if (orc_e4m3_decode((uint8_t)mid) <= a) lo_c = mid;
+        else hi_c = mid;
     }
-    /* best = largest code with value <= a; compare with its successor */
+    int best = lo_c;
     double lo = orc_e4m3_decode((uint8_t)best);
-    if (lo == a || best == 0x7E) return sign | (uint8_t)best;
+    if (lo == a) return sign | (uint8_t)best;
     double hi = orc_e4m3_decode((uint8_t)(best + 1));
     int pick;
     if (a - lo < hi - a) pick = best;
@@ -173,11 +174,13 @@ static int locate(const orc_kv *kv, int b, int p, int *page, int *slot) {
 /* Write n_rows K/V rows; row i goes to page-table row row_branch[i] at position
  * row_pos[i] (span-02 spec.rs, `SpecReq`: "its KV slot is page pages[pos / 16]").
  * bf16 pool: bit copy. FP8 pool: code = e4m3(float(x) / scale[page][g]).
- * Returns the OR of the error bits of skipped rows. */
+ * Returns the OR of the error bits of skipped rows. Rows must name distinct positions. */
 int orc_kv_write_rows(const orc_kv *kv, const int32_t *row_branch, const int32_t *row_pos,
                       int n_rows, const uint16_t *k_rows, const uint16_t *v_rows) {
     int err = 0;
     const int Hkv = kv->n_kv_heads, d = kv->head_dim;
+    /* rows are independent (they target distinct positions) */
+#pragma omp parallel for schedule(static) reduction(| : err)
     for (int i = 0; i < n_rows; ++i) {
         int page, slot;
         int e = locate(kv, row_branch[i], row_pos[i], &page, &slot);

@@ -18,8 +18,9 @@ import torch
 
 
 class ToyLM:
-    def __init__(self, V=512, H=64, Hq=4, Hkv=2, d=64, P=16, seed=7):
+    def __init__(self, V=512, H=64, Hq=4, Hkv=2, d=64, P=16, seed=7, use_attn=True):
         self.V, self.H, self.Hq, self.Hkv, self.d, self.P, self.seed = V, H, Hq, Hkv, d, P, seed
+        self.use_attn = use_attn  # False: the stream ignores attention bits (cross-precision checks)
         g = torch.Generator().manual_seed(seed)
         self.W = (0.02 * torch.randn((V, H), generator=g)).to(torch.bfloat16)
 
@@ -41,7 +42,7 @@ class ToyLM:
 
     def target(self, x: int, p: int, o_bf16: torch.Tensor) -> int:
         h = (int(x) * 1000003 + int(p) * 7919 + self.seed) % self.V
-        return (h + self.attn_tag(o_bf16)) % self.V
+        return (h + (self.attn_tag(o_bf16) if self.use_attn else 0)) % self.V
 
     def hidden(self, x: int, p: int, tgt: int) -> torch.Tensor:
         r = self._rng(x, p, 2)
