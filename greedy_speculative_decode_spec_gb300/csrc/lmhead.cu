@@ -1,5 +1,5 @@
 // lmhead.cu -- a3: LM head with a fused per-row argmax, and the skinny GEMM it shares
-// with the MTP fc.
+// with the MTP fc (a5).
 //
 // span-02 engine/crates/model/src/spec.rs, `Spec::body_inner`: `lm_head_argmax` turns
 // the verify rows' hidden states into target ids on the device; `greedy_logprob`: the
@@ -7,154 +7,447 @@
 // `generate_speculative`: argmax of the fp32 logits. memra-engine src/spec.rs: only the
 // ids cross to the host, never the logits.
 //
-// logit[m][v] = sum_h hidden[m][h] * W[v][h]. Every logit is accumulated by one thread
-// in ascending h order, the same program for every (m, v) and every M, so a row's
-// logits do not depend on the batch it is in and equal W rows give equal logits.
-// The argmax key packs (orderable fp32 logit, inverted index) into 64 bits: the
-// largest key is the largest logit and, among equal logits, the lowest index.
+// GB300 design. The weight W [V, H] is the big operand and is streamed from HBM exactly
+// once; the M <= 256 hidden rows are the small one. The MMA therefore runs "swap-AB":
+//   D[128 vocab rows x N rows] = W_tile[128 x K] . hidden[N x K]^T
+// with the vocab tile as the tcgen05 M = 128 side and the verify rows (padded to 16) as
+// N. A persistent CTA per SM owns a contiguous run of vocab tiles. Warp 0 streams
+// 64-wide K chunks of W and of the hidden rows into a shared-memory ring with TMA
+// (128-byte swizzle); warp 1 issues tcgen05.mma into one of two TMEM accumulators;
+// warps 2..5 read the finished accumulator with tcgen05.ld while the next tile is being
+// multiplied. Every logit of every row goes through the same K order, whatever M is, so
+// a row's logits do not depend on its batch and equal W rows give equal logits.
+//
+// Argmax: each (orderable fp32 logit, inverted vocab index) pair packs into 64 bits, so
+// the maximum key is the largest logit and, among equal logits, the lowest index. A warp
+// reduces its 32 vocab rows per column with one redux.sync + ballot; the four lane
+// quadrants and the CTA's tiles merge with 64-bit max; the last CTA to finish (atomic
+// counter) merges all CTAs' keys, applies d2t and writes the ids. Logits never reach HBM.
+//
+// Every pipeline wait is bounded (1 s); on a timeout the kernel raises
+// SPEC_DEVERR_TIMEOUT, lets the loads and MMAs already issued land, frees TMEM and exits.
+#include <cuda.h>
+
 #include "common.cuh"
 #include "gemm.cuh"
+#include "sm100.cuh"
 
 namespace spec {
 
-constexpr int TV = 64;   // vocab rows per block
-constexpr int TM = 16;   // hidden rows per pass
-constexpr int TK = 64;   // K chunk
+using namespace sm100;
 
-enum Epi { EPI_ARGMAX = 0, EPI_LOGITS = 1, EPI_STORE = 2 };
+constexpr int TC_BM = 128;            // W rows per tile (MMA M)
+constexpr int TC_BK = 64;             // K elements per pipeline stage (128 bytes of bf16)
+constexpr int TC_THREADS = 192;       // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr uint32_t W_STAGE_BYTES = TC_BM * TC_BK * 2;
+constexpr uint64_t WAIT_NS = 1000000000ull;
+constexpr int MAX_SPLITS = 8;
+constexpr int MAX_CTAS = 1024;
+constexpr int SMEM_LIMIT = 227 * 1024;
 
-__device__ __forceinline__ unsigned long long pack_key(float logit, int v) {
-    const float canon = __fadd_rn(logit, 0.0f);  // -0 -> +0
-    return ((unsigned long long)float_key(canon) << 32) | (unsigned)(0xFFFFFFFFu - (unsigned)v);
+enum TcEpi { TC_ARGMAX = 0, TC_LOGITS = 1, TC_PARTIAL = 2 };
+
+struct TcParams {
+    int M, N_pad, V, K;
+    int n_tiles, n_kc, splits, stages;
+    uint32_t a_stage_bytes, tmem_cols;
+    float *logits;                  // TC_LOGITS: [M][V]
+    float *partial;                 // TC_PARTIAL: [splits][M][V]
+    unsigned long long *keys;       // argmax: [gridDim.x][M]
+    unsigned int *counter;          // argmax: last-CTA detection (zero between calls)
+    const int32_t *d2t;
+    int d2t_limit;
+    int32_t *ids;
+    float *max_logit;
+    int32_t *err;
+};
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int EPI>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    tc_skinny_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_a,
+                     TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sw = smem_u32(smem);
+    const uint32_t sa = sw + p.stages * W_STAGE_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * (W_STAGE_BYTES + p.a_stage_bytes));
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = full0 + 8 * p.stages;
+    const uint32_t tfull0 = empty0 + 8 * p.stages;
+    const uint32_t tempty0 = tfull0 + 16;
+    const uint32_t drain = tempty0 + 16;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * p.stages + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
+    unsigned long long *cand = reinterpret_cast<unsigned long long *>(tmem_slot + 4);  // [2][4][N_pad]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull0 + 8 * a, 1);
+            mbar_init(tempty0 + 8 * a, 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *last_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmap_w);
+        prefetch_tmap(&tmap_a);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int G = gridDim.x;
+    const int n_work = p.n_tiles * p.splits;
+    const int wb = (int)(((long long)blockIdx.x * n_work) / G);
+    const int we = (int)(((long long)(blockIdx.x + 1) * n_work) / G);
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            const uint32_t tx = W_STAGE_BYTES + p.a_stage_bytes;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int w = wb; w < we && ok; ++w) {
+                const int tile = w / p.splits, sp = w % p.splits;
+                const int kb = sp * p.n_kc / p.splits, ke = (sp + 1) * p.n_kc / p.splits;
+                for (int kc = kb; kc < ke; ++kc, ++it) {
+                    const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
+                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag, WAIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full0 + 8 * s, tx);
+                    tma_load_2d(sw + s * W_STAGE_BYTES, &tmap_w, kc * TC_BK, tile * TC_BM, full0 + 8 * s);
+                    tma_load_2d(sa + s * p.a_stage_bytes, &tmap_a, kc * TC_BK, 0, full0 + 8 * s);
+                }
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                raise_error(p.err, SPEC_DEVERR_TIMEOUT);
+            }
+            // let the loads still in flight land before the CTA can exit
+            const uint32_t n_last = it < (uint32_t)p.stages ? it : (uint32_t)p.stages;
+            for (uint32_t j = 0; j < n_last; ++j) {
+                const uint32_t i2 = it - 1 - j;
+                mbar_wait(full0 + 8 * (i2 % p.stages), (i2 / p.stages) & 1u, nullptr, WAIT_NS);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(TC_BM, p.N_pad);
+            uint32_t it = 0, t = 0;
+            bool ok = true;
+            for (int w = wb; w < we && ok; ++w, ++t) {
+                const uint32_t acc = t & 1u, use = t >> 1;
+                if (!mbar_wait(tempty0 + 8 * acc, (use & 1u) ^ 1u, abort_flag, WAIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem + acc * (uint32_t)p.N_pad;
+                const int sp = w % p.splits;
+                const int kb = sp * p.n_kc / p.splits, ke = (sp + 1) * p.n_kc / p.splits;
+                for (int kc = kb; kc < ke; ++kc, ++it) {
+                    const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
+                    if (!mbar_wait(full0 + 8 * s, ph, abort_flag, WAIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = sw + s * W_STAGE_BYTES, b_base = sa + s * p.a_stage_bytes;
+#pragma unroll
+                    for (int k = 0; k < TC_BK / 16; ++k)
+                        mma_bf16(d_tmem, desc_kmajor_sw128(a_base + 32 * k), desc_kmajor_sw128(b_base + 32 * k), idesc,
+                                 (kc > kb || k > 0) ? 1u : 0u);
+                    mma_commit(empty0 + 8 * s);
+                }
+                if (ok) mma_commit(tfull0 + 8 * acc);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                raise_error(p.err, SPEC_DEVERR_TIMEOUT);
+            }
+            // every MMA issued by this thread completes before TMEM is released
+            mma_commit(drain);
+            mbar_wait(drain, 0, nullptr, WAIT_NS);
+        }
+    } else {
+        // ---------------- epilogue: 4 warps, one TMEM lane quadrant each ----------------
+        const int q = warp & 3;
+        const int etid = threadIdx.x - 64;
+        unsigned long long running[2] = {0ull, 0ull};
+        uint32_t t = 0;
+        bool ok = true;
+        for (int w = wb; w < we; ++w, ++t) {
+            const uint32_t acc = t & 1u, use = t >> 1;
+            if (!mbar_wait(tfull0 + 8 * acc, use & 1u, abort_flag, WAIT_NS)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int tile = w / p.splits, sp = w % p.splits;
+            const int v = tile * TC_BM + q * 32 + lane;
+            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * (uint32_t)p.N_pad;
+            unsigned long long *cq = cand + ((size_t)acc * 4 + q) * p.N_pad;
+            for (int c0 = 0; c0 < p.N_pad; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(taddr + c0, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int m = c0 + j;
+                    if (m >= p.M) break;
+                    const float x = __uint_as_float(r[j]);
+                    if (EPI == TC_PARTIAL) {
+                        if (v < p.V) p.partial[((size_t)sp * p.M + m) * p.V + v] = x;
+                        continue;
+                    }
+                    if (EPI == TC_LOGITS && v < p.V) p.logits[(size_t)m * p.V + v] = x;
+                    const uint32_t key = v < p.V ? float_key(__fadd_rn(x, 0.0f)) : 0u;
+                    const uint32_t best = __reduce_max_sync(0xFFFFFFFFu, key);
+                    const uint32_t who = __ballot_sync(0xFFFFFFFFu, key == best);
+                    if (lane == 0) {
+                        const uint32_t vw = (uint32_t)(tile * TC_BM + q * 32 + __ffs(who) - 1);
+                        cq[m] = ((unsigned long long)best << 32) | (0xFFFFFFFFu - vw);
+                    }
+                }
+            }
+            tc_fence_before();
+            if (EPI != TC_PARTIAL) {
+                epi_bar();
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int m = etid + 128 * i;
+                    if (m < p.M) {
+                        unsigned long long b = running[i];
+                        for (int qq = 0; qq < 4; ++qq) {
+                            const unsigned long long c = cand[((size_t)acc * 4 + qq) * p.N_pad + m];
+                            b = c > b ? c : b;
+                        }
+                        running[i] = b;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            raise_error(p.err, SPEC_DEVERR_TIMEOUT);
+        }
+        if (EPI != TC_PARTIAL) {
+            for (int i = 0; i < 2; ++i) {
+                const int m = etid + 128 * i;
+                if (m < p.M) p.keys[(size_t)blockIdx.x * p.M + m] = running[i];
+            }
+            __threadfence();
+            epi_bar();
+            if (etid == 0) *last_flag = (atomicAdd(p.counter, 1u) == (unsigned)G - 1u) ? 1 : 0;
+            epi_bar();
+            if (*last_flag) {
+                __threadfence();
+                for (int m = etid; m < p.M; m += 128) {
+                    unsigned long long b = 0ull;
+                    for (int c = 0; c < G; ++c) {
+                        const unsigned long long k = __ldcg(p.keys + (size_t)c * p.M + m);
+                        b = k > b ? k : b;
+                    }
+                    int id = (int)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
+                    if (p.max_logit) p.max_logit[m] = key_float((uint32_t)(b >> 32));
+                    if (p.d2t) {
+                        const int tgt = __ldg(p.d2t + id);
+                        if (tgt < 0 || tgt >= p.d2t_limit) {
+                            raise_error(p.err, SPEC_DEVERR_D2T);
+                            id = -1;
+                        } else {
+                            id = tgt;
+                        }
+                    }
+                    p.ids[m] = id;
+                }
+                if (etid == 0) atomicExch(p.counter, 0u);
+            }
+        }
+    }
+    // ---------------- teardown ----------------
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, p.tmem_cols);
+    }
+}
+
+// out[m][n] = bf16( sum_s partial[s][m][n] ), splits summed in ascending order.
+__global__ void splitk_reduce_bf16_kernel(const float *__restrict__ partial, int splits, int M, int N,
+                                          uint16_t *__restrict__ out) {
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t total = (size_t)M * N;
+    if (i >= total) return;
+    float s = 0.f;
+    for (int k = 0; k < splits; ++k) s += __ldcg(partial + (size_t)k * total + i);
+    __nv_bfloat16 b = __float2bfloat16_rn(s);
+    out[i] = *reinterpret_cast<uint16_t *>(&b);
+}
+
+// ---- host side ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 row-major [rows][cols] map with a (64 x box_rows) box and 128-byte swizzle.
+static bool make_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return n;
+}
+
+struct TcPlan {
+    TcParams p;
+    int grid;
+    size_t smem;
+};
+
+static int plan(int M, int V, int K, int splits, TcPlan &pl) {
+    TcParams &p = pl.p;
+    p = TcParams{};
+    p.M = M;
+    p.N_pad = ((M + 15) / 16) * 16;
+    p.V = V;
+    p.K = K;
+    p.n_tiles = (V + TC_BM - 1) / TC_BM;
+    p.n_kc = (K + TC_BK - 1) / TC_BK;
+    p.splits = splits < 1 ? 1 : (splits > p.n_kc ? p.n_kc : splits);
+    p.a_stage_bytes = (uint32_t)p.N_pad * TC_BK * 2;
+    uint32_t cols = 32;
+    while (cols < 2u * (uint32_t)p.N_pad) cols <<= 1;
+    p.tmem_cols = cols;
+    const size_t fixed = 1024 + 8 * 64 + 64 + (size_t)2 * 4 * p.N_pad * 8;
+    const size_t stage = W_STAGE_BYTES + p.a_stage_bytes;
+    int stages = (int)((SMEM_LIMIT - fixed) / stage);
+    if (stages > 8) stages = 8;
+    if (stages < 2) return SPEC_ERR_UNSUPPORTED;
+    p.stages = stages;
+    pl.smem = fixed + (size_t)stages * stage;
+    const int sms = sm_count();
+    if (sms < 1) return SPEC_ERR_CUDA;
+    const int work = p.n_tiles * p.splits;
+    int g = work < sms ? work : sms;
+    if (g > MAX_CTAS) g = MAX_CTAS;
+    pl.grid = g;
+    return SPEC_OK;
 }
 
 template <int EPI>
-__global__ void __launch_bounds__(256) skinny_simt_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ W,
-                                                          int M, int N, int K, float *logits,
-                                                          unsigned long long *partial, uint16_t *out) {
-    __shared__ float ws[TV][TK + 1];
-    __shared__ float as[TM][TK + 1];
-    __shared__ unsigned long long best[TM][TV];
-    const int t = threadIdx.x;
-    const int tv = t % TV, tm = t / TV;  // tm in 0..3, 4 rows each
-    const int v0 = blockIdx.x * TV;
-    const int v = v0 + tv;
-    for (int m0 = 0; m0 < M; m0 += TM) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int k0 = 0; k0 < K; k0 += TK) {
-            // W tile: 64 x 64 elements, 16 per thread
-            for (int i = t; i < TV * TK; i += 256) {
-                const int rr = i / TK, cc = i % TK;
-                const int gv = v0 + rr, gk = k0 + cc;
-                float x = 0.f;
-                if (gv < N && gk < K) x = __uint_as_float((uint32_t)W[(size_t)gv * K + gk] << 16);
-                ws[rr][cc] = x;
-            }
-            for (int i = t; i < TM * TK; i += 256) {
-                const int rr = i / TK, cc = i % TK;
-                const int gm = m0 + rr, gk = k0 + cc;
-                float x = 0.f;
-                if (gm < M && gk < K) x = __uint_as_float((uint32_t)A[(size_t)gm * K + gk] << 16);
-                as[rr][cc] = x;
-            }
-            __syncthreads();
-#pragma unroll 8
-            for (int kk = 0; kk < TK; ++kk) {
-                const float w = ws[tv][kk];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc[i] = fmaf(w, as[tm * 4 + i][kk], acc[i]);
-            }
-            __syncthreads();
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int m = m0 + tm * 4 + i;
-            if (EPI == EPI_STORE) {
-                if (m < M && v < N) {
-                    __nv_bfloat16 b = __float2bfloat16_rn(acc[i]);
-                    out[(size_t)m * N + v] = *reinterpret_cast<uint16_t *>(&b);
-                }
-                continue;
-            }
-            if (EPI == EPI_LOGITS && m < M && v < N) logits[(size_t)m * N + v] = acc[i];
-            best[tm * 4 + i][tv] = (v < N) ? pack_key(acc[i], v) : 0ull;
-        }
-        if (EPI != EPI_STORE) {
-            __syncthreads();
-            if (t < TM && m0 + t < M) {
-                unsigned long long bk = 0ull;
-                for (int j = 0; j < TV; ++j) bk = best[t][j] > bk ? best[t][j] : bk;
-                partial[(size_t)blockIdx.x * M + m0 + t] = bk;
-            }
-            __syncthreads();
-        }
-    }
-}
-
-// Reduce the per-block partial keys of each row (one thread per row).
-__global__ void argmax_final_kernel(const unsigned long long *partial, int n_parts, int M,
-                                    const int32_t *d2t, int d2t_limit, int32_t *ids, float *max_logit,
-                                    int32_t *err) {
-    const int m = blockIdx.x * blockDim.x + threadIdx.x;
-    if (m >= M) return;
-    unsigned long long bk = 0ull;
-    for (int p = 0; p < n_parts; ++p) {
-        const unsigned long long k = partial[(size_t)p * M + m];
-        bk = k > bk ? k : bk;
-    }
-    int id = (int)(0xFFFFFFFFu - (unsigned)(bk & 0xFFFFFFFFull));
-    if (max_logit) max_logit[m] = key_float((uint32_t)(bk >> 32));
-    if (d2t) {
-        const int t = d2t[id];
-        if (t < 0 || t >= d2t_limit) {
-            raise_error(err, SPEC_DEVERR_D2T);
-            id = -1;
-        } else {
-            id = t;
-        }
-    }
-    ids[m] = id;
+static int launch_tc(const void *A, const void *W, TcPlan &pl, cudaStream_t s) {
+    CUtensorMap mw, ma;
+    if (!make_map(&mw, W, pl.p.V, pl.p.K, TC_BM) || !make_map(&ma, A, pl.p.M, pl.p.K, pl.p.N_pad))
+        return SPEC_ERR_CUDA;
+    if (cudaFuncSetAttribute(tc_skinny_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
+        cudaSuccess)
+        return SPEC_ERR_CUDA;
+    tc_skinny_kernel<EPI><<<pl.grid, TC_THREADS, pl.smem, s>>>(mw, ma, pl.p);
+    return launch_status();
 }
 
 static size_t lmhead_ws_bytes(int M, int V) {
-    const size_t tiles = (size_t)(V + TV - 1) / TV;
-    return 256 + tiles * (size_t)M * sizeof(unsigned long long);
+    const size_t tiles = (size_t)(V + TC_BM - 1) / TC_BM;
+    const size_t ctas = tiles < (size_t)MAX_CTAS ? tiles : (size_t)MAX_CTAS;
+    return 256 + ctas * (size_t)M * sizeof(unsigned long long);
 }
 
-static int lmhead_run(const void *hidden, const void *W, int M, int V, int H, const int32_t *d2t,
-                      int d2t_limit, int32_t *ids, float *max_logit, float *logits, void *ws,
-                      size_t ws_bytes, int32_t *dev_err, cudaStream_t s) {
+static int lmhead_run(const void *hidden, const void *W, int M, int V, int H, const int32_t *d2t, int d2t_limit,
+                      int32_t *ids, float *max_logit, float *logits, void *ws, size_t ws_bytes, int32_t *dev_err,
+                      cudaStream_t s) {
     if (!hidden || !W || !ids) return SPEC_ERR_NULL;
     if (M < 1 || M > 256 || V < 1 || H < 8 || (H & 7)) return SPEC_ERR_ARG;
     if (d2t && d2t_limit < 1) return SPEC_ERR_ARG;
     if (!ws || ws_bytes < lmhead_ws_bytes(M, V)) return SPEC_ERR_WORKSPACE;
     if (!aligned16(hidden) || !aligned16(W) || (reinterpret_cast<uintptr_t>(ws) & 255u)) return SPEC_ERR_ALIGN;
-    unsigned long long *partial = (unsigned long long *)((char *)ws + 256);
-    const int tiles = (V + TV - 1) / TV;
-    if (logits)
-        skinny_simt_kernel<EPI_LOGITS><<<tiles, 256, 0, s>>>((const uint16_t *)hidden, (const uint16_t *)W, M, V, H,
-                                                              logits, partial, nullptr);
-    else
-        skinny_simt_kernel<EPI_ARGMAX><<<tiles, 256, 0, s>>>((const uint16_t *)hidden, (const uint16_t *)W, M, V, H,
-                                                              nullptr, partial, nullptr);
-    argmax_final_kernel<<<(M + 127) / 128, 128, 0, s>>>(partial, tiles, M, d2t, d2t_limit, ids, max_logit, dev_err);
-    return launch_status();
+    TcPlan pl;
+    int st = plan(M, V, H, 1, pl);
+    if (st) return st;
+    TcParams &p = pl.p;
+    p.counter = (unsigned int *)ws;
+    p.keys = (unsigned long long *)((char *)ws + 256);
+    p.logits = logits;
+    p.d2t = d2t;
+    p.d2t_limit = d2t_limit;
+    p.ids = ids;
+    p.max_logit = max_logit;
+    p.err = dev_err;
+    return logits ? launch_tc<TC_LOGITS>(hidden, W, pl, s) : launch_tc<TC_ARGMAX>(hidden, W, pl, s);
 }
 
 size_t gemm_store_ws_bytes(int M, int N, int K) {
-    (void)M;
-    (void)N;
     (void)K;
-    return 256;
+    return (size_t)MAX_SPLITS * M * N * sizeof(float);
 }
 
 int gemm_store_bf16(const void *A, const void *W, int M, int N, int K, void *out, void *ws, size_t ws_bytes,
                     cudaStream_t s) {
-    (void)ws;
-    (void)ws_bytes;
-    const int tiles = (N + TV - 1) / TV;
-    skinny_simt_kernel<EPI_STORE><<<tiles, 256, 0, s>>>((const uint16_t *)A, (const uint16_t *)W, M, N, K, nullptr,
-                                                         nullptr, (uint16_t *)out);
+    if (M < 1 || M > 256 || N < 1 || K < 8 || (K & 7)) return SPEC_ERR_ARG;
+    if (ws_bytes < gemm_store_ws_bytes(M, N, K)) return SPEC_ERR_WORKSPACE;
+    const int sms = sm_count();
+    if (sms < 1) return SPEC_ERR_CUDA;
+    const int tiles = (N + TC_BM - 1) / TC_BM;
+    int splits = sms / tiles;
+    if (splits < 1) splits = 1;
+    if (splits > MAX_SPLITS) splits = MAX_SPLITS;
+    TcPlan pl;
+    int st = plan(M, N, K, splits, pl);
+    if (st) return st;
+    pl.p.partial = (float *)ws;
+    st = launch_tc<TC_PARTIAL>(A, W, pl, s);
+    if (st) return st;
+    const size_t total = (size_t)M * N;
+    splitk_reduce_bf16_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>((const float *)ws, pl.p.splits, M, N,
+                                                                             (uint16_t *)out);
     return launch_status();
 }
 

@@ -106,6 +106,8 @@ def _gen(seed: int, device) -> torch.Generator:
 def _randn_bf16(shape, g, device, std=1.0, chunk_rows=8192) -> torch.Tensor:
     """N(0, std^2) rounded to bf16, drawn in row chunks to bound the fp32 temporary."""
     out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    if out.numel() == 0:
+        return out
     flat = out.view(shape[0], -1)
     for r0 in range(0, shape[0], chunk_rows):
         r1 = min(shape[0], r0 + chunk_rows)

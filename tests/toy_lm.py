@@ -18,7 +18,7 @@ import torch
 
 
 class ToyLM:
-    def __init__(self, V=512, H=64, Hq=4, Hkv=2, d=64, P=16, seed=7, use_attn=True):
+    def __init__(self, V=512, H=256, Hq=4, Hkv=2, d=64, P=16, seed=7, use_attn=True):
         self.V, self.H, self.Hq, self.Hkv, self.d, self.P, self.seed = V, H, Hq, Hkv, d, P, seed
         self.use_attn = use_attn  # False: the stream ignores attention bits (cross-precision checks)
         g = torch.Generator().manual_seed(seed)
