@@ -8,6 +8,7 @@ not on a CUDA device, the call fails loudly.
 from __future__ import annotations
 
 import ctypes
+import os
 from pathlib import Path
 
 import torch
@@ -105,9 +106,18 @@ def _stream(stream):
     return int(stream)
 
 
+_DEBUG_SYNC = os.environ.get("SPEC_DEBUG_SYNC", "0") == "1"
+
+
 def _check(fn: str, st: int):
     if st != SPEC_OK:
         raise SpecError(fn, st)
+    if _DEBUG_SYNC and not torch.cuda.is_current_stream_capturing():
+        # debugging aid: surface an asynchronous fault at the call that caused it
+        try:
+            torch.cuda.synchronize()
+        except Exception as e:  # noqa: BLE001
+            raise RuntimeError(f"{fn}: device fault after this call: {e}") from e
 
 
 def make_kv_desc(k_pool, v_pool, page_table, page_size: int, k_scale=None, v_scale=None) -> spec_kv_desc:

@@ -388,7 +388,10 @@ static int launch_tc(const void *A, const void *W, TcPlan &pl, cudaStream_t s) {
     CUtensorMap mw, ma;
     if (!make_map(&mw, W, pl.p.V, pl.p.K, TC_BM) || !make_map(&ma, A, pl.p.M, pl.p.K, pl.p.N_pad))
         return SPEC_ERR_CUDA;
-    if (cudaFuncSetAttribute(tc_skinny_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) !=
+    // Always the same ceiling, never the launch's own size: a CUDA graph may hold launches
+    // of this kernel with different shared-memory sizes, and lowering the attribute for a
+    // later launch would leave an earlier captured one above the function's maximum.
+    if (cudaFuncSetAttribute(tc_skinny_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_LIMIT) !=
         cudaSuccess)
         return SPEC_ERR_CUDA;
     tc_skinny_kernel<EPI><<<pl.grid, TC_THREADS, pl.smem, s>>>(mw, ma, pl.p);

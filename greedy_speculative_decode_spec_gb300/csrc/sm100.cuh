@@ -129,6 +129,26 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy
+// (TMA / tensor core) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes
 // (64 bf16), 8-row groups 1024 bytes apart. The tile base must be 1024-byte aligned;
 // stepping 16 elements along K adds 32 bytes to the start address.
@@ -142,13 +162,33 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D, shape M x N.
+// Shared-memory matrix descriptor: MN-major operand, 128-byte swizzle. Each row of 128
+// bytes holds 64 consecutive MN elements of one K index; 8 K rows form a 1024-byte atom
+// (stride byte offset 1024); the next 64 MN elements sit `lbo` bytes further.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((1024u >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: 16-bit A and B (bf16 or f16), fp32 D, shape M x N;
+// a_mn / b_mn select an MN-major operand.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool f16_inputs, bool a_mn, bool b_mn) {
+    return (1u << 4)                                  // D format: f32
+           | ((f16_inputs ? 0u : 1u) << 7)            // A format: f16 (0) or bf16 (1)
+           | ((f16_inputs ? 0u : 1u) << 10)           // B format
+           | ((a_mn ? 1u : 0u) << 15)                 // A major
+           | ((b_mn ? 1u : 0u) << 16)                 // B major
+           | ((uint32_t)(N >> 3) << 17)               // N / 8
+           | ((uint32_t)(M >> 4) << 24);              // M / 16
+}
+
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
-    return (1u << 4)                         // D format: f32
-           | (1u << 7)                       // A format: bf16
-           | (1u << 10)                      // B format: bf16
-           | ((uint32_t)(N >> 3) << 17)      // N / 8
-           | ((uint32_t)(M >> 4) << 24);     // M / 16
+    return idesc_f16kind(M, N, false, false, false);
 }
 
 }  // namespace sm100

@@ -82,7 +82,8 @@ class VerifyStep:
         if mtp is not None:
             self.mtp_ws = torch.zeros(bnd.spec_mtp_input_workspace(B, self.H), dtype=torch.uint8, device=device)
             self.out.mtp_x = torch.empty((B, self.H), dtype=torch.bfloat16, device=device)
-        self.launches_per_step = 6 + (2 if mtp is not None else 0)
+        # append 1, attention 2 (split + combine), LM head 1, accept 1, MTP input 3
+        self.launches_per_step = 5 + (3 if mtp is not None else 0)
 
     def run(self, pos, q, k_new, v_new, hidden, drafts, stream=None) -> StepOutputs:
         o, kv = self.out, self.kv

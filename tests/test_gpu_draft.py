@@ -100,3 +100,47 @@ def test_mtp_bad_token_is_reported():
     di.tok[3] = SMALL_DRAFT.V + 1
     x, e = _gpu_mtp(di)
     assert e & bnd.DEVERR_TOKEN
+
+
+def test_graph_replay_mixes_launch_sizes_of_one_kernel():
+    """One CUDA graph holding launches of the same kernel with different shared-memory
+    sizes (a 64-row and a 16-row MTP input, a 64-row and an 80-row LM head), replayed
+    twice: the replays must reproduce the eager results bit for bit."""
+    dc = SMALL_DRAFT
+    big = draft_inputs(dc, V=dc.V, H=dc.H, V_draft=dc.V_draft, M=64)
+    small = draft_inputs(dataclasses.replace(dc, seed=78), V=dc.V, H=dc.H, V_draft=dc.V_draft, M=16)
+    hid80 = torch.randn((80, dc.H), generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
+    W = small.W_draft.cuda()
+    bufs = []
+    for di in (big, small):
+        M, H = di.h.shape
+        bufs.append(dict(di=di, dev={k: getattr(di, k).cuda() for k in ("tok", "E", "h", "g_emb", "g_hid", "W_fc")},
+                         x=torch.empty((M, H), dtype=torch.bfloat16, device=DEV),
+                         ws=torch.zeros(bnd.spec_mtp_input_workspace(M, H), dtype=torch.uint8, device=DEV)))
+    ids64 = torch.empty(64, dtype=torch.int32, device=DEV)
+    ids80 = torch.empty(80, dtype=torch.int32, device=DEV)
+    ws64 = torch.zeros(bnd.spec_lmhead_workspace(64, W.shape[0], dc.H), dtype=torch.uint8, device=DEV)
+    ws80 = torch.zeros(bnd.spec_lmhead_workspace(80, W.shape[0], dc.H), dtype=torch.uint8, device=DEV)
+
+    def step():
+        for b in bufs:
+            d = b["dev"]
+            bnd.spec_mtp_input(d["tok"], d["E"], d["h"], d["g_emb"], d["g_hid"], dc.eps, d["W_fc"], b["x"], b["ws"])
+        bnd.spec_lmhead_argmax(bufs[0]["x"], W, ids64, ws64)
+        bnd.spec_lmhead_argmax(hid80, W, ids80, ws80)
+
+    step()
+    torch.cuda.synchronize()
+    want = [b["x"].clone() for b in bufs] + [ids64.clone(), ids80.clone()]
+    for t in [b["x"] for b in bufs] + [ids64, ids80]:
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    got = [b["x"] for b in bufs] + [ids64, ids80]
+    for w_, g_ in zip(want, got):
+        assert torch.equal(w_.view(torch.int16) if w_.dtype == torch.bfloat16 else w_,
+                           g_.view(torch.int16) if g_.dtype == torch.bfloat16 else g_)
