@@ -19,7 +19,7 @@ LIB_PATH = _PKG / "libspecverify.so"
 SPEC_OK = 0
 STATUS = {-1: "SPEC_ERR_NULL", -2: "SPEC_ERR_ARG", -3: "SPEC_ERR_UNSUPPORTED", -4: "SPEC_ERR_WORKSPACE",
           -5: "SPEC_ERR_CUDA", -6: "SPEC_ERR_ALIGN"}
-DEVERR_PAGE, DEVERR_COVER, DEVERR_TOKEN, DEVERR_D2T, DEVERR_POS, DEVERR_TIMEOUT = 1, 2, 4, 8, 16, 32
+DEVERR_PAGE, DEVERR_COVER, DEVERR_TOKEN, DEVERR_D2T, DEVERR_POS, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1, 2, 4, 8, 16, 32, 64
 KMAX = 15
 KV_BF16, KV_FP8_E4M3 = 0, 1
 

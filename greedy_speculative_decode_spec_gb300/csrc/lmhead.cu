@@ -258,18 +258,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             }
             __threadfence();
             epi_bar();
-            if (etid == 0) *last_flag = (atomicAdd(p.counter, 1u) == (unsigned)G - 1u) ? 1 : 0;
+            if (etid == 0) {
+                const unsigned prev = atomicAdd(p.counter, 1u);
+                if (prev >= (unsigned)G) raise_error(p.err, SPEC_DEVERR_INTERNAL);  // counter not zeroed
+                *last_flag = (prev == (unsigned)G - 1u) ? 1 : 0;
+            }
             epi_bar();
             if (*last_flag) {
                 __threadfence();
+                // merge every CTA's keys: coalesced reads spread over the 128 epilogue threads,
+                // 64-bit max in shared memory (order-independent, so the result is unique)
+                unsigned long long *red = cand;  // free now: [M]
+                for (int m = etid; m < p.M; m += 128) red[m] = 0ull;
+                epi_bar();
+                const int total = G * p.M;
+                for (int i = etid; i < total; i += 128)
+                    atomicMax(red + (i % p.M), __ldcg(p.keys + i));
+                epi_bar();
                 for (int m = etid; m < p.M; m += 128) {
-                    unsigned long long b = 0ull;
-                    for (int c = 0; c < G; ++c) {
-                        const unsigned long long k = __ldcg(p.keys + (size_t)c * p.M + m);
-                        b = k > b ? k : b;
-                    }
+                    const unsigned long long b = red[m];
                     int id = (int)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
                     if (p.max_logit) p.max_logit[m] = key_float((uint32_t)(b >> 32));
+                    if (id < 0 || id >= p.V) {
+                        // cannot happen when every CTA published its keys; never index with it
+                        raise_error(p.err, SPEC_DEVERR_INTERNAL);
+                        p.ids[m] = -1;
+                        continue;
+                    }
                     if (p.d2t) {
                         const int tgt = __ldg(p.d2t + id);
                         if (tgt < 0 || tgt >= p.d2t_limit) {

@@ -75,6 +75,7 @@ typedef struct CUstream_st *spec_stream_t;
 #define SPEC_DEVERR_D2T      8   /* d2t entry outside [0, d2t_limit)                    */
 #define SPEC_DEVERR_POS      16  /* pos[b] < 0, or pos[b]+k+1 > max_pos                 */
 #define SPEC_DEVERR_TIMEOUT  32  /* a bounded pipeline wait gave up (results invalid)   */
+#define SPEC_DEVERR_INTERNAL 64  /* an internal consistency check failed; the access was skipped */
 
 /* ---- limits ------------------------------------------------------------------------ */
 #define SPEC_KMAX            15  /* k <= 15: at most 16 verify rows per branch          */
