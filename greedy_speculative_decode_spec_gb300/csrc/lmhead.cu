@@ -343,6 +343,8 @@ static EncodeTiledFn encode_fn() {
 }
 
 // 2-D bf16 row-major [rows][cols] map with a (64 x box_rows) box and 128-byte swizzle.
+// No L2 promotion: a promoted fetch may reach past the box, and for the last rows of a
+// tensor that ends at the end of its mapping that would touch unmapped memory.
 static bool make_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -351,7 +353,7 @@ static bool make_map(CUtensorMap *map, const void *base, int rows, int cols, int
     cuuint32_t box[2] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -16,10 +16,14 @@
 // the branch's pages with TMA (one box per page and 64-element column block, 128-byte
 // swizzle) into a shared-memory ring; for FP8 pools it gathers the raw E4M3 bytes and
 // warps 6..9 convert them to f16 operand tiles (E4M3 is exact in f16). Warp 1 issues the
-// MMAs. Warps 2..5 run the online softmax on S (keys beyond a row's position are set to
-// -inf by select, never multiplied), write P to shared memory, rescale O in TMEM when a
-// column's maximum grows, and finally store the split's partial (m, l, O).
-// A combine pass merges the splits of each (row, head) in ascending order.
+// MMAs. Warps 2..5 do the softmax in two passes over the split, whose S tiles all stay in
+// TMEM: pass A takes each column's maximum over the split's keys (one cross-lane
+// reduction per column per split), pass B writes P = exp2(s - m) to shared memory for
+// P.V and sums it per thread (one cross-lane sum per column per split). O accumulates in
+// TMEM without rescaling; only when a split's S tiles do not fit in TMEM at once is it
+// processed in chunks, with O rescaled between chunks. Keys beyond a row's position are
+// set to -inf by select, never multiplied; V rows past the branch's last position are
+// zeroed. A combine pass merges the splits of each (row, head) in ascending order.
 // Tile and split boundaries sit at fixed key positions, every column of an MMA is
 // computed independently of the others, and masked keys contribute exact zeros, so a
 // row's output is identical whatever B, k or batch it is verified in.
@@ -43,7 +47,8 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float P_SCALE_FP8 = 1024.0f;   // f16 P is stored x 2^10 to stay clear of f16 subnormals
 constexpr uint64_t ATT_WAIT_NS = 1000000000ull;
 constexpr int ATT_SMEM_LIMIT = 227 * 1024;
-constexpr int MAX_NPAD = 128;
+constexpr int MAX_NPAD = 64;      // query vectors per (branch, kv head), padded to 16
+constexpr int MAX_TS = 8;         // = SPLIT_KEYS / TILE_KEYS
 
 struct AttnTcParams {
     KvView kv;
@@ -55,6 +60,7 @@ struct AttnTcParams {
     float *ws_o;           // [units][n_q][d]
     int32_t *err;
     int NS, NR;            // operand / raw ring depth
+    int TS, OB;            // S tiles held in TMEM at once (a chunk), O buffers (1 or 2)
     uint32_t tmem_cols;
     uint32_t off_q, off_p, off_raw, off_bar, off_small;  // shared-memory offsets
 };
@@ -70,7 +76,7 @@ struct AttnShape {
 };
 
 struct UnitInfo {
-    int b, g, split, pos_b, kv_end, s0, T;
+    int b, g, split, pos_b, kv_end, s0, T, n_chunks;
     bool bad_pos;
 };
 
@@ -86,6 +92,7 @@ __device__ __forceinline__ UnitInfo unit_info(const AttnTcParams &p, int u) {
     int n = ui.bad_pos ? 0 : ui.kv_end - ui.s0;
     n = n < 0 ? 0 : (n > SPLIT_KEYS ? SPLIT_KEYS : n);
     ui.T = (n + TILE_KEYS - 1) / TILE_KEYS;
+    ui.n_chunks = (ui.T + p.TS - 1) / p.TS;
     return ui;
 }
 
@@ -129,26 +136,26 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     const uint32_t s_q = s_op + p.off_q, s_p = s_op + p.off_p, s_rawb = s_op + p.off_raw;
     uint8_t *g_q = smem + p.off_q;
     uint8_t *g_p = smem + p.off_p;
-    const uint32_t bar0 = s_op + p.off_bar;
+    const int N_pad = p.N_pad, n_q = p.n_q, TS = p.TS;
     // barrier map
-    const uint32_t op_full = bar0, op_empty = op_full + 8 * p.NS;
+    const uint32_t op_full = s_op + p.off_bar, op_empty = op_full + 8 * p.NS;
     const uint32_t raw_full = op_empty + 8 * p.NS, raw_empty = raw_full + 8 * p.NR;
-    const uint32_t sfull = raw_empty + 8 * p.NR, sfree = sfull + 16;
-    const uint32_t pfull = sfree + 16, ofull = pfull + 8, ofree = ofull + 8, qready = ofree + 16, drain = qready + 8;
+    const uint32_t sfull = raw_empty + 8 * p.NR, sfree = sfull + 8 * TS;   // per S slot
+    const uint32_t pfull = sfree + 8 * TS, pfree = pfull + 16;             // P double buffer
+    const uint32_t ochunk = pfree + 16, ofree = ochunk + 8, qready = ofree + 16, drain = qready + 8;
     uint8_t *small = smem + p.off_small;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(small + 4);
     volatile int *fail_flag = reinterpret_cast<volatile int *>(small + 8);
-    volatile int *corr_flag = reinterpret_cast<volatile int *>(small + 12);  // [2]
-    float *red_max = reinterpret_cast<float *>(small + 64);                  // [4][N_pad]
-    float *red_sum = red_max + 4 * p.N_pad;                                  // [4][N_pad]
-    float *cor = red_sum + 4 * p.N_pad;                                      // [N_pad]
-    float *mnew = cor + p.N_pad;
-    float *mrun = mnew + p.N_pad;
-    float *lrun = mrun + p.N_pad;
+    volatile int *corr_flag = reinterpret_cast<volatile int *>(small + 12);
+    float *red_max = reinterpret_cast<float *>(small + 64);  // [4][N_pad]
+    float *red_sum = red_max + 4 * N_pad;                    // [4][N_pad]
+    float *cor = red_sum + 4 * N_pad;                        // [N_pad]
+    float *mnew = cor + N_pad;
+    float *mrun = mnew + N_pad;
+    float *lrun = mrun + N_pad;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int N_pad = p.N_pad, n_q = p.n_q;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.NS; ++s) {
@@ -159,19 +166,21 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             mbar_init(raw_full + 8 * s, 1);
             mbar_init(raw_empty + 8 * s, 4);
         }
+        for (int s = 0; s < TS; ++s) {
+            mbar_init(sfull + 8 * s, 1);
+            mbar_init(sfree + 8 * s, 4);
+        }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(sfull + 8 * a, 1);
-            mbar_init(sfree + 8 * a, 4);
+            mbar_init(pfull + 8 * a, 4);
+            mbar_init(pfree + 8 * a, 1);
             mbar_init(ofree + 8 * a, 4);
         }
-        mbar_init(pfull, 4);
-        mbar_init(ofull, 1);
+        mbar_init(ochunk, 1);
         mbar_init(qready, 4);
         mbar_init(drain, 1);
         *abort_flag = 0;
         *fail_flag = 0;
-        corr_flag[0] = 0;
-        corr_flag[1] = 0;
+        *corr_flag = 0;
         fence_mbar_init();
     }
     if (D == 64) {
@@ -192,105 +201,107 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t t_s = tmem, t_o = tmem + 2 * N_pad;  // S[2], O[2][NB]
+    const uint32_t t_o = tmem + (uint32_t)(TS * N_pad);  // S slots first, then O buffers
 
     const int BR = p.kv.page_size < TILE_KEYS ? p.kv.page_size : TILE_KEYS;  // rows per gather box
-    const int n_chunks = TILE_KEYS / BR;
+    const int n_chunks_tile = TILE_KEYS / BR;
 
     if (warp == 0) {
-        // ================= producer: page-gathered TMA loads =================
-        // Lanes look up the page of one box each; lane 0 announces the stage's bytes and
-        // issues the copies.
+        // ================= producer: page-gathered loads, per chunk K tiles then V tiles =================
         uint32_t gi = 0;
         bool ok = true;
         const uint32_t per_box = FP8 ? (uint32_t)(BR * D) : (uint32_t)(BR * 128 * S_::NATOM);
         for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
             const UnitInfo ui = unit_info(p, u);
-            for (int t = 0; t < ui.T && ok; ++t) {
-                const int key0 = ui.s0 + t * TILE_KEYS;
-                int rows[4];  // box row of chunks lane, lane+32, ... (n_chunks <= 128)
-                uint32_t nvalid = 0;
-#pragma unroll
-                for (int rr = 0; rr < 4; ++rr) {
-                    const int c = rr * 32 + lane;
-                    const int kc = key0 + c * BR;
-                    int row0 = -1;
-                    if (c < n_chunks && kc < ui.kv_end) {
-                        const int pg = page_of(p.kv, ui.b, kc);
-                        if (pg >= 0)
-                            row0 = (pg * p.kv.n_kv_heads + ui.g) * p.kv.page_size + (kc & (p.kv.page_size - 1));
-                        else
-                            raise_error(p.err, -pg);
-                    }
-                    rows[rr] = row0;
-                    nvalid += __popc(__ballot_sync(0xFFFFFFFFu, row0 >= 0));
-                }
-                for (int kv = 0; kv < 2; ++kv, ++gi) {
+            for (int ch = 0; ch < ui.n_chunks && ok; ++ch) {
+                const int t0 = ch * TS, t1 = min(ui.T, t0 + TS);
+                for (int kv = 0; kv < 2 && ok; ++kv) {
                     const CUtensorMap *map = kv ? &map_v : &map_k;
-                    uint32_t dst_base, bar;
-                    if (FP8) {
-                        const uint32_t s = gi % p.NR, ph = (gi / p.NR) & 1u;
-                        if (!warp_wait(raw_empty + 8 * s, ph ^ 1u, abort_flag)) { ok = false; break; }
-                        dst_base = s_rawb + s * S_::RAW_STAGE;
-                        bar = raw_full + 8 * s;
-                    } else {
-                        const uint32_t s = gi % p.NS, ph = (gi / p.NS) & 1u;
-                        if (!warp_wait(op_empty + 8 * s, ph ^ 1u, abort_flag)) { ok = false; break; }
-                        dst_base = s_op + s * S_::OP_STAGE;
-                        bar = op_full + 8 * s;
-                    }
-                    if (BR < 8) {
-                        // pages smaller than one 8-row swizzle atom: gather with plain copies
-                        // (a TMA box would not start on a 1024-byte boundary)
-                        const uint8_t *pool = reinterpret_cast<const uint8_t *>(kv ? p.kv.v_pool : p.kv.k_pool);
-                        uint8_t *dst = smem + (dst_base - s_op);
-                        constexpr int CH = FP8 ? D / 16 : D / 8;  // 16-byte pieces per row
-                        for (int i = lane; i < TILE_KEYS * CH; i += 32) {
-                            const int row = i / CH, ch = i % CH;
-                            const int key = key0 + row;
-                            if (key >= ui.kv_end) continue;
-                            const int pg = page_of(p.kv, ui.b, key);
-                            if (pg < 0) continue;
-                            const size_t elem = ((size_t)(pg * p.kv.n_kv_heads + ui.g) * p.kv.page_size +
-                                                 (key & (p.kv.page_size - 1))) * D;
-                            if (FP8) {
-                                *reinterpret_cast<uint4 *>(dst + row * D + ch * 16) =
-                                    __ldg(reinterpret_cast<const uint4 *>(pool + elem + ch * 16));
-                            } else {
-                                *reinterpret_cast<uint4 *>(dst + sw128_off(row, ch * 8, TILE_KEYS * 128)) =
-                                    __ldg(reinterpret_cast<const uint4 *>(pool + 2 * elem + ch * 16));
+                    for (int t = t0; t < t1; ++t, ++gi) {
+                        const int key0 = ui.s0 + t * TILE_KEYS;
+                        int rows[4];  // box row of chunk lane, lane+32, ... (<= 128 chunks)
+                        uint32_t nvalid = 0;
+#pragma unroll
+                        for (int rr = 0; rr < 4; ++rr) {
+                            const int c = rr * 32 + lane;
+                            const int kc = key0 + c * BR;
+                            int row0 = -1;
+                            if (c < n_chunks_tile && kc < ui.kv_end) {
+                                const int pg = page_of(p.kv, ui.b, kc);
+                                if (pg >= 0)
+                                    row0 = (pg * p.kv.n_kv_heads + ui.g) * p.kv.page_size +
+                                           (kc & (p.kv.page_size - 1));
+                                else if (kv == 0)
+                                    raise_error(p.err, -pg);
                             }
+                            rows[rr] = row0;
+                            nvalid += __popc(__ballot_sync(0xFFFFFFFFu, row0 >= 0));
                         }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(bar);
-                        __syncwarp();
-                        continue;
-                    }
-                    if (lane == 0) {
-                        if (nvalid) mbar_arrive_expect_tx(bar, nvalid * per_box);
-                        else mbar_arrive(bar);
-                    }
-#pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) {
-                        if (rr * 32 >= n_chunks) break;
-                        for (int cc = 0; cc < 32; ++cc) {
-                            const int c = rr * 32 + cc;
-                            if (c >= n_chunks) break;
-                            const int row0 = __shfl_sync(0xFFFFFFFFu, rows[rr], cc);
-                            if (lane == 0 && row0 >= 0) {
+                        uint32_t dst_base, bar;
+                        if (FP8) {
+                            const uint32_t s = gi % p.NR, ph = (gi / p.NR) & 1u;
+                            if (!warp_wait(raw_empty + 8 * s, ph ^ 1u, abort_flag)) { ok = false; break; }
+                            dst_base = s_rawb + s * S_::RAW_STAGE;
+                            bar = raw_full + 8 * s;
+                        } else {
+                            const uint32_t s = gi % p.NS, ph = (gi / p.NS) & 1u;
+                            if (!warp_wait(op_empty + 8 * s, ph ^ 1u, abort_flag)) { ok = false; break; }
+                            dst_base = s_op + s * S_::OP_STAGE;
+                            bar = op_full + 8 * s;
+                        }
+                        if (BR < 8) {
+                            // pages smaller than one 8-row swizzle atom: gather with plain copies
+                            // (a TMA box would not start on a 1024-byte boundary)
+                            const uint8_t *pool = reinterpret_cast<const uint8_t *>(kv ? p.kv.v_pool : p.kv.k_pool);
+                            uint8_t *dst = smem + (dst_base - s_op);
+                            constexpr int CH = FP8 ? D / 16 : D / 8;  // 16-byte pieces per row
+                            for (int i = lane; i < TILE_KEYS * CH; i += 32) {
+                                const int row = i / CH, chn = i % CH;
+                                const int key = key0 + row;
+                                if (key >= ui.kv_end) continue;
+                                const int pg = page_of(p.kv, ui.b, key);
+                                if (pg < 0) continue;
+                                const size_t elem = ((size_t)(pg * p.kv.n_kv_heads + ui.g) * p.kv.page_size +
+                                                     (key & (p.kv.page_size - 1))) * D;
                                 if (FP8) {
-                                    tma_load_2d(dst_base + c * BR * D, map, 0, row0, bar);
+                                    *reinterpret_cast<uint4 *>(dst + row * D + chn * 16) =
+                                        __ldg(reinterpret_cast<const uint4 *>(pool + elem + chn * 16));
                                 } else {
+                                    *reinterpret_cast<uint4 *>(dst + sw128_off(row, chn * 8, TILE_KEYS * 128)) =
+                                        __ldg(reinterpret_cast<const uint4 *>(pool + 2 * elem + chn * 16));
+                                }
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bar);
+                            __syncwarp();
+                            continue;
+                        }
+                        if (lane == 0) {
+                            if (nvalid) mbar_arrive_expect_tx(bar, nvalid * per_box);
+                            else mbar_arrive(bar);
+                        }
 #pragma unroll
-                                    for (int a = 0; a < S_::NATOM; ++a)
-                                        tma_load_2d(dst_base + a * (TILE_KEYS * 128) + c * BR * 128, map, a * 64, row0,
-                                                    bar);
+                        for (int rr = 0; rr < 4; ++rr) {
+                            if (rr * 32 >= n_chunks_tile) break;
+                            for (int cc = 0; cc < 32; ++cc) {
+                                const int c = rr * 32 + cc;
+                                if (c >= n_chunks_tile) break;
+                                const int row0 = __shfl_sync(0xFFFFFFFFu, rows[rr], cc);
+                                if (lane == 0 && row0 >= 0) {
+                                    if (FP8) {
+                                        tma_load_2d(dst_base + c * BR * D, map, 0, row0, bar);
+                                    } else {
+#pragma unroll
+                                        for (int a = 0; a < S_::NATOM; ++a)
+                                            tma_load_2d(dst_base + a * (TILE_KEYS * 128) + c * BR * 128, map, a * 64,
+                                                        row0, bar);
+                                    }
                                 }
                             }
                         }
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
             }
         }
@@ -313,78 +324,98 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         const uint32_t idesc_s = idesc_f16kind(128, N_pad, FP8, false, false);
         const uint32_t idesc_pv = idesc_f16kind(128, N_pad, FP8, true, false);
         const uint32_t qblk = (uint32_t)N_pad * 128, pblk = (uint32_t)N_pad * 128;
-        uint32_t gt = 0, ul = 0;
+        uint32_t gi = 0, gt = 0, ul = 0;
+        uint32_t slot_use[MAX_TS];
+#pragma unroll
+        for (int s = 0; s < MAX_TS; ++s) slot_use[s] = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
             const UnitInfo ui = unit_info(p, u);
             if (ui.T == 0) continue;
-            const uint32_t ob = ul & 1u;
-            if (!warp_wait(ofree + 8 * ob, ((ul >> 1) & 1u) ^ 1u, abort_flag) ||
-                !warp_wait(qready, ul & 1u, abort_flag)) {
+            const uint32_t ob = p.OB == 2 ? (ul & 1u) : 0u;
+            const uint32_t ob_use = p.OB == 2 ? (ul >> 1) : ul;
+            if (!warp_wait(qready, ul & 1u, abort_flag) ||
+                !warp_wait(ofree + 8 * ob, (ob_use & 1u) ^ 1u, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            auto issue_s = [&](uint32_t tt) -> bool {  // tt = global tile index
-                const uint32_t gi = 2 * tt, s = gi % p.NS, ph = (gi / p.NS) & 1u;
-                if (!warp_wait(op_full + 8 * s, ph, abort_flag)) return false;
-                if (!warp_wait(sfree + 8 * (tt & 1u), ((tt >> 1) & 1u) ^ 1u, abort_flag)) return false;
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t a_base = s_op + s * S_::OP_STAGE;
+            for (int ch = 0; ch < ui.n_chunks && ok; ++ch) {
+                const int t0 = ch * TS, t1 = min(ui.T, t0 + TS);
+                // S of every tile of the chunk
+                for (int t = t0; t < t1; ++t, ++gi) {
+                    const int slot = t - t0;
+                    uint32_t su = 0;
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t blk = ks >> 2, off = (ks & 3) * 32;
-                        mma_bf16(t_s + (tt & 1u) * N_pad, desc_kmajor_sw128(a_base + blk * (TILE_KEYS * 128) + off),
-                                 desc_kmajor_sw128(s_q + blk * qblk + off), idesc_s, ks > 0 ? 1u : 0u);
+                    for (int s = 0; s < MAX_TS; ++s)
+                        if (s == slot) su = slot_use[s];
+                    const uint32_t st = gi % p.NS;
+                    if (!warp_wait(op_full + 8 * st, (gi / p.NS) & 1u, abort_flag) ||
+                        !warp_wait(sfree + 8 * slot, (su & 1u) ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                    mma_commit(op_empty + 8 * s);
-                    mma_commit(sfull + 8 * (tt & 1u));
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t a_base = s_op + st * S_::OP_STAGE;
+#pragma unroll
+                        for (int ks = 0; ks < D / 16; ++ks) {
+                            const uint32_t blk = ks >> 2, off = (ks & 3) * 32;
+                            mma_bf16(tmem + slot * N_pad, desc_kmajor_sw128(a_base + blk * (TILE_KEYS * 128) + off),
+                                     desc_kmajor_sw128(s_q + blk * qblk + off), idesc_s, ks > 0 ? 1u : 0u);
+                        }
+                        mma_commit(op_empty + 8 * st);
+                        mma_commit(sfull + 8 * slot);
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int s = 0; s < MAX_TS; ++s)
+                        if (s == slot) slot_use[s] = su + 1;
                 }
-                __syncwarp();
-                return true;
-            };
-            if (!issue_s(gt)) { ok = false; break; }
-            for (int t = 0; t < ui.T; ++t) {
-                const uint32_t tt = gt + t;
-                if (t + 1 < ui.T && !issue_s(tt + 1)) { ok = false; break; }
-                const uint32_t gi = 2 * tt + 1, s = gi % p.NS, ph = (gi / p.NS) & 1u;
-                if (!warp_wait(op_full + 8 * s, ph, abort_flag)) { ok = false; break; }
-                const uint32_t vbase = s_op + s * S_::OP_STAGE;
-                const int key0 = ui.s0 + t * TILE_KEYS;
-                const int nvk = ui.kv_end - key0;  // valid keys in this tile
-                if (nvk < TILE_KEYS) {
-                    // keys past the branch's last position: zero their V rows (NaN-safe P.V)
-                    uint4 *vb = reinterpret_cast<uint4 *>(smem + s * S_::OP_STAGE);
-                    const int rows = TILE_KEYS - nvk;
-                    for (int i = lane; i < rows * S_::NATOM * 8; i += 32) {
-                        const int a = i / (rows * 8), rem = i % (rows * 8);
-                        const int r = nvk + rem / 8, ch = rem % 8;
-                        vb[(a * TILE_KEYS * 128 + r * 128) / 16 + ch] = make_uint4(0, 0, 0, 0);
+                if (!ok) break;
+                // P.V of every tile of the chunk, in order
+                for (int t = t0; t < t1; ++t, ++gi, ++gt) {
+                    const uint32_t st = gi % p.NS;
+                    if (!warp_wait(op_full + 8 * st, (gi / p.NS) & 1u, abort_flag)) { ok = false; break; }
+                    const int key0 = ui.s0 + t * TILE_KEYS;
+                    const int nvk = ui.kv_end - key0;  // valid keys in this tile
+                    if (nvk < TILE_KEYS) {
+                        // keys past the branch's last position: zero their V rows (NaN-safe P.V)
+                        uint4 *vb = reinterpret_cast<uint4 *>(smem + st * S_::OP_STAGE);
+                        const int rows = TILE_KEYS - nvk;
+                        for (int i = lane; i < rows * S_::NATOM * 8; i += 32) {
+                            const int a = i / (rows * 8), rem = i % (rows * 8);
+                            const int r = nvk + rem / 8, c = rem % 8;
+                            vb[(a * TILE_KEYS * 128 + r * 128) / 16 + c] = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
                     }
-                    fence_proxy_async_smem();
+                    const uint32_t pb = gt & 1u;
+                    if (!warp_wait(pfull + 8 * pb, (gt >> 1) & 1u, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+                    if (lane == 0) {
+                        const uint32_t vbase = s_op + st * S_::OP_STAGE, pbase = s_p + pb * 2 * pblk;
+#pragma unroll
+                        for (int nb = 0; nb < S_::NB; ++nb) {
+#pragma unroll
+                            for (int ks = 0; ks < TILE_KEYS / 16; ++ks) {
+                                const uint64_t ad = desc_mnmajor_sw128(vbase + (2 * nb) * (TILE_KEYS * 128) + ks * 2048,
+                                                                       TILE_KEYS * 128);
+                                const uint64_t bd = desc_kmajor_sw128(pbase + (ks >> 2) * pblk + (ks & 3) * 32);
+                                mma_bf16(t_o + (ob * S_::NB + nb) * N_pad, ad, bd, idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
+                            }
+                        }
+                        mma_commit(op_empty + 8 * st);
+                        mma_commit(pfree + 8 * pb);
+                    }
                     __syncwarp();
                 }
-                if (!warp_wait(pfull, tt & 1u, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                if (lane == 0) {
-#pragma unroll
-                    for (int nb = 0; nb < S_::NB; ++nb) {
-#pragma unroll
-                        for (int ks = 0; ks < TILE_KEYS / 16; ++ks) {
-                            const uint64_t ad = desc_mnmajor_sw128(vbase + (2 * nb) * (TILE_KEYS * 128) + ks * 2048,
-                                                                   TILE_KEYS * 128);
-                            const uint64_t bd = desc_kmajor_sw128(s_p + (ks >> 2) * pblk + (ks & 3) * 32);
-                            mma_bf16(t_o + (ob * S_::NB + nb) * N_pad, ad, bd, idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
-                        }
-                    }
-                    mma_commit(op_empty + 8 * s);
-                    mma_commit(ofull);
-                }
+                if (!ok) break;
+                if (lane == 0) mma_commit(ochunk);
                 __syncwarp();
             }
             if (!ok) break;
-            gt += ui.T;
             ++ul;
         }
         if (!ok) {
@@ -403,10 +434,16 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         // waiting at a barrier that another warp will never reach.
         const int q = warp & 3;
         const int etid = threadIdx.x - 64;  // 0..127
-        const int kk = q * 32 + lane;       // key within the tile / d row within a 128-block
+        const int kk = q * 32 + lane;       // key within a tile / d row within a 128-block
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const uint32_t qblk = (uint32_t)N_pad * 128, pblk = (uint32_t)N_pad * 128;
-        uint32_t gt = 0, ul = 0;
+        // byte offset of this thread's key column in P row 0 (the row's swizzle is added per row)
+        const uint32_t p_col = (uint32_t)(kk >> 6) * pblk + ((kk & 7) << 1);
+        const uint32_t p_chunk = (uint32_t)((kk & 63) >> 3);
+        uint32_t gt = 0, gch = 0, ul = 0;
+        uint32_t slot_use[MAX_TS];
+#pragma unroll
+        for (int s = 0; s < MAX_TS; ++s) slot_use[s] = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
             const UnitInfo ui = unit_info(p, u);
@@ -449,40 +486,53 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(qready);
             named_bar(1, 128);
-            const uint32_t ob = ul & 1u;
+            const uint32_t ob = p.OB == 2 ? (ul & 1u) : 0u;
             bool failed = false;
-            for (int t = 0; t < ui.T; ++t) {
-                const uint32_t tt = gt + t;
-                const int key = ui.s0 + t * TILE_KEYS + kk;
-                const bool kvalid = key < ui.kv_end;
-                float ksc = 1.f, vsc = 1.f;
-                if (kvalid) {
-                    const int pg = page_of(p.kv, ui.b, key);
-                    if (pg < 0) failed = true;
-                    else if (FP8) {
-                        const size_t si = (size_t)pg * p.kv.n_kv_heads + ui.g;
-                        ksc = __ldg(p.kv.k_scale + si);
-                        vsc = __ldg(p.kv.v_scale + si) * P_SCALE_FP8;
+            for (int ch = 0; ch < ui.n_chunks; ++ch) {
+                const int t0 = ch * TS, t1 = min(ui.T, t0 + TS);
+                // ---- pass A: each column's maximum over the chunk's keys ----
+                float mth[MAX_NPAD];
+#pragma unroll
+                for (int c = 0; c < MAX_NPAD; ++c) mth[c] = -INFINITY;
+                for (int t = t0; t < t1; ++t) {
+                    const int slot = t - t0;
+                    uint32_t su = 0;
+#pragma unroll
+                    for (int s = 0; s < MAX_TS; ++s)
+                        if (s == slot) su = slot_use[s];
+                    const int key = ui.s0 + t * TILE_KEYS + kk;
+                    const bool kvalid = key < ui.kv_end;
+                    float ksc = 1.f;
+                    if (kvalid) {
+                        const int pg = page_of(p.kv, ui.b, key);
+                        if (pg < 0) failed = true;
+                        else if (FP8) ksc = __ldg(p.kv.k_scale + (size_t)pg * p.kv.n_kv_heads + ui.g);
+                    }
+                    if (ok) ok = warp_wait(sfull + 8 * slot, su & 1u, abort_flag);
+                    if (!ok) continue;
+                    tc_fence_after();
+                    const float sl = p.scale_log2 * ksc;
+                    const int jmax = ui.pos_b - key;  // a row j sees this key iff j >= -jmax... key <= pos_b + j
+#pragma unroll
+                    for (int c0 = 0; c0 < MAX_NPAD; c0 += 16) {
+                        if (c0 < n_q) {
+                            uint32_t r[16];
+                            tmem_ld16(tmem + lane_base + slot * N_pad + c0, r);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int c = c0 + j;
+                                const bool valid = kvalid && c < n_q && (c / p.G) >= -jmax;
+                                mth[c] = valid ? fmaxf(mth[c], __uint_as_float(r[j]) * sl) : mth[c];
+                            }
+                        }
                     }
                 }
-                if (ok) ok = warp_wait(sfull + 8 * (tt & 1u), (tt >> 1) & 1u, abort_flag);
-                const uint32_t s_addr = t_s + lane_base + (tt & 1u) * N_pad;
-                const float sl = p.scale_log2 * ksc;
-                if (ok) {
-                    tc_fence_after();
-                    // pass 1: column maxima over the tile's 128 keys
-                    for (int c0 = 0; c0 < n_q; c0 += 16) {
-                        uint32_t r[16];
-                        tmem_ld16(s_addr + c0, r);
-                        tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int c = c0 + j;
-                            const bool valid = kvalid && c < n_q && key <= ui.pos_b + c / p.G;
-                            const float sv = valid ? __uint_as_float(r[j]) * sl : -INFINITY;
-                            const float mx = warp_max(sv);
-                            if (lane == 0) red_max[q * N_pad + c] = mx;
-                        }
+                for (int c = 0; c < MAX_NPAD; ++c) {
+                    if (c < n_q) {
+                        const float mx = warp_max(mth[c]);
+                        if (lane == 0) red_max[q * N_pad + c] = mx;
                     }
                 }
                 named_bar(1, 128);
@@ -495,72 +545,111 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                     cor[etid] = cr;
                     mnew[etid] = mn;
                     mrun[etid] = mn;
-                    if (cr != 1.f) corr_flag[tt & 1u] = 1;
+                    if (ch > 0 && cr != 1.f) *corr_flag = 1;
                 }
-                if (etid == 0) corr_flag[(tt + 1) & 1u] = 0;
                 named_bar(1, 128);
-                // the previous P.V has finished: the P buffer and O are free
-                if (ok && tt > 0) {
-                    ok = warp_wait(ofull, (tt - 1) & 1u, abort_flag);
-                    if (ok) tc_fence_after();
+                // ---- a later chunk whose maximum grew: rescale O once all earlier P.V are done ----
+                if (ch > 0 && *corr_flag) {
+                    if (ok) ok = warp_wait(ochunk, (gch - 1) & 1u, abort_flag);
+                    if (ok) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int nb = 0; nb < S_::NB; ++nb) {
+                            const uint32_t o_addr = t_o + lane_base + (ob * S_::NB + nb) * N_pad;
+                            for (int c0 = 0; c0 < n_q; c0 += 16) {
+                                uint32_t r[16];
+                                tmem_ld16(o_addr + c0, r);
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int j = 0; j < 16; ++j)
+                                    r[j] = __float_as_uint(__uint_as_float(r[j]) * cor[c0 + j]);
+                                tmem_st16(o_addr + c0, r);
+                            }
+                        }
+                        tmem_st_wait();
+                        tc_fence_before();
+                    }
                 }
-                if (ok && t > 0 && corr_flag[tt & 1u]) {
+                // ---- pass B: P = exp2(s - m) for P.V, per-thread sums ----
+                float lth[MAX_NPAD];
 #pragma unroll
-                    for (int nb = 0; nb < S_::NB; ++nb) {
-                        const uint32_t o_addr = t_o + lane_base + (ob * S_::NB + nb) * N_pad;
-                        for (int c0 = 0; c0 < n_q; c0 += 16) {
-                            uint32_t r[16];
-                            tmem_ld16(o_addr + c0, r);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * cor[c0 + j]);
-                            tmem_st16(o_addr + c0, r);
+                for (int c = 0; c < MAX_NPAD; ++c) lth[c] = 0.f;
+                for (int t = t0; t < t1; ++t, ++gt) {
+                    const int slot = t - t0;
+                    const int key = ui.s0 + t * TILE_KEYS + kk;
+                    const bool kvalid = key < ui.kv_end;
+                    float ksc = 1.f, vsc = 1.f;
+                    if (kvalid && FP8) {
+                        const int pg = page_of(p.kv, ui.b, key);
+                        if (pg >= 0) {
+                            const size_t si = (size_t)pg * p.kv.n_kv_heads + ui.g;
+                            ksc = __ldg(p.kv.k_scale + si);
+                            vsc = __ldg(p.kv.v_scale + si) * P_SCALE_FP8;
                         }
                     }
-                    tmem_st_wait();
-                }
-                if (ok) {
-                    // pass 2: P = exp2(s - m) into shared memory (K-major, swizzled), column sums
-                    for (int c0 = 0; c0 < n_q; c0 += 16) {
-                        uint32_t r[16];
-                        tmem_ld16(s_addr + c0, r);
-                        tmem_ld_wait();
+                    const uint32_t pb = gt & 1u;
+                    if (ok) ok = warp_wait(pfree + 8 * pb, ((gt >> 1) & 1u) ^ 1u, abort_flag);
+                    if (!ok) continue;
+                    const float sl = p.scale_log2 * ksc;
+                    const int jmax = ui.pos_b - key;
+                    uint8_t *pbuf = g_p + pb * 2 * pblk + p_col;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int c = c0 + j;
-                            const bool valid = kvalid && c < n_q && key <= ui.pos_b + c / p.G;
-                            const float pv = valid ? exp2f(__uint_as_float(r[j]) * sl - mnew[c]) : 0.f;
-                            const float sum = warp_sum(pv);
-                            if (lane == 0) red_sum[q * N_pad + c] = sum;
-                            uint16_t bits;
-                            if (FP8) {
-                                __half h = __float2half_rn(pv * vsc);
-                                bits = *reinterpret_cast<uint16_t *>(&h);
-                            } else {
-                                __nv_bfloat16 h = __float2bfloat16_rn(pv);
-                                bits = *reinterpret_cast<uint16_t *>(&h);
+                    for (int c0 = 0; c0 < MAX_NPAD; c0 += 16) {
+                        if (c0 < N_pad) {
+                            uint32_t r[16];
+                            if (c0 < n_q) {
+                                tmem_ld16(tmem + lane_base + slot * N_pad + c0, r);
+                                tmem_ld_wait();
                             }
-                            *reinterpret_cast<uint16_t *>(g_p + sw128_off(c, kk, pblk)) = bits;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int c = c0 + j;
+                                const bool valid = kvalid && c < n_q && (c / p.G) >= -jmax;
+                                const float pv = valid ? exp2f(__uint_as_float(r[j]) * sl - mnew[c]) : 0.f;
+                                lth[c] += pv;
+                                uint16_t bits;
+                                if (FP8) {
+                                    __half h = __float2half_rn(pv * vsc);
+                                    bits = *reinterpret_cast<uint16_t *>(&h);
+                                } else {
+                                    __nv_bfloat16 h = __float2bfloat16_rn(pv);
+                                    bits = *reinterpret_cast<uint16_t *>(&h);
+                                }
+                                *reinterpret_cast<uint16_t *>(pbuf + c * 128 + (((p_chunk ^ (c & 7)) & 7) << 4)) = bits;
+                            }
                         }
                     }
                     tc_fence_before();
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        mbar_arrive(sfree + 8 * (tt & 1u));
-                        mbar_arrive(pfull);
+                        mbar_arrive(sfree + 8 * slot);
+                        mbar_arrive(pfull + 8 * pb);
+                    }
+                }
+#pragma unroll
+                for (int s = 0; s < MAX_TS; ++s)
+                    if (s < t1 - t0) slot_use[s] += 1;
+                // ---- one cross-lane sum per column ----
+#pragma unroll
+                for (int c = 0; c < MAX_NPAD; ++c) {
+                    if (c < n_q) {
+                        const float sm = warp_sum(lth[c]);
+                        if (lane == 0) red_sum[q * N_pad + c] = sm;
                     }
                 }
                 named_bar(1, 128);
                 if (etid < n_q)
                     lrun[etid] = lrun[etid] * cor[etid] + ((red_sum[etid] + red_sum[N_pad + etid]) +
                                                            (red_sum[2 * N_pad + etid] + red_sum[3 * N_pad + etid]));
+                if (etid == 0) *corr_flag = 0;
+                ++gch;
+                named_bar(1, 128);
             }
             if (failed) *fail_flag = 1;
-            gt += ui.T;
             // the unit's last P.V, then its partial
             if (ok) {
-                ok = warp_wait(ofull, (gt - 1) & 1u, abort_flag);
+                ok = warp_wait(ochunk, (gch - 1) & 1u, abort_flag);
                 if (ok) tc_fence_after();
             }
             named_bar(1, 128);
@@ -616,8 +705,8 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                 const uint8_t *raw = smem + p.off_raw + rs * S_::RAW_STAGE;
                 uint8_t *op = smem + os * S_::OP_STAGE;
                 constexpr int CPR = D / 16;  // 16-byte chunks per raw row
-                for (int ch = ctid; ch < TILE_KEYS * CPR; ch += 128) {
-                    const int row = ch / CPR, cc = ch % CPR;
+                for (int chn = ctid; chn < TILE_KEYS * CPR; chn += 128) {
+                    const int row = chn / CPR, cc = chn % CPR;
                     const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * D + cc * 16);
                     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
                     uint32_t h[8];
@@ -724,6 +813,8 @@ static EncodeTiledFnA encode_fn_attn() {
 }
 
 // The pool viewed as [num_pages * Hkv * page_size rows][d] with a (box_cols x box_rows) box.
+// No L2 promotion: a promoted fetch may reach past the box, and for the last rows of a
+// tensor that ends at the end of its mapping that would touch unmapped memory.
 static bool make_pool_map(CUtensorMap *map, const void *base, const KvView &kv, bool fp8, int box_rows) {
     EncodeTiledFnA fn = encode_fn_attn();
     if (!fn) return false;
@@ -735,7 +826,7 @@ static bool make_pool_map(CUtensorMap *map, const void *base, const KvView &kv, 
     cuuint32_t estr[2] = {1, 1};
     return fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -751,7 +842,7 @@ static int launch_attn_tc(AttnTcParams &p, cudaStream_t s) {
     using S_ = AttnShape<D, FP8>;
     const int NATOM = S_::NATOM;
     p.off_q = 0;  // set below
-    const uint32_t q_bytes = NATOM * p.N_pad * 128, p_bytes = 2 * p.N_pad * 128;
+    const uint32_t q_bytes = NATOM * p.N_pad * 128, p_bytes = 2 * 2 * p.N_pad * 128;  // P: 2 buffers
     const uint32_t small = 64 + 12 * p.N_pad * 4 + 64;
     const uint32_t bars = 8 * 64;
     const uint32_t fixed = 1024 + q_bytes + p_bytes + small + bars;
@@ -824,7 +915,15 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     const int n_q = (k + 1) * G;
     const int N_pad = ((n_q + 15) / 16) * 16;
     const int NB = kvd->head_dim <= 128 ? 1 : 2;
-    if (N_pad > spec::MAX_NPAD || 2 * N_pad + 2 * NB * N_pad > 512) return SPEC_ERR_UNSUPPORTED;
+    if (N_pad > spec::MAX_NPAD) return SPEC_ERR_UNSUPPORTED;
+    // TMEM: TS S tiles of N_pad columns + OB output buffers of NB*N_pad columns <= 512
+    int OB = 2, TS = (512 - 2 * NB * N_pad) / N_pad;
+    if (TS < spec::MAX_TS) {
+        OB = 1;
+        TS = (512 - NB * N_pad) / N_pad;
+    }
+    TS = TS > spec::MAX_TS ? spec::MAX_TS : TS;
+    if (TS < 1) return SPEC_ERR_UNSUPPORTED;
     spec::AttnTcParams p{};
     p.kv = spec::make_view(kvd);
     p.pos = pos;
@@ -845,8 +944,10 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     p.ws_ml = (float *)ws;
     p.ws_o = (float *)((char *)ws + ml);
     p.err = dev_err;
+    p.TS = TS;
+    p.OB = OB;
     uint32_t cols = 32;
-    while (cols < (uint32_t)(2 * N_pad + 2 * NB * N_pad)) cols <<= 1;
+    while (cols < (uint32_t)(TS * N_pad + OB * NB * N_pad)) cols <<= 1;
     p.tmem_cols = cols;
     cudaStream_t s = (cudaStream_t)stream;
     const bool fp8 = kvd->kv_dtype == SPEC_KV_FP8_E4M3;

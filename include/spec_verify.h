@@ -153,7 +153,8 @@ int spec_kv_write_rows(const spec_kv_desc *kv, const int32_t *row_branch,
  *   ws      device workspace of spec_verify_attn_workspace(...) bytes, 256-byte
  *           aligned, contents need not be initialised.
  * Host errors: NULL, B < 1, k out of range, n_q_heads % n_kv_heads != 0,
- * head_dim not 64/128/256, max_pos < k+1, workspace too small.
+ * head_dim not 64/128/256, max_pos < k+1, workspace too small; SPEC_ERR_UNSUPPORTED
+ * when (k+1)*G, the query vectors sharing one kv head, exceeds 64.
  * Device errors: as spec_kv_append (the row's output is then left unwritten). */
 size_t spec_verify_attn_workspace(const spec_kv_desc *kv, int B, int k, int n_q_heads,
                                   int max_pos);
