@@ -112,11 +112,13 @@ def _setup_workload(cid: int, dev: str):
                                                                 verify_inputs)
     draft = None
     if cid == 4:
-        # the verify that follows the draft side (workload 2 with k = 4); the draft side's
-        # own kernels are not part of this timed step
+        # the draft side (MTP input for 64 rows, draft head + d2t), then the verify of
+        # workload 2 with k = 4; the LM head weight doubles as the tied embedding table
         dc = DRAFT_CONFIG
         cfg = config4_verify(dc)
-        vi = verify_inputs(cfg, device=dev)
+        W = make_lm_head(cfg.V, cfg.H, cfg.seed + 7, dev)
+        draft = draft_inputs(dc, device=dev, E=W)
+        vi = verify_inputs(cfg, device=dev, W=W)
     else:
         cfg = CONFIGS[cid]
         vi = verify_inputs(cfg, device=dev)
@@ -196,7 +198,11 @@ def run_ours(args):
     def flush():
         flush_buf.fill_(1)
 
+    def log(msg):
+        print(f"[bench] {msg}", file=sys.stderr, flush=True)
+
     def measure(cid, steps, warmup, with_e2e=False):
+        log(f"workload {cid}: set-up")
         w = _setup_workload(cid, dev)
         step, inp, c = w["step"], w["inputs"], w["cfg"]
         ds = DraftStage(w["draft"], dev) if w["draft"] is not None else None
@@ -206,10 +212,12 @@ def run_ours(args):
                 ds.run()
             step.run(inp["pos"], inp["q"], inp["k_new"], inp["v_new"], inp["hidden"], inp["drafts"])
 
+        log(f"workload {cid}: eager steps")
         for _ in range(2):
             one()
         torch.cuda.synchronize()
         assert int(step.out.dev_err.item()) == 0, "device error during the step"
+        log(f"workload {cid}: graph")
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             one()
@@ -228,6 +236,7 @@ def run_ours(args):
         clocks = sampler.stop() if sampler else None
         if world > 1:
             dist.barrier()
+        log(f"workload {cid}: per-kernel timing")
         # per-kernel times of the two bandwidth kernels (same stream, same flush)
         o, kv = step.out, step.kv
         t_attn = _time_region(lambda: bnd.spec_verify_attn(kv.desc, inp["pos"], c.B, c.k, c.Hq, inp["q"], step.scale,
@@ -240,7 +249,9 @@ def run_ours(args):
                    t_head=statistics.median(t_head), kv_bytes=w["kv_bytes"], w_bytes=w["w_bytes"], clocks=clocks,
                    launches=step.launches_per_step + (4 if ds is not None else 0))
         if with_e2e:
+            log(f"workload {cid}: end to end")
             res["e2e"] = measure_e2e(step, inp, steps, flush)
+        log(f"workload {cid}: done")
         del w, step, graph
         torch.cuda.empty_cache()
         return res

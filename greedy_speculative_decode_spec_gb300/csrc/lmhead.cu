@@ -186,6 +186,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // every MMA issued by this thread completes before TMEM is released
             mma_commit(drain);
             mbar_wait(drain, 0, nullptr, WAIT_NS);
+            // and every arrive those MMAs' commits send is delivered before the CTA may exit:
+            // wait for the last phase of each stage's "empty" barrier (a late arrive would
+            // land in shared memory this CTA no longer owns)
+            const uint32_t n_last = it < (uint32_t)p.stages ? it : (uint32_t)p.stages;
+            for (uint32_t j = 0; j < n_last; ++j) {
+                const uint32_t i2 = it - 1 - j;
+                mbar_wait(empty0 + 8 * (i2 % p.stages), (i2 / p.stages) & 1u, nullptr, WAIT_NS);
+            }
         }
     } else {
         // ---------------- epilogue: 4 warps, one TMEM lane quadrant each ----------------
@@ -343,8 +351,6 @@ static EncodeTiledFn encode_fn() {
 }
 
 // 2-D bf16 row-major [rows][cols] map with a (64 x box_rows) box and 128-byte swizzle.
-// No L2 promotion: a promoted fetch may reach past the box, and for the last rows of a
-// tensor that ends at the end of its mapping that would touch unmapped memory.
 static bool make_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -353,7 +359,7 @@ static bool make_map(CUtensorMap *map, const void *base, int rows, int cols, int
     cuuint32_t box[2] = {(cuuint32_t)TC_BK, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -49,14 +49,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase of the given parity to complete. Gives up (returns false) when
-// *abort becomes non-zero or after timeout_ns of wall time, so no wait can hang.
+// *abort becomes non-zero (abort may be null: then only the time limit applies) or after
+// timeout_ns of wall time, so no wait can hang.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           uint64_t timeout_ns) {
     uint64_t t0 = 0;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 31u) == 0) {
-            if (*abort) return false;
+            if (abort != nullptr && *abort) return false;
             const uint64_t t = globaltimer();
             if (t0 == 0) t0 = t;
             else if (t - t0 > timeout_ns) return false;

@@ -425,6 +425,18 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         if (lane == 0) {
             mma_commit(drain);
             mbar_wait(drain, 0, nullptr, ATT_WAIT_NS);
+            // every arrive sent by this thread's commits is delivered before the CTA may exit:
+            // the last phase of each operand stage's "empty" barrier and of both P buffers'
+            // "free" barriers (the others were waited on by their consumers)
+            const uint32_t n_last = gi < (uint32_t)p.NS ? gi : (uint32_t)p.NS;
+            for (uint32_t j = 0; j < n_last; ++j) {
+                const uint32_t i2 = gi - 1 - j;
+                mbar_wait(op_empty + 8 * (i2 % p.NS), (i2 / p.NS) & 1u, nullptr, ATT_WAIT_NS);
+            }
+            for (uint32_t j = 0; j < 2 && j < gt; ++j) {
+                const uint32_t t2 = gt - 1 - j;
+                mbar_wait(pfree + 8 * (t2 & 1u), (t2 >> 1) & 1u, nullptr, ATT_WAIT_NS);
+            }
         }
         __syncwarp();
     } else if (warp < 6) {
@@ -813,8 +825,6 @@ static EncodeTiledFnA encode_fn_attn() {
 }
 
 // The pool viewed as [num_pages * Hkv * page_size rows][d] with a (box_cols x box_rows) box.
-// No L2 promotion: a promoted fetch may reach past the box, and for the last rows of a
-// tensor that ends at the end of its mapping that would touch unmapped memory.
 static bool make_pool_map(CUtensorMap *map, const void *base, const KvView &kv, bool fp8, int box_rows) {
     EncodeTiledFnA fn = encode_fn_attn();
     if (!fn) return false;
@@ -826,7 +836,7 @@ static bool make_pool_map(CUtensorMap *map, const void *base, const KvView &kv, 
     cuuint32_t estr[2] = {1, 1};
     return fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -85,8 +85,6 @@ def test_draft_then_verify_small():
     _step_parity(vi, full_oracle=True)
 
 
-@pytest.mark.skip(reason="the 32768-row draft head (d2t) at full size faulted intermittently on the GPU; "
-                         "kept off the GPU until the cause is found (the small draft-chain tests cover the path)")
 def test_draft_then_verify_full_size():
     dc = DRAFT_CONFIG
     vcfg = config4_verify(dc)
