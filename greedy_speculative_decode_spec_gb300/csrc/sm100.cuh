@@ -142,6 +142,14 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy
 // (TMA / tensor core) accesses.
+// 2^x with the SFU's approximate base-2 exponential (PTX ex2.approx.ftz: about 2 ulp,
+// subnormal results flushed to zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -49,6 +49,7 @@ constexpr uint64_t ATT_WAIT_NS = 1000000000ull;
 constexpr int ATT_SMEM_LIMIT = 227 * 1024;
 constexpr int MAX_NPAD = 64;      // query vectors per (branch, kv head), padded to 16
 constexpr int MAX_TS = 8;         // = SPLIT_KEYS / TILE_KEYS
+constexpr uint32_t P_BUF = TILE_KEYS * 128;  // one P buffer: 128 keys x 64 columns, MN-major
 
 struct AttnTcParams {
     KvView kv;
@@ -322,8 +323,8 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     } else if (warp == 1) {
         // ================= MMA issuer =================
         const uint32_t idesc_s = idesc_f16kind(128, N_pad, FP8, false, false);
-        const uint32_t idesc_pv = idesc_f16kind(128, N_pad, FP8, true, false);
-        const uint32_t qblk = (uint32_t)N_pad * 128, pblk = (uint32_t)N_pad * 128;
+        const uint32_t idesc_pv = idesc_f16kind(128, N_pad, FP8, true, true);
+        const uint32_t qblk = (uint32_t)N_pad * 128;
         uint32_t gi = 0, gt = 0, ul = 0;
         uint32_t slot_use[MAX_TS];
 #pragma unroll
@@ -395,14 +396,14 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                     if (!warp_wait(pfull + 8 * pb, (gt >> 1) & 1u, abort_flag)) { ok = false; break; }
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t vbase = s_op + st * S_::OP_STAGE, pbase = s_p + pb * 2 * pblk;
+                        const uint32_t vbase = s_op + st * S_::OP_STAGE, pbase = s_p + pb * P_BUF;
 #pragma unroll
                         for (int nb = 0; nb < S_::NB; ++nb) {
 #pragma unroll
                             for (int ks = 0; ks < TILE_KEYS / 16; ++ks) {
                                 const uint64_t ad = desc_mnmajor_sw128(vbase + (2 * nb) * (TILE_KEYS * 128) + ks * 2048,
                                                                        TILE_KEYS * 128);
-                                const uint64_t bd = desc_kmajor_sw128(pbase + (ks >> 2) * pblk + (ks & 3) * 32);
+                                const uint64_t bd = desc_mnmajor_sw128(pbase + ks * 2048, P_BUF);
                                 mma_bf16(t_o + (ob * S_::NB + nb) * N_pad, ad, bd, idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
                             }
                         }
@@ -448,10 +449,7 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         const int etid = threadIdx.x - 64;  // 0..127
         const int kk = q * 32 + lane;       // key within a tile / d row within a 128-block
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        const uint32_t qblk = (uint32_t)N_pad * 128, pblk = (uint32_t)N_pad * 128;
-        // byte offset of this thread's key column in P row 0 (the row's swizzle is added per row)
-        const uint32_t p_col = (uint32_t)(kk >> 6) * pblk + ((kk & 7) << 1);
-        const uint32_t p_chunk = (uint32_t)((kk & 63) >> 3);
+        const uint32_t qblk = (uint32_t)N_pad * 128;
         uint32_t gt = 0, gch = 0, ul = 0;
         uint32_t slot_use[MAX_TS];
 #pragma unroll
@@ -512,19 +510,22 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
 #pragma unroll
                     for (int s = 0; s < MAX_TS; ++s)
                         if (s == slot) su = slot_use[s];
+                    // this key is seen by the columns [cth, cend): rows j with key <= pos_b + j
                     const int key = ui.s0 + t * TILE_KEYS + kk;
-                    const bool kvalid = key < ui.kv_end;
+                    int cth = 0, cend = 0;
                     float ksc = 1.f;
-                    if (kvalid) {
+                    if (key < ui.kv_end) {
                         const int pg = page_of(p.kv, ui.b, key);
                         if (pg < 0) failed = true;
                         else if (FP8) ksc = __ldg(p.kv.k_scale + (size_t)pg * p.kv.n_kv_heads + ui.g);
+                        const int J = key - ui.pos_b;
+                        cth = J > 0 ? J * p.G : 0;
+                        cend = n_q;
                     }
                     if (ok) ok = warp_wait(sfull + 8 * slot, su & 1u, abort_flag);
                     if (!ok) continue;
                     tc_fence_after();
                     const float sl = p.scale_log2 * ksc;
-                    const int jmax = ui.pos_b - key;  // a row j sees this key iff j >= -jmax... key <= pos_b + j
 #pragma unroll
                     for (int c0 = 0; c0 < MAX_NPAD; c0 += 16) {
                         if (c0 < n_q) {
@@ -534,8 +535,8 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
                                 const int c = c0 + j;
-                                const bool valid = kvalid && c < n_q && (c / p.G) >= -jmax;
-                                mth[c] = valid ? fmaxf(mth[c], __uint_as_float(r[j]) * sl) : mth[c];
+                                const float v = __uint_as_float(r[j]) * sl;
+                                if (c >= cth && c < cend) mth[c] = fmaxf(mth[c], v);
                             }
                         }
                     }
@@ -589,46 +590,71 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                 for (int t = t0; t < t1; ++t, ++gt) {
                     const int slot = t - t0;
                     const int key = ui.s0 + t * TILE_KEYS + kk;
-                    const bool kvalid = key < ui.kv_end;
+                    int cth = 0, cend = 0;
                     float ksc = 1.f, vsc = 1.f;
-                    if (kvalid && FP8) {
-                        const int pg = page_of(p.kv, ui.b, key);
-                        if (pg >= 0) {
-                            const size_t si = (size_t)pg * p.kv.n_kv_heads + ui.g;
-                            ksc = __ldg(p.kv.k_scale + si);
-                            vsc = __ldg(p.kv.v_scale + si) * P_SCALE_FP8;
+                    if (key < ui.kv_end) {
+                        if (FP8) {
+                            const int pg = page_of(p.kv, ui.b, key);
+                            if (pg >= 0) {
+                                const size_t si = (size_t)pg * p.kv.n_kv_heads + ui.g;
+                                ksc = __ldg(p.kv.k_scale + si);
+                                vsc = __ldg(p.kv.v_scale + si) * P_SCALE_FP8;
+                            }
                         }
+                        const int J = key - ui.pos_b;
+                        cth = J > 0 ? J * p.G : 0;
+                        cend = n_q;
                     }
                     const uint32_t pb = gt & 1u;
                     if (ok) ok = warp_wait(pfree + 8 * pb, ((gt >> 1) & 1u) ^ 1u, abort_flag);
                     if (!ok) continue;
                     const float sl = p.scale_log2 * ksc;
-                    const int jmax = ui.pos_b - key;
-                    uint8_t *pbuf = g_p + pb * 2 * pblk + p_col;
+                    // this key's row of P (MN-major: the columns are contiguous, 128-byte swizzle)
+                    uint8_t *prow = g_p + pb * P_BUF + kk * 128;
+                    const int swz = kk & 7;
 #pragma unroll
                     for (int c0 = 0; c0 < MAX_NPAD; c0 += 16) {
                         if (c0 < N_pad) {
-                            uint32_t r[16];
+                            uint32_t pk[8];
                             if (c0 < n_q) {
+                                uint32_t r[16];
                                 tmem_ld16(tmem + lane_base + slot * N_pad + c0, r);
-                                tmem_ld_wait();
-                            }
+                                float mv[16];
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int c = c0 + j;
-                                const bool valid = kvalid && c < n_q && (c / p.G) >= -jmax;
-                                const float pv = valid ? exp2f(__uint_as_float(r[j]) * sl - mnew[c]) : 0.f;
-                                lth[c] += pv;
-                                uint16_t bits;
-                                if (FP8) {
-                                    __half h = __float2half_rn(pv * vsc);
-                                    bits = *reinterpret_cast<uint16_t *>(&h);
-                                } else {
-                                    __nv_bfloat16 h = __float2bfloat16_rn(pv);
-                                    bits = *reinterpret_cast<uint16_t *>(&h);
+                                for (int e = 0; e < 4; ++e) {
+                                    const float4 m4 = reinterpret_cast<const float4 *>(mnew + c0)[e];
+                                    mv[4 * e] = m4.x;
+                                    mv[4 * e + 1] = m4.y;
+                                    mv[4 * e + 2] = m4.z;
+                                    mv[4 * e + 3] = m4.w;
                                 }
-                                *reinterpret_cast<uint16_t *>(pbuf + c * 128 + (((p_chunk ^ (c & 7)) & 7) << 4)) = bits;
+                                tmem_ld_wait();
+#pragma unroll
+                                for (int j = 0; j < 16; j += 2) {
+                                    const int c = c0 + j;
+                                    float a = ex2_approx(fmaf(__uint_as_float(r[j]), sl, -mv[j]));
+                                    float b = ex2_approx(fmaf(__uint_as_float(r[j + 1]), sl, -mv[j + 1]));
+                                    a = (c >= cth && c < cend) ? a : 0.f;
+                                    b = (c + 1 >= cth && c + 1 < cend) ? b : 0.f;
+                                    lth[c] += a;
+                                    lth[c + 1] += b;
+                                    if (FP8) {
+                                        const __half2 h = __floats2half2_rn(a * vsc, b * vsc);
+                                        pk[j >> 1] = *reinterpret_cast<const uint32_t *>(&h);
+                                    } else {
+                                        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+                                        pk[j >> 1] = *reinterpret_cast<const uint32_t *>(&h);
+                                    }
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) pk[e] = 0u;
                             }
+                            const int ch0 = c0 >> 3;
+                            *reinterpret_cast<uint4 *>(prow + (((ch0 ^ swz) & 7) << 4)) =
+                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            *reinterpret_cast<uint4 *>(prow + ((((ch0 + 1) ^ swz) & 7) << 4)) =
+                                make_uint4(pk[4], pk[5], pk[6], pk[7]);
                         }
                     }
                     tc_fence_before();
@@ -852,7 +878,7 @@ static int launch_attn_tc(AttnTcParams &p, cudaStream_t s) {
     using S_ = AttnShape<D, FP8>;
     const int NATOM = S_::NATOM;
     p.off_q = 0;  // set below
-    const uint32_t q_bytes = NATOM * p.N_pad * 128, p_bytes = 2 * 2 * p.N_pad * 128;  // P: 2 buffers
+    const uint32_t q_bytes = NATOM * p.N_pad * 128, p_bytes = 2 * P_BUF;  // P: 2 buffers
     const uint32_t small = 64 + 12 * p.N_pad * 4 + 64;
     const uint32_t bars = 8 * 64;
     const uint32_t fixed = 1024 + q_bytes + p_bytes + small + bars;
