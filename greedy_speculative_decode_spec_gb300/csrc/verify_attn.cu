@@ -8,25 +8,36 @@
 // rows in one launch); memra-engine `MtpScratch` (split count fixed by capacity, not by
 // the current length, so one program serves every length bit for bit).
 //
-// Work unit = (branch b, kv head g, split of SPLIT_KEYS positions). The (k+1)*G query
-// vectors that share kv head g form the N side of the MMAs, the keys the M side:
-//     S^T[128 keys x N] = K_tile[128 x d] . Q^T            (tcgen05, fp32 in TMEM)
-//     O^T[d x N]       += V_tile^T[d x 128] . P^T[128 x N]  (V read MN-major)
-// A persistent CTA per SM walks its units. Warp 0 gathers each 128-key K / V tile from
-// the branch's pages with TMA (one box per page and 64-element column block, 128-byte
-// swizzle) into a shared-memory ring; for FP8 pools it gathers the raw E4M3 bytes and
-// warps 6..9 convert them to f16 operand tiles (E4M3 is exact in f16). Warp 1 issues the
-// MMAs. Warps 2..5 do the softmax in two passes over the split, whose S tiles all stay in
-// TMEM: pass A takes each column's maximum over the split's keys (one cross-lane
-// reduction per column per split), pass B writes P = exp2(s - m) to shared memory for
-// P.V and sums it per thread (one cross-lane sum per column per split). O accumulates in
-// TMEM without rescaling; only when a split's S tiles do not fit in TMEM at once is it
-// processed in chunks, with O rescaled between chunks. Keys beyond a row's position are
-// set to -inf by select, never multiplied; V rows past the branch's last position are
-// zeroed. A combine pass merges the splits of each (row, head) in ascending order.
-// Tile and split boundaries sit at fixed key positions, every column of an MMA is
-// computed independently of the others, and masked keys contribute exact zeros, so a
-// row's output is identical whatever B, k or batch it is verified in.
+// Work unit = (branch b, kv head g, split of split_keys positions). The n_q = (k+1)*G
+// query vectors that share kv head g sit on the 128 TMEM lanes (the M side of the MMAs,
+// query i on lane i); the keys of a 128-key tile are the columns:
+//     S[q][key]  = Q . K_tile^T                 (tcgen05, fp32 in TMEM, double-buffered)
+//     O[q][d]   += P[q][key] . V_tile[key][d]   (tcgen05, fp32 in TMEM)
+// so every softmax quantity of a query (its running maximum and sum) lives in the lane's
+// threads: no cross-lane reductions. One pass per tile with a lazily raised maximum: a row's
+// running maximum m only moves when a tile's maximum exceeds it by more than RESCALE_TAU
+// (log2 units), so P = 2^(s - m) <= 2^RESCALE_TAU and O is rescaled (in TMEM, by the row's
+// own thread) only on such a move; the final O / l does not depend on which m was used.
+//
+// A persistent CTA per SM walks its units with warp-specialised roles:
+//   warp 0     per unit: the page-table entries (and FP8 scales) into a shared table, and
+//              Q by one 3-D TMA box per 64-column block (double-buffered);
+//   warp 1     issues the MMAs: S of tile t+1 before P.V of tile t when the operand ring
+//              can hold both, so the softmax of one tile overlaps the MMAs of the next;
+//   warps 4, 5, 8, 9  softmax: the threads of TMEM lane q own query q (lane quadrants 0 and 1
+//              hold the n_q <= 64 queries), two warps per quadrant, one per half of the key
+//              columns; a quadrant without queries has nothing to do;
+//   warps 2, 3, 6, 7  gather K and V rows with 16-byte cp.async copies into the swizzled operand
+//              ring (bf16), or into a raw ring from which the same threads convert E4M3 to
+//              f16 exactly (FP8; Q is converted bf16 -> f16 in place). The page scales are
+//              applied by the softmax: K's to the scores, V's to P (the row sum stays
+//              unscaled), so S and O come out in the pool's true units.
+// Keys beyond a row's position get P = 0 by select, never by multiplication, and V rows
+// past the branch's last position are zeroed before P.V, so NaN in unused pool slots
+// cannot reach a result. Tile and split boundaries sit at fixed key positions and every
+// MMA row is computed independently of the others, so a row's output is identical
+// whatever B, k or batch it is verified in. A combine pass merges the splits of each
+// (row, head) in ascending order.
 // Every pipeline wait is bounded (1 s): on a timeout the kernel raises
 // SPEC_DEVERR_TIMEOUT, lets issued copies and MMAs land, frees TMEM and exits.
 #include <cuda.h>
@@ -41,59 +52,88 @@ namespace spec {
 
 using namespace sm100;
 
-constexpr int SPLIT_KEYS = 1024;
+constexpr int SPLIT_KEYS = 1024;  // largest split; the split size is split_keys_for(Hkv)
 constexpr int TILE_KEYS = 128;
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr float P_SCALE_FP8 = 1024.0f;   // f16 P is stored x 2^10 to stay clear of f16 subnormals
+constexpr float RESCALE_TAU = 8.0f;   // P <= 2^8: exact range for bf16 and f16 alike
 constexpr uint64_t ATT_WAIT_NS = 1000000000ull;
 constexpr int ATT_SMEM_LIMIT = 227 * 1024;
-constexpr int MAX_NPAD = 64;      // query vectors per (branch, kv head), padded to 16
-constexpr int MAX_TS = 8;         // = SPLIT_KEYS / TILE_KEYS
-constexpr uint32_t P_BUF = TILE_KEYS * 128;  // one P buffer: 128 keys x 64 columns, MN-major
+constexpr int MAX_NPAD = 64;          // query vectors per (branch, kv head), padded to 16
+constexpr int MAX_RPAD = 64;          // TMEM lanes holding them (two blocks of <= 32 when split)
+
+// Per-unit table the producer warp fills: the page of each page-sized run of the split's
+// keys (-1 if the table entry is invalid), the page's FP8 K / V scales, and the error
+// bits of any invalid entry. Used for pages of >= 8 positions.
+constexpr int UT_ENTRIES = SPLIT_KEYS / 8;
+struct UnitTable {
+    int32_t page[UT_ENTRIES];
+    float ksc[UT_ENTRIES];
+    float vsc[UT_ENTRIES];
+    int32_t bad;
+    int32_t pad_[31];
+};
+
+// Split size in positions, a function of the model's KV-head count only (never of B, k or
+// the context length, so a row's split boundaries are the same in every batch): few KV
+// heads give few work units per branch, so their splits are shorter.
+__host__ __device__ constexpr int split_keys_for(int n_kv_heads) {
+    return n_kv_heads <= 2 ? 256 : (n_kv_heads <= 4 ? 512 : SPLIT_KEYS);
+}
 
 struct AttnTcParams {
     KvView kv;
     const int32_t *pos;
-    int B, k, Hq, G, n_q, N_pad, n_splits, max_pos, n_units;
+    int B, k, Hq, G, n_q, n_splits, max_pos, n_units, split_keys;
+    // query layout on the TMEM lanes: draft rows j < J1 on lanes [0, J1*G), the rest (if
+    // split) on lanes [32, 32 + (k+1-J1)*G); R_pad = lanes in use, padded to 16
+    int J1, split, R_pad;
     const uint16_t *q;     // bf16 [R][Hq][d]
     float scale_log2;      // softmax scale * log2(e)
     float *ws_ml;          // [units][n_q][2]  (m in log2 units, l)
     float *ws_o;           // [units][n_q][d]
     int32_t *err;
-    int NS, NR;            // operand / raw ring depth
-    int TS, OB;            // S tiles held in TMEM at once (a chunk), O buffers (1 or 2)
-    uint32_t tmem_cols;
-    uint32_t off_q, off_p, off_raw, off_bar, off_small;  // shared-memory offsets
+    int NS, NR;            // operand / raw ring depth (sub-tiles)
+    int OB;                // O buffers in TMEM (1 or 2)
+    int lookahead;         // issue S of tile t+1 before P.V of tile t
+    uint32_t off_q, off_p, off_op, off_raw, off_ut, off_bar, off_small;  // shared-memory offsets
 };
 
+// A ring stage holds one sub-tile: 128 keys x SUB_COLS columns of d (d = 256 tiles are
+// two sub-tiles, the halves of d: S accumulates over both, and each half of O reads its
+// own half of V).
 template <int D, bool FP8>
 struct AttnShape {
-    static constexpr int NATOM = D / 64;                    // 128-byte column blocks of a 16-bit row
-    static constexpr int OP_ATOMS = NATOM < 2 ? 2 : NATOM;  // V^T needs 2 blocks for M = 128
-    static constexpr uint32_t OP_STAGE = OP_ATOMS * TILE_KEYS * 128;
-    static constexpr uint32_t RAW_STAGE = FP8 ? TILE_KEYS * D : 0;
-    static constexpr int NB = D <= 128 ? 1 : 2;            // 128-row blocks of d for P.V
-    static constexpr int THREADS = FP8 ? 320 : 192;
+    static constexpr int NATOM = D / 64;                   // 128-byte column blocks of a 16-bit row
+    static constexpr int SUB_COLS = D < 128 ? D : 128;
+    static constexpr int NSUB = D / SUB_COLS;              // sub-tiles per tile
+    static constexpr int NATOM_SUB = SUB_COLS / 64;        // column blocks per sub-tile
+    static constexpr uint32_t OP_STAGE = NATOM_SUB * TILE_KEYS * 128;
+    static constexpr uint32_t RAW_STAGE = FP8 ? TILE_KEYS * SUB_COLS : 0;
+    static constexpr int THREADS = 320;
 };
 
 struct UnitInfo {
-    int b, g, split, pos_b, kv_end, s0, T, n_chunks;
+    int b, g, split, pos_b, kv_end, s0, T;
     bool bad_pos;
 };
 
-__device__ __forceinline__ UnitInfo unit_info(const AttnTcParams &p, int u) {
+// The CTAs walk the units split-major (every (branch, head) pair's first split, then every
+// pair's second split, ...), so that a grid stride never lines up with the split count;
+// `u` (the workspace slot) stays (branch, head, split)-major for the combine pass.
+__device__ __forceinline__ UnitInfo unit_info(const AttnTcParams &p, int iter, int &u) {
     UnitInfo ui;
-    ui.split = u % p.n_splits;
-    ui.g = (u / p.n_splits) % p.kv.n_kv_heads;
-    ui.b = u / (p.n_splits * p.kv.n_kv_heads);
+    const int pairs = p.B * p.kv.n_kv_heads;
+    ui.split = iter / pairs;
+    ui.g = (iter % pairs) % p.kv.n_kv_heads;
+    ui.b = (iter % pairs) / p.kv.n_kv_heads;
+    u = (ui.b * p.kv.n_kv_heads + ui.g) * p.n_splits + ui.split;
     ui.pos_b = __ldg(p.pos + ui.b);
     ui.bad_pos = ui.pos_b < 0 || ui.pos_b + p.k + 1 > p.max_pos;
     ui.kv_end = ui.pos_b + p.k + 1;
-    ui.s0 = ui.split * SPLIT_KEYS;
+    ui.s0 = ui.split * p.split_keys;
     int n = ui.bad_pos ? 0 : ui.kv_end - ui.s0;
-    n = n < 0 ? 0 : (n > SPLIT_KEYS ? SPLIT_KEYS : n);
+    n = n < 0 ? 0 : (n > p.split_keys ? p.split_keys : n);
     ui.T = (n + TILE_KEYS - 1) / TILE_KEYS;
-    ui.n_chunks = (ui.T + p.TS - 1) / p.TS;
     return ui;
 }
 
@@ -101,16 +141,7 @@ __device__ __forceinline__ UnitInfo unit_info(const AttnTcParams &p, int u) {
 // 64-column blocks are `block_bytes` apart
 __device__ __forceinline__ uint32_t sw128_off(int row, int col, uint32_t block_bytes) {
     const int blk = col >> 6, c = col & 63;
-    return blk * block_bytes + row * 128 + ((((c >> 3) ^ (row & 7)) & 7) << 4) + ((c & 7) << 1);
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-    // orderable-key maximum over the warp
-    uint32_t u = __float_as_uint(v);
-    uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-    k = __reduce_max_sync(0xFFFFFFFFu, k);
-    u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
-    return __uint_as_float(u);
+    return blk * block_bytes + row * 128 + ((((c >> 3) ^ (row & 7)) & 7) << 4);
 }
 
 // Every lane waits; the verdict is made uniform across the warp so that no lane can
@@ -120,304 +151,271 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xFFFFFFFFu, r);
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-    return v;
+__device__ __forceinline__ uint32_t pack2(float a, float b, bool f16) {
+    if (f16) {
+        const __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
 
 template <int D, bool FP8>
 __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+    attn_tc_kernel(const __grid_constant__ CUtensorMap map_q0, const __grid_constant__ CUtensorMap map_q1,
                    AttnTcParams p) {
     using S_ = AttnShape<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t s_op = smem_u32(smem);
-    const uint32_t s_q = s_op + p.off_q, s_p = s_op + p.off_p, s_rawb = s_op + p.off_raw;
-    uint8_t *g_q = smem + p.off_q;
+    const uint32_t s_base = smem_u32(smem);
+    const int R_pad = p.R_pad, n_q = p.n_q;
+    // Q and P buffers keep only R_pad rows per 64-column block; the M = 128 MMAs also read
+    // rows R_pad..127, which fall on the following memory: those rows only feed TMEM lanes
+    // no thread reads.
+    const uint32_t QATOM = (uint32_t)R_pad * 128, QBUF = S_::NATOM * QATOM;
+    const uint32_t PATOM = (uint32_t)R_pad * 128, PBUF = 2 * PATOM;
+    const uint32_t s_q = s_base + p.off_q, s_p = s_base + p.off_p, s_op = s_base + p.off_op;
+    const uint32_t s_raw = s_base + p.off_raw;
     uint8_t *g_p = smem + p.off_p;
-    const int N_pad = p.N_pad, n_q = p.n_q, TS = p.TS;
+    UnitTable *tables = reinterpret_cast<UnitTable *>(smem + p.off_ut);  // [2]
     // barrier map
-    const uint32_t op_full = s_op + p.off_bar, op_empty = op_full + 8 * p.NS;
-    const uint32_t raw_full = op_empty + 8 * p.NS, raw_empty = raw_full + 8 * p.NR;
-    const uint32_t sfull = raw_empty + 8 * p.NR, sfree = sfull + 8 * TS;   // per S slot
-    const uint32_t pfull = sfree + 8 * TS, pfree = pfull + 16;             // P double buffer
-    const uint32_t ochunk = pfree + 16, ofree = ochunk + 8, qready = ofree + 16, drain = qready + 8;
+    const uint32_t op_full = s_base + p.off_bar, op_empty = op_full + 8 * p.NS;
+    const uint32_t raw_full = op_empty + 8 * p.NS;                    // FP8 raw ring
+    const uint32_t sfull = raw_full + 8 * p.NR, sfree = sfull + 16;  // S double buffer
+    const uint32_t pfull = sfree + 16, pfree = pfull + 16;            // P double buffer
+    const uint32_t odone = pfree + 16, ofree = odone + 8;             // P.V completions, O buffers
+    const uint32_t qfull = ofree + 16, qconv = qfull + 16, qfree = qconv + 16;  // Q double buffer
+    const uint32_t ufull = qfree + 16, ufree = ufull + 16;                      // unit tables
+    const uint32_t drain = ufree + 16;
     uint8_t *small = smem + p.off_small;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(small + 4);
-    volatile int *fail_flag = reinterpret_cast<volatile int *>(small + 8);
-    volatile int *corr_flag = reinterpret_cast<volatile int *>(small + 12);
-    float *red_max = reinterpret_cast<float *>(small + 64);  // [4][N_pad]
-    float *red_sum = red_max + 4 * N_pad;                    // [4][N_pad]
-    float *cor = red_sum + 4 * N_pad;                        // [N_pad]
-    float *mnew = cor + N_pad;
-    float *mrun = mnew + N_pad;
-    float *lrun = mrun + N_pad;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_act = 2 * (p.split ? 2 : (n_q + 31) >> 5);  // softmax warps that own queries
+    const bool small_pages = p.kv.page_size < 8;  // more than UT_ENTRIES pages per split
+    const int log2P = p.kv.log2_page;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.NS; ++s) {
-            mbar_init(op_full + 8 * s, FP8 ? 4 : 1);
+            // bf16: each loader thread's copies arrive; FP8: each loader warp after converting
+            mbar_init(op_full + 8 * s, FP8 ? 4 : 128);
             mbar_init(op_empty + 8 * s, 1);
         }
-        for (int s = 0; s < p.NR; ++s) {
-            mbar_init(raw_full + 8 * s, 1);
-            mbar_init(raw_empty + 8 * s, 4);
-        }
-        for (int s = 0; s < TS; ++s) {
-            mbar_init(sfull + 8 * s, 1);
-            mbar_init(sfree + 8 * s, 4);
-        }
+        for (int s = 0; s < p.NR; ++s) mbar_init(raw_full + 8 * s, 128);
         for (int a = 0; a < 2; ++a) {
-            mbar_init(pfull + 8 * a, 4);
+            mbar_init(sfull + 8 * a, 1);
+            mbar_init(sfree + 8 * a, n_act);
+            mbar_init(pfull + 8 * a, n_act);
             mbar_init(pfree + 8 * a, 1);
-            mbar_init(ofree + 8 * a, 4);
+            mbar_init(ofree + 8 * a, n_act);
+            mbar_init(qfull + 8 * a, 1);
+            mbar_init(qconv + 8 * a, 4);
+            mbar_init(qfree + 8 * a, 1);
+            mbar_init(ufull + 8 * a, 1);
+            mbar_init(ufree + 8 * a, n_act + 4);  // softmax and loader warps
         }
-        mbar_init(ochunk, 1);
-        mbar_init(qready, 4);
+        mbar_init(odone, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
-        *fail_flag = 0;
-        *corr_flag = 0;
         fence_mbar_init();
     }
-    if (D == 64) {
-        // the second 64-row block of every V^T operand must read zeros
-        for (uint32_t i = threadIdx.x; i < (uint32_t)p.NS * S_::OP_STAGE / 16; i += blockDim.x)
-            reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
-    }
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(&map_k);
-        prefetch_tmap(&map_v);
+        prefetch_tmap(&map_q0);
+        if (p.split) prefetch_tmap(&map_q1);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+        tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t t_o = tmem + (uint32_t)(TS * N_pad);  // S slots first, then O buffers
-
-    const int BR = p.kv.page_size < TILE_KEYS ? p.kv.page_size : TILE_KEYS;  // rows per gather box
-    const int n_chunks_tile = TILE_KEYS / BR;
+    const uint32_t t_s = tmem;        // S buffers: columns [0, 128) and [128, 256)
+    const uint32_t t_o = tmem + 256;  // O buffers: D columns each
 
     if (warp == 0) {
-        // ================= producer: page-gathered loads, per chunk K tiles then V tiles =================
-        uint32_t gi = 0;
+        // ================= producer: per unit, the page table entries and Q =================
+        uint32_t ua = 0;
         bool ok = true;
-        const uint32_t per_box = FP8 ? (uint32_t)(BR * D) : (uint32_t)(BR * 128 * S_::NATOM);
-        for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-            const UnitInfo ui = unit_info(p, u);
-            for (int ch = 0; ch < ui.n_chunks && ok; ++ch) {
-                const int t0 = ch * TS, t1 = min(ui.T, t0 + TS);
-                for (int kv = 0; kv < 2 && ok; ++kv) {
-                    const CUtensorMap *map = kv ? &map_v : &map_k;
-                    for (int t = t0; t < t1; ++t, ++gi) {
-                        const int key0 = ui.s0 + t * TILE_KEYS;
-                        int rows[4];  // box row of chunk lane, lane+32, ... (<= 128 chunks)
-                        uint32_t nvalid = 0;
-#pragma unroll
-                        for (int rr = 0; rr < 4; ++rr) {
-                            const int c = rr * 32 + lane;
-                            const int kc = key0 + c * BR;
-                            int row0 = -1;
-                            if (c < n_chunks_tile && kc < ui.kv_end) {
-                                const int pg = page_of(p.kv, ui.b, kc);
-                                if (pg >= 0)
-                                    row0 = (pg * p.kv.n_kv_heads + ui.g) * p.kv.page_size +
-                                           (kc & (p.kv.page_size - 1));
-                                else if (kv == 0)
-                                    raise_error(p.err, -pg);
-                            }
-                            rows[rr] = row0;
-                            nvalid += __popc(__ballot_sync(0xFFFFFFFFu, row0 >= 0));
-                        }
-                        uint32_t dst_base, bar;
-                        if (FP8) {
-                            const uint32_t s = gi % p.NR, ph = (gi / p.NR) & 1u;
-                            if (!warp_wait(raw_empty + 8 * s, ph ^ 1u, abort_flag)) { ok = false; break; }
-                            dst_base = s_rawb + s * S_::RAW_STAGE;
-                            bar = raw_full + 8 * s;
-                        } else {
-                            const uint32_t s = gi % p.NS, ph = (gi / p.NS) & 1u;
-                            if (!warp_wait(op_empty + 8 * s, ph ^ 1u, abort_flag)) { ok = false; break; }
-                            dst_base = s_op + s * S_::OP_STAGE;
-                            bar = op_full + 8 * s;
-                        }
-                        if (BR < 8) {
-                            // pages smaller than one 8-row swizzle atom: gather with plain copies
-                            // (a TMA box would not start on a 1024-byte boundary)
-                            const uint8_t *pool = reinterpret_cast<const uint8_t *>(kv ? p.kv.v_pool : p.kv.k_pool);
-                            uint8_t *dst = smem + (dst_base - s_op);
-                            constexpr int CH = FP8 ? D / 16 : D / 8;  // 16-byte pieces per row
-                            for (int i = lane; i < TILE_KEYS * CH; i += 32) {
-                                const int row = i / CH, chn = i % CH;
-                                const int key = key0 + row;
-                                if (key >= ui.kv_end) continue;
-                                const int pg = page_of(p.kv, ui.b, key);
-                                if (pg < 0) continue;
-                                const size_t elem = ((size_t)(pg * p.kv.n_kv_heads + ui.g) * p.kv.page_size +
-                                                     (key & (p.kv.page_size - 1))) * D;
-                                if (FP8) {
-                                    *reinterpret_cast<uint4 *>(dst + row * D + chn * 16) =
-                                        __ldg(reinterpret_cast<const uint4 *>(pool + elem + chn * 16));
-                                } else {
-                                    *reinterpret_cast<uint4 *>(dst + sw128_off(row, chn * 8, TILE_KEYS * 128)) =
-                                        __ldg(reinterpret_cast<const uint4 *>(pool + 2 * elem + chn * 16));
-                                }
-                            }
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(bar);
-                            __syncwarp();
-                            continue;
-                        }
-                        if (lane == 0) {
-                            if (nvalid) mbar_arrive_expect_tx(bar, nvalid * per_box);
-                            else mbar_arrive(bar);
-                        }
-#pragma unroll
-                        for (int rr = 0; rr < 4; ++rr) {
-                            if (rr * 32 >= n_chunks_tile) break;
-                            for (int cc = 0; cc < 32; ++cc) {
-                                const int c = rr * 32 + cc;
-                                if (c >= n_chunks_tile) break;
-                                const int row0 = __shfl_sync(0xFFFFFFFFu, rows[rr], cc);
-                                if (lane == 0 && row0 >= 0) {
-                                    if (FP8) {
-                                        tma_load_2d(dst_base + c * BR * D, map, 0, row0, bar);
-                                    } else {
-#pragma unroll
-                                        for (int a = 0; a < S_::NATOM; ++a)
-                                            tma_load_2d(dst_base + a * (TILE_KEYS * 128) + c * BR * 128, map, a * 64,
-                                                        row0, bar);
-                                    }
-                                }
-                            }
-                        }
-                        __syncwarp();
+        for (int it_u = blockIdx.x; it_u < p.n_units && ok; it_u += gridDim.x) {
+            int u;
+            const UnitInfo ui = unit_info(p, it_u, u);
+            if (ui.T == 0) continue;
+            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+            UnitTable *tab = tables + ub;
+            if (!warp_wait(ufree + 8 * ub, uph ^ 1u, abort_flag)) { ok = false; break; }
+            int badbits = 0;
+            if (!small_pages) {
+                const int nkeys = min(ui.kv_end - ui.s0, p.split_keys);
+                const int nent = (nkeys + p.kv.page_size - 1) >> log2P;
+                for (int e = lane; e < nent; e += 32) {
+                    const int pg = page_of(p.kv, ui.b, ui.s0 + (e << log2P));
+                    float ks = 1.f, vs = 1.f;
+                    if (pg < 0) {
+                        badbits |= -pg;
+                    } else if (FP8) {
+                        const size_t si = (size_t)pg * p.kv.n_kv_heads + ui.g;
+                        ks = __ldg(p.kv.k_scale + si);
+                        vs = __ldg(p.kv.v_scale + si);
                     }
+                    tab->page[e] = pg < 0 ? -1 : pg;
+                    tab->ksc[e] = ks;
+                    tab->vsc[e] = vs;
+                }
+            } else {
+                // pages smaller than 8 positions: the loaders look each row up themselves;
+                // only the error bits are gathered here
+                const int nkeys = min(ui.kv_end - ui.s0, p.split_keys);
+                for (int e = lane; e < nkeys; e += 32) {
+                    const int pg = page_of(p.kv, ui.b, ui.s0 + e);
+                    if (pg < 0) badbits |= -pg;
                 }
             }
+            badbits = __reduce_or_sync(0xFFFFFFFFu, badbits);
+            if (lane == 0) {
+                tab->bad = badbits;
+                if (badbits) raise_error(p.err, badbits);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ufull + 8 * ub);
+            // ---- Q of (b, g): one 3-D box per 64-column block lands as rows j*G + i ----
+            if (!warp_wait(qfree + 8 * ub, uph ^ 1u, abort_flag)) { ok = false; break; }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(qfull + 8 * ub, (uint32_t)(S_::NATOM * n_q * 128));
+#pragma unroll
+                for (int a = 0; a < S_::NATOM; ++a) {
+                    tma_load_3d(s_q + ub * QBUF + a * QATOM, &map_q0, a * 64, ui.g * p.G, ui.b * (p.k + 1),
+                                qfull + 8 * ub);
+                    if (p.split)
+                        tma_load_3d(s_q + ub * QBUF + a * QATOM + 32 * 128, &map_q1, a * 64, ui.g * p.G,
+                                    ui.b * (p.k + 1) + p.J1, qfull + 8 * ub);
+                }
+            }
+            __syncwarp();
+            ++ua;
         }
         if (!ok) {
             *abort_flag = 1;
             if (lane == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
-        // let copies still in flight land before the CTA may exit
+        // the Q copies still in flight land before the CTA may exit
         if (lane == 0) {
-            const uint32_t depth = FP8 ? p.NR : p.NS;
-            const uint32_t n_last = gi < depth ? gi : depth;
-            for (uint32_t j = 0; j < n_last; ++j) {
-                const uint32_t i2 = gi - 1 - j;
-                mbar_wait((FP8 ? raw_full : op_full) + 8 * (i2 % depth), (i2 / depth) & 1u, nullptr, ATT_WAIT_NS);
+            for (uint32_t j = 0; j < 2 && j < ua; ++j) {
+                const uint32_t i2 = ua - 1 - j;
+                mbar_wait(qfull + 8 * (i2 & 1u), (i2 >> 1) & 1u, nullptr, ATT_WAIT_NS);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ================= MMA issuer =================
-        const uint32_t idesc_s = idesc_f16kind(128, N_pad, FP8, false, false);
-        const uint32_t idesc_pv = idesc_f16kind(128, N_pad, FP8, true, true);
-        const uint32_t qblk = (uint32_t)N_pad * 128;
-        uint32_t gi = 0, gt = 0, ul = 0;
-        uint32_t slot_use[MAX_TS];
-#pragma unroll
-        for (int s = 0; s < MAX_TS; ++s) slot_use[s] = 0;
+        const uint32_t idesc_s = idesc_f16kind(128, TILE_KEYS, FP8, false, false);
+        const uint32_t idesc_pv = idesc_f16kind(128, S_::SUB_COLS, FP8, false, true);
+        uint32_t gs = 0, gp = 0, ua = 0, gbase = 0;  // S, P.V, active units, first sub-tile of the unit
         bool ok = true;
-        for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-            const UnitInfo ui = unit_info(p, u);
+        // S(t) = Q . K_t^T into S buffer gs & 1
+        auto issue_s = [&](int t, uint32_t q_addr) -> bool {
+            const uint32_t sb = gs & 1u;
+            if (!warp_wait(sfree + 8 * sb, ((gs >> 1) & 1u) ^ 1u, abort_flag)) return false;
+#pragma unroll
+            for (int h = 0; h < S_::NSUB; ++h) {
+                const uint32_t g = gbase + (uint32_t)(t * 2 * S_::NSUB + h), st = g % p.NS;
+                if (!warp_wait(op_full + 8 * st, (g / p.NS) & 1u, abort_flag)) return false;
+                fence_proxy_async_smem();  // cp.async data -> tensor core reads
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t kb = s_op + st * S_::OP_STAGE;
+#pragma unroll
+                    for (int kl = 0; kl < S_::SUB_COLS / 16; ++kl) {
+                        const int ks = h * (S_::SUB_COLS / 16) + kl;  // k step over all of d
+                        mma_bf16(t_s + sb * TILE_KEYS, desc_kmajor_sw128(q_addr + (ks >> 2) * QATOM + (ks & 3) * 32),
+                                 desc_kmajor_sw128(kb + (kl >> 2) * (TILE_KEYS * 128) + (kl & 3) * 32), idesc_s,
+                                 ks > 0 ? 1u : 0u);
+                    }
+                    mma_commit(op_empty + 8 * st);
+                }
+                __syncwarp();
+            }
+            if (lane == 0) mma_commit(sfull + 8 * sb);
+            __syncwarp();
+            ++gs;
+            return true;
+        };
+        // O += P(t) . V_t
+        auto issue_pv = [&](const UnitInfo &ui, int t, uint32_t ob) -> bool {
+            const uint32_t pb = gp & 1u;
+            if (!warp_wait(pfull + 8 * pb, (gp >> 1) & 1u, abort_flag)) return false;
+            const int nvk = ui.kv_end - (ui.s0 + t * TILE_KEYS);  // valid keys in this tile
+#pragma unroll
+            for (int nb = 0; nb < S_::NSUB; ++nb) {
+                const uint32_t g = gbase + (uint32_t)(t * 2 * S_::NSUB + S_::NSUB + nb), st = g % p.NS;
+                if (!warp_wait(op_full + 8 * st, (g / p.NS) & 1u, abort_flag)) return false;
+                fence_proxy_async_smem();  // cp.async data -> tensor core reads
+                if (nvk < TILE_KEYS) {
+                    // keys past the branch's last position: zero their V rows (NaN-safe P.V)
+                    uint4 *vb = reinterpret_cast<uint4 *>(smem + p.off_op + st * S_::OP_STAGE);
+                    const int rows = TILE_KEYS - nvk;
+                    for (int i = lane; i < rows * S_::NATOM_SUB * 8; i += 32) {
+                        const int a = i / (rows * 8), rem = i % (rows * 8);
+                        const int r = nvk + rem / 8, c = rem % 8;
+                        vb[(a * TILE_KEYS * 128 + r * 128) / 16 + c] = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t vb = s_op + st * S_::OP_STAGE, pa = s_p + pb * PBUF;
+#pragma unroll
+                    for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
+                        mma_bf16(t_o + ob * D + nb * 128, desc_kmajor_sw128(pa + (ks >> 2) * PATOM + (ks & 3) * 32),
+                                 desc_mnmajor_sw128(vb + ks * 2048, TILE_KEYS * 128), idesc_pv,
+                                 (t > 0 || ks > 0) ? 1u : 0u);
+                    mma_commit(op_empty + 8 * st);
+                }
+                __syncwarp();
+            }
+            if (lane == 0) {
+                mma_commit(pfree + 8 * pb);
+                mma_commit(odone);
+            }
+            __syncwarp();
+            ++gp;
+            return true;
+        };
+        for (int it_u = blockIdx.x; it_u < p.n_units && ok; it_u += gridDim.x) {
+            int u;
+            const UnitInfo ui = unit_info(p, it_u, u);
             if (ui.T == 0) continue;
-            const uint32_t ob = p.OB == 2 ? (ul & 1u) : 0u;
-            const uint32_t ob_use = p.OB == 2 ? (ul >> 1) : ul;
-            if (!warp_wait(qready, ul & 1u, abort_flag) ||
+            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+            const uint32_t ob = p.OB == 2 ? (ua & 1u) : 0u;
+            const uint32_t ob_use = p.OB == 2 ? (ua >> 1) : ua;
+            if (!warp_wait((FP8 ? qconv : qfull) + 8 * ub, uph, abort_flag) ||
                 !warp_wait(ofree + 8 * ob, (ob_use & 1u) ^ 1u, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            for (int ch = 0; ch < ui.n_chunks && ok; ++ch) {
-                const int t0 = ch * TS, t1 = min(ui.T, t0 + TS);
-                // S of every tile of the chunk
-                for (int t = t0; t < t1; ++t, ++gi) {
-                    const int slot = t - t0;
-                    uint32_t su = 0;
-#pragma unroll
-                    for (int s = 0; s < MAX_TS; ++s)
-                        if (s == slot) su = slot_use[s];
-                    const uint32_t st = gi % p.NS;
-                    if (!warp_wait(op_full + 8 * st, (gi / p.NS) & 1u, abort_flag) ||
-                        !warp_wait(sfree + 8 * slot, (su & 1u) ^ 1u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t a_base = s_op + st * S_::OP_STAGE;
-#pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint32_t blk = ks >> 2, off = (ks & 3) * 32;
-                            mma_bf16(tmem + slot * N_pad, desc_kmajor_sw128(a_base + blk * (TILE_KEYS * 128) + off),
-                                     desc_kmajor_sw128(s_q + blk * qblk + off), idesc_s, ks > 0 ? 1u : 0u);
-                        }
-                        mma_commit(op_empty + 8 * st);
-                        mma_commit(sfull + 8 * slot);
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int s = 0; s < MAX_TS; ++s)
-                        if (s == slot) slot_use[s] = su + 1;
-                }
+            const uint32_t q_addr = s_q + ub * QBUF;
+            for (int t = 0; t < ui.T && ok; ++t) {
+                ok = issue_s(t, q_addr);
                 if (!ok) break;
-                // P.V of every tile of the chunk, in order
-                for (int t = t0; t < t1; ++t, ++gi, ++gt) {
-                    const uint32_t st = gi % p.NS;
-                    if (!warp_wait(op_full + 8 * st, (gi / p.NS) & 1u, abort_flag)) { ok = false; break; }
-                    const int key0 = ui.s0 + t * TILE_KEYS;
-                    const int nvk = ui.kv_end - key0;  // valid keys in this tile
-                    if (nvk < TILE_KEYS) {
-                        // keys past the branch's last position: zero their V rows (NaN-safe P.V)
-                        uint4 *vb = reinterpret_cast<uint4 *>(smem + st * S_::OP_STAGE);
-                        const int rows = TILE_KEYS - nvk;
-                        for (int i = lane; i < rows * S_::NATOM * 8; i += 32) {
-                            const int a = i / (rows * 8), rem = i % (rows * 8);
-                            const int r = nvk + rem / 8, c = rem % 8;
-                            vb[(a * TILE_KEYS * 128 + r * 128) / 16 + c] = make_uint4(0, 0, 0, 0);
-                        }
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                    }
-                    const uint32_t pb = gt & 1u;
-                    if (!warp_wait(pfull + 8 * pb, (gt >> 1) & 1u, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t vbase = s_op + st * S_::OP_STAGE, pbase = s_p + pb * P_BUF;
-#pragma unroll
-                        for (int nb = 0; nb < S_::NB; ++nb) {
-#pragma unroll
-                            for (int ks = 0; ks < TILE_KEYS / 16; ++ks) {
-                                const uint64_t ad = desc_mnmajor_sw128(vbase + (2 * nb) * (TILE_KEYS * 128) + ks * 2048,
-                                                                       TILE_KEYS * 128);
-                                const uint64_t bd = desc_mnmajor_sw128(pbase + ks * 2048, P_BUF);
-                                mma_bf16(t_o + (ob * S_::NB + nb) * N_pad, ad, bd, idesc_pv, (t > 0 || ks > 0) ? 1u : 0u);
-                            }
-                        }
-                        mma_commit(op_empty + 8 * st);
-                        mma_commit(pfree + 8 * pb);
-                    }
+                if (t == ui.T - 1) {
+                    // the unit's last S: its Q buffer is free once these MMAs complete
+                    if (lane == 0) mma_commit(qfree + 8 * ub);
                     __syncwarp();
                 }
-                if (!ok) break;
-                if (lane == 0) mma_commit(ochunk);
-                __syncwarp();
+                if (p.lookahead) {
+                    if (t > 0) ok = issue_pv(ui, t - 1, ob);
+                } else {
+                    ok = issue_pv(ui, t, ob);
+                }
             }
+            if (ok && p.lookahead) ok = issue_pv(ui, ui.T - 1, ob);
             if (!ok) break;
-            ++ul;
+            gbase += (uint32_t)(2 * S_::NSUB * ui.T);
+            ++ua;
         }
         if (!ok) {
             *abort_flag = 1;
@@ -427,350 +425,450 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             mma_commit(drain);
             mbar_wait(drain, 0, nullptr, ATT_WAIT_NS);
             // every arrive sent by this thread's commits is delivered before the CTA may exit:
-            // the last phase of each operand stage's "empty" barrier and of both P buffers'
-            // "free" barriers (the others were waited on by their consumers)
-            const uint32_t n_last = gi < (uint32_t)p.NS ? gi : (uint32_t)p.NS;
+            // the last phase of each operand stage's "empty" barrier, of both P and Q buffers'
+            // "free" barriers and of the P.V completion barrier
+            const uint32_t n_last = gbase < (uint32_t)p.NS ? gbase : (uint32_t)p.NS;
             for (uint32_t j = 0; j < n_last; ++j) {
-                const uint32_t i2 = gi - 1 - j;
+                const uint32_t i2 = gbase - 1 - j;
                 mbar_wait(op_empty + 8 * (i2 % p.NS), (i2 / p.NS) & 1u, nullptr, ATT_WAIT_NS);
             }
-            for (uint32_t j = 0; j < 2 && j < gt; ++j) {
-                const uint32_t t2 = gt - 1 - j;
+            for (uint32_t j = 0; j < 2 && j < gp; ++j) {
+                const uint32_t t2 = gp - 1 - j;
                 mbar_wait(pfree + 8 * (t2 & 1u), (t2 >> 1) & 1u, nullptr, ATT_WAIT_NS);
             }
+            for (uint32_t j = 0; j < 2 && j < ua; ++j) {
+                const uint32_t i2 = ua - 1 - j;
+                mbar_wait(qfree + 8 * (i2 & 1u), (i2 >> 1) & 1u, nullptr, ATT_WAIT_NS);
+            }
+            if (gp > 0) mbar_wait(odone, (gp - 1) & 1u, nullptr, ATT_WAIT_NS);
         }
         __syncwarp();
-    } else if (warp < 6) {
-        // ================= softmax / output: 4 warps, TMEM lane quadrant = warp % 4 =================
-        // The named-barrier sequence below does not depend on `ok`: after a failed wait a warp
-        // keeps stepping through the barriers and only skips the work, so no warp is left
-        // waiting at a barrier that another warp will never reach.
-        const int q = warp & 3;
-        const int etid = threadIdx.x - 64;  // 0..127
-        const int kk = q * 32 + lane;       // key within a tile / d row within a 128-block
-        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        const uint32_t qblk = (uint32_t)N_pad * 128;
-        uint32_t gt = 0, gch = 0, ul = 0;
-        uint32_t slot_use[MAX_TS];
-#pragma unroll
-        for (int s = 0; s < MAX_TS; ++s) slot_use[s] = 0;
+    } else if (warp == 4 || warp == 5 || warp == 8 || warp == 9) {
+        // ================= softmax: the threads of TMEM lane q own query q =================
+        // Two warps per lane quadrant, one per half of the tile's 128 key columns (and of the
+        // d columns of O). Per tile they exchange only the row's partial maxima; each keeps
+        // its own partial row sum, combined once per unit.
+        const int qd = warp & 3;          // TMEM lane quadrant (0 or 1)
+        const int hf = warp >> 3;         // column half
+        const int lrow = qd * 32 + lane;  // TMEM lane = row of Q, S, P and O
+        int myq;                          // the query this lane holds
+        bool vrow;
+        if (p.split) {
+            myq = qd == 0 ? lane : p.J1 * p.G + lane;
+            vrow = lane < (qd == 0 ? p.J1 : p.k + 1 - p.J1) * p.G;
+        } else {
+            myq = lrow;
+            vrow = lrow < n_q;
+        }
+        const bool active = p.split || qd * 32 < n_q;
+        const int jrow = vrow ? myq / p.G : 0;  // the row's draft index j
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        const float sl = p.scale_log2;
+        constexpr int HC = TILE_KEYS / 2;  // key columns per warp
+        constexpr int HD = D / 2;          // O columns per warp
+        float *xch = reinterpret_cast<float *>(small + 64);  // [2 tiles][2 quadrants][2 halves][32]
+        uint32_t gs = 0, gp = 0, ua = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
-            const UnitInfo ui = unit_info(p, u);
+        for (int it_u = blockIdx.x; it_u < p.n_units && active; it_u += gridDim.x) {
+            int u;
+            const UnitInfo ui = unit_info(p, it_u, u);
             float *ml = p.ws_ml + (size_t)u * n_q * 2;
             if (ui.T == 0) {
-                if (ui.bad_pos && ui.split == 0 && ui.g == 0 && etid == 0) raise_error(p.err, SPEC_DEVERR_POS);
-                for (int c = etid; c < n_q; c += 128) {
-                    ml[2 * c] = -INFINITY;
-                    ml[2 * c + 1] = ui.bad_pos ? -1.f : 0.f;
+                if (hf == 0) {
+                    if (ui.bad_pos && ui.split == 0 && ui.g == 0 && lrow == 0) raise_error(p.err, SPEC_DEVERR_POS);
+                    if (vrow) {
+                        ml[2 * myq] = -INFINITY;
+                        ml[2 * myq + 1] = ui.bad_pos ? -1.f : 0.f;
+                    }
                 }
                 continue;
             }
-            // ---- Q of (b, g): rows j*G + i -> q[b*(k+1)+j][g*G+i][:], zero padding rows ----
-            for (int i = etid; i < N_pad * (D / 8); i += 128) {
-                const int row = i / (D / 8), cc = i % (D / 8);
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (row < n_q) {
-                    const int j = row / p.G, hi = row % p.G;
-                    const uint16_t *src = p.q + ((size_t)(ui.b * (p.k + 1) + j) * p.Hq + ui.g * p.G + hi) * D + cc * 8;
-                    v = __ldg(reinterpret_cast<const uint4 *>(src));
-                    if (FP8) {
-                        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                        uint32_t h[4];
+            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+            const uint32_t ob = p.OB == 2 ? (ua & 1u) : 0u;
+            if (ok) ok = warp_wait(ufull + 8 * ub, uph, abort_flag);
+            const UnitTable *tab = tables + ub;
+            const bool failed = ok && tab->bad != 0;
+            float m = -INFINITY, l = 0.f;  // running maximum (log2 units) and this half's sum
+            // key offsets (from the split's start) this row sees: [0, climit0]; a lane without
+            // a query treats every key as seen (its row of P only feeds an unread row of O)
+            const int climit0 = vrow ? ui.pos_b + jrow - ui.s0 : (1 << 30);
+            for (int t = 0; t < ui.T; ++t, ++gs, ++gp) {
+                const uint32_t sb = gs & 1u, pb = gp & 1u;
+                if (ok) ok = warp_wait(sfull + 8 * sb, (gs >> 1) & 1u, abort_flag);
+                if (!ok) continue;
+                tc_fence_after();
+                // columns c (of this half) with HC*hf + c <= climit are seen
+                const int climit = climit0 - t * TILE_KEYS - HC * hf;
+                const bool all_seen = __all_sync(0xFFFFFFFFu, climit >= HC - 1);
+                uint32_t sv[HC / 16][16];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            __half2 hh = __floats2half2_rn(bf16_lo(w[e]), bf16_hi(w[e]));
-                            h[e] = *reinterpret_cast<uint32_t *>(&hh);
-                        }
-                        v = make_uint4(h[0], h[1], h[2], h[3]);
+                for (int c = 0; c < HC / 16; ++c) tmem_ld16(t_s + lane_base + sb * TILE_KEYS + HC * hf + c * 16, sv[c]);
+                // FP8 pools: the scores come from E4M3 codes and P multiplies E4M3 codes of V.
+                // The half-tile's K scale joins the softmax scale and its V scale multiplies P
+                // (the row sum stays unscaled); with pages shorter than the half-tile the
+                // scales are applied per key.
+                float slk = sl, vmul = 1.f;
+                bool percol = false;
+                if (FP8) {
+                    if (!small_pages && p.kv.page_size >= HC) {
+                        const int e = (t * TILE_KEYS + HC * hf) >> log2P;
+                        slk = sl * tab->ksc[e];
+                        vmul = tab->vsc[e];
+                    } else {
+                        percol = true;
                     }
                 }
-                *reinterpret_cast<uint4 *>(g_q + sw128_off(row, cc * 8, qblk)) = v;
-            }
-            fence_proxy_async_smem();
-            if (etid < N_pad) {
-                mrun[etid] = -INFINITY;
-                lrun[etid] = 0.f;
-            }
-            if (etid == 0) *fail_flag = 0;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(qready);
-            named_bar(1, 128);
-            const uint32_t ob = p.OB == 2 ? (ul & 1u) : 0u;
-            bool failed = false;
-            for (int ch = 0; ch < ui.n_chunks; ++ch) {
-                const int t0 = ch * TS, t1 = min(ui.T, t0 + TS);
-                // ---- pass A: each column's maximum over the chunk's keys ----
-                float mth[MAX_NPAD];
-#pragma unroll
-                for (int c = 0; c < MAX_NPAD; ++c) mth[c] = -INFINITY;
-                for (int t = t0; t < t1; ++t) {
-                    const int slot = t - t0;
-                    uint32_t su = 0;
-#pragma unroll
-                    for (int s = 0; s < MAX_TS; ++s)
-                        if (s == slot) su = slot_use[s];
-                    // this key is seen by the columns [cth, cend): rows j with key <= pos_b + j
-                    const int key = ui.s0 + t * TILE_KEYS + kk;
-                    int cth = 0, cend = 0;
-                    float ksc = 1.f;
-                    if (key < ui.kv_end) {
+                auto col_scales = [&](int c, float &ks, float &vs) {
+                    const int key = ui.s0 + t * TILE_KEYS + HC * hf + c;
+                    ks = 0.f;
+                    vs = 0.f;
+                    if (key >= ui.kv_end) return;
+                    if (!small_pages) {
+                        const int e = (key - ui.s0) >> log2P;
+                        ks = tab->ksc[e];
+                        vs = tab->vsc[e];
+                    } else {
                         const int pg = page_of(p.kv, ui.b, key);
-                        if (pg < 0) failed = true;
-                        else if (FP8) ksc = __ldg(p.kv.k_scale + (size_t)pg * p.kv.n_kv_heads + ui.g);
-                        const int J = key - ui.pos_b;
-                        cth = J > 0 ? J * p.G : 0;
-                        cend = n_q;
+                        if (pg >= 0) {
+                            ks = __ldg(p.kv.k_scale + (size_t)pg * p.kv.n_kv_heads + ui.g);
+                            vs = __ldg(p.kv.v_scale + (size_t)pg * p.kv.n_kv_heads + ui.g);
+                        }
                     }
-                    if (ok) ok = warp_wait(sfull + 8 * slot, su & 1u, abort_flag);
+                };
+                tmem_ld_wait();
+                if (FP8 && percol) {
+#pragma unroll
+                    for (int c = 0; c < HC; ++c) {
+                        float ks, vs;
+                        col_scales(c, ks, vs);
+                        sv[c >> 4][c & 15] = __float_as_uint(__uint_as_float(sv[c >> 4][c & 15]) * ks);
+                    }
+                }
+                // ---- pass 1: partial maximum of s*sl over the seen columns (8 short chains) ----
+                float acc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = -INFINITY;
+                if (slk >= 0.f && all_seen) {
+#pragma unroll
+                    for (int c = 0; c < HC; ++c) acc[c & 7] = fmaxf(acc[c & 7], __uint_as_float(sv[c >> 4][c & 15]));
+                } else {
+                    const float sgn = slk >= 0.f ? 1.f : -1.f;
+#pragma unroll
+                    for (int c = 0; c < HC; ++c)
+                        if (c <= climit) acc[c & 7] = fmaxf(acc[c & 7], sgn * __uint_as_float(sv[c >> 4][c & 15]));
+                    if (slk < 0.f) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[e] = -acc[e];  // now minima of s: scaled below
+                    }
+                }
+                float pm = slk >= 0.f ? fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
+                                              fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])))
+                                      : fminf(fminf(fminf(acc[0], acc[1]), fminf(acc[2], acc[3])),
+                                              fminf(fminf(acc[4], acc[5]), fminf(acc[6], acc[7])));
+                pm = (pm == -INFINITY || pm == INFINITY) ? -INFINITY : pm * slk;
+                // ---- the row's maximum: exchange with the other half ----
+                float *xt = xch + (sb * 2 + qd) * 64;
+                xt[hf * 32 + lane] = pm;
+                named_bar(1 + qd, 64);
+                const float mx = vrow ? fmaxf(pm, xt[(hf ^ 1) * 32 + lane]) : -INFINITY;
+                // ---- the P buffer is free once P.V of tile t-2 is done ----
+                ok = warp_wait(pfree + 8 * pb, ((gp >> 1) & 1u) ^ 1u, abort_flag);
+                if (!ok) continue;
+                // ---- lazily raised maximum; a move rescales l and the row of O ----
+                const float mnew = (mx > m + RESCALE_TAU) ? mx : m;
+                const bool resc = mnew != m && m != -INFINITY;
+                if (__any_sync(0xFFFFFFFFu, resc)) {
+                    // O is written by P.V of tile t-1 (the one before it is done: see above)
+                    ok = warp_wait(odone, (gp - 1) & 1u, abort_flag);
                     if (!ok) continue;
                     tc_fence_after();
-                    const float sl = p.scale_log2 * ksc;
+                    const float f = resc ? ex2_approx(m - mnew) : 1.f;
+                    l *= f;
+                    const uint32_t orow = t_o + lane_base + ob * D + HD * hf;
 #pragma unroll
-                    for (int c0 = 0; c0 < MAX_NPAD; c0 += 16) {
-                        if (c0 < n_q) {
-                            uint32_t r[16];
-                            tmem_ld16(tmem + lane_base + slot * N_pad + c0, r);
-                            tmem_ld_wait();
+                    for (int c0 = 0; c0 < HD; c0 += 32) {
+                        uint32_t r[2][16];
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int c = c0 + j;
-                                const float v = __uint_as_float(r[j]) * sl;
-                                if (c >= cth && c < cend) mth[c] = fmaxf(mth[c], v);
-                            }
-                        }
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < MAX_NPAD; ++c) {
-                    if (c < n_q) {
-                        const float mx = warp_max(mth[c]);
-                        if (lane == 0) red_max[q * N_pad + c] = mx;
-                    }
-                }
-                named_bar(1, 128);
-                if (etid < n_q) {
-                    const float mt = fmaxf(fmaxf(red_max[etid], red_max[N_pad + etid]),
-                                           fmaxf(red_max[2 * N_pad + etid], red_max[3 * N_pad + etid]));
-                    const float mo = mrun[etid];
-                    const float mn = fmaxf(mo, mt);
-                    const float cr = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
-                    cor[etid] = cr;
-                    mnew[etid] = mn;
-                    mrun[etid] = mn;
-                    if (ch > 0 && cr != 1.f) *corr_flag = 1;
-                }
-                named_bar(1, 128);
-                // ---- a later chunk whose maximum grew: rescale O once all earlier P.V are done ----
-                if (ch > 0 && *corr_flag) {
-                    if (ok) ok = warp_wait(ochunk, (gch - 1) & 1u, abort_flag);
-                    if (ok) {
-                        tc_fence_after();
-#pragma unroll
-                        for (int nb = 0; nb < S_::NB; ++nb) {
-                            const uint32_t o_addr = t_o + lane_base + (ob * S_::NB + nb) * N_pad;
-                            for (int c0 = 0; c0 < n_q; c0 += 16) {
-                                uint32_t r[16];
-                                tmem_ld16(o_addr + c0, r);
-                                tmem_ld_wait();
-#pragma unroll
-                                for (int j = 0; j < 16; ++j)
-                                    r[j] = __float_as_uint(__uint_as_float(r[j]) * cor[c0 + j]);
-                                tmem_st16(o_addr + c0, r);
-                            }
-                        }
-                        tmem_st_wait();
-                        tc_fence_before();
-                    }
-                }
-                // ---- pass B: P = exp2(s - m) for P.V, per-thread sums ----
-                float lth[MAX_NPAD];
-#pragma unroll
-                for (int c = 0; c < MAX_NPAD; ++c) lth[c] = 0.f;
-                for (int t = t0; t < t1; ++t, ++gt) {
-                    const int slot = t - t0;
-                    const int key = ui.s0 + t * TILE_KEYS + kk;
-                    int cth = 0, cend = 0;
-                    float ksc = 1.f, vsc = 1.f;
-                    if (key < ui.kv_end) {
-                        if (FP8) {
-                            const int pg = page_of(p.kv, ui.b, key);
-                            if (pg >= 0) {
-                                const size_t si = (size_t)pg * p.kv.n_kv_heads + ui.g;
-                                ksc = __ldg(p.kv.k_scale + si);
-                                vsc = __ldg(p.kv.v_scale + si) * P_SCALE_FP8;
-                            }
-                        }
-                        const int J = key - ui.pos_b;
-                        cth = J > 0 ? J * p.G : 0;
-                        cend = n_q;
-                    }
-                    const uint32_t pb = gt & 1u;
-                    if (ok) ok = warp_wait(pfree + 8 * pb, ((gt >> 1) & 1u) ^ 1u, abort_flag);
-                    if (!ok) continue;
-                    const float sl = p.scale_log2 * ksc;
-                    // this key's row of P (MN-major: the columns are contiguous, 128-byte swizzle)
-                    uint8_t *prow = g_p + pb * P_BUF + kk * 128;
-                    const int swz = kk & 7;
-#pragma unroll
-                    for (int c0 = 0; c0 < MAX_NPAD; c0 += 16) {
-                        if (c0 < N_pad) {
-                            uint32_t pk[8];
-                            if (c0 < n_q) {
-                                uint32_t r[16];
-                                tmem_ld16(tmem + lane_base + slot * N_pad + c0, r);
-                                float mv[16];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float4 m4 = reinterpret_cast<const float4 *>(mnew + c0)[e];
-                                    mv[4 * e] = m4.x;
-                                    mv[4 * e + 1] = m4.y;
-                                    mv[4 * e + 2] = m4.z;
-                                    mv[4 * e + 3] = m4.w;
-                                }
-                                tmem_ld_wait();
-#pragma unroll
-                                for (int j = 0; j < 16; j += 2) {
-                                    const int c = c0 + j;
-                                    float a = ex2_approx(fmaf(__uint_as_float(r[j]), sl, -mv[j]));
-                                    float b = ex2_approx(fmaf(__uint_as_float(r[j + 1]), sl, -mv[j + 1]));
-                                    a = (c >= cth && c < cend) ? a : 0.f;
-                                    b = (c + 1 >= cth && c + 1 < cend) ? b : 0.f;
-                                    lth[c] += a;
-                                    lth[c + 1] += b;
-                                    if (FP8) {
-                                        const __half2 h = __floats2half2_rn(a * vsc, b * vsc);
-                                        pk[j >> 1] = *reinterpret_cast<const uint32_t *>(&h);
-                                    } else {
-                                        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-                                        pk[j >> 1] = *reinterpret_cast<const uint32_t *>(&h);
-                                    }
-                                }
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) pk[e] = 0u;
-                            }
-                            const int ch0 = c0 >> 3;
-                            *reinterpret_cast<uint4 *>(prow + (((ch0 ^ swz) & 7) << 4)) =
-                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                            *reinterpret_cast<uint4 *>(prow + ((((ch0 + 1) ^ swz) & 7) << 4)) =
-                                make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                        }
-                    }
-                    tc_fence_before();
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(sfree + 8 * slot);
-                        mbar_arrive(pfull + 8 * pb);
-                    }
-                }
-#pragma unroll
-                for (int s = 0; s < MAX_TS; ++s)
-                    if (s < t1 - t0) slot_use[s] += 1;
-                // ---- one cross-lane sum per column ----
-#pragma unroll
-                for (int c = 0; c < MAX_NPAD; ++c) {
-                    if (c < n_q) {
-                        const float sm = warp_sum(lth[c]);
-                        if (lane == 0) red_sum[q * N_pad + c] = sm;
-                    }
-                }
-                named_bar(1, 128);
-                if (etid < n_q)
-                    lrun[etid] = lrun[etid] * cor[etid] + ((red_sum[etid] + red_sum[N_pad + etid]) +
-                                                           (red_sum[2 * N_pad + etid] + red_sum[3 * N_pad + etid]));
-                if (etid == 0) *corr_flag = 0;
-                ++gch;
-                named_bar(1, 128);
-            }
-            if (failed) *fail_flag = 1;
-            // the unit's last P.V, then its partial
-            if (ok) {
-                ok = warp_wait(ochunk, (gch - 1) & 1u, abort_flag);
-                if (ok) tc_fence_after();
-            }
-            named_bar(1, 128);
-            if (ok) {
-                float *o_ws = p.ws_o + (size_t)u * n_q * D;
-                const float oscale = FP8 ? 1.f / P_SCALE_FP8 : 1.f;
-#pragma unroll
-                for (int nb = 0; nb < S_::NB; ++nb) {
-                    const uint32_t o_addr = t_o + lane_base + (ob * S_::NB + nb) * N_pad;
-                    const int drow = nb * 128 + kk;
-                    for (int c0 = 0; c0 < n_q; c0 += 16) {
-                        uint32_t r[16];
-                        tmem_ld16(o_addr + c0, r);
+                        for (int e = 0; e < 2; ++e) tmem_ld16(orow + c0 + 16 * e, r[e]);
                         tmem_ld_wait();
-                        if (drow < D) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                if (c0 + j < n_q) o_ws[(size_t)(c0 + j) * D + drow] = __uint_as_float(r[j]) * oscale;
+                        for (int e = 0; e < 2; ++e) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) r[e][j] = __float_as_uint(__uint_as_float(r[e][j]) * f);
+                            tmem_st16(orow + c0 + 16 * e, r[e]);
                         }
+                    }
+                    tmem_st_wait();
+                }
+                m = mnew;
+                // ---- pass 2: P = 2^(s - m) of the row's half: 64-key block hf of P ----
+                float lacc[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) lacc[e] = 0.f;
+                uint8_t *prow = g_p + pb * PBUF + hf * PATOM + lrow * 128;
+                const int swz = lrow & 7;
+#pragma unroll
+                for (int c0 = 0; c0 < HC; c0 += 16) {
+                    const uint32_t(&r)[16] = sv[c0 >> 4];
+                    uint32_t pk[8];
+                    if (all_seen && !(FP8 && percol)) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 2) {
+                            const float a = ex2_approx(fmaf(__uint_as_float(r[j]), slk, -m));
+                            const float b = ex2_approx(fmaf(__uint_as_float(r[j + 1]), slk, -m));
+                            lacc[j >> 1] += a + b;
+                            pk[j >> 1] = FP8 ? pack2(a * vmul, b * vmul, true) : pack2(a, b, false);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 2) {
+                            float a = ex2_approx(fmaf(__uint_as_float(r[j]), slk, -m));
+                            float b = ex2_approx(fmaf(__uint_as_float(r[j + 1]), slk, -m));
+                            a = (c0 + j <= climit) ? a : 0.f;
+                            b = (c0 + j + 1 <= climit) ? b : 0.f;
+                            lacc[j >> 1] += a + b;
+                            float va = vmul, vb = vmul;
+                            if (FP8 && percol) {
+                                float ks;
+                                col_scales(c0 + j, ks, va);
+                                col_scales(c0 + j + 1, ks, vb);
+                            }
+                            pk[j >> 1] = FP8 ? pack2(a * va, b * vb, true) : pack2(a, b, false);
+                        }
+                    }
+                    if (lrow < R_pad) {
+                        const int ch0 = c0 >> 3;
+                        *reinterpret_cast<uint4 *>(prow + (((ch0 ^ swz) & 7) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        *reinterpret_cast<uint4 *>(prow + ((((ch0 + 1) ^ swz) & 7) << 4)) =
+                            make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    }
+                }
+                l += ((lacc[0] + lacc[1]) + (lacc[2] + lacc[3])) + ((lacc[4] + lacc[5]) + (lacc[6] + lacc[7]));
+                tc_fence_before();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(sfree + 8 * sb);
+                    mbar_arrive(pfull + 8 * pb);
+                }
+            }
+            // the unit table is no longer read
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(ufree + 8 * ub);
+            // ---- the unit's last P.V (P.V of the tile before it is done first) ----
+            if (ok) ok = warp_wait(pfree + 8 * (gp & 1u), ((gp >> 1) & 1u) ^ 1u, abort_flag);
+            if (ok) ok = warp_wait(odone, (gp - 1) & 1u, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                float *orow_g = p.ws_o + ((size_t)u * n_q + myq) * D + HD * hf;
+                const uint32_t orow = t_o + lane_base + ob * D + HD * hf;
+#pragma unroll
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    uint32_t r[2][16];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) tmem_ld16(orow + c0 + 16 * e, r[e]);
+                    tmem_ld_wait();
+                    if (vrow) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            reinterpret_cast<float4 *>(orow_g + c0)[e] =
+                                make_float4(__uint_as_float(r[e >> 2][4 * (e & 3)]), __uint_as_float(r[e >> 2][4 * (e & 3) + 1]),
+                                            __uint_as_float(r[e >> 2][4 * (e & 3) + 2]),
+                                            __uint_as_float(r[e >> 2][4 * (e & 3) + 3]));
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(ofree + 8 * ob);
             }
-            const bool unit_failed = *fail_flag != 0;
-            for (int c = etid; c < n_q; c += 128) {
-                ml[2 * c] = mrun[c];
-                ml[2 * c + 1] = (unit_failed || !ok) ? -1.f : lrun[c];
+            // ---- the row's sum: the two halves' partial sums ----
+            float *lx = xch + 256 + qd * 64;
+            lx[hf * 32 + lane] = l;
+            named_bar(1 + qd, 64);
+            if (hf == 0 && vrow) {
+                ml[2 * myq] = m;
+                ml[2 * myq + 1] = (failed || !ok) ? -1.f : l + lx[32 + lane];
             }
-            if (unit_failed && etid == 0) raise_error(p.err, SPEC_DEVERR_PAGE);
-            ++ul;
-            named_bar(1, 128);
+            named_bar(1 + qd, 64);  // lx is reused by the next unit
+            ++ua;
         }
         if (!ok) {
             *abort_flag = 1;
-            if (etid == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
+            if (lrow == 0 && hf == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
-    } else if (FP8) {
-        // ================= E4M3 -> f16 operand conversion: warps 6..9 =================
-        const int ctid = threadIdx.x - 192;  // 0..127
-        uint32_t gi = 0;
+    } else {
+        // ================= loaders, warps 2, 3, 6, 7: K / V gather (and FP8 conversion) =================
+        // Each thread copies its own 16-byte pieces of every sub-tile with cp.async and lets the
+        // copies arrive on the stage's barrier by themselves when they land
+        // (cp.async.mbarrier.arrive.noinc), so a sub-tile is visible to its consumer as soon as
+        // its data is in shared memory and no loader ever holds data back. bf16 rows go straight
+        // into the swizzled operand stage (the MMA warp fences for the async proxy after its
+        // wait). E4M3 rows go to a raw ring; once a raw stage has landed, the same threads
+        // convert exactly the pieces they loaded into an operand stage.
+        const int ltid = ((warp & 1) | ((warp >> 1) & 2)) * 32 + lane;  // warps 2, 3, 6, 7 -> 0..127
+        constexpr int ESZ = FP8 ? 1 : 2;
+        constexpr int CH = S_::SUB_COLS * ESZ / 16;  // 16-byte pieces per row of a sub-tile
+        constexpr int RPS = 128 / CH;                // rows per step of the 128 threads
+        constexpr int NPIECE = TILE_KEYS / RPS;      // pieces per thread per sub-tile
+        const int pch = ltid % CH, prow0 = ltid / CH;
+        const size_t row_bytes = (size_t)D * ESZ;
+        uint32_t gi = 0, gc = 0, ua = 0;  // sub-tiles issued / converted (FP8), active units
         bool ok = true;
-        for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-            const UnitInfo ui = unit_info(p, u);
-            for (int i = 0; i < 2 * ui.T; ++i, ++gi) {
-                const uint32_t rs = gi % p.NR, os = gi % p.NS;
-                if (!warp_wait(raw_full + 8 * rs, (gi / p.NR) & 1u, abort_flag) ||
-                    !warp_wait(op_empty + 8 * os, ((gi / p.NS) & 1u) ^ 1u, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t *raw = smem + p.off_raw + rs * S_::RAW_STAGE;
-                uint8_t *op = smem + os * S_::OP_STAGE;
-                constexpr int CPR = D / 16;  // 16-byte chunks per raw row
-                for (int chn = ctid; chn < TILE_KEYS * CPR; chn += 128) {
-                    const int row = chn / CPR, cc = chn % CPR;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * D + cc * 16);
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                    uint32_t h[8];
+        // FP8: convert raw sub-tile j (landed) into its operand stage
+        auto convert = [&](uint32_t j) -> bool {
+            const uint32_t rs = j % p.NR, os = j % p.NS;
+            if (!warp_wait(raw_full + 8 * rs, (j / p.NR) & 1u, abort_flag) ||
+                !warp_wait(op_empty + 8 * os, ((j / p.NS) & 1u) ^ 1u, abort_flag))
+                return false;
+            const uint8_t *raw = smem + p.off_raw + rs * S_::RAW_STAGE;
+            uint8_t *op = smem + p.off_op + os * S_::OP_STAGE;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] & 0xFFFFu), __NV_E4M3);
-                        __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] >> 16), __NV_E4M3);
-                        h[2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-                        h[2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
-                    }
-                    *reinterpret_cast<uint4 *>(op + sw128_off(row, cc * 16, TILE_KEYS * 128)) =
-                        make_uint4(h[0], h[1], h[2], h[3]);
-                    *reinterpret_cast<uint4 *>(op + sw128_off(row, cc * 16 + 8, TILE_KEYS * 128)) =
-                        make_uint4(h[4], h[5], h[6], h[7]);
+            for (int k = 0; k < NPIECE; ++k) {
+                const int row = k * RPS + prow0;
+                const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * S_::SUB_COLS + pch * 16);
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t hv[8];  // E4M3 is exact in f16; the page scales are applied by the softmax
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] & 0xFFFFu), __NV_E4M3);
+                    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] >> 16), __NV_E4M3);
+                    hv[2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+                    hv[2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+                }
+                *reinterpret_cast<uint4 *>(op + sw128_off(row, pch * 16, TILE_KEYS * 128)) =
+                    make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                *reinterpret_cast<uint4 *>(op + sw128_off(row, pch * 16 + 8, TILE_KEYS * 128)) =
+                    make_uint4(hv[4], hv[5], hv[6], hv[7]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(op_full + 8 * os);
+            return true;
+        };
+        // FP8: convert every issued sub-tile whose data has landed and whose operand stage is
+        // free, without blocking
+        auto convert_ready = [&]() -> bool {
+            while (gc < gi) {
+                const bool ready = mbar_test(raw_full + 8 * (gc % p.NR), (gc / p.NR) & 1u) &&
+                                   mbar_test(op_empty + 8 * (gc % p.NS), ((gc / p.NS) & 1u) ^ 1u);
+                if (!__all_sync(0xFFFFFFFFu, ready)) break;
+                if (!convert(gc)) return false;
+                ++gc;
+            }
+            return true;
+        };
+        // FP8: convert everything issued (blocking); done before any wait that might block
+        auto convert_all = [&]() -> bool {
+            for (; gc < gi; ++gc)
+                if (!convert(gc)) return false;
+            return true;
+        };
+        for (int it_u = blockIdx.x; it_u < p.n_units && ok; it_u += gridDim.x) {
+            int u;
+            const UnitInfo ui = unit_info(p, it_u, u);
+            if (ui.T == 0) continue;
+            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+            const UnitTable *tab = tables + ub;
+            if (FP8 && __any_sync(0xFFFFFFFFu, !mbar_test(ufull + 8 * ub, uph)) && !convert_all()) { ok = false; break; }
+            if (!warp_wait(ufull + 8 * ub, uph, abort_flag)) { ok = false; break; }
+            if (FP8) {
+                // Q arrives as bf16; the f16-kind MMA needs f16 on both sides: convert in place
+                if (__any_sync(0xFFFFFFFFu, !mbar_test(qfull + 8 * ub, uph)) && !convert_all()) { ok = false; break; }
+                if (!warp_wait(qfull + 8 * ub, uph, abort_flag)) { ok = false; break; }
+                uint8_t *qb = smem + p.off_q + ub * QBUF;
+                for (int i = ltid; i < S_::NATOM * R_pad * 8; i += 128) {
+                    const int a = i / (R_pad * 8), rem = i % (R_pad * 8);
+                    uint4 *ptr = reinterpret_cast<uint4 *>(qb + a * QATOM + rem * 16);
+                    const uint4 v = *ptr;
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t hq[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) hq[e] = pack2(bf16_lo(w[e]), bf16_hi(w[e]), true);
+                    *ptr = make_uint4(hq[0], hq[1], hq[2], hq[3]);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(op_full + 8 * os);
-                    mbar_arrive(raw_empty + 8 * rs);
+                if (lane == 0) mbar_arrive(qconv + 8 * ub);
+            }
+            ++ua;
+            for (int t = 0; t < ui.T && ok; ++t) {
+                const int key0 = ui.s0 + t * TILE_KEYS;
+                for (int it = 0; it < 2 * S_::NSUB; ++it) {
+                    const int kv = it / S_::NSUB, h = it % S_::NSUB;  // K or V, half of d
+                    const uint8_t *pool = reinterpret_cast<const uint8_t *>(kv ? p.kv.v_pool : p.kv.k_pool);
+                    uint32_t dst_base, bar;
+                    if (FP8) {
+                        // the raw stage is free once this warp converted its previous use
+                        if (gi - gc == (uint32_t)p.NR) {
+                            if (!convert(gc)) { ok = false; break; }
+                            ++gc;
+                        }
+                        dst_base = s_raw + (gi % p.NR) * S_::RAW_STAGE;
+                        bar = raw_full + 8 * (gi % p.NR);
+                    } else {
+                        const uint32_t s = gi % p.NS;
+                        if (!warp_wait(op_empty + 8 * s, ((gi / p.NS) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+                        dst_base = s_op + s * S_::OP_STAGE;
+                        bar = op_full + 8 * s;
+                    }
+                    const uint8_t *src_col = pool + (size_t)h * S_::SUB_COLS * ESZ + pch * 16;
+                    // rows past the branch's last position, or of an invalid page, stay unloaded.
+                    // Per group of 8 pieces: the page lookups and offsets first (independent
+                    // loads), then the copies.
+                    constexpr int GRP = NPIECE < 8 ? NPIECE : 8;
+#pragma unroll
+                    for (int k0 = 0; k0 < NPIECE; k0 += GRP) {
+                        uint32_t rowi[GRP];  // row index in the pool viewed as [num_pages * Hkv * P][d]
+                        uint32_t valid = 0;
+                        if (!small_pages) {
+                            int pgk[GRP];
+#pragma unroll
+                            for (int k = 0; k < GRP; ++k) {  // (key - s0) < split_keys: inside the table
+                                const int e = (t * TILE_KEYS + (k0 + k) * RPS + prow0) >> log2P;
+                                pgk[k] = tab->page[e];
+                            }
+#pragma unroll
+                            for (int k = 0; k < GRP; ++k) {
+                                const int key = key0 + (k0 + k) * RPS + prow0;
+                                const int pg = key < ui.kv_end ? pgk[k] : -1;
+                                valid |= (pg >= 0 ? 1u : 0u) << k;
+                                rowi[k] = (uint32_t)(pg * p.kv.n_kv_heads + ui.g) * (uint32_t)p.kv.page_size +
+                                          (uint32_t)(key & (p.kv.page_size - 1));
+                            }
+                        } else {
+                            for (int k = 0; k < GRP; ++k) {
+                                const int key = key0 + (k0 + k) * RPS + prow0;
+                                const int pg = key < ui.kv_end ? page_of(p.kv, ui.b, key) : -1;
+                                valid |= (pg >= 0 ? 1u : 0u) << k;
+                                rowi[k] = (uint32_t)(pg * p.kv.n_kv_heads + ui.g) * (uint32_t)p.kv.page_size +
+                                          (uint32_t)(key & (p.kv.page_size - 1));
+                            }
+                        }
+#pragma unroll
+                        for (int k = 0; k < GRP; ++k) {
+                            const int row = (k0 + k) * RPS + prow0;
+                            const uint32_t dst =
+                                FP8 ? dst_base + row * S_::SUB_COLS + pch * 16
+                                    : dst_base + (pch >> 3) * (TILE_KEYS * 128) + row * 128 +
+                                          ((((pch & 7) ^ (row & 7)) & 7) << 4);
+                            if ((valid >> k) & 1u) cp_async16(dst, src_col + (size_t)rowi[k] * row_bytes);
+                        }
+                    }
+                    cp_async_arrive(bar);
+                    ++gi;
+                    if (FP8 && !convert_ready()) { ok = false; break; }
                 }
             }
+            // the unit's table is no longer read by this warp
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(ufree + 8 * ub);
         }
+        if (FP8 && ok) ok = convert_all();
+        // every copy lands before the CTA may exit
+        cp_async_wait_all();
         if (!ok) {
             *abort_flag = 1;
-            if (ctid == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
+            if (ltid == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
     }
     // ================= teardown =================
@@ -778,54 +876,100 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, p.tmem_cols);
+        tmem_dealloc(tmem, 512);
     }
 }
 
-// One warp per (row, q head): merge the splits in ascending order.
+// One CTA of 8 warps per (row, q head): merge the row's splits. The maximum over the
+// splits is reduced in parallel; warp w sums the splits s = w, w+8, ... in ascending
+// order, and the 8 partial sums are added in warp order. Empty splits (l = 0) are skipped,
+// so the result depends only on the row's own splits, not on the batch's split count.
+constexpr int CMB_WARPS = 8;
 template <int D>
-__global__ void __launch_bounds__(256) attn_combine_kernel(const float *__restrict__ ws_ml,
-                                                           const float *__restrict__ ws_o, int B, int k, int Hq,
-                                                           int G, int Hkv, int n_splits, uint16_t *out) {
-    constexpr int E = D / 32;
-    const int warp_global = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    const int R = B * (k + 1);
-    if (warp_global >= R * Hq) return;
-    const int r = warp_global / Hq, h = warp_global % Hq;
+__global__ void __launch_bounds__(CMB_WARPS * 32) attn_combine_kernel(const float *__restrict__ ws_ml,
+                                                                      const float *__restrict__ ws_o, int B, int k,
+                                                                      int Hq, int G, int Hkv, int n_splits,
+                                                                      uint16_t *out) {
+    constexpr int E = D / 32;  // columns per lane
+    __shared__ float red_m[CMB_WARPS];
+    __shared__ int red_f[CMB_WARPS];
+    __shared__ float part_o[CMB_WARPS][D];
+    __shared__ float part_l[CMB_WARPS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = blockIdx.x / Hq, h = blockIdx.x % Hq;
     const int b = r / (k + 1), j = r % (k + 1);
     const int g = h / G, hi = h % G;
     const int n_q = (k + 1) * G;
     const int qi = j * G + hi;
     const size_t unit0 = ((size_t)b * Hkv + g) * n_splits;
+    // ---- the maximum over the non-empty splits; any failed split fails the row ----
     float M = -INFINITY;
-    bool failed = false;
-    for (int s = 0; s < n_splits; ++s) {
+    int failed = 0;
+    for (int s = threadIdx.x; s < n_splits; s += CMB_WARPS * 32) {
         const float *ml = ws_ml + ((unit0 + s) * n_q + qi) * 2;
         const float l = ml[1];
-        if (l < 0.f) failed = true;
+        if (l < 0.f) failed = 1;
         if (l > 0.f) M = fmaxf(M, ml[0]);
     }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+        failed |= __shfl_xor_sync(0xFFFFFFFFu, failed, off);
+    }
+    if (lane == 0) {
+        red_m[warp] = M;
+        red_f[warp] = failed;
+    }
+    __syncthreads();
+    M = -INFINITY;
+    failed = 0;
+#pragma unroll
+    for (int w = 0; w < CMB_WARPS; ++w) {
+        M = fmaxf(M, red_m[w]);
+        failed |= red_f[w];
+    }
     if (failed || M == -INFINITY) return;  // error already raised; output left unwritten
+    // ---- this warp's splits ----
     float L = 0.f, o[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) o[e] = 0.f;
-    for (int s = 0; s < n_splits; ++s) {
+    for (int s = warp; s < n_splits; s += CMB_WARPS) {
         const float *ml = ws_ml + ((unit0 + s) * n_q + qi) * 2;
         const float l = ml[1];
         if (!(l > 0.f)) continue;
         const float w = exp2f(ml[0] - M);
         L = fmaf(l, w, L);
-        const float *os = ws_o + ((unit0 + s) * n_q + qi) * D;
+        const float *os = ws_o + ((unit0 + s) * n_q + qi) * D + lane * E;
+        if (E % 4 == 0) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[e] = fmaf(w, __ldg(os + lane + 32 * e), o[e]);
+            for (int e = 0; e < E; e += 4) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(os + e));
+                o[e] = fmaf(w, v.x, o[e]);
+                o[e + 1] = fmaf(w, v.y, o[e + 1]);
+                o[e + 2] = fmaf(w, v.z, o[e + 2]);
+                o[e + 3] = fmaf(w, v.w, o[e + 3]);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) o[e] = fmaf(w, __ldg(os + e), o[e]);
+        }
     }
-    const float inv = 1.f / L;
-    uint16_t *dst = out + ((size_t)r * Hq + h) * D;
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-        __nv_bfloat16 v = __float2bfloat16_rn(o[e] * inv);
-        dst[lane + 32 * e] = *reinterpret_cast<uint16_t *>(&v);
+    for (int e = 0; e < E; ++e) part_o[warp][lane * E + e] = o[e];
+    if (lane == 0) part_l[warp] = L;
+    __syncthreads();
+    // ---- the warps' partial sums, in warp order ----
+    float Lt = 0.f;
+#pragma unroll
+    for (int w = 0; w < CMB_WARPS; ++w) Lt += part_l[w];
+    const float inv = 1.f / Lt;
+    uint16_t *dst = out + ((size_t)r * Hq + h) * D;
+    for (int c = threadIdx.x; c < D; c += CMB_WARPS * 32) {
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < CMB_WARPS; ++w) acc += part_o[w][c];
+        __nv_bfloat16 v = __float2bfloat16_rn(acc * inv);
+        dst[c] = *reinterpret_cast<uint16_t *>(&v);
     }
 }
 
@@ -850,22 +994,6 @@ static EncodeTiledFnA encode_fn_attn() {
     return fn;
 }
 
-// The pool viewed as [num_pages * Hkv * page_size rows][d] with a (box_cols x box_rows) box.
-static bool make_pool_map(CUtensorMap *map, const void *base, const KvView &kv, bool fp8, int box_rows) {
-    EncodeTiledFnA fn = encode_fn_attn();
-    if (!fn) return false;
-    const cuuint64_t rows = (cuuint64_t)kv.num_pages * kv.n_kv_heads * kv.page_size;
-    const int esz = fp8 ? 1 : 2;
-    cuuint64_t dims[2] = {(cuuint64_t)kv.head_dim, rows};
-    cuuint64_t strides[1] = {(cuuint64_t)kv.head_dim * esz};
-    cuuint32_t box[2] = {(cuuint32_t)(fp8 ? kv.head_dim : 64), (cuuint32_t)box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base),
-              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 static int attn_sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
@@ -873,40 +1001,73 @@ static int attn_sm_count() {
     return n;
 }
 
+// Q [R][Hq][d] viewed as a 3-D tensor (d, Hq, R): a (64, G, J) box at (a*64, g*G, b*(k+1) + j0)
+// holds the J*G query vectors of (branch b, kv head g) with draft rows j0..j0+J-1, in row
+// order (j - j0)*G + i.
+static bool make_q_map(CUtensorMap *map, const void *q, int R, int Hq, int d, int G, int J) {
+    EncodeTiledFnA fn = encode_fn_attn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hq, (cuuint64_t)R};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)Hq * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)J};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Shared-memory plan, in this order (every block 1024-aligned): 2 Q buffers, 2 P buffers,
+// the operand ring, the raw ring and its row scales (FP8), 2 unit tables, barriers, flags.
+// The M = 128 MMAs read up to (128 - R_pad) rows past the last Q / P block; the operand
+// ring that follows is always larger than that.
+template <int D, bool FP8>
+static int plan_attn(AttnTcParams &p, size_t *smem_bytes) {
+    using S_ = AttnShape<D, FP8>;
+    const uint32_t q_bytes = 2 * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.R_pad * 128;
+    const uint32_t ut_bytes = 2 * (uint32_t)sizeof(UnitTable);
+    const uint32_t bars = 8 * 64, small = 64 + 1024 + 512;
+    const uint32_t fixed = 1024 + q_bytes + p_bytes + ut_bytes + bars + small;
+    const uint32_t raw_row = FP8 ? S_::RAW_STAGE : 0;
+    if (ATT_SMEM_LIMIT < fixed + 2 * S_::OP_STAGE + 2 * raw_row) return SPEC_ERR_UNSUPPORTED;
+    const uint32_t avail = ATT_SMEM_LIMIT - fixed;
+    if (!FP8) {
+        p.NS = (int)(avail / S_::OP_STAGE);
+        p.NS = p.NS > 6 ? 6 : p.NS;
+        p.NR = 0;
+    } else {
+        // the raw ring holds the bytes in flight from HBM, the operand ring converted
+        // sub-tiles waiting for their MMA: one stage more than two tiles' worth, so that the
+        // converter (which works in ring order) never waits on V of a tile behind its softmax
+        p.NS = 2 * S_::NSUB + 1;
+        if (avail < p.NS * S_::OP_STAGE + 4 * raw_row) p.NS = 2 * S_::NSUB;
+        if (avail < p.NS * S_::OP_STAGE + 2 * raw_row) p.NS = 2;
+        p.NR = (int)((avail - p.NS * S_::OP_STAGE) / (raw_row ? raw_row : 1u));
+        p.NR = p.NR > 8 ? 8 : p.NR;
+        if (p.NR < 2) return SPEC_ERR_UNSUPPORTED;
+    }
+    // S of tile t+1 ahead of P.V of tile t needs the ring to hold V_t and K_{t+1} at once
+    p.lookahead = p.NS >= 2 * S_::NSUB ? 1 : 0;
+    p.OB = 256 + 2 * D <= 512 ? 2 : 1;
+    p.off_q = 0;
+    p.off_p = p.off_q + q_bytes;
+    p.off_op = p.off_p + p_bytes;
+    p.off_raw = p.off_op + p.NS * S_::OP_STAGE;
+    p.off_ut = p.off_raw + p.NR * S_::RAW_STAGE;
+    p.off_bar = p.off_ut + ut_bytes;
+    p.off_small = p.off_bar + bars;
+    *smem_bytes = 1024 + p.off_small + small;
+    return SPEC_OK;
+}
+
 template <int D, bool FP8>
 static int launch_attn_tc(AttnTcParams &p, cudaStream_t s) {
     using S_ = AttnShape<D, FP8>;
-    const int NATOM = S_::NATOM;
-    p.off_q = 0;  // set below
-    const uint32_t q_bytes = NATOM * p.N_pad * 128, p_bytes = 2 * P_BUF;  // P: 2 buffers
-    const uint32_t small = 64 + 12 * p.N_pad * 4 + 64;
-    const uint32_t bars = 8 * 64;
-    const uint32_t fixed = 1024 + q_bytes + p_bytes + small + bars;
-    const uint32_t per = S_::OP_STAGE + S_::RAW_STAGE;
-    int depth = (int)((ATT_SMEM_LIMIT - fixed) / per);
-    depth = depth > 6 ? 6 : depth;
-    if (depth >= 2) {
-        p.NS = depth;
-        p.NR = FP8 ? depth : 0;
-    } else if (FP8 && ATT_SMEM_LIMIT >= fixed + 2 * S_::OP_STAGE + S_::RAW_STAGE) {
-        // two operand stages are the minimum (the next K tile loads while the current V
-        // tile is in use); the raw ring takes what is left
-        p.NS = 2;
-        p.NR = (int)((ATT_SMEM_LIMIT - fixed - 2 * S_::OP_STAGE) / (S_::RAW_STAGE ? S_::RAW_STAGE : 1));
-        p.NR = p.NR > 2 ? 2 : p.NR;
-    } else {
-        return SPEC_ERR_UNSUPPORTED;
-    }
-    p.off_q = p.NS * S_::OP_STAGE;
-    p.off_p = p.off_q + q_bytes;
-    p.off_raw = p.off_p + p_bytes;
-    p.off_bar = p.off_raw + p.NR * S_::RAW_STAGE;
-    p.off_small = p.off_bar + bars;
-    const size_t smem = 1024 + p.off_small + small;
-    CUtensorMap mk, mv;
-    const int box_rows = p.kv.page_size < TILE_KEYS ? p.kv.page_size : TILE_KEYS;
-    if (!make_pool_map(&mk, p.kv.k_pool, p.kv, FP8, box_rows) || !make_pool_map(&mv, p.kv.v_pool, p.kv, FP8, box_rows))
-        return SPEC_ERR_CUDA;
+    size_t smem = 0;
+    const int st = plan_attn<D, FP8>(p, &smem);
+    if (st) return st;
+    CUtensorMap mq0, mq1;
+    if (!make_q_map(&mq0, p.q, p.B * (p.k + 1), p.Hq, D, p.G, p.J1)) return SPEC_ERR_CUDA;
+    if (!make_q_map(&mq1, p.q, p.B * (p.k + 1), p.Hq, D, p.G, p.split ? p.k + 1 - p.J1 : p.J1)) return SPEC_ERR_CUDA;
     // a fixed ceiling (see the skinny GEMM launcher): graphs may mix launch sizes
     if (cudaFuncSetAttribute(attn_tc_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM_LIMIT) !=
         cudaSuccess)
@@ -914,7 +1075,7 @@ static int launch_attn_tc(AttnTcParams &p, cudaStream_t s) {
     const int sms = attn_sm_count();
     if (sms < 1) return SPEC_ERR_CUDA;
     const int grid = p.n_units < sms ? p.n_units : sms;
-    attn_tc_kernel<D, FP8><<<grid, S_::THREADS, smem, s>>>(mk, mv, p);
+    attn_tc_kernel<D, FP8><<<grid, S_::THREADS, smem, s>>>(mq0, mq1, p);
     return launch_status();
 }
 
@@ -931,7 +1092,8 @@ SPEC_API size_t spec_verify_attn_workspace(const spec_kv_desc *kv, int B, int k,
     if (spec::check_kv_desc(kv) || B < 1 || k < 0 || k > SPEC_KMAX || n_q_heads < 1 || max_pos < 1) return 0;
     if (n_q_heads % kv->n_kv_heads) return 0;
     const int G = n_q_heads / kv->n_kv_heads;
-    const int n_splits = (max_pos + spec::SPLIT_KEYS - 1) / spec::SPLIT_KEYS;
+    const int sk = spec::split_keys_for(kv->n_kv_heads);
+    const int n_splits = (max_pos + sk - 1) / sk;
     return spec::ws_bytes_for(B, kv->n_kv_heads, n_splits, (k + 1) * G, kv->head_dim);
 }
 
@@ -950,16 +1112,13 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     const int G = n_q_heads / kvd->n_kv_heads;
     const int n_q = (k + 1) * G;
     const int N_pad = ((n_q + 15) / 16) * 16;
-    const int NB = kvd->head_dim <= 128 ? 1 : 2;
     if (N_pad > spec::MAX_NPAD) return SPEC_ERR_UNSUPPORTED;
-    // TMEM: TS S tiles of N_pad columns + OB output buffers of NB*N_pad columns <= 512
-    int OB = 2, TS = (512 - 2 * NB * N_pad) / N_pad;
-    if (TS < spec::MAX_TS) {
-        OB = 1;
-        TS = (512 - NB * N_pad) / N_pad;
-    }
-    TS = TS > spec::MAX_TS ? spec::MAX_TS : TS;
-    if (TS < 1) return SPEC_ERR_UNSUPPORTED;
+    // spread the queries over two TMEM lane quadrants (two softmax warps) when both halves
+    // of the draft rows fit in 32 lanes each
+    const int J1 = (k + 2) / 2;
+    const bool split = k >= 1 && J1 * G <= 32 && (k + 1 - J1) * G <= 32;
+    const int R_pad = split ? 32 + (((k + 1 - J1) * G + 15) / 16) * 16 : N_pad;
+    if (R_pad > spec::MAX_RPAD) return SPEC_ERR_UNSUPPORTED;
     spec::AttnTcParams p{};
     p.kv = spec::make_view(kvd);
     p.pos = pos;
@@ -968,8 +1127,11 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     p.Hq = n_q_heads;
     p.G = G;
     p.n_q = n_q;
-    p.N_pad = N_pad;
-    p.n_splits = (max_pos + spec::SPLIT_KEYS - 1) / spec::SPLIT_KEYS;
+    p.J1 = split ? J1 : k + 1;
+    p.split = split ? 1 : 0;
+    p.R_pad = R_pad;
+    p.split_keys = spec::split_keys_for(kvd->n_kv_heads);
+    p.n_splits = (max_pos + p.split_keys - 1) / p.split_keys;
     p.max_pos = max_pos;
     p.n_units = B * kvd->n_kv_heads * p.n_splits;
     p.q = (const uint16_t *)q;
@@ -980,11 +1142,6 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     p.ws_ml = (float *)ws;
     p.ws_o = (float *)((char *)ws + ml);
     p.err = dev_err;
-    p.TS = TS;
-    p.OB = OB;
-    uint32_t cols = 32;
-    while (cols < (uint32_t)(TS * N_pad + OB * NB * N_pad)) cols <<= 1;
-    p.tmem_cols = cols;
     cudaStream_t s = (cudaStream_t)stream;
     const bool fp8 = kvd->kv_dtype == SPEC_KV_FP8_E4M3;
     switch (kvd->head_dim * 2 + (fp8 ? 1 : 0)) {
@@ -997,18 +1154,19 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     }
     if (st) return st;
     const int R = B * (k + 1);
-    const int cblocks = (R * n_q_heads + 7) / 8;
+    const int cblocks = R * n_q_heads;
+    constexpr int CT = spec::CMB_WARPS * 32;
     switch (kvd->head_dim) {
         case 64:
-            spec::attn_combine_kernel<64><<<cblocks, 256, 0, s>>>(p.ws_ml, p.ws_o, B, k, n_q_heads, G,
+            spec::attn_combine_kernel<64><<<cblocks, CT, 0, s>>>(p.ws_ml, p.ws_o, B, k, n_q_heads, G,
                                                                   kvd->n_kv_heads, p.n_splits, (uint16_t *)out);
             break;
         case 128:
-            spec::attn_combine_kernel<128><<<cblocks, 256, 0, s>>>(p.ws_ml, p.ws_o, B, k, n_q_heads, G,
+            spec::attn_combine_kernel<128><<<cblocks, CT, 0, s>>>(p.ws_ml, p.ws_o, B, k, n_q_heads, G,
                                                                    kvd->n_kv_heads, p.n_splits, (uint16_t *)out);
             break;
         default:
-            spec::attn_combine_kernel<256><<<cblocks, 256, 0, s>>>(p.ws_ml, p.ws_o, B, k, n_q_heads, G,
+            spec::attn_combine_kernel<256><<<cblocks, CT, 0, s>>>(p.ws_ml, p.ws_o, B, k, n_q_heads, G,
                                                                    kvd->n_kv_heads, p.n_splits, (uint16_t *)out);
             break;
     }

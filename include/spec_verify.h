@@ -142,9 +142,11 @@ int spec_kv_write_rows(const spec_kv_desc *kv, const int32_t *row_branch,
  * attended: kv_hi = position"); memra-engine spec.rs, `full_attn_verify`
  * ("query row r attends to keys [0..base_len+r+1)"); DSSD-dev fast.py,
  * `_attention` (per-row exact key path).
- * Split-KV: keys are cut into fixed 1024-position splits, independent of B, k
- * and context, so a row's output is byte-identical whatever batch it is
- * verified in (memra-engine spec.rs, `MtpScratch`: fixed split geometry).
+ * Split-KV: keys are cut into fixed splits of 256 positions (n_kv_heads <= 2),
+ * 512 (n_kv_heads <= 4) or 1024 (otherwise): a function of the model's shape
+ * only, independent of B, k and context, so a row's output is byte-identical
+ * whatever batch it is verified in (memra-engine spec.rs, `MtpScratch`: fixed
+ * split geometry).
  *   q       device bf16 [B*(k+1)][n_q_heads][head_dim]
  *   out     device bf16 [B*(k+1)][n_q_heads][head_dim]
  *   scale   softmax scale (normally 1/sqrt(head_dim))
