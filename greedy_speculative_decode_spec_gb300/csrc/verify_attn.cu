@@ -28,8 +28,8 @@
 //              hold the n_q <= 64 queries), two warps per quadrant, one per half of the key
 //              columns; a quadrant without queries has nothing to do;
 //   warps 2, 3, 6, 7  gather K and V rows with 16-byte cp.async copies into the swizzled operand
-//              ring (bf16), or into a raw ring from which the same threads convert E4M3 to
-//              f16 exactly (FP8; Q is converted bf16 -> f16 in place). The page scales are
+//              ring (bf16); for FP8 pools warps 2, 3 gather E4M3 rows into a raw ring and
+//              warps 6, 7 convert them to f16 exactly (and Q bf16 -> f16 in place). The page scales are
 //              applied by the softmax: K's to the scores, V's to P (the row sum stays
 //              unscaled), so S and O come out in the pool's true units.
 // Keys beyond a row's position get P = 0 by select, never by multiplication, and V rows
@@ -180,8 +180,8 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     UnitTable *tables = reinterpret_cast<UnitTable *>(smem + p.off_ut);  // [2]
     // barrier map
     const uint32_t op_full = s_base + p.off_bar, op_empty = op_full + 8 * p.NS;
-    const uint32_t raw_full = op_empty + 8 * p.NS;                    // FP8 raw ring
-    const uint32_t sfull = raw_full + 8 * p.NR, sfree = sfull + 16;  // S double buffer
+    const uint32_t raw_full = op_empty + 8 * p.NS, raw_empty = raw_full + 8 * p.NR;  // FP8 raw ring
+    const uint32_t sfull = raw_empty + 8 * p.NR, sfree = sfull + 16;                 // S double buffer
     const uint32_t pfull = sfree + 16, pfree = pfull + 16;            // P double buffer
     const uint32_t odone = pfree + 16, ofree = odone + 8;             // P.V completions, O buffers
     const uint32_t qfull = ofree + 16, qconv = qfull + 16, qfree = qconv + 16;  // Q double buffer
@@ -198,11 +198,14 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.NS; ++s) {
-            // bf16: each loader thread's copies arrive; FP8: each loader warp after converting
-            mbar_init(op_full + 8 * s, FP8 ? 4 : 128);
+            // bf16: each loader thread's copies arrive; FP8: each converter warp
+            mbar_init(op_full + 8 * s, FP8 ? 2 : 128);
             mbar_init(op_empty + 8 * s, 1);
         }
-        for (int s = 0; s < p.NR; ++s) mbar_init(raw_full + 8 * s, 128);
+        for (int s = 0; s < p.NR; ++s) {
+            mbar_init(raw_full + 8 * s, 64);  // each FP8 loader thread's copies arrive
+            mbar_init(raw_empty + 8 * s, 2);  // the converter warps
+        }
         for (int a = 0; a < 2; ++a) {
             mbar_init(sfull + 8 * a, 1);
             mbar_init(sfree + 8 * a, n_act);
@@ -210,10 +213,10 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             mbar_init(pfree + 8 * a, 1);
             mbar_init(ofree + 8 * a, n_act);
             mbar_init(qfull + 8 * a, 1);
-            mbar_init(qconv + 8 * a, 4);
+            mbar_init(qconv + 8 * a, 2);
             mbar_init(qfree + 8 * a, 1);
             mbar_init(ufull + 8 * a, 1);
-            mbar_init(ufree + 8 * a, n_act + 4);  // softmax and loader warps
+            mbar_init(ufree + 8 * a, n_act + (FP8 ? 2 : 4));  // softmax and loader warps
         }
         mbar_init(odone, 1);
         mbar_init(drain, 1);
@@ -696,121 +699,45 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             *abort_flag = 1;
             if (lrow == 0 && hf == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
-    } else {
-        // ================= loaders, warps 2, 3, 6, 7: K / V gather (and FP8 conversion) =================
+    } else if (!FP8 || warp == 2 || warp == 3) {
+        // ================= loaders: K / V gather (bf16: warps 2, 3, 6, 7; FP8: warps 2, 3) =================
         // Each thread copies its own 16-byte pieces of every sub-tile with cp.async and lets the
         // copies arrive on the stage's barrier by themselves when they land
         // (cp.async.mbarrier.arrive.noinc), so a sub-tile is visible to its consumer as soon as
         // its data is in shared memory and no loader ever holds data back. bf16 rows go straight
         // into the swizzled operand stage (the MMA warp fences for the async proxy after its
-        // wait). E4M3 rows go to a raw ring; once a raw stage has landed, the same threads
-        // convert exactly the pieces they loaded into an operand stage.
+        // wait); E4M3 rows go to the raw ring, which the converter warps turn into operand
+        // stages. A loader waits only for a free stage.
+        constexpr int NT = FP8 ? 64 : 128;           // loader threads
         const int ltid = ((warp & 1) | ((warp >> 1) & 2)) * 32 + lane;  // warps 2, 3, 6, 7 -> 0..127
         constexpr int ESZ = FP8 ? 1 : 2;
         constexpr int CH = S_::SUB_COLS * ESZ / 16;  // 16-byte pieces per row of a sub-tile
-        constexpr int RPS = 128 / CH;                // rows per step of the 128 threads
+        constexpr int RPS = NT / CH;                 // rows per step of the loader threads
         constexpr int NPIECE = TILE_KEYS / RPS;      // pieces per thread per sub-tile
         const int pch = ltid % CH, prow0 = ltid / CH;
         const size_t row_bytes = (size_t)D * ESZ;
-        uint32_t gi = 0, gc = 0, ua = 0;  // sub-tiles issued / converted (FP8), active units
+        const uint32_t depth = FP8 ? (uint32_t)p.NR : (uint32_t)p.NS;
+        const uint32_t full_base = FP8 ? raw_full : op_full, empty_base = FP8 ? raw_empty : op_empty;
+        const uint32_t ring_base = FP8 ? s_raw : s_op;
+        const uint32_t stage_bytes = FP8 ? S_::RAW_STAGE : S_::OP_STAGE;
+        uint32_t gi = 0, ua = 0;  // sub-tiles issued, active units
         bool ok = true;
-        // FP8: convert raw sub-tile j (landed) into its operand stage
-        auto convert = [&](uint32_t j) -> bool {
-            const uint32_t rs = j % p.NR, os = j % p.NS;
-            if (!warp_wait(raw_full + 8 * rs, (j / p.NR) & 1u, abort_flag) ||
-                !warp_wait(op_empty + 8 * os, ((j / p.NS) & 1u) ^ 1u, abort_flag))
-                return false;
-            const uint8_t *raw = smem + p.off_raw + rs * S_::RAW_STAGE;
-            uint8_t *op = smem + p.off_op + os * S_::OP_STAGE;
-#pragma unroll
-            for (int k = 0; k < NPIECE; ++k) {
-                const int row = k * RPS + prow0;
-                const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * S_::SUB_COLS + pch * 16);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                uint32_t hv[8];  // E4M3 is exact in f16; the page scales are applied by the softmax
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] & 0xFFFFu), __NV_E4M3);
-                    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] >> 16), __NV_E4M3);
-                    hv[2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-                    hv[2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
-                }
-                *reinterpret_cast<uint4 *>(op + sw128_off(row, pch * 16, TILE_KEYS * 128)) =
-                    make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                *reinterpret_cast<uint4 *>(op + sw128_off(row, pch * 16 + 8, TILE_KEYS * 128)) =
-                    make_uint4(hv[4], hv[5], hv[6], hv[7]);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(op_full + 8 * os);
-            return true;
-        };
-        // FP8: convert every issued sub-tile whose data has landed and whose operand stage is
-        // free, without blocking
-        auto convert_ready = [&]() -> bool {
-            while (gc < gi) {
-                const bool ready = mbar_test(raw_full + 8 * (gc % p.NR), (gc / p.NR) & 1u) &&
-                                   mbar_test(op_empty + 8 * (gc % p.NS), ((gc / p.NS) & 1u) ^ 1u);
-                if (!__all_sync(0xFFFFFFFFu, ready)) break;
-                if (!convert(gc)) return false;
-                ++gc;
-            }
-            return true;
-        };
-        // FP8: convert everything issued (blocking); done before any wait that might block
-        auto convert_all = [&]() -> bool {
-            for (; gc < gi; ++gc)
-                if (!convert(gc)) return false;
-            return true;
-        };
         for (int it_u = blockIdx.x; it_u < p.n_units && ok; it_u += gridDim.x) {
             int u;
             const UnitInfo ui = unit_info(p, it_u, u);
             if (ui.T == 0) continue;
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
             const UnitTable *tab = tables + ub;
-            if (FP8 && __any_sync(0xFFFFFFFFu, !mbar_test(ufull + 8 * ub, uph)) && !convert_all()) { ok = false; break; }
             if (!warp_wait(ufull + 8 * ub, uph, abort_flag)) { ok = false; break; }
-            if (FP8) {
-                // Q arrives as bf16; the f16-kind MMA needs f16 on both sides: convert in place
-                if (__any_sync(0xFFFFFFFFu, !mbar_test(qfull + 8 * ub, uph)) && !convert_all()) { ok = false; break; }
-                if (!warp_wait(qfull + 8 * ub, uph, abort_flag)) { ok = false; break; }
-                uint8_t *qb = smem + p.off_q + ub * QBUF;
-                for (int i = ltid; i < S_::NATOM * R_pad * 8; i += 128) {
-                    const int a = i / (R_pad * 8), rem = i % (R_pad * 8);
-                    uint4 *ptr = reinterpret_cast<uint4 *>(qb + a * QATOM + rem * 16);
-                    const uint4 v = *ptr;
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                    uint32_t hq[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) hq[e] = pack2(bf16_lo(w[e]), bf16_hi(w[e]), true);
-                    *ptr = make_uint4(hq[0], hq[1], hq[2], hq[3]);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(qconv + 8 * ub);
-            }
             ++ua;
             for (int t = 0; t < ui.T && ok; ++t) {
                 const int key0 = ui.s0 + t * TILE_KEYS;
                 for (int it = 0; it < 2 * S_::NSUB; ++it) {
                     const int kv = it / S_::NSUB, h = it % S_::NSUB;  // K or V, half of d
                     const uint8_t *pool = reinterpret_cast<const uint8_t *>(kv ? p.kv.v_pool : p.kv.k_pool);
-                    uint32_t dst_base, bar;
-                    if (FP8) {
-                        // the raw stage is free once this warp converted its previous use
-                        if (gi - gc == (uint32_t)p.NR) {
-                            if (!convert(gc)) { ok = false; break; }
-                            ++gc;
-                        }
-                        dst_base = s_raw + (gi % p.NR) * S_::RAW_STAGE;
-                        bar = raw_full + 8 * (gi % p.NR);
-                    } else {
-                        const uint32_t s = gi % p.NS;
-                        if (!warp_wait(op_empty + 8 * s, ((gi / p.NS) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-                        dst_base = s_op + s * S_::OP_STAGE;
-                        bar = op_full + 8 * s;
-                    }
+                    const uint32_t s = gi % depth;
+                    if (!warp_wait(empty_base + 8 * s, ((gi / depth) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+                    const uint32_t dst_base = ring_base + s * stage_bytes;
                     const uint8_t *src_col = pool + (size_t)h * S_::SUB_COLS * ESZ + pch * 16;
                     // rows past the branch's last position, or of an invalid page, stay unloaded.
                     // Per group of 8 pieces: the page lookups and offsets first (independent
@@ -854,21 +781,92 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                             if ((valid >> k) & 1u) cp_async16(dst, src_col + (size_t)rowi[k] * row_bytes);
                         }
                     }
-                    cp_async_arrive(bar);
+                    cp_async_arrive(full_base + 8 * s);
                     ++gi;
-                    if (FP8 && !convert_ready()) { ok = false; break; }
                 }
             }
             // the unit's table is no longer read by this warp
             __syncwarp();
             if (ok && lane == 0) mbar_arrive(ufree + 8 * ub);
         }
-        if (FP8 && ok) ok = convert_all();
         // every copy lands before the CTA may exit
         cp_async_wait_all();
         if (!ok) {
             *abort_flag = 1;
             if (ltid == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
+        }
+    } else {
+        // ================= FP8 converters, warps 6, 7: E4M3 -> f16 operand stages =================
+        // E4M3 is exact in f16 (the page scales are applied by the softmax). Per unit the bf16
+        // Q is first converted to f16 in place, then every landed raw sub-tile in ring order.
+        const int ctid = (warp - 6) * 32 + lane;  // 0..63
+        constexpr int CCH = S_::SUB_COLS / 16;     // 16-byte raw pieces per row
+        constexpr int NPC = TILE_KEYS * CCH / 64;  // pieces per converter thread per sub-tile
+        uint32_t gc = 0, ua = 0;                   // sub-tiles converted, active units
+        bool ok = true;
+        for (int it_u = blockIdx.x; it_u < p.n_units && ok; it_u += gridDim.x) {
+            int u;
+            const UnitInfo ui = unit_info(p, it_u, u);
+            if (ui.T == 0) continue;
+            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+            // ---- Q arrives as bf16; the f16-kind MMA needs f16 on both sides ----
+            if (!warp_wait(qfull + 8 * ub, uph, abort_flag)) { ok = false; break; }
+            uint8_t *qb = smem + p.off_q + ub * QBUF;
+            for (int i = ctid; i < S_::NATOM * R_pad * 8; i += 64) {
+                const int a = i / (R_pad * 8), rem = i % (R_pad * 8);
+                uint4 *ptr = reinterpret_cast<uint4 *>(qb + a * QATOM + rem * 16);
+                const uint4 v = *ptr;
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t hq[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) hq[e] = pack2(bf16_lo(w[e]), bf16_hi(w[e]), true);
+                *ptr = make_uint4(hq[0], hq[1], hq[2], hq[3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qconv + 8 * ub);
+            ++ua;
+            // ---- the unit's K / V sub-tiles ----
+            const uint32_t n_sub = (uint32_t)(2 * S_::NSUB * ui.T);
+            for (uint32_t i = 0; i < n_sub; ++i, ++gc) {
+                const uint32_t rs = gc % p.NR, os = gc % p.NS;
+                if (!warp_wait(raw_full + 8 * rs, (gc / p.NR) & 1u, abort_flag) ||
+                    !warp_wait(op_empty + 8 * os, ((gc / p.NS) & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *raw = smem + p.off_raw + rs * S_::RAW_STAGE;
+                uint8_t *op = smem + p.off_op + os * S_::OP_STAGE;
+#pragma unroll
+                for (int k = 0; k < NPC; ++k) {
+                    const int piece = k * 64 + ctid;
+                    const int row = piece / CCH, pc = piece % CCH;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * S_::SUB_COLS + pc * 16);
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    uint32_t hv[8];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] & 0xFFFFu), __NV_E4M3);
+                        const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] >> 16), __NV_E4M3);
+                        hv[2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
+                        hv[2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+                    }
+                    *reinterpret_cast<uint4 *>(op + sw128_off(row, pc * 16, TILE_KEYS * 128)) =
+                        make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                    *reinterpret_cast<uint4 *>(op + sw128_off(row, pc * 16 + 8, TILE_KEYS * 128)) =
+                        make_uint4(hv[4], hv[5], hv[6], hv[7]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(op_full + 8 * os);
+                    mbar_arrive(raw_empty + 8 * rs);
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (ctid == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
     }
     // ================= teardown =================
