@@ -5,7 +5,7 @@
 // [H, 2H], the embedding half first. memra-engine src/spec.rs, `mtp_head_forward_dev`:
 // embedding gather, the two RMSNorms and the eh_proj matmul on the device.
 //
-// Kernel 1 (one block per row): gather E[tok], both RMSNorms in fp32 with a fixed
+// Kernel 1 (one block per row and half): gather E[tok], the RMSNorms in fp32 with a fixed
 // reduction order, the two halves rounded to bf16 into c[m] = [e ; h] (workspace).
 // Kernel 2: x = c . W_fc^T through the skinny GEMM, stored as bf16.
 #include "common.cuh"
@@ -13,54 +13,81 @@
 
 namespace spec {
 
-__device__ __forceinline__ float block_sum_256(float v, float *red) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float s = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];  // fixed order
-    return s;
-}
-
-__global__ void __launch_bounds__(256) mtp_norm_concat_kernel(const int32_t *tok, const uint16_t *E,
-                                                              const uint16_t *h, const float *g_emb,
-                                                              const float *g_hid, float eps, int H, int V,
-                                                              uint16_t *concat, int32_t *err) {
-    __shared__ float red[8];
-    const int m = blockIdx.x;
-    const int t = __ldg(tok + m);
-    uint16_t *c = concat + (size_t)m * 2 * H;
-    for (int half = 0; half < 2; ++half) {
-        const uint16_t *src;
-        const float *gain;
-        if (half == 0) {
-            if (t < 0 || t >= V) {
-                if (threadIdx.x == 0) raise_error(err, SPEC_DEVERR_TOKEN);
-                for (int i = threadIdx.x; i < H; i += blockDim.x) c[i] = 0;
-                continue;
-            }
-            src = E + (size_t)t * H;
-            gain = g_emb;
-        } else {
-            src = h + (size_t)m * H;
-            gain = g_hid;
+// One block per (row m, half): half 0 normalises E[tok[m]], half 1 normalises h[m]. Each
+// thread holds up to MAXC 8-element chunks of the vector in registers (16-byte loads), so
+// the vector is read once; longer vectors are re-read for the second pass.
+constexpr int NC_THREADS = 256, NC_MAXC = 8;
+__global__ void __launch_bounds__(NC_THREADS) mtp_norm_concat_kernel(const int32_t *tok, const uint16_t *E,
+                                                                     const uint16_t *h, const float *g_emb,
+                                                                     const float *g_hid, float eps, int H, int V,
+                                                                     uint16_t *concat, int32_t *err) {
+    __shared__ float red[NC_THREADS / 32];
+    const int m = blockIdx.x >> 1, half = blockIdx.x & 1;
+    uint16_t *c = concat + (size_t)m * 2 * H + (size_t)half * H;
+    const int nch = H / 8;  // 8-element chunks
+    const uint16_t *src;
+    const float *gain;
+    if (half == 0) {
+        const int t = __ldg(tok + m);
+        if (t < 0 || t >= V) {
+            if (threadIdx.x == 0) raise_error(err, SPEC_DEVERR_TOKEN);
+            for (int i = threadIdx.x; i < nch; i += NC_THREADS) reinterpret_cast<uint4 *>(c)[i] = make_uint4(0, 0, 0, 0);
+            return;
         }
-        float ss = 0.f;
-        for (int i = threadIdx.x; i < H; i += blockDim.x) {
-            const float x = __uint_as_float((uint32_t)src[i] << 16);
-            ss = fmaf(x, x, ss);
-        }
-        ss = block_sum_256(ss, red);
-        const float inv = 1.0f / sqrtf(ss / (float)H + eps);
-        for (int i = threadIdx.x; i < H; i += blockDim.x) {
-            const float x = __uint_as_float((uint32_t)src[i] << 16);
-            __nv_bfloat16 b = __float2bfloat16_rn(x * inv * __ldg(gain + i));
-            c[half * H + i] = *reinterpret_cast<uint16_t *>(&b);
-        }
+        src = E + (size_t)t * H;
+        gain = g_emb;
+    } else {
+        src = h + (size_t)m * H;
+        gain = g_hid;
     }
+    const uint4 *src4 = reinterpret_cast<const uint4 *>(src);
+    uint4 v[NC_MAXC];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < NC_MAXC; ++k) {
+        const int i = threadIdx.x + k * NC_THREADS;
+        v[k] = i < nch ? __ldg(src4 + i) : make_uint4(0, 0, 0, 0);
+    }
+    for (int i = threadIdx.x + NC_MAXC * NC_THREADS; i < nch; i += NC_THREADS) {  // H > 16384 only
+        const uint4 w = __ldg(src4 + i);
+        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ss = fmaf(bf16_lo(q[e]), bf16_lo(q[e]), fmaf(bf16_hi(q[e]), bf16_hi(q[e]), ss));
+    }
+#pragma unroll
+    for (int k = 0; k < NC_MAXC; ++k) {
+        const uint32_t q[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) ss = fmaf(bf16_lo(q[e]), bf16_lo(q[e]), fmaf(bf16_hi(q[e]), bf16_hi(q[e]), ss));
+    }
+    // block sum, fixed order
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < NC_THREADS / 32; ++w) tot += red[w];
+    const float inv = 1.0f / sqrtf(tot / (float)H + eps);
+    auto emit = [&](int i, const uint4 &w) {
+        const uint32_t q[4] = {w.x, w.y, w.z, w.w};
+        const float4 g0 = __ldg(reinterpret_cast<const float4 *>(gain) + 2 * i);
+        const float4 g1 = __ldg(reinterpret_cast<const float4 *>(gain) + 2 * i + 1);
+        const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 b = __floats2bfloat162_rn(bf16_lo(q[e]) * inv * gg[2 * e], bf16_hi(q[e]) * inv * gg[2 * e + 1]);
+            o[e] = *reinterpret_cast<const uint32_t *>(&b);
+        }
+        reinterpret_cast<uint4 *>(c)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    };
+#pragma unroll
+    for (int k = 0; k < NC_MAXC; ++k) {
+        const int i = threadIdx.x + k * NC_THREADS;
+        if (i < nch) emit(i, v[k]);
+    }
+    for (int i = threadIdx.x + NC_MAXC * NC_THREADS; i < nch; i += NC_THREADS) emit(i, __ldg(src4 + i));
 }
 
 static size_t concat_bytes(int M, int H) { return (((size_t)M * 2 * H * 2) + 255) & ~(size_t)255; }
@@ -84,7 +111,8 @@ SPEC_API int spec_mtp_input(const int32_t *tok, const void *E, const void *h, co
         return SPEC_ERR_ALIGN;
     cudaStream_t s = (cudaStream_t)stream;
     uint16_t *concat = (uint16_t *)((char *)ws + 256);
-    spec::mtp_norm_concat_kernel<<<M, 256, 0, s>>>(tok, (const uint16_t *)E, (const uint16_t *)h, g_emb, g_hid, eps,
+    if (!spec::aligned16(g_emb) || !spec::aligned16(g_hid)) return SPEC_ERR_ALIGN;
+    spec::mtp_norm_concat_kernel<<<2 * M, spec::NC_THREADS, 0, s>>>(tok, (const uint16_t *)E, (const uint16_t *)h, g_emb, g_hid, eps,
                                                    H, V, concat, dev_err);
     int st = spec::launch_status();
     if (st) return st;

@@ -228,7 +228,8 @@ int spec_accept(const int32_t *drafts, const int32_t *ids, const int32_t *pos, i
  *   g_emb, g_hid  device fp32 [H];  W_fc  device bf16 [H][2H];  x_out  device bf16 [M][H]
  *   ws     device workspace of spec_mtp_input_workspace(M, H) bytes; its first 256
  *          bytes follow the same zero rule as spec_lmhead_workspace.
- * Limits: 1 <= M <= 256, H % 64 == 0. Device error SPEC_DEVERR_TOKEN for tok[m]
+ * Limits: 1 <= M <= 256, H % 64 == 0; E, h, g_emb, g_hid, W_fc and x_out 16-byte
+ * aligned (SPEC_ERR_ALIGN otherwise). Device error SPEC_DEVERR_TOKEN for tok[m]
  * outside [0, V) (that row's c is written as zeros). */
 size_t spec_mtp_input_workspace(int M, int H);
 int spec_mtp_input(const int32_t *tok, const void *E, const void *h, const float *g_emb,
