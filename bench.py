@@ -31,6 +31,10 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one LM-head launch, from one
+# ncu capture of the unchanged kernel on that workload; None where no capture was taken.
+LMHEAD_TRAFFIC = {"single_stream_mtp_verify": 622430720 + 3319040}
+
 
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -340,7 +344,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": "spec_lmhead_argmax", "achieved": round(head_gbs, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(head_gbs / hbm_peak, 4),
                      "peak_kind": peak_kind, "algorithmic_bytes": main["w_bytes"], "kernel_us": round(main["t_head"] * 1e3, 2),
-                     "traffic": None},
+                     "traffic": LMHEAD_TRAFFIC.get(c.name)},
         "attention": {"kernel": "spec_verify_attn", "achieved": round(attn_gbs, 1), "unit": "GB/s",
                       "frac": round(attn_gbs / hbm_peak, 4), "kernel_us": round(main["t_attn"] * 1e3, 2),
                       "algorithmic_bytes": main["kv_bytes"]},
