@@ -166,6 +166,19 @@ class DraftStage:
                              dev_err=self.err)
 
 
+def replica_rate(ms_local: float, rows: int, world: int, device) -> tuple[float, float]:
+    """Whole-job rate of `world` independent replicas, each verifying `rows` rows per step:
+    the slowest rank's step time sets the pace (max over ranks)."""
+    import torch
+    import torch.distributed as dist
+    ms_max = ms_local
+    if world > 1:
+        t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    return ms_max, world * rows / (ms_max * 1e-3)
+
+
 def _graph_of(fn):
     """A CUDA graph holding one call of fn (so that timing sees device work only, not the
     host cost of the call)."""
@@ -306,12 +319,7 @@ def run_ours(args):
     main = measure(args.config, args.steps, args.warmup, with_e2e=True)
     c = main["cfg"]
     rows = c.B * (c.k + 1)
-    ms_max = main["ms"]
-    if world > 1:
-        t = torch.tensor([ms_max], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = world * rows / (ms_max * 1e-3)
+    ms_max, value = replica_rate(main["ms"], rows, world, dev)
     head_gbs = main["w_bytes"] / (main["t_head"] * 1e-3) / 1e9
     attn_gbs = main["kv_bytes"] / (main["t_attn"] * 1e-3) / 1e9
     others = {}

@@ -212,6 +212,28 @@ def test_bad_page_id_is_reported_not_trapped():
     assert e == 0 and np.array_equal(ids, vi.planted.numpy())
 
 
+def test_position_past_page_table_coverage_is_reported():
+    vi = verify_inputs(SMALL["tiny"])
+    c = vi.cfg
+    gkv = gpu_pool(vi)
+    last = (int(vi.pos.max()) + c.k) // c.P     # the page-table column of the last verify row
+    pt = gkv.page_table[:, :last].contiguous()  # that column is missing: not covered
+    desc = bnd.make_kv_desc(gkv.k, gkv.v, pt, c.P)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pos_d = vi.pos.cuda()
+    before = gkv.k.clone()
+    bnd.spec_kv_append(desc, pos_d, c.B, c.k, vi.k_new.cuda(), vi.v_new.cuda(), err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & bnd.DEVERR_COVER
+    assert torch.equal(gkv.k.view(torch.int16), before.view(torch.int16))   # skipped, nothing written
+    err.zero_()
+    out = torch.zeros((c.R, c.Hq, c.d), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(bnd.spec_verify_attn_workspace(desc, c.B, c.k, c.Hq, vi.max_pos), dtype=torch.uint8, device=DEV)
+    bnd.spec_verify_attn(desc, pos_d, c.B, c.k, c.Hq, vi.q.cuda(), 0.125, out, ws, vi.max_pos, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & bnd.DEVERR_COVER
+
+
 def test_d2t_out_of_range_is_reported():
     vi = verify_inputs(SMALL["tiny"])
     d2t = torch.arange(vi.cfg.V, dtype=torch.int32, device=DEV) * 3
