@@ -23,10 +23,13 @@ DEVERR_PAGE, DEVERR_COVER, DEVERR_TOKEN, DEVERR_D2T, DEVERR_POS, DEVERR_TIMEOUT,
 KMAX = 15
 KV_BF16, KV_FP8_E4M3 = 0, 1
 
+ERR_NULL, ERR_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_ALIGN = -1, -2, -3, -4, -5, -6
+SPEC_LMHEAD_STATIC_SCRATCH_BYTES = 256 + 1024 * 64 * 8  # as in include/spec_verify.h
+
 EXPORTS = ("spec_strerror", "spec_version", "spec_kv_append", "spec_kv_write_rows",
            "spec_verify_attn_workspace", "spec_verify_attn", "spec_lmhead_workspace",
            "spec_lmhead_argmax", "spec_lmhead_logits", "spec_accept", "spec_mtp_input_workspace",
-           "spec_mtp_input")
+           "spec_mtp_input", "spec_lmhead_argmax_static")
 
 
 class SpecError(RuntimeError):
@@ -68,6 +71,7 @@ def lib() -> ctypes.CDLL:
         L.spec_lmhead_workspace.argtypes = [_i32, _i32, _i32]
         L.spec_lmhead_argmax.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _sz, _vp, _vp]
         L.spec_lmhead_logits.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]
+        L.spec_lmhead_argmax_static.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp]
         L.spec_accept.argtypes = [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp]
         L.spec_mtp_input_workspace.restype = _sz
         L.spec_mtp_input_workspace.argtypes = [_i32, _i32]
@@ -178,6 +182,19 @@ def spec_lmhead_argmax(hidden, W, ids, ws, d2t=None, d2t_limit: int = 0, max_log
                                                           _ptr(max_logit, "max_logit", torch.float32),
                                                           _ptr(ws, "ws"), ws.numel() * ws.element_size(),
                                                           _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
+
+
+def spec_lmhead_argmax_static(hidden, W, ids, d2t=None, d2t_limit: int = 0, max_logit=None, dev_err=None,
+                              stream=None):
+    """spec_lmhead_argmax without a workspace: the library's own device scratch is used (see
+    the header for the size limit, the first-call set-up and the one-call-at-a-time rule)."""
+    M, H = hidden.shape
+    V = W.shape[0]
+    _check("spec_lmhead_argmax_static",
+           lib().spec_lmhead_argmax_static(_ptr(hidden, "hidden", torch.bfloat16), _ptr(W, "W", torch.bfloat16), M, V,
+                                           H, _ptr(d2t, "d2t", torch.int32), int(d2t_limit),
+                                           _ptr(ids, "ids", torch.int32), _ptr(max_logit, "max_logit", torch.float32),
+                                           _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
 
 
 def spec_lmhead_logits(hidden, W, logits, ids, ws, stream=None):

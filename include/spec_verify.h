@@ -194,6 +194,28 @@ int spec_lmhead_logits(const void *hidden, const void *W, int M, int V, int H,
                        float *logits, int32_t *ids, void *ws, size_t ws_bytes,
                        spec_stream_t stream);
 
+/* ---- a3 without a workspace ---------------------------------------------------------
+ * The source pages have no counterpart of this entry point. It computes exactly what
+ * spec_lmhead_argmax computes (same kernel, same ids and max_logit) for callers that
+ * cannot allocate device memory, e.g. an engine that gives its whole HBM budget to its own
+ * pool up front, or glue code that can only pass the call's tensors. The kernel's scratch
+ * (a launch counter and the per-CTA argmax keys) is a library-owned device array of
+ * SPEC_LMHEAD_STATIC_SCRATCH_BYTES bytes per device; no memory is allocated or freed.
+ *   arguments as spec_lmhead_argmax, without ws / ws_bytes.
+ * Limits: the call's spec_lmhead_workspace(M, V, H) must not exceed
+ * SPEC_LMHEAD_STATIC_SCRATCH_BYTES (always true for M <= 64); otherwise SPEC_ERR_WORKSPACE
+ * and nothing is launched.
+ * Set-up: the first call on a device (the current device) looks the array up and zeroes
+ * its counter with a synchronous cudaMemset; make that first call before any stream
+ * capture. Every completed call leaves the counter zero again.
+ * Concurrency: all calls on a device share the one array; calls that may be in flight at
+ * the same time race on it and may return wrong ids: order them on one stream or with
+ * events. */
+#define SPEC_LMHEAD_STATIC_SCRATCH_BYTES ((size_t)256 + (size_t)1024 * 64 * 8)
+int spec_lmhead_argmax_static(const void *hidden, const void *W, int M, int V, int H,
+                              const int32_t *d2t, int d2t_limit, int32_t *ids,
+                              float *max_logit, int32_t *dev_err, spec_stream_t stream);
+
 /* ---- a4: greedy chain acceptance --------------------------------------------------
  * Per branch b, with target ids g_j = ids[b*(k+1)+j]:
  *   a = the largest a <= k with drafts[b][i] == g_i for every i < a
