@@ -70,7 +70,8 @@ struct UnitTable {
     float ksc[UT_ENTRIES];
     float vsc[UT_ENTRIES];
     int32_t bad;
-    int32_t pad_[31];
+    int32_t iter;          // the unit's index in the walk order, or -1: no more units
+    int32_t pad_[30];
 };
 
 // Split size in positions, a function of the model's KV-head count only (never of B, k or
@@ -89,6 +90,7 @@ struct AttnTcParams {
     int J1, split, R_pad;
     const uint16_t *q;     // bf16 [R][Hq][d]
     float scale_log2;      // softmax scale * log2(e)
+    unsigned int *sched;   // [2]: next unit to hand out, CTAs done (zero between calls)
     float *ws_ml;          // [units][n_q][2]  (m in log2 units, l)
     float *ws_o;           // [units][n_q][d]
     int32_t *err;
@@ -187,6 +189,8 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     const uint32_t qfull = ofree + 16, qconv = qfull + 16, qfree = qconv + 16;  // Q double buffer
     const uint32_t ufull = qfree + 16, ufree = ufull + 16;                      // unit tables
     const uint32_t drain = ufree + 16;
+    // softmax half-warps' exchanges, per lane quadrant and buffer: row maxima, row sums
+    const uint32_t xfull = drain + 8, lfull = xfull + 32;
     uint8_t *small = smem + p.off_small;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(small + 4);
@@ -220,6 +224,10 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         }
         mbar_init(odone, 1);
         mbar_init(drain, 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(xfull + 8 * i, 2);
+            mbar_init(lfull + 8 * i, 2);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -240,15 +248,35 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
 
     if (warp == 0) {
         // ================= producer: per unit, the page table entries and Q =================
+        // Units are handed out dynamically: the producer takes the next index of the
+        // split-major walk from a global counter, skips empty units, and publishes the unit
+        // in the shared table that every other role waits on (-1 ends their loops).
         uint32_t ua = 0;
         bool ok = true;
-        for (int it_u = blockIdx.x; it_u < p.n_units && ok; it_u += gridDim.x) {
-            int u;
-            const UnitInfo ui = unit_info(p, it_u, u);
-            if (ui.T == 0) continue;
+        for (;;) {
+            int it_u = -1, u = 0;
+            UnitInfo ui;
+            for (;;) {
+                int cand = 0;
+                if (lane == 0) cand = (int)atomicAdd(p.sched, 1u);
+                cand = __shfl_sync(0xFFFFFFFFu, cand, 0);
+                if (cand >= p.n_units) break;
+                ui = unit_info(p, cand, u);
+                if (ui.T > 0) {
+                    it_u = cand;
+                    break;
+                }
+                if (ui.bad_pos && ui.split == 0 && ui.g == 0 && lane == 0) raise_error(p.err, SPEC_DEVERR_POS);
+            }
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
             UnitTable *tab = tables + ub;
             if (!warp_wait(ufree + 8 * ub, uph ^ 1u, abort_flag)) { ok = false; break; }
+            if (it_u < 0) {
+                if (lane == 0) tab->iter = -1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ufull + 8 * ub);
+                break;
+            }
             int badbits = 0;
             if (!small_pages) {
                 const int nkeys = min(ui.kv_end - ui.s0, p.split_keys);
@@ -279,6 +307,7 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             badbits = __reduce_or_sync(0xFFFFFFFFu, badbits);
             if (lane == 0) {
                 tab->bad = badbits;
+                tab->iter = it_u;
                 if (badbits) raise_error(p.err, badbits);
             }
             __syncwarp();
@@ -302,6 +331,14 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         if (!ok) {
             *abort_flag = 1;
             if (lane == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
+        }
+        // the last CTA to finish handing out units leaves the counters zero for the next call
+        if (lane == 0) {
+            __threadfence();
+            if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+                atomicExch(p.sched, 0u);
+                atomicExch(p.sched + 1, 0u);
+            }
         }
         // the Q copies still in flight land before the CTA may exit
         if (lane == 0) {
@@ -387,11 +424,13 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             ++gp;
             return true;
         };
-        for (int it_u = blockIdx.x; it_u < p.n_units && ok; it_u += gridDim.x) {
+        for (;;) {
+            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+            if (!warp_wait(ufull + 8 * ub, uph, abort_flag)) { ok = false; break; }
+            const int it_u = tables[ub].iter;
+            if (it_u < 0) break;
             int u;
             const UnitInfo ui = unit_info(p, it_u, u);
-            if (ui.T == 0) continue;
-            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
             const uint32_t ob = p.OB == 2 ? (ua & 1u) : 0u;
             const uint32_t ob_use = p.OB == 2 ? (ua >> 1) : ua;
             if (!warp_wait((FP8 ? qconv : qfull) + 8 * ub, uph, abort_flag) ||
@@ -469,28 +508,22 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         const float sl = p.scale_log2;
         constexpr int HC = TILE_KEYS / 2;  // key columns per warp
         constexpr int HD = D / 2;          // O columns per warp
-        float *xch = reinterpret_cast<float *>(small + 64);  // [2 tiles][2 quadrants][2 halves][32]
+        // row-maximum exchange [2 tiles][2 quadrants][2 halves][32], then row-sum exchange
+        // [2 units][2 quadrants][2 halves][32]
+        float *xch = reinterpret_cast<float *>(small + 64);
         uint32_t gs = 0, gp = 0, ua = 0;
         bool ok = true;
-        for (int it_u = blockIdx.x; it_u < p.n_units && active; it_u += gridDim.x) {
+        while (active && ok) {
+            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+            const uint32_t ob = p.OB == 2 ? (ua & 1u) : 0u;
+            if (!warp_wait(ufull + 8 * ub, uph, abort_flag)) { ok = false; break; }
+            const UnitTable *tab = tables + ub;
+            const int it_u = tab->iter;
+            if (it_u < 0) break;
             int u;
             const UnitInfo ui = unit_info(p, it_u, u);
             float *ml = p.ws_ml + (size_t)u * n_q * 2;
-            if (ui.T == 0) {
-                if (hf == 0) {
-                    if (ui.bad_pos && ui.split == 0 && ui.g == 0 && lrow == 0) raise_error(p.err, SPEC_DEVERR_POS);
-                    if (vrow) {
-                        ml[2 * myq] = -INFINITY;
-                        ml[2 * myq + 1] = ui.bad_pos ? -1.f : 0.f;
-                    }
-                }
-                continue;
-            }
-            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
-            const uint32_t ob = p.OB == 2 ? (ua & 1u) : 0u;
-            if (ok) ok = warp_wait(ufull + 8 * ub, uph, abort_flag);
-            const UnitTable *tab = tables + ub;
-            const bool failed = ok && tab->bad != 0;
+            const bool failed = tab->bad != 0;
             float m = -INFINITY, l = 0.f;  // running maximum (log2 units) and this half's sum
             // key offsets (from the split's start) this row sees: [0, climit0]; a lane without
             // a query treats every key as seen (its row of P only feeds an unread row of O)
@@ -572,7 +605,10 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                 // ---- the row's maximum: exchange with the other half ----
                 float *xt = xch + (sb * 2 + qd) * 64;
                 xt[hf * 32 + lane] = pm;
-                named_bar(1 + qd, 64);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xfull + 8 * (qd * 2 + sb));
+                ok = warp_wait(xfull + 8 * (qd * 2 + sb), (gs >> 1) & 1u, abort_flag);
+                if (!ok) continue;
                 const float mx = vrow ? fmaxf(pm, xt[(hf ^ 1) * 32 + lane]) : -INFINITY;
                 // ---- the P buffer is free once P.V of tile t-2 is done ----
                 ok = warp_wait(pfree + 8 * pb, ((gp >> 1) & 1u) ^ 1u, abort_flag);
@@ -685,14 +721,17 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                 if (lane == 0) mbar_arrive(ofree + 8 * ob);
             }
             // ---- the row's sum: the two halves' partial sums ----
-            float *lx = xch + 256 + qd * 64;
+            const uint32_t lb = qd * 2 + (ua & 1u);
+            float *lx = xch + 256 + lb * 64;
             lx[hf * 32 + lane] = l;
-            named_bar(1 + qd, 64);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(lfull + 8 * lb);
+            const bool lok = warp_wait(lfull + 8 * lb, (ua >> 1) & 1u, abort_flag);
             if (hf == 0 && vrow) {
                 ml[2 * myq] = m;
-                ml[2 * myq + 1] = (failed || !ok) ? -1.f : l + lx[32 + lane];
+                ml[2 * myq + 1] = (failed || !ok || !lok) ? -1.f : l + lx[32 + lane];
             }
-            named_bar(1 + qd, 64);  // lx is reused by the next unit
+            if (!lok) ok = false;
             ++ua;
         }
         if (!ok) {
@@ -722,13 +761,14 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         const uint32_t stage_bytes = FP8 ? S_::RAW_STAGE : S_::OP_STAGE;
         uint32_t gi = 0, ua = 0;  // sub-tiles issued, active units
         bool ok = true;
-        for (int it_u = blockIdx.x; it_u < p.n_units && ok; it_u += gridDim.x) {
-            int u;
-            const UnitInfo ui = unit_info(p, it_u, u);
-            if (ui.T == 0) continue;
+        for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
             const UnitTable *tab = tables + ub;
             if (!warp_wait(ufull + 8 * ub, uph, abort_flag)) { ok = false; break; }
+            const int it_u = tab->iter;
+            if (it_u < 0) break;
+            int u;
+            const UnitInfo ui = unit_info(p, it_u, u);
             ++ua;
             for (int t = 0; t < ui.T && ok; ++t) {
                 const int key0 = ui.s0 + t * TILE_KEYS;
@@ -804,11 +844,13 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         constexpr int NPC = TILE_KEYS * CCH / 64;  // pieces per converter thread per sub-tile
         uint32_t gc = 0, ua = 0;                   // sub-tiles converted, active units
         bool ok = true;
-        for (int it_u = blockIdx.x; it_u < p.n_units && ok; it_u += gridDim.x) {
+        for (;;) {
+            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+            if (!warp_wait(ufull + 8 * ub, uph, abort_flag)) { ok = false; break; }
+            const int it_u = tables[ub].iter;
+            if (it_u < 0) break;
             int u;
             const UnitInfo ui = unit_info(p, it_u, u);
-            if (ui.T == 0) continue;
-            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
             // ---- Q arrives as bf16; the f16-kind MMA needs f16 on both sides ----
             if (!warp_wait(qfull + 8 * ub, uph, abort_flag)) { ok = false; break; }
             uint8_t *qb = smem + p.off_q + ub * QBUF;
@@ -878,16 +920,19 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     }
 }
 
-// One CTA of 8 warps per (row, q head): merge the row's splits. The maximum over the
-// splits is reduced in parallel; warp w sums the splits s = w, w+8, ... in ascending
-// order, and the 8 partial sums are added in warp order. Empty splits (l = 0) are skipped,
-// so the result depends only on the row's own splits, not on the batch's split count.
+// One CTA of 8 warps per (row, q head): merge the row's splits. Only the branch's
+// non-empty splits were computed (split s holds keys from s * split_keys on); among them,
+// splits the row does not reach (l = 0) are skipped, so the result depends only on the
+// row's own splits, not on the batch's split count. The maximum over the splits is reduced
+// in parallel; warp w sums the splits s = w, w+8, ... in ascending order, and the 8 partial
+// sums are added in warp order.
 constexpr int CMB_WARPS = 8;
 template <int D>
 __global__ void __launch_bounds__(CMB_WARPS * 32) attn_combine_kernel(const float *__restrict__ ws_ml,
-                                                                      const float *__restrict__ ws_o, int B, int k,
+                                                                      const float *__restrict__ ws_o,
+                                                                      const int32_t *__restrict__ pos, int B, int k,
                                                                       int Hq, int G, int Hkv, int n_splits,
-                                                                      uint16_t *out) {
+                                                                      int split_keys, int max_pos, uint16_t *out) {
     constexpr int E = D / 32;  // columns per lane
     __shared__ float red_m[CMB_WARPS];
     __shared__ int red_f[CMB_WARPS];
@@ -900,10 +945,13 @@ __global__ void __launch_bounds__(CMB_WARPS * 32) attn_combine_kernel(const floa
     const int n_q = (k + 1) * G;
     const int qi = j * G + hi;
     const size_t unit0 = ((size_t)b * Hkv + g) * n_splits;
+    const int pos_b = __ldg(pos + b);
+    if (pos_b < 0 || pos_b + k + 1 > max_pos) return;  // error raised by the split kernel
+    const int n_used = (pos_b + k + split_keys) / split_keys;  // splits holding keys 0..pos_b+k
     // ---- the maximum over the non-empty splits; any failed split fails the row ----
     float M = -INFINITY;
     int failed = 0;
-    for (int s = threadIdx.x; s < n_splits; s += CMB_WARPS * 32) {
+    for (int s = threadIdx.x; s < n_used; s += CMB_WARPS * 32) {
         const float *ml = ws_ml + ((unit0 + s) * n_q + qi) * 2;
         const float l = ml[1];
         if (l < 0.f) failed = 1;
@@ -931,7 +979,7 @@ __global__ void __launch_bounds__(CMB_WARPS * 32) attn_combine_kernel(const floa
     float L = 0.f, o[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) o[e] = 0.f;
-    for (int s = warp; s < n_splits; s += CMB_WARPS) {
+    for (int s = warp; s < n_used; s += CMB_WARPS) {
         const float *ml = ws_ml + ((unit0 + s) * n_q + qi) * 2;
         const float l = ml[1];
         if (!(l > 0.f)) continue;
@@ -1023,7 +1071,7 @@ static int plan_attn(AttnTcParams &p, size_t *smem_bytes) {
     using S_ = AttnShape<D, FP8>;
     const uint32_t q_bytes = 2 * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.R_pad * 128;
     const uint32_t ut_bytes = 2 * (uint32_t)sizeof(UnitTable);
-    const uint32_t bars = 8 * 64, small = 64 + 1024 + 512;
+    const uint32_t bars = 8 * 64, small = 64 + 2048;
     const uint32_t fixed = 1024 + q_bytes + p_bytes + ut_bytes + bars + small;
     const uint32_t raw_row = FP8 ? S_::RAW_STAGE : 0;
     if (ATT_SMEM_LIMIT < fixed + 2 * S_::OP_STAGE + 2 * raw_row) return SPEC_ERR_UNSUPPORTED;
@@ -1077,11 +1125,13 @@ static int launch_attn_tc(AttnTcParams &p, cudaStream_t s) {
     return launch_status();
 }
 
+// workspace: a 256-byte header (the unit scheduler's counters: zero before the first call,
+// left zero by every call), the (m, l) pairs, the partial outputs
 static size_t ws_bytes_for(int B, int Hkv, int n_splits, int n_q, int d) {
     const size_t units = (size_t)B * Hkv * n_splits;
     size_t ml = units * n_q * 2 * sizeof(float);
     ml = (ml + 255) & ~(size_t)255;
-    return ml + units * n_q * d * sizeof(float);
+    return 256 + ml + units * n_q * d * sizeof(float);
 }
 
 }  // namespace spec
@@ -1137,8 +1187,9 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     const size_t units = (size_t)p.n_units;
     size_t ml = units * n_q * 2 * sizeof(float);
     ml = (ml + 255) & ~(size_t)255;
-    p.ws_ml = (float *)ws;
-    p.ws_o = (float *)((char *)ws + ml);
+    p.sched = (unsigned int *)ws;
+    p.ws_ml = (float *)((char *)ws + 256);
+    p.ws_o = (float *)((char *)ws + 256 + ml);
     p.err = dev_err;
     cudaStream_t s = (cudaStream_t)stream;
     const bool fp8 = kvd->kv_dtype == SPEC_KV_FP8_E4M3;
@@ -1156,16 +1207,19 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     constexpr int CT = spec::CMB_WARPS * 32;
     switch (kvd->head_dim) {
         case 64:
-            spec::attn_combine_kernel<64><<<cblocks, CT, 0, s>>>(p.ws_ml, p.ws_o, B, k, n_q_heads, G,
-                                                                  kvd->n_kv_heads, p.n_splits, (uint16_t *)out);
+            spec::attn_combine_kernel<64><<<cblocks, CT, 0, s>>>(p.ws_ml, p.ws_o, pos, B, k, n_q_heads, G,
+                                                                  kvd->n_kv_heads, p.n_splits, p.split_keys, max_pos,
+                                                                  (uint16_t *)out);
             break;
         case 128:
-            spec::attn_combine_kernel<128><<<cblocks, CT, 0, s>>>(p.ws_ml, p.ws_o, B, k, n_q_heads, G,
-                                                                   kvd->n_kv_heads, p.n_splits, (uint16_t *)out);
+            spec::attn_combine_kernel<128><<<cblocks, CT, 0, s>>>(p.ws_ml, p.ws_o, pos, B, k, n_q_heads, G,
+                                                                   kvd->n_kv_heads, p.n_splits, p.split_keys, max_pos,
+                                                                  (uint16_t *)out);
             break;
         default:
-            spec::attn_combine_kernel<256><<<cblocks, CT, 0, s>>>(p.ws_ml, p.ws_o, B, k, n_q_heads, G,
-                                                                   kvd->n_kv_heads, p.n_splits, (uint16_t *)out);
+            spec::attn_combine_kernel<256><<<cblocks, CT, 0, s>>>(p.ws_ml, p.ws_o, pos, B, k, n_q_heads, G,
+                                                                   kvd->n_kv_heads, p.n_splits, p.split_keys, max_pos,
+                                                                  (uint16_t *)out);
             break;
     }
     return spec::launch_status();

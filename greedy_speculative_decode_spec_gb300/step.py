@@ -68,7 +68,7 @@ class VerifyStep:
         d = kv.head_dim
         self.scale = 1.0 / (d ** 0.5)
         i32 = dict(dtype=torch.int32, device=device)
-        self.attn_ws = torch.empty(max(bnd.spec_verify_attn_workspace(kv.desc, B, k, n_q_heads, max_pos), 256),
+        self.attn_ws = torch.zeros(max(bnd.spec_verify_attn_workspace(kv.desc, B, k, n_q_heads, max_pos), 256),
                                    dtype=torch.uint8, device=device)
         self.head_ws = torch.zeros(bnd.spec_lmhead_workspace(R, self.V, self.H), dtype=torch.uint8, device=device)
         self.out = StepOutputs(

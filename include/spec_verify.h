@@ -153,7 +153,10 @@ int spec_kv_write_rows(const spec_kv_desc *kv, const int32_t *row_branch,
  *   max_pos host bound: pos[b]+k+1 <= max_pos for every b (sizes the grid and
  *           the workspace; rows beyond it are a device error SPEC_DEVERR_POS).
  *   ws      device workspace of spec_verify_attn_workspace(...) bytes, 256-byte
- *           aligned, contents need not be initialised.
+ *           aligned. Its first 256 bytes (the work-unit scheduler's counters) must be
+ *           ZERO before the first call; every call leaves them zero again, so a
+ *           workspace is zeroed once, not per call. The rest needs no initialisation.
+ *           Calls sharing a workspace must not overlap in time.
  * Host errors: NULL, B < 1, k out of range, n_q_heads % n_kv_heads != 0,
  * head_dim not 64/128/256, max_pos < k+1, workspace too small; SPEC_ERR_UNSUPPORTED
  * when (k+1)*G, the query vectors sharing one kv head, exceeds 64.

@@ -77,7 +77,7 @@ def lm_ws(M, V, H):
 
 
 def attn_ws(kv: PagedKv, B, k, Hq, max_pos):
-    return torch.empty(max(bnd.spec_verify_attn_workspace(kv.desc, B, k, Hq, max_pos), 256), dtype=torch.uint8,
+    return torch.zeros(max(bnd.spec_verify_attn_workspace(kv.desc, B, k, Hq, max_pos), 256), dtype=torch.uint8,
                        device=DEV)
 
 

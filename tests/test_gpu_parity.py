@@ -198,7 +198,7 @@ def test_bad_page_id_is_reported_not_trapped():
     assert torch.equal(gkv.k.view(torch.int16), before.view(torch.int16))   # skipped, nothing written
     err.zero_()
     out = torch.zeros((c.R, c.Hq, c.d), dtype=torch.bfloat16, device=DEV)
-    ws = torch.empty(bnd.spec_verify_attn_workspace(desc, c.B, c.k, c.Hq, vi.max_pos), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(bnd.spec_verify_attn_workspace(desc, c.B, c.k, c.Hq, vi.max_pos), dtype=torch.uint8, device=DEV)
     bnd.spec_verify_attn(desc, pos_d, c.B, c.k, c.Hq, vi.q.cuda(), 0.125, out, ws, vi.max_pos, err)
     torch.cuda.synchronize()
     assert int(err.item()) & bnd.DEVERR_PAGE
@@ -228,7 +228,7 @@ def test_position_past_page_table_coverage_is_reported():
     assert torch.equal(gkv.k.view(torch.int16), before.view(torch.int16))   # skipped, nothing written
     err.zero_()
     out = torch.zeros((c.R, c.Hq, c.d), dtype=torch.bfloat16, device=DEV)
-    ws = torch.empty(bnd.spec_verify_attn_workspace(desc, c.B, c.k, c.Hq, vi.max_pos), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(bnd.spec_verify_attn_workspace(desc, c.B, c.k, c.Hq, vi.max_pos), dtype=torch.uint8, device=DEV)
     bnd.spec_verify_attn(desc, pos_d, c.B, c.k, c.Hq, vi.q.cuda(), 0.125, out, ws, vi.max_pos, err)
     torch.cuda.synchronize()
     assert int(err.item()) & bnd.DEVERR_COVER

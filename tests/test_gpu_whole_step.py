@@ -48,7 +48,7 @@ class GpuSide:
         pos_d = torch.tensor([pos], dtype=torch.int32, device=DEV)
         bnd.spec_kv_append(self.kv.desc, pos_d, 1, k, kn, vn, self.err)
         out = torch.empty((k + 1, lm.Hq, lm.d), dtype=torch.bfloat16, device=DEV)
-        ws = torch.empty(bnd.spec_verify_attn_workspace(self.kv.desc, 1, k, lm.Hq, self.max_len), dtype=torch.uint8,
+        ws = torch.zeros(bnd.spec_verify_attn_workspace(self.kv.desc, 1, k, lm.Hq, self.max_len), dtype=torch.uint8,
                          device=DEV)
         bnd.spec_verify_attn(self.kv.desc, pos_d, 1, k, lm.Hq, q, 1 / math.sqrt(lm.d), out, ws, self.max_len, self.err)
         o = out.cpu()
