@@ -20,18 +20,20 @@
 // own thread) only on such a move; the final O / l does not depend on which m was used.
 //
 // A persistent CTA per SM walks its units with warp-specialised roles:
-//   warp 0     per unit: the page-table entries (and FP8 scales) into a shared table, and
-//              Q by one 3-D TMA box per 64-column block (double-buffered);
-//   warp 1     issues the MMAs: S of tile t+1 before P.V of tile t when the operand ring
-//              can hold both, so the softmax of one tile overlaps the MMAs of the next;
+//   warps 0-3  gather K and V rows with 16-byte cp.async copies into the swizzled operand
+//              ring (bf16), one warp per SM sub-partition (cp.async issue is throughput-
+//              bound per sub-partition); for FP8 pools warps 0, 1 gather E4M3 rows into a raw
+//              ring and warps 2, 3 convert them to f16 exactly (and Q bf16 -> f16 in place);
 //   warps 4, 5, 8, 9  softmax: the threads of TMEM lane q own query q (lane quadrants 0 and 1
 //              hold the n_q <= 64 queries), two warps per quadrant, one per half of the key
 //              columns; a quadrant without queries has nothing to do;
-//   warps 2, 3, 6, 7  gather K and V rows with 16-byte cp.async copies into the swizzled operand
-//              ring (bf16); for FP8 pools warps 2, 3 gather E4M3 rows into a raw ring and
-//              warps 6, 7 convert them to f16 exactly (and Q bf16 -> f16 in place). The page scales are
-//              applied by the softmax: K's to the scores, V's to P (the row sum stays
-//              unscaled), so S and O come out in the pool's true units.
+//   warp 6     per unit: takes the next work unit, fills the page-table entries (and FP8
+//              scales) into a shared table, and loads Q by one 3-D TMA box per 64-column
+//              block (double-buffered);
+//   warp 7     issues the MMAs: S of tile t+1 before P.V of tile t when the operand ring
+//              can hold both, so the softmax of one tile overlaps the MMAs of the next.
+// The page scales of FP8 pools are applied by the softmax: K's to the scores, V's to P (the
+// row sum stays unscaled), so S and O come out in the pool's true units.
 // Keys beyond a row's position get P = 0 by select, never by multiplication, and V rows
 // past the branch's last position are zeroed before P.V, so NaN in unused pool slots
 // cannot reach a result. Tile and split boundaries sit at fixed key positions and every
@@ -96,6 +98,7 @@ struct AttnTcParams {
     int32_t *err;
     int NS, NR;            // operand / raw ring depth (sub-tiles)
     int OB;                // O buffers in TMEM (1 or 2)
+    int QB;                // Q buffers in shared memory (1 or 2)
     int lookahead;         // issue S of tile t+1 before P.V of tile t
     uint32_t off_q, off_p, off_op, off_raw, off_ut, off_bar, off_small;  // shared-memory offsets
 };
@@ -231,11 +234,11 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == 6 && lane == 0) {
         prefetch_tmap(&map_q0);
         if (p.split) prefetch_tmap(&map_q1);
     }
-    if (warp == 1) {
+    if (warp == 7) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     const uint32_t t_s = tmem;        // S buffers: columns [0, 128) and [128, 256)
     const uint32_t t_o = tmem + 256;  // O buffers: D columns each
 
-    if (warp == 0) {
+    if (warp == 6) {
         // ================= producer: per unit, the page table entries and Q =================
         // Units are handed out dynamically: the producer takes the next index of the
         // split-major walk from a global counter, skips empty units, and publishes the unit
@@ -313,16 +316,17 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(ufull + 8 * ub);
             // ---- Q of (b, g): one 3-D box per 64-column block lands as rows j*G + i ----
-            if (!warp_wait(qfree + 8 * ub, uph ^ 1u, abort_flag)) { ok = false; break; }
+            const uint32_t qs = p.QB == 2 ? ub : 0u, qph = p.QB == 2 ? uph : (ua & 1u);  // Q buffer, phase
+            if (!warp_wait(qfree + 8 * qs, qph ^ 1u, abort_flag)) { ok = false; break; }
             if (lane == 0) {
-                mbar_arrive_expect_tx(qfull + 8 * ub, (uint32_t)(S_::NATOM * n_q * 128));
+                mbar_arrive_expect_tx(qfull + 8 * qs, (uint32_t)(S_::NATOM * n_q * 128));
 #pragma unroll
                 for (int a = 0; a < S_::NATOM; ++a) {
-                    tma_load_3d(s_q + ub * QBUF + a * QATOM, &map_q0, a * 64, ui.g * p.G, ui.b * (p.k + 1),
-                                qfull + 8 * ub);
+                    tma_load_3d(s_q + qs * QBUF + a * QATOM, &map_q0, a * 64, ui.g * p.G, ui.b * (p.k + 1),
+                                qfull + 8 * qs);
                     if (p.split)
-                        tma_load_3d(s_q + ub * QBUF + a * QATOM + 32 * 128, &map_q1, a * 64, ui.g * p.G,
-                                    ui.b * (p.k + 1) + p.J1, qfull + 8 * ub);
+                        tma_load_3d(s_q + qs * QBUF + a * QATOM + 32 * 128, &map_q1, a * 64, ui.g * p.G,
+                                    ui.b * (p.k + 1) + p.J1, qfull + 8 * qs);
                 }
             }
             __syncwarp();
@@ -342,13 +346,14 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         }
         // the Q copies still in flight land before the CTA may exit
         if (lane == 0) {
-            for (uint32_t j = 0; j < 2 && j < ua; ++j) {
+            for (uint32_t j = 0; j < (uint32_t)p.QB && j < ua; ++j) {
                 const uint32_t i2 = ua - 1 - j;
-                mbar_wait(qfull + 8 * (i2 & 1u), (i2 >> 1) & 1u, nullptr, ATT_WAIT_NS);
+                mbar_wait(qfull + 8 * (p.QB == 2 ? (i2 & 1u) : 0u), p.QB == 2 ? (i2 >> 1) & 1u : i2 & 1u, nullptr,
+                          ATT_WAIT_NS);
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 7) {
         // ================= MMA issuer =================
         const uint32_t idesc_s = idesc_f16kind(128, TILE_KEYS, FP8, false, false);
         const uint32_t idesc_pv = idesc_f16kind(128, S_::SUB_COLS, FP8, false, true);
@@ -433,19 +438,20 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             const UnitInfo ui = unit_info(p, it_u, u);
             const uint32_t ob = p.OB == 2 ? (ua & 1u) : 0u;
             const uint32_t ob_use = p.OB == 2 ? (ua >> 1) : ua;
-            if (!warp_wait((FP8 ? qconv : qfull) + 8 * ub, uph, abort_flag) ||
+            const uint32_t qs = p.QB == 2 ? ub : 0u, qph = p.QB == 2 ? uph : (ua & 1u);  // Q buffer, phase
+            if (!warp_wait((FP8 ? qconv : qfull) + 8 * qs, qph, abort_flag) ||
                 !warp_wait(ofree + 8 * ob, (ob_use & 1u) ^ 1u, abort_flag)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint32_t q_addr = s_q + ub * QBUF;
+            const uint32_t q_addr = s_q + qs * QBUF;
             for (int t = 0; t < ui.T && ok; ++t) {
                 ok = issue_s(t, q_addr);
                 if (!ok) break;
                 if (t == ui.T - 1) {
                     // the unit's last S: its Q buffer is free once these MMAs complete
-                    if (lane == 0) mma_commit(qfree + 8 * ub);
+                    if (lane == 0) mma_commit(qfree + 8 * qs);
                     __syncwarp();
                 }
                 if (p.lookahead) {
@@ -478,9 +484,10 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                 const uint32_t t2 = gp - 1 - j;
                 mbar_wait(pfree + 8 * (t2 & 1u), (t2 >> 1) & 1u, nullptr, ATT_WAIT_NS);
             }
-            for (uint32_t j = 0; j < 2 && j < ua; ++j) {
+            for (uint32_t j = 0; j < (uint32_t)p.QB && j < ua; ++j) {
                 const uint32_t i2 = ua - 1 - j;
-                mbar_wait(qfree + 8 * (i2 & 1u), (i2 >> 1) & 1u, nullptr, ATT_WAIT_NS);
+                mbar_wait(qfree + 8 * (p.QB == 2 ? (i2 & 1u) : 0u), p.QB == 2 ? (i2 >> 1) & 1u : i2 & 1u, nullptr,
+                          ATT_WAIT_NS);
             }
             if (gp > 0) mbar_wait(odone, (gp - 1) & 1u, nullptr, ATT_WAIT_NS);
         }
@@ -738,8 +745,8 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             *abort_flag = 1;
             if (lrow == 0 && hf == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
-    } else if (!FP8 || warp == 2 || warp == 3) {
-        // ================= loaders: K / V gather (bf16: warps 2, 3, 6, 7; FP8: warps 2, 3) =================
+    } else if (!FP8 || warp < 2) {
+        // ================= loaders: K / V gather (bf16: warps 0..3; FP8: warps 0, 1) =================
         // Each thread copies its own 16-byte pieces of every sub-tile with cp.async and lets the
         // copies arrive on the stage's barrier by themselves when they land
         // (cp.async.mbarrier.arrive.noinc), so a sub-tile is visible to its consumer as soon as
@@ -748,7 +755,7 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         // wait); E4M3 rows go to the raw ring, which the converter warps turn into operand
         // stages. A loader waits only for a free stage.
         constexpr int NT = FP8 ? 64 : 128;           // loader threads
-        const int ltid = ((warp & 1) | ((warp >> 1) & 2)) * 32 + lane;  // warps 2, 3, 6, 7 -> 0..127
+        const int ltid = warp * 32 + lane;  // warps 0..3 (one per SM sub-partition)
         constexpr int ESZ = FP8 ? 1 : 2;
         constexpr int CH = S_::SUB_COLS * ESZ / 16;  // 16-byte pieces per row of a sub-tile
         constexpr int RPS = NT / CH;                 // rows per step of the loader threads
@@ -836,10 +843,10 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             if (ltid == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
     } else {
-        // ================= FP8 converters, warps 6, 7: E4M3 -> f16 operand stages =================
+        // ================= FP8 converters, warps 2, 3: E4M3 -> f16 operand stages =================
         // E4M3 is exact in f16 (the page scales are applied by the softmax). Per unit the bf16
         // Q is first converted to f16 in place, then every landed raw sub-tile in ring order.
-        const int ctid = (warp - 6) * 32 + lane;  // 0..63
+        const int ctid = (warp - 2) * 32 + lane;  // 0..63
         constexpr int CCH = S_::SUB_COLS / 16;     // 16-byte raw pieces per row
         constexpr int NPC = TILE_KEYS * CCH / 64;  // pieces per converter thread per sub-tile
         uint32_t gc = 0, ua = 0;                   // sub-tiles converted, active units
@@ -852,8 +859,9 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             int u;
             const UnitInfo ui = unit_info(p, it_u, u);
             // ---- Q arrives as bf16; the f16-kind MMA needs f16 on both sides ----
-            if (!warp_wait(qfull + 8 * ub, uph, abort_flag)) { ok = false; break; }
-            uint8_t *qb = smem + p.off_q + ub * QBUF;
+            const uint32_t qs = p.QB == 2 ? ub : 0u, qph = p.QB == 2 ? uph : (ua & 1u);  // Q buffer, phase
+            if (!warp_wait(qfull + 8 * qs, qph, abort_flag)) { ok = false; break; }
+            uint8_t *qb = smem + p.off_q + qs * QBUF;
             for (int i = ctid; i < S_::NATOM * R_pad * 8; i += 64) {
                 const int a = i / (R_pad * 8), rem = i % (R_pad * 8);
                 uint4 *ptr = reinterpret_cast<uint4 *>(qb + a * QATOM + rem * 16);
@@ -866,7 +874,7 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(qconv + 8 * ub);
+            if (lane == 0) mbar_arrive(qconv + 8 * qs);
             ++ua;
             // ---- the unit's K / V sub-tiles ----
             const uint32_t n_sub = (uint32_t)(2 * S_::NSUB * ui.T);
@@ -914,7 +922,7 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     // ================= teardown =================
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 7) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -1067,13 +1075,14 @@ static bool make_q_map(CUtensorMap *map, const void *q, int R, int Hq, int d, in
 // The M = 128 MMAs read up to (128 - R_pad) rows past the last Q / P block; the operand
 // ring that follows is always larger than that.
 template <int D, bool FP8>
-static int plan_attn(AttnTcParams &p, size_t *smem_bytes) {
+static int plan_rings(AttnTcParams &p, int QB, uint32_t *fixed_out) {
     using S_ = AttnShape<D, FP8>;
-    const uint32_t q_bytes = 2 * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.R_pad * 128;
+    const uint32_t q_bytes = QB * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.R_pad * 128;
     const uint32_t ut_bytes = 2 * (uint32_t)sizeof(UnitTable);
     const uint32_t bars = 8 * 64, small = 64 + 2048;
     const uint32_t fixed = 1024 + q_bytes + p_bytes + ut_bytes + bars + small;
     const uint32_t raw_row = FP8 ? S_::RAW_STAGE : 0;
+    *fixed_out = fixed;
     if (ATT_SMEM_LIMIT < fixed + 2 * S_::OP_STAGE + 2 * raw_row) return SPEC_ERR_UNSUPPORTED;
     const uint32_t avail = ATT_SMEM_LIMIT - fixed;
     if (!FP8) {
@@ -1091,9 +1100,34 @@ static int plan_attn(AttnTcParams &p, size_t *smem_bytes) {
         p.NR = p.NR > 8 ? 8 : p.NR;
         if (p.NR < 2) return SPEC_ERR_UNSUPPORTED;
     }
+    p.QB = QB;
+    return SPEC_OK;
+}
+
+// Shared-memory plan, in this order (every block 1024-aligned): the Q buffer(s), 2 P
+// buffers, the operand ring, the raw ring (FP8), 2 unit tables, barriers, flags. The M =
+// 128 MMAs read up to (128 - R_pad) rows past the last Q / P block; the operand ring that
+// follows is always larger than that. Two Q buffers let a unit's Q load during the previous
+// unit; one is used instead when that buys a deeper ring (the bytes in flight per SM).
+template <int D, bool FP8>
+static int plan_attn(AttnTcParams &p, size_t *smem_bytes) {
+    using S_ = AttnShape<D, FP8>;
+    uint32_t fixed = 0;
+    AttnTcParams p1 = p;
+    const int st2 = plan_rings<D, FP8>(p, 2, &fixed);
+    uint32_t fixed1 = 0;
+    const int st1 = plan_rings<D, FP8>(p1, 1, &fixed1);
+    if (st2 && st1) return st2;
+    if (st2 || (FP8 ? p1.NR > p.NR : p1.NS > p.NS)) {
+        p = p1;
+        fixed = fixed1;
+    }
     // S of tile t+1 ahead of P.V of tile t needs the ring to hold V_t and K_{t+1} at once
     p.lookahead = p.NS >= 2 * S_::NSUB ? 1 : 0;
     p.OB = 256 + 2 * D <= 512 ? 2 : 1;
+    const uint32_t q_bytes = p.QB * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.R_pad * 128;
+    const uint32_t ut_bytes = 2 * (uint32_t)sizeof(UnitTable);
+    const uint32_t bars = 8 * 64, small = 64 + 2048;
     p.off_q = 0;
     p.off_p = p.off_q + q_bytes;
     p.off_op = p.off_p + p_bytes;
@@ -1161,10 +1195,11 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     const int n_q = (k + 1) * G;
     const int N_pad = ((n_q + 15) / 16) * 16;
     if (N_pad > spec::MAX_NPAD) return SPEC_ERR_UNSUPPORTED;
-    // spread the queries over two TMEM lane quadrants (two softmax warps) when both halves
-    // of the draft rows fit in 32 lanes each
+    // more than 32 query vectors need two TMEM lane quadrants: the draft rows are then split
+    // in two halves of at most 32 lanes each when they fit (otherwise the vectors run
+    // contiguously over both quadrants)
     const int J1 = (k + 2) / 2;
-    const bool split = k >= 1 && J1 * G <= 32 && (k + 1 - J1) * G <= 32;
+    const bool split = n_q > 32 && k >= 1 && J1 * G <= 32 && (k + 1 - J1) * G <= 32;
     const int R_pad = split ? 32 + (((k + 1 - J1) * G + 15) / 16) * 16 : N_pad;
     if (R_pad > spec::MAX_RPAD) return SPEC_ERR_UNSUPPORTED;
     spec::AttnTcParams p{};
