@@ -13,8 +13,9 @@
 // query i on lane i); the keys of a 128-key tile are the columns:
 //     S[q][key]  = Q . K_tile^T                 (tcgen05, fp32 in TMEM, double-buffered)
 //     O[q][d]   += P[q][key] . V_tile[key][d]   (tcgen05, fp32 in TMEM)
-// so every softmax quantity of a query (its running maximum and sum) lives in the lane's
-// threads: no cross-lane reductions. One pass per tile with a lazily raised maximum: a row's
+// so every softmax quantity of a query (its running maximum and sum) lives in the lanes'
+// threads: no cross-lane reductions, only an exchange of partial maxima between the warps
+// that hold copies of the same queries. One pass per tile with a lazily raised maximum: a row's
 // running maximum m only moves when a tile's maximum exceeds it by more than RESCALE_TAU
 // (log2 units), so P = 2^(s - m) <= 2^RESCALE_TAU and O is rescaled (in TMEM, by the row's
 // own thread) only on such a move; the final O / l does not depend on which m was used.
@@ -24,14 +25,18 @@
 //              ring (bf16), one warp per SM sub-partition (cp.async issue is throughput-
 //              bound per sub-partition); for FP8 pools warps 0, 1 gather E4M3 rows into a raw
 //              ring and warps 2, 3 convert them to f16 exactly (and Q bf16 -> f16 in place);
-//   warps 4, 5, 8, 9  softmax: the threads of TMEM lane q own query q (lane quadrants 0 and 1
-//              hold the n_q <= 64 queries), two warps per quadrant, one per half of the key
-//              columns; a quadrant without queries has nothing to do;
-//   warp 6     per unit: takes the next work unit, fills the page-table entries (and FP8
-//              scales) into a shared table, and loads Q by one 3-D TMA box per 64-column
-//              block (double-buffered);
-//   warp 7     issues the MMAs: S of tile t+1 before P.V of tile t when the operand ring
-//              can hold both, so the softmax of one tile overlaps the MMAs of the next.
+//   warps 4-7  softmax, one per TMEM lane quadrant (a warp reaches only the lanes of its
+//              own quadrant, and quadrant w % 4 is also SM sub-partition w % 4): Q is loaded
+//              in copies, four when the n_q queries fit one quadrant and two when they span
+//              two, so that every quadrant holds the queries and the S MMA computes each
+//              copy's scores at no extra cost (M = 128 either way); each warp takes its
+//              copy's share of the tile's key columns;
+//   warp 8     per unit: takes the next work unit, fills the page-table entries (and FP8
+//              scales) into a shared table, and loads the Q copies by 3-D TMA boxes;
+//   warp 9     issues S = Q . K^T of each tile as soon as its keys and an S buffer are there
+//              (TMEM allocation is also this warp's);
+//   warp 10    issues O += P . V of each tile as soon as its P is there, so the softmax of
+//              one tile overlaps the MMAs of its neighbours.
 // The page scales of FP8 pools are applied by the softmax: K's to the scores, V's to P (the
 // row sum stays unscaled), so S and O come out in the pool's true units.
 // Keys beyond a row's position get P = 0 by select, never by multiplication, and V rows
@@ -61,7 +66,7 @@ constexpr float RESCALE_TAU = 8.0f;   // P <= 2^8: exact range for bf16 and f16 
 constexpr uint64_t ATT_WAIT_NS = 1000000000ull;
 constexpr int ATT_SMEM_LIMIT = 227 * 1024;
 constexpr int MAX_NPAD = 64;          // query vectors per (branch, kv head), padded to 16
-constexpr int MAX_RPAD = 64;          // TMEM lanes holding them (two blocks of <= 32 when split)
+constexpr int MAX_RPAD = 128;         // TMEM lanes holding the copies of the query layout
 
 // Per-unit table the producer warp fills: the page of each page-sized run of the split's
 // keys (-1 if the table entry is invalid), the page's FP8 K / V scales, and the error
@@ -88,8 +93,12 @@ struct AttnTcParams {
     const int32_t *pos;
     int B, k, Hq, G, n_q, n_splits, max_pos, n_units, split_keys;
     // query layout on the TMEM lanes: draft rows j < J1 on lanes [0, J1*G), the rest (if
-    // split) on lanes [32, 32 + (k+1-J1)*G); R_pad = lanes in use, padded to 16
+    // split) on lanes [32, 32 + (k+1-J1)*G); R_pad = rows of a Q buffer (all copies)
     int J1, split, R_pad;
+    // copies of the query layout on the TMEM lanes (copy c starts at lane 32*qpc*c), so that
+    // every lane quadrant, and with it every SM sub-partition, holds the queries; PR = rows
+    // of P (copy 0's layout, padded to 16)
+    int copies, qpc, PR;
     const uint16_t *q;     // bf16 [R][Hq][d]
     float scale_log2;      // softmax scale * log2(e)
     unsigned int *sched;   // [2]: next unit to hand out, CTAs done (zero between calls)
@@ -99,7 +108,6 @@ struct AttnTcParams {
     int NS, NR;            // operand / raw ring depth (sub-tiles)
     int OB;                // O buffers in TMEM (1 or 2)
     int QB;                // Q buffers in shared memory (1 or 2)
-    int lookahead;         // issue S of tile t+1 before P.V of tile t
     uint32_t off_q, off_p, off_op, off_raw, off_ut, off_bar, off_small;  // shared-memory offsets
 };
 
@@ -114,7 +122,7 @@ struct AttnShape {
     static constexpr int NATOM_SUB = SUB_COLS / 64;        // column blocks per sub-tile
     static constexpr uint32_t OP_STAGE = NATOM_SUB * TILE_KEYS * 128;
     static constexpr uint32_t RAW_STAGE = FP8 ? TILE_KEYS * SUB_COLS : 0;
-    static constexpr int THREADS = 320;
+    static constexpr int THREADS = 352;
 };
 
 struct UnitInfo {
@@ -174,11 +182,11 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_u32(smem);
     const int R_pad = p.R_pad, n_q = p.n_q;
-    // Q and P buffers keep only R_pad rows per 64-column block; the M = 128 MMAs also read
-    // rows R_pad..127, which fall on the following memory: those rows only feed TMEM lanes
-    // no thread reads.
+    // Q buffers keep R_pad rows and P buffers PR rows per 64-column block; the M = 128 MMAs
+    // also read the rows after those, which fall on the following memory: those rows only
+    // feed TMEM lanes no thread reads.
     const uint32_t QATOM = (uint32_t)R_pad * 128, QBUF = S_::NATOM * QATOM;
-    const uint32_t PATOM = (uint32_t)R_pad * 128, PBUF = 2 * PATOM;
+    const uint32_t PATOM = (uint32_t)p.PR * 128, PBUF = 2 * PATOM;
     const uint32_t s_q = s_base + p.off_q, s_p = s_base + p.off_p, s_op = s_base + p.off_op;
     const uint32_t s_raw = s_base + p.off_raw;
     uint8_t *g_p = smem + p.off_p;
@@ -191,15 +199,16 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     const uint32_t odone = pfree + 16, ofree = odone + 8;             // P.V completions, O buffers
     const uint32_t qfull = ofree + 16, qconv = qfull + 16, qfree = qconv + 16;  // Q double buffer
     const uint32_t ufull = qfree + 16, ufree = ufull + 16;                      // unit tables
-    const uint32_t drain = ufree + 16;
-    // softmax half-warps' exchanges, per lane quadrant and buffer: row maxima, row sums
-    const uint32_t xfull = drain + 8, lfull = xfull + 32;
+    const uint32_t drain = ufree + 16;  // one per MMA issuer
+    // softmax warps' exchanges, per lane quadrant and buffer: row maxima, row sums
+    const uint32_t xfull = drain + 16, lfull = xfull + 32;
+    const uint32_t lfin = lfull + 32;  // the loaders have issued every copy of a unit
     uint8_t *small = smem + p.off_small;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(small + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_act = 2 * (p.split ? 2 : (n_q + 31) >> 5);  // softmax warps that own queries
+    const int n_act = p.copies * p.qpc;  // softmax warps with queries
     const bool small_pages = p.kv.page_size < 8;  // more than UT_ENTRIES pages per split
     const int log2P = p.kv.log2_page;
 
@@ -223,22 +232,23 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             mbar_init(qconv + 8 * a, 2);
             mbar_init(qfree + 8 * a, 1);
             mbar_init(ufull + 8 * a, 1);
-            mbar_init(ufree + 8 * a, n_act + (FP8 ? 2 : 4));  // softmax and loader warps
+            mbar_init(ufree + 8 * a, n_act + (FP8 ? 2 : 4) + 1);  // softmax, loader and P.V warps
+            mbar_init(drain + 8 * a, 1);
+            mbar_init(lfin + 8 * a, FP8 ? 2 : 4);
         }
         mbar_init(odone, 1);
-        mbar_init(drain, 1);
         for (int i = 0; i < 4; ++i) {
-            mbar_init(xfull + 8 * i, 2);
-            mbar_init(lfull + 8 * i, 2);
+            mbar_init(xfull + 8 * i, p.copies);  // the copies of one lane quadrant's queries
+            mbar_init(lfull + 8 * i, p.copies);
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 6 && lane == 0) {
+    if (warp == 8 && lane == 0) {
         prefetch_tmap(&map_q0);
         if (p.split) prefetch_tmap(&map_q1);
     }
-    if (warp == 7) {
+    if (warp == 9) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
@@ -249,14 +259,24 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     const uint32_t t_s = tmem;        // S buffers: columns [0, 128) and [128, 256)
     const uint32_t t_o = tmem + 256;  // O buffers: D columns each
 
-    if (warp == 6) {
+    if (warp == 8) {
         // ================= producer: per unit, the page table entries and Q =================
         // Units are handed out dynamically: the producer takes the next index of the
         // split-major walk from a global counter, skips empty units, and publishes the unit
-        // in the shared table that every other role waits on (-1 ends their loops).
+        // in the shared table that every other role waits on (-1 ends their loops). It takes
+        // a unit only once a table is free and the loaders have issued every copy of the
+        // previous unit, so that a CTA holds little more than the work in its rings and the
+        // last units go to whichever CTAs run out of work first.
         uint32_t ua = 0;
         bool ok = true;
         for (;;) {
+            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+            UnitTable *tab = tables + ub;
+            if (!warp_wait(ufree + 8 * ub, uph ^ 1u, abort_flag)) { ok = false; break; }
+            if (ua > 0 && !warp_wait(lfin + 8 * ((ua - 1) & 1u), ((ua - 1) >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
             int it_u = -1, u = 0;
             UnitInfo ui;
             for (;;) {
@@ -271,9 +291,6 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                 }
                 if (ui.bad_pos && ui.split == 0 && ui.g == 0 && lane == 0) raise_error(p.err, SPEC_DEVERR_POS);
             }
-            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
-            UnitTable *tab = tables + ub;
-            if (!warp_wait(ufree + 8 * ub, uph ^ 1u, abort_flag)) { ok = false; break; }
             if (it_u < 0) {
                 if (lane == 0) tab->iter = -1;
                 __syncwarp();
@@ -319,14 +336,16 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             const uint32_t qs = p.QB == 2 ? ub : 0u, qph = p.QB == 2 ? uph : (ua & 1u);  // Q buffer, phase
             if (!warp_wait(qfree + 8 * qs, qph ^ 1u, abort_flag)) { ok = false; break; }
             if (lane == 0) {
-                mbar_arrive_expect_tx(qfull + 8 * qs, (uint32_t)(S_::NATOM * n_q * 128));
+                mbar_arrive_expect_tx(qfull + 8 * qs, (uint32_t)(p.copies * S_::NATOM * n_q * 128));
+                for (int c = 0; c < p.copies; ++c) {
+                    const uint32_t dst = s_q + qs * QBUF + (uint32_t)(c * p.qpc * 32 * 128);
 #pragma unroll
-                for (int a = 0; a < S_::NATOM; ++a) {
-                    tma_load_3d(s_q + qs * QBUF + a * QATOM, &map_q0, a * 64, ui.g * p.G, ui.b * (p.k + 1),
-                                qfull + 8 * qs);
-                    if (p.split)
-                        tma_load_3d(s_q + qs * QBUF + a * QATOM + 32 * 128, &map_q1, a * 64, ui.g * p.G,
-                                    ui.b * (p.k + 1) + p.J1, qfull + 8 * qs);
+                    for (int a = 0; a < S_::NATOM; ++a) {
+                        tma_load_3d(dst + a * QATOM, &map_q0, a * 64, ui.g * p.G, ui.b * (p.k + 1), qfull + 8 * qs);
+                        if (p.split)
+                            tma_load_3d(dst + a * QATOM + 32 * 128, &map_q1, a * 64, ui.g * p.G,
+                                        ui.b * (p.k + 1) + p.J1, qfull + 8 * qs);
+                    }
                 }
             }
             __syncwarp();
@@ -353,82 +372,17 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 7) {
-        // ================= MMA issuer =================
+    } else if (warp == 9 || warp == 10) {
+        // ================= MMA issuers: warp 9 S = Q . K^T, warp 10 O += P . V =================
+        // Two issuing threads, so that S of a tile goes to the tensor pipe as soon as its keys
+        // and an S buffer are there and P.V as soon as P is: the issue, commit and wait
+        // instructions of both MMA chains take longer than the tensor pipe needs for them.
+        // Each thread's commits track its own MMAs.
+        const bool s_role = warp == 9;
         const uint32_t idesc_s = idesc_f16kind(128, TILE_KEYS, FP8, false, false);
         const uint32_t idesc_pv = idesc_f16kind(128, S_::SUB_COLS, FP8, false, true);
-        uint32_t gs = 0, gp = 0, ua = 0, gbase = 0;  // S, P.V, active units, first sub-tile of the unit
+        uint32_t gt = 0, ua = 0, gbase = 0;  // tiles, active units, first sub-tile of the unit
         bool ok = true;
-        // S(t) = Q . K_t^T into S buffer gs & 1
-        auto issue_s = [&](int t, uint32_t q_addr) -> bool {
-            const uint32_t sb = gs & 1u;
-            if (!warp_wait(sfree + 8 * sb, ((gs >> 1) & 1u) ^ 1u, abort_flag)) return false;
-#pragma unroll
-            for (int h = 0; h < S_::NSUB; ++h) {
-                const uint32_t g = gbase + (uint32_t)(t * 2 * S_::NSUB + h), st = g % p.NS;
-                if (!warp_wait(op_full + 8 * st, (g / p.NS) & 1u, abort_flag)) return false;
-                fence_proxy_async_smem();  // cp.async data -> tensor core reads
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t kb = s_op + st * S_::OP_STAGE;
-#pragma unroll
-                    for (int kl = 0; kl < S_::SUB_COLS / 16; ++kl) {
-                        const int ks = h * (S_::SUB_COLS / 16) + kl;  // k step over all of d
-                        mma_bf16(t_s + sb * TILE_KEYS, desc_kmajor_sw128(q_addr + (ks >> 2) * QATOM + (ks & 3) * 32),
-                                 desc_kmajor_sw128(kb + (kl >> 2) * (TILE_KEYS * 128) + (kl & 3) * 32), idesc_s,
-                                 ks > 0 ? 1u : 0u);
-                    }
-                    mma_commit(op_empty + 8 * st);
-                }
-                __syncwarp();
-            }
-            if (lane == 0) mma_commit(sfull + 8 * sb);
-            __syncwarp();
-            ++gs;
-            return true;
-        };
-        // O += P(t) . V_t
-        auto issue_pv = [&](const UnitInfo &ui, int t, uint32_t ob) -> bool {
-            const uint32_t pb = gp & 1u;
-            if (!warp_wait(pfull + 8 * pb, (gp >> 1) & 1u, abort_flag)) return false;
-            const int nvk = ui.kv_end - (ui.s0 + t * TILE_KEYS);  // valid keys in this tile
-#pragma unroll
-            for (int nb = 0; nb < S_::NSUB; ++nb) {
-                const uint32_t g = gbase + (uint32_t)(t * 2 * S_::NSUB + S_::NSUB + nb), st = g % p.NS;
-                if (!warp_wait(op_full + 8 * st, (g / p.NS) & 1u, abort_flag)) return false;
-                fence_proxy_async_smem();  // cp.async data -> tensor core reads
-                if (nvk < TILE_KEYS) {
-                    // keys past the branch's last position: zero their V rows (NaN-safe P.V)
-                    uint4 *vb = reinterpret_cast<uint4 *>(smem + p.off_op + st * S_::OP_STAGE);
-                    const int rows = TILE_KEYS - nvk;
-                    for (int i = lane; i < rows * S_::NATOM_SUB * 8; i += 32) {
-                        const int a = i / (rows * 8), rem = i % (rows * 8);
-                        const int r = nvk + rem / 8, c = rem % 8;
-                        vb[(a * TILE_KEYS * 128 + r * 128) / 16 + c] = make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                }
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t vb = s_op + st * S_::OP_STAGE, pa = s_p + pb * PBUF;
-#pragma unroll
-                    for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
-                        mma_bf16(t_o + ob * D + nb * 128, desc_kmajor_sw128(pa + (ks >> 2) * PATOM + (ks & 3) * 32),
-                                 desc_mnmajor_sw128(vb + ks * 2048, TILE_KEYS * 128), idesc_pv,
-                                 (t > 0 || ks > 0) ? 1u : 0u);
-                    mma_commit(op_empty + 8 * st);
-                }
-                __syncwarp();
-            }
-            if (lane == 0) {
-                mma_commit(pfree + 8 * pb);
-                mma_commit(odone);
-            }
-            __syncwarp();
-            ++gp;
-            return true;
-        };
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
             if (!warp_wait(ufull + 8 * ub, uph, abort_flag)) { ok = false; break; }
@@ -436,33 +390,95 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             if (it_u < 0) break;
             int u;
             const UnitInfo ui = unit_info(p, it_u, u);
-            const uint32_t ob = p.OB == 2 ? (ua & 1u) : 0u;
-            const uint32_t ob_use = p.OB == 2 ? (ua >> 1) : ua;
-            const uint32_t qs = p.QB == 2 ? ub : 0u, qph = p.QB == 2 ? uph : (ua & 1u);  // Q buffer, phase
-            if (!warp_wait((FP8 ? qconv : qfull) + 8 * qs, qph, abort_flag) ||
-                !warp_wait(ofree + 8 * ob, (ob_use & 1u) ^ 1u, abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t q_addr = s_q + qs * QBUF;
-            for (int t = 0; t < ui.T && ok; ++t) {
-                ok = issue_s(t, q_addr);
-                if (!ok) break;
-                if (t == ui.T - 1) {
-                    // the unit's last S: its Q buffer is free once these MMAs complete
-                    if (lane == 0) mma_commit(qfree + 8 * qs);
+            __syncwarp();
+            if (!s_role && lane == 0) mbar_arrive(ufree + 8 * ub);  // done with the unit table
+            if (s_role) {
+                const uint32_t qs = p.QB == 2 ? ub : 0u, qph = p.QB == 2 ? uph : (ua & 1u);  // Q buffer, phase
+                if (!warp_wait((FP8 ? qconv : qfull) + 8 * qs, qph, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t q_addr = s_q + qs * QBUF;
+                for (int t = 0; t < ui.T; ++t) {
+                    // S(t) = Q . K_t^T into S buffer t & 1 (of the CTA's tile count)
+                    const uint32_t g_t = gt + (uint32_t)t, sb = g_t & 1u;
+                    if (!warp_wait(sfree + 8 * sb, ((g_t >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+#pragma unroll
+                    for (int h = 0; h < S_::NSUB; ++h) {
+                        const uint32_t g = gbase + (uint32_t)(t * 2 * S_::NSUB + h), st = g % p.NS;
+                        if (!warp_wait(op_full + 8 * st, (g / p.NS) & 1u, abort_flag)) { ok = false; break; }
+                        fence_proxy_async_smem();  // cp.async data -> tensor core reads
+                        tc_fence_after();
+                        if (lane == 0) {
+                            const uint32_t kb = s_op + st * S_::OP_STAGE;
+#pragma unroll
+                            for (int kl = 0; kl < S_::SUB_COLS / 16; ++kl) {
+                                const int ks = h * (S_::SUB_COLS / 16) + kl;  // k step over all of d
+                                mma_bf16(t_s + sb * TILE_KEYS,
+                                         desc_kmajor_sw128(q_addr + (ks >> 2) * QATOM + (ks & 3) * 32),
+                                         desc_kmajor_sw128(kb + (kl >> 2) * (TILE_KEYS * 128) + (kl & 3) * 32),
+                                         idesc_s, ks > 0 ? 1u : 0u);
+                            }
+                            mma_commit(op_empty + 8 * st);
+                        }
+                        __syncwarp();
+                    }
+                    if (!ok) break;
+                    if (lane == 0) {
+                        mma_commit(sfull + 8 * sb);
+                        // the unit's last S: its Q buffer is free once these MMAs complete
+                        if (t == ui.T - 1) mma_commit(qfree + 8 * qs);
+                    }
                     __syncwarp();
                 }
-                if (p.lookahead) {
-                    if (t > 0) ok = issue_pv(ui, t - 1, ob);
-                } else {
-                    ok = issue_pv(ui, t, ob);
+            } else {
+                const uint32_t ob = p.OB == 2 ? (ua & 1u) : 0u;
+                const uint32_t ob_use = p.OB == 2 ? (ua >> 1) : ua;
+                if (!warp_wait(ofree + 8 * ob, (ob_use & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                for (int t = 0; t < ui.T; ++t) {
+                    // O += P(t) . V_t
+                    const uint32_t g_t = gt + (uint32_t)t, pb = g_t & 1u;
+                    if (!warp_wait(pfull + 8 * pb, (g_t >> 1) & 1u, abort_flag)) { ok = false; break; }
+                    const int nvk = ui.kv_end - (ui.s0 + t * TILE_KEYS);  // valid keys in this tile
+#pragma unroll
+                    for (int nb = 0; nb < S_::NSUB; ++nb) {
+                        const uint32_t g = gbase + (uint32_t)(t * 2 * S_::NSUB + S_::NSUB + nb), st = g % p.NS;
+                        if (!warp_wait(op_full + 8 * st, (g / p.NS) & 1u, abort_flag)) { ok = false; break; }
+                        fence_proxy_async_smem();  // cp.async data -> tensor core reads
+                        if (nvk < TILE_KEYS) {
+                            // keys past the branch's last position: zero their V rows (NaN-safe P.V)
+                            uint4 *vb = reinterpret_cast<uint4 *>(smem + p.off_op + st * S_::OP_STAGE);
+                            const int rows = TILE_KEYS - nvk;
+                            for (int i = lane; i < rows * S_::NATOM_SUB * 8; i += 32) {
+                                const int a = i / (rows * 8), rem = i % (rows * 8);
+                                const int r = nvk + rem / 8, c = rem % 8;
+                                vb[(a * TILE_KEYS * 128 + r * 128) / 16 + c] = make_uint4(0, 0, 0, 0);
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                        }
+                        tc_fence_after();
+                        if (lane == 0) {
+                            const uint32_t vb = s_op + st * S_::OP_STAGE, pa = s_p + pb * PBUF;
+#pragma unroll
+                            for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
+                                mma_bf16(t_o + ob * D + nb * 128, desc_kmajor_sw128(pa + (ks >> 2) * PATOM + (ks & 3) * 32),
+                                         desc_mnmajor_sw128(vb + ks * 2048, TILE_KEYS * 128), idesc_pv,
+                                         (t > 0 || ks > 0) ? 1u : 0u);
+                            mma_commit(op_empty + 8 * st);
+                        }
+                        __syncwarp();
+                    }
+                    if (!ok) break;
+                    if (lane == 0) {
+                        mma_commit(pfree + 8 * pb);
+                        mma_commit(odone);
+                    }
+                    __syncwarp();
                 }
             }
-            if (ok && p.lookahead) ok = issue_pv(ui, ui.T - 1, ob);
             if (!ok) break;
             gbase += (uint32_t)(2 * S_::NSUB * ui.T);
+            gt += (uint32_t)ui.T;
             ++ua;
         }
         if (!ok) {
@@ -470,18 +486,18 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             if (lane == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
         if (lane == 0) {
-            mma_commit(drain);
-            mbar_wait(drain, 0, nullptr, ATT_WAIT_NS);
-            // every arrive sent by this thread's commits is delivered before the CTA may exit:
-            // the last phase of each operand stage's "empty" barrier, of both P and Q buffers'
-            // "free" barriers and of the P.V completion barrier
+            mma_commit(drain + 8 * (s_role ? 0 : 1));
+            mbar_wait(drain + 8 * (s_role ? 0 : 1), 0, nullptr, ATT_WAIT_NS);
+            // every arrive sent by the commits of either issuer is delivered before the CTA
+            // may exit: the last phase of each operand stage's "empty" barrier, of both P and
+            // Q buffers' "free" barriers and of the P.V completion barrier
             const uint32_t n_last = gbase < (uint32_t)p.NS ? gbase : (uint32_t)p.NS;
             for (uint32_t j = 0; j < n_last; ++j) {
                 const uint32_t i2 = gbase - 1 - j;
                 mbar_wait(op_empty + 8 * (i2 % p.NS), (i2 / p.NS) & 1u, nullptr, ATT_WAIT_NS);
             }
-            for (uint32_t j = 0; j < 2 && j < gp; ++j) {
-                const uint32_t t2 = gp - 1 - j;
+            for (uint32_t j = 0; j < 2 && j < gt; ++j) {
+                const uint32_t t2 = gt - 1 - j;
                 mbar_wait(pfree + 8 * (t2 & 1u), (t2 >> 1) & 1u, nullptr, ATT_WAIT_NS);
             }
             for (uint32_t j = 0; j < (uint32_t)p.QB && j < ua; ++j) {
@@ -489,34 +505,42 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                 mbar_wait(qfree + 8 * (p.QB == 2 ? (i2 & 1u) : 0u), p.QB == 2 ? (i2 >> 1) & 1u : i2 & 1u, nullptr,
                           ATT_WAIT_NS);
             }
-            if (gp > 0) mbar_wait(odone, (gp - 1) & 1u, nullptr, ATT_WAIT_NS);
+            if (gt > 0) mbar_wait(odone, (gt - 1) & 1u, nullptr, ATT_WAIT_NS);
         }
         __syncwarp();
-    } else if (warp == 4 || warp == 5 || warp == 8 || warp == 9) {
-        // ================= softmax: the threads of TMEM lane q own query q =================
-        // Two warps per lane quadrant, one per half of the tile's 128 key columns (and of the
-        // d columns of O). Per tile they exchange only the row's partial maxima; each keeps
-        // its own partial row sum, combined once per unit.
-        const int qd = warp & 3;          // TMEM lane quadrant (0 or 1)
-        const int hf = warp >> 3;         // column half
-        const int lrow = qd * 32 + lane;  // TMEM lane = row of Q, S, P and O
-        int myq;                          // the query this lane holds
+    } else if (warp >= 4 && warp < 8) {
+        // ================= softmax: one warp per TMEM lane quadrant =================
+        // The queries are held in p.copies copies on the TMEM lanes (a copy spans p.qpc lane
+        // quadrants), so that each of the four SM sub-partitions has a warp that can read
+        // their scores. A warp takes the tile's 32-key quarters of its copy (copy c owns
+        // quarters [c*nqw, (c+1)*nqw)); the copies exchange only the row's partial maxima per
+        // tile, and each warp keeps one partial row sum per quarter, added once per unit in a
+        // fixed order. P is written for the rows of copy 0, whose lanes of O the P.V MMA
+        // accumulates; only copy 0's warps rescale and read out O.
+        const int qd = warp & 3;                     // TMEM lane quadrant
+        const int QPC = p.qpc, C = p.copies;         // quadrants per copy, copies
+        const int cpy = qd / QPC, qq = qd % QPC;     // this warp's copy, quadrant within it
+        const int nqw = 4 / C;                       // 32-key quarters per warp (1 or 2)
+        const int kq0 = cpy * nqw;                   // first quarter of this warp
+        const bool owner = cpy == 0;                 // copy 0: the rows of O
+        const bool active = cpy < C;                 // quadrants past the last copy idle
+        const int prow_i = qq * 32 + lane;           // row of P, lane of O (copy 0)
+        int myq;                                     // the query this lane holds
         bool vrow;
         if (p.split) {
-            myq = qd == 0 ? lane : p.J1 * p.G + lane;
-            vrow = lane < (qd == 0 ? p.J1 : p.k + 1 - p.J1) * p.G;
+            myq = qq == 0 ? lane : p.J1 * p.G + lane;
+            vrow = lane < (qq == 0 ? p.J1 : p.k + 1 - p.J1) * p.G;
         } else {
-            myq = lrow;
-            vrow = lrow < n_q;
+            myq = qq * 32 + lane;
+            vrow = myq < n_q;
         }
-        const bool active = p.split || qd * 32 < n_q;
         const int jrow = vrow ? myq / p.G : 0;  // the row's draft index j
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        const uint32_t olane_base = (uint32_t)(qq * 32) << 16;  // copy 0's lanes of O
         const float sl = p.scale_log2;
-        constexpr int HC = TILE_KEYS / 2;  // key columns per warp
-        constexpr int HD = D / 2;          // O columns per warp
-        // row-maximum exchange [2 tiles][2 quadrants][2 halves][32], then row-sum exchange
-        // [2 units][2 quadrants][2 halves][32]
+        constexpr int QC = 32;  // key columns per quarter
+        // row-maximum exchange [2 tiles][qq][copy][32], then row-sum exchange
+        // [2 units][qq][quarter][32]
         float *xch = reinterpret_cast<float *>(small + 64);
         uint32_t gs = 0, gp = 0, ua = 0;
         bool ok = true;
@@ -531,7 +555,8 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             const UnitInfo ui = unit_info(p, it_u, u);
             float *ml = p.ws_ml + (size_t)u * n_q * 2;
             const bool failed = tab->bad != 0;
-            float m = -INFINITY, l = 0.f;  // running maximum (log2 units) and this half's sum
+            float m = -INFINITY;             // running maximum (log2 units)
+            float lq[2] = {0.f, 0.f};        // this warp's partial sums, one per quarter
             // key offsets (from the split's start) this row sees: [0, climit0]; a lane without
             // a query treats every key as seen (its row of P only feeds an unread row of O)
             const int climit0 = vrow ? ui.pos_b + jrow - ui.s0 : (1 << 30);
@@ -540,29 +565,31 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                 if (ok) ok = warp_wait(sfull + 8 * sb, (gs >> 1) & 1u, abort_flag);
                 if (!ok) continue;
                 tc_fence_after();
-                // columns c (of this half) with HC*hf + c <= climit are seen
-                const int climit = climit0 - t * TILE_KEYS - HC * hf;
-                const bool all_seen = __all_sync(0xFFFFFFFFu, climit >= HC - 1);
-                uint32_t sv[HC / 16][16];
+                uint32_t sv[2][2][16];  // [quarter of this warp][16-column block][column]
 #pragma unroll
-                for (int c = 0; c < HC / 16; ++c) tmem_ld16(t_s + lane_base + sb * TILE_KEYS + HC * hf + c * 16, sv[c]);
-                // FP8 pools: the scores come from E4M3 codes and P multiplies E4M3 codes of V.
-                // The half-tile's K scale joins the softmax scale and its V scale multiplies P
-                // (the row sum stays unscaled); with pages shorter than the half-tile the
-                // scales are applied per key.
-                float slk = sl, vmul = 1.f;
-                bool percol = false;
-                if (FP8) {
-                    if (!small_pages && p.kv.page_size >= HC) {
-                        const int e = (t * TILE_KEYS + HC * hf) >> log2P;
-                        slk = sl * tab->ksc[e];
-                        vmul = tab->vsc[e];
-                    } else {
-                        percol = true;
+                for (int i = 0; i < 2; ++i)
+                    if (i < nqw) {
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+                            tmem_ld16(t_s + lane_base + sb * TILE_KEYS + QC * (kq0 + i) + c * 16, sv[i][c]);
                     }
+                // FP8 pools: the scores come from E4M3 codes and P multiplies E4M3 codes of V.
+                // A quarter's K scale joins the softmax scale and its V scale multiplies P (the
+                // row sum stays unscaled); with pages shorter than a quarter the scales are
+                // applied per key.
+                float slk[2] = {sl, sl}, vmul[2] = {1.f, 1.f};
+                const bool percol = FP8 && (small_pages || p.kv.page_size < QC);
+                if (FP8 && !percol) {
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+                        if (i < nqw) {
+                            const int e = (t * TILE_KEYS + QC * (kq0 + i)) >> log2P;
+                            slk[i] = sl * tab->ksc[e];
+                            vmul[i] = tab->vsc[e];
+                        }
                 }
-                auto col_scales = [&](int c, float &ks, float &vs) {
-                    const int key = ui.s0 + t * TILE_KEYS + HC * hf + c;
+                auto col_scales = [&](int qi, int c, float &ks, float &vs) {
+                    const int key = ui.s0 + t * TILE_KEYS + QC * (kq0 + qi) + c;
                     ks = 0.f;
                     vs = 0.f;
                     if (key >= ui.kv_end) return;
@@ -579,44 +606,57 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                     }
                 };
                 tmem_ld_wait();
-                if (FP8 && percol) {
+                if (percol) {
 #pragma unroll
-                    for (int c = 0; c < HC; ++c) {
-                        float ks, vs;
-                        col_scales(c, ks, vs);
-                        sv[c >> 4][c & 15] = __float_as_uint(__uint_as_float(sv[c >> 4][c & 15]) * ks);
-                    }
+                    for (int i = 0; i < 2; ++i)
+                        if (i < nqw) {
+#pragma unroll
+                            for (int c = 0; c < QC; ++c) {
+                                float ks, vs;
+                                col_scales(i, c, ks, vs);
+                                sv[i][c >> 4][c & 15] = __float_as_uint(__uint_as_float(sv[i][c >> 4][c & 15]) * ks);
+                            }
+                        }
                 }
-                // ---- pass 1: partial maximum of s*sl over the seen columns (8 short chains) ----
-                float acc[8];
+                // ---- pass 1: partial maximum of s*slk over the seen columns of each quarter ----
+                float pm = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = -INFINITY;
-                if (slk >= 0.f && all_seen) {
+                for (int i = 0; i < 2; ++i) {
+                    if (i >= nqw) continue;
+                    // columns c (of this quarter) with QC*(kq0+i) + c <= climit are seen
+                    const int climit = climit0 - t * TILE_KEYS - QC * (kq0 + i);
+                    const bool all_seen = __all_sync(0xFFFFFFFFu, climit >= QC - 1);
+                    float acc[8];
 #pragma unroll
-                    for (int c = 0; c < HC; ++c) acc[c & 7] = fmaxf(acc[c & 7], __uint_as_float(sv[c >> 4][c & 15]));
-                } else {
-                    const float sgn = slk >= 0.f ? 1.f : -1.f;
+                    for (int e = 0; e < 8; ++e) acc[e] = -INFINITY;
+                    const float sgn = slk[i] >= 0.f ? 1.f : -1.f;
+                    if (all_seen) {
 #pragma unroll
-                    for (int c = 0; c < HC; ++c)
-                        if (c <= climit) acc[c & 7] = fmaxf(acc[c & 7], sgn * __uint_as_float(sv[c >> 4][c & 15]));
-                    if (slk < 0.f) {
+                        for (int c = 0; c < QC; ++c)
+                            acc[c & 7] = fmaxf(acc[c & 7], sgn * __uint_as_float(sv[i][c >> 4][c & 15]));
+                    } else {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[e] = -acc[e];  // now minima of s: scaled below
+                        for (int c = 0; c < QC; ++c)
+                            if (c <= climit) acc[c & 7] = fmaxf(acc[c & 7], sgn * __uint_as_float(sv[i][c >> 4][c & 15]));
                     }
+                    float q = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
+                                    fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
+                    // q = max of sgn*s: the quarter's maximum of s*slk is q*|slk|
+                    q = (q == -INFINITY || q == INFINITY) ? -INFINITY : q * (sgn * slk[i]);
+                    pm = fmaxf(pm, q);
                 }
-                float pm = slk >= 0.f ? fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
-                                              fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])))
-                                      : fminf(fminf(fminf(acc[0], acc[1]), fminf(acc[2], acc[3])),
-                                              fminf(fminf(acc[4], acc[5]), fminf(acc[6], acc[7])));
-                pm = (pm == -INFINITY || pm == INFINITY) ? -INFINITY : pm * slk;
-                // ---- the row's maximum: exchange with the other half ----
-                float *xt = xch + (sb * 2 + qd) * 64;
-                xt[hf * 32 + lane] = pm;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xfull + 8 * (qd * 2 + sb));
-                ok = warp_wait(xfull + 8 * (qd * 2 + sb), (gs >> 1) & 1u, abort_flag);
-                if (!ok) continue;
-                const float mx = vrow ? fmaxf(pm, xt[(hf ^ 1) * 32 + lane]) : -INFINITY;
+                // ---- the row's maximum: exchange with the other copies ----
+                float mx = pm;
+                if (C > 1) {
+                    float *xt = xch + sb * 128 + qq * C * 32;
+                    xt[cpy * 32 + lane] = pm;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xfull + 8 * (qq * 2 + sb));
+                    ok = warp_wait(xfull + 8 * (qq * 2 + sb), (gs >> 1) & 1u, abort_flag);
+                    if (!ok) continue;
+                    for (int c = 0; c < C; ++c) mx = fmaxf(mx, xt[c * 32 + lane]);
+                }
+                if (!vrow) mx = -INFINITY;
                 // ---- the P buffer is free once P.V of tile t-2 is done ----
                 ok = warp_wait(pfree + 8 * pb, ((gp >> 1) & 1u) ^ 1u, abort_flag);
                 if (!ok) continue;
@@ -624,72 +664,85 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                 const float mnew = (mx > m + RESCALE_TAU) ? mx : m;
                 const bool resc = mnew != m && m != -INFINITY;
                 if (__any_sync(0xFFFFFFFFu, resc)) {
-                    // O is written by P.V of tile t-1 (the one before it is done: see above)
-                    ok = warp_wait(odone, (gp - 1) & 1u, abort_flag);
-                    if (!ok) continue;
-                    tc_fence_after();
                     const float f = resc ? ex2_approx(m - mnew) : 1.f;
-                    l *= f;
-                    const uint32_t orow = t_o + lane_base + ob * D + HD * hf;
+                    lq[0] *= f;
+                    lq[1] *= f;
+                    if (owner) {
+                        // O is written by P.V of tile t-1 (the one before it is done: see above)
+                        ok = warp_wait(odone, (gp - 1) & 1u, abort_flag);
+                        if (!ok) continue;
+                        tc_fence_after();
+                        const uint32_t orow = t_o + olane_base + ob * D;
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t r[2][16];
 #pragma unroll
-                    for (int c0 = 0; c0 < HD; c0 += 32) {
-                        uint32_t r[2][16];
+                            for (int e = 0; e < 2; ++e) tmem_ld16(orow + c0 + 16 * e, r[e]);
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) tmem_ld16(orow + c0 + 16 * e, r[e]);
-                        tmem_ld_wait();
+                            for (int e = 0; e < 2; ++e) {
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) r[e][j] = __float_as_uint(__uint_as_float(r[e][j]) * f);
-                            tmem_st16(orow + c0 + 16 * e, r[e]);
+                                for (int j = 0; j < 16; ++j) r[e][j] = __float_as_uint(__uint_as_float(r[e][j]) * f);
+                                tmem_st16(orow + c0 + 16 * e, r[e]);
+                            }
                         }
+                        tmem_st_wait();
                     }
-                    tmem_st_wait();
                 }
                 m = mnew;
-                // ---- pass 2: P = 2^(s - m) of the row's half: 64-key block hf of P ----
-                float lacc[8];
+                // ---- pass 2: P = 2^(s*slk - m) of this warp's quarters, into copy 0's rows ----
+                uint8_t *prow = g_p + pb * PBUF + prow_i * 128;
+                const int swz = prow_i & 7;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) lacc[e] = 0.f;
-                uint8_t *prow = g_p + pb * PBUF + hf * PATOM + lrow * 128;
-                const int swz = lrow & 7;
+                for (int i = 0; i < 2; ++i) {
+                    if (i >= nqw) continue;
+                    const int kq = kq0 + i;
+                    const int climit = climit0 - t * TILE_KEYS - QC * kq;
+                    const bool all_seen = __all_sync(0xFFFFFFFFu, climit >= QC - 1);
+                    float lacc[8];
 #pragma unroll
-                for (int c0 = 0; c0 < HC; c0 += 16) {
-                    const uint32_t(&r)[16] = sv[c0 >> 4];
-                    uint32_t pk[8];
-                    if (all_seen && !(FP8 && percol)) {
+                    for (int e = 0; e < 8; ++e) lacc[e] = 0.f;
+                    uint8_t *pq = prow + (kq >> 1) * PATOM;
 #pragma unroll
-                        for (int j = 0; j < 16; j += 2) {
-                            const float a = ex2_approx(fmaf(__uint_as_float(r[j]), slk, -m));
-                            const float b = ex2_approx(fmaf(__uint_as_float(r[j + 1]), slk, -m));
-                            lacc[j >> 1] += a + b;
-                            pk[j >> 1] = FP8 ? pack2(a * vmul, b * vmul, true) : pack2(a, b, false);
-                        }
-                    } else {
+                    for (int c0 = 0; c0 < QC; c0 += 16) {
+                        const uint32_t(&r)[16] = sv[i][c0 >> 4];
+                        uint32_t pk[8];
+                        if (all_seen && !percol) {
 #pragma unroll
-                        for (int j = 0; j < 16; j += 2) {
-                            float a = ex2_approx(fmaf(__uint_as_float(r[j]), slk, -m));
-                            float b = ex2_approx(fmaf(__uint_as_float(r[j + 1]), slk, -m));
-                            a = (c0 + j <= climit) ? a : 0.f;
-                            b = (c0 + j + 1 <= climit) ? b : 0.f;
-                            lacc[j >> 1] += a + b;
-                            float va = vmul, vb = vmul;
-                            if (FP8 && percol) {
-                                float ks;
-                                col_scales(c0 + j, ks, va);
-                                col_scales(c0 + j + 1, ks, vb);
+                            for (int j = 0; j < 16; j += 2) {
+                                const float a = ex2_approx(fmaf(__uint_as_float(r[j]), slk[i], -m));
+                                const float b = ex2_approx(fmaf(__uint_as_float(r[j + 1]), slk[i], -m));
+                                lacc[j >> 1] += a + b;
+                                pk[j >> 1] = FP8 ? pack2(a * vmul[i], b * vmul[i], true) : pack2(a, b, false);
                             }
-                            pk[j >> 1] = FP8 ? pack2(a * va, b * vb, true) : pack2(a, b, false);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; j += 2) {
+                                float a = ex2_approx(fmaf(__uint_as_float(r[j]), slk[i], -m));
+                                float b = ex2_approx(fmaf(__uint_as_float(r[j + 1]), slk[i], -m));
+                                a = (c0 + j <= climit) ? a : 0.f;
+                                b = (c0 + j + 1 <= climit) ? b : 0.f;
+                                lacc[j >> 1] += a + b;
+                                float va = vmul[i], vb = vmul[i];
+                                if (percol) {
+                                    float ks;
+                                    col_scales(i, c0 + j, ks, va);
+                                    col_scales(i, c0 + j + 1, ks, vb);
+                                }
+                                pk[j >> 1] = FP8 ? pack2(a * va, b * vb, true) : pack2(a, b, false);
+                            }
+                        }
+                        // 16-byte chunk (within the 128-byte row of the 64-key block) of keys c0..c0+7
+                        const int ch0 = (kq & 1) * 4 + (c0 >> 3);
+                        if (prow_i < p.PR) {
+                            *reinterpret_cast<uint4 *>(pq + (((ch0 ^ swz) & 7) << 4)) =
+                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            *reinterpret_cast<uint4 *>(pq + ((((ch0 + 1) ^ swz) & 7) << 4)) =
+                                make_uint4(pk[4], pk[5], pk[6], pk[7]);
                         }
                     }
-                    if (lrow < R_pad) {
-                        const int ch0 = c0 >> 3;
-                        *reinterpret_cast<uint4 *>(prow + (((ch0 ^ swz) & 7) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        *reinterpret_cast<uint4 *>(prow + ((((ch0 + 1) ^ swz) & 7) << 4)) =
-                            make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                    }
+                    lq[i] += ((lacc[0] + lacc[1]) + (lacc[2] + lacc[3])) + ((lacc[4] + lacc[5]) + (lacc[6] + lacc[7]));
                 }
-                l += ((lacc[0] + lacc[1]) + (lacc[2] + lacc[3])) + ((lacc[4] + lacc[5]) + (lacc[6] + lacc[7]));
                 tc_fence_before();
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -701,49 +754,55 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             // the unit table is no longer read
             __syncwarp();
             if (ok && lane == 0) mbar_arrive(ufree + 8 * ub);
-            // ---- the unit's last P.V (P.V of the tile before it is done first) ----
-            if (ok) ok = warp_wait(pfree + 8 * (gp & 1u), ((gp >> 1) & 1u) ^ 1u, abort_flag);
-            if (ok) ok = warp_wait(odone, (gp - 1) & 1u, abort_flag);
-            if (ok) {
-                tc_fence_after();
-                float *orow_g = p.ws_o + ((size_t)u * n_q + myq) * D + HD * hf;
-                const uint32_t orow = t_o + lane_base + ob * D + HD * hf;
+            // ---- copy 0: the unit's last P.V (P.V of the tile before it is done first) ----
+            if (owner) {
+                if (ok) ok = warp_wait(pfree + 8 * (gp & 1u), ((gp >> 1) & 1u) ^ 1u, abort_flag);
+                if (ok) ok = warp_wait(odone, (gp - 1) & 1u, abort_flag);
+                if (ok) {
+                    tc_fence_after();
+                    float *orow_g = p.ws_o + ((size_t)u * n_q + myq) * D;
+                    const uint32_t orow = t_o + olane_base + ob * D;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t r[2][16];
 #pragma unroll
-                for (int c0 = 0; c0 < HD; c0 += 32) {
-                    uint32_t r[2][16];
+                        for (int e = 0; e < 2; ++e) tmem_ld16(orow + c0 + 16 * e, r[e]);
+                        tmem_ld_wait();
+                        if (vrow) {
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) tmem_ld16(orow + c0 + 16 * e, r[e]);
-                    tmem_ld_wait();
-                    if (vrow) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            reinterpret_cast<float4 *>(orow_g + c0)[e] =
-                                make_float4(__uint_as_float(r[e >> 2][4 * (e & 3)]), __uint_as_float(r[e >> 2][4 * (e & 3) + 1]),
-                                            __uint_as_float(r[e >> 2][4 * (e & 3) + 2]),
-                                            __uint_as_float(r[e >> 2][4 * (e & 3) + 3]));
+                            for (int e = 0; e < 8; ++e)
+                                reinterpret_cast<float4 *>(orow_g + c0)[e] =
+                                    make_float4(__uint_as_float(r[e >> 2][4 * (e & 3)]),
+                                                __uint_as_float(r[e >> 2][4 * (e & 3) + 1]),
+                                                __uint_as_float(r[e >> 2][4 * (e & 3) + 2]),
+                                                __uint_as_float(r[e >> 2][4 * (e & 3) + 3]));
+                        }
                     }
+                    tc_fence_before();
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(ofree + 8 * ob);
             }
-            // ---- the row's sum: the two halves' partial sums ----
-            const uint32_t lb = qd * 2 + (ua & 1u);
-            float *lx = xch + 256 + lb * 64;
-            lx[hf * 32 + lane] = l;
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(ofree + 8 * ob);
+            // ---- the row's sum: the quarters' partial sums, in quarter order ----
+            const uint32_t lb = qq * 2 + (ua & 1u);
+            float *lx = xch + 256 + (ua & 1u) * 256 + qq * 128;
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                if (i < nqw) lx[(kq0 + i) * 32 + lane] = lq[i];
             __syncwarp();
             if (lane == 0) mbar_arrive(lfull + 8 * lb);
             const bool lok = warp_wait(lfull + 8 * lb, (ua >> 1) & 1u, abort_flag);
-            if (hf == 0 && vrow) {
+            if (owner && vrow) {
+                const float l = (lx[lane] + lx[32 + lane]) + (lx[64 + lane] + lx[96 + lane]);
                 ml[2 * myq] = m;
-                ml[2 * myq + 1] = (failed || !ok || !lok) ? -1.f : l + lx[32 + lane];
+                ml[2 * myq + 1] = (failed || !ok || !lok) ? -1.f : l;
             }
             if (!lok) ok = false;
             ++ua;
         }
         if (!ok) {
             *abort_flag = 1;
-            if (lrow == 0 && hf == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
+            if (qd == 0 && lane == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
     } else if (!FP8 || warp < 2) {
         // ================= loaders: K / V gather (bf16: warps 0..3; FP8: warps 0, 1) =================
@@ -834,7 +893,10 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             }
             // the unit's table is no longer read by this warp
             __syncwarp();
-            if (ok && lane == 0) mbar_arrive(ufree + 8 * ub);
+            if (ok && lane == 0) {
+                mbar_arrive(lfin + 8 * ub);
+                mbar_arrive(ufree + 8 * ub);
+            }
         }
         // every copy lands before the CTA may exit
         cp_async_wait_all();
@@ -922,7 +984,7 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     // ================= teardown =================
     tc_fence_before();
     __syncthreads();
-    if (warp == 7) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -1070,19 +1132,18 @@ static bool make_q_map(CUtensorMap *map, const void *q, int R, int Hq, int d, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Shared-memory plan, in this order (every block 1024-aligned): 2 Q buffers, 2 P buffers,
-// the operand ring, the raw ring and its row scales (FP8), 2 unit tables, barriers, flags.
-// The M = 128 MMAs read up to (128 - R_pad) rows past the last Q / P block; the operand
-// ring that follows is always larger than that.
+// Shared-memory plan, in this order (every block 1024-aligned): the Q buffer(s), 2 P
+// buffers, the operand ring, the raw ring (FP8), 2 unit tables, barriers, flags. The M =
+// 128 MMAs read up to (128 - R_pad) rows past the last Q block and (128 - PR) past the last
+// P block; the operand ring that follows is always larger than that.
 template <int D, bool FP8>
-static int plan_rings(AttnTcParams &p, int QB, uint32_t *fixed_out) {
+static int plan_rings(AttnTcParams &p, int QB) {
     using S_ = AttnShape<D, FP8>;
-    const uint32_t q_bytes = QB * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.R_pad * 128;
+    const uint32_t q_bytes = QB * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.PR * 128;
     const uint32_t ut_bytes = 2 * (uint32_t)sizeof(UnitTable);
-    const uint32_t bars = 8 * 64, small = 64 + 2048;
+    const uint32_t bars = 8 * 64, small = 64 + 3072;
     const uint32_t fixed = 1024 + q_bytes + p_bytes + ut_bytes + bars + small;
     const uint32_t raw_row = FP8 ? S_::RAW_STAGE : 0;
-    *fixed_out = fixed;
     if (ATT_SMEM_LIMIT < fixed + 2 * S_::OP_STAGE + 2 * raw_row) return SPEC_ERR_UNSUPPORTED;
     const uint32_t avail = ATT_SMEM_LIMIT - fixed;
     if (!FP8) {
@@ -1104,30 +1165,52 @@ static int plan_rings(AttnTcParams &p, int QB, uint32_t *fixed_out) {
     return SPEC_OK;
 }
 
-// Shared-memory plan, in this order (every block 1024-aligned): the Q buffer(s), 2 P
-// buffers, the operand ring, the raw ring (FP8), 2 unit tables, barriers, flags. The M =
-// 128 MMAs read up to (128 - R_pad) rows past the last Q / P block; the operand ring that
-// follows is always larger than that. Two Q buffers let a unit's Q load during the previous
-// unit; one is used instead when that buys a deeper ring (the bytes in flight per SM).
+// The plan for `copies` copies of the query layout: two Q buffers let a unit's Q load
+// during the previous unit; one is used instead when that buys a deeper ring (the bytes in
+// flight per SM).
+template <int D, bool FP8>
+static int plan_copies(AttnTcParams &p, int copies) {
+    p.copies = copies;
+    p.R_pad = (copies - 1) * p.qpc * 32 + p.PR;
+    if (p.R_pad > MAX_RPAD) return SPEC_ERR_UNSUPPORTED;
+    AttnTcParams p1 = p;
+    const int st2 = plan_rings<D, FP8>(p, 2);
+    const int st1 = plan_rings<D, FP8>(p1, 1);
+    if (st2 && st1) return st2;
+    if (st2 || (FP8 ? p1.NR > p.NR : p1.NS > p.NS)) p = p1;
+    return SPEC_OK;
+}
+
+// Four copies (queries within one lane quadrant) put a softmax warp on every SM
+// sub-partition; two copies are used when four leave the operand ring too shallow to issue
+// S of the next tile ahead of P.V (long head dims), or when the queries span two quadrants.
 template <int D, bool FP8>
 static int plan_attn(AttnTcParams &p, size_t *smem_bytes) {
     using S_ = AttnShape<D, FP8>;
-    uint32_t fixed = 0;
-    AttnTcParams p1 = p;
-    const int st2 = plan_rings<D, FP8>(p, 2, &fixed);
-    uint32_t fixed1 = 0;
-    const int st1 = plan_rings<D, FP8>(p1, 1, &fixed1);
-    if (st2 && st1) return st2;
-    if (st2 || (FP8 ? p1.NR > p.NR : p1.NS > p.NS)) {
-        p = p1;
-        fixed = fixed1;
+    int st = SPEC_ERR_UNSUPPORTED;
+    if (p.qpc == 1) {
+        AttnTcParams p4 = p;
+        st = plan_copies<D, FP8>(p4, 4);
+        if (!st && p4.NS >= 2 * S_::NSUB) {
+            p = p4;
+        } else {
+            AttnTcParams p2 = p;
+            const int st2 = plan_copies<D, FP8>(p2, 2);
+            if (!st2) {
+                p = p2;
+                st = SPEC_OK;
+            } else if (!st) {
+                p = p4;
+            }
+        }
+    } else {
+        st = plan_copies<D, FP8>(p, 2);
     }
-    // S of tile t+1 ahead of P.V of tile t needs the ring to hold V_t and K_{t+1} at once
-    p.lookahead = p.NS >= 2 * S_::NSUB ? 1 : 0;
+    if (st) return st;
     p.OB = 256 + 2 * D <= 512 ? 2 : 1;
-    const uint32_t q_bytes = p.QB * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.R_pad * 128;
+    const uint32_t q_bytes = p.QB * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.PR * 128;
     const uint32_t ut_bytes = 2 * (uint32_t)sizeof(UnitTable);
-    const uint32_t bars = 8 * 64, small = 64 + 2048;
+    const uint32_t bars = 8 * 64, small = 64 + 3072;
     p.off_q = 0;
     p.off_p = p.off_q + q_bytes;
     p.off_op = p.off_p + p_bytes;
@@ -1197,11 +1280,10 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     if (N_pad > spec::MAX_NPAD) return SPEC_ERR_UNSUPPORTED;
     // more than 32 query vectors need two TMEM lane quadrants: the draft rows are then split
     // in two halves of at most 32 lanes each when they fit (otherwise the vectors run
-    // contiguously over both quadrants)
+    // contiguously over both quadrants); PR = the lanes of one copy of that layout
     const int J1 = (k + 2) / 2;
     const bool split = n_q > 32 && k >= 1 && J1 * G <= 32 && (k + 1 - J1) * G <= 32;
-    const int R_pad = split ? 32 + (((k + 1 - J1) * G + 15) / 16) * 16 : N_pad;
-    if (R_pad > spec::MAX_RPAD) return SPEC_ERR_UNSUPPORTED;
+    const int PR = split ? 32 + (((k + 1 - J1) * G + 15) / 16) * 16 : N_pad;
     spec::AttnTcParams p{};
     p.kv = spec::make_view(kvd);
     p.pos = pos;
@@ -1212,7 +1294,8 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     p.n_q = n_q;
     p.J1 = split ? J1 : k + 1;
     p.split = split ? 1 : 0;
-    p.R_pad = R_pad;
+    p.PR = PR;
+    p.qpc = n_q > 32 ? 2 : 1;
     p.split_keys = spec::split_keys_for(kvd->n_kv_heads);
     p.n_splits = (max_pos + p.split_keys - 1) / p.split_keys;
     p.max_pos = max_pos;
