@@ -18,6 +18,28 @@ inline int launch_status() {
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
+// Launches `kernel` so that it may be scheduled while the kernel before it in the stream is
+// still finishing (programmatic dependent launch): the kernel must call grid_dep_wait()
+// before it reads anything an earlier kernel wrote. Falls back to an ordinary launch where
+// the attribute is not available.
+template <typename... KArgs, typename... Args>
+inline int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...) == cudaSuccess) return SPEC_OK;
+    (void)cudaGetLastError();
+    kernel<<<grid, block, smem, s>>>(static_cast<KArgs>(args)...);
+    return launch_status();
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }

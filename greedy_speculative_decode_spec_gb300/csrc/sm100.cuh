@@ -76,6 +76,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// ---- programmatic dependent launch ----------------------------------------------------------
+
+// Waits until the grids this one depends on (launched before it in the stream) have completed
+// and their memory is visible; returns at once for a grid launched without that dependency.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the grid launched after this one in the stream be scheduled before this grid ends (it
+// still waits, in grid_dep_wait, for this grid to complete before it reads its results).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- TMA ---------------------------------------------------------------------------------
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar) {

@@ -255,6 +255,9 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // the set-up above overlaps the end of the previous kernel in the stream; nothing it wrote
+    // (the KV pool, Q, the positions) is read before this point
+    grid_dep_wait();
     const uint32_t tmem = *tmem_slot;
     const uint32_t t_s = tmem;        // S buffers: columns [0, 128) and [128, 256)
     const uint32_t t_o = tmem + 256;  // O buffers: D columns each
@@ -294,7 +297,11 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             if (it_u < 0) {
                 if (lane == 0) tab->iter = -1;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(ufull + 8 * ub);
+                if (lane == 0) {
+                    mbar_arrive(ufull + 8 * ub);
+                    // no new work for this CTA: the combine pass may be scheduled
+                    grid_dep_launch();
+                }
                 break;
             }
             int badbits = 0;
@@ -1009,6 +1016,7 @@ __global__ void __launch_bounds__(CMB_WARPS * 32) attn_combine_kernel(const floa
     __shared__ float part_o[CMB_WARPS][D];
     __shared__ float part_l[CMB_WARPS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    grid_dep_wait();  // the split kernel's partial results
     const int r = blockIdx.x / Hq, h = blockIdx.x % Hq;
     const int b = r / (k + 1), j = r % (k + 1);
     const int g = h / G, hi = h % G;
@@ -1238,8 +1246,7 @@ static int launch_attn_tc(AttnTcParams &p, cudaStream_t s) {
     const int sms = attn_sm_count();
     if (sms < 1) return SPEC_ERR_CUDA;
     const int grid = p.n_units < sms ? p.n_units : sms;
-    attn_tc_kernel<D, FP8><<<grid, S_::THREADS, smem, s>>>(mq0, mq1, p);
-    return launch_status();
+    return launch_pdl(attn_tc_kernel<D, FP8>, dim3(grid), dim3(S_::THREADS), smem, s, mq0, mq1, p);
 }
 
 // workspace: a 256-byte header (the unit scheduler's counters: zero before the first call,
@@ -1323,22 +1330,18 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     const int R = B * (k + 1);
     const int cblocks = R * n_q_heads;
     constexpr int CT = spec::CMB_WARPS * 32;
+    uint16_t *o16 = (uint16_t *)out;
+    const float *wml = p.ws_ml, *wo = p.ws_o;
+    const int Hkv = kvd->n_kv_heads, ns = p.n_splits, sk = p.split_keys;
     switch (kvd->head_dim) {
         case 64:
-            spec::attn_combine_kernel<64><<<cblocks, CT, 0, s>>>(p.ws_ml, p.ws_o, pos, B, k, n_q_heads, G,
-                                                                  kvd->n_kv_heads, p.n_splits, p.split_keys, max_pos,
-                                                                  (uint16_t *)out);
-            break;
+            return spec::launch_pdl(spec::attn_combine_kernel<64>, dim3(cblocks), dim3(CT), 0, s, wml, wo, pos, B, k,
+                                    n_q_heads, G, Hkv, ns, sk, max_pos, o16);
         case 128:
-            spec::attn_combine_kernel<128><<<cblocks, CT, 0, s>>>(p.ws_ml, p.ws_o, pos, B, k, n_q_heads, G,
-                                                                   kvd->n_kv_heads, p.n_splits, p.split_keys, max_pos,
-                                                                  (uint16_t *)out);
-            break;
+            return spec::launch_pdl(spec::attn_combine_kernel<128>, dim3(cblocks), dim3(CT), 0, s, wml, wo, pos, B, k,
+                                    n_q_heads, G, Hkv, ns, sk, max_pos, o16);
         default:
-            spec::attn_combine_kernel<256><<<cblocks, CT, 0, s>>>(p.ws_ml, p.ws_o, pos, B, k, n_q_heads, G,
-                                                                   kvd->n_kv_heads, p.n_splits, p.split_keys, max_pos,
-                                                                  (uint16_t *)out);
-            break;
+            return spec::launch_pdl(spec::attn_combine_kernel<256>, dim3(cblocks), dim3(CT), 0, s, wml, wo, pos, B, k,
+                                    n_q_heads, G, Hkv, ns, sk, max_pos, o16);
     }
-    return spec::launch_status();
 }
