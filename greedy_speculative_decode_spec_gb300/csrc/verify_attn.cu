@@ -24,7 +24,8 @@
 //   warps 0-3  gather K and V rows with 16-byte cp.async copies into the swizzled operand
 //              ring (bf16), one warp per SM sub-partition (cp.async issue is throughput-
 //              bound per sub-partition); for FP8 pools warps 0, 1 gather E4M3 rows into a raw
-//              ring and warps 2, 3 convert them to f16 exactly (and Q bf16 -> f16 in place);
+//              ring (by TMA boxes of one page-run each when pages hold >= 64 positions) and
+//              warps 2, 3 convert them to f16 exactly (and Q bf16 -> f16 in place);
 //   warps 4-7  softmax, one per TMEM lane quadrant (a warp reaches only the lanes of its
 //              own quadrant, and quadrant w % 4 is also SM sub-partition w % 4): Q is loaded
 //              in copies, four when the n_q queries fit one quadrant and two when they span
@@ -99,6 +100,9 @@ struct AttnTcParams {
     // every lane quadrant, and with it every SM sub-partition, holds the queries; PR = rows
     // of P (copy 0's layout, padded to 16)
     int copies, qpc, PR;
+    // FP8 pools: rows per TMA box of the K / V gather (one page-run: min(page size, 128));
+    // 0 = the rows are gathered by 16-byte cp.async copies
+    int tma_rows;
     const uint16_t *q;     // bf16 [R][Hq][d]
     float scale_log2;      // softmax scale * log2(e)
     unsigned int *sched;   // [2]: next unit to hand out, CTAs done (zero between calls)
@@ -176,6 +180,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool f16) {
 template <int D, bool FP8>
 __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap map_q0, const __grid_constant__ CUtensorMap map_q1,
+                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                    AttnTcParams p) {
     using S_ = AttnShape<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
@@ -215,11 +220,12 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.NS; ++s) {
             // bf16: each loader thread's copies arrive; FP8: each converter warp
+            // FP8: each converter warp arrives; bf16: each loader thread's copies
             mbar_init(op_full + 8 * s, FP8 ? 2 : 128);
             mbar_init(op_empty + 8 * s, 1);
         }
         for (int s = 0; s < p.NR; ++s) {
-            mbar_init(raw_full + 8 * s, 64);  // each FP8 loader thread's copies arrive
+            mbar_init(raw_full + 8 * s, p.tma_rows ? 2 : 64);  // each FP8 loader warp / thread arrives
             mbar_init(raw_empty + 8 * s, 2);  // the converter warps
         }
         for (int a = 0; a < 2; ++a) {
@@ -247,6 +253,10 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     if (warp == 8 && lane == 0) {
         prefetch_tmap(&map_q0);
         if (p.split) prefetch_tmap(&map_q1);
+        if (FP8 && p.tma_rows) {
+            prefetch_tmap(&map_k);
+            prefetch_tmap(&map_v);
+        }
     }
     if (warp == 9) {
         tmem_alloc(smem_u32(tmem_slot), 512);
@@ -851,6 +861,34 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                     const uint32_t s = gi % depth;
                     if (!warp_wait(empty_base + 8 * s, ((gi / depth) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
                     const uint32_t dst_base = ring_base + s * stage_bytes;
+                    if (FP8 && p.tma_rows) {
+                        // one TMA box per page-run of rows into the raw stage; loader warp w
+                        // issues runs w, w + 2, ... and announces their bytes on the stage's
+                        // barrier. Runs past the branch's last position or of an invalid page
+                        // are not loaded.
+                        const int BR = p.tma_rows, nruns = TILE_KEYS / BR;
+                        const CUtensorMap *map = kv ? &map_v : &map_k;
+                        if (lane == 0) {
+                            uint32_t bytes = 0;
+                            for (int r = warp; r < nruns; r += 2) {
+                                if (key0 + r * BR >= ui.kv_end) break;
+                                if (tab->page[(t * TILE_KEYS + r * BR) >> log2P] >= 0) bytes += (uint32_t)(BR * S_::SUB_COLS);
+                            }
+                            mbar_arrive_expect_tx(full_base + 8 * s, bytes);
+                            for (int r = warp; r < nruns; r += 2) {
+                                const int kr = key0 + r * BR;
+                                if (kr >= ui.kv_end) break;
+                                const int pg = tab->page[(t * TILE_KEYS + r * BR) >> log2P];
+                                if (pg < 0) continue;
+                                const int row = (pg * p.kv.n_kv_heads + ui.g) * p.kv.page_size + (kr & (p.kv.page_size - 1));
+                                tma_load_2d(dst_base + (uint32_t)(r * BR) * S_::SUB_COLS, map, h * S_::SUB_COLS, row,
+                                            full_base + 8 * s);
+                            }
+                        }
+                        __syncwarp();
+                        ++gi;
+                        continue;
+                    }
                     const uint8_t *src_col = pool + (size_t)h * S_::SUB_COLS * ESZ + pch * 16;
                     // rows past the branch's last position, or of an invalid page, stay unloaded.
                     // Per group of 8 pieces: the page lookups and offsets first (independent
@@ -905,8 +943,16 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                 mbar_arrive(ufree + 8 * ub);
             }
         }
-        // every copy lands before the CTA may exit
+        // every copy lands before the CTA may exit (TMA boxes: the last phase of each stage)
         cp_async_wait_all();
+        if (FP8 && p.tma_rows && lane == 0) {
+            const uint32_t n_last = gi < depth ? gi : depth;
+            for (uint32_t j = 0; j < n_last; ++j) {
+                const uint32_t i2 = gi - 1 - j;
+                mbar_wait(full_base + 8 * (i2 % depth), (i2 / depth) & 1u, nullptr, ATT_WAIT_NS);
+            }
+        }
+        __syncwarp();
         if (!ok) {
             *abort_flag = 1;
             if (ltid == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
@@ -1140,6 +1186,21 @@ static bool make_q_map(CUtensorMap *map, const void *q, int R, int Hq, int d, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// An FP8 K or V pool viewed as a 2-D byte tensor (d, num_pages * Hkv * P): a box of
+// box_rows rows of one raw sub-tile row's width (min(d, 128) bytes) is one page-run of a
+// (page, kv head), landing unswizzled in the raw ring.
+static bool make_kv_map(CUtensorMap *map, const void *pool, uint64_t rows, int d, int box_rows) {
+    EncodeTiledFnA fn = encode_fn_attn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d};
+    cuuint32_t box[2] = {(cuuint32_t)(d < 128 ? d : 128), (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pool), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Shared-memory plan, in this order (every block 1024-aligned): the Q buffer(s), 2 P
 // buffers, the operand ring, the raw ring (FP8), 2 unit tables, barriers, flags. The M =
 // 128 MMAs read up to (128 - R_pad) rows past the last Q block and (128 - PR) past the last
@@ -1236,9 +1297,24 @@ static int launch_attn_tc(AttnTcParams &p, cudaStream_t s) {
     size_t smem = 0;
     const int st = plan_attn<D, FP8>(p, &smem);
     if (st) return st;
-    CUtensorMap mq0, mq1;
+    CUtensorMap mq0, mq1, mk, mv;
     if (!make_q_map(&mq0, p.q, p.B * (p.k + 1), p.Hq, D, p.G, p.J1)) return SPEC_ERR_CUDA;
     if (!make_q_map(&mq1, p.q, p.B * (p.k + 1), p.Hq, D, p.G, p.split ? p.k + 1 - p.J1 : p.J1)) return SPEC_ERR_CUDA;
+    // FP8 pools with pages of at least 64 positions: K / V rows go to the raw ring by TMA
+    // boxes of one page-run each, so the two loader warps issue a few boxes per sub-tile
+    // instead of 16-byte copies (measured faster there; shorter runs make boxes too small
+    // for the TMA issue rate, and on bf16 pools the branch's registers cost the cp.async
+    // gather more than the boxes gained). A pool too large for 32-bit row coordinates also
+    // takes the cp.async path.
+    p.tma_rows = 0;
+    mk = mq0;
+    mv = mq0;
+    const uint64_t pool_rows = (uint64_t)p.kv.num_pages * p.kv.n_kv_heads * p.kv.page_size;
+    if (FP8 && p.kv.page_size >= 64 && pool_rows < (1ull << 31)) {
+        const int br = p.kv.page_size < TILE_KEYS ? p.kv.page_size : TILE_KEYS;
+        if (make_kv_map(&mk, p.kv.k_pool, pool_rows, D, br) && make_kv_map(&mv, p.kv.v_pool, pool_rows, D, br))
+            p.tma_rows = br;
+    }
     // a fixed ceiling (see the skinny GEMM launcher): graphs may mix launch sizes
     if (cudaFuncSetAttribute(attn_tc_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM_LIMIT) !=
         cudaSuccess)
@@ -1246,7 +1322,7 @@ static int launch_attn_tc(AttnTcParams &p, cudaStream_t s) {
     const int sms = attn_sm_count();
     if (sms < 1) return SPEC_ERR_CUDA;
     const int grid = p.n_units < sms ? p.n_units : sms;
-    return launch_pdl(attn_tc_kernel<D, FP8>, dim3(grid), dim3(S_::THREADS), smem, s, mq0, mq1, p);
+    return launch_pdl(attn_tc_kernel<D, FP8>, dim3(grid), dim3(S_::THREADS), smem, s, mq0, mq1, mk, mv, p);
 }
 
 // workspace: a 256-byte header (the unit scheduler's counters: zero before the first call,
