@@ -25,11 +25,12 @@ KV_BF16, KV_FP8_E4M3 = 0, 1
 
 ERR_NULL, ERR_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_ALIGN = -1, -2, -3, -4, -5, -6
 SPEC_LMHEAD_STATIC_SCRATCH_BYTES = 256 + 1024 * 64 * 8  # as in include/spec_verify.h
+SPEC_MAX_STOP = 32                                       # as in include/spec_verify.h
 
 EXPORTS = ("spec_strerror", "spec_version", "spec_kv_append", "spec_kv_write_rows",
            "spec_verify_attn_workspace", "spec_verify_attn", "spec_lmhead_workspace",
            "spec_lmhead_argmax", "spec_lmhead_logits", "spec_accept", "spec_mtp_input_workspace",
-           "spec_mtp_input", "spec_lmhead_argmax_static")
+           "spec_mtp_input", "spec_lmhead_argmax_static", "spec_accept_stop")
 
 
 class SpecError(RuntimeError):
@@ -73,6 +74,8 @@ def lib() -> ctypes.CDLL:
         L.spec_lmhead_logits.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]
         L.spec_lmhead_argmax_static.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp]
         L.spec_accept.argtypes = [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp]
+        L.spec_accept_stop.argtypes = [_vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                       _vp, _i32, _vp, _vp]
         L.spec_mtp_input_workspace.restype = _sz
         L.spec_mtp_input_workspace.argtypes = [_i32, _i32]
         L.spec_mtp_input.argtypes = [_vp, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp, _vp]
@@ -219,6 +222,22 @@ def spec_accept(drafts, ids, pos, B: int, k: int, out_tokens, out_n, out_accepte
                                             _ptr(out_next, "out_next", torch.int32),
                                             _ptr(hidden, "hidden", torch.bfloat16), H,
                                             _ptr(h_out, "h_out", torch.bfloat16), _stream(stream)))
+
+
+def spec_accept_stop(drafts, ids, pos, B: int, k: int, stop_ids, budget, out_tokens, out_n, out_accepted, out_pos,
+                     out_next, out_done=None, hidden=None, h_out=None, stream=None):
+    """spec_accept with a stop set (device int32 tensor, entries < 0 unused, or None) and a
+    per-branch budget (device int32 [B] or None)."""
+    H = int(hidden.shape[-1]) if hidden is not None else 0
+    n_stop = 0 if stop_ids is None else int(stop_ids.numel())
+    _check("spec_accept_stop", lib().spec_accept_stop(
+        _ptr(drafts, "drafts", torch.int32) if k > 0 else None, _ptr(ids, "ids", torch.int32),
+        _ptr(pos, "pos", torch.int32), B, k, _ptr(stop_ids, "stop_ids", torch.int32), n_stop,
+        _ptr(budget, "budget", torch.int32), _ptr(out_tokens, "out_tokens", torch.int32),
+        _ptr(out_n, "out_n", torch.int32), _ptr(out_accepted, "out_accepted", torch.int32),
+        _ptr(out_pos, "out_pos", torch.int32), _ptr(out_next, "out_next", torch.int32),
+        _ptr(out_done, "out_done", torch.int32), _ptr(hidden, "hidden", torch.bfloat16), H,
+        _ptr(h_out, "h_out", torch.bfloat16), _stream(stream)))
 
 
 def spec_mtp_input_workspace(M: int, H: int) -> int:

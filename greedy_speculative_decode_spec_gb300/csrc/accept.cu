@@ -10,6 +10,15 @@
 //
 // Lane i < k compares draft i with the target of row i; the first mismatching lane
 // (a ballot) is the accepted count a. Lanes 0..k write the emitted tokens.
+//
+// With a stop set and a budget (spec_accept_stop): the run drafts[0..a) ++ [ids[a]] is
+// cut right after its first token in the stop set (flashrt-structures speculative loop:
+// the stop token stays; memra-engine spec.rs `Spec::body_inner`: a small stop-id buffer,
+// -1 = unused entry) and then to at most the branch's budget (DSSD-dev `_commit`: the
+// generation limit). Lane i <= a tests run token i against the stop ids; a second ballot
+// gives the first stop.
+#include <climits>
+
 #include "common.cuh"
 
 namespace spec {
@@ -20,7 +29,9 @@ __global__ void __launch_bounds__(128) accept_kernel(const int32_t *__restrict__
                                                      int32_t *out_tokens, int32_t *out_n,
                                                      int32_t *out_accepted, int32_t *out_pos,
                                                      int32_t *out_next, const uint16_t *hidden, int H,
-                                                     uint16_t *h_out) {
+                                                     uint16_t *h_out, const int32_t *__restrict__ stop,
+                                                     int n_stop, const int32_t *__restrict__ budget,
+                                                     int32_t *out_done) {
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (b >= B) return;
@@ -34,16 +45,39 @@ __global__ void __launch_bounds__(128) accept_kernel(const int32_t *__restrict__
     const unsigned bad = __ballot_sync(0xFFFFFFFFu, mismatch);
     const int a = bad ? (__ffs(bad) - 1) : k;
     const int32_t bonus = __ldg(tgt + a);
-    if (lane <= k) out_tokens[(size_t)b * (k + 1) + lane] = lane < a ? d : (lane == a ? bonus : -1);
-    if (lane == 0) {
-        out_n[b] = a + 1;
-        out_accepted[b] = a;
-        out_pos[b] = __ldg(pos + b) + a + 1;
-        out_next[b] = bonus;
+    const int32_t tok = lane < a ? d : (lane == a ? bonus : -1);  // run token `lane`
+    // the first run token in the stop set, then the budget
+    bool is_stop = false;
+    if (lane <= a)
+        for (int j = 0; j < n_stop; ++j) {
+            const int32_t sid = __ldg(stop + j);
+            is_stop |= sid >= 0 && sid == tok;
+        }
+    const unsigned hits = __ballot_sync(0xFFFFFFFFu, is_stop);
+    int n = hits ? __ffs(hits) : a + 1;  // tokens kept
+    bool stopped = hits != 0;
+    int cap = INT_MAX;
+    if (budget) {
+        cap = __ldg(budget + b);
+        cap = cap < 0 ? 0 : cap;
+        if (n > cap) {
+            n = cap;
+            stopped = false;  // the stop token was cut off
+        }
     }
-    if (h_out) {
-        // the next draft step's hidden state: the target row that produced the bonus
-        const uint16_t *src = hidden + ((size_t)b * (k + 1) + a) * H;
+    const int32_t last = __shfl_sync(0xFFFFFFFFu, tok, n > 0 ? n - 1 : 0);
+    if (lane <= k) out_tokens[(size_t)b * (k + 1) + lane] = lane < n ? tok : -1;
+    if (lane == 0) {
+        out_n[b] = n;
+        out_accepted[b] = a < n ? a : n;
+        out_pos[b] = __ldg(pos + b) + n;
+        out_next[b] = n > 0 ? last : -1;
+        if (out_done) out_done[b] = (stopped || (budget && n == cap)) ? 1 : 0;
+    }
+    if (h_out && n > 0) {
+        // the next draft step's hidden state: the target row that produced the last kept
+        // token (the bonus when nothing was cut)
+        const uint16_t *src = hidden + ((size_t)b * (k + 1) + (n - 1)) * H;
         uint16_t *dst = h_out + (size_t)b * H;
         if ((H & 7) == 0) {
             const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
@@ -74,6 +108,29 @@ SPEC_API int spec_accept(const int32_t *drafts, const int32_t *ids, const int32_
     const int blocks = (B + warps - 1) / warps;
     spec::accept_kernel<<<blocks, warps * 32, 0, (cudaStream_t)stream>>>(
         drafts, ids, pos, B, k, out_tokens, out_n, out_accepted, out_pos, out_next,
-        (const uint16_t *)hidden, gather ? H : 0, (uint16_t *)h_out);
+        (const uint16_t *)hidden, gather ? H : 0, (uint16_t *)h_out, nullptr, 0, nullptr, nullptr);
+    return spec::launch_status();
+}
+
+SPEC_API int spec_accept_stop(const int32_t *drafts, const int32_t *ids, const int32_t *pos, int B, int k,
+                              const int32_t *stop_ids, int n_stop, const int32_t *budget, int32_t *out_tokens,
+                              int32_t *out_n, int32_t *out_accepted, int32_t *out_pos, int32_t *out_next,
+                              int32_t *out_done, const void *hidden, int H, void *h_out, spec_stream_t stream) {
+    if (!ids || !pos || !out_tokens || !out_n || !out_accepted || !out_pos || !out_next) return SPEC_ERR_NULL;
+    if (k > 0 && !drafts) return SPEC_ERR_NULL;
+    if (B < 1 || k < 0 || k > SPEC_KMAX) return SPEC_ERR_ARG;
+    if (n_stop < 0 || n_stop > SPEC_MAX_STOP) return SPEC_ERR_ARG;
+    if (n_stop > 0 && !stop_ids) return SPEC_ERR_NULL;
+    const bool gather = hidden || h_out;
+    if (gather) {
+        if (!hidden || !h_out) return SPEC_ERR_NULL;
+        if (H < 1) return SPEC_ERR_ARG;
+        if ((H & 7) == 0 && (!spec::aligned16(hidden) || !spec::aligned16(h_out))) return SPEC_ERR_ALIGN;
+    }
+    const int warps = 4;
+    const int blocks = (B + warps - 1) / warps;
+    spec::accept_kernel<<<blocks, warps * 32, 0, (cudaStream_t)stream>>>(
+        drafts, ids, pos, B, k, out_tokens, out_n, out_accepted, out_pos, out_next,
+        (const uint16_t *)hidden, gather ? H : 0, (uint16_t *)h_out, stop_ids, n_stop, budget, out_done);
     return spec::launch_status();
 }

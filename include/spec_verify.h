@@ -10,6 +10,7 @@
  *   spec_verify_attn    causal GQA attention of the R rows over their pages
  *   spec_lmhead_argmax  logits = hidden . W^T with a fused per-row argmax
  *   spec_accept         greedy chain acceptance
+ *   spec_accept_stop    greedy chain acceptance with stop tokens and a generation budget
  *   spec_mtp_input      the draft head's input  fc([rmsnorm(E[tok]), rmsnorm(h)])
  *
  * The method follows the span-02 page `engine/crates/model/src/spec.rs`
@@ -242,6 +243,32 @@ int spec_accept(const int32_t *drafts, const int32_t *ids, const int32_t *pos, i
                 int k, int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted,
                 int32_t *out_pos, int32_t *out_next, const void *hidden, int H,
                 void *h_out, spec_stream_t stream);
+
+/* ---- a4 with stop tokens and a generation budget ------------------------------------
+ * The greedy run of branch b (drafts[b][0..a) followed by g_a) is cut right after its
+ * first token that is in the stop set, then to at most budget[b] tokens:
+ *   n = min(first stop index + 1 (or a+1 without one), max(budget[b], 0))
+ *   emitted = the first n run tokens;  accepted = min(a, n);  new pos = pos[b] + n
+ *   next = the last emitted token (-1 when n == 0)
+ *   done = the emitted run ends on a stop token, or n reached budget[b]
+ * With no stop ids and no budget it returns exactly what spec_accept returns.
+ * Sources: flashrt-structures speculative decode loop (the emitted tokens are cut after
+ * the first stop token, which stays); memra-engine spec.rs, `Spec::body_inner` (the
+ * acceptance kernel takes a stop-id buffer whose unused entries are -1, and a token
+ * limit); DSSD-dev `_commit` (a cycle's tokens are also cut at the generation limit).
+ *   stop_ids   device int32 [n_stop] (entries < 0 are unused); NULL when n_stop == 0;
+ *              0 <= n_stop <= SPEC_MAX_STOP
+ *   budget     device int32 [B]: tokens branch b may still emit, or NULL (no limit)
+ *   out_done   device int32 [B] (0/1), or NULL
+ *   the other arguments are those of spec_accept; h_out[b] is the hidden row of the
+ *   last emitted token (row b*(k+1) + n-1) and is left unwritten when n == 0.
+ * Host errors: those of spec_accept; n_stop out of range; n_stop > 0 with NULL stop_ids. */
+#define SPEC_MAX_STOP 32
+int spec_accept_stop(const int32_t *drafts, const int32_t *ids, const int32_t *pos, int B,
+                     int k, const int32_t *stop_ids, int n_stop, const int32_t *budget,
+                     int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted,
+                     int32_t *out_pos, int32_t *out_next, int32_t *out_done,
+                     const void *hidden, int H, void *h_out, spec_stream_t stream);
 
 /* ---- a5: MTP draft-head input -----------------------------------------------------
  *   c[m]  = [ rmsnorm(E[tok[m]]; g_emb) ; rmsnorm(h[m]; g_hid) ]  rounded to bf16

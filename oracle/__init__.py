@@ -78,6 +78,8 @@ def lib():
         _lib.orc_lmhead_logits.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_void_p]
         _lib.orc_accept.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 5
+        _lib.orc_accept_stop.argtypes = ([ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                          ctypes.c_int] + [ctypes.c_void_p] * 7)
         _lib.orc_mtp_input.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_double, ctypes.c_void_p, ctypes.c_int,
                                                                ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                                                ctypes.c_void_p]
@@ -215,6 +217,21 @@ def accept(drafts, ids, pos, B: int, k: int):
     n, a, npos, nxt = (np.empty(B, np.int32) for _ in range(4))
     lib().orc_accept(_p(drafts), _p(ids), _p(pos), B, k, _p(tokens), _p(n), _p(a), _p(npos), _p(nxt))
     return tokens, n, a, npos, nxt
+
+
+def accept_stop(drafts, ids, pos, B: int, k: int, stop=(), budget=None):
+    """Greedy acceptance cut at the first stop token and at the branch's budget:
+    tokens [B][k+1], n, accepted, new_pos, next, done."""
+    assert k <= 63
+    drafts = _c(np.asarray(drafts).reshape(B, k) if k > 0 else np.zeros((B, 1)), np.int32)
+    ids, pos = _c(ids, np.int32), _c(pos, np.int32)
+    stop_a = _c(np.asarray(stop, np.int32).reshape(-1) if len(stop) else np.full(1, -1), np.int32)
+    bud = None if budget is None else _c(budget, np.int32)
+    tokens = np.empty((B, k + 1), np.int32)
+    n, a, npos, nxt, done = (np.empty(B, np.int32) for _ in range(5))
+    lib().orc_accept_stop(_p(drafts), _p(ids), _p(pos), B, k, _p(stop_a), len(stop),
+                          None if bud is None else _p(bud), _p(tokens), _p(n), _p(a), _p(npos), _p(nxt), _p(done))
+    return tokens, n, a, npos, nxt, done
 
 
 # ---- MTP input ----------------------------------------------------------------------------

@@ -427,6 +427,59 @@ void orc_accept(const int32_t *drafts, const int32_t *ids, const int32_t *pos, i
     }
 }
 
+/* Stop tokens and a generation budget on top of the greedy run. memra-engine spec.rs,
+ * `Spec::body_inner`: the acceptance kernel takes a small stop-id buffer (-1 = unused
+ * entry) and a token limit; flashrt-structures speculative loop: the emitted tokens are
+ * cut right after the first stop token (the stop token itself is kept); DSSD-dev
+ * `_commit`: a cycle's tokens are also cut at the generation limit. The run of branch b
+ * (drafts[0..a) then ids[b(k+1)+a]) is cut after its first token that is in the stop
+ * set, then to at most budget[b] tokens (budget NULL: no limit; a negative entry counts
+ * as 0). n = tokens kept, accepted = drafts among them, new_pos = pos + n, next = the
+ * last kept token (-1 when none), done = the kept run ends on a stop token or used the
+ * whole budget. */
+void orc_accept_stop(const int32_t *drafts, const int32_t *ids, const int32_t *pos, int B, int k,
+                     const int32_t *stop, int n_stop, const int32_t *budget, int32_t *out_tokens,
+                     int32_t *out_n, int32_t *out_accepted, int32_t *out_pos, int32_t *out_next,
+                     int32_t *out_done) {
+    for (int b = 0; b < B; ++b) {
+        const int32_t *target = ids + (size_t)b * (k + 1);
+        int32_t run[64];
+        int a = 0;
+        while (a < k && drafts[(size_t)b * k + a] == target[a]) {
+            run[a] = drafts[(size_t)b * k + a];
+            ++a;
+        }
+        run[a] = target[a];
+        int n = a + 1, stopped = 0;
+        for (int i = 0; i <= a; ++i) {
+            int hit = 0;
+            for (int j = 0; j < n_stop; ++j)
+                if (stop[j] >= 0 && stop[j] == run[i]) hit = 1;
+            if (hit) {
+                n = i + 1;
+                stopped = 1;
+                break;
+            }
+        }
+        int capped = 0;
+        if (budget) {
+            int cap = budget[b] < 0 ? 0 : budget[b];
+            if (n > cap) {
+                n = cap;
+                stopped = 0; /* the stop token was cut off */
+            }
+            if (n == cap) capped = 1;
+        }
+        int32_t *emit = out_tokens + (size_t)b * (k + 1);
+        for (int j = 0; j <= k; ++j) emit[j] = j < n ? run[j] : -1;
+        out_n[b] = n;
+        out_accepted[b] = a < n ? a : n;
+        out_pos[b] = pos[b] + n;
+        out_next[b] = n > 0 ? run[n - 1] : -1;
+        out_done[b] = stopped || capped;
+    }
+}
+
 /* ------------------------------------------------------------------------------------
  * MTP draft-head input
  * ---------------------------------------------------------------------------------- */

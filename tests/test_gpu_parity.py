@@ -277,3 +277,62 @@ def test_accept_random_patterns_max_k():
         want = orc.accept(drafts, ids, pos, B, k)
         for g_, o_ in zip(got, want):
             np.testing.assert_array_equal(g_, o_)
+
+
+def _gpu_accept_stop(drafts, ids, pos, B, k, stop, budget, hidden=None):
+    i32 = dict(dtype=torch.int32, device=DEV)
+    toks = torch.empty((B, k + 1), **i32)
+    n, a, npos, nxt, done = (torch.full((B,), -7, **i32) for _ in range(5))
+    stop_d = torch.tensor(stop, **i32) if len(stop) else None
+    bud_d = None if budget is None else torch.from_numpy(budget).to(DEV)
+    h_out = None if hidden is None else torch.zeros((B, hidden.shape[1]), dtype=torch.bfloat16, device=DEV)
+    bnd.spec_accept_stop(torch.from_numpy(drafts).to(DEV), torch.from_numpy(ids).to(DEV), torch.from_numpy(pos).to(DEV),
+                         B, k, stop_d, bud_d, toks, n, a, npos, nxt, done, hidden=hidden, h_out=h_out)
+    torch.cuda.synchronize()
+    return [t.cpu().numpy() for t in (toks, n, a, npos, nxt, done)], h_out
+
+
+def test_accept_stop_matches_oracle():
+    rng = np.random.default_rng(21)
+    for B, k in ((16, 15), (9, 4), (5, 0), (33, 6)):
+        ids = rng.integers(0, 12, B * (k + 1)).astype(np.int32)
+        hit = rng.random((B, k)) < 0.85
+        drafts = np.where(hit, ids.reshape(B, k + 1)[:, :k], 99).astype(np.int32)
+        pos = rng.integers(0, 10 ** 6, B).astype(np.int32)
+        for stop, budget in (([], None), ([3, -1, 7], None), ([], rng.integers(-2, k + 3, B).astype(np.int32)),
+                             (list(range(0, 12, 2)) + [-1] * 26, rng.integers(0, k + 2, B).astype(np.int32))):
+            got, _ = _gpu_accept_stop(drafts, ids, pos, B, k, stop, budget)
+            want = orc.accept_stop(drafts, ids, pos, B, k, stop, budget)
+            for g_, o_ in zip(got, want):
+                np.testing.assert_array_equal(g_, o_)
+    # no stop set, no budget: exactly spec_accept
+    got, _ = _gpu_accept_stop(drafts, ids, pos, B, k, [], None)
+    base = gpu_accept(torch.from_numpy(drafts).cuda(), torch.from_numpy(ids).cuda(), torch.from_numpy(pos).cuda(), B, k)
+    for g_, o_ in zip(got[:5], base):
+        np.testing.assert_array_equal(g_, o_)
+
+
+def test_accept_stop_hidden_row_of_last_token():
+    rng = np.random.default_rng(22)
+    B, k, H = 6, 4, 64
+    ids = rng.integers(0, 6, B * (k + 1)).astype(np.int32)
+    drafts = ids.reshape(B, k + 1)[:, :k].copy()          # full acceptance everywhere
+    pos = np.arange(B, dtype=np.int32) * 10
+    hidden = torch.randn((B * (k + 1), H), device=DEV).to(torch.bfloat16)
+    budget = np.array([0, 1, 2, 3, 5, 9], np.int32)
+    (toks, n, a, npos, nxt, done), h_out = _gpu_accept_stop(drafts, ids, pos, B, k, [], budget, hidden)
+    want = orc.accept_stop(drafts, ids, pos, B, k, [], budget)
+    np.testing.assert_array_equal(n, want[1])
+    for b in range(B):
+        if n[b] == 0:
+            assert torch.count_nonzero(h_out[b]) == 0     # left unwritten
+        else:
+            assert torch.equal(h_out[b], hidden[b * (k + 1) + n[b] - 1])
+
+
+def test_accept_stop_host_errors():
+    i32 = dict(dtype=torch.int32, device=DEV)
+    t = torch.zeros(8, **i32)
+    toks = torch.zeros((1, 2), **i32)
+    with pytest.raises(bnd.SpecError):
+        bnd.spec_accept_stop(t[:1], t[:2], t[:1], 1, 1, torch.zeros(33, **i32), None, toks, t[:1], t[:1], t[:1], t[:1])

@@ -373,6 +373,48 @@ def test_accept_exhaustive_patterns(orc, k):
         assert np.all(toks[b, want_a + 1:] == -1)
 
 
+def test_accept_stop_golden(orc):
+    with open(os.path.join(GOLDEN, "accept_stop_example.json")) as f:
+        fx = json.load(f)
+    for c in fx["cases"]:
+        k = len(c["drafts"])
+        bud = None if c["budget"] is None else [c["budget"]]
+        toks, n, a, npos, nxt, done = orc.accept_stop(c["drafts"], c["ids"], [c["pos"]], 1, k, c["stop"], bud)
+        assert toks[0].tolist() == c["tokens"], c["note"]
+        assert (n[0], a[0], npos[0], nxt[0], done[0]) == (c["n"], c["accepted"], c["new_pos"], c["next"], c["done"]), c["note"]
+
+
+@pytest.mark.parametrize("k", [0, 1, 3, 6])
+def test_accept_stop_reduces_to_greedy_and_is_a_prefix(orc, k):
+    """No stop set and no budget gives the plain greedy result; with them, the kept tokens
+    are a prefix of it, ending on the first stop token of the run or at the budget."""
+    rng = np.random.default_rng(40 + k)
+    pats = list(itertools.product([True, False], repeat=k))
+    B = len(pats)
+    ids = rng.integers(0, 8, (B, k + 1)).astype(np.int32)
+    drafts = np.where(np.array(pats, bool).reshape(B, k), ids[:, :k], ids[:, :k] + 8).astype(np.int32)
+    pos = rng.integers(0, 5000, B).astype(np.int32)
+    base = orc.accept(drafts, ids.reshape(-1), pos, B, k)
+    same = orc.accept_stop(drafts, ids.reshape(-1), pos, B, k)
+    for x, y in zip(base, same[:5]):
+        np.testing.assert_array_equal(x, y)
+    assert not same[5].any()
+    stop = [3, -1, 6]
+    budget = rng.integers(-1, k + 3, B).astype(np.int32)
+    toks, n, a, npos, nxt, done = orc.accept_stop(drafts, ids.reshape(-1), pos, B, k, stop, budget)
+    btoks, bn = base[0], base[1]
+    for b in range(B):
+        run = btoks[b, :bn[b]].tolist()
+        first = next((i for i, t in enumerate(run) if t in (3, 6)), None)
+        want = len(run) if first is None else first + 1
+        want = min(want, max(int(budget[b]), 0))
+        assert n[b] == want and toks[b, :want].tolist() == run[:want] and np.all(toks[b, want:] == -1)
+        assert npos[b] == pos[b] + want and a[b] == min(base[2][b], want)
+        assert nxt[b] == (run[want - 1] if want else -1)
+        ends_on_stop = want > 0 and run[want - 1] in (3, 6)
+        assert done[b] == int(ends_on_stop or want == max(int(budget[b]), 0))
+
+
 # ---- MTP input -----------------------------------------------------------------------------------
 
 def test_mtp_input_closed_form(orc):
