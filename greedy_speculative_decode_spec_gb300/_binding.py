@@ -26,11 +26,15 @@ KV_BF16, KV_FP8_E4M3 = 0, 1
 ERR_NULL, ERR_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_ALIGN = -1, -2, -3, -4, -5, -6
 SPEC_LMHEAD_STATIC_SCRATCH_BYTES = 256 + 1024 * 64 * 8  # as in include/spec_verify.h
 SPEC_MAX_STOP = 32                                       # as in include/spec_verify.h
+SPEC_ATTN_PLAN_FIELDS = 16                               # as in include/spec_verify.h
+ATTN_PLAN_KEYS = ("smem", "copies", "quadrants_per_copy", "q_rows", "p_rows", "ring_stages", "raw_stages",
+                  "q_buffers", "o_buffers", "split_keys", "n_splits", "n_units", "split_layout", "tma_rows",
+                  "barrier_bytes", "barrier_bytes_reserved")
 
 EXPORTS = ("spec_strerror", "spec_version", "spec_kv_append", "spec_kv_write_rows",
            "spec_verify_attn_workspace", "spec_verify_attn", "spec_lmhead_workspace",
            "spec_lmhead_argmax", "spec_lmhead_logits", "spec_accept", "spec_mtp_input_workspace",
-           "spec_mtp_input", "spec_lmhead_argmax_static", "spec_accept_stop")
+           "spec_mtp_input", "spec_lmhead_argmax_static", "spec_accept_stop", "spec_verify_attn_plan")
 
 
 class SpecError(RuntimeError):
@@ -74,6 +78,7 @@ def lib() -> ctypes.CDLL:
         L.spec_lmhead_logits.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]
         L.spec_lmhead_argmax_static.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp]
         L.spec_accept.argtypes = [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp]
+        L.spec_verify_attn_plan.argtypes = [ctypes.POINTER(spec_kv_desc), _i32, _i32, _i32, _i32, _vp, _i32]
         L.spec_accept_stop.argtypes = [_vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _vp, _i32, _vp, _vp]
         L.spec_mtp_input_workspace.restype = _sz
@@ -222,6 +227,22 @@ def spec_accept(drafts, ids, pos, B: int, k: int, out_tokens, out_n, out_accepte
                                             _ptr(out_next, "out_next", torch.int32),
                                             _ptr(hidden, "hidden", torch.bfloat16), H,
                                             _ptr(h_out, "h_out", torch.bfloat16), _stream(stream)))
+
+
+def kv_shape(num_pages: int, max_pages: int, page_size: int, n_kv_heads: int, head_dim: int,
+             fp8: bool = False) -> spec_kv_desc:
+    """A descriptor that carries only shapes (no memory): for spec_verify_attn_plan."""
+    return spec_kv_desc(None, None, None, None, None, num_pages, max_pages, page_size, n_kv_heads, head_dim,
+                        KV_FP8_E4M3 if fp8 else KV_BF16)
+
+
+def spec_verify_attn_plan(kv: spec_kv_desc, B: int, k: int, n_q_heads: int, max_pos: int) -> dict:
+    """The launch plan spec_verify_attn would use (host arithmetic only, no GPU)."""
+    out = (ctypes.c_int32 * SPEC_ATTN_PLAN_FIELDS)()
+    _check("spec_verify_attn_plan", lib().spec_verify_attn_plan(ctypes.byref(kv), B, k, n_q_heads, max_pos,
+                                                                ctypes.cast(out, ctypes.c_void_p),
+                                                                SPEC_ATTN_PLAN_FIELDS))
+    return dict(zip(ATTN_PLAN_KEYS, list(out)))
 
 
 def spec_accept_stop(drafts, ids, pos, B: int, k: int, stop_ids, budget, out_tokens, out_n, out_accepted, out_pos,

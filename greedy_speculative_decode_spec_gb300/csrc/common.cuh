@@ -51,12 +51,20 @@ inline int log2i(int x) {
 }
 
 // Validates a pool descriptor; returns SPEC_OK or an error code.
-inline int check_kv_desc(const spec_kv_desc *kv) {
-    if (!kv || !kv->k_pool || !kv->v_pool || !kv->page_table) return SPEC_ERR_NULL;
+// The descriptor's shape fields (no pointer is looked at).
+inline int check_kv_shape(const spec_kv_desc *kv) {
+    if (!kv) return SPEC_ERR_NULL;
     if (kv->num_pages < 1 || kv->max_pages < 1 || kv->n_kv_heads < 1) return SPEC_ERR_ARG;
     if (!is_pow2(kv->page_size) || kv->page_size > 1024) return SPEC_ERR_ARG;
     if (kv->head_dim != 64 && kv->head_dim != 128 && kv->head_dim != 256) return SPEC_ERR_UNSUPPORTED;
     if (kv->kv_dtype != SPEC_KV_BF16 && kv->kv_dtype != SPEC_KV_FP8_E4M3) return SPEC_ERR_UNSUPPORTED;
+    return SPEC_OK;
+}
+
+inline int check_kv_desc(const spec_kv_desc *kv) {
+    if (!kv || !kv->k_pool || !kv->v_pool || !kv->page_table) return SPEC_ERR_NULL;
+    const int st = check_kv_shape(kv);
+    if (st) return st;
     if (kv->kv_dtype == SPEC_KV_FP8_E4M3 && (!kv->k_scale || !kv->v_scale)) return SPEC_ERR_NULL;
     if (!aligned16(kv->k_pool) || !aligned16(kv->v_pool)) return SPEC_ERR_ALIGN;
     return SPEC_OK;

@@ -115,6 +115,39 @@ struct AttnTcParams {
     uint32_t off_q, off_p, off_op, off_raw, off_ut, off_bar, off_small;  // shared-memory offsets
 };
 
+// The CTA's mbarriers, as byte offsets from the barrier region (one definition for the
+// kernel and the host plan, which checks that they fit BAR_BYTES).
+struct BarMap {
+    uint32_t op_full, op_empty, raw_full, raw_empty, sfull, sfree, pfull, pfree, odone, ofree;
+    uint32_t qfull, qconv, qfree, ufull, ufree, drain, xfull, lfull, lfin, end;
+};
+__host__ __device__ inline BarMap bar_map(int NS, int NR) {
+    BarMap m;
+    uint32_t o = 0;
+    m.op_full = o;   o += 8 * NS;  // operand ring: full / empty per stage
+    m.op_empty = o;  o += 8 * NS;
+    m.raw_full = o;  o += 8 * NR;  // FP8 raw ring
+    m.raw_empty = o; o += 8 * NR;
+    m.sfull = o;     o += 16;      // S double buffer
+    m.sfree = o;     o += 16;
+    m.pfull = o;     o += 16;      // P double buffer
+    m.pfree = o;     o += 16;
+    m.odone = o;     o += 8;       // P.V completions
+    m.ofree = o;     o += 16;      // O buffers
+    m.qfull = o;     o += 16;      // Q buffers
+    m.qconv = o;     o += 16;
+    m.qfree = o;     o += 16;
+    m.ufull = o;     o += 16;      // unit tables
+    m.ufree = o;     o += 16;
+    m.drain = o;     o += 16;      // one per MMA issuer
+    m.xfull = o;     o += 32;      // softmax exchanges: row maxima, row sums
+    m.lfull = o;     o += 32;
+    m.lfin = o;      o += 16;      // the loaders have issued every copy of a unit
+    m.end = o;
+    return m;
+}
+constexpr uint32_t BAR_BYTES = 8 * 64;
+
 // A ring stage holds one sub-tile: 128 keys x SUB_COLS columns of d (d = 256 tiles are
 // two sub-tiles, the halves of d: S accumulates over both, and each half of O reads its
 // own half of V).
@@ -197,17 +230,18 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     uint8_t *g_p = smem + p.off_p;
     UnitTable *tables = reinterpret_cast<UnitTable *>(smem + p.off_ut);  // [2]
     // barrier map
-    const uint32_t op_full = s_base + p.off_bar, op_empty = op_full + 8 * p.NS;
-    const uint32_t raw_full = op_empty + 8 * p.NS, raw_empty = raw_full + 8 * p.NR;  // FP8 raw ring
-    const uint32_t sfull = raw_empty + 8 * p.NR, sfree = sfull + 16;                 // S double buffer
-    const uint32_t pfull = sfree + 16, pfree = pfull + 16;            // P double buffer
-    const uint32_t odone = pfree + 16, ofree = odone + 8;             // P.V completions, O buffers
-    const uint32_t qfull = ofree + 16, qconv = qfull + 16, qfree = qconv + 16;  // Q double buffer
-    const uint32_t ufull = qfree + 16, ufree = ufull + 16;                      // unit tables
-    const uint32_t drain = ufree + 16;  // one per MMA issuer
-    // softmax warps' exchanges, per lane quadrant and buffer: row maxima, row sums
-    const uint32_t xfull = drain + 16, lfull = xfull + 32;
-    const uint32_t lfin = lfull + 32;  // the loaders have issued every copy of a unit
+    const BarMap bm = bar_map(p.NS, p.NR);
+    const uint32_t bar0 = s_base + p.off_bar;
+    const uint32_t op_full = bar0 + bm.op_full, op_empty = bar0 + bm.op_empty;
+    const uint32_t raw_full = bar0 + bm.raw_full, raw_empty = bar0 + bm.raw_empty;
+    const uint32_t sfull = bar0 + bm.sfull, sfree = bar0 + bm.sfree;
+    const uint32_t pfull = bar0 + bm.pfull, pfree = bar0 + bm.pfree;
+    const uint32_t odone = bar0 + bm.odone, ofree = bar0 + bm.ofree;
+    const uint32_t qfull = bar0 + bm.qfull, qconv = bar0 + bm.qconv, qfree = bar0 + bm.qfree;
+    const uint32_t ufull = bar0 + bm.ufull, ufree = bar0 + bm.ufree;
+    const uint32_t drain = bar0 + bm.drain;
+    const uint32_t xfull = bar0 + bm.xfull, lfull = bar0 + bm.lfull;
+    const uint32_t lfin = bar0 + bm.lfin;
     uint8_t *small = smem + p.off_small;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(small + 4);
@@ -1210,7 +1244,7 @@ static int plan_rings(AttnTcParams &p, int QB) {
     using S_ = AttnShape<D, FP8>;
     const uint32_t q_bytes = QB * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.PR * 128;
     const uint32_t ut_bytes = 2 * (uint32_t)sizeof(UnitTable);
-    const uint32_t bars = 8 * 64, small = 64 + 3072;
+    const uint32_t bars = BAR_BYTES, small = 64 + 3072;
     const uint32_t fixed = 1024 + q_bytes + p_bytes + ut_bytes + bars + small;
     const uint32_t raw_row = FP8 ? S_::RAW_STAGE : 0;
     if (ATT_SMEM_LIMIT < fixed + 2 * S_::OP_STAGE + 2 * raw_row) return SPEC_ERR_UNSUPPORTED;
@@ -1246,7 +1280,8 @@ static int plan_copies(AttnTcParams &p, int copies) {
     const int st2 = plan_rings<D, FP8>(p, 2);
     const int st1 = plan_rings<D, FP8>(p1, 1);
     if (st2 && st1) return st2;
-    if (st2 || (FP8 ? p1.NR > p.NR : p1.NS > p.NS)) p = p1;
+    // FP8: the raw ring first (bytes in flight), then the operand ring (converted stages)
+    if (st2 || (FP8 ? (p1.NR > p.NR || (p1.NR == p.NR && p1.NS > p.NS)) : p1.NS > p.NS)) p = p1;
     return SPEC_OK;
 }
 
@@ -1276,10 +1311,11 @@ static int plan_attn(AttnTcParams &p, size_t *smem_bytes) {
         st = plan_copies<D, FP8>(p, 2);
     }
     if (st) return st;
+    if (bar_map(p.NS, p.NR).end > BAR_BYTES) return SPEC_ERR_UNSUPPORTED;
     p.OB = 256 + 2 * D <= 512 ? 2 : 1;
     const uint32_t q_bytes = p.QB * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.PR * 128;
     const uint32_t ut_bytes = 2 * (uint32_t)sizeof(UnitTable);
-    const uint32_t bars = 8 * 64, small = 64 + 3072;
+    const uint32_t bars = BAR_BYTES, small = 64 + 3072;
     p.off_q = 0;
     p.off_p = p.off_q + q_bytes;
     p.off_op = p.off_p + p_bytes;
@@ -1334,7 +1370,72 @@ static size_t ws_bytes_for(int B, int Hkv, int n_splits, int n_q, int d) {
     return 256 + ml + units * n_q * d * sizeof(float);
 }
 
+// The launch parameters that depend only on the shapes (the caller checks the descriptor
+// and fills in the pointers).
+static int attn_setup(const spec_kv_desc *kvd, int B, int k, int n_q_heads, int max_pos, AttnTcParams &p) {
+    if (B < 1 || k < 0 || k > SPEC_KMAX || n_q_heads < 1 || max_pos < k + 1) return SPEC_ERR_ARG;
+    if (n_q_heads % kvd->n_kv_heads) return SPEC_ERR_ARG;
+    const int G = n_q_heads / kvd->n_kv_heads;
+    const int n_q = (k + 1) * G;
+    const int N_pad = ((n_q + 15) / 16) * 16;
+    // more than 32 query vectors need two TMEM lane quadrants: the draft rows are then split
+    // in two halves of at most 32 lanes each when they fit (otherwise the vectors run
+    // contiguously over both quadrants); PR = the lanes of one copy of that layout
+    const int J1 = (k + 2) / 2;
+    const bool split = n_q > 32 && k >= 1 && J1 * G <= 32 && (k + 1 - J1) * G <= 32;
+    p = AttnTcParams{};
+    p.kv = make_view(kvd);
+    p.B = B;
+    p.k = k;
+    p.Hq = n_q_heads;
+    p.G = G;
+    p.n_q = n_q;
+    p.J1 = split ? J1 : k + 1;
+    p.split = split ? 1 : 0;
+    p.PR = split ? 32 + (((k + 1 - J1) * G + 15) / 16) * 16 : N_pad;
+    p.qpc = n_q > 32 ? 2 : 1;
+    p.split_keys = split_keys_for(kvd->n_kv_heads);
+    p.n_splits = (max_pos + p.split_keys - 1) / p.split_keys;
+    p.max_pos = max_pos;
+    p.n_units = B * kvd->n_kv_heads * p.n_splits;
+    return N_pad > MAX_NPAD ? SPEC_ERR_UNSUPPORTED : SPEC_OK;
+}
+
+static int plan_dispatch(AttnTcParams &p, size_t *smem) {
+    switch (p.kv.head_dim * 2 + (p.kv.kv_dtype == SPEC_KV_FP8_E4M3 ? 1 : 0)) {
+        case 128: return plan_attn<64, false>(p, smem);
+        case 129: return plan_attn<64, true>(p, smem);
+        case 256: return plan_attn<128, false>(p, smem);
+        case 257: return plan_attn<128, true>(p, smem);
+        case 512: return plan_attn<256, false>(p, smem);
+        default: return plan_attn<256, true>(p, smem);
+    }
+}
+
 }  // namespace spec
+
+SPEC_API int spec_verify_attn_plan(const spec_kv_desc *kvd, int B, int k, int n_q_heads, int max_pos, int32_t *out,
+                                   int n_out) {
+    if (!out || n_out < SPEC_ATTN_PLAN_FIELDS) return SPEC_ERR_ARG;
+    int st = spec::check_kv_shape(kvd);
+    if (st) return st;
+    spec::AttnTcParams p;
+    st = spec::attn_setup(kvd, B, k, n_q_heads, max_pos, p);
+    if (st) return st;
+    size_t smem = 0;
+    st = spec::plan_dispatch(p, &smem);
+    if (st) return st;
+    const bool fp8 = kvd->kv_dtype == SPEC_KV_FP8_E4M3;
+    const uint64_t pool_rows = (uint64_t)kvd->num_pages * kvd->n_kv_heads * kvd->page_size;
+    const int tma_rows = fp8 && kvd->page_size >= 64 && pool_rows < (1ull << 31)
+                             ? (kvd->page_size < spec::TILE_KEYS ? kvd->page_size : spec::TILE_KEYS)
+                             : 0;
+    const int32_t v[SPEC_ATTN_PLAN_FIELDS] = {(int32_t)smem, p.copies, p.qpc, p.R_pad, p.PR, p.NS, p.NR, p.QB, p.OB,
+                                              p.split_keys, p.n_splits, p.n_units, p.split, tma_rows,
+                                              (int32_t)spec::bar_map(p.NS, p.NR).end, (int32_t)spec::BAR_BYTES};
+    for (int i = 0; i < SPEC_ATTN_PLAN_FIELDS; ++i) out[i] = v[i];
+    return SPEC_OK;
+}
 
 SPEC_API size_t spec_verify_attn_workspace(const spec_kv_desc *kv, int B, int k, int n_q_heads, int max_pos) {
     if (spec::check_kv_desc(kv) || B < 1 || k < 0 || k > SPEC_KMAX || n_q_heads < 1 || max_pos < 1) return 0;
@@ -1357,32 +1458,11 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     if (!ws || ws_bytes < need) return SPEC_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SPEC_ERR_ALIGN;
     if (!spec::aligned16(q) || !spec::aligned16(out)) return SPEC_ERR_ALIGN;
-    const int G = n_q_heads / kvd->n_kv_heads;
-    const int n_q = (k + 1) * G;
-    const int N_pad = ((n_q + 15) / 16) * 16;
-    if (N_pad > spec::MAX_NPAD) return SPEC_ERR_UNSUPPORTED;
-    // more than 32 query vectors need two TMEM lane quadrants: the draft rows are then split
-    // in two halves of at most 32 lanes each when they fit (otherwise the vectors run
-    // contiguously over both quadrants); PR = the lanes of one copy of that layout
-    const int J1 = (k + 2) / 2;
-    const bool split = n_q > 32 && k >= 1 && J1 * G <= 32 && (k + 1 - J1) * G <= 32;
-    const int PR = split ? 32 + (((k + 1 - J1) * G + 15) / 16) * 16 : N_pad;
-    spec::AttnTcParams p{};
-    p.kv = spec::make_view(kvd);
+    spec::AttnTcParams p;
+    st = spec::attn_setup(kvd, B, k, n_q_heads, max_pos, p);
+    if (st) return st;
+    const int G = p.G, n_q = p.n_q;
     p.pos = pos;
-    p.B = B;
-    p.k = k;
-    p.Hq = n_q_heads;
-    p.G = G;
-    p.n_q = n_q;
-    p.J1 = split ? J1 : k + 1;
-    p.split = split ? 1 : 0;
-    p.PR = PR;
-    p.qpc = n_q > 32 ? 2 : 1;
-    p.split_keys = spec::split_keys_for(kvd->n_kv_heads);
-    p.n_splits = (max_pos + p.split_keys - 1) / p.split_keys;
-    p.max_pos = max_pos;
-    p.n_units = B * kvd->n_kv_heads * p.n_splits;
     p.q = (const uint16_t *)q;
     p.scale_log2 = scale * spec::LOG2E;
     const size_t units = (size_t)p.n_units;

@@ -134,6 +134,18 @@ int spec_kv_write_rows(const spec_kv_desc *kv, const int32_t *row_branch,
                        const int32_t *row_pos, int n_rows, const void *k_rows,
                        const void *v_rows, int32_t *dev_err, spec_stream_t stream);
 
+/* Diagnostic (no GPU needed, nothing launched): the launch plan spec_verify_attn would
+ * use for these shapes. Only the descriptor's shape fields are read (its pointers are not
+ * looked at). out[0..15] = dynamic shared memory bytes, query copies on the TMEM lanes,
+ * lane quadrants per copy, Q rows per buffer (all copies), P rows, operand ring stages,
+ * FP8 raw ring stages, Q buffers, O buffers, split size in positions, splits per branch,
+ * work units, split query layout (0/1), FP8 TMA box rows (0 = cp.async gather), barrier
+ * bytes used, barrier bytes reserved. Returns the status the host checks and the
+ * planning of spec_verify_attn would give (n_out < SPEC_ATTN_PLAN_FIELDS: SPEC_ERR_ARG). */
+#define SPEC_ATTN_PLAN_FIELDS 16
+int spec_verify_attn_plan(const spec_kv_desc *kv, int B, int k, int n_q_heads, int max_pos,
+                          int32_t *out, int n_out);
+
 /* ---- a2: verify attention ---------------------------------------------------------
  * For every row r = b*(k+1)+j (position p = pos[b]+j) and q head h (kv head
  * g = h / (n_q_heads / n_kv_heads)):
