@@ -72,6 +72,10 @@ CONFIGS: dict[int, VerifyConfig] = {
 }
 
 
+# the same workloads by name
+WORKLOADS: dict[str, VerifyConfig] = {c.name: c for c in CONFIGS.values()}
+
+
 @dataclass(frozen=True)
 class DraftConfig:
     name: str = "draft_side_batch"
@@ -89,7 +93,7 @@ DRAFT_CONFIG = DraftConfig()
 
 def config4_verify(dc: DraftConfig = DRAFT_CONFIG) -> VerifyConfig:
     """The verify that follows the draft side: workload 2 with k = verify_k."""
-    base = CONFIGS[2]
+    base = WORKLOADS["batched_branches_shared_pool"]
     B = dc.M // dc.verify_k
     return dataclasses.replace(base, name="draft_side_verify", B=B, k=dc.verify_k,
                                accept_p=_decay(dc.verify_k, 0.8, 0.4), seed=dc.seed + 100)

@@ -8,7 +8,7 @@ import itertools
 import pytest
 
 from greedy_speculative_decode_spec_gb300 import _binding as bnd
-from greedy_speculative_decode_spec_gb300.workloads import CONFIGS, DRAFT_CONFIG, config4_verify
+from greedy_speculative_decode_spec_gb300.workloads import DRAFT_CONFIG, WORKLOADS, config4_verify
 
 SMEM_LIMIT = 227 * 1024
 
@@ -61,22 +61,22 @@ def test_split_geometry_does_not_depend_on_the_batch():
 def test_plans_of_the_benchmark_workloads():
     """The plans the measured numbers were taken with (see the ncu summaries)."""
     want = {
-        1: dict(copies=2, quadrants_per_copy=2, split_layout=1, split_keys=256, n_units=2 * 17, tma_rows=0),
-        2: dict(copies=4, quadrants_per_copy=1, q_rows=128, ring_stages=5, q_buffers=1, o_buffers=2,
+        "single_stream_mtp_verify": dict(copies=2, quadrants_per_copy=2, split_layout=1, split_keys=256, n_units=2 * 17, tma_rows=0),
+        "batched_branches_shared_pool": dict(copies=4, quadrants_per_copy=1, q_rows=128, ring_stages=5, q_buffers=1, o_buffers=2,
                 split_keys=1024, tma_rows=0),
-        3: dict(copies=4, quadrants_per_copy=1, q_rows=128, ring_stages=3, raw_stages=4, q_buffers=1,
+        "long_context_fp8": dict(copies=4, quadrants_per_copy=1, q_rows=128, ring_stages=3, raw_stages=4, q_buffers=1,
                 split_keys=1024, tma_rows=64),
     }
-    for cid, w in want.items():
-        c = CONFIGS[cid]
+    for name, w in want.items():
+        c = WORKLOADS[name]
         ctx = max(c.ctx) if c.ctx else c.ctx_range[1]
         max_pos = ctx + c.k + 1 + 4
         kv = bnd.kv_shape(c.num_pages or 4096, -(-max_pos // c.P), c.P, c.Hkv, c.d, c.kv_dtype == "fp8")
-        pl = bnd.spec_verify_attn_plan(kv, 1 if cid == 1 else c.B, c.k, c.Hq, max_pos)
+        pl = bnd.spec_verify_attn_plan(kv, c.B, c.k, c.Hq, max_pos)
         for key, v in w.items():
             if key == "n_units":
                 continue
-            assert pl[key] == v, (cid, key, pl[key], v)
+            assert pl[key] == v, (name, key, pl[key], v)
         assert pl["smem"] <= SMEM_LIMIT
     c4 = config4_verify(DRAFT_CONFIG)
     kv = bnd.kv_shape(c4.num_pages, 600, c4.P, c4.Hkv, c4.d)

@@ -13,16 +13,16 @@ import oracle as orc
 from gpu_harness import (DEV, assert_attn_close, assert_pools_equal, gpu_accept, gpu_attention, gpu_lmhead,
                          gpu_pool, lm_ws, oracle_pool)
 from greedy_speculative_decode_spec_gb300 import _binding as bnd
-from greedy_speculative_decode_spec_gb300.workloads import CONFIGS, bits, scaled, verify_inputs
+from greedy_speculative_decode_spec_gb300.workloads import WORKLOADS, bits, scaled, verify_inputs
 
 pytestmark = pytest.mark.gpu
 
 # Smaller cases of each workload: several tiles and splits, ragged vocab / K / page tails.
 SMALL = {
-    "tiny": CONFIGS[0],
-    "single_stream": scaled(CONFIGS[1], ctx=(2500,), V=5003, num_pages=48, seed=11),
-    "branches": scaled(CONFIGS[2], B=5, ctx_range=(20, 2100), V=3001, H=520, num_pages=1024, seed=12),
-    "long_fp8": scaled(CONFIGS[3], ctx=(1000, 2500, 60, 3100), V=2050, H=200, num_pages=140, near_tie=16,
+    "tiny": WORKLOADS["tiny_verify"],
+    "single_stream": scaled(WORKLOADS["single_stream_mtp_verify"], ctx=(2500,), V=5003, num_pages=48, seed=11),
+    "branches": scaled(WORKLOADS["batched_branches_shared_pool"], B=5, ctx_range=(20, 2100), V=3001, H=520, num_pages=1024, seed=12),
+    "long_fp8": scaled(WORKLOADS["long_context_fp8"], ctx=(1000, 2500, 60, 3100), V=2050, H=200, num_pages=140, near_tie=16,
                        seed=13),
 }
 
@@ -105,11 +105,12 @@ def test_step_parity_small(name):
     _step_parity(verify_inputs(SMALL[name]), full_oracle=True)
 
 
-@pytest.mark.parametrize("cid", [0, 1, 2, 3])
-def test_step_parity_full_size(cid):
+@pytest.mark.parametrize("name", ["tiny_verify", "single_stream_mtp_verify", "batched_branches_shared_pool",
+                                  "long_context_fp8"])
+def test_step_parity_full_size(name):
     """The full workloads, in the launch configuration the benchmark times: pools compared
     byte for byte, attention and logits on sampled outputs, ids on every row."""
-    _step_parity(verify_inputs(CONFIGS[cid]), full_oracle=(cid == 0))
+    _step_parity(verify_inputs(WORKLOADS[name]), full_oracle=(name == "tiny_verify"))
 
 
 # ---- row invariance: a row's result does not depend on the batch it is verified in ---------
@@ -259,7 +260,7 @@ def test_lmhead_edge_shapes(M, V, H):
 
 @pytest.mark.parametrize("P,d,k,B", [(1, 64, 0, 1), (4, 128, 15, 2), (256, 256, 1, 3), (1024, 64, 2, 2)])
 def test_attention_edge_shapes(P, d, k, B):
-    cfg = scaled(CONFIGS[0], B=B, k=k, P=P, d=d, Hq=4, Hkv=2, ctx=tuple([0, 1030, 5][:B]), num_pages=0,
+    cfg = scaled(WORKLOADS["tiny_verify"], B=B, k=k, P=P, d=d, Hq=4, Hkv=2, ctx=tuple([0, 1030, 5][:B]), num_pages=0,
                  permute_all_pages=False, accept_p=(0.7,) * k, V=64, H=256, seed=50 + P + k)
     vi = verify_inputs(cfg)
     _step_parity(vi, full_oracle=True)

@@ -105,8 +105,8 @@ def _replicas(rank, world):
     set by the slowest rank."""
     import bench
     import oracle as orc
-    from greedy_speculative_decode_spec_gb300.workloads import CONFIGS, verify_inputs
-    vi = verify_inputs(CONFIGS[0])
+    from greedy_speculative_decode_spec_gb300.workloads import WORKLOADS, verify_inputs
+    vi = verify_inputs(WORKLOADS["tiny_verify"])
     c = vi.cfg
     # rank r takes branch copies r, r + world, ... of a 4-branch batch built from workload 0
     drafts = np.asarray(vi.drafts, np.int32)
