@@ -101,6 +101,15 @@ def test_host_argument_errors(L):
     assert L.spec_accept(p, p, p, 1, 16, p, p, p, p, p, None, 0, None, s) == -2
     assert L.spec_accept(None, p, p, 1, 3, p, p, p, p, p, None, 0, None, s) == -1
     assert L.spec_accept(p, p, p, 1, 3, p, p, p, p, p, p, 64, None, s) == -1                  # hidden without h_out
+    # accept with stops and budget: the same checks, plus the stop list
+    acs = L.spec_accept_stop
+    assert acs(p, p, p, 0, 3, None, 0, None, p, p, p, p, p, None, None, 0, None, s) == -2
+    assert acs(p, p, p, 1, 16, None, 0, None, p, p, p, p, p, None, None, 0, None, s) == -2
+    assert acs(None, p, p, 1, 3, None, 0, None, p, p, p, p, p, None, None, 0, None, s) == -1
+    assert acs(p, p, p, 1, 3, p, 33, None, p, p, p, p, p, None, None, 0, None, s) == -2      # too many stop ids
+    assert acs(p, p, p, 1, 3, p, -1, None, p, p, p, p, p, None, None, 0, None, s) == -2
+    assert acs(p, p, p, 1, 3, None, 2, None, p, p, p, p, p, None, None, 0, None, s) == -1    # stop ids missing
+    assert acs(p, p, p, 1, 3, None, 0, None, p, p, p, p, p, None, p, 64, None, s) == -1      # hidden without h_out
     # MTP input
     assert L.spec_mtp_input_workspace(64, 100) == 0
     mw = L.spec_mtp_input_workspace(64, 256)
