@@ -10,7 +10,7 @@
 //
 // Work unit = (branch b, kv head g, split of split_keys positions). The n_q = (k+1)*G
 // query vectors that share kv head g sit on the 128 TMEM lanes (the M side of the MMAs,
-// query i on lane i); the keys of a 128-key tile are the columns:
+// query i on lane i of each copy, see below); the keys of a 128-key tile are the columns:
 //     S[q][key]  = Q . K_tile^T                 (tcgen05, fp32 in TMEM, double-buffered)
 //     O[q][d]   += P[q][key] . V_tile[key][d]   (tcgen05, fp32 in TMEM)
 // so every softmax quantity of a query (its running maximum and sum) lives in the lanes'
@@ -31,7 +31,8 @@
 //              in copies, four when the n_q queries fit one quadrant and two when they span
 //              two, so that every quadrant holds the queries and the S MMA computes each
 //              copy's scores at no extra cost (M = 128 either way); each warp takes its
-//              copy's share of the tile's key columns;
+//              copy's share of the tile's key columns (when four copies would leave the
+//              operand ring too shallow, two copies on one quadrant each, and two warps idle);
 //   warp 8     per unit: takes the next work unit, fills the page-table entries (and FP8
 //              scales) into a shared table, and loads the Q copies by 3-D TMA boxes;
 //   warp 9     issues S = Q . K^T of each tile as soon as its keys and an S buffer are there
@@ -45,7 +46,8 @@
 // cannot reach a result. Tile and split boundaries sit at fixed key positions and every
 // MMA row is computed independently of the others, so a row's output is identical
 // whatever B, k or batch it is verified in. A combine pass merges the splits of each
-// (row, head) in ascending order.
+// (row, head) in ascending order; it and this kernel are programmatic dependent launches
+// that wait on the device (griddepcontrol.wait) for the kernel before them.
 // Every pipeline wait is bounded (1 s): on a timeout the kernel raises
 // SPEC_DEVERR_TIMEOUT, lets issued copies and MMAs land, frees TMEM and exits.
 #include <cuda.h>
@@ -167,8 +169,8 @@ struct UnitInfo {
     bool bad_pos;
 };
 
-// The CTAs walk the units split-major (every (branch, head) pair's first split, then every
-// pair's second split, ...), so that a grid stride never lines up with the split count;
+// The scheduler hands out units split-major (every (branch, head) pair's first split, then
+// every pair's second split, ...), which puts each pair's short last split late;
 // `u` (the workspace slot) stays (branch, head, split)-major for the combine pass.
 __device__ __forceinline__ UnitInfo unit_info(const AttnTcParams &p, int iter, int &u) {
     UnitInfo ui;
