@@ -19,7 +19,7 @@ _HERE = Path(__file__).resolve().parent
 _SRC = _HERE / "oracle.c"
 _LIB = _HERE / "liboracle.so"
 
-ERR_PAGE, ERR_COVER, ERR_TOKEN, ERR_D2T, ERR_POS = 1, 2, 4, 8, 16
+ERR_PAGE, ERR_COVER, ERR_TOKEN, ERR_D2T, ERR_POS, ERR_TREE = 1, 2, 4, 8, 16, 32
 
 
 def build(force: bool = False) -> Path:
@@ -78,6 +78,11 @@ def lib():
         _lib.orc_lmhead_logits.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_void_p]
         _lib.orc_accept.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 5
+        _lib.orc_verify_attn_tree.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_void_p, ctypes.c_double, ctypes.c_void_p,
+                                              ctypes.c_void_p]
+        _lib.orc_accept_tree.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 6
+        _lib.orc_kv_compact.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_int]
         _lib.orc_accept_stop.argtypes = ([ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                           ctypes.c_int] + [ctypes.c_void_p] * 7)
         _lib.orc_mtp_input.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_double, ctypes.c_void_p, ctypes.c_int,
@@ -171,6 +176,42 @@ def verify_attn(kv: KvPool, pos, B: int, k: int, n_q_heads: int, q, scale: float
     s = kv._struct()
     err = lib().orc_verify_attn(ctypes.byref(s), _p(pos), B, k, n_q_heads, _p(q), float(scale), _p(out))
     return out, int(err)
+
+
+def chain_masks(B: int, k: int) -> np.ndarray:
+    """The ancestor masks of a chain: row j reads verify slots 0..j."""
+    return np.tile(((1 << (np.arange(k + 1) + 1)) - 1).astype(np.int32), B).reshape(B, k + 1)
+
+
+def verify_attn_tree(kv: KvPool, pos, B: int, k: int, n_q_heads: int, q, scale: float, anc_mask):
+    """Tree verify attention: row j of branch b reads the committed prefix [0, pos_b) and
+    the verify slots pos_b + i with bit i of anc_mask[b][j] set. fp64 [R][Hq][d], errors."""
+    pos, q, m = _c(pos, np.int32), _c(q, np.uint16), _c(np.asarray(anc_mask).reshape(-1), np.int32)
+    R = B * (k + 1)
+    assert m.size == R
+    out = np.empty((R, n_q_heads, kv.head_dim), dtype=np.float64)
+    s = kv._struct()
+    err = lib().orc_verify_attn_tree(ctypes.byref(s), _p(pos), B, k, n_q_heads, _p(q), float(scale), _p(m), _p(out))
+    return out, int(err)
+
+
+def accept_tree(drafts, ids, pos, parent, B: int, k: int):
+    """Greedy tree walk: tokens [B][k+1], n, accepted, new_pos, next, path [B][k+1], errors."""
+    drafts = _c(np.asarray(drafts).reshape(B, k) if k > 0 else np.zeros((B, 1)), np.int32)
+    ids, pos = _c(ids, np.int32), _c(pos, np.int32)
+    parent = _c(np.asarray(parent).reshape(B, k + 1), np.int32)
+    tokens, path = np.empty((B, k + 1), np.int32), np.empty((B, k + 1), np.int32)
+    n, a, npos, nxt = (np.empty(B, np.int32) for _ in range(4))
+    err = lib().orc_accept_tree(_p(drafts), _p(ids), _p(pos), _p(parent), B, k, _p(tokens), _p(n), _p(a),
+                                _p(npos), _p(nxt), _p(path))
+    return tokens, n, a, npos, nxt, path, int(err)
+
+
+def kv_compact(kv: KvPool, pos, path, accepted, B: int, k: int) -> int:
+    """Move each accepted row's K/V to the contiguous slot of its rank (in place)."""
+    pos, path, acc = _c(pos, np.int32), _c(np.asarray(path).reshape(B, k + 1), np.int32), _c(accepted, np.int32)
+    s = kv._struct()
+    return int(lib().orc_kv_compact(ctypes.byref(s), _p(pos), _p(path), _p(acc), B, k))
 
 
 def verify_attn_items(kv: KvPool, pos, B: int, k: int, n_q_heads: int, q, scale: float, items):

@@ -299,6 +299,71 @@ int orc_verify_attn(const orc_kv *kv, const int32_t *pos, int B, int k, int n_q_
     return err;
 }
 
+/* ---- tree / star verify (a next row) -------------------------------------------------
+ * DSSD-dev `_set_rows` / `_star_cycle`: a tree row reads the contiguous committed prefix
+ * (keys t < cl at their own index) and then the slots of its own path; chains are the case
+ * slot = position. Here the k+1 verify rows of branch b own the slots pos_b .. pos_b+k
+ * (row j writes slot pos_b+j), and row j's path is given as a bit mask over them:
+ * anc_mask[b][j] bit i set = row j reads slot pos_b+i (its ancestors and itself). Keys
+ * are visited in ascending slot order, as in attn_one; a chain's masks (bits 0..j) give
+ * attn_one's key set exactly. */
+static int attn_keys(const orc_kv *kv, int b, const int32_t *keys, int n_keys, int g, const uint16_t *q,
+                     double scale, double *o, double *s) {
+    const int d = kv->head_dim;
+    double mx = -INFINITY;
+    for (int i = 0; i < n_keys; ++i) {
+        int page, slot;
+        int e = locate(kv, b, keys[i], &page, &slot);
+        if (e) return e;
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c) dot += orc_bf16_to_double(q[c]) * kv_value(kv, 0, page, g, slot, c);
+        s[i] = scale * dot;
+        if (s[i] > mx) mx = s[i];
+    }
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    double den = 0.0;
+    for (int i = 0; i < n_keys; ++i) {
+        int page, slot;
+        locate(kv, b, keys[i], &page, &slot);
+        double w = exp(s[i] - mx);
+        den += w;
+        for (int c = 0; c < d; ++c) o[c] += w * kv_value(kv, 1, page, g, slot, c);
+    }
+    for (int c = 0; c < d; ++c) o[c] /= den;
+    return 0;
+}
+
+int orc_verify_attn_tree(const orc_kv *kv, const int32_t *pos, int B, int k, int n_q_heads,
+                         const uint16_t *q, double scale, const int32_t *anc_mask, double *out) {
+    const int d = kv->head_dim, Hq = n_q_heads, G = n_q_heads / kv->n_kv_heads;
+    const int R = B * (k + 1);
+    int err = 0;
+    int maxp = 0;
+    for (int b = 0; b < B; ++b)
+        if (pos[b] + k + 1 > maxp) maxp = pos[b] + k + 1;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int item = 0; item < R * Hq; ++item) {
+        int r = item / Hq, h = item % Hq, b = r / (k + 1);
+        double *s = (double *)malloc(sizeof(double) * (size_t)(maxp + 1));
+        int32_t *keys = (int32_t *)malloc(sizeof(int32_t) * (size_t)(maxp + 1));
+        double *o = out + ((size_t)r * Hq + h) * d;
+        int e = pos[b] < 0 ? ORC_ERR_POS : 0, n = 0;
+        if (!e) {
+            for (int t = 0; t < pos[b]; ++t) keys[n++] = t;
+            for (int i = 0; i <= k; ++i)
+                if ((anc_mask[r] >> i) & 1) keys[n++] = pos[b] + i;
+            e = n ? attn_keys(kv, b, keys, n, h / G, q + ((size_t)r * Hq + h) * d, scale, o, s) : ORC_ERR_POS;
+        }
+        if (e) {
+            for (int c = 0; c < d; ++c) o[c] = NAN;
+            err |= e;
+        }
+        free(keys);
+        free(s);
+    }
+    return err;
+}
+
 /* A chosen subset of (row, head) outputs, for full-size checks:
  * items[i] = r * Hq + h; out fp64 [n_items][d]. */
 int orc_verify_attn_items(const orc_kv *kv, const int32_t *pos, int B, int k, int n_q_heads,
@@ -478,6 +543,84 @@ void orc_accept_stop(const int32_t *drafts, const int32_t *ids, const int32_t *p
         out_next[b] = n > 0 ? run[n - 1] : -1;
         out_done[b] = stopped || capped;
     }
+}
+
+/* Tree acceptance (greedy). DSSD-dev `_star_cycle`: a child is accepted when its token is
+ * the target's choice at its parent (the root's argmax for a depth-1 star), and the
+ * committed tokens are that choice followed by the accepted child's own choice. Here the
+ * k+1 rows of branch b form a tree: row 0 is the root (the fed token), row j >= 1 carries
+ * draft token drafts[b][j-1] and has parent[b][j] < j. From the root, the walk moves to the
+ * lowest-numbered child whose token equals the current row's argmax ids[b(k+1)+cur], and
+ * stops when none does. Emitted: the accepted drafts in walk order, then the last row's
+ * argmax (the bonus); path[b][0] = 0 and path[b][i] = the i-th accepted row, -1 after.
+ * A parent array with parent[j] outside [0, j) gives an error bit and no walk past it.
+ * With parent[j] = j-1 this is orc_accept. */
+#define ORC_ERR_TREE 32
+int orc_accept_tree(const int32_t *drafts, const int32_t *ids, const int32_t *pos, const int32_t *parent,
+                    int B, int k, int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted,
+                    int32_t *out_pos, int32_t *out_next, int32_t *out_path) {
+    int err = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t *target = ids + (size_t)b * (k + 1);
+        const int32_t *par = parent + (size_t)b * (k + 1);
+        int32_t *emit = out_tokens + (size_t)b * (k + 1);
+        int32_t *path = out_path + (size_t)b * (k + 1);
+        for (int j = 1; j <= k; ++j)
+            if (par[j] < 0 || par[j] >= j) err |= ORC_ERR_TREE;
+        int cur = 0, a = 0;
+        path[0] = 0;
+        for (;;) {
+            int next = -1;
+            for (int c = cur + 1; c <= k; ++c)
+                if (par[c] == cur && drafts[(size_t)b * k + c - 1] == target[cur]) { next = c; break; }
+            if (next < 0) break;
+            emit[a] = drafts[(size_t)b * k + next - 1];
+            path[++a] = next;
+            cur = next;
+        }
+        emit[a] = target[cur];
+        for (int j = a + 1; j <= k; ++j) { emit[j] = -1; path[j] = -1; }
+        out_n[b] = a + 1;
+        out_accepted[b] = a;
+        out_pos[b] = pos[b] + a + 1;
+        out_next[b] = target[cur];
+    }
+    return err;
+}
+
+/* KV compaction after a tree walk (DSSD-dev `_star_cycle`: the accepted child's K/V is
+ * copied to slot pos0+1). Accepted row path[b][i] (written at slot pos_b + path[b][i])
+ * moves to slot pos_b + i, for i = 1..accepted[b], in ascending i: a path's rows increase,
+ * so a source is never overwritten before it is read. bf16 pools copy bits; FP8 pools
+ * decode with the source page's scale and re-encode with the destination page's scale. */
+int orc_kv_compact(const orc_kv *kv, const int32_t *pos, const int32_t *path, const int32_t *accepted, int B,
+                   int k) {
+    int err = 0;
+    const int Hkv = kv->n_kv_heads, d = kv->head_dim;
+    for (int b = 0; b < B; ++b)
+        for (int i = 1; i <= accepted[b]; ++i) {
+            const int src_row = path[(size_t)b * (k + 1) + i];
+            if (src_row == i) continue;
+            int sp, ss, dp, ds;
+            int e = locate(kv, b, pos[b] + src_row, &sp, &ss) | locate(kv, b, pos[b] + i, &dp, &ds);
+            if (e) { err |= e; continue; }
+            for (int g = 0; g < Hkv; ++g) {
+                size_t src = pool_index(kv, sp, g, ss), dst = pool_index(kv, dp, g, ds);
+                if (kv->kv_dtype == 0) {
+                    memcpy((uint16_t *)kv->k_pool + dst, (uint16_t *)kv->k_pool + src, (size_t)d * 2);
+                    memcpy((uint16_t *)kv->v_pool + dst, (uint16_t *)kv->v_pool + src, (size_t)d * 2);
+                } else {
+                    for (int c = 0; c < d; ++c) {
+                        double xk = kv_value(kv, 0, sp, g, ss, c), xv = kv_value(kv, 1, sp, g, ss, c);
+                        ((uint8_t *)kv->k_pool)[dst + c] =
+                            orc_e4m3_encode((float)xk / kv->k_scale[(size_t)dp * Hkv + g]);
+                        ((uint8_t *)kv->v_pool)[dst + c] =
+                            orc_e4m3_encode((float)xv / kv->v_scale[(size_t)dp * Hkv + g]);
+                    }
+                }
+            }
+        }
+    return err;
 }
 
 /* ------------------------------------------------------------------------------------
