@@ -83,6 +83,8 @@ def lib():
                                               ctypes.c_void_p]
         _lib.orc_accept_tree.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 6
         _lib.orc_kv_compact.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_int]
+        _lib.orc_accept_sample.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int] * 3 + [ctypes.c_double]
+                                           + [ctypes.c_void_p] * 7)
         _lib.orc_accept_stop.argtypes = ([ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                           ctypes.c_int] + [ctypes.c_void_p] * 7)
         _lib.orc_mtp_input.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_double, ctypes.c_void_p, ctypes.c_int,
@@ -205,6 +207,22 @@ def accept_tree(drafts, ids, pos, parent, B: int, k: int):
     err = lib().orc_accept_tree(_p(drafts), _p(ids), _p(pos), _p(parent), B, k, _p(tokens), _p(n), _p(a),
                                 _p(npos), _p(nxt), _p(path))
     return tokens, n, a, npos, nxt, path, int(err)
+
+
+def accept_sample(drafts, logits, q, pos, B: int, k: int, temperature: float, u_acc, u_res):
+    """Speculative sampling acceptance with the random numbers given: tokens, n, accepted,
+    new_pos, next. logits fp32 [B*(k+1)][V]; q fp32 [B][k][V]; u_acc [B][k]; u_res [B]."""
+    logits = _c(logits, np.float32)
+    V = logits.shape[-1]
+    drafts = _c(np.asarray(drafts).reshape(B, k) if k > 0 else np.zeros((B, 1)), np.int32)
+    q = _c(np.asarray(q).reshape(B, k, V) if k > 0 else np.zeros((B, 1, V)), np.float32)
+    u_acc = _c(np.asarray(u_acc).reshape(B, k) if k > 0 else np.zeros((B, 1)), np.float32)
+    pos, u_res = _c(pos, np.int32), _c(u_res, np.float32)
+    tokens = np.empty((B, k + 1), np.int32)
+    n, a, npos, nxt = (np.empty(B, np.int32) for _ in range(4))
+    lib().orc_accept_sample(_p(drafts), _p(logits), _p(q), _p(pos), B, k, V, float(temperature), _p(u_acc), _p(u_res),
+                            _p(tokens), _p(n), _p(a), _p(npos), _p(nxt))
+    return tokens, n, a, npos, nxt
 
 
 def kv_compact(kv: KvPool, pos, path, accepted, B: int, k: int) -> int:

@@ -623,6 +623,83 @@ int orc_kv_compact(const orc_kv *kv, const int32_t *pos, const int32_t *path, co
     return err;
 }
 
+/* Speculative sampling acceptance (the next row f4). oxinfer `speculative_accept`: a draft d
+ * drawn from q is kept with probability min(1, p(d) / q(d)), otherwise replaced by a token
+ * drawn from the normalised max(0, p - q) (from p when that is all zero); DSSD-dev
+ * `_sample_verify`: walk the chain, stop at the first rejection, and sample the bonus from
+ * the last row's p after a full acceptance. The random numbers are inputs here (u in
+ * [0, 1)): u_acc[b][i] for draft i's test, u_res[b] for the one token drawn at the end.
+ * p_j = softmax(logits[b(k+1)+j] / temperature) in fp64; q [B][k][V] are the draft
+ * distributions (probabilities). Drawing t from a non-negative weight vector w uses the
+ * inverse CDF in index order: the smallest t whose running sum exceeds u * sum(w). */
+static int draw_index(const double *w, int V, double u) {
+    double tot = 0.0;
+    for (int t = 0; t < V; ++t) tot += w[t];
+    double c = 0.0, lim = u * tot;
+    for (int t = 0; t < V; ++t) {
+        c += w[t];
+        if (c > lim) return t;
+    }
+    for (int t = V - 1; t >= 0; --t)
+        if (w[t] > 0.0) return t;
+    return 0;
+}
+
+static void softmax_t(const float *z, int V, double temperature, double *p) {
+    double mx = -INFINITY;
+    for (int t = 0; t < V; ++t)
+        if ((double)z[t] / temperature > mx) mx = (double)z[t] / temperature;
+    double den = 0.0;
+    for (int t = 0; t < V; ++t) {
+        p[t] = exp((double)z[t] / temperature - mx);
+        den += p[t];
+    }
+    for (int t = 0; t < V; ++t) p[t] /= den;
+}
+
+void orc_accept_sample(const int32_t *drafts, const float *logits, const float *q, const int32_t *pos, int B,
+                       int k, int V, double temperature, const float *u_acc, const float *u_res,
+                       int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted, int32_t *out_pos,
+                       int32_t *out_next) {
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int b = 0; b < B; ++b) {
+        double *p = (double *)malloc(sizeof(double) * (size_t)V);
+        double *w = (double *)malloc(sizeof(double) * (size_t)V);
+        int32_t *emit = out_tokens + (size_t)b * (k + 1);
+        int a = 0, last = -1;
+        for (int i = 0; i < k; ++i) {
+            softmax_t(logits + ((size_t)b * (k + 1) + i) * V, V, temperature, p);
+            const int d = drafts[(size_t)b * k + i];
+            const float *qi = q + ((size_t)b * k + i) * V;
+            const double pd = p[d], qd = (double)qi[d];
+            if (pd >= qd || (double)u_acc[(size_t)b * k + i] < pd / qd) {
+                emit[a++] = d;
+                continue;
+            }
+            int any = 0;
+            for (int t = 0; t < V; ++t) {
+                w[t] = p[t] - (double)qi[t];
+                if (w[t] < 0.0) w[t] = 0.0;
+                if (w[t] > 0.0) any = 1;
+            }
+            last = draw_index(any ? w : p, V, (double)u_res[b]);
+            break;
+        }
+        if (last < 0) {  /* every draft kept: the bonus from the last row's p */
+            softmax_t(logits + ((size_t)b * (k + 1) + a) * V, V, temperature, p);
+            last = draw_index(p, V, (double)u_res[b]);
+        }
+        emit[a] = last;
+        for (int j = a + 1; j <= k; ++j) emit[j] = -1;
+        out_n[b] = a + 1;
+        out_accepted[b] = a;
+        out_pos[b] = pos[b] + a + 1;
+        out_next[b] = last;
+        free(p);
+        free(w);
+    }
+}
+
 /* ------------------------------------------------------------------------------------
  * MTP draft-head input
  * ---------------------------------------------------------------------------------- */
