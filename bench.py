@@ -3,11 +3,17 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-all]
 
-A step = one pass of the whole hot path on one batch of synthetic input:
-KV append -> verify attention -> LM head + argmax -> chain acceptance -> the next
-draft step's MTP input, on one stream (captured in a CUDA graph).
-The headline workload is the single-stream MTP verify (B=1, k=4, H=2048, 16/2 heads,
-d=256, ctx 4096, P=64, V=151936). The other workloads are reported under "all_configs".
+A step = one pass of the verify hot path on one batch of synthetic input:
+KV append -> verify attention -> LM head + argmax -> chain acceptance, on one stream
+(captured in a CUDA graph). The draft-side workload (4) adds the MTP input and the trimmed
+draft head in front of its verify. The same step followed by the next draft step's MTP
+input is reported separately ("us_per_step_with_mtp_input").
+The headline workload is the long-context FP8 verify (B=4, k=3, contexts 32K..128K, 40/8
+heads, d=128, E4M3 pages of 64, H=5120, V=151936): the largest single-GPU workload, with
+the most bytes per step. The other workloads are reported under "all_configs".
+
+--only attn|lmhead runs just that call of the workload (W + K plain launches, no graph):
+the command the ncu summaries under profiles/ are taken with.
 
 --impl reference times the CPU oracle (the plain fp64 reference) on the same workload,
 one bounded sample per step, on this host's cores.
@@ -31,9 +37,12 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one LM-head launch, from one
-# ncu capture of the unchanged kernel on that workload; None where no capture was taken.
-LMHEAD_TRAFFIC = {"single_stream_mtp_verify": 622430720 + 3319040}
+METRIC = "verified rows/s (B*(k+1) rows per verify step); us per verify step; HBM GB/s of the bandwidth kernels"
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the kernel as it
+# stands, from one ncu capture on that workload (profiles/); absent where none was taken.
+LMHEAD_TRAFFIC: dict = {}
+ATTN_TRAFFIC: dict = {}
 
 
 def _peaks():
@@ -236,34 +245,51 @@ def run_ours(args):
     def log(msg):
         print(f"[bench] {msg}", file=sys.stderr, flush=True)
 
-    def measure(cid, steps, warmup, with_e2e=False):
-        log(f"workload {cid}: set-up")
-        w = _setup_workload(cid, dev)
+    def calls(w):
+        """The step's calls of workload w: (verify step, attention alone, LM head alone)."""
         step, inp, c = w["step"], w["inputs"], w["cfg"]
-        ds = DraftStage(w["draft"], dev) if w["draft"] is not None else None
+        ds = w["ds"]
+        o, kv = step.out, step.kv
 
-        def one():
+        def one(with_mtp=False):
             if ds is not None:
                 ds.run()
-            step.run(inp["pos"], inp["q"], inp["k_new"], inp["v_new"], inp["hidden"], inp["drafts"])
+            step.run(inp["pos"], inp["q"], inp["k_new"], inp["v_new"], inp["hidden"], inp["drafts"],
+                     with_mtp=with_mtp)
 
+        def attn():
+            bnd.spec_verify_attn(kv.desc, inp["pos"], c.B, c.k, c.Hq, inp["q"], step.scale, o.attn, step.attn_ws,
+                                 step.max_pos, o.dev_err)
+
+        def head():
+            bnd.spec_lmhead_argmax(inp["hidden"], step.W, o.ids, step.head_ws, max_logit=o.max_logit,
+                                   dev_err=o.dev_err)
+        return one, attn, head
+
+    def setup(cid):
+        log(f"workload {cid}: set-up")
+        w = _setup_workload(cid, dev)
+        w["ds"] = DraftStage(w["draft"], dev) if w["draft"] is not None else None
+        return w
+
+    def measure(cid, steps, warmup, with_e2e=False, with_clocks=False):
+        w = setup(cid)
+        step, inp, c = w["step"], w["inputs"], w["cfg"]
+        one, attn, head = calls(w)
         log(f"workload {cid}: eager steps")
         for _ in range(2):
             one()
         torch.cuda.synchronize()
         assert int(step.out.dev_err.item()) == 0, "device error during the step"
         log(f"workload {cid}: graph")
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            one()
-        torch.cuda.synchronize()
+        graph = _graph_of(one)
         for _ in range(warmup):
             graph.replay()
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        sampler = ClockSampler(local) if cid == args.config else None
+        sampler = ClockSampler(local) if with_clocks else None
         if sampler:
             sampler.start()
         t_steps = _time_region(graph.replay, steps, flush, stream)
@@ -271,24 +297,28 @@ def run_ours(args):
         clocks = sampler.stop() if sampler else None
         if world > 1:
             dist.barrier()
+        del graph
         log(f"workload {cid}: per-kernel timing")
         # per-call times of the two bandwidth calls (graph replays: same stream, same flush)
-        o, kv = step.out, step.kv
-        g_attn = _graph_of(lambda: bnd.spec_verify_attn(kv.desc, inp["pos"], c.B, c.k, c.Hq, inp["q"], step.scale,
-                                                        o.attn, step.attn_ws, step.max_pos, o.dev_err))
-        g_head = _graph_of(lambda: bnd.spec_lmhead_argmax(inp["hidden"], step.W, o.ids, step.head_ws,
-                                                          max_logit=o.max_logit, dev_err=o.dev_err))
+        g_attn, g_head = _graph_of(attn), _graph_of(head)
         t_attn = _time_region(g_attn.replay, steps, flush, stream)
         t_head = _time_region(g_head.replay, steps, flush, stream)
         del g_attn, g_head
-        res = dict(cfg=c, ms=statistics.median(t_steps), ms_mean=statistics.mean(t_steps), t_attn=statistics.median(t_attn),
-                   t_head=statistics.median(t_head), kv_bytes=w["kv_bytes"], w_bytes=w["w_bytes"], clocks=clocks,
-                   launches=step.launches_per_step + (4 if ds is not None else 0))
+        # the same step followed by the next draft step's MTP input
+        g_mtp = _graph_of(lambda: one(with_mtp=True))
+        for _ in range(warmup):
+            g_mtp.replay()
+        t_mtp = _time_region(g_mtp.replay, steps, flush, stream)
+        del g_mtp
+        res = dict(cfg=c, ms=statistics.median(t_steps), t_attn=statistics.median(t_attn),
+                   t_head=statistics.median(t_head), ms_mtp=statistics.median(t_mtp), kv_bytes=w["kv_bytes"],
+                   w_bytes=w["w_bytes"], clocks=clocks,
+                   launches=step.launches_verify + (4 if w["ds"] is not None else 0))
         if with_e2e:
             log(f"workload {cid}: end to end")
             res["e2e"] = measure_e2e(step, inp, steps, flush)
         log(f"workload {cid}: done")
-        del w, step, graph
+        del w, step
         torch.cuda.empty_cache()
         return res
 
@@ -306,7 +336,8 @@ def run_ours(args):
         def one():
             for n in names_in:
                 dev_in[n].copy_(host[n], non_blocking=True)
-            step.run(dev_in["pos"], dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["hidden"], dev_in["drafts"])
+            step.run(dev_in["pos"], dev_in["q"], dev_in["k_new"], dev_in["v_new"], dev_in["hidden"], dev_in["drafts"],
+                     with_mtp=False)
             for h, t in zip(host_out, outs):
                 h.copy_(t, non_blocking=True)
 
@@ -316,46 +347,66 @@ def run_ours(args):
         ts = _time_region(one, steps, flush, stream)
         return dict(ms=statistics.median(ts), h2d=h2d, d2h=d2h)
 
-    main = measure(args.config, args.steps, args.warmup, with_e2e=True)
+    if args.only:
+        # one call of the workload, W + K plain launches (the command ncu captures use)
+        w = setup(args.config)
+        _, attn, head = calls(w)
+        fn = attn if args.only == "attn" else head
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ts = _time_region(fn, args.steps, flush, stream)
+        assert int(w["step"].out.dev_err.item()) == 0, "device error"
+        print(json.dumps({"only": args.only, "workload": w["cfg"].name, "us": round(statistics.median(ts) * 1e3, 2),
+                          "calls": args.warmup + args.steps}), flush=True)
+        return
+
+    def kernel_entry(name, bytes_, ms, workload, traffic):
+        gbs = bytes_ / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "kernel": name, "achieved": round(gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(gbs / hbm_peak, 4), "peak_kind": peak_kind, "algorithmic_bytes": bytes_,
+                "kernel_us": round(ms * 1e3, 2), "traffic": traffic.get(workload)}
+
+    main = measure(args.config, args.steps, args.warmup, with_e2e=True, with_clocks=True)
     c = main["cfg"]
     rows = c.B * (c.k + 1)
     ms_max, value = replica_rate(main["ms"], rows, world, dev)
-    head_gbs = main["w_bytes"] / (main["t_head"] * 1e-3) / 1e9
-    attn_gbs = main["kv_bytes"] / (main["t_attn"] * 1e-3) / 1e9
     others = {}
     if args.all and rank == 0:
-        for cid in (0, 2, 3, 4):
+        for cid in (0, 1, 2, 3, 4):
             if cid == args.config:
                 continue
             r = measure(cid, max(5, min(args.steps, 20)), max(3, args.warmup))
             rc = r["cfg"]
             R = rc.B * (rc.k + 1)
+            a = kernel_entry("spec_verify_attn", r["kv_bytes"], r["t_attn"], rc.name, ATTN_TRAFFIC)
+            h = kernel_entry("spec_lmhead_argmax", r["w_bytes"], r["t_head"], rc.name, LMHEAD_TRAFFIC)
             others[str(cid)] = {
                 "workload": rc.name, "us_per_step": round(r["ms"] * 1e3, 2), "rows_per_s": round(R / (r["ms"] * 1e-3), 1),
-                "attn_us": round(r["t_attn"] * 1e3, 2), "attn_gbs": round(r["kv_bytes"] / (r["t_attn"] * 1e-3) / 1e9, 1),
-                "attn_frac": round(r["kv_bytes"] / (r["t_attn"] * 1e-3) / 1e9 / hbm_peak, 4),
-                "lmhead_us": round(r["t_head"] * 1e3, 2), "lmhead_gbs": round(r["w_bytes"] / (r["t_head"] * 1e-3) / 1e9, 1),
-                "lmhead_frac": round(r["w_bytes"] / (r["t_head"] * 1e-3) / 1e9 / hbm_peak, 4),
-                "kv_bytes": r["kv_bytes"], "w_bytes": r["w_bytes"]}
+                "us_per_step_with_mtp_input": round(r["ms_mtp"] * 1e3, 2),
+                "attn_us": a["kernel_us"], "attn_gbs": a["achieved"], "attn_frac": a["frac"], "attn_traffic": a["traffic"],
+                "lmhead_us": h["kernel_us"], "lmhead_gbs": h["achieved"], "lmhead_frac": h["frac"],
+                "lmhead_traffic": h["traffic"], "kv_bytes": r["kv_bytes"], "w_bytes": r["w_bytes"]}
     if rank != 0:
         return
     e2e = main["e2e"]
+    attn_e = kernel_entry("spec_verify_attn", main["kv_bytes"], main["t_attn"], c.name, ATTN_TRAFFIC)
+    head_e = kernel_entry("spec_lmhead_argmax", main["w_bytes"], main["t_head"], c.name, LMHEAD_TRAFFIC)
+    # the dominant kernel (the larger share of the step) is the line's roofline
+    dom, sec = (head_e, attn_e) if main["t_head"] >= main["t_attn"] else (attn_e, head_e)
     line = {
-        "metric": "verified rows/s (B*(k+1) rows per verify step); us per verify step; HBM GB/s of the LM head",
-        "value": round(value, 1), "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms_max, 4), "us_per_step": round(ms_max * 1e3, 2), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init weights)",
+        "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max, 4), "us_per_step": round(ms_max * 1e3, 2),
+        "us_per_step_with_mtp_input": round(main["ms_mtp"] * 1e3, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": c.kv_dtype if c.kv_dtype == "bf16" else "bf16+e4m3",
+        "data": "synthetic (seeded; random-init weights)",
         "config": {"workload": c.name, "B": c.B, "k": c.k, "rows": rows, "H": c.H, "q_heads": c.Hq, "kv_heads": c.Hkv,
-                   "head_dim": c.d, "context": list(c.ctx), "page_size": c.P, "vocab": c.V, "kv_dtype": c.kv_dtype,
+                   "head_dim": c.d, "context": list(c.ctx) or list(c.ctx_range), "page_size": c.P, "vocab": c.V,
+                   "kv_dtype": c.kv_dtype, "step": "kv append + verify attention + LM head argmax + accept",
                    "parallelism": f"replicas x{world}", "graph": "CUDA graph per step",
                    "l2": "flushed before every timed step (512 MiB write, then 256 MiB read so that the dirty lines are written back before the timed region)"},
-        "roofline": {"bound": "hbm", "kernel": "spec_lmhead_argmax", "achieved": round(head_gbs, 1),
-                     "peak": hbm_peak, "unit": "GB/s", "frac": round(head_gbs / hbm_peak, 4),
-                     "peak_kind": peak_kind, "algorithmic_bytes": main["w_bytes"], "kernel_us": round(main["t_head"] * 1e3, 2),
-                     "traffic": LMHEAD_TRAFFIC.get(c.name)},
-        "attention": {"kernel": "spec_verify_attn", "achieved": round(attn_gbs, 1), "unit": "GB/s",
-                      "frac": round(attn_gbs / hbm_peak, 4), "kernel_us": round(main["t_attn"] * 1e3, 2),
-                      "algorithmic_bytes": main["kv_bytes"]},
+        "roofline": dom,
+        "roofline_other": sec,
         "e2e": {"value": round(rows / (e2e["ms"] * 1e-3), 1), "unit": "rows/s", "ms_per_step": round(e2e["ms"], 4),
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
         "gpu_launches": main["launches"] * args.steps,
@@ -436,8 +487,7 @@ def run_reference(args):
         ts.append(time.perf_counter() - t0)
     sec = statistics.median(ts)
     value = 1.0 / sec  # one verify row per sample
-    line = {"impl": "reference", "metric": "verified rows/s (B*(k+1) rows per verify step); us per verify step; "
-            "HBM GB/s of the LM head", "value": round(value, 4), "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "rows/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
             "config": {"workload": c.name, "B": c.B, "k": c.k, "rows_per_sample": 1},
@@ -453,7 +503,8 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--config", type=int, default=3, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--only", choices=["attn", "lmhead"], default=None)
     ap.add_argument("--no-all", dest="all", action="store_false")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)

@@ -12,11 +12,12 @@
 // (a ballot) is the accepted count a. Lanes 0..k write the emitted tokens.
 //
 // With a stop set and a budget (spec_accept_stop): the run drafts[0..a) ++ [ids[a]] is
-// cut right after its first token in the stop set (flashrt-structures speculative loop:
-// the stop token stays; memra-engine spec.rs `Spec::body_inner`: a small stop-id buffer,
-// -1 = unused entry) and then to at most the branch's budget (DSSD-dev `_commit`: the
-// generation limit). Lane i <= a tests run token i against the stop ids; a second ballot
-// gives the first stop.
+// cut right after its first token in the stop set and then to at most the branch's budget
+// (DSSD-dev dssd/fast.py, `_commit`: the committed tokens are appended until the stop rule
+// fires on one, which is kept, or the generation limit is reached; span-02
+// engine/crates/model/src/spec.rs, `Spec::body_inner`: a small stop-id buffer whose unused
+// entries are -1, and a token limit). Lane i <= a tests run token i against the stop ids;
+// a second ballot gives the first stop.
 #include <climits>
 
 #include "common.cuh"

@@ -82,10 +82,13 @@ class VerifyStep:
         if mtp is not None:
             self.mtp_ws = torch.zeros(bnd.spec_mtp_input_workspace(B, self.H), dtype=torch.uint8, device=device)
             self.out.mtp_x = torch.empty((B, self.H), dtype=torch.bfloat16, device=device)
-        # append 1, attention 2 (split + combine), LM head 1, accept 1, MTP input 3
-        self.launches_per_step = 5 + (3 if mtp is not None else 0)
+        # append 1, attention 1, LM head 1, accept 1; the MTP input adds 3
+        self.launches_verify = 4
+        self.launches_mtp = 3 if mtp is not None else 0
 
-    def run(self, pos, q, k_new, v_new, hidden, drafts, stream=None) -> StepOutputs:
+    def run(self, pos, q, k_new, v_new, hidden, drafts, stream=None, with_mtp: bool = True) -> StepOutputs:
+        """The verify step's calls on `stream`; with_mtp adds the next draft step's MTP input
+        (when the step was built with one)."""
         o, kv = self.out, self.kv
         bnd.spec_kv_append(kv.desc, pos, self.B, self.k, k_new, v_new, o.dev_err, stream)
         bnd.spec_verify_attn(kv.desc, pos, self.B, self.k, self.Hq, q, self.scale, o.attn, self.attn_ws,
@@ -94,7 +97,7 @@ class VerifyStep:
                                stream=stream)
         bnd.spec_accept(drafts, o.ids, pos, self.B, self.k, o.tokens, o.n, o.accepted, o.new_pos, o.next_tok,
                         hidden=hidden, h_out=o.h_next, stream=stream)
-        if self.mtp is not None:
+        if self.mtp is not None and with_mtp:
             m = self.mtp
             bnd.spec_mtp_input(o.next_tok, m["E"], o.h_next, m["g_emb"], m["g_hid"], m["eps"], m["W_fc"], o.mtp_x,
                                self.mtp_ws, o.dev_err, stream)

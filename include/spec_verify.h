@@ -264,10 +264,10 @@ int spec_accept(const int32_t *drafts, const int32_t *ids, const int32_t *pos, i
  *   next = the last emitted token (-1 when n == 0)
  *   done = the emitted run ends on a stop token, or n reached budget[b]
  * With no stop ids and no budget it returns exactly what spec_accept returns.
- * Sources: flashrt-structures speculative decode loop (the emitted tokens are cut after
- * the first stop token, which stays); memra-engine spec.rs, `Spec::body_inner` (the
- * acceptance kernel takes a stop-id buffer whose unused entries are -1, and a token
- * limit); DSSD-dev `_commit` (a cycle's tokens are also cut at the generation limit).
+ * Sources: DSSD-dev dssd/fast.py, `_commit` (a cycle's committed tokens are appended until
+ * the stop rule fires on one, which is kept, or the output reaches the generation limit);
+ * span-02 engine/crates/model/src/spec.rs, `Spec::body_inner` (the device acceptance call
+ * takes a stop-id buffer whose unused entries are -1, and a token limit).
  *   stop_ids   device int32 [n_stop] (entries < 0 are unused); NULL when n_stop == 0;
  *              0 <= n_stop <= SPEC_MAX_STOP
  *   budget     device int32 [B]: tokens branch b may still emit, or NULL (no limit)

@@ -492,11 +492,12 @@ void orc_accept(const int32_t *drafts, const int32_t *ids, const int32_t *pos, i
     }
 }
 
-/* Stop tokens and a generation budget on top of the greedy run. memra-engine spec.rs,
- * `Spec::body_inner`: the acceptance kernel takes a small stop-id buffer (-1 = unused
- * entry) and a token limit; flashrt-structures speculative loop: the emitted tokens are
- * cut right after the first stop token (the stop token itself is kept); DSSD-dev
- * `_commit`: a cycle's tokens are also cut at the generation limit. The run of branch b
+/* Stop tokens and a generation budget on top of the greedy run. DSSD-dev dssd/fast.py,
+ * `_commit`: a cycle's committed tokens are appended one by one and the loop breaks right
+ * after the first token the stop rule fires on (that token is kept), or once the output
+ * reaches the generation limit max_new; span-02 engine/crates/model/src/spec.rs,
+ * `Spec::body_inner`: the device acceptance call takes a small stop-id buffer (initialised
+ * to -1, i.e. unused entries) and a token limit (1 << 30 = none). The run of branch b
  * (drafts[0..a) then ids[b(k+1)+a]) is cut after its first token that is in the stop
  * set, then to at most budget[b] tokens (budget NULL: no limit; a negative entry counts
  * as 0). n = tokens kept, accepted = drafts among them, new_pos = pos + n, next = the

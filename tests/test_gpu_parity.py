@@ -35,7 +35,7 @@ def _lib():
     bnd.lib()
 
 
-def _step_parity(vi, full_oracle: bool, n_items=24, n_rows=4):
+def _step_parity(vi, full_oracle: bool, n_items=24, n_rows=32):
     c = vi.cfg
     B, k, Hq, d = c.B, c.k, c.Hq, c.d
     okv = oracle_pool(vi)
@@ -58,10 +58,14 @@ def _step_parity(vi, full_oracle: bool, n_items=24, n_rows=4):
         assert oe == 0
         assert_attn_close(out, ref)
     else:
+        # sampled outputs: every branch and every kv head, each at the branch's first and
+        # last verify row (a random q head of the group), plus random (row, head) items
         R = B * (k + 1)
+        G = Hq // c.Hkv
         rng = np.random.default_rng(c.seed)
-        last = [(b * (k + 1) + k) * Hq + int(rng.integers(Hq)) for b in range(B)]
-        items = np.unique(np.concatenate([rng.integers(0, R * Hq, n_items), last])).astype(np.int32)
+        cover = [(b * (k + 1) + j) * Hq + g * G + int(rng.integers(G))
+                 for b in range(B) for g in range(c.Hkv) for j in sorted({0, k})]
+        items = np.unique(np.concatenate([rng.integers(0, R * Hq, n_items), cover])).astype(np.int32)
         ref, oe = orc.verify_attn_items(okv, vi.pos.numpy(), B, k, Hq, bits(vi.q), scale, items)
         assert oe == 0
         assert_attn_close(out.reshape(R * Hq, d)[torch.from_numpy(items).long().cuda()], ref)
@@ -73,9 +77,17 @@ def _step_parity(vi, full_oracle: bool, n_items=24, n_rows=4):
     ids, mx, e = gpu_lmhead(hid, W)
     assert e == 0
     np.testing.assert_array_equal(ids, vi.planted.numpy())
-    rows = np.arange(c.R) if full_oracle else np.random.default_rng(c.seed + 1).choice(c.R, n_rows, replace=False)
+    if full_oracle or c.R <= 16:
+        rows = np.arange(c.R)
+    else:
+        # at least 32 rows: every branch's first and last verify row, then random ones
+        ends = {b * (k + 1) + j for b in range(B) for j in (0, k)}
+        rest = np.setdiff1d(np.arange(c.R), sorted(ends))
+        fill = np.random.default_rng(c.seed + 1).choice(rest, max(0, min(len(rest), n_rows - len(ends))),
+                                                          replace=False)
+        rows = np.sort(np.concatenate([sorted(ends), fill])).astype(np.int64)
     oids, omx, gap, _ = orc.lmhead_argmax(bits(vi.hidden)[rows], bits(vi.W))
-    assert gap.min() >= 0.5, "planted margin not met (generator)"
+    assert gap.min() >= 0.5, "planted margin not met (generator)"   # on every row the oracle sees
     np.testing.assert_array_equal(ids[rows], oids)
     np.testing.assert_allclose(mx[rows], omx, rtol=1e-4, atol=1e-3)
 
@@ -93,7 +105,7 @@ def _step_parity(vi, full_oracle: bool, n_items=24, n_rows=4):
         tids, _, e = gpu_lmhead(vi.tie_hidden.cuda(), W)
         assert e == 0
         np.testing.assert_array_equal(tids, vi.tie_expect.numpy())
-        sel = np.arange(len(tids)) if full_oracle else np.arange(4)
+        sel = np.arange(len(tids))
         oti, _, tgap, _ = orc.lmhead_argmax(bits(vi.tie_hidden)[sel], bits(vi.W))
         np.testing.assert_array_equal(tids[sel], oti)
         assert np.all(tgap == 0.0)
