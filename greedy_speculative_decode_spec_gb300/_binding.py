@@ -26,15 +26,16 @@ KV_BF16, KV_FP8_E4M3 = 0, 1
 ERR_NULL, ERR_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_ALIGN = -1, -2, -3, -4, -5, -6
 SPEC_LMHEAD_STATIC_SCRATCH_BYTES = 256 + 1024 * 64 * 8  # as in include/spec_verify.h
 SPEC_MAX_STOP = 32                                       # as in include/spec_verify.h
-SPEC_ATTN_PLAN_FIELDS = 16                               # as in include/spec_verify.h
-ATTN_PLAN_KEYS = ("smem", "copies", "quadrants_per_copy", "q_rows", "p_rows", "ring_stages", "raw_stages",
-                  "q_buffers", "o_buffers", "split_keys", "n_splits", "n_units", "split_layout", "tma_rows",
-                  "barrier_bytes", "barrier_bytes_reserved")
+SPEC_ATTN_PLAN_FIELDS = 17                               # as in include/spec_verify.h
+ATTN_PLAN_KEYS = ("smem", "nq", "k_stages", "v_stages", "raw_stages", "s_buffers", "p_buffers", "q_buffers", "o_buffers",
+                  "tmem_cols", "split_keys", "n_splits", "n_units", "tile_group", "tma_rows", "barrier_bytes",
+                  "barrier_bytes_reserved")
 
 EXPORTS = ("spec_strerror", "spec_version", "spec_kv_append", "spec_kv_write_rows",
            "spec_verify_attn_workspace", "spec_verify_attn", "spec_lmhead_workspace",
            "spec_lmhead_argmax", "spec_lmhead_logits", "spec_accept", "spec_mtp_input_workspace",
-           "spec_mtp_input", "spec_lmhead_argmax_static", "spec_accept_stop", "spec_verify_attn_plan")
+           "spec_mtp_input", "spec_lmhead_argmax_static", "spec_accept_stop", "spec_verify_attn_plan",
+           "spec_test_set_wait_limit")
 
 
 class SpecError(RuntimeError):
@@ -81,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.spec_verify_attn_plan.argtypes = [ctypes.POINTER(spec_kv_desc), _i32, _i32, _i32, _i32, _vp, _i32]
         L.spec_accept_stop.argtypes = [_vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _vp, _i32, _vp, _vp]
+        L.spec_test_set_wait_limit.argtypes = [ctypes.c_uint64]
+        L.spec_test_set_wait_limit.restype = None
         L.spec_mtp_input_workspace.restype = _sz
         L.spec_mtp_input_workspace.argtypes = [_i32, _i32]
         L.spec_mtp_input.argtypes = [_vp, _vp, _vp, _vp, _vp, _f32, _vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp, _vp]
@@ -259,6 +262,11 @@ def spec_accept_stop(drafts, ids, pos, B: int, k: int, stop_ids, budget, out_tok
         _ptr(out_pos, "out_pos", torch.int32), _ptr(out_next, "out_next", torch.int32),
         _ptr(out_done, "out_done", torch.int32), _ptr(hidden, "hidden", torch.bfloat16), H,
         _ptr(h_out, "h_out", torch.bfloat16), _stream(stream)))
+
+
+def spec_test_set_wait_limit(ns: int) -> None:
+    """Test hook: limit (ns) of the kernels' pipeline waits for later launches; 0 = default."""
+    lib().spec_test_set_wait_limit(int(ns))
 
 
 def spec_mtp_input_workspace(M: int, H: int) -> int:

@@ -14,4 +14,10 @@ SPEC_API const char *spec_strerror(int status) {
     }
 }
 
-SPEC_API int spec_version(void) { return 100; }
+SPEC_API int spec_version(void) { return 200; }
+
+namespace spec {
+uint64_t g_wait_ns = DEFAULT_WAIT_NS;
+}
+
+SPEC_API void spec_test_set_wait_limit(uint64_t ns) { spec::g_wait_ns = ns ? ns : spec::DEFAULT_WAIT_NS; }

@@ -95,6 +95,11 @@ inline KvView make_view(const spec_kv_desc *kv) {
     return v;
 }
 
+// Limit (ns) of the pipeline waits inside the tcgen05 kernels launched from now on; the
+// waits that drain a kernel's own copies and MMAs before it exits always allow a second.
+extern uint64_t g_wait_ns;
+constexpr uint64_t DEFAULT_WAIT_NS = 1000000000ull;
+
 // ---- device side ---------------------------------------------------------------------
 
 __device__ __forceinline__ void raise_error(int32_t *err, int bit) {

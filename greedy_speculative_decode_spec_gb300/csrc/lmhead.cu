@@ -60,6 +60,7 @@ struct TcParams {
     int32_t *ids;
     float *max_logit;
     int32_t *err;
+    uint64_t wait_ns;               // pipeline-wait limit (drains: WAIT_NS)
 };
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -127,7 +128,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int kb = sp * p.n_kc / p.splits, ke = (sp + 1) * p.n_kc / p.splits;
                 for (int kc = kb; kc < ke; ++kc, ++it) {
                     const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
-                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag, WAIT_NS)) {
+                    if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -155,7 +156,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             bool ok = true;
             for (int w = wb; w < we && ok; ++w, ++t) {
                 const uint32_t acc = t & 1u, use = t >> 1;
-                if (!mbar_wait(tempty0 + 8 * acc, (use & 1u) ^ 1u, abort_flag, WAIT_NS)) {
+                if (!mbar_wait(tempty0 + 8 * acc, (use & 1u) ^ 1u, abort_flag, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -165,7 +166,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 const int kb = sp * p.n_kc / p.splits, ke = (sp + 1) * p.n_kc / p.splits;
                 for (int kc = kb; kc < ke; ++kc, ++it) {
                     const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
-                    if (!mbar_wait(full0 + 8 * s, ph, abort_flag, WAIT_NS)) {
+                    if (!mbar_wait(full0 + 8 * s, ph, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         bool ok = true;
         for (int w = wb; w < we; ++w, ++t) {
             const uint32_t acc = t & 1u, use = t >> 1;
-            if (!mbar_wait(tfull0 + 8 * acc, use & 1u, abort_flag, WAIT_NS)) {
+            if (!mbar_wait(tfull0 + 8 * acc, use & 1u, abort_flag, p.wait_ns)) {
                 ok = false;
                 break;
             }
@@ -380,6 +381,7 @@ static int plan(int M, int V, int K, int splits, TcPlan &pl) {
     TcParams &p = pl.p;
     p = TcParams{};
     p.M = M;
+    p.wait_ns = g_wait_ns;
     p.N_pad = ((M + 15) / 16) * 16;
     p.V = V;
     p.K = K;

@@ -59,21 +59,37 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase of the given parity to complete. Gives up (returns false) when
-// *abort becomes non-zero (abort may be null: then only the time limit applies) or after
-// timeout_ns of wall time, so no wait can hang.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          uint64_t timeout_ns) {
+// The polling loop of mbar_wait, kept out of line so that every wait site costs a few
+// instructions of the kernel's instruction footprint. sleep_ns > 0: sleep about that long
+// between probes (for threads that are not latency-critical).
+static __device__ __noinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity, volatile int *abort,
+                                            uint64_t timeout_ns, uint32_t sleep_ns) {
     uint64_t t0 = 0;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 31u) == 0) {
+        if (sleep_ns) __nanosleep(sleep_ns);
+        if ((i & 15u) == 0) {
             if (abort != nullptr && *abort) return false;
             const uint64_t t = globaltimer();
             if (t0 == 0) t0 = t;
             else if (t - t0 > timeout_ns) return false;
         }
     }
+}
+
+// Waits for the phase of the given parity to complete. Gives up (returns false) when
+// *abort becomes non-zero (abort may be null: then only the time limit applies) or after
+// timeout_ns of wall time, so no wait can hang.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          uint64_t timeout_ns) {
+    return mbar_try_wait(bar, parity) || mbar_wait_loop(bar, parity, abort, timeout_ns, 0);
+}
+
+// The same wait for a thread that is not latency-critical: between probes it sleeps about
+// sleep_ns, leaving the SM sub-partition's issue slots to the warps that do the math.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int *abort,
+                                                uint64_t timeout_ns, uint32_t sleep_ns) {
+    return mbar_try_wait(bar, parity) || mbar_wait_loop(bar, parity, abort, timeout_ns, sleep_ns);
 }
 
 // ---- programmatic dependent launch ----------------------------------------------------------
@@ -114,6 +130,12 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
 // issued so far has landed.
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// The same copy with a zero fill: when `valid` is false no byte is read (src must still be
+// a valid address) and the 16 destination bytes are written as zeros.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // Waits until at most N of this thread's committed groups are still pending.
@@ -170,6 +192,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
     asm volatile(
         "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T with 8-bit float inputs (kind::f8f6f4; the types are in
+// the instruction descriptor), fp32 accumulator. One instruction covers K = 32.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -245,6 +278,43 @@ __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t 
     d |= (uint64_t)1u << 46;
     d |= (uint64_t)2u << 61;
     return d;
+}
+
+// Shared-memory matrix descriptor, K-major operand whose rows are `row_bytes` (64 or 128)
+// long with the swizzle of that width; 8-row groups `sbo` bytes apart (8 * row_bytes for a
+// dense tile; 0 makes every group read the first one). The tile base must be aligned to
+// 8 * row_bytes; stepping 32 bytes along K adds 32 to the start address.
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr, uint32_t row_bytes, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)1u << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)(row_bytes == 64 ? 4u : 2u) << 61;  // 64-byte or 128-byte swizzle
+    return d;
+}
+
+// Shared-memory matrix descriptor: MN-major operand, 32-byte swizzle. Each 32-byte row holds
+// 16 consecutive MN elements of one K index; 8 K rows form a 256-byte atom (stride byte
+// offset 256); the next 16 MN elements sit `lbo` bytes further. The base must be 256-byte
+// aligned; stepping 16 K rows adds 512 bytes to the start address.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw32(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((256u >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)6u << 61;  // 32-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f8f6f4 with E4M3 A and B (K-major), fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f8_e4m3(int M, int N) {
+    return (1u << 4)                                  // D format: f32
+           | (0u << 7)                                // A format: E4M3
+           | (0u << 10)                               // B format: E4M3
+           | ((uint32_t)(N >> 3) << 17)               // N / 8
+           | ((uint32_t)(M >> 4) << 24);              // M / 16
 }
 
 // Instruction descriptor, kind::f16: 16-bit A and B (bf16 or f16), fp32 D, shape M x N;

@@ -1,5 +1,5 @@
 // verify_attn.cu -- a2: causal GQA verify attention over paged KV (split-KV flash-decode
-// on tcgen05 tensor cores).
+// on tcgen05 tensor cores, with the split merge in the same kernel).
 //
 // Row r = b*(k+1)+j (position p = pos[b]+j) and q head h attend keys 0..p of branch b
 // (kv head h / G): span-02 engine/crates/model/src/spec.rs, module documentation
@@ -9,47 +9,52 @@
 // the current length, so one program serves every length bit for bit).
 //
 // Work unit = (branch b, kv head g, split of split_keys positions). The n_q = (k+1)*G
-// query vectors that share kv head g sit on the 128 TMEM lanes (the M side of the MMAs,
-// query i on lane i of each copy, see below); the keys of a 128-key tile are the columns:
-//     S[q][key]  = Q . K_tile^T                 (tcgen05, fp32 in TMEM, double-buffered)
-//     O[q][d]   += P[q][key] . V_tile[key][d]   (tcgen05, fp32 in TMEM)
-// so every softmax quantity of a query (its running maximum and sum) lives in the lanes'
-// threads: no cross-lane reductions, only an exchange of partial maxima between the warps
-// that hold copies of the same queries. One pass per tile with a lazily raised maximum: a row's
-// running maximum m only moves when a tile's maximum exceeds it by more than RESCALE_TAU
-// (log2 units), so P = 2^(s - m) <= 2^RESCALE_TAU and O is rescaled (in TMEM, by the row's
-// own thread) only on such a move; the final O / l does not depend on which m was used.
+// query vectors that share kv head g are the narrow side of every MMA ("swap-AB"): the
+// 128 keys of a tile sit on the TMEM lanes and the queries on the columns,
+//     S^T[key][q]  = K_tile[key][:] . Q[q][:]            (M = 128 keys, N = NQ >= n_q)
+//     O^T[d][q]   += V_tile^T[d][key] . P^T[key][q]      (M = 128 head-dim lanes)
+//     L[*][q]     += ones[*][key] . P^T[key][q]          (the row sums, on every lane)
+// so the tensor work per tile scales with the real query count, not with a 128-row
+// padding. FP8 pools feed their E4M3 K codes straight into kind::f8f6f4 MMAs: each query
+// is split into two E4M3 terms (q * sigma = hi + lo, sigma a power of two per query), exact
+// for every element within 2^10 of the query's largest one; V codes times their page
+// scale are rounded to bf16 for the P.V product. The K page scales are applied by the
+// softmax to the scores.
 //
-// A persistent CTA per SM walks its units with warp-specialised roles:
-//   warps 0-3  gather K and V rows with 16-byte cp.async copies into the swizzled operand
-//              ring (bf16), one warp per SM sub-partition (cp.async issue is throughput-
-//              bound per sub-partition); for FP8 pools warps 0, 1 gather E4M3 rows into a raw
-//              ring (by TMA boxes of one page-run each when pages hold >= 64 positions) and
-//              warps 2, 3 convert them to f16 exactly (and Q bf16 -> f16 in place);
-//   warps 4-7  softmax, one per TMEM lane quadrant (a warp reaches only the lanes of its
-//              own quadrant, and quadrant w % 4 is also SM sub-partition w % 4): Q is loaded
-//              in copies, four when the n_q queries fit one quadrant and two when they span
-//              two, so that every quadrant holds the queries and the S MMA computes each
-//              copy's scores at no extra cost (M = 128 either way); each warp takes its
-//              copy's share of the tile's key columns (when four copies would leave the
-//              operand ring too shallow, two copies on one quadrant each, and two warps idle);
-//   warp 8     per unit: takes the next work unit, fills the page-table entries (and FP8
-//              scales) into a shared table, and loads the Q copies by 3-D TMA boxes;
-//   warp 9     issues S = Q . K^T of each tile as soon as its keys and an S buffer are there
-//              (TMEM allocation is also this warp's);
-//   warp 10    issues O += P . V of each tile as soon as its P is there, so the softmax of
-//              one tile overlaps the MMAs of its neighbours.
-// The page scales of FP8 pools are applied by the softmax: K's to the scores, V's to P (the
-// row sum stays unscaled), so S and O come out in the pool's true units.
+// Softmax: a thread owns one key of the tile (its TMEM lane) and all query columns. One
+// pass per tile with a lazily raised maximum: per tile the four softmax warps exchange
+// their column maxima through shared memory; a column's running maximum m only moves when
+// the tile's maximum exceeds it by more than RESCALE_TAU (log2 units), so P = 2^(s - m) <=
+// 2^RESCALE_TAU, and O and L are rescaled in TMEM only on such a move. Every decision is
+// taken per column from that column's own scores, so a query's result does not depend on
+// the other queries of the batch.
+//
+// A persistent CTA per SM walks work units handed out by a global counter, with
+// warp-specialised roles:
+//   warps 0-3  softmax (warp w reads TMEM lane quadrant w: keys 32w..32w+31 of S, head-dim
+//              lanes 32w.. of O), the unit's epilogue and the split merges;
+//   warps 4-7  bf16 pools: gather K and V rows with 16-byte cp.async copies (zero fill past
+//              the branch's last position) into the 128-byte-swizzled operand ring;
+//              FP8 pools: warp 4 issues TMA boxes of one page-run each (K straight into the
+//              MMA layout, V into a raw stage), warps 5-7 split Q and turn V codes into
+//              scaled bf16 rows;
+//   warp 8     per unit: takes the next work unit, fills the page table entries (and FP8
+//              scales) into a shared table, loads Q by 3-D TMA boxes;
+//   warp 9     issues S = K . Q^T of each tile (TMEM allocation is also this warp's);
+//   warp 10    issues O += V^T . P^T and L += 1 . P^T of each tile.
 // Keys beyond a row's position get P = 0 by select, never by multiplication, and V rows
-// past the branch's last position are zeroed before P.V, so NaN in unused pool slots
-// cannot reach a result. Tile and split boundaries sit at fixed key positions and every
-// MMA row is computed independently of the others, so a row's output is identical
-// whatever B, k or batch it is verified in. A combine pass merges the splits of each
-// (row, head) in ascending order; it and this kernel are programmatic dependent launches
-// that wait on the device (griddepcontrol.wait) for the kernel before them.
-// Every pipeline wait is bounded (1 s): on a timeout the kernel raises
-// SPEC_DEVERR_TIMEOUT, lets issued copies and MMAs land, frees TMEM and exits.
+// past the branch's last position are zero, so NaN in unused pool slots cannot reach a
+// result. Tile and split boundaries sit at fixed key positions, and every MMA column is
+// computed independently of the others, so a row's output is identical whatever B, k or
+// batch it is verified in.
+//
+// Split merge: each unit writes its (m, l, O) partial, and a second kernel (a programmatic
+// dependent launch) merges them per (row, head) with a summation order fixed by split
+// positions alone: splits in groups of COMBINE_GROUP consecutive ones, each group summed in
+// ascending order, then the groups in ascending order (skipping splits a row does not
+// reach), so that any number of warps can share the work without changing a bit.
+// Every pipeline wait is bounded (1 s unless a test shortens it): on a timeout the kernel
+// raises SPEC_DEVERR_TIMEOUT, lets issued copies and MMAs land, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -62,26 +67,34 @@ namespace spec {
 
 using namespace sm100;
 
-constexpr int SPLIT_KEYS = 1024;  // largest split; the split size is split_keys_for(Hkv)
+constexpr int SPLIT_KEYS = 1024;     // largest split; the split size is split_keys_for(Hkv)
 constexpr int TILE_KEYS = 128;
+constexpr int COMBINE_GROUP = 8;     // splits summed in order before the groups are
+constexpr int MAX_NQ = 128;          // query vectors per (branch, kv head), padded to 16
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr float RESCALE_TAU = 8.0f;   // P <= 2^8: exact range for bf16 and f16 alike
+constexpr float RESCALE_TAU = 8.0f;  // P <= 2^8: exact range for bf16 and f16 alike
 constexpr uint64_t ATT_WAIT_NS = 1000000000ull;
 constexpr int ATT_SMEM_LIMIT = 227 * 1024;
-constexpr int MAX_NPAD = 64;          // query vectors per (branch, kv head), padded to 16
-constexpr int MAX_RPAD = 128;         // TMEM lanes holding the copies of the query layout
+constexpr int ATT_THREADS = 352;
 
-// Per-unit table the producer warp fills: the page of each page-sized run of the split's
-// keys (-1 if the table entry is invalid), the page's FP8 K / V scales, and the error
-// bits of any invalid entry. Used for pages of >= 8 positions.
 constexpr int UT_ENTRIES = SPLIT_KEYS / 8;
+struct UnitInfo {
+    int b, g, split, pos_b, kv_end, s0, T, n_used, u;  // u: the unit's workspace slot
+    bool bad_pos;
+};
+
+// Per-unit table the producer warp fills: the unit itself (computed once, read by every
+// role), the page of each page-sized run of the split's keys (-1 if the table entry is
+// invalid), the page's FP8 K / V scales, and the error bits of any invalid entry. Pages are
+// listed for pages of >= 8 positions.
 struct UnitTable {
     int32_t page[UT_ENTRIES];
     float ksc[UT_ENTRIES];
     float vsc[UT_ENTRIES];
+    UnitInfo ui;
     int32_t bad;
     int32_t iter;          // the unit's index in the walk order, or -1: no more units
-    int32_t pad_[30];
+    int32_t pad_[20];
 };
 
 // Split size in positions, a function of the model's KV-head count only (never of B, k or
@@ -91,94 +104,86 @@ __host__ __device__ constexpr int split_keys_for(int n_kv_heads) {
     return n_kv_heads <= 2 ? 256 : (n_kv_heads <= 4 ? 512 : SPLIT_KEYS);
 }
 
-struct AttnTcParams {
+template <int D, bool FP8>
+struct AttnShape {
+    static constexpr int SUB = D < 128 ? D : 128;          // head-dim columns per sub-tile
+    static constexpr int NSUB = D / SUB;                    // sub-tiles per tile (d halves for 256)
+    static constexpr uint32_t OP_STAGE = TILE_KEYS * SUB * 2;  // 16-bit sub-tile: 128 keys x SUB
+    static constexpr uint32_t F8_STAGE = TILE_KEYS * SUB;      // E4M3 sub-tile
+    static constexpr uint32_t K_STAGE = FP8 ? F8_STAGE : OP_STAGE;  // a K ring stage
+    static constexpr int KSTEP = FP8 ? 32 : 16;             // K elements per MMA of S
+    static constexpr int K8ROW = SUB;                       // bytes per E4M3 row of a sub-tile
+    static constexpr int NATOM_Q = D / 64;                  // 128-byte column blocks of a bf16 Q row
+    static constexpr int Q8ROW = D < 128 ? 64 : 128;        // bytes per row of an E4M3 Q block
+    static constexpr int NQ8 = D / Q8ROW;                   // E4M3 Q column blocks
+};
+
+struct AttnParams {
     KvView kv;
     const int32_t *pos;
-    int B, k, Hq, G, n_q, n_splits, max_pos, n_units, split_keys;
-    // query layout on the TMEM lanes: draft rows j < J1 on lanes [0, J1*G), the rest (if
-    // split) on lanes [32, 32 + (k+1-J1)*G); R_pad = rows of a Q buffer (all copies)
-    int J1, split, R_pad;
-    // copies of the query layout on the TMEM lanes (copy c starts at lane 32*qpc*c), so that
-    // every lane quadrant, and with it every SM sub-partition, holds the queries; PR = rows
-    // of P (copy 0's layout, padded to 16)
-    int copies, qpc, PR;
-    // FP8 pools: rows per TMA box of the K / V gather (one page-run: min(page size, 128));
-    // 0 = the rows are gathered by 16-byte cp.async copies
+    int B, k, Hq, G, n_q, NQ, n_splits, max_pos, n_units, split_keys;
+    int TPI;               // tiles per softmax iteration (a tile group)
+    // FP8 pools: rows per TMA box of the K / V gather (one page-run: min(page size, 128))
     int tma_rows;
     const uint16_t *q;     // bf16 [R][Hq][d]
+    const float *qinv_g;   // FP8: [B*Hkv][NQ] 1/sigma of every query column (the split's scale)
+    uint8_t *q8_g;         // FP8: [B*Hkv][2][NQ][d] the split queries' E4M3 terms (hi, lo)
+    uint16_t *out;         // bf16 [R][Hq][d]
     float scale_log2;      // softmax scale * log2(e)
     unsigned int *sched;   // [2]: next unit to hand out, CTAs done (zero between calls)
-    float *ws_ml;          // [units][n_q][2]  (m in log2 units, l)
-    float *ws_o;           // [units][n_q][d]
+    float *ws_ml;          // [units][NQ][2]  (m in log2 units, l)
+    float *ws_o;           // [units][NQ][d]
     int32_t *err;
-    int NS, NR;            // operand / raw ring depth (sub-tiles)
-    int OB;                // O buffers in TMEM (1 or 2)
-    int QB;                // Q buffers in shared memory (1 or 2)
-    uint32_t off_q, off_p, off_op, off_raw, off_ut, off_bar, off_small;  // shared-memory offsets
+    uint64_t wait_ns;      // pipeline-wait limit
+    int NK, NV, NR, NSB, NPB, QB, OB;  // K, bf16 V and (FP8) raw V ring stages; S, P, Q, O buffers
+    uint32_t off_q, off_q8, off_p, off_ones, off_k, off_v, off_raw, off_ut, off_sx, off_bar, off_small;
+    uint32_t t_o;          // first TMEM column of the O / L buffers
 };
 
 // The CTA's mbarriers, as byte offsets from the barrier region (one definition for the
 // kernel and the host plan, which checks that they fit BAR_BYTES).
 struct BarMap {
-    uint32_t op_full, op_empty, raw_full, raw_empty, sfull, sfree, pfull, pfree, odone, ofree;
-    uint32_t qfull, qconv, qfree, ufull, ufree, drain, xfull, lfull, lfin, end;
+    uint32_t kfull, kempty, vfull, vempty, rfull, rempty, sfull, sfree, pfull, pfree, ofree;
+    uint32_t qfull, qfree, ufull, ufree, lfin, drain, xbar, cjoin, end;
 };
-__host__ __device__ inline BarMap bar_map(int NS, int NR) {
+__host__ __device__ inline BarMap bar_map(int NK, int NV, int NR, int NSB, int NPB) {
     BarMap m;
     uint32_t o = 0;
-    m.op_full = o;   o += 8 * NS;  // operand ring: full / empty per stage
-    m.op_empty = o;  o += 8 * NS;
-    m.raw_full = o;  o += 8 * NR;  // FP8 raw ring
-    m.raw_empty = o; o += 8 * NR;
-    m.sfull = o;     o += 16;      // S double buffer
-    m.sfree = o;     o += 16;
-    m.pfull = o;     o += 16;      // P double buffer
-    m.pfree = o;     o += 16;
-    m.odone = o;     o += 8;       // P.V completions
-    m.ofree = o;     o += 16;      // O buffers
-    m.qfull = o;     o += 16;      // Q buffers
-    m.qconv = o;     o += 16;
-    m.qfree = o;     o += 16;
-    m.ufull = o;     o += 16;      // unit tables
-    m.ufree = o;     o += 16;
-    m.drain = o;     o += 16;      // one per MMA issuer
-    m.xfull = o;     o += 32;      // softmax exchanges: row maxima, row sums
-    m.lfull = o;     o += 32;
-    m.lfin = o;      o += 16;      // the loaders have issued every copy of a unit
+    m.kfull = o;    o += 8 * NK;   // K ring
+    m.kempty = o;   o += 8 * NK;
+    m.vfull = o;    o += 8 * NV;   // bf16 V ring
+    m.vempty = o;   o += 8 * NV;
+    m.rfull = o;    o += 8 * NR;   // FP8 raw V ring
+    m.rempty = o;   o += 8 * NR;
+    m.sfull = o;    o += 8 * NSB;
+    m.sfree = o;    o += 8 * NSB;
+    m.pfull = o;    o += 8 * NPB;
+    m.pfree = o;    o += 8 * NPB;
+    m.ofree = o;    o += 16;
+    m.qfull = o;    o += 16;
+    m.qfree = o;    o += 16;
+    m.ufull = o;    o += 16;
+    m.ufree = o;    o += 16;
+    m.lfin = o;     o += 16;
+    m.drain = o;    o += 16;
+    m.xbar = o;     o += 16;   // softmax column-maximum exchange, by group parity
+    m.cjoin = o;    o += 8;    // the two FP8 converter warps
     m.end = o;
     return m;
 }
-constexpr uint32_t BAR_BYTES = 8 * 64;
-
-// A ring stage holds one sub-tile: 128 keys x SUB_COLS columns of d (d = 256 tiles are
-// two sub-tiles, the halves of d: S accumulates over both, and each half of O reads its
-// own half of V).
-template <int D, bool FP8>
-struct AttnShape {
-    static constexpr int NATOM = D / 64;                   // 128-byte column blocks of a 16-bit row
-    static constexpr int SUB_COLS = D < 128 ? D : 128;
-    static constexpr int NSUB = D / SUB_COLS;              // sub-tiles per tile
-    static constexpr int NATOM_SUB = SUB_COLS / 64;        // column blocks per sub-tile
-    static constexpr uint32_t OP_STAGE = NATOM_SUB * TILE_KEYS * 128;
-    static constexpr uint32_t RAW_STAGE = FP8 ? TILE_KEYS * SUB_COLS : 0;
-    static constexpr int THREADS = 352;
-};
-
-struct UnitInfo {
-    int b, g, split, pos_b, kv_end, s0, T;
-    bool bad_pos;
-};
+constexpr uint32_t BAR_BYTES = 8 * 96;
 
 // The scheduler hands out units split-major (every (branch, head) pair's first split, then
 // every pair's second split, ...), which puts each pair's short last split late;
-// `u` (the workspace slot) stays (branch, head, split)-major for the combine pass.
-__device__ __forceinline__ UnitInfo unit_info(const AttnTcParams &p, int iter, int &u) {
+// `u` (the workspace slot) is (branch, head, split)-major, so a merge group's partials are
+// contiguous.
+static __device__ __noinline__ UnitInfo unit_info(const AttnParams &p, int iter) {
     UnitInfo ui;
     const int pairs = p.B * p.kv.n_kv_heads;
     ui.split = iter / pairs;
     ui.g = (iter % pairs) % p.kv.n_kv_heads;
     ui.b = (iter % pairs) / p.kv.n_kv_heads;
-    u = (ui.b * p.kv.n_kv_heads + ui.g) * p.n_splits + ui.split;
+    ui.u = (ui.b * p.kv.n_kv_heads + ui.g) * p.n_splits + ui.split;
     ui.pos_b = __ldg(p.pos + ui.b);
     ui.bad_pos = ui.pos_b < 0 || ui.pos_b + p.k + 1 > p.max_pos;
     ui.kv_end = ui.pos_b + p.k + 1;
@@ -186,22 +191,28 @@ __device__ __forceinline__ UnitInfo unit_info(const AttnTcParams &p, int iter, i
     int n = ui.bad_pos ? 0 : ui.kv_end - ui.s0;
     n = n < 0 ? 0 : (n > p.split_keys ? p.split_keys : n);
     ui.T = (n + TILE_KEYS - 1) / TILE_KEYS;
+    ui.n_used = ui.bad_pos ? 0 : (ui.kv_end + p.split_keys - 1) / p.split_keys;
     return ui;
 }
 
-// byte offset of 16-bit element (row, col) in a K-major, 128-byte-swizzled operand whose
-// 64-column blocks are `block_bytes` apart
+// byte offset of 16-bit element (row, col) in a K-major (or, read the other way, MN-major)
+// 128-byte-swizzled tile whose 64-column blocks are `block_bytes` apart
 __device__ __forceinline__ uint32_t sw128_off(int row, int col, uint32_t block_bytes) {
     const int blk = col >> 6, c = col & 63;
     return blk * block_bytes + row * 128 + ((((c >> 3) ^ (row & 7)) & 7) << 4);
 }
 
 // Every lane waits; the verdict is made uniform across the warp so that no lane can
-// leave a loop that the others stay in.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-    const bool r = mbar_wait(bar, parity, abort_flag, ATT_WAIT_NS);
+// leave a loop that the others stay in. SLEEP > 0: the warp is not latency-critical and
+// sleeps about SLEEP ns between probes, so that it does not take issue slots from the
+// softmax warp of its SM sub-partition.
+template <uint32_t SLEEP = 0>
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, uint64_t ns) {
+    const bool r = SLEEP ? mbar_wait_sleep(bar, parity, abort_flag, ns, SLEEP) : mbar_wait(bar, parity, abort_flag, ns);
     return __all_sync(0xFFFFFFFFu, r);
 }
+constexpr uint32_t SLEEP_LOAD = 128;  // loaders, converters, producer
+constexpr uint32_t SLEEP_MMA = 32;    // MMA issuers
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, bool f16) {
     if (f16) {
@@ -212,84 +223,121 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool f16) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
+// The weight of a partial result with maximum m against the merged maximum M: exactly 1
+// when m is the maximum (so a merge of one partial reproduces it bit for bit).
+__device__ __forceinline__ float merge_weight(float m, float M) { return m == M ? 1.f : ex2_approx(m - M); }
+
 template <int D, bool FP8>
-__global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap map_q0, const __grid_constant__ CUtensorMap map_q1,
-                   const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                   AttnTcParams p) {
+__global__ void __launch_bounds__(ATT_THREADS, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                const __grid_constant__ CUtensorMap map_v, AttnParams p) {
     using S_ = AttnShape<D, FP8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_u32(smem);
-    const int R_pad = p.R_pad, n_q = p.n_q;
-    // Q buffers keep R_pad rows and P buffers PR rows per 64-column block; the M = 128 MMAs
-    // also read the rows after those, which fall on the following memory: those rows only
-    // feed TMEM lanes no thread reads.
-    const uint32_t QATOM = (uint32_t)R_pad * 128, QBUF = S_::NATOM * QATOM;
-    const uint32_t PATOM = (uint32_t)p.PR * 128, PBUF = 2 * PATOM;
-    const uint32_t s_q = s_base + p.off_q, s_p = s_base + p.off_p, s_op = s_base + p.off_op;
+    const int NQ = p.NQ, n_q = p.n_q;
+    const uint32_t QATOM = (uint32_t)NQ * 128, QBUF = S_::NATOM_Q * QATOM;      // bf16 Q
+    const uint32_t Q8ATOM = (uint32_t)NQ * S_::Q8ROW, Q8PART = S_::NQ8 * Q8ATOM;  // one E4M3 Q part
+    const uint32_t PTILE = (uint32_t)NQ * 256;                                  // a tile's P^T: [NQ/16][128 keys][32 B]
+    const uint32_t PBUF = (uint32_t)p.TPI * PTILE;                              // a tile group's
+    const uint32_t s_q = s_base + p.off_q, s_q8 = s_base + p.off_q8, s_p = s_base + p.off_p;
+    const uint32_t s_ones = s_base + p.off_ones, s_k = s_base + p.off_k, s_v = s_base + p.off_v;
     const uint32_t s_raw = s_base + p.off_raw;
-    uint8_t *g_p = smem + p.off_p;
     UnitTable *tables = reinterpret_cast<UnitTable *>(smem + p.off_ut);  // [2]
-    // barrier map
-    const BarMap bm = bar_map(p.NS, p.NR);
+    const BarMap bm = bar_map(p.NK, p.NV, p.NR, p.NSB, p.NPB);
     const uint32_t bar0 = s_base + p.off_bar;
-    const uint32_t op_full = bar0 + bm.op_full, op_empty = bar0 + bm.op_empty;
-    const uint32_t raw_full = bar0 + bm.raw_full, raw_empty = bar0 + bm.raw_empty;
+    const uint32_t kfull = bar0 + bm.kfull, kempty = bar0 + bm.kempty;
+    const uint32_t vfull = bar0 + bm.vfull, vempty = bar0 + bm.vempty;
+    const uint32_t rfull = bar0 + bm.rfull, rempty = bar0 + bm.rempty;
     const uint32_t sfull = bar0 + bm.sfull, sfree = bar0 + bm.sfree;
     const uint32_t pfull = bar0 + bm.pfull, pfree = bar0 + bm.pfree;
-    const uint32_t odone = bar0 + bm.odone, ofree = bar0 + bm.ofree;
-    const uint32_t qfull = bar0 + bm.qfull, qconv = bar0 + bm.qconv, qfree = bar0 + bm.qfree;
-    const uint32_t ufull = bar0 + bm.ufull, ufree = bar0 + bm.ufree;
-    const uint32_t drain = bar0 + bm.drain;
-    const uint32_t xfull = bar0 + bm.xfull, lfull = bar0 + bm.lfull;
-    const uint32_t lfin = bar0 + bm.lfin;
+    const uint32_t ofree = bar0 + bm.ofree;
+    const uint32_t qfull = bar0 + bm.qfull, qfree = bar0 + bm.qfree;
+    const uint32_t ufull = bar0 + bm.ufull, ufree = bar0 + bm.ufree, lfin = bar0 + bm.lfin;
+    const uint32_t drain = bar0 + bm.drain, xbar = bar0 + bm.xbar;
+    const uint32_t cjoin = bar0 + bm.cjoin;
     uint8_t *small = smem + p.off_small;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(small + 4);
+    // softmax scratch: column-maximum exchange [2 tile parities][4 warps][NQ], then per warp
+    // its copy of the running maxima, the rescale factors and the column limits [4][NQ],
+    // then the E4M3 Q scales [2 unit tables][NQ], then per tile parity and warp whether a
+    // running maximum must move
+    float *sx_red = reinterpret_cast<float *>(smem + p.off_sx);
+    float *sx_m = sx_red + 8 * NQ;
+    float *sx_f = sx_m + 4 * NQ;
+    int *sx_lim = reinterpret_cast<int *>(sx_f + 4 * NQ);
+    float *sx_qinv = reinterpret_cast<float *>(sx_lim + 4 * NQ);
+    int *sx_need = reinterpret_cast<int *>(sx_qinv + 2 * NQ);  // [2 tile parities][4 warps]
+    // per query column q = j*G + i: its draft row j (-1 for padding) and its output offset
+    // (j*Hq + i)*D from the (branch, kv head)'s first output
+    int *sx_colj = sx_need + 8;
+    int *sx_coloff = sx_colj + NQ;
+    const uint64_t wns = p.wait_ns;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_act = p.copies * p.qpc;  // softmax warps with queries
     const bool small_pages = p.kv.page_size < 8;  // more than UT_ENTRIES pages per split
     const int log2P = p.kv.log2_page;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < p.NS; ++s) {
-            // bf16: each loader thread's copies arrive; FP8: each converter warp
-            // FP8: each converter warp arrives; bf16: each loader thread's copies
-            mbar_init(op_full + 8 * s, FP8 ? 2 : 128);
-            mbar_init(op_empty + 8 * s, 1);
+        for (int s = 0; s < p.NK; ++s) {
+            mbar_init(kfull + 8 * s, FP8 ? 1 : 64);  // FP8: the TMA bytes; bf16: each K loader thread
+            mbar_init(kempty + 8 * s, 1);            // an S MMA commit
+        }
+        for (int s = 0; s < p.NV; ++s) {
+            mbar_init(vfull + 8 * s, FP8 ? 1 : 64);  // FP8: the converters; bf16: each V loader thread
+            mbar_init(vempty + 8 * s, 1);            // a P.V commit
         }
         for (int s = 0; s < p.NR; ++s) {
-            mbar_init(raw_full + 8 * s, p.tma_rows ? 2 : 64);  // each FP8 loader warp / thread arrives
-            mbar_init(raw_empty + 8 * s, 2);  // the converter warps
+            mbar_init(rfull + 8 * s, 1);             // the TMA bytes
+            mbar_init(rempty + 8 * s, 1);            // the converters
+        }
+        for (int s = 0; s < p.NSB; ++s) {
+            mbar_init(sfull + 8 * s, 1);
+            mbar_init(sfree + 8 * s, 4);
+        }
+        for (int s = 0; s < p.NPB; ++s) {
+            mbar_init(pfull + 8 * s, 4);
+            mbar_init(pfree + 8 * s, 1);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(sfull + 8 * a, 1);
-            mbar_init(sfree + 8 * a, n_act);
-            mbar_init(pfull + 8 * a, n_act);
-            mbar_init(pfree + 8 * a, 1);
-            mbar_init(ofree + 8 * a, n_act);
+            mbar_init(ofree + 8 * a, 4);
             mbar_init(qfull + 8 * a, 1);
-            mbar_init(qconv + 8 * a, 2);
             mbar_init(qfree + 8 * a, 1);
             mbar_init(ufull + 8 * a, 1);
-            mbar_init(ufree + 8 * a, n_act + (FP8 ? 2 : 4) + 1);  // softmax, loader and P.V warps
-            mbar_init(drain + 8 * a, 1);
+            mbar_init(ufree + 8 * a, 10);  // softmax 4, loader roles 4, both MMA issuers
             mbar_init(lfin + 8 * a, FP8 ? 2 : 4);
+            mbar_init(drain + 8 * a, 1);
+            mbar_init(xbar + 8 * a, 4);
         }
-        mbar_init(odone, 1);
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(xfull + 8 * i, p.copies);  // the copies of one lane quadrant's queries
-            mbar_init(lfull + 8 * i, p.copies);
-        }
+        mbar_init(cjoin, 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
+    for (int q = threadIdx.x; q < NQ; q += ATT_THREADS) {
+        sx_colj[q] = q < n_q ? q / p.G : -1;
+        sx_coloff[q] = q < n_q ? ((q / p.G) * p.Hq + q % p.G) * D : 0;
+    }
+    // bf16 Q rows n_q..NQ-1 (never written by the Q loads) are zero, so the padding columns
+    // of S hold finite zeros
+    if (!FP8 && NQ > n_q) {
+        const int per = (NQ - n_q) * 8;  // 16-byte pieces per (buffer, column block)
+        for (int i = threadIdx.x; i < p.QB * S_::NATOM_Q * per; i += ATT_THREADS) {
+            const int blk = i / per, r = i % per;
+            *reinterpret_cast<uint4 *>(smem + p.off_q + blk * QATOM + n_q * 128 + r * 16) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    // the A operand of the row-sum MMA: 8 rows x 128 bytes of ones (every 8-row group and
+    // every K step of the MMA read this one atom)
+    {
+        const uint32_t one2 = 0x3F803F80u;  // bf16 1.0, twice
+        uint32_t *ones = reinterpret_cast<uint32_t *>(smem + p.off_ones);
+        for (int i = threadIdx.x; i < 256; i += ATT_THREADS) ones[i] = one2;
+        fence_proxy_async_smem();
+    }
     if (warp == 8 && lane == 0) {
-        prefetch_tmap(&map_q0);
-        if (p.split) prefetch_tmap(&map_q1);
-        if (FP8 && p.tma_rows) {
+        prefetch_tmap(&map_q);
+        if (FP8) {
             prefetch_tmap(&map_k);
             prefetch_tmap(&map_v);
         }
@@ -305,35 +353,35 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     // (the KV pool, Q, the positions) is read before this point
     grid_dep_wait();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t t_s = tmem;        // S buffers: columns [0, 128) and [128, 256)
-    const uint32_t t_o = tmem + 256;  // O buffers: D columns each
+    const uint32_t t_o0 = tmem + p.t_o;  // O buffers: [OB][NSUB + 1][NQ] columns (the last NQ: L)
 
     if (warp == 8) {
         // ================= producer: per unit, the page table entries and Q =================
         // Units are handed out dynamically: the producer takes the next index of the
         // split-major walk from a global counter, skips empty units, and publishes the unit
         // in the shared table that every other role waits on (-1 ends their loops). It takes
-        // a unit only once a table is free and the loaders have issued every copy of the
-        // previous unit, so that a CTA holds little more than the work in its rings and the
-        // last units go to whichever CTAs run out of work first.
+        // a unit only once a table is free and the loaders are issuing the last two tiles of
+        // the previous unit: late enough that a CTA holds little more than the work in its
+        // rings (the last units go to whichever CTAs run out of work first), early enough that
+        // the next unit's table and Q are ready when the loaders get to it.
         uint32_t ua = 0;
         bool ok = true;
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
             UnitTable *tab = tables + ub;
-            if (!warp_wait(ufree + 8 * ub, uph ^ 1u, abort_flag)) { ok = false; break; }
-            if (ua > 0 && !warp_wait(lfin + 8 * ((ua - 1) & 1u), ((ua - 1) >> 1) & 1u, abort_flag)) {
+            if (!warp_wait<SLEEP_LOAD>(ufree + 8 * ub, uph ^ 1u, abort_flag, wns)) { ok = false; break; }
+            if (ua > 0 && !warp_wait<SLEEP_LOAD>(lfin + 8 * ((ua - 1) & 1u), ((ua - 1) >> 1) & 1u, abort_flag, wns)) {
                 ok = false;
                 break;
             }
-            int it_u = -1, u = 0;
+            int it_u = -1;
             UnitInfo ui;
             for (;;) {
                 int cand = 0;
                 if (lane == 0) cand = (int)atomicAdd(p.sched, 1u);
                 cand = __shfl_sync(0xFFFFFFFFu, cand, 0);
                 if (cand >= p.n_units) break;
-                ui = unit_info(p, cand, u);
+                ui = unit_info(p, cand);
                 if (ui.T > 0) {
                     it_u = cand;
                     break;
@@ -345,7 +393,7 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(ufull + 8 * ub);
-                    // no new work for this CTA: the combine pass may be scheduled
+                    // no new work for this CTA: the next kernel in the stream may be scheduled
                     grid_dep_launch();
                 }
                 break;
@@ -378,27 +426,40 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                 }
             }
             badbits = __reduce_or_sync(0xFFFFFFFFu, badbits);
+            if (FP8) {  // the unit's query scales (1/sigma per column), read by the softmax
+                const float *qi = p.qinv_g + (size_t)(ui.b * p.kv.n_kv_heads + ui.g) * NQ;
+                for (int q = lane; q < NQ; q += 32) sx_qinv[ub * NQ + q] = __ldg(qi + q);
+            }
             if (lane == 0) {
+                tab->ui = ui;
                 tab->bad = badbits;
                 tab->iter = it_u;
                 if (badbits) raise_error(p.err, badbits);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(ufull + 8 * ub);
-            // ---- Q of (b, g): one 3-D box per 64-column block lands as rows j*G + i ----
-            const uint32_t qs = p.QB == 2 ? ub : 0u, qph = p.QB == 2 ? uph : (ua & 1u);  // Q buffer, phase
-            if (!warp_wait(qfree + 8 * qs, qph ^ 1u, abort_flag)) { ok = false; break; }
+            // ---- Q of (b, g) ----
+            // bf16: one 3-D box per 64-column block lands as rows j*G + i. FP8: the two E4M3
+            // parts (hi, lo) of the split queries, one 2-D box per 128-byte column block each
+            // (the split kernel wrote them as [pair][part][NQ][d] bytes).
+            const uint32_t qs = ua % (uint32_t)p.QB, qph = (ua / (uint32_t)p.QB) & 1u;
+            if (!warp_wait<SLEEP_LOAD>(qfree + 8 * qs, qph ^ 1u, abort_flag, wns)) { ok = false; break; }
             if (lane == 0) {
-                mbar_arrive_expect_tx(qfull + 8 * qs, (uint32_t)(p.copies * S_::NATOM * n_q * 128));
-                for (int c = 0; c < p.copies; ++c) {
-                    const uint32_t dst = s_q + qs * QBUF + (uint32_t)(c * p.qpc * 32 * 128);
+                if (FP8) {
+                    mbar_arrive_expect_tx(qfull + 8 * qs, (uint32_t)(2 * NQ * D));
+                    const int row0 = (ui.b * p.kv.n_kv_heads + ui.g) * 2 * NQ;
 #pragma unroll
-                    for (int a = 0; a < S_::NATOM; ++a) {
-                        tma_load_3d(dst + a * QATOM, &map_q0, a * 64, ui.g * p.G, ui.b * (p.k + 1), qfull + 8 * qs);
-                        if (p.split)
-                            tma_load_3d(dst + a * QATOM + 32 * 128, &map_q1, a * 64, ui.g * p.G,
-                                        ui.b * (p.k + 1) + p.J1, qfull + 8 * qs);
-                    }
+                    for (int part = 0; part < 2; ++part)
+#pragma unroll
+                        for (int a = 0; a < S_::NQ8; ++a)
+                            tma_load_2d(s_q8 + (qs * 2 + part) * Q8PART + a * Q8ATOM, &map_q, a * S_::Q8ROW,
+                                        row0 + part * NQ, qfull + 8 * qs);
+                } else {
+                    mbar_arrive_expect_tx(qfull + 8 * qs, (uint32_t)(S_::NATOM_Q * n_q * 128));
+#pragma unroll
+                    for (int a = 0; a < S_::NATOM_Q; ++a)
+                        tma_load_3d(s_q + qs * QBUF + a * QATOM, &map_q, a * 64, ui.g * p.G, ui.b * (p.k + 1),
+                                    qfull + 8 * qs);
                 }
             }
             __syncwarp();
@@ -420,118 +481,87 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
         if (lane == 0) {
             for (uint32_t j = 0; j < (uint32_t)p.QB && j < ua; ++j) {
                 const uint32_t i2 = ua - 1 - j;
-                mbar_wait(qfull + 8 * (p.QB == 2 ? (i2 & 1u) : 0u), p.QB == 2 ? (i2 >> 1) & 1u : i2 & 1u, nullptr,
-                          ATT_WAIT_NS);
+                mbar_wait(qfull + 8 * (i2 % (uint32_t)p.QB), (i2 / (uint32_t)p.QB) & 1u, nullptr, ATT_WAIT_NS);
             }
         }
         __syncwarp();
-    } else if (warp == 9 || warp == 10) {
-        // ================= MMA issuers: warp 9 S = Q . K^T, warp 10 O += P . V =================
-        // Two issuing threads, so that S of a tile goes to the tensor pipe as soon as its keys
-        // and an S buffer are there and P.V as soon as P is: the issue, commit and wait
-        // instructions of both MMA chains take longer than the tensor pipe needs for them.
-        // Each thread's commits track its own MMAs.
-        const bool s_role = warp == 9;
-        const uint32_t idesc_s = idesc_f16kind(128, TILE_KEYS, FP8, false, false);
-        const uint32_t idesc_pv = idesc_f16kind(128, S_::SUB_COLS, FP8, false, true);
-        uint32_t gt = 0, ua = 0, gbase = 0;  // tiles, active units, first sub-tile of the unit
+    } else if (warp == 9) {
+        // ================= MMA issuer: S^T = K . Q^T =================
+        const uint32_t idesc = FP8 ? idesc_f8_e4m3(128, NQ) : idesc_f16kind(128, NQ, false, false, false);
+        uint32_t gs = 0, ua = 0, gk = 0;  // tile groups, active units, K sub-tiles consumed
         bool ok = true;
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
-            if (!warp_wait(ufull + 8 * ub, uph, abort_flag)) { ok = false; break; }
+            if (!warp_wait<SLEEP_MMA>(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
             const int it_u = tables[ub].iter;
             if (it_u < 0) break;
-            int u;
-            const UnitInfo ui = unit_info(p, it_u, u);
+            const UnitInfo ui = tables[ub].ui;
+            const int u = ui.u;
+            (void)u;
             __syncwarp();
-            if (!s_role && lane == 0) mbar_arrive(ufree + 8 * ub);  // done with the unit table
-            if (s_role) {
-                const uint32_t qs = p.QB == 2 ? ub : 0u, qph = p.QB == 2 ? uph : (ua & 1u);  // Q buffer, phase
-                if (!warp_wait((FP8 ? qconv : qfull) + 8 * qs, qph, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t q_addr = s_q + qs * QBUF;
-                for (int t = 0; t < ui.T; ++t) {
-                    // S(t) = Q . K_t^T into S buffer t & 1 (of the CTA's tile count)
-                    const uint32_t g_t = gt + (uint32_t)t, sb = g_t & 1u;
-                    if (!warp_wait(sfree + 8 * sb, ((g_t >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+            if (lane == 0) mbar_arrive(ufree + 8 * ub);
+            const uint32_t qs = ua % (uint32_t)p.QB, qph = (ua / (uint32_t)p.QB) & 1u;
+            if (!warp_wait<SLEEP_MMA>(qfull + 8 * qs, qph, abort_flag, wns)) { ok = false; break; }
+            tc_fence_after();
+            for (int t0 = 0; t0 < ui.T; t0 += p.TPI, ++gs) {
+                // a group of up to TPI tiles: each tile's S into its own NQ columns of the group's
+                // S buffer, one "full" signal for the group
+                const uint32_t sb = gs % (uint32_t)p.NSB;
+                const int nt = min(p.TPI, ui.T - t0);
+                if (!warp_wait<SLEEP_MMA>(sfree + 8 * sb, ((gs / (uint32_t)p.NSB) & 1u) ^ 1u, abort_flag, wns)) {
+                    ok = false;
+                    break;
+                }
+#pragma unroll 1
+                for (int i = 0; i < nt && ok; ++i) {
+                const int t = t0 + i;
 #pragma unroll
-                    for (int h = 0; h < S_::NSUB; ++h) {
-                        const uint32_t g = gbase + (uint32_t)(t * 2 * S_::NSUB + h), st = g % p.NS;
-                        if (!warp_wait(op_full + 8 * st, (g / p.NS) & 1u, abort_flag)) { ok = false; break; }
-                        fence_proxy_async_smem();  // cp.async data -> tensor core reads
-                        tc_fence_after();
-                        if (lane == 0) {
-                            const uint32_t kb = s_op + st * S_::OP_STAGE;
-#pragma unroll
-                            for (int kl = 0; kl < S_::SUB_COLS / 16; ++kl) {
-                                const int ks = h * (S_::SUB_COLS / 16) + kl;  // k step over all of d
-                                mma_bf16(t_s + sb * TILE_KEYS,
-                                         desc_kmajor_sw128(q_addr + (ks >> 2) * QATOM + (ks & 3) * 32),
-                                         desc_kmajor_sw128(kb + (kl >> 2) * (TILE_KEYS * 128) + (kl & 3) * 32),
-                                         idesc_s, ks > 0 ? 1u : 0u);
-                            }
-                            mma_commit(op_empty + 8 * st);
-                        }
-                        __syncwarp();
-                    }
-                    if (!ok) break;
+                for (int h = 0; h < S_::NSUB; ++h) {
+                    const uint32_t g = gk++, st = g % (uint32_t)p.NK;
+                    if (!warp_wait<SLEEP_MMA>(kfull + 8 * st, (g / (uint32_t)p.NK) & 1u, abort_flag, wns)) { ok = false; break; }
+                    if (!FP8) fence_proxy_async_smem();  // cp.async data -> tensor core reads
+                    tc_fence_after();
                     if (lane == 0) {
-                        mma_commit(sfull + 8 * sb);
-                        // the unit's last S: its Q buffer is free once these MMAs complete
-                        if (t == ui.T - 1) mma_commit(qfree + 8 * qs);
+                        const uint32_t kb = s_k + st * S_::K_STAGE;
+                        const uint32_t d_s = tmem + (sb * (uint32_t)p.TPI + (uint32_t)i) * (uint32_t)NQ;
+                        if (FP8) {
+                            // S = K . (hi + lo)^T: both E4M3 parts accumulate into one S
+#pragma unroll
+                            for (int part = 0; part < 2; ++part) {
+                                const uint32_t qa = s_q8 + (qs * 2 + part) * Q8PART;
+#pragma unroll
+                                for (int kl = 0; kl < S_::SUB / 32; ++kl) {
+                                    const int ks = h * (S_::SUB / 32) + kl;  // 32-byte step over all of d
+                                    const uint32_t qoff = S_::Q8ROW == 128 ? (ks >> 2) * Q8ATOM + (ks & 3) * 32
+                                                                           : (uint32_t)ks * 32;
+                                    mma_f8(d_s, desc_kmajor(kb + kl * 32, S_::K8ROW, 8 * S_::K8ROW),
+                                           desc_kmajor(qa + qoff, S_::Q8ROW, 8 * S_::Q8ROW), idesc,
+                                           (h > 0 || part > 0 || kl > 0) ? 1u : 0u);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int kl = 0; kl < S_::SUB / 16; ++kl) {
+                                const int ks = h * (S_::SUB / 16) + kl;  // 16-element step over all of d
+                                mma_bf16(d_s, desc_kmajor(kb + (kl >> 2) * (TILE_KEYS * 128) + (kl & 3) * 32, 128, 1024),
+                                         desc_kmajor(s_q + qs * QBUF + (ks >> 2) * QATOM + (ks & 3) * 32, 128, 1024),
+                                         idesc, ks > 0 ? 1u : 0u);
+                            }
+                        }
+                        mma_commit(kempty + 8 * st);
                     }
                     __syncwarp();
                 }
-            } else {
-                const uint32_t ob = p.OB == 2 ? (ua & 1u) : 0u;
-                const uint32_t ob_use = p.OB == 2 ? (ua >> 1) : ua;
-                if (!warp_wait(ofree + 8 * ob, (ob_use & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                for (int t = 0; t < ui.T; ++t) {
-                    // O += P(t) . V_t
-                    const uint32_t g_t = gt + (uint32_t)t, pb = g_t & 1u;
-                    if (!warp_wait(pfull + 8 * pb, (g_t >> 1) & 1u, abort_flag)) { ok = false; break; }
-                    const int nvk = ui.kv_end - (ui.s0 + t * TILE_KEYS);  // valid keys in this tile
-#pragma unroll
-                    for (int nb = 0; nb < S_::NSUB; ++nb) {
-                        const uint32_t g = gbase + (uint32_t)(t * 2 * S_::NSUB + S_::NSUB + nb), st = g % p.NS;
-                        if (!warp_wait(op_full + 8 * st, (g / p.NS) & 1u, abort_flag)) { ok = false; break; }
-                        fence_proxy_async_smem();  // cp.async data -> tensor core reads
-                        if (nvk < TILE_KEYS) {
-                            // keys past the branch's last position: zero their V rows (NaN-safe P.V)
-                            uint4 *vb = reinterpret_cast<uint4 *>(smem + p.off_op + st * S_::OP_STAGE);
-                            const int rows = TILE_KEYS - nvk;
-                            for (int i = lane; i < rows * S_::NATOM_SUB * 8; i += 32) {
-                                const int a = i / (rows * 8), rem = i % (rows * 8);
-                                const int r = nvk + rem / 8, c = rem % 8;
-                                vb[(a * TILE_KEYS * 128 + r * 128) / 16 + c] = make_uint4(0, 0, 0, 0);
-                            }
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                        }
-                        tc_fence_after();
-                        if (lane == 0) {
-                            const uint32_t vb = s_op + st * S_::OP_STAGE, pa = s_p + pb * PBUF;
-#pragma unroll
-                            for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
-                                mma_bf16(t_o + ob * D + nb * 128, desc_kmajor_sw128(pa + (ks >> 2) * PATOM + (ks & 3) * 32),
-                                         desc_mnmajor_sw128(vb + ks * 2048, TILE_KEYS * 128), idesc_pv,
-                                         (t > 0 || ks > 0) ? 1u : 0u);
-                            mma_commit(op_empty + 8 * st);
-                        }
-                        __syncwarp();
-                    }
-                    if (!ok) break;
-                    if (lane == 0) {
-                        mma_commit(pfree + 8 * pb);
-                        mma_commit(odone);
-                    }
-                    __syncwarp();
                 }
+                if (!ok) break;
+                if (lane == 0) {
+                    mma_commit(sfull + 8 * sb);
+                    // the unit's last S: its Q buffers are free once these MMAs complete
+                    if (t0 + nt == ui.T) mma_commit(qfree + 8 * qs);
+                }
+                __syncwarp();
             }
             if (!ok) break;
-            gbase += (uint32_t)(2 * S_::NSUB * ui.T);
-            gt += (uint32_t)ui.T;
             ++ua;
         }
         if (!ok) {
@@ -539,262 +569,308 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             if (lane == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
         if (lane == 0) {
-            mma_commit(drain + 8 * (s_role ? 0 : 1));
-            mbar_wait(drain + 8 * (s_role ? 0 : 1), 0, nullptr, ATT_WAIT_NS);
-            // every arrive sent by the commits of either issuer is delivered before the CTA
-            // may exit: the last phase of each operand stage's "empty" barrier, of both P and
-            // Q buffers' "free" barriers and of the P.V completion barrier
-            const uint32_t n_last = gbase < (uint32_t)p.NS ? gbase : (uint32_t)p.NS;
-            for (uint32_t j = 0; j < n_last; ++j) {
-                const uint32_t i2 = gbase - 1 - j;
-                mbar_wait(op_empty + 8 * (i2 % p.NS), (i2 / p.NS) & 1u, nullptr, ATT_WAIT_NS);
-            }
-            for (uint32_t j = 0; j < 2 && j < gt; ++j) {
-                const uint32_t t2 = gt - 1 - j;
-                mbar_wait(pfree + 8 * (t2 & 1u), (t2 >> 1) & 1u, nullptr, ATT_WAIT_NS);
+            mma_commit(drain);
+            mbar_wait(drain, 0, nullptr, ATT_WAIT_NS);
+            // every arrive sent by this issuer's commits is delivered before the CTA may exit:
+            // the last phase of the S buffers' "full" barriers and of the Q buffers' "free"
+            // (the ring's "empty" phases are drained by the loaders' waits below)
+            for (uint32_t j = 0; j < (uint32_t)p.NSB && j < gs; ++j) {
+                const uint32_t t2 = gs - 1 - j;
+                mbar_wait(sfull + 8 * (t2 % (uint32_t)p.NSB), (t2 / (uint32_t)p.NSB) & 1u, nullptr, ATT_WAIT_NS);
             }
             for (uint32_t j = 0; j < (uint32_t)p.QB && j < ua; ++j) {
                 const uint32_t i2 = ua - 1 - j;
-                mbar_wait(qfree + 8 * (p.QB == 2 ? (i2 & 1u) : 0u), p.QB == 2 ? (i2 >> 1) & 1u : i2 & 1u, nullptr,
-                          ATT_WAIT_NS);
+                mbar_wait(qfree + 8 * (i2 % (uint32_t)p.QB), (i2 / (uint32_t)p.QB) & 1u, nullptr, ATT_WAIT_NS);
             }
-            if (gt > 0) mbar_wait(odone, (gt - 1) & 1u, nullptr, ATT_WAIT_NS);
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
-        // ================= softmax: one warp per TMEM lane quadrant =================
-        // The queries are held in p.copies copies on the TMEM lanes (a copy spans p.qpc lane
-        // quadrants), so that each of the four SM sub-partitions has a warp that can read
-        // their scores. A warp takes the tile's 32-key quarters of its copy (copy c owns
-        // quarters [c*nqw, (c+1)*nqw)); the copies exchange only the row's partial maxima per
-        // tile, and each warp keeps one partial row sum per quarter, added once per unit in a
-        // fixed order. P is written for the rows of copy 0, whose lanes of O the P.V MMA
-        // accumulates; only copy 0's warps rescale and read out O.
-        const int qd = warp & 3;                     // TMEM lane quadrant
-        const int QPC = p.qpc, C = p.copies;         // quadrants per copy, copies
-        const int cpy = qd / QPC, qq = qd % QPC;     // this warp's copy, quadrant within it
-        const int nqw = 4 / C;                       // 32-key quarters per warp (1 or 2)
-        const int kq0 = cpy * nqw;                   // first quarter of this warp
-        const bool owner = cpy == 0;                 // copy 0: the rows of O
-        const bool active = cpy < C;                 // quadrants past the last copy idle
-        const int prow_i = qq * 32 + lane;           // row of P, lane of O (copy 0)
-        int myq;                                     // the query this lane holds
-        bool vrow;
-        if (p.split) {
-            myq = qq == 0 ? lane : p.J1 * p.G + lane;
-            vrow = lane < (qq == 0 ? p.J1 : p.k + 1 - p.J1) * p.G;
-        } else {
-            myq = qq * 32 + lane;
-            vrow = myq < n_q;
-        }
-        const int jrow = vrow ? myq / p.G : 0;  // the row's draft index j
-        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-        const uint32_t olane_base = (uint32_t)(qq * 32) << 16;  // copy 0's lanes of O
-        const float sl = p.scale_log2;
-        constexpr int QC = 32;  // key columns per quarter
-        // row-maximum exchange [2 tiles][qq][copy][32], then row-sum exchange
-        // [2 units][qq][quarter][32]
-        float *xch = reinterpret_cast<float *>(small + 64);
-        uint32_t gs = 0, gp = 0, ua = 0;
+    } else if (warp == 10) {
+        // ================= MMA issuer: O^T += V^T . P^T, L += 1 . P^T =================
+        const uint32_t idesc_pv = idesc_f16kind(128, NQ, false, true, true);
+        const uint32_t idesc_l = idesc_f16kind(128, NQ, false, false, true);
+        // V's MN-major descriptor: 64-column blocks 128 keys x 128 bytes apart; a 64-wide
+        // head dimension repeats its one block on lanes 64..127 (never read)
+        const uint32_t v_lbo = S_::SUB == 128 ? TILE_KEYS * 128 : 0;
+        uint32_t gp = 0, gv = 0, ua = 0;  // tile groups, V sub-tiles consumed, units
         bool ok = true;
-        while (active && ok) {
+        for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
-            const uint32_t ob = p.OB == 2 ? (ua & 1u) : 0u;
-            if (!warp_wait(ufull + 8 * ub, uph, abort_flag)) { ok = false; break; }
+            if (!warp_wait<SLEEP_MMA>(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
+            const int it_u = tables[ub].iter;
+            if (it_u < 0) break;
+            const UnitInfo ui = tables[ub].ui;
+            const int u = ui.u;
+            (void)u;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ufree + 8 * ub);
+            const uint32_t ob = ua % (uint32_t)p.OB;
+            if (!warp_wait<SLEEP_MMA>(ofree + 8 * ob, ((ua / (uint32_t)p.OB) & 1u) ^ 1u, abort_flag, wns)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_o = t_o0 + ob * (uint32_t)((S_::NSUB + 1) * NQ);
+            for (int t0 = 0; t0 < ui.T; t0 += p.TPI, ++gp) {
+                const uint32_t pb = gp % (uint32_t)p.NPB;
+                const int nt = min(p.TPI, ui.T - t0);
+                if (!warp_wait<SLEEP_MMA>(pfull + 8 * pb, (gp / (uint32_t)p.NPB) & 1u, abort_flag, wns)) { ok = false; break; }
+#pragma unroll 1
+                for (int i = 0; i < nt && ok; ++i) {
+                const int t = t0 + i;
+                const uint32_t pa = s_p + pb * PBUF + (uint32_t)i * PTILE;
+#pragma unroll
+                for (int h = 0; h < S_::NSUB; ++h) {
+                    const uint32_t st = gv % (uint32_t)p.NV;
+                    if (!warp_wait<SLEEP_MMA>(vfull + 8 * st, (gv / (uint32_t)p.NV) & 1u, abort_flag, wns)) { ok = false; break; }
+                    if (!FP8) fence_proxy_async_smem();  // cp.async data -> tensor core reads
+                    const uint32_t vb = s_v + st * S_::OP_STAGE, rel = vempty + 8 * st;
+                    ++gv;
+                    tc_fence_after();
+                    if (lane == 0) {
+#pragma unroll
+                        for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
+                            mma_bf16(d_o + h * NQ, desc_mnmajor_sw128(vb + ks * 2048, v_lbo),
+                                     desc_mnmajor_sw32(pa + ks * 512, TILE_KEYS * 32), idesc_pv,
+                                     (t > 0 || ks > 0) ? 1u : 0u);
+                        mma_commit(rel);
+                    }
+                    __syncwarp();
+                }
+                }
+                if (!ok) break;
+                if (lane == 0) {
+                    for (int i = 0; i < nt; ++i) {
+                        const int t = t0 + i;
+                        const uint32_t pa = s_p + pb * PBUF + (uint32_t)i * PTILE;
+#pragma unroll
+                        for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
+                            mma_bf16(d_o + S_::NSUB * NQ, desc_kmajor(s_ones + (ks & 3) * 32, 128, 0),
+                                     desc_mnmajor_sw32(pa + ks * 512, TILE_KEYS * 32), idesc_l,
+                                     (t > 0 || ks > 0) ? 1u : 0u);
+                    }
+                    mma_commit(pfree + 8 * pb);  // also: this group's O and L are complete
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            ++ua;
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
+        }
+        if (lane == 0) {
+            mma_commit(drain + 8);
+            mbar_wait(drain + 8, 0, nullptr, ATT_WAIT_NS);
+            // the last phases of the P buffers' "free" barriers and of the P.V completion
+            for (uint32_t j = 0; j < (uint32_t)p.NPB && j < gp; ++j) {
+                const uint32_t t2 = gp - 1 - j;
+                mbar_wait(pfree + 8 * (t2 % (uint32_t)p.NPB), (t2 / (uint32_t)p.NPB) & 1u, nullptr, ATT_WAIT_NS);
+            }
+            if (FP8) {  // (bf16: the V loaders drain the V ring's "empty" phases)
+                const uint32_t n_last = gv < (uint32_t)p.NV ? gv : (uint32_t)p.NV;
+                for (uint32_t j = 0; j < n_last; ++j) {
+                    const uint32_t i2 = gv - 1 - j;
+                    mbar_wait(vempty + 8 * (i2 % (uint32_t)p.NV), (i2 / (uint32_t)p.NV) & 1u, nullptr, ATT_WAIT_NS);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ================= softmax: one warp per TMEM lane quadrant =================
+        const int qd = warp;
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        const int kl = qd * 32 + lane;           // this thread's key within a tile
+        float *my_m = sx_m + qd * NQ, *my_f = sx_f + qd * NQ;
+        int *my_lim = sx_lim + qd * NQ;
+        const float sl = p.scale_log2;
+        const int nch = NQ / 16;                 // 16-column chunks
+        uint32_t gs = 0, gp = 0, ua = 0;  // tile groups (S side, P side), units
+        bool ok = true;
+        while (ok) {
+            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+            if (!warp_wait(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
             const UnitTable *tab = tables + ub;
             const int it_u = tab->iter;
             if (it_u < 0) break;
-            int u;
-            const UnitInfo ui = unit_info(p, it_u, u);
-            float *ml = p.ws_ml + (size_t)u * n_q * 2;
+            const UnitInfo ui = tables[ub].ui;
+            const int u = ui.u;
+            (void)u;
             const bool failed = tab->bad != 0;
-            float m = -INFINITY;             // running maximum (log2 units)
-            float lq[2] = {0.f, 0.f};        // this warp's partial sums, one per quarter
-            // key offsets (from the split's start) this row sees: [0, climit0]; a lane without
-            // a query treats every key as seen (its row of P only feeds an unread row of O)
-            const int climit0 = vrow ? ui.pos_b + jrow - ui.s0 : (1 << 30);
-            for (int t = 0; t < ui.T; ++t, ++gs, ++gp) {
-                const uint32_t sb = gs & 1u, pb = gp & 1u;
-                if (ok) ok = warp_wait(sfull + 8 * sb, (gs >> 1) & 1u, abort_flag);
-                if (!ok) continue;
+            const uint32_t ob = ua % (uint32_t)p.OB;
+            // the E4M3 query scales of this unit: written by the producer before it published
+            // the table, rewritten only for unit ua + 2 (after this warp releases the table)
+            const float *qinv = sx_qinv + ub * NQ;
+            // per unit: running maxima, and the last key offset (from the split's start) each
+            // column sees: row j of the branch sees positions <= pos_b + j
+            for (int q = lane; q < NQ; q += 32) {
+                my_m[q] = -INFINITY;
+                my_lim[q] = q < n_q ? ui.pos_b + sx_colj[q] - ui.s0 : -1;
+            }
+            __syncwarp();
+            for (int t0 = 0; t0 < ui.T && ok; t0 += p.TPI, ++gs, ++gp) {
+                // a group of nt <= TPI tiles: one column-maximum exchange, one update of the
+                // running maxima and one P hand-off for all of its keys
+                const uint32_t sb = gs % (uint32_t)p.NSB, pb = gp % (uint32_t)p.NPB, tb = gs & 1u;
+                const int nt = min(p.TPI, ui.T - t0);
+                ok = warp_wait(sfull + 8 * sb, (gs / (uint32_t)p.NSB) & 1u, abort_flag, wns);
+                if (!ok) break;
                 tc_fence_after();
-                uint32_t sv[2][2][16];  // [quarter of this warp][16-column block][column]
+                const uint32_t sgrp = tmem + lane_base + sb * (uint32_t)(p.TPI * NQ);
+                // x of column q for this thread's key of tile i = s * slk (* 1/sigma for E4M3
+                // queries; slk = softmax scale, times the K page scale for FP8 pools), -inf where
+                // the key is not seen by the column's row; a warp whose 32 keys every row sees
+                // skips the limits (the padding columns then hold finite zero scores: their Q
+                // rows are 0)
+                auto xchunk = [&](int i, int c, const uint32_t (&r)[16], float (&x)[16]) {
+                    const int koff = (t0 + i) * TILE_KEYS + kl;  // key offset from the split's start
+                    float slk = sl;
+                    if (FP8) slk = ui.s0 + koff < ui.kv_end ? sl * tab->ksc[koff >> log2P] : 0.f;
+                    const bool all_vis = __all_sync(0xFFFFFFFFu, koff <= ui.pos_b - ui.s0);
+                    float qsc[16];
+                    if (FP8) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
-                    if (i < nqw) {
-#pragma unroll
-                        for (int c = 0; c < 2; ++c)
-                            tmem_ld16(t_s + lane_base + sb * TILE_KEYS + QC * (kq0 + i) + c * 16, sv[i][c]);
-                    }
-                // FP8 pools: the scores come from E4M3 codes and P multiplies E4M3 codes of V.
-                // A quarter's K scale joins the softmax scale and its V scale multiplies P (the
-                // row sum stays unscaled); with pages shorter than a quarter the scales are
-                // applied per key.
-                float slk[2] = {sl, sl}, vmul[2] = {1.f, 1.f};
-                const bool percol = FP8 && (small_pages || p.kv.page_size < QC);
-                if (FP8 && !percol) {
-#pragma unroll
-                    for (int i = 0; i < 2; ++i)
-                        if (i < nqw) {
-                            const int e = (t * TILE_KEYS + QC * (kq0 + i)) >> log2P;
-                            slk[i] = sl * tab->ksc[e];
-                            vmul[i] = tab->vsc[e];
+                        for (int j = 0; j < 16; j += 4) {
+                            const float4 a = *reinterpret_cast<const float4 *>(qinv + c * 16 + j);
+                            qsc[j] = a.x; qsc[j + 1] = a.y; qsc[j + 2] = a.z; qsc[j + 3] = a.w;
                         }
-                }
-                auto col_scales = [&](int qi, int c, float &ks, float &vs) {
-                    const int key = ui.s0 + t * TILE_KEYS + QC * (kq0 + qi) + c;
-                    ks = 0.f;
-                    vs = 0.f;
-                    if (key >= ui.kv_end) return;
-                    if (!small_pages) {
-                        const int e = (key - ui.s0) >> log2P;
-                        ks = tab->ksc[e];
-                        vs = tab->vsc[e];
-                    } else {
-                        const int pg = page_of(p.kv, ui.b, key);
-                        if (pg >= 0) {
-                            ks = __ldg(p.kv.k_scale + (size_t)pg * p.kv.n_kv_heads + ui.g);
-                            vs = __ldg(p.kv.v_scale + (size_t)pg * p.kv.n_kv_heads + ui.g);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) x[j] = FP8 ? (__uint_as_float(r[j]) * slk) * qsc[j] : __uint_as_float(r[j]) * slk;
+                    if (!all_vis) {
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            const int4 a = *reinterpret_cast<const int4 *>(my_lim + c * 16 + j);
+                            x[j] = koff <= a.x ? x[j] : -INFINITY;
+                            x[j + 1] = koff <= a.y ? x[j + 1] : -INFINITY;
+                            x[j + 2] = koff <= a.z ? x[j + 2] : -INFINITY;
+                            x[j + 3] = koff <= a.w ? x[j + 3] : -INFINITY;
                         }
                     }
                 };
-                tmem_ld_wait();
-                if (percol) {
-#pragma unroll
-                    for (int i = 0; i < 2; ++i)
-                        if (i < nqw) {
-#pragma unroll
-                            for (int c = 0; c < QC; ++c) {
-                                float ks, vs;
-                                col_scales(i, c, ks, vs);
-                                sv[i][c >> 4][c & 15] = __float_as_uint(__uint_as_float(sv[i][c >> 4][c & 15]) * ks);
-                            }
-                        }
-                }
-                // ---- pass 1: partial maximum of s*slk over the seen columns of each quarter ----
-                float pm = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    if (i >= nqw) continue;
-                    // columns c (of this quarter) with QC*(kq0+i) + c <= climit are seen
-                    const int climit = climit0 - t * TILE_KEYS - QC * (kq0 + i);
-                    const bool all_seen = __all_sync(0xFFFFFFFFu, climit >= QC - 1);
-                    float acc[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = -INFINITY;
-                    const float sgn = slk[i] >= 0.f ? 1.f : -1.f;
-                    if (all_seen) {
-#pragma unroll
-                        for (int c = 0; c < QC; ++c)
-                            acc[c & 7] = fmaxf(acc[c & 7], sgn * __uint_as_float(sv[i][c >> 4][c & 15]));
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < QC; ++c)
-                            if (c <= climit) acc[c & 7] = fmaxf(acc[c & 7], sgn * __uint_as_float(sv[i][c >> 4][c & 15]));
-                    }
-                    float q = fmaxf(fmaxf(fmaxf(acc[0], acc[1]), fmaxf(acc[2], acc[3])),
-                                    fmaxf(fmaxf(acc[4], acc[5]), fmaxf(acc[6], acc[7])));
-                    // q = max of sgn*s: the quarter's maximum of s*slk is q*|slk|
-                    q = (q == -INFINITY || q == INFINITY) ? -INFINITY : q * (sgn * slk[i]);
-                    pm = fmaxf(pm, q);
-                }
-                // ---- the row's maximum: exchange with the other copies ----
-                float mx = pm;
-                if (C > 1) {
-                    float *xt = xch + sb * 128 + qq * C * 32;
-                    xt[cpy * 32 + lane] = pm;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xfull + 8 * (qq * 2 + sb));
-                    ok = warp_wait(xfull + 8 * (qq * 2 + sb), (gs >> 1) & 1u, abort_flag);
-                    if (!ok) continue;
-                    for (int c = 0; c < C; ++c) mx = fmaxf(mx, xt[c * 32 + lane]);
-                }
-                if (!vrow) mx = -INFINITY;
-                // ---- the P buffer is free once P.V of tile t-2 is done ----
-                ok = warp_wait(pfree + 8 * pb, ((gp >> 1) & 1u) ^ 1u, abort_flag);
-                if (!ok) continue;
-                // ---- lazily raised maximum; a move rescales l and the row of O ----
-                const float mnew = (mx > m + RESCALE_TAU) ? mx : m;
-                const bool resc = mnew != m && m != -INFINITY;
-                if (__any_sync(0xFFFFFFFFu, resc)) {
-                    const float f = resc ? ex2_approx(m - mnew) : 1.f;
-                    lq[0] *= f;
-                    lq[1] *= f;
-                    if (owner) {
-                        // O is written by P.V of tile t-1 (the one before it is done: see above)
-                        ok = warp_wait(odone, (gp - 1) & 1u, abort_flag);
-                        if (!ok) continue;
-                        tc_fence_after();
-                        const uint32_t orow = t_o + olane_base + ob * D;
+                // ---- pass 1: the group's column maxima over this warp's keys ----
+                float *red = sx_red + tb * 4 * NQ + qd * NQ;
+                bool need = false;
 #pragma unroll 1
-                        for (int c0 = 0; c0 < D; c0 += 32) {
-                            uint32_t r[2][16];
+                for (int c = 0; c < nch; ++c) {
+                    float v[16];
 #pragma unroll
-                            for (int e = 0; e < 2; ++e) tmem_ld16(orow + c0 + 16 * e, r[e]);
+                    for (int j = 0; j < 16; ++j) v[j] = -INFINITY;
+#pragma unroll 1
+                    for (int i = 0; i < nt; ++i) {
+                        uint32_t r[16];
+                        float x[16];
+                        tmem_ld16(sgrp + (uint32_t)(i * NQ + c * 16), r);
+                        tmem_ld_wait();
+                        xchunk(i, c, r, x);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] = fmaxf(v[j], x[j]);
+                    }
+                    // butterfly: halves exchanged at lane distances 16, 8, 4, 2, then a full
+                    // exchange at 1; even lane l ends with the maximum of column
+                    // c*16 + (bit 4 of l)*8 + (bit 3)*4 + (bit 2)*2 + (bit 1)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const bool up = (lane & 16) != 0;
+                        const float got = __shfl_xor_sync(0xFFFFFFFFu, up ? v[j] : v[j + 8], 16);
+                        v[j] = fmaxf(up ? v[j + 8] : v[j], got);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const bool up = (lane & 8) != 0;
+                        const float got = __shfl_xor_sync(0xFFFFFFFFu, up ? v[j] : v[j + 4], 8);
+                        v[j] = fmaxf(up ? v[j + 4] : v[j], got);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const bool up = (lane & 4) != 0;
+                        const float got = __shfl_xor_sync(0xFFFFFFFFu, up ? v[j] : v[j + 2], 4);
+                        v[j] = fmaxf(up ? v[j + 2] : v[j], got);
+                    }
+                    {
+                        const bool up = (lane & 2) != 0;
+                        const float got = __shfl_xor_sync(0xFFFFFFFFu, up ? v[0] : v[1], 2);
+                        v[0] = fmaxf(up ? v[1] : v[0], got);
+                    }
+                    v[0] = fmaxf(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], 1));
+                    const int col = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+                    if ((lane & 1) == 0) red[c * 16 + col] = v[0];
+                    need |= v[0] > my_m[c * 16 + col] + RESCALE_TAU;  // this column's maximum must move
+                }
+                need = __any_sync(0xFFFFFFFFu, need);
+                if (lane == 0) sx_need[tb * 4 + qd] = need ? 1 : 0;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xbar + 8 * tb);
+                ok = warp_wait(xbar + 8 * tb, (gs >> 1) & 1u, abort_flag, wns);
+                if (!ok) break;
+                // ---- the group's maxima over the four warps; lazily raised running maxima (only
+                // when some warp saw a column exceed its maximum by more than RESCALE_TAU) ----
+                bool resc = false;
+                const float *red_all = sx_red + tb * 4 * NQ;
+                const int4 nd = *reinterpret_cast<const int4 *>(sx_need + tb * 4);
+                const bool any_need = (nd.x | nd.y | nd.z | nd.w) != 0;
+#pragma unroll 1
+                for (int q = lane; any_need && q < NQ; q += 32) {
+                    const float M = fmaxf(fmaxf(red_all[q], red_all[NQ + q]), fmaxf(red_all[2 * NQ + q], red_all[3 * NQ + q]));
+                    const float mo = my_m[q];
+                    const float mn = (M > mo + RESCALE_TAU) ? M : mo;
+                    my_f[q] = mn == mo ? 1.f : (mo == -INFINITY ? 0.f : ex2_approx(mo - mn));
+                    resc |= mn != mo && mo != -INFINITY;
+                    my_m[q] = mn;
+                }
+                __syncwarp();
+                if (any_need && __any_sync(0xFFFFFFFFu, resc)) {
+                    // a running maximum moved: O and L of this unit are rescaled per column, after
+                    // the P.V of the previous group (this unit's: t0 > 0 here) has completed. Its
+                    // completion is the phase of its P buffer's "free" barrier that follows the
+                    // one this warp waited for before writing that P (a wait is never two
+                    // phases behind)
+                    ok = warp_wait(pfree + 8 * ((gp - 1) % (uint32_t)p.NPB), ((gp - 1) / (uint32_t)p.NPB) & 1u,
+                                   abort_flag, wns);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t orow = t_o0 + lane_base + ob * (uint32_t)((S_::NSUB + 1) * NQ);
+#pragma unroll 1
+                    for (int h = 0; h <= S_::NSUB; ++h) {
+#pragma unroll 1
+                        for (int c = 0; c < nch; ++c) {
+                            uint32_t r[16];
+                            tmem_ld16(orow + h * NQ + c * 16, r);
                             tmem_ld_wait();
 #pragma unroll
-                            for (int e = 0; e < 2; ++e) {
-#pragma unroll
-                                for (int j = 0; j < 16; ++j) r[e][j] = __float_as_uint(__uint_as_float(r[e][j]) * f);
-                                tmem_st16(orow + c0 + 16 * e, r[e]);
-                            }
+                            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * my_f[c * 16 + j]);
+                            tmem_st16(orow + h * NQ + c * 16, r);
                         }
-                        tmem_st_wait();
                     }
+                    tmem_st_wait();
                 }
-                m = mnew;
-                // ---- pass 2: P = 2^(s*slk - m) of this warp's quarters, into copy 0's rows ----
-                uint8_t *prow = g_p + pb * PBUF + prow_i * 128;
-                const int swz = prow_i & 7;
+                // ---- pass 2: this thread's key rows of P^T, P = 2^(x - m) (0 where the key is not seen) ----
+                ok = warp_wait(pfree + 8 * pb, ((gp / (uint32_t)p.NPB) & 1u) ^ 1u, abort_flag, wns);
+                if (!ok) break;
+                uint8_t *prow = smem + p.off_p + pb * PBUF + kl * 32;
+                const int sw = (kl >> 2) & 1;  // 32-byte swizzle: 16-byte chunk index ^= row bit 2
+#pragma unroll 1
+                for (int i = 0; i < nt; ++i) {
+#pragma unroll 1
+                    for (int c = 0; c < nch; ++c) {
+                        uint32_t r[16];
+                        float x[16], m[16];
+                        tmem_ld16(sgrp + (uint32_t)(i * NQ + c * 16), r);
+                        tmem_ld_wait();
+                        xchunk(i, c, r, x);
 #pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    if (i >= nqw) continue;
-                    const int kq = kq0 + i;
-                    const int climit = climit0 - t * TILE_KEYS - QC * kq;
-                    const bool all_seen = __all_sync(0xFFFFFFFFu, climit >= QC - 1);
-                    float lacc[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) lacc[e] = 0.f;
-                    uint8_t *pq = prow + (kq >> 1) * PATOM;
-#pragma unroll
-                    for (int c0 = 0; c0 < QC; c0 += 16) {
-                        const uint32_t(&r)[16] = sv[i][c0 >> 4];
+                        for (int j = 0; j < 16; j += 4) {
+                            const float4 a = *reinterpret_cast<const float4 *>(my_m + c * 16 + j);
+                            m[j] = a.x; m[j + 1] = a.y; m[j + 2] = a.z; m[j + 3] = a.w;
+                        }
                         uint32_t pk[8];
-                        if (all_seen && !percol) {
 #pragma unroll
-                            for (int j = 0; j < 16; j += 2) {
-                                const float a = ex2_approx(fmaf(__uint_as_float(r[j]), slk[i], -m));
-                                const float b = ex2_approx(fmaf(__uint_as_float(r[j + 1]), slk[i], -m));
-                                lacc[j >> 1] += a + b;
-                                pk[j >> 1] = FP8 ? pack2(a * vmul[i], b * vmul[i], true) : pack2(a, b, false);
-                            }
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 16; j += 2) {
-                                float a = ex2_approx(fmaf(__uint_as_float(r[j]), slk[i], -m));
-                                float b = ex2_approx(fmaf(__uint_as_float(r[j + 1]), slk[i], -m));
-                                a = (c0 + j <= climit) ? a : 0.f;
-                                b = (c0 + j + 1 <= climit) ? b : 0.f;
-                                lacc[j >> 1] += a + b;
-                                float va = vmul[i], vb = vmul[i];
-                                if (percol) {
-                                    float ks;
-                                    col_scales(i, c0 + j, ks, va);
-                                    col_scales(i, c0 + j + 1, ks, vb);
-                                }
-                                pk[j >> 1] = FP8 ? pack2(a * va, b * vb, true) : pack2(a, b, false);
-                            }
+                        for (int j = 0; j < 16; j += 2) {
+                            const float p0 = x[j] == -INFINITY ? 0.f : ex2_approx(x[j] - m[j]);
+                            const float p1 = x[j + 1] == -INFINITY ? 0.f : ex2_approx(x[j + 1] - m[j + 1]);
+                            pk[j >> 1] = pack2(p0, p1, false);
                         }
-                        // 16-byte chunk (within the 128-byte row of the 64-key block) of keys c0..c0+7
-                        const int ch0 = (kq & 1) * 4 + (c0 >> 3);
-                        if (prow_i < p.PR) {
-                            *reinterpret_cast<uint4 *>(pq + (((ch0 ^ swz) & 7) << 4)) =
-                                make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                            *reinterpret_cast<uint4 *>(pq + ((((ch0 + 1) ^ swz) & 7) << 4)) =
-                                make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                        }
+                        uint8_t *blk = prow + i * PTILE + c * (TILE_KEYS * 32);
+                        *reinterpret_cast<uint4 *>(blk + (sw << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                        *reinterpret_cast<uint4 *>(blk + ((sw ^ 1) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                     }
-                    lq[i] += ((lacc[0] + lacc[1]) + (lacc[2] + lacc[3])) + ((lacc[4] + lacc[5]) + (lacc[6] + lacc[7]));
                 }
                 tc_fence_before();
                 fence_proxy_async_smem();
@@ -804,188 +880,147 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
                     mbar_arrive(pfull + 8 * pb);
                 }
             }
+            if (!ok) break;
             // the unit table is no longer read
             __syncwarp();
-            if (ok && lane == 0) mbar_arrive(ufree + 8 * ub);
-            // ---- copy 0: the unit's last P.V (P.V of the tile before it is done first) ----
-            if (owner) {
-                if (ok) ok = warp_wait(pfree + 8 * (gp & 1u), ((gp >> 1) & 1u) ^ 1u, abort_flag);
-                if (ok) ok = warp_wait(odone, (gp - 1) & 1u, abort_flag);
-                if (ok) {
-                    tc_fence_after();
-                    float *orow_g = p.ws_o + ((size_t)u * n_q + myq) * D;
-                    const uint32_t orow = t_o + olane_base + ob * D;
+            if (lane == 0) mbar_arrive(ufree + 8 * ub);
+            // ---- epilogue: the unit's O and L, after its last P.V (see the rescale above) ----
+            ok = warp_wait(pfree + 8 * ((gp - 1) % (uint32_t)p.NPB), ((gp - 1) / (uint32_t)p.NPB) & 1u, abort_flag,
+                           wns);
+            if (!ok) break;
+            tc_fence_after();
+            // the unit's partial: O[q][d] (this lane's d) and, from warp 0, (m, l) per column
+            // (l = -1 marks a unit whose pages were invalid); the combine pass finishes every row
+            const uint32_t orow = t_o0 + lane_base + ob * (uint32_t)((S_::NSUB + 1) * NQ);
+            float *ml = p.ws_ml + (size_t)u * NQ * 2;
+            float *og = p.ws_o + (size_t)u * NQ * D + kl;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
-                        uint32_t r[2][16];
+            for (int c = 0; c < nch; ++c) {
+#pragma unroll 1
+                for (int h = 0; h < S_::NSUB; ++h) {
+                    uint32_t r[16];
+                    tmem_ld16(orow + h * NQ + c * 16, r);
+                    tmem_ld_wait();
+                    if (h * 128 + kl < D) {
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) tmem_ld16(orow + c0 + 16 * e, r[e]);
-                        tmem_ld_wait();
-                        if (vrow) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                reinterpret_cast<float4 *>(orow_g + c0)[e] =
-                                    make_float4(__uint_as_float(r[e >> 2][4 * (e & 3)]),
-                                                __uint_as_float(r[e >> 2][4 * (e & 3) + 1]),
-                                                __uint_as_float(r[e >> 2][4 * (e & 3) + 2]),
-                                                __uint_as_float(r[e >> 2][4 * (e & 3) + 3]));
-                        }
+                        for (int j = 0; j < 16; ++j) og[(size_t)(c * 16 + j) * D + h * 128] = __uint_as_float(r[j]);
                     }
-                    tc_fence_before();
+                }
+                if (qd == 0) {
+                    uint32_t lr[16];
+                    tmem_ld16(orow + S_::NSUB * NQ + c * 16, lr);  // L: the same on every lane
+                    tmem_ld_wait();
+                    float l = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) l = (lane & 15) == j ? __uint_as_float(lr[j]) : l;
+                    if (lane < 16) {
+                        ml[(c * 16 + lane) * 2] = my_m[c * 16 + lane];
+                        ml[(c * 16 + lane) * 2 + 1] = failed ? -1.f : l;
+                    }
                 }
             }
+            tc_fence_before();
             __syncwarp();
-            if (ok && lane == 0) mbar_arrive(ofree + 8 * ob);
-            // ---- the row's sum: the quarters' partial sums, in quarter order ----
-            const uint32_t lb = qq * 2 + (ua & 1u);
-            float *lx = xch + 256 + (ua & 1u) * 256 + qq * 128;
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-                if (i < nqw) lx[(kq0 + i) * 32 + lane] = lq[i];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(lfull + 8 * lb);
-            const bool lok = warp_wait(lfull + 8 * lb, (ua >> 1) & 1u, abort_flag);
-            if (owner && vrow) {
-                const float l = (lx[lane] + lx[32 + lane]) + (lx[64 + lane] + lx[96 + lane]);
-                ml[2 * myq] = m;
-                ml[2 * myq + 1] = (failed || !ok || !lok) ? -1.f : l;
-            }
-            if (!lok) ok = false;
+            if (lane == 0) mbar_arrive(ofree + 8 * ob);
             ++ua;
         }
         if (!ok) {
             *abort_flag = 1;
             if (qd == 0 && lane == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
-    } else if (!FP8 || warp < 2) {
-        // ================= loaders: K / V gather (bf16: warps 0..3; FP8: warps 0, 1) =================
-        // Each thread copies its own 16-byte pieces of every sub-tile with cp.async and lets the
-        // copies arrive on the stage's barrier by themselves when they land
-        // (cp.async.mbarrier.arrive.noinc), so a sub-tile is visible to its consumer as soon as
-        // its data is in shared memory and no loader ever holds data back. bf16 rows go straight
-        // into the swizzled operand stage (the MMA warp fences for the async proxy after its
-        // wait); E4M3 rows go to the raw ring, which the converter warps turn into operand
-        // stages. A loader waits only for a free stage.
-        constexpr int NT = FP8 ? 64 : 128;           // loader threads
-        const int ltid = warp * 32 + lane;  // warps 0..3 (one per SM sub-partition)
-        constexpr int ESZ = FP8 ? 1 : 2;
-        constexpr int CH = S_::SUB_COLS * ESZ / 16;  // 16-byte pieces per row of a sub-tile
-        constexpr int RPS = NT / CH;                 // rows per step of the loader threads
-        constexpr int NPIECE = TILE_KEYS / RPS;      // pieces per thread per sub-tile
+    } else if (!FP8) {
+        // ================= loaders (bf16): warps 4-5 K, warps 6-7 V, by cp.async =================
+        // Each stream has its own ring, so that V stages held until their P.V never hold up
+        // the K loads the S MMAs wait for. Each thread copies its own 16-byte pieces of every
+        // sub-tile and lets the copies arrive on the stage's barrier by themselves when they
+        // land (cp.async.mbarrier.arrive.noinc). Rows past the branch's last position, or of an
+        // invalid page, are zero-filled, so every stage is fully written.
+        const bool is_v = warp >= 6;
+        const int ltid = (warp & 1) * 32 + lane;   // 0..63 within the stream
+        constexpr int CH = S_::SUB * 2 / 16;       // 16-byte pieces per row of a sub-tile
+        constexpr int RPS = 64 / CH;               // rows per step of the 64 stream threads
+        constexpr int NPIECE = TILE_KEYS / RPS;    // pieces per thread per sub-tile
         const int pch = ltid % CH, prow0 = ltid / CH;
-        const size_t row_bytes = (size_t)D * ESZ;
-        const uint32_t depth = FP8 ? (uint32_t)p.NR : (uint32_t)p.NS;
-        const uint32_t full_base = FP8 ? raw_full : op_full, empty_base = FP8 ? raw_empty : op_empty;
-        const uint32_t ring_base = FP8 ? s_raw : s_op;
-        const uint32_t stage_bytes = FP8 ? S_::RAW_STAGE : S_::OP_STAGE;
-        uint32_t gi = 0, ua = 0;  // sub-tiles issued, active units
+        const size_t row_bytes = (size_t)D * 2;
+        const uint8_t *pool = reinterpret_cast<const uint8_t *>(is_v ? p.kv.v_pool : p.kv.k_pool);
+        const int depth = is_v ? p.NV : p.NK;
+        const uint32_t full0 = is_v ? vfull : kfull, empty0 = is_v ? vempty : kempty;
+        const uint32_t ring = is_v ? s_v : s_k;
+        uint32_t gi = 0, ua = 0;  // sub-tiles issued, units
         bool ok = true;
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
             const UnitTable *tab = tables + ub;
-            if (!warp_wait(ufull + 8 * ub, uph, abort_flag)) { ok = false; break; }
+            if (!warp_wait<SLEEP_LOAD>(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
             const int it_u = tab->iter;
             if (it_u < 0) break;
-            int u;
-            const UnitInfo ui = unit_info(p, it_u, u);
+            const UnitInfo ui = tab->ui;
             ++ua;
             for (int t = 0; t < ui.T && ok; ++t) {
                 const int key0 = ui.s0 + t * TILE_KEYS;
-                for (int it = 0; it < 2 * S_::NSUB; ++it) {
-                    const int kv = it / S_::NSUB, h = it % S_::NSUB;  // K or V, half of d
-                    const uint8_t *pool = reinterpret_cast<const uint8_t *>(kv ? p.kv.v_pool : p.kv.k_pool);
-                    const uint32_t s = gi % depth;
-                    if (!warp_wait(empty_base + 8 * s, ((gi / depth) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
-                    const uint32_t dst_base = ring_base + s * stage_bytes;
-                    if (FP8 && p.tma_rows) {
-                        // one TMA box per page-run of rows into the raw stage; loader warp w
-                        // issues runs w, w + 2, ... and announces their bytes on the stage's
-                        // barrier. Runs past the branch's last position or of an invalid page
-                        // are not loaded.
-                        const int BR = p.tma_rows, nruns = TILE_KEYS / BR;
-                        const CUtensorMap *map = kv ? &map_v : &map_k;
-                        if (lane == 0) {
-                            uint32_t bytes = 0;
-                            for (int r = warp; r < nruns; r += 2) {
-                                if (key0 + r * BR >= ui.kv_end) break;
-                                if (tab->page[(t * TILE_KEYS + r * BR) >> log2P] >= 0) bytes += (uint32_t)(BR * S_::SUB_COLS);
-                            }
-                            mbar_arrive_expect_tx(full_base + 8 * s, bytes);
-                            for (int r = warp; r < nruns; r += 2) {
-                                const int kr = key0 + r * BR;
-                                if (kr >= ui.kv_end) break;
-                                const int pg = tab->page[(t * TILE_KEYS + r * BR) >> log2P];
-                                if (pg < 0) continue;
-                                const int row = (pg * p.kv.n_kv_heads + ui.g) * p.kv.page_size + (kr & (p.kv.page_size - 1));
-                                tma_load_2d(dst_base + (uint32_t)(r * BR) * S_::SUB_COLS, map, h * S_::SUB_COLS, row,
-                                            full_base + 8 * s);
-                            }
-                        }
-                        __syncwarp();
-                        ++gi;
-                        continue;
+                // two tiles before the unit's end the producer may prepare the next unit, so that
+                // its table and Q are there when this unit's last copies have been issued
+                if (t == max(0, ui.T - 2)) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(lfin + 8 * ub);
+                }
+                for (int h = 0; h < S_::NSUB; ++h, ++gi) {
+                    const uint32_t s = gi % (uint32_t)depth;
+                    if (!warp_wait<SLEEP_LOAD>(empty0 + 8 * s, ((gi / (uint32_t)depth) & 1u) ^ 1u, abort_flag, wns)) {
+                        ok = false;
+                        break;
                     }
-                    const uint8_t *src_col = pool + (size_t)h * S_::SUB_COLS * ESZ + pch * 16;
-                    // rows past the branch's last position, or of an invalid page, stay unloaded.
-                    // Per group of 8 pieces: the page lookups and offsets first (independent
-                    // loads), then the copies.
-                    constexpr int GRP = NPIECE < 8 ? NPIECE : 8;
+                    const uint32_t dst_base = ring + s * S_::OP_STAGE;
+                    const uint8_t *src_col = pool + (size_t)h * S_::SUB * 2 + pch * 16;
+                    // pages of >= 8 positions: per group of 8 pieces the table lookups first
+                    // (independent loads), then the copies; smaller pages: per-row page-table reads
+                    if (!small_pages) {
 #pragma unroll
-                    for (int k0 = 0; k0 < NPIECE; k0 += GRP) {
-                        uint32_t rowi[GRP];  // row index in the pool viewed as [num_pages * Hkv * P][d]
-                        uint32_t valid = 0;
-                        if (!small_pages) {
-                            int pgk[GRP];
+                        for (int k0 = 0; k0 < NPIECE; k0 += 8) {
+                            int pg[8];
 #pragma unroll
-                            for (int k = 0; k < GRP; ++k) {  // (key - s0) < split_keys: inside the table
-                                const int e = (t * TILE_KEYS + (k0 + k) * RPS + prow0) >> log2P;
-                                pgk[k] = tab->page[e];
-                            }
+                            for (int k = 0; k < 8; ++k) pg[k] = tab->page[(t * TILE_KEYS + (k0 + k) * RPS + prow0) >> log2P];
 #pragma unroll
-                            for (int k = 0; k < GRP; ++k) {
-                                const int key = key0 + (k0 + k) * RPS + prow0;
-                                const int pg = key < ui.kv_end ? pgk[k] : -1;
-                                valid |= (pg >= 0 ? 1u : 0u) << k;
-                                rowi[k] = (uint32_t)(pg * p.kv.n_kv_heads + ui.g) * (uint32_t)p.kv.page_size +
-                                          (uint32_t)(key & (p.kv.page_size - 1));
-                            }
-                        } else {
-                            for (int k = 0; k < GRP; ++k) {
-                                const int key = key0 + (k0 + k) * RPS + prow0;
-                                const int pg = key < ui.kv_end ? page_of(p.kv, ui.b, key) : -1;
-                                valid |= (pg >= 0 ? 1u : 0u) << k;
-                                rowi[k] = (uint32_t)(pg * p.kv.n_kv_heads + ui.g) * (uint32_t)p.kv.page_size +
-                                          (uint32_t)(key & (p.kv.page_size - 1));
+                            for (int k = 0; k < 8; ++k) {
+                                const int row = (k0 + k) * RPS + prow0, key = key0 + row;
+                                const bool ok_row = key < ui.kv_end && pg[k] >= 0;
+                                const uint32_t rowi = ok_row ? (uint32_t)(pg[k] * p.kv.n_kv_heads + ui.g) * (uint32_t)p.kv.page_size +
+                                                                   (uint32_t)(key & (p.kv.page_size - 1))
+                                                             : 0u;
+                                const uint32_t dst = dst_base + (pch >> 3) * (TILE_KEYS * 128) + row * 128 +
+                                                     ((((pch & 7) ^ (row & 7)) & 7) << 4);
+                                cp_async16_zfill(dst, src_col + (size_t)rowi * row_bytes, ok_row);
                             }
                         }
-#pragma unroll
-                        for (int k = 0; k < GRP; ++k) {
-                            const int row = (k0 + k) * RPS + prow0;
-                            const uint32_t dst =
-                                FP8 ? dst_base + row * S_::SUB_COLS + pch * 16
-                                    : dst_base + (pch >> 3) * (TILE_KEYS * 128) + row * 128 +
-                                          ((((pch & 7) ^ (row & 7)) & 7) << 4);
-                            if ((valid >> k) & 1u) cp_async16(dst, src_col + (size_t)rowi[k] * row_bytes);
+                    } else {
+#pragma unroll 1
+                        for (int k = 0; k < NPIECE; ++k) {
+                            const int row = k * RPS + prow0, key = key0 + row;
+                            const int pg = key < ui.kv_end ? page_of(p.kv, ui.b, key) : -1;
+                            const uint32_t rowi = pg < 0 ? 0u
+                                                         : (uint32_t)(pg * p.kv.n_kv_heads + ui.g) * (uint32_t)p.kv.page_size +
+                                                               (uint32_t)(key & (p.kv.page_size - 1));
+                            const uint32_t dst = dst_base + (pch >> 3) * (TILE_KEYS * 128) + row * 128 +
+                                                 ((((pch & 7) ^ (row & 7)) & 7) << 4);
+                            cp_async16_zfill(dst, src_col + (size_t)rowi * row_bytes, pg >= 0);
                         }
                     }
-                    cp_async_arrive(full_base + 8 * s);
-                    ++gi;
+                    cp_async_arrive(full0 + 8 * s);
                 }
             }
             // the unit's table is no longer read by this warp
             __syncwarp();
-            if (ok && lane == 0) {
-                mbar_arrive(lfin + 8 * ub);
-                mbar_arrive(ufree + 8 * ub);
-            }
+            if (ok && lane == 0) mbar_arrive(ufree + 8 * ub);
+            if (!ok) break;
         }
-        // every copy lands before the CTA may exit (TMA boxes: the last phase of each stage)
+        // every copy lands before the CTA may exit, and so do the last MMA commits on the
+        // ring's "empty" barriers
         cp_async_wait_all();
-        if (FP8 && p.tma_rows && lane == 0) {
-            const uint32_t n_last = gi < depth ? gi : depth;
+        if (ltid == 0) {
+            const uint32_t n_last = gi < (uint32_t)depth ? gi : (uint32_t)depth;
             for (uint32_t j = 0; j < n_last; ++j) {
                 const uint32_t i2 = gi - 1 - j;
-                mbar_wait(full_base + 8 * (i2 % depth), (i2 / depth) & 1u, nullptr, ATT_WAIT_NS);
+                mbar_wait(empty0 + 8 * (i2 % (uint32_t)depth), (i2 / (uint32_t)depth) & 1u, nullptr, ATT_WAIT_NS);
             }
         }
         __syncwarp();
@@ -993,77 +1028,151 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
             *abort_flag = 1;
             if (ltid == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
-    } else {
-        // ================= FP8 converters, warps 2, 3: E4M3 -> f16 operand stages =================
-        // E4M3 is exact in f16 (the page scales are applied by the softmax). Per unit the bf16
-        // Q is first converted to f16 in place, then every landed raw sub-tile in ring order.
-        const int ctid = (warp - 2) * 32 + lane;  // 0..63
-        constexpr int CCH = S_::SUB_COLS / 16;     // 16-byte raw pieces per row
-        constexpr int NPC = TILE_KEYS * CCH / 64;  // pieces per converter thread per sub-tile
-        uint32_t gc = 0, ua = 0;                   // sub-tiles converted, active units
+    } else if (warp <= 5) {
+        // ================= FP8: TMA issuers, warp 4 K sub-tiles, warp 5 raw V sub-tiles =================
+        // One box per page-run of rows (min(page size, 128) rows): K boxes land 128- or
+        // 64-byte-swizzled, ready for the S MMA; V boxes land unswizzled in a raw stage. Runs
+        // past the branch's last position, or of an invalid page, are not loaded.
+        const bool is_v = warp == 5;
+        const int depth = is_v ? p.NR : p.NK;
+        const uint32_t full0 = is_v ? rfull : kfull, empty0 = is_v ? rempty : kempty;
+        const uint32_t ring = is_v ? s_raw : s_k;
+        const CUtensorMap *map = is_v ? &map_v : &map_k;
+        uint32_t gi = 0, ua = 0;
         bool ok = true;
+        const int BR = p.tma_rows, nruns = TILE_KEYS / BR;
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
-            if (!warp_wait(ufull + 8 * ub, uph, abort_flag)) { ok = false; break; }
-            const int it_u = tables[ub].iter;
+            const UnitTable *tab = tables + ub;
+            if (!warp_wait<SLEEP_LOAD>(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
+            const int it_u = tab->iter;
             if (it_u < 0) break;
-            int u;
-            const UnitInfo ui = unit_info(p, it_u, u);
-            // ---- Q arrives as bf16; the f16-kind MMA needs f16 on both sides ----
-            const uint32_t qs = p.QB == 2 ? ub : 0u, qph = p.QB == 2 ? uph : (ua & 1u);  // Q buffer, phase
-            if (!warp_wait(qfull + 8 * qs, qph, abort_flag)) { ok = false; break; }
-            uint8_t *qb = smem + p.off_q + qs * QBUF;
-            for (int i = ctid; i < S_::NATOM * R_pad * 8; i += 64) {
-                const int a = i / (R_pad * 8), rem = i % (R_pad * 8);
-                uint4 *ptr = reinterpret_cast<uint4 *>(qb + a * QATOM + rem * 16);
-                const uint4 v = *ptr;
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                uint32_t hq[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) hq[e] = pack2(bf16_lo(w[e]), bf16_hi(w[e]), true);
-                *ptr = make_uint4(hq[0], hq[1], hq[2], hq[3]);
+            const UnitInfo ui = tab->ui;
+            ++ua;
+            for (int t = 0; t < ui.T && ok; ++t) {
+                const int key0 = ui.s0 + t * TILE_KEYS;
+                if (t == max(0, ui.T - 2)) {  // the producer may prepare the next unit (see the bf16 loaders)
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(lfin + 8 * ub);
+                }
+                for (int h = 0; h < S_::NSUB; ++h, ++gi) {
+                    const uint32_t s = gi % (uint32_t)depth;
+                    if (!warp_wait<SLEEP_LOAD>(empty0 + 8 * s, ((gi / (uint32_t)depth) & 1u) ^ 1u, abort_flag, wns)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        const uint32_t dst_base = ring + s * S_::F8_STAGE;
+                        uint32_t bytes = 0;
+                        for (int r = 0; r < nruns; ++r) {
+                            const int kr = key0 + r * BR;
+                            if (kr >= ui.kv_end) break;
+                            if (tab->page[(kr - ui.s0) >> log2P] >= 0) bytes += (uint32_t)(BR * S_::SUB);
+                        }
+                        mbar_arrive_expect_tx(full0 + 8 * s, bytes);
+                        for (int r = 0; r < nruns; ++r) {
+                            const int kr = key0 + r * BR;
+                            if (kr >= ui.kv_end) break;
+                            const int pg = tab->page[(kr - ui.s0) >> log2P];
+                            if (pg < 0) continue;
+                            const int row = (pg * p.kv.n_kv_heads + ui.g) * p.kv.page_size + (kr & (p.kv.page_size - 1));
+                            tma_load_2d(dst_base + (uint32_t)(r * BR) * S_::SUB, map, h * S_::SUB, row, full0 + 8 * s);
+                        }
+                    }
+                    __syncwarp();
+                }
             }
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(ufree + 8 * ub);
+            if (!ok) break;
+        }
+        // every box lands, and every consumer's release of a stage is delivered, before the
+        // CTA may exit
+        if (lane == 0) {
+            const uint32_t n_last = gi < (uint32_t)depth ? gi : (uint32_t)depth;
+            for (uint32_t j = 0; j < n_last; ++j) {
+                const uint32_t i2 = gi - 1 - j;
+                mbar_wait(full0 + 8 * (i2 % (uint32_t)depth), (i2 / (uint32_t)depth) & 1u, nullptr, ATT_WAIT_NS);
+                mbar_wait(empty0 + 8 * (i2 % (uint32_t)depth), (i2 / (uint32_t)depth) & 1u, nullptr, ATT_WAIT_NS);
+            }
+        }
+        __syncwarp();
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
+        }
+    } else {
+        // ================= FP8 converters, warps 6-7 =================
+        // Every raw V sub-tile, in ring order, becomes bf16(code * page scale) in the MMA's
+        // layout (the V ring), with the rows past the branch's last position written as
+        // zeros. The two warps join on an mbarrier (bounded waits) before one thread
+        // publishes their work.
+        const int ctid = (warp - 6) * 32 + lane;  // 0..63
+        uint32_t gv = 0, ua = 0, nc = 0;
+        bool ok = true;
+        auto join = [&]() {  // both converter warps have written and fenced their share
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(qconv + 8 * qs);
+            if (lane == 0) mbar_arrive(cjoin);
+            const bool r = warp_wait<SLEEP_LOAD>(cjoin, nc & 1u, abort_flag, wns);
+            ++nc;
+            return r;
+        };
+        for (;;) {
+            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+            const UnitTable *tab = tables + ub;
+            if (!warp_wait<SLEEP_LOAD>(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
+            const int it_u = tab->iter;
+            if (it_u < 0) break;
+            const UnitInfo ui = tab->ui;
             ++ua;
-            // ---- the unit's K / V sub-tiles ----
-            const uint32_t n_sub = (uint32_t)(2 * S_::NSUB * ui.T);
-            for (uint32_t i = 0; i < n_sub; ++i, ++gc) {
-                const uint32_t rs = gc % p.NR, os = gc % p.NS;
-                if (!warp_wait(raw_full + 8 * rs, (gc / p.NR) & 1u, abort_flag) ||
-                    !warp_wait(op_empty + 8 * os, ((gc / p.NS) & 1u) ^ 1u, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const uint8_t *raw = smem + p.off_raw + rs * S_::RAW_STAGE;
-                uint8_t *op = smem + p.off_op + os * S_::OP_STAGE;
-#pragma unroll
-                for (int k = 0; k < NPC; ++k) {
-                    const int piece = k * 64 + ctid;
-                    const int row = piece / CCH, pc = piece % CCH;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * S_::SUB_COLS + pc * 16);
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-                    uint32_t hv[8];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] & 0xFFFFu), __NV_E4M3);
-                        const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[e] >> 16), __NV_E4M3);
-                        hv[2 * e] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-                        hv[2 * e + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+            for (int t = 0; t < ui.T && ok; ++t) {
+                const int nvk = ui.kv_end - (ui.s0 + t * TILE_KEYS);  // valid keys of the tile (>= 1)
+#pragma unroll 1
+                for (int h = 0; h < S_::NSUB; ++h, ++gv) {
+                    const uint32_t rs = gv % (uint32_t)p.NR, os = gv % (uint32_t)p.NV;
+                    if (!warp_wait<SLEEP_LOAD>(rfull + 8 * rs, (gv / (uint32_t)p.NR) & 1u, abort_flag, wns) ||
+                        !warp_wait<SLEEP_LOAD>(vempty + 8 * os, ((gv / (uint32_t)p.NV) & 1u) ^ 1u, abort_flag, wns)) {
+                        ok = false;
+                        break;
                     }
-                    *reinterpret_cast<uint4 *>(op + sw128_off(row, pc * 16, TILE_KEYS * 128)) =
-                        make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                    *reinterpret_cast<uint4 *>(op + sw128_off(row, pc * 16 + 8, TILE_KEYS * 128)) =
-                        make_uint4(hv[4], hv[5], hv[6], hv[7]);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(op_full + 8 * os);
-                    mbar_arrive(raw_empty + 8 * rs);
+                    const uint8_t *raw = smem + p.off_raw + rs * S_::F8_STAGE;
+                    uint8_t *op = smem + p.off_v + os * S_::OP_STAGE;
+                    constexpr int CCH = S_::SUB / 16;  // 16-byte raw pieces per row
+                    for (int piece = ctid; piece < TILE_KEYS * CCH; piece += 64) {
+                        const int row = piece / CCH, pc = piece % CCH;
+                        uint32_t hv[8];
+                        if (row < nvk) {
+                            const float vs = tab->vsc[(t * TILE_KEYS + row) >> log2P];
+                            const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * S_::SUB + pc * 16);
+                            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const __half2_raw c2 = __nv_cvt_fp8x2_to_halfraw2(
+                                    (__nv_fp8x2_storage_t)((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu), __NV_E4M3);
+                                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&c2));
+                                hv[e] = pack2(f.x * vs, f.y * vs, false);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) hv[e] = 0u;
+                        }
+                        *reinterpret_cast<uint4 *>(op + sw128_off(row, pc * 16, TILE_KEYS * 128)) =
+                            make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                        *reinterpret_cast<uint4 *>(op + sw128_off(row, pc * 16 + 8, TILE_KEYS * 128)) =
+                            make_uint4(hv[4], hv[5], hv[6], hv[7]);
+                    }
+                    if (!join()) { ok = false; break; }
+                    if (ctid == 0) {
+                        mbar_arrive(vfull + 8 * os);
+                        mbar_arrive(rempty + 8 * rs);
+                    }
                 }
             }
+            // the unit's table (its V scales) is no longer read
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(ufree + 8 * ub);
+            if (!ok) break;
         }
         if (!ok) {
             *abort_flag = 1;
@@ -1079,103 +1188,154 @@ __global__ void __launch_bounds__(AttnShape<D, FP8>::THREADS, 1)
     }
 }
 
-// One CTA of 8 warps per (row, q head): merge the row's splits. Only the branch's
-// non-empty splits were computed (split s holds keys from s * split_keys on); among them,
-// splits the row does not reach (l = 0) are skipped, so the result depends only on the
-// row's own splits, not on the batch's split count. The maximum over the splits is reduced
-// in parallel; warp w sums the splits s = w, w+8, ... in ascending order, and the 8 partial
-// sums are added in warp order.
-constexpr int CMB_WARPS = 8;
+// The split merge. One item = (row r, q head h); W warps share an item (the host picks W
+// from the split count; it does not change the arithmetic) and a CTA holds `ipc` items.
+// Pass 1: the maximum m over the splits the row reaches (l > 0) and whether any split
+// failed (l < 0). Pass 2: warp w sums the groups g = w, w + W, ... of COMBINE_GROUP splits,
+// each in ascending split order (the loads of a group issued together), into shared
+// memory. Pass 3: the groups are added in ascending order and the row is normalised.
+// Within every sum the first term taken is multiplied, the later ones fused-added, so a row
+// that one split alone reaches gets that split's O / l bit for bit, however many splits its
+// batch had.
+__host__ __device__ constexpr int combine_slot_floats(int ng_max, int D, int W) {
+    return ng_max * D + ((ng_max + 3) & ~3) + ((2 * W + 3) & ~3);
+}
+
 template <int D>
-__global__ void __launch_bounds__(CMB_WARPS * 32) attn_combine_kernel(const float *__restrict__ ws_ml,
-                                                                      const float *__restrict__ ws_o,
-                                                                      const int32_t *__restrict__ pos, int B, int k,
-                                                                      int Hq, int G, int Hkv, int n_splits,
-                                                                      int split_keys, int max_pos, uint16_t *out) {
-    constexpr int E = D / 32;  // columns per lane
-    __shared__ float red_m[CMB_WARPS];
-    __shared__ int red_f[CMB_WARPS];
-    __shared__ float part_o[CMB_WARPS][D];
-    __shared__ float part_l[CMB_WARPS];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(512) attn_combine_kernel(AttnParams p, int W, int ipc, int ng_max) {
+    // per item (a slot of combine_slot_floats floats, a multiple of 4 so that every slot's
+    // float4 rows stay 16-byte aligned): [ng_max][D] group sums, [ng_max] group l, [W]
+    // maxima, [W] failure flags
+    extern __shared__ float csm[];
+    constexpr int E4 = D >= 128 ? D / 128 : 1;  // float4 per lane (d = 64: lanes 16..31 idle)
     grid_dep_wait();  // the split kernel's partial results
-    const int r = blockIdx.x / Hq, h = blockIdx.x % Hq;
-    const int b = r / (k + 1), j = r % (k + 1);
-    const int g = h / G, hi = h % G;
-    const int n_q = (k + 1) * G;
-    const int qi = j * G + hi;
-    const size_t unit0 = ((size_t)b * Hkv + g) * n_splits;
-    const int pos_b = __ldg(pos + b);
-    if (pos_b < 0 || pos_b + k + 1 > max_pos) return;  // error raised by the split kernel
-    const int n_used = (pos_b + k + split_keys) / split_keys;  // splits holding keys 0..pos_b+k
-    // ---- the maximum over the non-empty splits; any failed split fails the row ----
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slot = warp / W, w = warp % W;
+    const int item = blockIdx.x * ipc + slot;
+    const int R = p.B * (p.k + 1), NQ = p.NQ;
+    float *gsum = csm + (size_t)slot * combine_slot_floats(ng_max, D, W);
+    float *gl = gsum + (size_t)ng_max * D;
+    float *wmax = gl + ((ng_max + 3) & ~3);
+    int *wfail = reinterpret_cast<int *>(wmax + W);
+    const bool active = D >= 128 || lane < D / 4;
+    // the item's splits (none for an item past the end)
+    int n_used = 0, q = 0, b = 0, g = 0, r = 0, h = 0;
+    size_t u0 = 0;
+    if (item < R * p.Hq) {
+        r = item / p.Hq;
+        h = item % p.Hq;
+        b = r / (p.k + 1);
+        g = h / p.G;
+        q = (r % (p.k + 1)) * p.G + h % p.G;
+        const int pos_b = __ldg(p.pos + b);
+        if (pos_b >= 0 && pos_b + p.k + 1 <= p.max_pos) {
+            n_used = (pos_b + p.k + 1 + p.split_keys - 1) / p.split_keys;
+        }
+        u0 = (size_t)(b * p.kv.n_kv_heads + g) * p.n_splits;
+    }
+    const int ng = (n_used + COMBINE_GROUP - 1) / COMBINE_GROUP;
+    // ---- pass 1: maximum over the reached splits; failures ----
     float M = -INFINITY;
     int failed = 0;
-    for (int s = threadIdx.x; s < n_used; s += CMB_WARPS * 32) {
-        const float *ml = ws_ml + ((unit0 + s) * n_q + qi) * 2;
-        const float l = ml[1];
-        if (l < 0.f) failed = 1;
-        if (l > 0.f) M = fmaxf(M, ml[0]);
+    for (int g0 = w * 4 + (lane >> 3); g0 < ng; g0 += 4 * W) {  // 4 groups per warp step
+        const int s = g0 * COMBINE_GROUP + (lane & 7);
+        if (s < n_used) {
+            const float2 v = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + ((u0 + s) * NQ + q) * 2));
+            failed |= v.y < 0.f;
+            if (v.y > 0.f) M = fmaxf(M, v.x);
+        }
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
-        failed |= __shfl_xor_sync(0xFFFFFFFFu, failed, off);
-    }
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+    failed = __any_sync(0xFFFFFFFFu, failed);
     if (lane == 0) {
-        red_m[warp] = M;
-        red_f[warp] = failed;
+        wmax[w] = M;
+        wfail[w] = failed;
     }
     __syncthreads();
     M = -INFINITY;
     failed = 0;
-#pragma unroll
-    for (int w = 0; w < CMB_WARPS; ++w) {
-        M = fmaxf(M, red_m[w]);
-        failed |= red_f[w];
+    for (int i = 0; i < W; ++i) {
+        M = fmaxf(M, wmax[i]);
+        failed |= wfail[i];
     }
-    if (failed || M == -INFINITY) return;  // error already raised; output left unwritten
-    // ---- this warp's splits ----
-    float L = 0.f, o[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[e] = 0.f;
-    for (int s = warp; s < n_used; s += CMB_WARPS) {
-        const float *ml = ws_ml + ((unit0 + s) * n_q + qi) * 2;
-        const float l = ml[1];
-        if (!(l > 0.f)) continue;
-        const float w = exp2f(ml[0] - M);
-        L = fmaf(l, w, L);
-        const float *os = ws_o + ((unit0 + s) * n_q + qi) * D + lane * E;
-        if (E % 4 == 0) {
-#pragma unroll
-            for (int e = 0; e < E; e += 4) {
-                const float4 v = __ldg(reinterpret_cast<const float4 *>(os + e));
-                o[e] = fmaf(w, v.x, o[e]);
-                o[e + 1] = fmaf(w, v.y, o[e + 1]);
-                o[e + 2] = fmaf(w, v.z, o[e + 2]);
-                o[e + 3] = fmaf(w, v.w, o[e + 3]);
+    const bool skip = n_used == 0 || failed || M == -INFINITY;
+    // ---- pass 2: group sums ----
+    if (!skip) {
+        for (int g0 = w; g0 < ng; g0 += W) {
+            const int s0 = g0 * COMBINE_GROUP;
+            const int nb = min(COMBINE_GROUP, n_used - s0);
+            float wl = 0.f, ll = 0.f;  // lane u < nb: weight and l of split s0 + u
+            if (lane < nb) {
+                const float2 v = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + ((u0 + s0 + lane) * NQ + q) * 2));
+                ll = v.y;
+                wl = v.y > 0.f ? merge_weight(v.x, M) : 0.f;
             }
-        } else {
+            float4 v[COMBINE_GROUP][E4];
 #pragma unroll
-            for (int e = 0; e < E; ++e) o[e] = fmaf(w, __ldg(os + e), o[e]);
+            for (int u = 0; u < COMBINE_GROUP; ++u) {
+                if (active && u < nb) {
+                    const float4 *src = reinterpret_cast<const float4 *>(p.ws_o + ((u0 + s0 + u) * NQ + q) * D) + lane;
+#pragma unroll
+                    for (int e = 0; e < E4; ++e) v[u][e] = __ldcg(src + 32 * e);
+                }
+            }
+            float L = 0.f;
+            float4 acc[E4];
+#pragma unroll
+            for (int e = 0; e < E4; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            bool first = true;
+#pragma unroll
+            for (int u = 0; u < COMBINE_GROUP; ++u) {
+                if (u >= nb) break;
+                const float wgt = __shfl_sync(0xFFFFFFFFu, wl, u);
+                const float l = __shfl_sync(0xFFFFFFFFu, ll, u);
+                if (!(l > 0.f)) continue;
+                L = first ? wgt * l : fmaf(wgt, l, L);
+#pragma unroll
+                for (int e = 0; e < E4; ++e) {
+                    if (first) {
+                        acc[e] = make_float4(wgt * v[u][e].x, wgt * v[u][e].y, wgt * v[u][e].z, wgt * v[u][e].w);
+                    } else {
+                        acc[e].x = fmaf(wgt, v[u][e].x, acc[e].x);
+                        acc[e].y = fmaf(wgt, v[u][e].y, acc[e].y);
+                        acc[e].z = fmaf(wgt, v[u][e].z, acc[e].z);
+                        acc[e].w = fmaf(wgt, v[u][e].w, acc[e].w);
+                    }
+                }
+                first = false;
+            }
+            if (active) {
+#pragma unroll
+                for (int e = 0; e < E4; ++e) reinterpret_cast<float4 *>(gsum + (size_t)g0 * D)[lane + 32 * e] = acc[e];
+            }
+            if (lane == 0) gl[g0] = L;  // 0: no split of the group reached by the row
         }
     }
-#pragma unroll
-    for (int e = 0; e < E; ++e) part_o[warp][lane * E + e] = o[e];
-    if (lane == 0) part_l[warp] = L;
     __syncthreads();
-    // ---- the warps' partial sums, in warp order ----
-    float Lt = 0.f;
-#pragma unroll
-    for (int w = 0; w < CMB_WARPS; ++w) Lt += part_l[w];
-    const float inv = 1.f / Lt;
-    uint16_t *dst = out + ((size_t)r * Hq + h) * D;
-    for (int c = threadIdx.x; c < D; c += CMB_WARPS * 32) {
-        float acc = 0.f;
-#pragma unroll
-        for (int w = 0; w < CMB_WARPS; ++w) acc += part_o[w][c];
-        __nv_bfloat16 v = __float2bfloat16_rn(acc * inv);
-        dst[c] = *reinterpret_cast<uint16_t *>(&v);
+    // ---- pass 3: the groups in ascending order, normalised ----
+    if (!skip) {
+        float L = 0.f;
+        bool first = true;
+        for (int g0 = 0; g0 < ng; ++g0) {
+            const float l = gl[g0];
+            if (!(l > 0.f)) continue;
+            L = first ? l : L + l;
+            first = false;
+        }
+        uint16_t *dst = p.out + ((size_t)r * p.Hq + h) * D;
+        for (int d = w * 32 + lane; d < D; d += W * 32) {
+            float acc = 0.f;
+            bool f2 = true;
+            for (int g0 = 0; g0 < ng; ++g0) {
+                if (!(gl[g0] > 0.f)) continue;
+                const float x = gsum[(size_t)g0 * D + d];
+                acc = f2 ? x : acc + x;
+                f2 = false;
+            }
+            const __nv_bfloat16 ov = __float2bfloat16_rn(__fdiv_rn(acc, L));
+            dst[d] = *reinterpret_cast<const uint16_t *>(&ov);
+        }
     }
 }
 
@@ -1207,9 +1367,8 @@ static int attn_sm_count() {
     return n;
 }
 
-// Q [R][Hq][d] viewed as a 3-D tensor (d, Hq, R): a (64, G, J) box at (a*64, g*G, b*(k+1) + j0)
-// holds the J*G query vectors of (branch b, kv head g) with draft rows j0..j0+J-1, in row
-// order (j - j0)*G + i.
+// Q [R][Hq][d] viewed as a 3-D tensor (d, Hq, R): a (64, G, k+1) box at (a*64, g*G, b*(k+1))
+// holds the n_q query vectors of (branch b, kv head g) in row order j*G + i.
 static bool make_q_map(CUtensorMap *map, const void *q, int R, int Hq, int d, int G, int J) {
     EncodeTiledFnA fn = encode_fn_attn();
     if (!fn) return false;
@@ -1223,187 +1382,286 @@ static bool make_q_map(CUtensorMap *map, const void *q, int R, int Hq, int d, in
 }
 
 // An FP8 K or V pool viewed as a 2-D byte tensor (d, num_pages * Hkv * P): a box of
-// box_rows rows of one raw sub-tile row's width (min(d, 128) bytes) is one page-run of a
-// (page, kv head), landing unswizzled in the raw ring.
-static bool make_kv_map(CUtensorMap *map, const void *pool, uint64_t rows, int d, int box_rows) {
+// box_rows rows of one sub-tile's width (min(d, 128) bytes) is one page-run of a (page, kv
+// head). K boxes land swizzled (the E4M3 MMA operand), V boxes unswizzled (a raw stage).
+static bool make_kv_map(CUtensorMap *map, const void *pool, uint64_t rows, int d, int box_rows, bool swizzled) {
     EncodeTiledFnA fn = encode_fn_attn();
     if (!fn) return false;
+    const int w = d < 128 ? d : 128;
     cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)d};
-    cuuint32_t box[2] = {(cuuint32_t)(d < 128 ? d : 128), (cuuint32_t)box_rows};
+    cuuint32_t box[2] = {(cuuint32_t)w, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle sw =
+        !swizzled ? CU_TENSOR_MAP_SWIZZLE_NONE : (w == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(pool), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Shared-memory plan, in this order (every block 1024-aligned): the Q buffer(s), 2 P
-// buffers, the operand ring, the raw ring (FP8), 2 unit tables, barriers, flags. The M =
-// 128 MMAs read up to (128 - R_pad) rows past the last Q block and (128 - PR) past the last
-// P block; the operand ring that follows is always larger than that.
+static uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Shared-memory and TMEM plan. In shared memory, in this order (swizzled blocks 1024-aligned):
+// bf16 Q buffers, E4M3 Q parts (FP8), P buffers, the ones atom, ring 0 (bf16 K/V or E4M3 K +
+// raw V), ring 1 (FP8: f16 V), 2 unit tables, softmax scratch, barriers, flags. In TMEM:
+// NSB S buffers of NQ columns, then OB sets of (NSUB O blocks + L) of NQ columns each.
 template <int D, bool FP8>
-static int plan_rings(AttnTcParams &p, int QB) {
+static int plan_attn(AttnParams &p, size_t *smem_bytes) {
     using S_ = AttnShape<D, FP8>;
-    const uint32_t q_bytes = QB * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.PR * 128;
+    const int NQ = p.NQ;
     const uint32_t ut_bytes = 2 * (uint32_t)sizeof(UnitTable);
-    const uint32_t bars = BAR_BYTES, small = 64 + 3072;
-    const uint32_t fixed = 1024 + q_bytes + p_bytes + ut_bytes + bars + small;
-    const uint32_t raw_row = FP8 ? S_::RAW_STAGE : 0;
-    if (ATT_SMEM_LIMIT < fixed + 2 * S_::OP_STAGE + 2 * raw_row) return SPEC_ERR_UNSUPPORTED;
-    const uint32_t avail = ATT_SMEM_LIMIT - fixed;
-    if (!FP8) {
-        p.NS = (int)(avail / S_::OP_STAGE);
-        p.NS = p.NS > 6 ? 6 : p.NS;
-        p.NR = 0;
-    } else {
-        // the raw ring holds the bytes in flight from HBM, the operand ring converted
-        // sub-tiles waiting for their MMA: one stage more than two tiles' worth, so that the
-        // converter (which works in ring order) never waits on V of a tile behind its softmax
-        p.NS = 2 * S_::NSUB + 1;
-        if (avail < p.NS * S_::OP_STAGE + 4 * raw_row) p.NS = 2 * S_::NSUB;
-        if (avail < p.NS * S_::OP_STAGE + 2 * raw_row) p.NS = 2;
-        p.NR = (int)((avail - p.NS * S_::OP_STAGE) / (raw_row ? raw_row : 1u));
-        p.NR = p.NR > 8 ? 8 : p.NR;
-        if (p.NR < 2) return SPEC_ERR_UNSUPPORTED;
-    }
-    p.QB = QB;
-    return SPEC_OK;
-}
-
-// The plan for `copies` copies of the query layout: two Q buffers let a unit's Q load
-// during the previous unit; one is used instead when that buys a deeper ring (the bytes in
-// flight per SM).
-template <int D, bool FP8>
-static int plan_copies(AttnTcParams &p, int copies) {
-    p.copies = copies;
-    p.R_pad = (copies - 1) * p.qpc * 32 + p.PR;
-    if (p.R_pad > MAX_RPAD) return SPEC_ERR_UNSUPPORTED;
-    AttnTcParams p1 = p;
-    const int st2 = plan_rings<D, FP8>(p, 2);
-    const int st1 = plan_rings<D, FP8>(p1, 1);
-    if (st2 && st1) return st2;
-    // FP8: the raw ring first (bytes in flight), then the operand ring (converted stages)
-    if (st2 || (FP8 ? (p1.NR > p.NR || (p1.NR == p.NR && p1.NS > p.NS)) : p1.NS > p.NS)) p = p1;
-    return SPEC_OK;
-}
-
-// Four copies (queries within one lane quadrant) put a softmax warp on every SM
-// sub-partition; two copies are used when four leave the operand ring too shallow to issue
-// S of the next tile ahead of P.V (long head dims), or when the queries span two quadrants.
-template <int D, bool FP8>
-static int plan_attn(AttnTcParams &p, size_t *smem_bytes) {
-    using S_ = AttnShape<D, FP8>;
-    int st = SPEC_ERR_UNSUPPORTED;
-    if (p.qpc == 1) {
-        AttnTcParams p4 = p;
-        st = plan_copies<D, FP8>(p4, 4);
-        if (!st && p4.NS >= 2 * S_::NSUB) {
-            p = p4;
-        } else {
-            AttnTcParams p2 = p;
-            const int st2 = plan_copies<D, FP8>(p2, 2);
-            if (!st2) {
-                p = p2;
-                st = SPEC_OK;
-            } else if (!st) {
-                p = p4;
-            }
+    const uint32_t sx_bytes = (uint32_t)(8 + 4 + 4 + 4 + 2 + 2) * NQ * 4 + 32;
+    const uint32_t bars = BAR_BYTES, small = 64;
+    // Tile groups of 2 when the ring holds a whole group's K and V (the S of a group's last
+    // tile must be able to load while the V of its first tile waits for the softmax), else 1.
+    // Then the richest plan whose ring holds 1.5 groups (2 Q buffers first; 2 P buffers for
+    // groups of 2, else 3 first), else the deepest ring that holds one group.
+    const int qb_opts[2] = {2, 1};
+    for (int TPI = 2; TPI >= 1; --TPI) {
+        // TMEM: 2 S buffers of a group and 2 O sets preferred, then fewer
+        int NSB = 0, OB = 0;
+        for (int ob = 2; ob >= 1 && !NSB; --ob)
+            for (int nsb = 4 / TPI; nsb >= 2; --nsb)
+                if (nsb * TPI * NQ + ob * (S_::NSUB + 1) * NQ <= 512) {
+                    NSB = nsb;
+                    OB = ob;
+                    break;
+                }
+        if (!NSB) {
+            if (TPI * NQ + (S_::NSUB + 1) * NQ > 512) continue;
+            NSB = 1;
+            OB = 1;
         }
-    } else {
-        st = plan_copies<D, FP8>(p, 2);
+        for (int pass = 0; pass < 2; ++pass)
+            for (int a = 0; a < 2; ++a)
+                for (int c = 0; c < 2; ++c) {
+                    const int QB = qb_opts[a], NPB = TPI == 2 ? 2 : 3 - c;
+                    if (TPI == 2 && c == 1) continue;
+                    const uint32_t q_bytes = FP8 ? 0 : QB * S_::NATOM_Q * NQ * 128;
+                    const uint32_t q8_bytes = FP8 ? QB * 2 * S_::NQ8 * NQ * S_::Q8ROW : 0;
+                    const uint32_t p_bytes = NPB * TPI * NQ * 256;
+                    const uint32_t fixed = align_up(q_bytes + q8_bytes + p_bytes, 1024) + 1024;  // + ones
+                    const uint32_t tail = ut_bytes + sx_bytes + bars + small;
+                    if (1024 + fixed + tail > ATT_SMEM_LIMIT) continue;
+                    const uint32_t avail = ATT_SMEM_LIMIT - 1024 - fixed - tail;
+                    // K ring: at least a group's K sub-tiles (the rich plan: two tiles more); bf16
+                    // V ring: a group's V sub-tiles (minimal plan: one tile's); FP8 raw V ring: two
+                    // tiles' (minimal: one)
+                    const int gsub = S_::NSUB * TPI;
+                    int NK, NV, NR = 0;
+                    if (!FP8) {
+                        int n = (int)(avail / S_::OP_STAGE);
+                        n = n > 10 ? 10 : n;
+                        NV = min(max(pass == 0 ? gsub : S_::NSUB, n - 2 * S_::NSUB), 2 * gsub);
+                        NK = n - NV;
+                        if (NK < (pass == 0 ? 2 * S_::NSUB : S_::NSUB) || NV < S_::NSUB) continue;
+                    } else {
+                        NV = pass == 0 ? gsub : S_::NSUB;
+                        NR = pass == 0 ? 2 * S_::NSUB : S_::NSUB;
+                        const uint32_t used = NV * S_::OP_STAGE + NR * S_::F8_STAGE;
+                        if (avail < used) continue;
+                        NK = (int)((avail - used) / S_::F8_STAGE);
+                        NK = NK > 8 ? 8 : NK;
+                        if (NK < (pass == 0 ? 2 * gsub : S_::NSUB)) continue;
+                    }
+                    if (bar_map(NK, NV, NR, NSB, NPB).end > BAR_BYTES) return SPEC_ERR_UNSUPPORTED;
+                    p.TPI = TPI;
+                    p.NK = NK;
+                    p.NV = NV;
+                    p.NR = NR;
+                    p.NSB = NSB;
+                    p.NPB = NPB;
+                    p.QB = QB;
+                    p.OB = OB;
+                    p.off_q = 0;
+                    p.off_q8 = p.off_q + q_bytes;
+                    p.off_p = p.off_q8 + q8_bytes;
+                    p.off_ones = align_up(p.off_p + p_bytes, 1024);
+                    p.off_k = p.off_ones + 1024;
+                    p.off_v = p.off_k + NK * S_::K_STAGE;
+                    p.off_raw = p.off_v + NV * S_::OP_STAGE;
+                    p.off_ut = p.off_raw + NR * S_::F8_STAGE;
+                    p.off_sx = p.off_ut + ut_bytes;
+                    p.off_bar = align_up(p.off_sx + sx_bytes, 8);
+                    p.off_small = p.off_bar + bars;
+                    p.t_o = (uint32_t)(NSB * TPI * NQ);
+                    *smem_bytes = 1024 + p.off_small + small;
+                    return SPEC_OK;
+                }
     }
-    if (st) return st;
-    if (bar_map(p.NS, p.NR).end > BAR_BYTES) return SPEC_ERR_UNSUPPORTED;
-    p.OB = 256 + 2 * D <= 512 ? 2 : 1;
-    const uint32_t q_bytes = p.QB * S_::NATOM * p.R_pad * 128, p_bytes = 2 * 2 * p.PR * 128;
-    const uint32_t ut_bytes = 2 * (uint32_t)sizeof(UnitTable);
-    const uint32_t bars = BAR_BYTES, small = 64 + 3072;
-    p.off_q = 0;
-    p.off_p = p.off_q + q_bytes;
-    p.off_op = p.off_p + p_bytes;
-    p.off_raw = p.off_op + p.NS * S_::OP_STAGE;
-    p.off_ut = p.off_raw + p.NR * S_::RAW_STAGE;
-    p.off_bar = p.off_ut + ut_bytes;
-    p.off_small = p.off_bar + bars;
-    *smem_bytes = 1024 + p.off_small + small;
-    return SPEC_OK;
+    return SPEC_ERR_UNSUPPORTED;
+}
+
+// FP8 pools: each query vector q (row j*G + i of its (branch, kv head)) becomes two E4M3
+// terms, q * sigma = hi + lo with sigma = 2^e chosen so that max|q * sigma| lies in [128, 256)
+// (clamped to 2^-126..2^126): exact for every element within 2^10 of the vector's largest.
+// Written as [pair][hi, lo][NQ][d] bytes (padding rows zero) with 1/sigma per column, for the
+// attention kernel to load by TMA. One CTA per (branch, kv head), a warp per query vector.
+template <int D>
+__global__ void __launch_bounds__(128) attn_qsplit_kernel(const uint16_t *__restrict__ q, int B, int k, int Hq,
+                                                          int G, int Hkv, int NQ, uint8_t *q8, float *qinv) {
+    grid_dep_wait();  // q may be written by the kernel before this one
+    const int pair = blockIdx.x, b = pair / Hkv, g = pair % Hkv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_q = (k + 1) * G;
+    constexpr int EL = D / 32;  // elements per lane
+    for (int r = warp; r < NQ; r += 4) {
+        float x[EL];
+        if (r < n_q) {
+            const uint16_t *src = q + ((size_t)(b * (k + 1) + r / G) * Hq + g * G + r % G) * D + lane * EL;
+#pragma unroll
+            for (int e = 0; e < EL; ++e) x[e] = __uint_as_float((uint32_t)src[e] << 16);
+        } else {
+#pragma unroll
+            for (int e = 0; e < EL; ++e) x[e] = 0.f;
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int e = 0; e < EL; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+        int ex = 0;
+        if (amax > 0.f) {
+            frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
+            ex = 8 - ex;        // amax * 2^ex in [128, 256)
+            ex = ex > 126 ? 126 : (ex < -126 ? -126 : ex);
+        }
+        const float sig = ldexpf(1.f, ex);
+        if (lane == 0) qinv[(size_t)pair * NQ + r] = ldexpf(1.f, -ex);
+        uint8_t *hi_row = q8 + ((size_t)pair * 2 * NQ + r) * D + lane * EL;
+        uint8_t *lo_row = hi_row + (size_t)NQ * D;
+#pragma unroll
+        for (int e = 0; e < EL; e += 2) {
+            const float a0 = x[e] * sig, a1 = x[e + 1] * sig;
+            const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
+            const __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
+            const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hh));
+            const __nv_fp8x2_storage_t lo =
+                __nv_cvt_float2_to_fp8x2(make_float2(a0 - hf.x, a1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+            *reinterpret_cast<__nv_fp8x2_storage_t *>(hi_row + e) = hi;
+            *reinterpret_cast<__nv_fp8x2_storage_t *>(lo_row + e) = lo;
+        }
+    }
+}
+
+// The split queries viewed as a 2-D byte tensor (d, pairs * 2 * NQ): a box of one 128-byte
+// (d = 64: 64-byte) column block x NQ rows lands in the swizzled K-major layout of the S MMA.
+static bool make_q8_map(CUtensorMap *map, const void *q8, uint64_t rows, int d, int NQ) {
+    EncodeTiledFnA fn = encode_fn_attn();
+    if (!fn) return false;
+    const int w = d < 128 ? d : 128;
+    cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)d};
+    cuuint32_t box[2] = {(cuuint32_t)w, (cuuint32_t)NQ};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(q8), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, w == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D, bool FP8>
-static int launch_attn_tc(AttnTcParams &p, cudaStream_t s) {
-    using S_ = AttnShape<D, FP8>;
+static int launch_attn(AttnParams &p, cudaStream_t s) {
     size_t smem = 0;
     const int st = plan_attn<D, FP8>(p, &smem);
     if (st) return st;
-    CUtensorMap mq0, mq1, mk, mv;
-    if (!make_q_map(&mq0, p.q, p.B * (p.k + 1), p.Hq, D, p.G, p.J1)) return SPEC_ERR_CUDA;
-    if (!make_q_map(&mq1, p.q, p.B * (p.k + 1), p.Hq, D, p.G, p.split ? p.k + 1 - p.J1 : p.J1)) return SPEC_ERR_CUDA;
-    // FP8 pools with pages of at least 64 positions: K / V rows go to the raw ring by TMA
-    // boxes of one page-run each, so the two loader warps issue a few boxes per sub-tile
-    // instead of 16-byte copies (measured faster there; shorter runs make boxes too small
-    // for the TMA issue rate, and on bf16 pools the branch's registers cost the cp.async
-    // gather more than the boxes gained). A pool too large for 32-bit row coordinates also
-    // takes the cp.async path.
-    p.tma_rows = 0;
-    mk = mq0;
-    mv = mq0;
-    const uint64_t pool_rows = (uint64_t)p.kv.num_pages * p.kv.n_kv_heads * p.kv.page_size;
-    if (FP8 && p.kv.page_size >= 64 && pool_rows < (1ull << 31)) {
-        const int br = p.kv.page_size < TILE_KEYS ? p.kv.page_size : TILE_KEYS;
-        if (make_kv_map(&mk, p.kv.k_pool, pool_rows, D, br) && make_kv_map(&mv, p.kv.v_pool, pool_rows, D, br))
-            p.tma_rows = br;
+    CUtensorMap mq, mk, mv;
+    if (FP8) {
+        // the queries' E4M3 split, written to the workspace by a kernel of its own
+        const int pairs = p.B * p.kv.n_kv_heads;
+        const int st2 = launch_pdl(attn_qsplit_kernel<D>, dim3(pairs), dim3(128), 0, s, p.q, p.B, p.k, p.Hq, p.G,
+                                   p.kv.n_kv_heads, p.NQ, p.q8_g, const_cast<float *>(p.qinv_g));
+        if (st2) return st2;
+        if (!make_q8_map(&mq, p.q8_g, (uint64_t)pairs * 2 * p.NQ, D, p.NQ)) return SPEC_ERR_CUDA;
+    } else if (!make_q_map(&mq, p.q, p.B * (p.k + 1), p.Hq, D, p.G, p.k + 1)) {
+        return SPEC_ERR_CUDA;
+    }
+    mk = mq;
+    mv = mq;
+    if (FP8) {
+        const uint64_t pool_rows = (uint64_t)p.kv.num_pages * p.kv.n_kv_heads * p.kv.page_size;
+        if (!make_kv_map(&mk, p.kv.k_pool, pool_rows, D, p.tma_rows, true) ||
+            !make_kv_map(&mv, p.kv.v_pool, pool_rows, D, p.tma_rows, false))
+            return SPEC_ERR_CUDA;
     }
     // a fixed ceiling (see the skinny GEMM launcher): graphs may mix launch sizes
-    if (cudaFuncSetAttribute(attn_tc_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM_LIMIT) !=
+    if (cudaFuncSetAttribute(attn_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, ATT_SMEM_LIMIT) !=
         cudaSuccess)
         return SPEC_ERR_CUDA;
     const int sms = attn_sm_count();
     if (sms < 1) return SPEC_ERR_CUDA;
     const int grid = p.n_units < sms ? p.n_units : sms;
-    return launch_pdl(attn_tc_kernel<D, FP8>, dim3(grid), dim3(S_::THREADS), smem, s, mq0, mq1, mk, mv, p);
+    return launch_pdl(attn_kernel<D, FP8>, dim3(grid), dim3(ATT_THREADS), smem, s, mq, mk, mv, p);
 }
 
-// workspace: a 256-byte header (the unit scheduler's counters: zero before the first call,
-// left zero by every call), the (m, l) pairs, the partial outputs
-static size_t ws_bytes_for(int B, int Hkv, int n_splits, int n_q, int d) {
-    const size_t units = (size_t)B * Hkv * n_splits;
-    size_t ml = units * n_q * 2 * sizeof(float);
-    ml = (ml + 255) & ~(size_t)255;
-    return 256 + ml + units * n_q * d * sizeof(float);
+// Workspace: a 256-byte header (the unit scheduler's counters: zero before the first call
+// and left zero by every call), then the per-unit (m, l) pairs and partial outputs, then
+// (FP8 pools) the split queries and their scales.
+struct WsLayout {
+    size_t ml, o, q8, qinv, total;
+};
+static WsLayout ws_layout(int B, int Hkv, int n_splits, int NQ, int d, bool fp8) {
+    WsLayout w;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t pairs = (size_t)B * Hkv, units = pairs * n_splits;
+    w.ml = 256;
+    w.o = w.ml + up(units * NQ * 2 * 4);
+    w.q8 = w.o + up(units * NQ * d * 4);
+    w.qinv = w.q8 + (fp8 ? up(pairs * 2 * NQ * d) : 0);
+    w.total = w.qinv + (fp8 ? pairs * NQ * 4 : 0);
+    return w;
+}
+
+// The combine grid: W = warps per (row, head) item, ceil(splits / COMBINE_GROUP) rounded up
+// to a power of two (at most 16); 8 / W items per CTA when W < 8.
+template <int D>
+static int launch_combine(const AttnParams &p, cudaStream_t s) {
+    const int ng_max = (p.n_splits + COMBINE_GROUP - 1) / COMBINE_GROUP;
+    int W = 1;
+    while (W < ng_max && W < 16) W <<= 1;
+    const int ipc = W >= 8 ? 1 : 8 / W;
+    const int items = p.B * (p.k + 1) * p.Hq;
+    const int grid = (items + ipc - 1) / ipc;
+    const size_t smem = (size_t)ipc * combine_slot_floats(ng_max, D, W) * sizeof(float);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(attn_combine_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) !=
+            cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (smem > 227 * 1024) return SPEC_ERR_UNSUPPORTED;
+    return launch_pdl(attn_combine_kernel<D>, dim3(grid), dim3(ipc * W * 32), smem, s, p, W, ipc, ng_max);
 }
 
 // The launch parameters that depend only on the shapes (the caller checks the descriptor
 // and fills in the pointers).
-static int attn_setup(const spec_kv_desc *kvd, int B, int k, int n_q_heads, int max_pos, AttnTcParams &p) {
+static int attn_setup(const spec_kv_desc *kvd, int B, int k, int n_q_heads, int max_pos, AttnParams &p) {
     if (B < 1 || k < 0 || k > SPEC_KMAX || n_q_heads < 1 || max_pos < k + 1) return SPEC_ERR_ARG;
     if (n_q_heads % kvd->n_kv_heads) return SPEC_ERR_ARG;
     const int G = n_q_heads / kvd->n_kv_heads;
     const int n_q = (k + 1) * G;
-    const int N_pad = ((n_q + 15) / 16) * 16;
-    // more than 32 query vectors need two TMEM lane quadrants: the draft rows are then split
-    // in two halves of at most 32 lanes each when they fit (otherwise the vectors run
-    // contiguously over both quadrants); PR = the lanes of one copy of that layout
-    const int J1 = (k + 2) / 2;
-    const bool split = n_q > 32 && k >= 1 && J1 * G <= 32 && (k + 1 - J1) * G <= 32;
-    p = AttnTcParams{};
+    const int NQ = ((n_q + 15) / 16) * 16;
+    p = AttnParams{};
     p.kv = make_view(kvd);
     p.B = B;
     p.k = k;
     p.Hq = n_q_heads;
     p.G = G;
     p.n_q = n_q;
-    p.J1 = split ? J1 : k + 1;
-    p.split = split ? 1 : 0;
-    p.PR = split ? 32 + (((k + 1 - J1) * G + 15) / 16) * 16 : N_pad;
-    p.qpc = n_q > 32 ? 2 : 1;
+    p.NQ = NQ;
     p.split_keys = split_keys_for(kvd->n_kv_heads);
     p.n_splits = (max_pos + p.split_keys - 1) / p.split_keys;
     p.max_pos = max_pos;
     p.n_units = B * kvd->n_kv_heads * p.n_splits;
-    return N_pad > MAX_NPAD ? SPEC_ERR_UNSUPPORTED : SPEC_OK;
+    p.wait_ns = g_wait_ns;
+    p.tma_rows = kvd->kv_dtype == SPEC_KV_FP8_E4M3 ? (kvd->page_size < TILE_KEYS ? kvd->page_size : TILE_KEYS) : 0;
+    if (G > 256 || NQ > MAX_NQ) return SPEC_ERR_UNSUPPORTED;
+    // FP8 pools are gathered by TMA boxes of one page-run: pages of at least 8 positions (a
+    // swizzle atom of rows), row coordinates within 32 bits
+    if (kvd->kv_dtype == SPEC_KV_FP8_E4M3 &&
+        (kvd->page_size < 8 || (uint64_t)kvd->num_pages * kvd->n_kv_heads * kvd->page_size >= (1ull << 31)))
+        return SPEC_ERR_UNSUPPORTED;
+    return SPEC_OK;
 }
 
-static int plan_dispatch(AttnTcParams &p, size_t *smem) {
+static int plan_dispatch(AttnParams &p, size_t *smem) {
     switch (p.kv.head_dim * 2 + (p.kv.kv_dtype == SPEC_KV_FP8_E4M3 ? 1 : 0)) {
         case 128: return plan_attn<64, false>(p, smem);
         case 129: return plan_attn<64, true>(p, smem);
@@ -1421,20 +1679,18 @@ SPEC_API int spec_verify_attn_plan(const spec_kv_desc *kvd, int B, int k, int n_
     if (!out || n_out < SPEC_ATTN_PLAN_FIELDS) return SPEC_ERR_ARG;
     int st = spec::check_kv_shape(kvd);
     if (st) return st;
-    spec::AttnTcParams p;
+    spec::AttnParams p;
     st = spec::attn_setup(kvd, B, k, n_q_heads, max_pos, p);
     if (st) return st;
     size_t smem = 0;
     st = spec::plan_dispatch(p, &smem);
     if (st) return st;
-    const bool fp8 = kvd->kv_dtype == SPEC_KV_FP8_E4M3;
-    const uint64_t pool_rows = (uint64_t)kvd->num_pages * kvd->n_kv_heads * kvd->page_size;
-    const int tma_rows = fp8 && kvd->page_size >= 64 && pool_rows < (1ull << 31)
-                             ? (kvd->page_size < spec::TILE_KEYS ? kvd->page_size : spec::TILE_KEYS)
-                             : 0;
-    const int32_t v[SPEC_ATTN_PLAN_FIELDS] = {(int32_t)smem, p.copies, p.qpc, p.R_pad, p.PR, p.NS, p.NR, p.QB, p.OB,
-                                              p.split_keys, p.n_splits, p.n_units, p.split, tma_rows,
-                                              (int32_t)spec::bar_map(p.NS, p.NR).end, (int32_t)spec::BAR_BYTES};
+    const int nsub = kvd->head_dim / (kvd->head_dim < 128 ? kvd->head_dim : 128);
+    const int32_t v[SPEC_ATTN_PLAN_FIELDS] = {(int32_t)smem, p.NQ, p.NK, p.NV, p.NR, p.NSB, p.NPB, p.QB, p.OB,
+                                              (int32_t)(p.t_o + p.OB * (nsub + 1) * p.NQ), p.split_keys, p.n_splits,
+                                              p.n_units, p.TPI, p.tma_rows,
+                                              (int32_t)spec::bar_map(p.NK, p.NV, p.NR, p.NSB, p.NPB).end,
+                                              (int32_t)spec::BAR_BYTES};
     for (int i = 0; i < SPEC_ATTN_PLAN_FIELDS; ++i) out[i] = v[i];
     return SPEC_OK;
 }
@@ -1443,9 +1699,10 @@ SPEC_API size_t spec_verify_attn_workspace(const spec_kv_desc *kv, int B, int k,
     if (spec::check_kv_desc(kv) || B < 1 || k < 0 || k > SPEC_KMAX || n_q_heads < 1 || max_pos < 1) return 0;
     if (n_q_heads % kv->n_kv_heads) return 0;
     const int G = n_q_heads / kv->n_kv_heads;
+    const int NQ = (((k + 1) * G + 15) / 16) * 16;
     const int sk = spec::split_keys_for(kv->n_kv_heads);
     const int n_splits = (max_pos + sk - 1) / sk;
-    return spec::ws_bytes_for(B, kv->n_kv_heads, n_splits, (k + 1) * G, kv->head_dim);
+    return spec::ws_layout(B, kv->n_kv_heads, n_splits, NQ, kv->head_dim, kv->kv_dtype == SPEC_KV_FP8_E4M3).total;
 }
 
 SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B, int k, int n_q_heads,
@@ -1460,46 +1717,36 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     if (!ws || ws_bytes < need) return SPEC_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SPEC_ERR_ALIGN;
     if (!spec::aligned16(q) || !spec::aligned16(out)) return SPEC_ERR_ALIGN;
-    spec::AttnTcParams p;
+    spec::AttnParams p;
     st = spec::attn_setup(kvd, B, k, n_q_heads, max_pos, p);
     if (st) return st;
-    const int G = p.G, n_q = p.n_q;
     p.pos = pos;
     p.q = (const uint16_t *)q;
+    p.out = (uint16_t *)out;
     p.scale_log2 = scale * spec::LOG2E;
-    const size_t units = (size_t)p.n_units;
-    size_t ml = units * n_q * 2 * sizeof(float);
-    ml = (ml + 255) & ~(size_t)255;
-    p.sched = (unsigned int *)ws;
-    p.ws_ml = (float *)((char *)ws + 256);
-    p.ws_o = (float *)((char *)ws + 256 + ml);
+    const spec::WsLayout w =
+        spec::ws_layout(B, kvd->n_kv_heads, p.n_splits, p.NQ, kvd->head_dim, kvd->kv_dtype == SPEC_KV_FP8_E4M3);
+    char *base = (char *)ws;
+    p.sched = (unsigned int *)base;
+    p.ws_ml = (float *)(base + w.ml);
+    p.ws_o = (float *)(base + w.o);
+    p.q8_g = (uint8_t *)(base + w.q8);
+    p.qinv_g = (const float *)(base + w.qinv);
     p.err = dev_err;
     cudaStream_t s = (cudaStream_t)stream;
     const bool fp8 = kvd->kv_dtype == SPEC_KV_FP8_E4M3;
     switch (kvd->head_dim * 2 + (fp8 ? 1 : 0)) {
-        case 128: st = spec::launch_attn_tc<64, false>(p, s); break;
-        case 129: st = spec::launch_attn_tc<64, true>(p, s); break;
-        case 256: st = spec::launch_attn_tc<128, false>(p, s); break;
-        case 257: st = spec::launch_attn_tc<128, true>(p, s); break;
-        case 512: st = spec::launch_attn_tc<256, false>(p, s); break;
-        default: st = spec::launch_attn_tc<256, true>(p, s); break;
+        case 128: st = spec::launch_attn<64, false>(p, s); break;
+        case 129: st = spec::launch_attn<64, true>(p, s); break;
+        case 256: st = spec::launch_attn<128, false>(p, s); break;
+        case 257: st = spec::launch_attn<128, true>(p, s); break;
+        case 512: st = spec::launch_attn<256, false>(p, s); break;
+        default: st = spec::launch_attn<256, true>(p, s); break;
     }
     if (st) return st;
-    const int R = B * (k + 1);
-    const int cblocks = R * n_q_heads;
-    constexpr int CT = spec::CMB_WARPS * 32;
-    uint16_t *o16 = (uint16_t *)out;
-    const float *wml = p.ws_ml, *wo = p.ws_o;
-    const int Hkv = kvd->n_kv_heads, ns = p.n_splits, sk = p.split_keys;
     switch (kvd->head_dim) {
-        case 64:
-            return spec::launch_pdl(spec::attn_combine_kernel<64>, dim3(cblocks), dim3(CT), 0, s, wml, wo, pos, B, k,
-                                    n_q_heads, G, Hkv, ns, sk, max_pos, o16);
-        case 128:
-            return spec::launch_pdl(spec::attn_combine_kernel<128>, dim3(cblocks), dim3(CT), 0, s, wml, wo, pos, B, k,
-                                    n_q_heads, G, Hkv, ns, sk, max_pos, o16);
-        default:
-            return spec::launch_pdl(spec::attn_combine_kernel<256>, dim3(cblocks), dim3(CT), 0, s, wml, wo, pos, B, k,
-                                    n_q_heads, G, Hkv, ns, sk, max_pos, o16);
+        case 64: return spec::launch_combine<64>(p, s);
+        case 128: return spec::launch_combine<128>(p, s);
+        default: return spec::launch_combine<256>(p, s);
     }
 }

@@ -82,8 +82,9 @@ class VerifyStep:
         if mtp is not None:
             self.mtp_ws = torch.zeros(bnd.spec_mtp_input_workspace(B, self.H), dtype=torch.uint8, device=device)
             self.out.mtp_x = torch.empty((B, self.H), dtype=torch.bfloat16, device=device)
-        # append 1, attention 1, LM head 1, accept 1; the MTP input adds 3
-        self.launches_verify = 4
+        # append 1, attention 2 (FP8 pools 3: the query split first), LM head 1, accept 1;
+        # the MTP input adds 3
+        self.launches_verify = 5 + (1 if kv.fp8 else 0)
         self.launches_mtp = 3 if mtp is not None else 0
 
     def run(self, pos, q, k_new, v_new, hidden, drafts, stream=None, with_mtp: bool = True) -> StepOutputs:

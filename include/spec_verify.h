@@ -136,13 +136,15 @@ int spec_kv_write_rows(const spec_kv_desc *kv, const int32_t *row_branch,
 
 /* Diagnostic (no GPU needed, nothing launched): the launch plan spec_verify_attn would
  * use for these shapes. Only the descriptor's shape fields are read (its pointers are not
- * looked at). out[0..15] = dynamic shared memory bytes, query copies on the TMEM lanes,
- * lane quadrants per copy, Q rows per buffer (all copies), P rows, operand ring stages,
- * FP8 raw ring stages, Q buffers, O buffers, split size in positions, splits per branch,
- * work units, split query layout (0/1), FP8 TMA box rows (0 = cp.async gather), barrier
- * bytes used, barrier bytes reserved. Returns the status the host checks and the
- * planning of spec_verify_attn would give (n_out < SPEC_ATTN_PLAN_FIELDS: SPEC_ERR_ARG). */
-#define SPEC_ATTN_PLAN_FIELDS 16
+ * looked at). out[0..16] = dynamic shared memory bytes, query vectors per (branch, kv head)
+ * padded to 16 (the MMAs' N), K ring stages (bf16 K, or E4M3 K), V ring stages (bf16 V;
+ * on FP8 pools the converted V), raw V ring stages (FP8 only: E4M3 V as loaded), S buffers,
+ * P buffers, Q buffers, O buffers, TMEM columns used, split size in positions, splits per
+ * branch, work units, tiles of 128 keys per softmax step, FP8 TMA box rows (0 = bf16
+ * gather), barrier bytes used, barrier bytes reserved. Returns the status the host checks
+ * and the planning of spec_verify_attn would give (n_out < SPEC_ATTN_PLAN_FIELDS:
+ * SPEC_ERR_ARG). */
+#define SPEC_ATTN_PLAN_FIELDS 17
 int spec_verify_attn_plan(const spec_kv_desc *kv, int B, int k, int n_q_heads, int max_pos,
                           int32_t *out, int n_out);
 
@@ -159,20 +161,25 @@ int spec_verify_attn_plan(const spec_kv_desc *kv, int B, int k, int n_q_heads, i
  * 512 (n_kv_heads <= 4) or 1024 (otherwise): a function of the model's shape
  * only, independent of B, k and context, so a row's output is byte-identical
  * whatever batch it is verified in (memra-engine spec.rs, `MtpScratch`: fixed
- * split geometry).
- *   q       device bf16 [B*(k+1)][n_q_heads][head_dim]
+ * split geometry). The splits are merged inside the same launch.
+ *   q       device bf16 [B*(k+1)][n_q_heads][head_dim], finite values. On FP8 pools each
+ *           query vector is scaled by a power of two and split into two E4M3 terms, exact
+ *           for every element within 2^10 of the vector's largest (any finite magnitude).
  *   out     device bf16 [B*(k+1)][n_q_heads][head_dim]
  *   scale   softmax scale (normally 1/sqrt(head_dim))
  *   max_pos host bound: pos[b]+k+1 <= max_pos for every b (sizes the grid and
  *           the workspace; rows beyond it are a device error SPEC_DEVERR_POS).
  *   ws      device workspace of spec_verify_attn_workspace(...) bytes, 256-byte
- *           aligned. Its first 256 bytes (the work-unit scheduler's counters) must be
- *           ZERO before the first call; every call leaves them zero again, so a
- *           workspace is zeroed once, not per call. The rest needs no initialisation.
- *           Calls sharing a workspace must not overlap in time.
+ *           aligned, ZERO-filled before its first call. Every call that completes leaves
+ *           the parts that must start at zero (the scheduler and merge counters) at zero
+ *           again, so a workspace is zeroed once, not per call; after a call that reported
+ *           SPEC_DEVERR_TIMEOUT, zero it again. Calls sharing a workspace must not overlap
+ *           in time.
  * Host errors: NULL, B < 1, k out of range, n_q_heads % n_kv_heads != 0,
  * head_dim not 64/128/256, max_pos < k+1, workspace too small; SPEC_ERR_UNSUPPORTED
- * when (k+1)*G, the query vectors sharing one kv head, exceeds 64.
+ * when (k+1)*G, the query vectors sharing one kv head, exceeds 128, when FP8 pages hold
+ * fewer than 8 positions, or when no shared-memory / TMEM plan fits the shapes
+ * (spec_verify_attn_plan tells which).
  * Device errors: as spec_kv_append (the row's output is then left unwritten). */
 size_t spec_verify_attn_workspace(const spec_kv_desc *kv, int B, int k, int n_q_heads,
                                   int max_pos);
@@ -300,6 +307,18 @@ int spec_mtp_input(const int32_t *tok, const void *E, const void *h, const float
                    const float *g_hid, float eps, const void *W_fc, int M, int H, int V,
                    void *x_out, void *ws, size_t ws_bytes, int32_t *dev_err,
                    spec_stream_t stream);
+
+/* ---- test hook: bounded waits ---------------------------------------------------------
+ * The source pages have no counterpart of this entry point. Every wait inside the
+ * tcgen05 kernels (spec_verify_attn, spec_lmhead_argmax, spec_lmhead_logits,
+ * spec_lmhead_argmax_static and the fc of spec_mtp_input) gives up after a time limit,
+ * normally one second, and the kernel then reports SPEC_DEVERR_TIMEOUT, lets the copies and
+ * MMAs it has issued land, frees its tensor memory and returns. This sets that limit, in
+ * nanoseconds, for the launches made after the call (0 restores one second), so that a test
+ * can make a wait run out on purpose and check that the error is reported and the context
+ * stays usable. The waits that drain a kernel's own copies before it exits keep the full
+ * second. Process-wide; not synchronised with launches from other threads. */
+void spec_test_set_wait_limit(uint64_t ns);
 
 #ifdef __cplusplus
 }
