@@ -50,7 +50,9 @@ enum TcEpi { TC_ARGMAX = 0, TC_LOGITS = 1, TC_PARTIAL = 2 };
 struct TcParams {
     int M, N_pad, V, K;
     int n_tiles, n_kc, splits, stages;
-    uint32_t a_stage_bytes, tmem_cols;
+    int tps;                        // W tiles per stage (1 or 2): the hidden chunk of a stage serves them all
+    int n_groups;                   // groups of tps tiles
+    uint32_t w_stage_bytes, a_stage_bytes, tmem_cols;
     float *logits;                  // TC_LOGITS: [M][V]
     float *partial;                 // TC_PARTIAL: [splits][M][V]
     unsigned long long *keys;       // argmax: [gridDim.x][M]
@@ -72,8 +74,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sw = smem_u32(smem);
-    const uint32_t sa = sw + p.stages * W_STAGE_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * (W_STAGE_BYTES + p.a_stage_bytes));
+    const uint32_t sa = sw + p.stages * p.w_stage_bytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * (p.w_stage_bytes + p.a_stage_bytes));
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8 * p.stages;
     const uint32_t tfull0 = empty0 + 8 * p.stages;
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * p.stages + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
-    unsigned long long *cand = reinterpret_cast<unsigned long long *>(tmem_slot + 4);  // [2][4][N_pad]
+    unsigned long long *cand = reinterpret_cast<unsigned long long *>(tmem_slot + 4);  // [2][tps][4][N_pad]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -113,28 +115,32 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
 
     const int G = gridDim.x;
-    const int n_work = p.n_tiles * p.splits;
+    const int n_work = p.n_groups * p.splits;
     const int wb = (int)(((long long)blockIdx.x * n_work) / G);
     const int we = (int)(((long long)(blockIdx.x + 1) * n_work) / G);
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
-            const uint32_t tx = W_STAGE_BYTES + p.a_stage_bytes;
-            uint32_t it = 0;
+            const uint32_t tx = p.w_stage_bytes + p.a_stage_bytes;
+            uint32_t it = 0, s = 0, ph = 0;  // stages issued; the next stage and its phase parity
             bool ok = true;
             for (int w = wb; w < we && ok; ++w) {
-                const int tile = w / p.splits, sp = w % p.splits;
+                const int grp = w / p.splits, sp = w % p.splits;
                 const int kb = sp * p.n_kc / p.splits, ke = (sp + 1) * p.n_kc / p.splits;
                 for (int kc = kb; kc < ke; ++kc, ++it) {
-                    const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
                     if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(full0 + 8 * s, tx);
-                    tma_load_2d(sw + s * W_STAGE_BYTES, &tmap_w, kc * TC_BK, tile * TC_BM, full0 + 8 * s);
+                    // one box of tps * 128 W rows (rows past V read as zeros)
+                    tma_load_2d(sw + s * p.w_stage_bytes, &tmap_w, kc * TC_BK, grp * TC_BM * p.tps, full0 + 8 * s);
                     tma_load_2d(sa + s * p.a_stage_bytes, &tmap_a, kc * TC_BK, 0, full0 + 8 * s);
+                    if (++s == (uint32_t)p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
             if (!ok) {
@@ -142,17 +148,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 raise_error(p.err, SPEC_DEVERR_TIMEOUT);
             }
             // let the loads still in flight land before the CTA can exit
-            const uint32_t n_last = it < (uint32_t)p.stages ? it : (uint32_t)p.stages;
-            for (uint32_t j = 0; j < n_last; ++j) {
-                const uint32_t i2 = it - 1 - j;
-                mbar_wait(full0 + 8 * (i2 % p.stages), (i2 / p.stages) & 1u, nullptr, WAIT_NS);
+            for (uint32_t j = 0; j < (uint32_t)p.stages && j < it; ++j) {
+                if (s == 0) {
+                    s = (uint32_t)p.stages;
+                    ph ^= 1u;
+                }
+                --s;
+                mbar_wait(full0 + 8 * s, ph, nullptr, WAIT_NS);
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(TC_BM, p.N_pad);
-            uint32_t it = 0, t = 0;
+            uint32_t it = 0, t = 0, s = 0, ph = 0;
             bool ok = true;
             for (int w = wb; w < we && ok; ++w, ++t) {
                 const uint32_t acc = t & 1u, use = t >> 1;
@@ -161,22 +170,28 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + acc * (uint32_t)p.N_pad;
+                const uint32_t d_tmem = tmem + acc * (uint32_t)(p.tps * p.N_pad);  // tile i: + i * N_pad
                 const int sp = w % p.splits;
                 const int kb = sp * p.n_kc / p.splits, ke = (sp + 1) * p.n_kc / p.splits;
                 for (int kc = kb; kc < ke; ++kc, ++it) {
-                    const uint32_t s = it % p.stages, ph = (it / p.stages) & 1u;
                     if (!mbar_wait(full0 + 8 * s, ph, abort_flag, p.wait_ns)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = sw + s * W_STAGE_BYTES, b_base = sa + s * p.a_stage_bytes;
+                    const uint32_t a_base = sw + s * p.w_stage_bytes, b_base = sa + s * p.a_stage_bytes;
+                    const uint64_t wa0 = desc_kmajor_sw128(a_base), hb0 = desc_kmajor_sw128(b_base);
+                    for (int i = 0; i < p.tps; ++i) {
 #pragma unroll
-                    for (int k = 0; k < TC_BK / 16; ++k)
-                        mma_bf16(d_tmem, desc_kmajor_sw128(a_base + 32 * k), desc_kmajor_sw128(b_base + 32 * k), idesc,
-                                 (kc > kb || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < TC_BK / 16; ++k)
+                            mma_bf16(d_tmem + i * p.N_pad, desc_advance(wa0, i * W_STAGE_BYTES + 32 * k),
+                                     desc_advance(hb0, 32 * k), idesc, (kc > kb || k > 0) ? 1u : 0u);
+                    }
                     mma_commit(empty0 + 8 * s);
+                    if (++s == (uint32_t)p.stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (ok) mma_commit(tfull0 + 8 * acc);
             }
@@ -190,10 +205,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             // and every arrive those MMAs' commits send is delivered before the CTA may exit:
             // wait for the last phase of each stage's "empty" barrier (a late arrive would
             // land in shared memory this CTA no longer owns)
-            const uint32_t n_last = it < (uint32_t)p.stages ? it : (uint32_t)p.stages;
-            for (uint32_t j = 0; j < n_last; ++j) {
-                const uint32_t i2 = it - 1 - j;
-                mbar_wait(empty0 + 8 * (i2 % p.stages), (i2 / p.stages) & 1u, nullptr, WAIT_NS);
+            for (uint32_t j = 0; j < (uint32_t)p.stages && j < it; ++j) {
+                if (s == 0) {
+                    s = (uint32_t)p.stages;
+                    ph ^= 1u;
+                }
+                --s;
+                mbar_wait(empty0 + 8 * s, ph, nullptr, WAIT_NS);
             }
         }
     } else {
@@ -210,30 +228,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            const int tile = w / p.splits, sp = w % p.splits;
-            const int v = tile * TC_BM + q * 32 + lane;
-            const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + acc * (uint32_t)p.N_pad;
-            unsigned long long *cq = cand + ((size_t)acc * 4 + q) * p.N_pad;
-            for (int c0 = 0; c0 < p.N_pad; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(taddr + c0, r);
-                tmem_ld_wait();
+            const int grp = w / p.splits, sp = w % p.splits;
+            for (int i = 0; i < p.tps; ++i) {
+                const int tile = grp * p.tps + i;
+                const int v = tile * TC_BM + q * 32 + lane;
+                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (acc * p.tps + i) * (uint32_t)p.N_pad;
+                unsigned long long *cq = cand + (((size_t)acc * p.tps + i) * 4 + q) * p.N_pad;
+                for (int c0 = 0; c0 < p.N_pad; c0 += 16) {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + c0, r);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int m = c0 + j;
-                    if (m >= p.M) break;
-                    const float x = __uint_as_float(r[j]);
-                    if (EPI == TC_PARTIAL) {
-                        if (v < p.V) p.partial[((size_t)sp * p.M + m) * p.V + v] = x;
-                        continue;
-                    }
-                    if (EPI == TC_LOGITS && v < p.V) p.logits[(size_t)m * p.V + v] = x;
-                    const uint32_t key = v < p.V ? float_key(__fadd_rn(x, 0.0f)) : 0u;
-                    const uint32_t best = __reduce_max_sync(0xFFFFFFFFu, key);
-                    const uint32_t who = __ballot_sync(0xFFFFFFFFu, key == best);
-                    if (lane == 0) {
-                        const uint32_t vw = (uint32_t)(tile * TC_BM + q * 32 + __ffs(who) - 1);
-                        cq[m] = ((unsigned long long)best << 32) | (0xFFFFFFFFu - vw);
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = c0 + j;
+                        if (m >= p.M) break;
+                        const float x = __uint_as_float(r[j]);
+                        if (EPI == TC_PARTIAL) {
+                            if (v < p.V) p.partial[((size_t)sp * p.M + m) * p.V + v] = x;
+                            continue;
+                        }
+                        if (EPI == TC_LOGITS && v < p.V) p.logits[(size_t)m * p.V + v] = x;
+                        const uint32_t key = v < p.V ? float_key(__fadd_rn(x, 0.0f)) : 0u;
+                        const uint32_t best = __reduce_max_sync(0xFFFFFFFFu, key);
+                        const uint32_t who = __ballot_sync(0xFFFFFFFFu, key == best);
+                        if (lane == 0) {
+                            const uint32_t vw = (uint32_t)(tile * TC_BM + q * 32 + __ffs(who) - 1);
+                            cq[m] = ((unsigned long long)best << 32) | (0xFFFFFFFFu - vw);
+                        }
                     }
                 }
             }
@@ -245,8 +266,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
                     const int m = etid + 128 * i;
                     if (m < p.M) {
                         unsigned long long b = running[i];
-                        for (int qq = 0; qq < 4; ++qq) {
-                            const unsigned long long c = cand[((size_t)acc * 4 + qq) * p.N_pad + m];
+                        for (int qq = 0; qq < 4 * p.tps; ++qq) {
+                            const unsigned long long c = cand[((size_t)acc * p.tps * 4 + qq) * p.N_pad + m];
                             b = c > b ? c : b;
                         }
                         running[i] = b;
@@ -389,19 +410,27 @@ static int plan(int M, int V, int K, int splits, TcPlan &pl) {
     p.n_kc = (K + TC_BK - 1) / TC_BK;
     p.splits = splits < 1 ? 1 : (splits > p.n_kc ? p.n_kc : splits);
     p.a_stage_bytes = (uint32_t)p.N_pad * TC_BK * 2;
+    // Two W tiles per stage when both accumulators of both fit TMEM (N_pad <= 128): the
+    // stage's hidden chunk then serves 256 W rows, which halves the hidden-row traffic per
+    // weight byte (a pure TMA stream of 128-row boxes plus a hidden box ran ~12 % slower than
+    // the W boxes alone; 256-row boxes with the hidden box ran within 1 % of it)
+    p.tps = (p.N_pad <= 128 && V >= 2 * TC_BM) ? 2 : 1;
+    p.n_groups = (p.n_tiles + p.tps - 1) / p.tps;
+    p.w_stage_bytes = W_STAGE_BYTES * (uint32_t)p.tps;
     uint32_t cols = 32;
-    while (cols < 2u * (uint32_t)p.N_pad) cols <<= 1;
+    while (cols < 2u * (uint32_t)(p.tps * p.N_pad)) cols <<= 1;
     p.tmem_cols = cols;
-    const size_t fixed = 1024 + 8 * 64 + 64 + (size_t)2 * 4 * p.N_pad * 8;
-    const size_t stage = W_STAGE_BYTES + p.a_stage_bytes;
+    const size_t fixed = 1024 + 8 * 64 + 64 + (size_t)2 * p.tps * 4 * p.N_pad * 8;
+    const size_t stage = p.w_stage_bytes + p.a_stage_bytes;
     int stages = (int)((SMEM_LIMIT - fixed) / stage);
-    if (stages > 8) stages = 8;
+    const int max_stages = p.tps == 2 ? 6 : 8;
+    if (stages > max_stages) stages = max_stages;
     if (stages < 2) return SPEC_ERR_UNSUPPORTED;
     p.stages = stages;
     pl.smem = fixed + (size_t)stages * stage;
     const int sms = sm_count();
     if (sms < 1) return SPEC_ERR_CUDA;
-    const int work = p.n_tiles * p.splits;
+    const int work = p.n_groups * p.splits;
     int g = work < sms ? work : sms;
     if (g > MAX_CTAS) g = MAX_CTAS;
     pl.grid = g;
@@ -411,7 +440,7 @@ static int plan(int M, int V, int K, int splits, TcPlan &pl) {
 template <int EPI>
 static int launch_tc(const void *A, const void *W, TcPlan &pl, cudaStream_t s) {
     CUtensorMap mw, ma;
-    if (!make_map(&mw, W, pl.p.V, pl.p.K, TC_BM) || !make_map(&ma, A, pl.p.M, pl.p.K, pl.p.N_pad))
+    if (!make_map(&mw, W, pl.p.V, pl.p.K, TC_BM * pl.p.tps) || !make_map(&ma, A, pl.p.M, pl.p.K, pl.p.N_pad))
         return SPEC_ERR_CUDA;
     // Always the same ceiling, never the launch's own size: a CUDA graph may hold launches
     // of this kernel with different shared-memory sizes, and lowering the attribute for a
@@ -463,12 +492,13 @@ int gemm_store_bf16(const void *A, const void *W, int M, int N, int K, void *out
     if (ws_bytes < gemm_store_ws_bytes(M, N, K)) return SPEC_ERR_WORKSPACE;
     const int sms = sm_count();
     if (sms < 1) return SPEC_ERR_CUDA;
-    const int tiles = (N + TC_BM - 1) / TC_BM;
-    int splits = sms / tiles;
+    TcPlan pl;
+    int st = plan(M, N, K, 1, pl);  // for the number of tile groups
+    if (st) return st;
+    int splits = sms / pl.p.n_groups;
     if (splits < 1) splits = 1;
     if (splits > MAX_SPLITS) splits = MAX_SPLITS;
-    TcPlan pl;
-    int st = plan(M, N, K, splits, pl);
+    st = plan(M, N, K, splits, pl);
     if (st) return st;
     pl.p.partial = (float *)ws;
     st = launch_tc<TC_PARTIAL>(A, W, pl, s);

@@ -85,6 +85,23 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     return mbar_try_wait(bar, parity) || mbar_wait_loop(bar, parity, abort, timeout_ns, 0);
 }
 
+// The same wait by non-blocking probes (mbarrier.test_wait), for threads that share a warp
+// with another thread on its own loop: a probe never holds the warp, so the other thread's
+// path keeps being issued while this one waits.
+static __device__ __noinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, volatile int *abort,
+                                            uint64_t timeout_ns) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            const uint64_t t = globaltimer();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > timeout_ns) return false;
+        }
+    }
+}
+
 // The same wait for a thread that is not latency-critical: between probes it sleeps about
 // sleep_ns, leaving the SM sub-partition's issue slots to the warps that do the math.
 __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int *abort,
@@ -240,6 +257,14 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 // (TMA / tensor core) accesses.
 // 2^x with the SFU's approximate base-2 exponential (PTX ex2.approx.ftz: about 2 ulp,
 // subnormal results flushed to zero; 2^-inf = 0).
+// maximum of v over the 32 lanes of the warp, in every lane (NaN inputs are ignored, as by
+// fmaxf)
+__device__ __forceinline__ float warp_max_f32(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -293,6 +318,11 @@ __device__ __forceinline__ uint64_t desc_kmajor(uint32_t saddr, uint32_t row_byt
     d |= (uint64_t)(row_bytes == 64 ? 4u : 2u) << 61;  // 64-byte or 128-byte swizzle
     return d;
 }
+
+// Advances a shared-memory matrix descriptor's start address by `bytes` (a multiple of 16).
+// The address field holds bits 4..17 of the byte address, so for any shared-memory address
+// the sum never carries out of it: two integer adds instead of a new descriptor per MMA.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
 
 // Shared-memory matrix descriptor: MN-major operand, 32-byte swizzle. Each 32-byte row holds
 // 16 consecutive MN elements of one K index; 8 K rows form a 256-byte atom (stride byte

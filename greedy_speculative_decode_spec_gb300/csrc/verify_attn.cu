@@ -32,16 +32,19 @@
 // A persistent CTA per SM walks work units handed out by a global counter, with
 // warp-specialised roles:
 //   warps 0-3  softmax (warp w reads TMEM lane quadrant w: keys 32w..32w+31 of S, head-dim
-//              lanes 32w.. of O), the unit's epilogue and the split merges;
-//   warps 4-7  bf16 pools: gather K and V rows with 16-byte cp.async copies (zero fill past
-//              the branch's last position) into the 128-byte-swizzled operand ring;
-//              FP8 pools: warp 4 issues TMA boxes of one page-run each (K straight into the
-//              MMA layout, V into a raw stage), warps 5-7 split Q and turn V codes into
-//              scaled bf16 rows;
+//              lanes 32w.. of O) and each unit's epilogue, deferred until the next unit's
+//              first P has been handed off;
+//   warps 4-7  bf16 pools: warps 4-5 gather K rows, warps 6-7 V rows, with 16-byte cp.async
+//              copies (zero fill past the branch's last position) into the 128-byte-swizzled
+//              K and V rings; FP8 pools: turn the raw E4M3 V sub-tiles into scaled bf16 rows
+//              of the V ring (one warp per SM sub-partition);
 //   warp 8     per unit: takes the next work unit, fills the page table entries (and FP8
-//              scales) into a shared table, loads Q by 3-D TMA boxes;
+//              scales) into a shared table, loads Q by TMA boxes;
 //   warp 9     issues S = K . Q^T of each tile (TMEM allocation is also this warp's);
-//   warp 10    issues O += V^T . P^T and L += 1 . P^T of each tile.
+//   warp 10    issues O += V^T . P^T and L += 1 . P^T of each tile;
+//   warp 11    FP8 pools: TMA boxes of one page-run each, lane 0 K (straight into the MMA
+//              layout), lane 1 V (into the raw ring), each lane on its own loop; no role for
+//              bf16 pools.
 // Keys beyond a row's position get P = 0 by select, never by multiplication, and V rows
 // past the branch's last position are zero, so NaN in unused pool slots cannot reach a
 // result. Tile and split boundaries sit at fixed key positions, and every MMA column is
@@ -75,11 +78,11 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_TAU = 8.0f;  // P <= 2^8: exact range for bf16 and f16 alike
 constexpr uint64_t ATT_WAIT_NS = 1000000000ull;
 constexpr int ATT_SMEM_LIMIT = 227 * 1024;
-constexpr int ATT_THREADS = 352;
+constexpr int ATT_THREADS = 384;
 
 constexpr int UT_ENTRIES = SPLIT_KEYS / 8;
 struct UnitInfo {
-    int b, g, split, pos_b, kv_end, s0, T, n_used, u;  // u: the unit's workspace slot
+    int b, g, split, rank, pos_b, kv_end, s0, T, n_used, u;  // u: the unit's workspace slot
     bool bad_pos;
 };
 
@@ -87,15 +90,16 @@ struct UnitInfo {
 // role), the page of each page-sized run of the split's keys (-1 if the table entry is
 // invalid), the page's FP8 K / V scales, and the error bits of any invalid entry. Pages are
 // listed for pages of >= 8 positions.
-struct UnitTable {
+struct alignas(16) UnitTable {
     int32_t page[UT_ENTRIES];
     float ksc[UT_ENTRIES];
     float vsc[UT_ENTRIES];
     UnitInfo ui;
     int32_t bad;
     int32_t iter;          // the unit's index in the walk order, or -1: no more units
-    int32_t pad_[20];
 };
+// the softmax scratch that follows the two tables is read with 16-byte vector loads
+static_assert(sizeof(UnitTable) % 16 == 0, "unit table size must keep 16-byte alignment");
 
 // Split size in positions, a function of the model's KV-head count only (never of B, k or
 // the context length, so a row's split boundaries are the same in every batch): few KV
@@ -144,7 +148,7 @@ struct AttnParams {
 // kernel and the host plan, which checks that they fit BAR_BYTES).
 struct BarMap {
     uint32_t kfull, kempty, vfull, vempty, rfull, rempty, sfull, sfree, pfull, pfree, ofree;
-    uint32_t qfull, qfree, ufull, ufree, lfin, drain, xbar, cjoin, end;
+    uint32_t qfull, qfree, ufull, ufree, lfin, drain, xbar, end;
 };
 __host__ __device__ inline BarMap bar_map(int NK, int NV, int NR, int NSB, int NPB) {
     BarMap m;
@@ -167,31 +171,34 @@ __host__ __device__ inline BarMap bar_map(int NK, int NV, int NR, int NSB, int N
     m.lfin = o;     o += 16;
     m.drain = o;    o += 16;
     m.xbar = o;     o += 16;   // softmax column-maximum exchange, by group parity
-    m.cjoin = o;    o += 8;    // the two FP8 converter warps
     m.end = o;
     return m;
 }
 constexpr uint32_t BAR_BYTES = 8 * 96;
 
-// The scheduler hands out units split-major (every (branch, head) pair's first split, then
-// every pair's second split, ...), which puts each pair's short last split late;
-// `u` (the workspace slot) is (branch, head, split)-major, so a merge group's partials are
-// contiguous.
+// The scheduler hands out units by rank, the rank of a split being its distance from its
+// pair's last split: first every (branch, head) pair's split of rank n_splits - 1 (only the
+// longest pairs have one), ..., last every pair's rank-0 split, its last and only partial
+// one. Long pairs thus start first and the short partial units come last, where they fill
+// the gaps of the grid's final wave; walk entries with no split (rank >= the pair's split
+// count) are empty. `u` (the workspace slot) is (branch, head, split)-major, so a merge
+// group's partials are contiguous.
 static __device__ __noinline__ UnitInfo unit_info(const AttnParams &p, int iter) {
     UnitInfo ui;
     const int pairs = p.B * p.kv.n_kv_heads;
-    ui.split = iter / pairs;
+    ui.rank = p.n_splits - 1 - iter / pairs;
     ui.g = (iter % pairs) % p.kv.n_kv_heads;
     ui.b = (iter % pairs) / p.kv.n_kv_heads;
-    ui.u = (ui.b * p.kv.n_kv_heads + ui.g) * p.n_splits + ui.split;
     ui.pos_b = __ldg(p.pos + ui.b);
     ui.bad_pos = ui.pos_b < 0 || ui.pos_b + p.k + 1 > p.max_pos;
     ui.kv_end = ui.pos_b + p.k + 1;
-    ui.s0 = ui.split * p.split_keys;
-    int n = ui.bad_pos ? 0 : ui.kv_end - ui.s0;
-    n = n < 0 ? 0 : (n > p.split_keys ? p.split_keys : n);
-    ui.T = (n + TILE_KEYS - 1) / TILE_KEYS;
     ui.n_used = ui.bad_pos ? 0 : (ui.kv_end + p.split_keys - 1) / p.split_keys;
+    ui.split = ui.n_used - 1 - ui.rank;  // < 0: no such split
+    ui.u = (ui.b * p.kv.n_kv_heads + ui.g) * p.n_splits + (ui.split < 0 ? 0 : ui.split);
+    ui.s0 = ui.split * p.split_keys;
+    int n = ui.split < 0 ? 0 : ui.kv_end - ui.s0;
+    n = n > p.split_keys ? p.split_keys : n;
+    ui.T = (n + TILE_KEYS - 1) / TILE_KEYS;
     return ui;
 }
 
@@ -210,6 +217,32 @@ template <uint32_t SLEEP = 0>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, uint64_t ns) {
     const bool r = SLEEP ? mbar_wait_sleep(bar, parity, abort_flag, ns, SLEEP) : mbar_wait(bar, parity, abort_flag, ns);
     return __all_sync(0xFFFFFFFFu, r);
+}
+// A position in a ring of n stages: the stage and the parity of its current use (kept by
+// increments, so that no loop divides by a run-time ring size).
+struct RingPos {
+    uint32_t s = 0, ph = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++s == (uint32_t)n) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+    __device__ __forceinline__ void prev(int n) {
+        if (s == 0) {
+            s = (uint32_t)n;
+            ph ^= 1u;
+        }
+        --s;
+    }
+};
+// Waits (drain, bounded) for the last min(used, n) completed phases of a ring's barriers,
+// walking back from the position after the last use.
+__device__ __noinline__ void drain_ring(uint32_t bar0, RingPos r, int n, uint32_t used) {
+    for (uint32_t j = 0; j < (uint32_t)n && j < used; ++j) {
+        r.prev(n);
+        mbar_wait(bar0 + 8 * r.s, r.ph, nullptr, ATT_WAIT_NS);
+    }
 }
 constexpr uint32_t SLEEP_LOAD = 128;  // loaders, converters, producer
 constexpr uint32_t SLEEP_MMA = 32;    // MMA issuers
@@ -255,20 +288,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const uint32_t qfull = bar0 + bm.qfull, qfree = bar0 + bm.qfree;
     const uint32_t ufull = bar0 + bm.ufull, ufree = bar0 + bm.ufree, lfin = bar0 + bm.lfin;
     const uint32_t drain = bar0 + bm.drain, xbar = bar0 + bm.xbar;
-    const uint32_t cjoin = bar0 + bm.cjoin;
     uint8_t *small = smem + p.off_small;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(small);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(small + 4);
-    // softmax scratch: column-maximum exchange [2 tile parities][4 warps][NQ], then per warp
-    // its copy of the running maxima, the rescale factors and the column limits [4][NQ],
-    // then the E4M3 Q scales [2 unit tables][NQ], then per tile parity and warp whether a
-    // running maximum must move
+    // softmax scratch: column-maximum exchange [2 exchange slots][4 warps][NQ], then per warp
+    // its copy of the running maxima [2 unit parities][4][NQ] (a unit's maxima outlive it
+    // until its deferred epilogue), the rescale factors and the column limits [4][NQ], then
+    // the E4M3 Q scales [2 unit tables][NQ], then per exchange slot and warp whether a running
+    // maximum must move
     float *sx_red = reinterpret_cast<float *>(smem + p.off_sx);
     float *sx_m = sx_red + 8 * NQ;
-    float *sx_f = sx_m + 4 * NQ;
+    float *sx_f = sx_m + 8 * NQ;
     int *sx_lim = reinterpret_cast<int *>(sx_f + 4 * NQ);
     float *sx_qinv = reinterpret_cast<float *>(sx_lim + 4 * NQ);
-    int *sx_need = reinterpret_cast<int *>(sx_qinv + 2 * NQ);  // [2 tile parities][4 warps]
+    int *sx_need = reinterpret_cast<int *>(sx_qinv + 2 * NQ);  // [2 exchange slots][4 warps]
     // per query column q = j*G + i: its draft row j (-1 for padding) and its output offset
     // (j*Hq + i)*D from the (branch, kv head)'s first output
     int *sx_colj = sx_need + 8;
@@ -285,12 +318,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             mbar_init(kempty + 8 * s, 1);            // an S MMA commit
         }
         for (int s = 0; s < p.NV; ++s) {
-            mbar_init(vfull + 8 * s, FP8 ? 1 : 64);  // FP8: the converters; bf16: each V loader thread
+            mbar_init(vfull + 8 * s, FP8 ? 4 : 64);  // FP8: each converter warp; bf16: each V loader thread
             mbar_init(vempty + 8 * s, 1);            // a P.V commit
         }
         for (int s = 0; s < p.NR; ++s) {
             mbar_init(rfull + 8 * s, 1);             // the TMA bytes
-            mbar_init(rempty + 8 * s, 1);            // the converters
+            mbar_init(rempty + 8 * s, 4);            // each converter warp
         }
         for (int s = 0; s < p.NSB; ++s) {
             mbar_init(sfull + 8 * s, 1);
@@ -305,12 +338,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             mbar_init(qfull + 8 * a, 1);
             mbar_init(qfree + 8 * a, 1);
             mbar_init(ufull + 8 * a, 1);
-            mbar_init(ufree + 8 * a, 10);  // softmax 4, loader roles 4, both MMA issuers
-            mbar_init(lfin + 8 * a, FP8 ? 2 : 4);
+            // softmax 4, both MMA issuers, bf16 loaders 4 / FP8 converters 4 and the two TMA lanes
+            mbar_init(ufree + 8 * a, FP8 ? 12 : 10);
+            mbar_init(lfin + 8 * a, FP8 ? 1 : 2);  // the K stream: FP8 its TMA lane, bf16 its two loader warps
             mbar_init(drain + 8 * a, 1);
             mbar_init(xbar + 8 * a, 4);
         }
-        mbar_init(cjoin, 2);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -358,13 +391,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     if (warp == 8) {
         // ================= producer: per unit, the page table entries and Q =================
         // Units are handed out dynamically: the producer takes the next index of the
-        // split-major walk from a global counter, skips empty units, and publishes the unit
+        // rank-ordered walk from a global counter, skips empty units, and publishes the unit
         // in the shared table that every other role waits on (-1 ends their loops). It takes
-        // a unit only once a table is free and the loaders are issuing the last two tiles of
+        // a unit only once a table is free and the K loads are issuing the last three tiles of
         // the previous unit: late enough that a CTA holds little more than the work in its
         // rings (the last units go to whichever CTAs run out of work first), early enough that
         // the next unit's table and Q are ready when the loaders get to it.
         uint32_t ua = 0;
+        RingPos qr;  // Q buffers
         bool ok = true;
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
@@ -386,7 +420,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                     it_u = cand;
                     break;
                 }
-                if (ui.bad_pos && ui.split == 0 && ui.g == 0 && lane == 0) raise_error(p.err, SPEC_DEVERR_POS);
+                if (ui.bad_pos && ui.rank == 0 && ui.g == 0 && lane == 0) raise_error(p.err, SPEC_DEVERR_POS);
             }
             if (it_u < 0) {
                 if (lane == 0) tab->iter = -1;
@@ -442,8 +476,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             // bf16: one 3-D box per 64-column block lands as rows j*G + i. FP8: the two E4M3
             // parts (hi, lo) of the split queries, one 2-D box per 128-byte column block each
             // (the split kernel wrote them as [pair][part][NQ][d] bytes).
-            const uint32_t qs = ua % (uint32_t)p.QB, qph = (ua / (uint32_t)p.QB) & 1u;
-            if (!warp_wait<SLEEP_LOAD>(qfree + 8 * qs, qph ^ 1u, abort_flag, wns)) { ok = false; break; }
+            const uint32_t qs = qr.s;
+            if (!warp_wait<SLEEP_LOAD>(qfree + 8 * qs, qr.ph ^ 1u, abort_flag, wns)) { ok = false; break; }
             if (lane == 0) {
                 if (FP8) {
                     mbar_arrive_expect_tx(qfull + 8 * qs, (uint32_t)(2 * NQ * D));
@@ -464,6 +498,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             }
             __syncwarp();
             ++ua;
+            qr.next(p.QB);
         }
         if (!ok) {
             *abort_flag = 1;
@@ -478,17 +513,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             }
         }
         // the Q copies still in flight land before the CTA may exit
-        if (lane == 0) {
-            for (uint32_t j = 0; j < (uint32_t)p.QB && j < ua; ++j) {
-                const uint32_t i2 = ua - 1 - j;
-                mbar_wait(qfull + 8 * (i2 % (uint32_t)p.QB), (i2 / (uint32_t)p.QB) & 1u, nullptr, ATT_WAIT_NS);
-            }
-        }
+        if (lane == 0) drain_ring(qfull, qr, p.QB, ua);
         __syncwarp();
     } else if (warp == 9) {
         // ================= MMA issuer: S^T = K . Q^T =================
         const uint32_t idesc = FP8 ? idesc_f8_e4m3(128, NQ) : idesc_f16kind(128, NQ, false, false, false);
-        uint32_t gs = 0, ua = 0, gk = 0;  // tile groups, active units, K sub-tiles consumed
+        uint32_t gs = 0, ua = 0;  // tile groups, active units
+        RingPos kr, sr, qr;       // K ring, S buffers, Q buffers
         bool ok = true;
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
@@ -500,15 +531,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             (void)u;
             __syncwarp();
             if (lane == 0) mbar_arrive(ufree + 8 * ub);
-            const uint32_t qs = ua % (uint32_t)p.QB, qph = (ua / (uint32_t)p.QB) & 1u;
-            if (!warp_wait<SLEEP_MMA>(qfull + 8 * qs, qph, abort_flag, wns)) { ok = false; break; }
+            const uint32_t qs = qr.s;
+            if (!warp_wait<SLEEP_MMA>(qfull + 8 * qs, qr.ph, abort_flag, wns)) { ok = false; break; }
             tc_fence_after();
-            for (int t0 = 0; t0 < ui.T; t0 += p.TPI, ++gs) {
+            for (int t0 = 0; t0 < ui.T; t0 += p.TPI, ++gs, sr.next(p.NSB)) {
                 // a group of up to TPI tiles: each tile's S into its own NQ columns of the group's
                 // S buffer, one "full" signal for the group
-                const uint32_t sb = gs % (uint32_t)p.NSB;
+                const uint32_t sb = sr.s;
                 const int nt = min(p.TPI, ui.T - t0);
-                if (!warp_wait<SLEEP_MMA>(sfree + 8 * sb, ((gs / (uint32_t)p.NSB) & 1u) ^ 1u, abort_flag, wns)) {
+                if (!warp_wait<SLEEP_MMA>(sfree + 8 * sb, sr.ph ^ 1u, abort_flag, wns)) {
                     ok = false;
                     break;
                 }
@@ -517,8 +548,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 const int t = t0 + i;
 #pragma unroll
                 for (int h = 0; h < S_::NSUB; ++h) {
-                    const uint32_t g = gk++, st = g % (uint32_t)p.NK;
-                    if (!warp_wait<SLEEP_MMA>(kfull + 8 * st, (g / (uint32_t)p.NK) & 1u, abort_flag, wns)) { ok = false; break; }
+                    const uint32_t st = kr.s;
+                    if (!warp_wait<SLEEP_MMA>(kfull + 8 * st, kr.ph, abort_flag, wns)) { ok = false; break; }
+                    kr.next(p.NK);
                     if (!FP8) fence_proxy_async_smem();  // cp.async data -> tensor core reads
                     tc_fence_after();
                     if (lane == 0) {
@@ -526,26 +558,26 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                         const uint32_t d_s = tmem + (sb * (uint32_t)p.TPI + (uint32_t)i) * (uint32_t)NQ;
                         if (FP8) {
                             // S = K . (hi + lo)^T: both E4M3 parts accumulate into one S
+                            const uint64_t ka0 = desc_kmajor(kb, S_::K8ROW, 8 * S_::K8ROW);
+                            const uint64_t qa0 = desc_kmajor(s_q8 + qs * 2 * Q8PART, S_::Q8ROW, 8 * S_::Q8ROW);
 #pragma unroll
                             for (int part = 0; part < 2; ++part) {
-                                const uint32_t qa = s_q8 + (qs * 2 + part) * Q8PART;
 #pragma unroll
                                 for (int kl = 0; kl < S_::SUB / 32; ++kl) {
                                     const int ks = h * (S_::SUB / 32) + kl;  // 32-byte step over all of d
                                     const uint32_t qoff = S_::Q8ROW == 128 ? (ks >> 2) * Q8ATOM + (ks & 3) * 32
                                                                            : (uint32_t)ks * 32;
-                                    mma_f8(d_s, desc_kmajor(kb + kl * 32, S_::K8ROW, 8 * S_::K8ROW),
-                                           desc_kmajor(qa + qoff, S_::Q8ROW, 8 * S_::Q8ROW), idesc,
+                                    mma_f8(d_s, desc_advance(ka0, kl * 32), desc_advance(qa0, part * Q8PART + qoff), idesc,
                                            (h > 0 || part > 0 || kl > 0) ? 1u : 0u);
                                 }
                             }
                         } else {
+                            const uint64_t ka0 = desc_kmajor(kb, 128, 1024), qb0 = desc_kmajor(s_q + qs * QBUF, 128, 1024);
 #pragma unroll
                             for (int kl = 0; kl < S_::SUB / 16; ++kl) {
                                 const int ks = h * (S_::SUB / 16) + kl;  // 16-element step over all of d
-                                mma_bf16(d_s, desc_kmajor(kb + (kl >> 2) * (TILE_KEYS * 128) + (kl & 3) * 32, 128, 1024),
-                                         desc_kmajor(s_q + qs * QBUF + (ks >> 2) * QATOM + (ks & 3) * 32, 128, 1024),
-                                         idesc, ks > 0 ? 1u : 0u);
+                                mma_bf16(d_s, desc_advance(ka0, (kl >> 2) * (TILE_KEYS * 128) + (kl & 3) * 32),
+                                         desc_advance(qb0, (ks >> 2) * QATOM + (ks & 3) * 32), idesc, ks > 0 ? 1u : 0u);
                             }
                         }
                         mma_commit(kempty + 8 * st);
@@ -563,6 +595,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             }
             if (!ok) break;
             ++ua;
+            qr.next(p.QB);
         }
         if (!ok) {
             *abort_flag = 1;
@@ -574,14 +607,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             // every arrive sent by this issuer's commits is delivered before the CTA may exit:
             // the last phase of the S buffers' "full" barriers and of the Q buffers' "free"
             // (the ring's "empty" phases are drained by the loaders' waits below)
-            for (uint32_t j = 0; j < (uint32_t)p.NSB && j < gs; ++j) {
-                const uint32_t t2 = gs - 1 - j;
-                mbar_wait(sfull + 8 * (t2 % (uint32_t)p.NSB), (t2 / (uint32_t)p.NSB) & 1u, nullptr, ATT_WAIT_NS);
-            }
-            for (uint32_t j = 0; j < (uint32_t)p.QB && j < ua; ++j) {
-                const uint32_t i2 = ua - 1 - j;
-                mbar_wait(qfree + 8 * (i2 % (uint32_t)p.QB), (i2 / (uint32_t)p.QB) & 1u, nullptr, ATT_WAIT_NS);
-            }
+            drain_ring(sfull, sr, p.NSB, gs);
+            drain_ring(qfree, qr, p.QB, ua);
         }
         __syncwarp();
     } else if (warp == 10) {
@@ -592,6 +619,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         // head dimension repeats its one block on lanes 64..127 (never read)
         const uint32_t v_lbo = S_::SUB == 128 ? TILE_KEYS * 128 : 0;
         uint32_t gp = 0, gv = 0, ua = 0;  // tile groups, V sub-tiles consumed, units
+        RingPos pr, vr, orr;              // P buffers, V ring, O buffers
         bool ok = true;
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
@@ -603,31 +631,32 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             (void)u;
             __syncwarp();
             if (lane == 0) mbar_arrive(ufree + 8 * ub);
-            const uint32_t ob = ua % (uint32_t)p.OB;
-            if (!warp_wait<SLEEP_MMA>(ofree + 8 * ob, ((ua / (uint32_t)p.OB) & 1u) ^ 1u, abort_flag, wns)) { ok = false; break; }
+            const uint32_t ob = orr.s;
+            if (!warp_wait<SLEEP_MMA>(ofree + 8 * ob, orr.ph ^ 1u, abort_flag, wns)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d_o = t_o0 + ob * (uint32_t)((S_::NSUB + 1) * NQ);
-            for (int t0 = 0; t0 < ui.T; t0 += p.TPI, ++gp) {
-                const uint32_t pb = gp % (uint32_t)p.NPB;
+            for (int t0 = 0; t0 < ui.T; t0 += p.TPI, ++gp, pr.next(p.NPB)) {
+                const uint32_t pb = pr.s;
                 const int nt = min(p.TPI, ui.T - t0);
-                if (!warp_wait<SLEEP_MMA>(pfull + 8 * pb, (gp / (uint32_t)p.NPB) & 1u, abort_flag, wns)) { ok = false; break; }
+                if (!warp_wait<SLEEP_MMA>(pfull + 8 * pb, pr.ph, abort_flag, wns)) { ok = false; break; }
 #pragma unroll 1
                 for (int i = 0; i < nt && ok; ++i) {
                 const int t = t0 + i;
                 const uint32_t pa = s_p + pb * PBUF + (uint32_t)i * PTILE;
 #pragma unroll
                 for (int h = 0; h < S_::NSUB; ++h) {
-                    const uint32_t st = gv % (uint32_t)p.NV;
-                    if (!warp_wait<SLEEP_MMA>(vfull + 8 * st, (gv / (uint32_t)p.NV) & 1u, abort_flag, wns)) { ok = false; break; }
+                    const uint32_t st = vr.s;
+                    if (!warp_wait<SLEEP_MMA>(vfull + 8 * st, vr.ph, abort_flag, wns)) { ok = false; break; }
                     if (!FP8) fence_proxy_async_smem();  // cp.async data -> tensor core reads
                     const uint32_t vb = s_v + st * S_::OP_STAGE, rel = vempty + 8 * st;
                     ++gv;
+                    vr.next(p.NV);
                     tc_fence_after();
                     if (lane == 0) {
+                        const uint64_t va0 = desc_mnmajor_sw128(vb, v_lbo), pa0 = desc_mnmajor_sw32(pa, TILE_KEYS * 32);
 #pragma unroll
                         for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
-                            mma_bf16(d_o + h * NQ, desc_mnmajor_sw128(vb + ks * 2048, v_lbo),
-                                     desc_mnmajor_sw32(pa + ks * 512, TILE_KEYS * 32), idesc_pv,
+                            mma_bf16(d_o + h * NQ, desc_advance(va0, ks * 2048), desc_advance(pa0, ks * 512), idesc_pv,
                                      (t > 0 || ks > 0) ? 1u : 0u);
                         mma_commit(rel);
                     }
@@ -636,14 +665,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 }
                 if (!ok) break;
                 if (lane == 0) {
+                    const uint64_t one0 = desc_kmajor(s_ones, 128, 0);
+#pragma unroll 1
                     for (int i = 0; i < nt; ++i) {
                         const int t = t0 + i;
-                        const uint32_t pa = s_p + pb * PBUF + (uint32_t)i * PTILE;
+                        const uint64_t pa0 = desc_mnmajor_sw32(s_p + pb * PBUF + (uint32_t)i * PTILE, TILE_KEYS * 32);
 #pragma unroll
                         for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
-                            mma_bf16(d_o + S_::NSUB * NQ, desc_kmajor(s_ones + (ks & 3) * 32, 128, 0),
-                                     desc_mnmajor_sw32(pa + ks * 512, TILE_KEYS * 32), idesc_l,
-                                     (t > 0 || ks > 0) ? 1u : 0u);
+                            mma_bf16(d_o + S_::NSUB * NQ, desc_advance(one0, (ks & 3) * 32), desc_advance(pa0, ks * 512),
+                                     idesc_l, (t > 0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(pfree + 8 * pb);  // also: this group's O and L are complete
                 }
@@ -651,6 +681,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             }
             if (!ok) break;
             ++ua;
+            orr.next(p.OB);
         }
         if (!ok) {
             *abort_flag = 1;
@@ -660,17 +691,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             mma_commit(drain + 8);
             mbar_wait(drain + 8, 0, nullptr, ATT_WAIT_NS);
             // the last phases of the P buffers' "free" barriers and of the P.V completion
-            for (uint32_t j = 0; j < (uint32_t)p.NPB && j < gp; ++j) {
-                const uint32_t t2 = gp - 1 - j;
-                mbar_wait(pfree + 8 * (t2 % (uint32_t)p.NPB), (t2 / (uint32_t)p.NPB) & 1u, nullptr, ATT_WAIT_NS);
-            }
-            if (FP8) {  // (bf16: the V loaders drain the V ring's "empty" phases)
-                const uint32_t n_last = gv < (uint32_t)p.NV ? gv : (uint32_t)p.NV;
-                for (uint32_t j = 0; j < n_last; ++j) {
-                    const uint32_t i2 = gv - 1 - j;
-                    mbar_wait(vempty + 8 * (i2 % (uint32_t)p.NV), (i2 / (uint32_t)p.NV) & 1u, nullptr, ATT_WAIT_NS);
-                }
-            }
+            drain_ring(pfree, pr, p.NPB, gp);
+            if (FP8) drain_ring(vempty, vr, p.NV, gv);  // (bf16: the V loaders drain the V ring's "empty" phases)
         }
         __syncwarp();
     } else if (warp < 4) {
@@ -678,222 +700,31 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         const int qd = warp;
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
         const int kl = qd * 32 + lane;           // this thread's key within a tile
-        float *my_m = sx_m + qd * NQ, *my_f = sx_f + qd * NQ;
+        float *my_f = sx_f + qd * NQ;
         int *my_lim = sx_lim + qd * NQ;
         const float sl = p.scale_log2;
         const int nch = NQ / 16;                 // 16-column chunks
-        uint32_t gs = 0, gp = 0, ua = 0;  // tile groups (S side, P side), units
+        uint32_t ua = 0;                  // units
+        RingPos sr, pr, pr_last, orr;     // S buffers, P buffers (and the last group's), O buffers
+        uint32_t nx = 0;                  // exchanges among the softmax warps (two barriers, alternating)
         bool ok = true;
-        while (ok) {
-            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
-            if (!warp_wait(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
-            const UnitTable *tab = tables + ub;
-            const int it_u = tab->iter;
-            if (it_u < 0) break;
-            const UnitInfo ui = tables[ub].ui;
-            const int u = ui.u;
-            (void)u;
-            const bool failed = tab->bad != 0;
-            const uint32_t ob = ua % (uint32_t)p.OB;
-            // the E4M3 query scales of this unit: written by the producer before it published
-            // the table, rewritten only for unit ua + 2 (after this warp releases the table)
-            const float *qinv = sx_qinv + ub * NQ;
-            // per unit: running maxima, and the last key offset (from the split's start) each
-            // column sees: row j of the branch sees positions <= pos_b + j
-            for (int q = lane; q < NQ; q += 32) {
-                my_m[q] = -INFINITY;
-                my_lim[q] = q < n_q ? ui.pos_b + sx_colj[q] - ui.s0 : -1;
-            }
-            __syncwarp();
-            for (int t0 = 0; t0 < ui.T && ok; t0 += p.TPI, ++gs, ++gp) {
-                // a group of nt <= TPI tiles: one column-maximum exchange, one update of the
-                // running maxima and one P hand-off for all of its keys
-                const uint32_t sb = gs % (uint32_t)p.NSB, pb = gp % (uint32_t)p.NPB, tb = gs & 1u;
-                const int nt = min(p.TPI, ui.T - t0);
-                ok = warp_wait(sfull + 8 * sb, (gs / (uint32_t)p.NSB) & 1u, abort_flag, wns);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t sgrp = tmem + lane_base + sb * (uint32_t)(p.TPI * NQ);
-                // x of column q for this thread's key of tile i = s * slk (* 1/sigma for E4M3
-                // queries; slk = softmax scale, times the K page scale for FP8 pools), -inf where
-                // the key is not seen by the column's row; a warp whose 32 keys every row sees
-                // skips the limits (the padding columns then hold finite zero scores: their Q
-                // rows are 0)
-                auto xchunk = [&](int i, int c, const uint32_t (&r)[16], float (&x)[16]) {
-                    const int koff = (t0 + i) * TILE_KEYS + kl;  // key offset from the split's start
-                    float slk = sl;
-                    if (FP8) slk = ui.s0 + koff < ui.kv_end ? sl * tab->ksc[koff >> log2P] : 0.f;
-                    const bool all_vis = __all_sync(0xFFFFFFFFu, koff <= ui.pos_b - ui.s0);
-                    float qsc[16];
-                    if (FP8) {
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const float4 a = *reinterpret_cast<const float4 *>(qinv + c * 16 + j);
-                            qsc[j] = a.x; qsc[j + 1] = a.y; qsc[j + 2] = a.z; qsc[j + 3] = a.w;
-                        }
-                    }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) x[j] = FP8 ? (__uint_as_float(r[j]) * slk) * qsc[j] : __uint_as_float(r[j]) * slk;
-                    if (!all_vis) {
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const int4 a = *reinterpret_cast<const int4 *>(my_lim + c * 16 + j);
-                            x[j] = koff <= a.x ? x[j] : -INFINITY;
-                            x[j + 1] = koff <= a.y ? x[j + 1] : -INFINITY;
-                            x[j + 2] = koff <= a.z ? x[j + 2] : -INFINITY;
-                            x[j + 3] = koff <= a.w ? x[j + 3] : -INFINITY;
-                        }
-                    }
-                };
-                // ---- pass 1: the group's column maxima over this warp's keys ----
-                float *red = sx_red + tb * 4 * NQ + qd * NQ;
-                bool need = false;
-#pragma unroll 1
-                for (int c = 0; c < nch; ++c) {
-                    float v[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = -INFINITY;
-#pragma unroll 1
-                    for (int i = 0; i < nt; ++i) {
-                        uint32_t r[16];
-                        float x[16];
-                        tmem_ld16(sgrp + (uint32_t)(i * NQ + c * 16), r);
-                        tmem_ld_wait();
-                        xchunk(i, c, r, x);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = fmaxf(v[j], x[j]);
-                    }
-                    // butterfly: halves exchanged at lane distances 16, 8, 4, 2, then a full
-                    // exchange at 1; even lane l ends with the maximum of column
-                    // c*16 + (bit 4 of l)*8 + (bit 3)*4 + (bit 2)*2 + (bit 1)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const bool up = (lane & 16) != 0;
-                        const float got = __shfl_xor_sync(0xFFFFFFFFu, up ? v[j] : v[j + 8], 16);
-                        v[j] = fmaxf(up ? v[j + 8] : v[j], got);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const bool up = (lane & 8) != 0;
-                        const float got = __shfl_xor_sync(0xFFFFFFFFu, up ? v[j] : v[j + 4], 8);
-                        v[j] = fmaxf(up ? v[j + 4] : v[j], got);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const bool up = (lane & 4) != 0;
-                        const float got = __shfl_xor_sync(0xFFFFFFFFu, up ? v[j] : v[j + 2], 4);
-                        v[j] = fmaxf(up ? v[j + 2] : v[j], got);
-                    }
-                    {
-                        const bool up = (lane & 2) != 0;
-                        const float got = __shfl_xor_sync(0xFFFFFFFFu, up ? v[0] : v[1], 2);
-                        v[0] = fmaxf(up ? v[1] : v[0], got);
-                    }
-                    v[0] = fmaxf(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], 1));
-                    const int col = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
-                    if ((lane & 1) == 0) red[c * 16 + col] = v[0];
-                    need |= v[0] > my_m[c * 16 + col] + RESCALE_TAU;  // this column's maximum must move
-                }
-                need = __any_sync(0xFFFFFFFFu, need);
-                if (lane == 0) sx_need[tb * 4 + qd] = need ? 1 : 0;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(xbar + 8 * tb);
-                ok = warp_wait(xbar + 8 * tb, (gs >> 1) & 1u, abort_flag, wns);
-                if (!ok) break;
-                // ---- the group's maxima over the four warps; lazily raised running maxima (only
-                // when some warp saw a column exceed its maximum by more than RESCALE_TAU) ----
-                bool resc = false;
-                const float *red_all = sx_red + tb * 4 * NQ;
-                const int4 nd = *reinterpret_cast<const int4 *>(sx_need + tb * 4);
-                const bool any_need = (nd.x | nd.y | nd.z | nd.w) != 0;
-#pragma unroll 1
-                for (int q = lane; any_need && q < NQ; q += 32) {
-                    const float M = fmaxf(fmaxf(red_all[q], red_all[NQ + q]), fmaxf(red_all[2 * NQ + q], red_all[3 * NQ + q]));
-                    const float mo = my_m[q];
-                    const float mn = (M > mo + RESCALE_TAU) ? M : mo;
-                    my_f[q] = mn == mo ? 1.f : (mo == -INFINITY ? 0.f : ex2_approx(mo - mn));
-                    resc |= mn != mo && mo != -INFINITY;
-                    my_m[q] = mn;
-                }
-                __syncwarp();
-                if (any_need && __any_sync(0xFFFFFFFFu, resc)) {
-                    // a running maximum moved: O and L of this unit are rescaled per column, after
-                    // the P.V of the previous group (this unit's: t0 > 0 here) has completed. Its
-                    // completion is the phase of its P buffer's "free" barrier that follows the
-                    // one this warp waited for before writing that P (a wait is never two
-                    // phases behind)
-                    ok = warp_wait(pfree + 8 * ((gp - 1) % (uint32_t)p.NPB), ((gp - 1) / (uint32_t)p.NPB) & 1u,
-                                   abort_flag, wns);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t orow = t_o0 + lane_base + ob * (uint32_t)((S_::NSUB + 1) * NQ);
-#pragma unroll 1
-                    for (int h = 0; h <= S_::NSUB; ++h) {
-#pragma unroll 1
-                        for (int c = 0; c < nch; ++c) {
-                            uint32_t r[16];
-                            tmem_ld16(orow + h * NQ + c * 16, r);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * my_f[c * 16 + j]);
-                            tmem_st16(orow + h * NQ + c * 16, r);
-                        }
-                    }
-                    tmem_st_wait();
-                }
-                // ---- pass 2: this thread's key rows of P^T, P = 2^(x - m) (0 where the key is not seen) ----
-                ok = warp_wait(pfree + 8 * pb, ((gp / (uint32_t)p.NPB) & 1u) ^ 1u, abort_flag, wns);
-                if (!ok) break;
-                uint8_t *prow = smem + p.off_p + pb * PBUF + kl * 32;
-                const int sw = (kl >> 2) & 1;  // 32-byte swizzle: 16-byte chunk index ^= row bit 2
-#pragma unroll 1
-                for (int i = 0; i < nt; ++i) {
-#pragma unroll 1
-                    for (int c = 0; c < nch; ++c) {
-                        uint32_t r[16];
-                        float x[16], m[16];
-                        tmem_ld16(sgrp + (uint32_t)(i * NQ + c * 16), r);
-                        tmem_ld_wait();
-                        xchunk(i, c, r, x);
-#pragma unroll
-                        for (int j = 0; j < 16; j += 4) {
-                            const float4 a = *reinterpret_cast<const float4 *>(my_m + c * 16 + j);
-                            m[j] = a.x; m[j + 1] = a.y; m[j + 2] = a.z; m[j + 3] = a.w;
-                        }
-                        uint32_t pk[8];
-#pragma unroll
-                        for (int j = 0; j < 16; j += 2) {
-                            const float p0 = x[j] == -INFINITY ? 0.f : ex2_approx(x[j] - m[j]);
-                            const float p1 = x[j + 1] == -INFINITY ? 0.f : ex2_approx(x[j + 1] - m[j + 1]);
-                            pk[j >> 1] = pack2(p0, p1, false);
-                        }
-                        uint8_t *blk = prow + i * PTILE + c * (TILE_KEYS * 32);
-                        *reinterpret_cast<uint4 *>(blk + (sw << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                        *reinterpret_cast<uint4 *>(blk + ((sw ^ 1) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                    }
-                }
-                tc_fence_before();
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(sfree + 8 * sb);
-                    mbar_arrive(pfull + 8 * pb);
-                }
-            }
-            if (!ok) break;
-            // the unit table is no longer read
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ufree + 8 * ub);
-            // ---- epilogue: the unit's O and L, after its last P.V (see the rescale above) ----
-            ok = warp_wait(pfree + 8 * ((gp - 1) % (uint32_t)p.NPB), ((gp - 1) / (uint32_t)p.NPB) & 1u, abort_flag,
-                           wns);
-            if (!ok) break;
+        // The epilogue of a unit is deferred until the first P of the next unit has been handed
+        // off (by then the unit's last P.V has normally completed), so that the softmax warps
+        // do not sit idle waiting for it. Pending: its workspace slot, failure, O buffer, the
+        // parity of its maxima buffer and its last tile group.
+        int pend_u = -1;
+        bool pend_failed = false;
+        uint32_t pend_ob = 0, pend_mb = 0;
+        RingPos pend_pr;
+        auto epilogue = [&]() -> bool {
+            if (!warp_wait(pfree + 8 * pend_pr.s, pend_pr.ph, abort_flag, wns)) return false;
             tc_fence_after();
             // the unit's partial: O[q][d] (this lane's d) and, from warp 0, (m, l) per column
             // (l = -1 marks a unit whose pages were invalid); the combine pass finishes every row
-            const uint32_t orow = t_o0 + lane_base + ob * (uint32_t)((S_::NSUB + 1) * NQ);
-            float *ml = p.ws_ml + (size_t)u * NQ * 2;
-            float *og = p.ws_o + (size_t)u * NQ * D + kl;
+            const uint32_t orow = t_o0 + lane_base + pend_ob * (uint32_t)((S_::NSUB + 1) * NQ);
+            const float *pm = sx_m + (pend_mb * 4 + qd) * NQ;
+            float *ml = p.ws_ml + (size_t)pend_u * NQ * 2;
+            float *og = p.ws_o + (size_t)pend_u * NQ * D + kl;
 #pragma unroll 1
             for (int c = 0; c < nch; ++c) {
 #pragma unroll 1
@@ -914,20 +745,345 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) l = (lane & 15) == j ? __uint_as_float(lr[j]) : l;
                     if (lane < 16) {
-                        ml[(c * 16 + lane) * 2] = my_m[c * 16 + lane];
-                        ml[(c * 16 + lane) * 2 + 1] = failed ? -1.f : l;
+                        ml[(c * 16 + lane) * 2] = pm[c * 16 + lane];
+                        ml[(c * 16 + lane) * 2 + 1] = pend_failed ? -1.f : l;
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(ofree + 8 * ob);
+            if (lane == 0) mbar_arrive(ofree + 8 * pend_ob);
+            pend_u = -1;
+            return true;
+        };
+        while (ok) {
+            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+            if (!warp_wait(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
+            const UnitTable *tab = tables + ub;
+            const int it_u = tab->iter;
+            if (it_u < 0) break;
+            const UnitInfo ui = tables[ub].ui;
+            const int u = ui.u;
+            (void)u;
+            const bool failed = tab->bad != 0;
+            const uint32_t ob = orr.s, mb = ua & 1u;
+            float *my_m = sx_m + (mb * 4 + qd) * NQ;
+            // the E4M3 query scales of this unit: written by the producer before it published
+            // the table, rewritten only for unit ua + 2 (after this warp releases the table)
+            const float *qinv = sx_qinv + ub * NQ;
+            // per unit: running maxima, and the last key offset (from the split's start) each
+            // column sees: row j of the branch sees positions <= pos_b + j
+            for (int q = lane; q < NQ; q += 32) {
+                my_m[q] = -INFINITY;
+                my_lim[q] = q < n_q ? ui.pos_b + sx_colj[q] - ui.s0 : -1;
+            }
+            __syncwarp();
+            for (int t0 = 0; t0 < ui.T && ok; t0 += p.TPI, sr.next(p.NSB), pr_last = pr, pr.next(p.NPB)) {
+                // A group of nt <= TPI tiles shares one P hand-off. After the unit's first group the
+                // group is first tried in one pass with the running maxima: P is written and each
+                // warp notes whether any of its scores exceeds its column's maximum by more than
+                // RESCALE_TAU; only if one does (a flag exchange tells every warp) does the group
+                // take the full path: column maxima, their exchange, the lazily raised maxima
+                // (with O and L rescaled) and P written again. Each pass exists once in the code
+                // (the tiles of a group are selected at run time), to keep the instruction
+                // footprint of the softmax warps small.
+                const uint32_t sb = sr.s, pb = pr.s;
+                const int nt = min(p.TPI, ui.T - t0);
+                ok = warp_wait(sfull + 8 * sb, sr.ph, abort_flag, wns);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sgrp = tmem + lane_base + sb * (uint32_t)(p.TPI * NQ);
+                // per tile i of the group: this thread's key offset from the split's start, its
+                // score factor slk (softmax scale in log2 units; FP8: times the key's K page scale,
+                // 0 past the branch's last position) and whether every row sees all 32 keys of
+                // the warp (then the per-column limits are skipped; the padding columns hold finite
+                // zero scores, their Q rows being 0)
+                const int koff0 = t0 * TILE_KEYS + kl, koff1 = koff0 + TILE_KEYS;
+                float slk0 = sl, slk1 = sl;
+                if (FP8) {
+                    slk0 = ui.s0 + koff0 < ui.kv_end ? sl * tab->ksc[koff0 >> log2P] : 0.f;
+                    slk1 = nt > 1 && ui.s0 + koff1 < ui.kv_end ? sl * tab->ksc[koff1 >> log2P] : 0.f;
+                }
+                const bool vis0 = __all_sync(0xFFFFFFFFu, koff0 <= ui.pos_b - ui.s0);
+                const bool vis1 = __all_sync(0xFFFFFFFFu, koff1 <= ui.pos_b - ui.s0);
+                uint8_t *prow = smem + p.off_p + pb * PBUF + kl * 32;
+                const int sw = (kl >> 2) & 1;  // 32-byte swizzle: 16-byte chunk index ^= row bit 2
+                // the scores s * slk of chunk c of tile i (both tiles' TMEM loads in flight
+                // together, then tile i's registers selected), -inf where the key is not seen by
+                // the column's row
+                auto scores = [&](int i, int c, const uint32_t (&r0)[16], const uint32_t (&r1)[16], float (&x)[16]) {
+                    const float slk = i ? slk1 : slk0;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(i ? r1[j] : r0[j]) * slk;
+                    if (!(i ? vis1 : vis0)) {
+                        const int koff = i ? koff1 : koff0;
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            const int4 a = *reinterpret_cast<const int4 *>(my_lim + c * 16 + j);
+                            x[j] = koff <= a.x ? x[j] : -INFINITY;
+                            x[j + 1] = koff <= a.y ? x[j + 1] : -INFINITY;
+                            x[j + 2] = koff <= a.z ? x[j + 2] : -INFINITY;
+                            x[j + 3] = koff <= a.w ? x[j + 3] : -INFINITY;
+                        }
+                    }
+                };
+                auto load2 = [&](int c, uint32_t (&r0)[16], uint32_t (&r1)[16]) {
+                    tmem_ld16(sgrp + (uint32_t)(c * 16), r0);
+                    if (nt > 1) tmem_ld16(sgrp + (uint32_t)(NQ + c * 16), r1);
+                    tmem_ld_wait();
+                };
+                // the flag (and, on the full path, maxima) exchange among the four warps
+                auto exchange = [&](bool need_w) -> bool {
+                    const uint32_t slot = nx & 1u;
+                    if (lane == 0) sx_need[slot * 4 + qd] = need_w ? 1 : 0;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(xbar + 8 * slot);
+                    ok = warp_wait(xbar + 8 * slot, (nx >> 1) & 1u, abort_flag, wns);
+                    ++nx;
+                    if (!ok) return false;
+                    const int4 nd = *reinterpret_cast<const int4 *>(sx_need + slot * 4);
+                    return (nd.x | nd.y | nd.z | nd.w) != 0;
+                };
+                bool full = t0 == 0, waited = false;
+#pragma unroll 1
+                for (int attempt = 0; attempt < 2; ++attempt) {
+                    if (full) {
+                        // ---- the group's column maxima over this warp's keys: the maximum over the
+                        // tiles, then over the warp's 32 keys by one warp reduction per column; lane
+                        // l < 16 publishes column c*16 + l. For E4M3 queries the 1/sigma factor is
+                        // applied to the maximum (rounding is monotonic, so the result is the maximum
+                        // of the scaled scores exactly) ----
+                        const uint32_t slot = nx & 1u;
+                        float *red = sx_red + slot * 4 * NQ + qd * NQ;
+                        bool need = false;
+#pragma unroll 1
+                        for (int c = 0; c < nch; ++c) {
+                            uint32_t r0[16], r1[16];
+                            load2(c, r0, r1);
+                            float v[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) v[j] = -INFINITY;
+#pragma unroll 1
+                            for (int i = 0; i < nt; ++i) {
+                                float x[16];
+                                scores(i, c, r0, r1, x);
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) v[j] = fmaxf(v[j], x[j]);
+                            }
+                            float mine = -INFINITY;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const float cm = warp_max_f32(v[j]);
+                                mine = (lane & 15) == j ? cm : mine;
+                            }
+                            const int col = c * 16 + (lane & 15);
+                            if (FP8) mine *= qinv[col];
+                            if (lane < 16) red[col] = mine;
+                            need |= mine > my_m[col] + RESCALE_TAU;  // this column's maximum must move
+                        }
+                        need = __any_sync(0xFFFFFFFFu, need);
+                        const bool any_need = exchange(need);
+                        if (!ok) break;
+                        // ---- the group's maxima over the four warps; lazily raised running maxima
+                        // (only when some warp saw a column exceed its maximum by more than
+                        // RESCALE_TAU) ----
+                        bool resc = false;
+                        const float *red_all = sx_red + slot * 4 * NQ;
+#pragma unroll 1
+                        for (int q = lane; any_need && q < NQ; q += 32) {
+                            const float M = fmaxf(fmaxf(red_all[q], red_all[NQ + q]), fmaxf(red_all[2 * NQ + q], red_all[3 * NQ + q]));
+                            const float mo = my_m[q];
+                            const float mn = (M > mo + RESCALE_TAU) ? M : mo;
+                            my_f[q] = mn == mo ? 1.f : (mo == -INFINITY ? 0.f : ex2_approx(mo - mn));
+                            resc |= mn != mo && mo != -INFINITY;
+                            my_m[q] = mn;
+                        }
+                        __syncwarp();
+                        if (any_need && __any_sync(0xFFFFFFFFu, resc)) {
+                            // a running maximum moved: O and L of this unit are rescaled per column,
+                            // after the P.V of the previous group (this unit's: t0 > 0 here) has
+                            // completed. Its completion is the phase of its P buffer's "free"
+                            // barrier that follows the one this warp waited for before writing that
+                            // P (a wait is never two phases behind)
+                            ok = warp_wait(pfree + 8 * pr_last.s, pr_last.ph, abort_flag, wns);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const uint32_t orow = t_o0 + lane_base + ob * (uint32_t)((S_::NSUB + 1) * NQ);
+#pragma unroll 1
+                            for (int h = 0; h <= S_::NSUB; ++h) {
+#pragma unroll 1
+                                for (int c = 0; c < nch; ++c) {
+                                    uint32_t r[16];
+                                    tmem_ld16(orow + h * NQ + c * 16, r);
+                                    tmem_ld_wait();
+#pragma unroll
+                                    for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * my_f[c * 16 + j]);
+                                    tmem_st16(orow + h * NQ + c * 16, r);
+                                }
+                            }
+                            tmem_st_wait();
+                        }
+                    }
+                    if (!waited) {
+                        ok = warp_wait(pfree + 8 * pb, pr.ph ^ 1u, abort_flag, wns);
+                        if (!ok) break;
+                        waited = true;
+                    }
+                    // ---- P^T rows of this thread's keys: P = 2^y, y = s * slk (* 1/sigma) - m, the
+                    // product and the subtraction fused; ymax: whether some y exceeds RESCALE_TAU ----
+                    float ymax = -INFINITY;
+#pragma unroll 1
+                    for (int c = 0; c < nch; ++c) {
+                        uint32_t r0[16], r1[16];
+                        load2(c, r0, r1);
+                        float m[16], qs[16];
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4) {
+                            const float4 a = *reinterpret_cast<const float4 *>(my_m + c * 16 + j);
+                            m[j] = a.x; m[j + 1] = a.y; m[j + 2] = a.z; m[j + 3] = a.w;
+                            if (FP8) {
+                                const float4 b4 = *reinterpret_cast<const float4 *>(qinv + c * 16 + j);
+                                qs[j] = b4.x; qs[j + 1] = b4.y; qs[j + 2] = b4.z; qs[j + 3] = b4.w;
+                            }
+                        }
+#pragma unroll 1
+                        for (int i = 0; i < nt; ++i) {
+                            const float slk = i ? slk1 : slk0;
+                            float y[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const float sj = __uint_as_float(i ? r1[j] : r0[j]);
+                                y[j] = FP8 ? fmaf(sj * slk, qs[j], -m[j]) : fmaf(sj, slk, -m[j]);
+                            }
+                            if (!(i ? vis1 : vis0)) {
+                                const int koff = i ? koff1 : koff0;
+#pragma unroll
+                                for (int j = 0; j < 16; j += 4) {
+                                    const int4 a = *reinterpret_cast<const int4 *>(my_lim + c * 16 + j);
+                                    y[j] = koff <= a.x ? y[j] : -INFINITY;
+                                    y[j + 1] = koff <= a.y ? y[j + 1] : -INFINITY;
+                                    y[j + 2] = koff <= a.z ? y[j + 2] : -INFINITY;
+                                    y[j + 3] = koff <= a.w ? y[j + 3] : -INFINITY;
+                                }
+                            }
+                            uint32_t pk[8];
+#pragma unroll
+                            for (int j = 0; j < 16; j += 2) {
+                                ymax = fmaxf(ymax, fmaxf(y[j], y[j + 1]));
+                                pk[j >> 1] = pack2(ex2_approx(y[j]), ex2_approx(y[j + 1]), false);
+                            }
+                            uint8_t *blk = prow + i * PTILE + c * (TILE_KEYS * 32);
+                            *reinterpret_cast<uint4 *>(blk + (sw << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                            *reinterpret_cast<uint4 *>(blk + ((sw ^ 1) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                        }
+                    }
+                    if (attempt == 0 && !full) {
+                        // the one-pass try: keep it unless some warp saw a score above its maximum
+                        full = exchange(__any_sync(0xFFFFFFFFu, ymax > RESCALE_TAU));
+                        if (!ok) break;
+                        if (full) continue;
+                    }
+                    break;
+                }
+                if (!ok) break;
+                tc_fence_before();
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(sfree + 8 * sb);
+                    mbar_arrive(pfull + 8 * pb);
+                }
+                // the previous unit's epilogue, once this unit's first P is on its way
+                if (pend_u >= 0) {
+                    ok = epilogue();
+                    if (!ok) break;
+                }
+            }
+            if (!ok) break;
+            // the unit table is no longer read
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ufree + 8 * ub);
+            pend_u = u;
+            pend_failed = failed;
+            pend_ob = ob;
+            pend_mb = mb;
+            pend_pr = pr_last;
             ++ua;
+            orr.next(p.OB);
         }
+        if (ok && pend_u >= 0) ok = epilogue();
         if (!ok) {
             *abort_flag = 1;
             if (qd == 0 && lane == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
+    } else if (warp == 11) {
+        // ================= FP8: TMA issuers, warp 11: lane 0 K sub-tiles, lane 1 raw V sub-tiles =================
+        // (bf16 pools: this warp has no role). The two lanes run independent loops (their waits
+        // are per thread, with no warp-wide step), so that the K stream runs ahead of the V
+        // stream by the K ring's depth. One box per page-run of rows (min(page size, 128)
+        // rows): K boxes land 128- or 64-byte-swizzled, ready for the S MMA; V boxes land
+        // unswizzled in a raw stage. Runs past the branch's last position, or of an invalid
+        // page, are not loaded.
+        if (FP8 && lane < 2) {
+            const bool is_v = lane == 1;
+            const int depth = is_v ? p.NR : p.NK;
+            const uint32_t full0 = is_v ? rfull : kfull, empty0 = is_v ? rempty : kempty;
+            const uint32_t ring = is_v ? s_raw : s_k;
+            const CUtensorMap *map = is_v ? &map_v : &map_k;
+            uint32_t gi = 0, ua = 0;
+            RingPos rr;
+            bool ok = true;
+            const int BR = p.tma_rows, nruns = TILE_KEYS / BR;
+            for (;;) {
+                const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
+                const UnitTable *tab = tables + ub;
+                if (!mbar_wait_poll(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
+                const int it_u = tab->iter;
+                if (it_u < 0) break;
+                const UnitInfo ui = tab->ui;
+                ++ua;
+                for (int t = 0; t < ui.T && ok; ++t) {
+                    const int key0 = ui.s0 + t * TILE_KEYS;
+                    // the producer may prepare the next unit (see the bf16 loaders)
+                    if (!is_v && t == max(0, ui.T - 3)) mbar_arrive(lfin + 8 * ub);
+                    for (int h = 0; h < S_::NSUB; ++h, ++gi) {
+                        const uint32_t s = rr.s;
+                        if (!mbar_wait_poll(empty0 + 8 * s, rr.ph ^ 1u, abort_flag, wns)) {
+                            ok = false;
+                            break;
+                        }
+                        rr.next(depth);
+                        const uint32_t dst_base = ring + s * S_::F8_STAGE;
+                        uint32_t bytes = 0;
+                        for (int r = 0; r < nruns; ++r) {
+                            const int kr = key0 + r * BR;
+                            if (kr >= ui.kv_end) break;
+                            if (tab->page[(kr - ui.s0) >> log2P] >= 0) bytes += (uint32_t)(BR * S_::SUB);
+                        }
+                        mbar_arrive_expect_tx(full0 + 8 * s, bytes);
+                        for (int r = 0; r < nruns; ++r) {
+                            const int kr = key0 + r * BR;
+                            if (kr >= ui.kv_end) break;
+                            const int pg = tab->page[(kr - ui.s0) >> log2P];
+                            if (pg < 0) continue;
+                            const int row = (pg * p.kv.n_kv_heads + ui.g) * p.kv.page_size + (kr & (p.kv.page_size - 1));
+                            tma_load_2d(dst_base + (uint32_t)(r * BR) * S_::SUB, map, h * S_::SUB, row, full0 + 8 * s);
+                        }
+                    }
+                }
+                if (!ok) break;
+                mbar_arrive(ufree + 8 * ub);
+            }
+            // every box lands, and every consumer's release of a stage is delivered, before the
+            // CTA may exit
+            drain_ring(full0, rr, depth, gi);
+            drain_ring(empty0, rr, depth, gi);
+            if (!ok) {
+                *abort_flag = 1;
+                raise_error(p.err, SPEC_DEVERR_TIMEOUT);
+            }
+        }
+        __syncwarp();
     } else if (!FP8) {
         // ================= loaders (bf16): warps 4-5 K, warps 6-7 V, by cp.async =================
         // Each stream has its own ring, so that V stages held until their P.V never hold up
@@ -947,6 +1103,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         const uint32_t full0 = is_v ? vfull : kfull, empty0 = is_v ? vempty : kempty;
         const uint32_t ring = is_v ? s_v : s_k;
         uint32_t gi = 0, ua = 0;  // sub-tiles issued, units
+        RingPos rr;
         bool ok = true;
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
@@ -958,24 +1115,26 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             ++ua;
             for (int t = 0; t < ui.T && ok; ++t) {
                 const int key0 = ui.s0 + t * TILE_KEYS;
-                // two tiles before the unit's end the producer may prepare the next unit, so that
-                // its table and Q are there when this unit's last copies have been issued
-                if (t == max(0, ui.T - 2)) {
+                // three tiles before the unit's end the K loaders let the producer prepare the next
+                // unit, so that its table and Q are there when this unit's last copies have been
+                // issued (the K stream runs ahead of the V stream)
+                if (!is_v && t == max(0, ui.T - 3)) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(lfin + 8 * ub);
                 }
                 for (int h = 0; h < S_::NSUB; ++h, ++gi) {
-                    const uint32_t s = gi % (uint32_t)depth;
-                    if (!warp_wait<SLEEP_LOAD>(empty0 + 8 * s, ((gi / (uint32_t)depth) & 1u) ^ 1u, abort_flag, wns)) {
+                    const uint32_t s = rr.s;
+                    if (!warp_wait<SLEEP_LOAD>(empty0 + 8 * s, rr.ph ^ 1u, abort_flag, wns)) {
                         ok = false;
                         break;
                     }
+                    rr.next(depth);
                     const uint32_t dst_base = ring + s * S_::OP_STAGE;
                     const uint8_t *src_col = pool + (size_t)h * S_::SUB * 2 + pch * 16;
                     // pages of >= 8 positions: per group of 8 pieces the table lookups first
                     // (independent loads), then the copies; smaller pages: per-row page-table reads
                     if (!small_pages) {
-#pragma unroll
+#pragma unroll 1
                         for (int k0 = 0; k0 < NPIECE; k0 += 8) {
                             int pg[8];
 #pragma unroll
@@ -1016,108 +1175,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         // every copy lands before the CTA may exit, and so do the last MMA commits on the
         // ring's "empty" barriers
         cp_async_wait_all();
-        if (ltid == 0) {
-            const uint32_t n_last = gi < (uint32_t)depth ? gi : (uint32_t)depth;
-            for (uint32_t j = 0; j < n_last; ++j) {
-                const uint32_t i2 = gi - 1 - j;
-                mbar_wait(empty0 + 8 * (i2 % (uint32_t)depth), (i2 / (uint32_t)depth) & 1u, nullptr, ATT_WAIT_NS);
-            }
-        }
+        if (ltid == 0) drain_ring(empty0, rr, depth, gi);
         __syncwarp();
         if (!ok) {
             *abort_flag = 1;
             if (ltid == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
-    } else if (warp <= 5) {
-        // ================= FP8: TMA issuers, warp 4 K sub-tiles, warp 5 raw V sub-tiles =================
-        // One box per page-run of rows (min(page size, 128) rows): K boxes land 128- or
-        // 64-byte-swizzled, ready for the S MMA; V boxes land unswizzled in a raw stage. Runs
-        // past the branch's last position, or of an invalid page, are not loaded.
-        const bool is_v = warp == 5;
-        const int depth = is_v ? p.NR : p.NK;
-        const uint32_t full0 = is_v ? rfull : kfull, empty0 = is_v ? rempty : kempty;
-        const uint32_t ring = is_v ? s_raw : s_k;
-        const CUtensorMap *map = is_v ? &map_v : &map_k;
-        uint32_t gi = 0, ua = 0;
-        bool ok = true;
-        const int BR = p.tma_rows, nruns = TILE_KEYS / BR;
-        for (;;) {
-            const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
-            const UnitTable *tab = tables + ub;
-            if (!warp_wait<SLEEP_LOAD>(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
-            const int it_u = tab->iter;
-            if (it_u < 0) break;
-            const UnitInfo ui = tab->ui;
-            ++ua;
-            for (int t = 0; t < ui.T && ok; ++t) {
-                const int key0 = ui.s0 + t * TILE_KEYS;
-                if (t == max(0, ui.T - 2)) {  // the producer may prepare the next unit (see the bf16 loaders)
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(lfin + 8 * ub);
-                }
-                for (int h = 0; h < S_::NSUB; ++h, ++gi) {
-                    const uint32_t s = gi % (uint32_t)depth;
-                    if (!warp_wait<SLEEP_LOAD>(empty0 + 8 * s, ((gi / (uint32_t)depth) & 1u) ^ 1u, abort_flag, wns)) {
-                        ok = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        const uint32_t dst_base = ring + s * S_::F8_STAGE;
-                        uint32_t bytes = 0;
-                        for (int r = 0; r < nruns; ++r) {
-                            const int kr = key0 + r * BR;
-                            if (kr >= ui.kv_end) break;
-                            if (tab->page[(kr - ui.s0) >> log2P] >= 0) bytes += (uint32_t)(BR * S_::SUB);
-                        }
-                        mbar_arrive_expect_tx(full0 + 8 * s, bytes);
-                        for (int r = 0; r < nruns; ++r) {
-                            const int kr = key0 + r * BR;
-                            if (kr >= ui.kv_end) break;
-                            const int pg = tab->page[(kr - ui.s0) >> log2P];
-                            if (pg < 0) continue;
-                            const int row = (pg * p.kv.n_kv_heads + ui.g) * p.kv.page_size + (kr & (p.kv.page_size - 1));
-                            tma_load_2d(dst_base + (uint32_t)(r * BR) * S_::SUB, map, h * S_::SUB, row, full0 + 8 * s);
-                        }
-                    }
-                    __syncwarp();
-                }
-            }
-            __syncwarp();
-            if (ok && lane == 0) mbar_arrive(ufree + 8 * ub);
-            if (!ok) break;
-        }
-        // every box lands, and every consumer's release of a stage is delivered, before the
-        // CTA may exit
-        if (lane == 0) {
-            const uint32_t n_last = gi < (uint32_t)depth ? gi : (uint32_t)depth;
-            for (uint32_t j = 0; j < n_last; ++j) {
-                const uint32_t i2 = gi - 1 - j;
-                mbar_wait(full0 + 8 * (i2 % (uint32_t)depth), (i2 / (uint32_t)depth) & 1u, nullptr, ATT_WAIT_NS);
-                mbar_wait(empty0 + 8 * (i2 % (uint32_t)depth), (i2 / (uint32_t)depth) & 1u, nullptr, ATT_WAIT_NS);
-            }
-        }
-        __syncwarp();
-        if (!ok) {
-            *abort_flag = 1;
-            if (lane == 0) raise_error(p.err, SPEC_DEVERR_TIMEOUT);
-        }
     } else {
-        // ================= FP8 converters, warps 6-7 =================
+        // ================= FP8 converters, warps 4-7 (one per SM sub-partition) =================
         // Every raw V sub-tile, in ring order, becomes bf16(code * page scale) in the MMA's
         // layout (the V ring), with the rows past the branch's last position written as
-        // zeros. The two warps join on an mbarrier (bounded waits) before one thread
-        // publishes their work.
-        const int ctid = (warp - 6) * 32 + lane;  // 0..63
-        uint32_t gv = 0, ua = 0, nc = 0;
+        // zeros. Each warp fences its own share and arrives on the stage's barriers (count 4).
+        // Their waits do not sleep: the converted V is on the P.V MMAs' critical path.
+        const int ctid = (warp - 4) * 32 + lane;  // 0..127
+        uint32_t ua = 0;
+        RingPos rawr, vr;  // raw V ring, bf16 V ring
         bool ok = true;
-        auto join = [&]() {  // both converter warps have written and fenced their share
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(cjoin);
-            const bool r = warp_wait<SLEEP_LOAD>(cjoin, nc & 1u, abort_flag, wns);
-            ++nc;
-            return r;
-        };
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
             const UnitTable *tab = tables + ub;
@@ -1129,41 +1202,54 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             for (int t = 0; t < ui.T && ok; ++t) {
                 const int nvk = ui.kv_end - (ui.s0 + t * TILE_KEYS);  // valid keys of the tile (>= 1)
 #pragma unroll 1
-                for (int h = 0; h < S_::NSUB; ++h, ++gv) {
-                    const uint32_t rs = gv % (uint32_t)p.NR, os = gv % (uint32_t)p.NV;
-                    if (!warp_wait<SLEEP_LOAD>(rfull + 8 * rs, (gv / (uint32_t)p.NR) & 1u, abort_flag, wns) ||
-                        !warp_wait<SLEEP_LOAD>(vempty + 8 * os, ((gv / (uint32_t)p.NV) & 1u) ^ 1u, abort_flag, wns)) {
+                for (int h = 0; h < S_::NSUB; ++h, rawr.next(p.NR), vr.next(p.NV)) {
+                    const uint32_t rs = rawr.s, os = vr.s;
+                    if (!warp_wait(rfull + 8 * rs, rawr.ph, abort_flag, wns) ||
+                        !warp_wait(vempty + 8 * os, vr.ph ^ 1u, abort_flag, wns)) {
                         ok = false;
                         break;
                     }
                     const uint8_t *raw = smem + p.off_raw + rs * S_::F8_STAGE;
                     uint8_t *op = smem + p.off_v + os * S_::OP_STAGE;
-                    constexpr int CCH = S_::SUB / 16;  // 16-byte raw pieces per row
-                    for (int piece = ctid; piece < TILE_KEYS * CCH; piece += 64) {
-                        const int row = piece / CCH, pc = piece % CCH;
-                        uint32_t hv[8];
-                        if (row < nvk) {
-                            const float vs = tab->vsc[(t * TILE_KEYS + row) >> log2P];
-                            const uint4 v = *reinterpret_cast<const uint4 *>(raw + row * S_::SUB + pc * 16);
-                            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                    // thread ctid converts the 16-byte piece pc of rows row0, row0 + RSTEP, ...: all
+                    // its loads first, then the conversions (a warp reads 4 whole rows per load)
+                    constexpr int CCH = S_::SUB / 16;        // 16-byte raw pieces per row
+                    constexpr int RSTEP = 128 / CCH;         // rows between a thread's pieces
+                    constexpr int NIT = TILE_KEYS / RSTEP;   // pieces per thread
+                    constexpr int BATCH = NIT < 4 ? NIT : 4; // pieces loaded together
+                    const int pc = ctid % CCH, row0 = ctid / CCH;
+#pragma unroll 1
+                    for (int i0 = 0; i0 < NIT; i0 += BATCH) {
+                        uint4 v[BATCH];
+                        float vs[BATCH];
+#pragma unroll
+                        for (int i = 0; i < BATCH; ++i) {
+                            const int row = row0 + (i0 + i) * RSTEP;
+                            v[i] = *reinterpret_cast<const uint4 *>(raw + row * S_::SUB + pc * 16);
+                            vs[i] = tab->vsc[(t * TILE_KEYS + (row < nvk ? row : 0)) >> log2P];
+                        }
+#pragma unroll
+                        for (int i = 0; i < BATCH; ++i) {
+                            const int row = row0 + (i0 + i) * RSTEP;
+                            const bool live = row < nvk;  // rows past the last position: zeros, never code * 0
+                            const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                            uint32_t hv[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const __half2_raw c2 = __nv_cvt_fp8x2_to_halfraw2(
                                     (__nv_fp8x2_storage_t)((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu), __NV_E4M3);
                                 const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&c2));
-                                hv[e] = pack2(f.x * vs, f.y * vs, false);
+                                hv[e] = live ? pack2(f.x * vs[i], f.y * vs[i], false) : 0u;
                             }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) hv[e] = 0u;
+                            *reinterpret_cast<uint4 *>(op + sw128_off(row, pc * 16, TILE_KEYS * 128)) =
+                                make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                            *reinterpret_cast<uint4 *>(op + sw128_off(row, pc * 16 + 8, TILE_KEYS * 128)) =
+                                make_uint4(hv[4], hv[5], hv[6], hv[7]);
                         }
-                        *reinterpret_cast<uint4 *>(op + sw128_off(row, pc * 16, TILE_KEYS * 128)) =
-                            make_uint4(hv[0], hv[1], hv[2], hv[3]);
-                        *reinterpret_cast<uint4 *>(op + sw128_off(row, pc * 16 + 8, TILE_KEYS * 128)) =
-                            make_uint4(hv[4], hv[5], hv[6], hv[7]);
                     }
-                    if (!join()) { ok = false; break; }
-                    if (ctid == 0) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
                         mbar_arrive(vfull + 8 * os);
                         mbar_arrive(rempty + 8 * rs);
                     }
@@ -1410,7 +1496,7 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
     using S_ = AttnShape<D, FP8>;
     const int NQ = p.NQ;
     const uint32_t ut_bytes = 2 * (uint32_t)sizeof(UnitTable);
-    const uint32_t sx_bytes = (uint32_t)(8 + 4 + 4 + 4 + 2 + 2) * NQ * 4 + 32;
+    const uint32_t sx_bytes = (uint32_t)(8 + 8 + 4 + 4 + 2 + 2) * NQ * 4 + 32;
     const uint32_t bars = BAR_BYTES, small = 64;
     // Tile groups of 2 when the ring holds a whole group's K and V (the S of a group's last
     // tile must be able to load while the V of its first tile waits for the softmax), else 1.
@@ -1441,7 +1527,7 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
                     const uint32_t q8_bytes = FP8 ? QB * 2 * S_::NQ8 * NQ * S_::Q8ROW : 0;
                     const uint32_t p_bytes = NPB * TPI * NQ * 256;
                     const uint32_t fixed = align_up(q_bytes + q8_bytes + p_bytes, 1024) + 1024;  // + ones
-                    const uint32_t tail = ut_bytes + sx_bytes + bars + small;
+                    const uint32_t tail = ut_bytes + sx_bytes + bars + small + 32;  // + alignment slack
                     if (1024 + fixed + tail > ATT_SMEM_LIMIT) continue;
                     const uint32_t avail = ATT_SMEM_LIMIT - 1024 - fixed - tail;
                     // K ring: at least a group's K sub-tiles (the rich plan: two tiles more); bf16
@@ -1481,7 +1567,7 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
                     p.off_v = p.off_k + NK * S_::K_STAGE;
                     p.off_raw = p.off_v + NV * S_::OP_STAGE;
                     p.off_ut = p.off_raw + NR * S_::F8_STAGE;
-                    p.off_sx = p.off_ut + ut_bytes;
+                    p.off_sx = align_up(p.off_ut + ut_bytes, 16);
                     p.off_bar = align_up(p.off_sx + sx_bytes, 8);
                     p.off_small = p.off_bar + bars;
                     p.t_o = (uint32_t)(NSB * TPI * NQ);
