@@ -148,6 +148,9 @@ def _setup_workload(cid: int, dev: str):
                W_fc=(0.02 * torch.randn((c.H, 2 * c.H), generator=g, device=dev)).to(torch.bfloat16))
     step = VerifyStep(kv, c.B, c.k, c.Hq, vi.W, vi.max_pos, mtp=mtp, device=dev)
     inputs = dict(pos=vi.pos.to(dev), q=vi.q, k_new=vi.k_new, v_new=vi.v_new, hidden=vi.hidden, drafts=vi.drafts.to(dev))
+    # the verify rows' K/V in their slots, so that a call timed alone (--only) reads the same pool a step does
+    from greedy_speculative_decode_spec_gb300 import _binding as bnd
+    bnd.spec_kv_append(kv.desc, inputs["pos"], c.B, c.k, vi.k_new, vi.v_new)
     kv_bytes = algorithmic_kv_bytes(c, vi.pos.tolist())
     w_bytes = c.V * c.H * 2
     return dict(cfg=c, vi=vi, kv=kv, step=step, inputs=inputs, draft=draft, kv_bytes=kv_bytes, w_bytes=w_bytes)

@@ -20,6 +20,7 @@ SPEC_OK = 0
 STATUS = {-1: "SPEC_ERR_NULL", -2: "SPEC_ERR_ARG", -3: "SPEC_ERR_UNSUPPORTED", -4: "SPEC_ERR_WORKSPACE",
           -5: "SPEC_ERR_CUDA", -6: "SPEC_ERR_ALIGN"}
 DEVERR_PAGE, DEVERR_COVER, DEVERR_TOKEN, DEVERR_D2T, DEVERR_POS, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1, 2, 4, 8, 16, 32, 64
+DEVERR_TREE = 128
 KMAX = 15
 KV_BF16, KV_FP8_E4M3 = 0, 1
 
@@ -35,7 +36,8 @@ EXPORTS = ("spec_strerror", "spec_version", "spec_kv_append", "spec_kv_write_row
            "spec_verify_attn_workspace", "spec_verify_attn", "spec_lmhead_workspace",
            "spec_lmhead_argmax", "spec_lmhead_logits", "spec_accept", "spec_mtp_input_workspace",
            "spec_mtp_input", "spec_lmhead_argmax_static", "spec_accept_stop", "spec_verify_attn_plan",
-           "spec_test_set_wait_limit")
+           "spec_test_set_wait_limit", "spec_accept_sample", "spec_verify_attn_tree", "spec_accept_tree",
+           "spec_kv_compact")
 
 
 class SpecError(RuntimeError):
@@ -82,6 +84,11 @@ def lib() -> ctypes.CDLL:
         L.spec_verify_attn_plan.argtypes = [ctypes.POINTER(spec_kv_desc), _i32, _i32, _i32, _i32, _vp, _i32]
         L.spec_accept_stop.argtypes = [_vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _vp, _i32, _vp, _vp]
+        L.spec_accept_sample.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _vp, _vp, _vp,
+                                         _vp, _vp, _vp]
+        L.spec_verify_attn_tree.argtypes = [_KVP, _vp, _i32, _i32, _i32, _vp, _f32, _vp, _vp, _vp, _sz, _i32, _vp, _vp]
+        L.spec_accept_tree.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.spec_kv_compact.argtypes = [_KVP, _vp, _vp, _vp, _i32, _i32, _vp, _vp]
         L.spec_test_set_wait_limit.argtypes = [ctypes.c_uint64]
         L.spec_test_set_wait_limit.restype = None
         L.spec_mtp_input_workspace.restype = _sz
@@ -262,6 +269,45 @@ def spec_accept_stop(drafts, ids, pos, B: int, k: int, stop_ids, budget, out_tok
         _ptr(out_pos, "out_pos", torch.int32), _ptr(out_next, "out_next", torch.int32),
         _ptr(out_done, "out_done", torch.int32), _ptr(hidden, "hidden", torch.bfloat16), H,
         _ptr(h_out, "h_out", torch.bfloat16), _stream(stream)))
+
+
+def spec_accept_sample(drafts, logits, q, pos, B: int, k: int, temperature: float, u_acc, u_res, out_tokens, out_n,
+                       out_accepted, out_pos, out_next, dev_err=None, stream=None):
+    """Speculative sampling acceptance; logits fp32 [B*(k+1)][V], q fp32 [B][k][V]."""
+    V = int(logits.shape[-1])
+    _check("spec_accept_sample", lib().spec_accept_sample(
+        _ptr(drafts, "drafts", torch.int32) if k > 0 else None, _ptr(logits, "logits", torch.float32),
+        _ptr(q, "q", torch.float32) if k > 0 else None, _ptr(pos, "pos", torch.int32), B, k, V, float(temperature),
+        _ptr(u_acc, "u_acc", torch.float32) if k > 0 else None, _ptr(u_res, "u_res", torch.float32),
+        _ptr(out_tokens, "out_tokens", torch.int32), _ptr(out_n, "out_n", torch.int32),
+        _ptr(out_accepted, "out_accepted", torch.int32), _ptr(out_pos, "out_pos", torch.int32),
+        _ptr(out_next, "out_next", torch.int32), _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
+
+
+def spec_verify_attn_tree(kv: spec_kv_desc, pos, B: int, k: int, n_q_heads: int, q, scale: float, anc_mask, out, ws,
+                          max_pos: int, dev_err=None, stream=None):
+    """Tree verify attention: row j reads the committed prefix and the verify slots of its mask."""
+    _check("spec_verify_attn_tree", lib().spec_verify_attn_tree(
+        ctypes.byref(kv), _ptr(pos, "pos", torch.int32), B, k, n_q_heads, _ptr(q, "q", torch.bfloat16), float(scale),
+        _ptr(anc_mask, "anc_mask", torch.int32), _ptr(out, "out", torch.bfloat16), _ptr(ws, "ws"),
+        ws.numel() * ws.element_size(), max_pos, _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
+
+
+def spec_accept_tree(drafts, ids, pos, parent, B: int, k: int, out_tokens, out_n, out_accepted, out_pos, out_next,
+                     out_path, dev_err=None, stream=None):
+    _check("spec_accept_tree", lib().spec_accept_tree(
+        _ptr(drafts, "drafts", torch.int32) if k > 0 else None, _ptr(ids, "ids", torch.int32),
+        _ptr(pos, "pos", torch.int32), _ptr(parent, "parent", torch.int32), B, k,
+        _ptr(out_tokens, "out_tokens", torch.int32), _ptr(out_n, "out_n", torch.int32),
+        _ptr(out_accepted, "out_accepted", torch.int32), _ptr(out_pos, "out_pos", torch.int32),
+        _ptr(out_next, "out_next", torch.int32), _ptr(out_path, "out_path", torch.int32),
+        _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
+
+
+def spec_kv_compact(kv: spec_kv_desc, pos, path, accepted, B: int, k: int, dev_err=None, stream=None):
+    _check("spec_kv_compact", lib().spec_kv_compact(
+        ctypes.byref(kv), _ptr(pos, "pos", torch.int32), _ptr(path, "path", torch.int32),
+        _ptr(accepted, "accepted", torch.int32), B, k, _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
 
 
 def spec_test_set_wait_limit(ns: int) -> None:

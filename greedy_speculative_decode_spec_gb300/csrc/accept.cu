@@ -11,6 +11,14 @@
 // Lane i < k compares draft i with the target of row i; the first mismatching lane
 // (a ballot) is the accepted count a. Lanes 0..k write the emitted tokens.
 //
+// Device-resident step state: out_pos may be the pos array itself (the branch's position
+// is read once, by the lane that writes it), so a loop captured in a CUDA graph advances its
+// positions on the device, and out_next / h_out give the next step's first fed token and
+// its draft-head hidden row without a host round trip (span-02 spec.rs, module
+// documentation: the state stays on the device between steps; flashrt-structures
+// decode_loop/whole_step.py, `generate_speculative`: pos advances by accepted + 1 on the
+// device).
+//
 // With a stop set and a budget (spec_accept_stop): the run drafts[0..a) ++ [ids[a]] is
 // cut right after its first token in the stop set and then to at most the branch's budget
 // (DSSD-dev dssd/fast.py, `_commit`: the committed tokens are appended until the stop rule
@@ -26,7 +34,7 @@ namespace spec {
 
 __global__ void __launch_bounds__(128) accept_kernel(const int32_t *__restrict__ drafts,
                                                      const int32_t *__restrict__ ids,
-                                                     const int32_t *__restrict__ pos, int B, int k,
+                                                     const int32_t *pos, int B, int k,
                                                      int32_t *out_tokens, int32_t *out_n,
                                                      int32_t *out_accepted, int32_t *out_pos,
                                                      int32_t *out_next, const uint16_t *hidden, int H,
@@ -71,7 +79,7 @@ __global__ void __launch_bounds__(128) accept_kernel(const int32_t *__restrict__
     if (lane == 0) {
         out_n[b] = n;
         out_accepted[b] = a < n ? a : n;
-        out_pos[b] = __ldg(pos + b) + n;
+        out_pos[b] = pos[b] + n;  // pos may be out_pos: the position advances in place
         out_next[b] = n > 0 ? last : -1;
         if (out_done) out_done[b] = (stopped || (budget && n == cap)) ? 1 : 0;
     }

@@ -48,6 +48,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same probe with a bound on how long the thread may be suspended waiting for the
+// phase (the suspend-time hint, in ns), so that a short wait limit and an abort are seen.
+__device__ __forceinline__ bool mbar_try_wait_for(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+// the suspend bound of the bounded waits: the wait limit, at most 20 us
+__device__ __forceinline__ uint32_t wait_hint(uint64_t timeout_ns) {
+    return timeout_ns < 20000u ? (uint32_t)timeout_ns : 20000u;
+}
+
 // Non-blocking probe of a phase (mbarrier.test_wait): true if it has completed.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -64,15 +80,29 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 // between probes (for threads that are not latency-critical).
 static __device__ __noinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity, volatile int *abort,
                                             uint64_t timeout_ns, uint32_t sleep_ns) {
-    uint64_t t0 = 0;
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+    // every probe (a try_wait may itself suspend the thread for a while) is followed by the
+    // abort and time checks, so that a short limit is honoured
+    const uint64_t t0 = globaltimer();
+    const uint32_t hint = wait_hint(timeout_ns);
+    for (;;) {
+        if (mbar_try_wait_for(bar, parity, hint)) return true;
         if (sleep_ns) __nanosleep(sleep_ns);
-        if ((i & 15u) == 0) {
+        if (abort != nullptr && *abort) return false;
+        if (globaltimer() - t0 > timeout_ns) return false;
+    }
+}
+
+// The same wait by non-blocking probes (mbarrier.test_wait), for threads that share a warp
+// with another thread on its own loop: a probe never holds the warp, so the other thread's
+// path keeps being issued while this one waits.
+static __device__ __noinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, volatile int *abort,
+                                            uint64_t timeout_ns) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(bar, parity)) return true;
+        if ((i & 7u) == 0) {
             if (abort != nullptr && *abort) return false;
-            const uint64_t t = globaltimer();
-            if (t0 == 0) t0 = t;
-            else if (t - t0 > timeout_ns) return false;
+            if (globaltimer() - t0 > timeout_ns) return false;
         }
     }
 }
@@ -82,31 +112,19 @@ static __device__ __noinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity
 // timeout_ns of wall time, so no wait can hang.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           uint64_t timeout_ns) {
-    return mbar_try_wait(bar, parity) || mbar_wait_loop(bar, parity, abort, timeout_ns, 0);
-}
-
-// The same wait by non-blocking probes (mbarrier.test_wait), for threads that share a warp
-// with another thread on its own loop: a probe never holds the warp, so the other thread's
-// path keeps being issued while this one waits.
-static __device__ __noinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, volatile int *abort,
-                                            uint64_t timeout_ns) {
-    uint64_t t0 = 0;
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_test(bar, parity)) return true;
-        if ((i & 63u) == 0) {
-            if (abort != nullptr && *abort) return false;
-            const uint64_t t = globaltimer();
-            if (t0 == 0) t0 = t;
-            else if (t - t0 > timeout_ns) return false;
-        }
-    }
+    // a limit below 1 us (a test setting) is watched with non-blocking probes: a suspended
+    // probe could outlast it
+    if (timeout_ns < 1000u) return mbar_test(bar, parity) || mbar_wait_poll(bar, parity, abort, timeout_ns);
+    return mbar_try_wait_for(bar, parity, wait_hint(timeout_ns)) || mbar_wait_loop(bar, parity, abort, timeout_ns, 0);
 }
 
 // The same wait for a thread that is not latency-critical: between probes it sleeps about
 // sleep_ns, leaving the SM sub-partition's issue slots to the warps that do the math.
 __device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int *abort,
                                                 uint64_t timeout_ns, uint32_t sleep_ns) {
-    return mbar_try_wait(bar, parity) || mbar_wait_loop(bar, parity, abort, timeout_ns, sleep_ns);
+    if (timeout_ns < 1000u) return mbar_test(bar, parity) || mbar_wait_poll(bar, parity, abort, timeout_ns);
+    return mbar_try_wait_for(bar, parity, wait_hint(timeout_ns)) ||
+           mbar_wait_loop(bar, parity, abort, timeout_ns, sleep_ns);
 }
 
 // ---- programmatic dependent launch ----------------------------------------------------------

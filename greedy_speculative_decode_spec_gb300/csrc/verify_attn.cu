@@ -125,6 +125,7 @@ struct AttnShape {
 struct AttnParams {
     KvView kv;
     const int32_t *pos;
+    const int32_t *anc;    // tree verify: [B*(k+1)] ancestor masks over the verify slots; null: a chain
     int B, k, Hq, G, n_q, NQ, n_splits, max_pos, n_units, split_keys;
     int TPI;               // tiles per softmax iteration (a tile group)
     // FP8 pools: rows per TMA box of the K / V gather (one page-run: min(page size, 128))
@@ -299,8 +300,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     float *sx_red = reinterpret_cast<float *>(smem + p.off_sx);
     float *sx_m = sx_red + 8 * NQ;
     float *sx_f = sx_m + 8 * NQ;
-    int *sx_lim = reinterpret_cast<int *>(sx_f + 4 * NQ);
-    float *sx_qinv = reinterpret_cast<float *>(sx_lim + 4 * NQ);
+    int *sx_msk = reinterpret_cast<int *>(sx_f + 4 * NQ);
+    float *sx_qinv = reinterpret_cast<float *>(sx_msk + 4 * NQ);
     int *sx_need = reinterpret_cast<int *>(sx_qinv + 2 * NQ);  // [2 exchange slots][4 warps]
     // per query column q = j*G + i: its draft row j (-1 for padding) and its output offset
     // (j*Hq + i)*D from the (branch, kv head)'s first output
@@ -518,8 +519,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     } else if (warp == 9) {
         // ================= MMA issuer: S^T = K . Q^T =================
         const uint32_t idesc = FP8 ? idesc_f8_e4m3(128, NQ) : idesc_f16kind(128, NQ, false, false, false);
-        uint32_t gs = 0, ua = 0;  // tile groups, active units
-        RingPos kr, sr, qr;       // K ring, S buffers, Q buffers
+        uint32_t gs = 0, ua = 0, gk = 0;  // tile groups, active units, K sub-tiles consumed
+        RingPos kr, sr, qr;               // K ring, S buffers, Q buffers
         bool ok = true;
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
@@ -551,6 +552,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                     const uint32_t st = kr.s;
                     if (!warp_wait<SLEEP_MMA>(kfull + 8 * st, kr.ph, abort_flag, wns)) { ok = false; break; }
                     kr.next(p.NK);
+                    ++gk;
                     if (!FP8) fence_proxy_async_smem();  // cp.async data -> tensor core reads
                     tc_fence_after();
                     if (lane == 0) {
@@ -605,8 +607,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             mma_commit(drain);
             mbar_wait(drain, 0, nullptr, ATT_WAIT_NS);
             // every arrive sent by this issuer's commits is delivered before the CTA may exit:
-            // the last phase of the S buffers' "full" barriers and of the Q buffers' "free"
-            // (the ring's "empty" phases are drained by the loaders' waits below)
+            // the last phases of the K ring's "empty" barriers, of the S buffers' "full" and of
+            // the Q buffers' "free" (only commits that were issued are waited for, so a CTA that
+            // gave up on a wait also leaves at once)
+            drain_ring(kempty, kr, p.NK, gk);
             drain_ring(sfull, sr, p.NSB, gs);
             drain_ring(qfree, qr, p.QB, ua);
         }
@@ -692,7 +696,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             mbar_wait(drain + 8, 0, nullptr, ATT_WAIT_NS);
             // the last phases of the P buffers' "free" barriers and of the P.V completion
             drain_ring(pfree, pr, p.NPB, gp);
-            if (FP8) drain_ring(vempty, vr, p.NV, gv);  // (bf16: the V loaders drain the V ring's "empty" phases)
+            drain_ring(vempty, vr, p.NV, gv);
         }
         __syncwarp();
     } else if (warp < 4) {
@@ -701,7 +705,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
         const int kl = qd * 32 + lane;           // this thread's key within a tile
         float *my_f = sx_f + qd * NQ;
-        int *my_lim = sx_lim + qd * NQ;
+        int *my_msk = sx_msk + qd * NQ;
         const float sl = p.scale_log2;
         const int nch = NQ / 16;                 // 16-column chunks
         uint32_t ua = 0;                  // units
@@ -771,11 +775,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             // the E4M3 query scales of this unit: written by the producer before it published
             // the table, rewritten only for unit ua + 2 (after this warp releases the table)
             const float *qinv = sx_qinv + ub * NQ;
-            // per unit: running maxima, and the last key offset (from the split's start) each
-            // column sees: row j of the branch sees positions <= pos_b + j
+            // per unit: running maxima, and each column's mask over the verify slots: row j of the
+            // branch sees every committed position (< pos_b) and the verify slot pos_b + i when
+            // bit i of its mask is set (a chain: bits 0..j; a tree: the row's ancestors and itself)
             for (int q = lane; q < NQ; q += 32) {
                 my_m[q] = -INFINITY;
-                my_lim[q] = q < n_q ? ui.pos_b + sx_colj[q] - ui.s0 : -1;
+                const int j = sx_colj[q];
+                my_msk[q] = q < n_q ? (p.anc ? __ldg(p.anc + ui.b * (p.k + 1) + j) : (int)((2u << j) - 1u)) : 0;
             }
             __syncwarp();
             for (int t0 = 0; t0 < ui.T && ok; t0 += p.TPI, sr.next(p.NSB), pr_last = pr, pr.next(p.NPB)) {
@@ -796,16 +802,21 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 // per tile i of the group: this thread's key offset from the split's start, its
                 // score factor slk (softmax scale in log2 units; FP8: times the key's K page scale,
                 // 0 past the branch's last position) and whether every row sees all 32 keys of
-                // the warp (then the per-column limits are skipped; the padding columns hold finite
-                // zero scores, their Q rows being 0)
+                // the warp (then the per-column masks are skipped; the padding columns hold finite
+                // zero scores, their Q rows being 0); bit0/bit1: this key's verify-slot bit (0 past
+                // the last slot), all0/all1: the key is a committed one, seen by every row
                 const int koff0 = t0 * TILE_KEYS + kl, koff1 = koff0 + TILE_KEYS;
+                const int rel0 = koff0 - (ui.pos_b - ui.s0), rel1 = rel0 + TILE_KEYS;
+                const bool all0 = rel0 < 0, all1 = rel1 < 0;
+                const uint32_t bit0 = (rel0 >= 0 && rel0 < 32) ? 1u << rel0 : 0u;
+                const uint32_t bit1 = (rel1 >= 0 && rel1 < 32) ? 1u << rel1 : 0u;
                 float slk0 = sl, slk1 = sl;
                 if (FP8) {
                     slk0 = ui.s0 + koff0 < ui.kv_end ? sl * tab->ksc[koff0 >> log2P] : 0.f;
                     slk1 = nt > 1 && ui.s0 + koff1 < ui.kv_end ? sl * tab->ksc[koff1 >> log2P] : 0.f;
                 }
-                const bool vis0 = __all_sync(0xFFFFFFFFu, koff0 <= ui.pos_b - ui.s0);
-                const bool vis1 = __all_sync(0xFFFFFFFFu, koff1 <= ui.pos_b - ui.s0);
+                const bool vis0 = __all_sync(0xFFFFFFFFu, all0);
+                const bool vis1 = __all_sync(0xFFFFFFFFu, all1);
                 uint8_t *prow = smem + p.off_p + pb * PBUF + kl * 32;
                 const int sw = (kl >> 2) & 1;  // 32-byte swizzle: 16-byte chunk index ^= row bit 2
                 // the scores s * slk of chunk c of tile i (both tiles' TMEM loads in flight
@@ -816,14 +827,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) x[j] = __uint_as_float(i ? r1[j] : r0[j]) * slk;
                     if (!(i ? vis1 : vis0)) {
-                        const int koff = i ? koff1 : koff0;
+                        const bool all = i ? all1 : all0;
+                        const uint32_t bit = i ? bit1 : bit0;
 #pragma unroll
                         for (int j = 0; j < 16; j += 4) {
-                            const int4 a = *reinterpret_cast<const int4 *>(my_lim + c * 16 + j);
-                            x[j] = koff <= a.x ? x[j] : -INFINITY;
-                            x[j + 1] = koff <= a.y ? x[j + 1] : -INFINITY;
-                            x[j + 2] = koff <= a.z ? x[j + 2] : -INFINITY;
-                            x[j + 3] = koff <= a.w ? x[j + 3] : -INFINITY;
+                            const int4 a = *reinterpret_cast<const int4 *>(my_msk + c * 16 + j);
+                            x[j] = (all || ((uint32_t)a.x & bit)) ? x[j] : -INFINITY;
+                            x[j + 1] = (all || ((uint32_t)a.y & bit)) ? x[j + 1] : -INFINITY;
+                            x[j + 2] = (all || ((uint32_t)a.z & bit)) ? x[j + 2] : -INFINITY;
+                            x[j + 3] = (all || ((uint32_t)a.w & bit)) ? x[j + 3] : -INFINITY;
                         }
                     }
                 };
@@ -956,14 +968,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                                 y[j] = FP8 ? fmaf(sj * slk, qs[j], -m[j]) : fmaf(sj, slk, -m[j]);
                             }
                             if (!(i ? vis1 : vis0)) {
-                                const int koff = i ? koff1 : koff0;
+                                const bool all = i ? all1 : all0;
+                                const uint32_t bit = i ? bit1 : bit0;
 #pragma unroll
                                 for (int j = 0; j < 16; j += 4) {
-                                    const int4 a = *reinterpret_cast<const int4 *>(my_lim + c * 16 + j);
-                                    y[j] = koff <= a.x ? y[j] : -INFINITY;
-                                    y[j + 1] = koff <= a.y ? y[j + 1] : -INFINITY;
-                                    y[j + 2] = koff <= a.z ? y[j + 2] : -INFINITY;
-                                    y[j + 3] = koff <= a.w ? y[j + 3] : -INFINITY;
+                                    const int4 a = *reinterpret_cast<const int4 *>(my_msk + c * 16 + j);
+                                    y[j] = (all || ((uint32_t)a.x & bit)) ? y[j] : -INFINITY;
+                                    y[j + 1] = (all || ((uint32_t)a.y & bit)) ? y[j + 1] : -INFINITY;
+                                    y[j + 2] = (all || ((uint32_t)a.z & bit)) ? y[j + 2] : -INFINITY;
+                                    y[j + 3] = (all || ((uint32_t)a.w & bit)) ? y[j + 3] : -INFINITY;
                                 }
                             }
                             uint32_t pk[8];
@@ -1076,8 +1089,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             }
             // every box lands, and every consumer's release of a stage is delivered, before the
             // CTA may exit
-            drain_ring(full0, rr, depth, gi);
-            drain_ring(empty0, rr, depth, gi);
+            drain_ring(full0, rr, depth, gi);  // (the stages' releases are plain arrives or drained by their MMA issuer)
             if (!ok) {
                 *abort_flag = 1;
                 raise_error(p.err, SPEC_DEVERR_TIMEOUT);
@@ -1172,10 +1184,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             if (ok && lane == 0) mbar_arrive(ufree + 8 * ub);
             if (!ok) break;
         }
-        // every copy lands before the CTA may exit, and so do the last MMA commits on the
-        // ring's "empty" barriers
+        // every copy lands before the CTA may exit (the stages' releases, MMA commits, are
+        // drained by the MMA issuers)
         cp_async_wait_all();
-        if (ltid == 0) drain_ring(empty0, rr, depth, gi);
         __syncwarp();
         if (!ok) {
             *abort_flag = 1;
@@ -1328,7 +1339,7 @@ __global__ void __launch_bounds__(512) attn_combine_kernel(AttnParams p, int W, 
         if (s < n_used) {
             const float2 v = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + ((u0 + s) * NQ + q) * 2));
             failed |= v.y < 0.f;
-            if (v.y > 0.f) M = fmaxf(M, v.x);
+            if (v.y != 0.f) M = fmaxf(M, v.x);  // (a NaN sum from NaN data is reached: it propagates)
         }
     }
 #pragma unroll
@@ -1346,6 +1357,8 @@ __global__ void __launch_bounds__(512) attn_combine_kernel(AttnParams p, int W, 
         failed |= wfail[i];
     }
     const bool skip = n_used == 0 || failed || M == -INFINITY;
+    // a tree row whose mask sees no key at all (nothing committed, no slot bit): no output
+    if (n_used > 0 && !failed && M == -INFINITY && threadIdx.x % (W * 32) == 0) raise_error(p.err, SPEC_DEVERR_POS);
     // ---- pass 2: group sums ----
     if (!skip) {
         for (int g0 = w; g0 < ng; g0 += W) {
@@ -1355,7 +1368,7 @@ __global__ void __launch_bounds__(512) attn_combine_kernel(AttnParams p, int W, 
             if (lane < nb) {
                 const float2 v = __ldcg(reinterpret_cast<const float2 *>(p.ws_ml + ((u0 + s0 + lane) * NQ + q) * 2));
                 ll = v.y;
-                wl = v.y > 0.f ? merge_weight(v.x, M) : 0.f;
+                wl = v.y != 0.f ? merge_weight(v.x, M) : 0.f;
             }
             float4 v[COMBINE_GROUP][E4];
 #pragma unroll
@@ -1376,7 +1389,7 @@ __global__ void __launch_bounds__(512) attn_combine_kernel(AttnParams p, int W, 
                 if (u >= nb) break;
                 const float wgt = __shfl_sync(0xFFFFFFFFu, wl, u);
                 const float l = __shfl_sync(0xFFFFFFFFu, ll, u);
-                if (!(l > 0.f)) continue;
+                if (l == 0.f) continue;
                 L = first ? wgt * l : fmaf(wgt, l, L);
 #pragma unroll
                 for (int e = 0; e < E4; ++e) {
@@ -1405,7 +1418,7 @@ __global__ void __launch_bounds__(512) attn_combine_kernel(AttnParams p, int W, 
         bool first = true;
         for (int g0 = 0; g0 < ng; ++g0) {
             const float l = gl[g0];
-            if (!(l > 0.f)) continue;
+            if (l == 0.f) continue;
             L = first ? l : L + l;
             first = false;
         }
@@ -1414,7 +1427,7 @@ __global__ void __launch_bounds__(512) attn_combine_kernel(AttnParams p, int W, 
             float acc = 0.f;
             bool f2 = true;
             for (int g0 = 0; g0 < ng; ++g0) {
-                if (!(gl[g0] > 0.f)) continue;
+                if (gl[g0] == 0.f) continue;
                 const float x = gsum[(size_t)g0 * D + d];
                 acc = f2 ? x : acc + x;
                 f2 = false;
@@ -1503,7 +1516,8 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
     // Then the richest plan whose ring holds 1.5 groups (2 Q buffers first; 2 P buffers for
     // groups of 2, else 3 first), else the deepest ring that holds one group.
     const int qb_opts[2] = {2, 1};
-    for (int TPI = 2; TPI >= 1; --TPI) {
+    // (splits of at most two tiles: single tiles, so that a unit's tiles still pipeline)
+    for (int TPI = p.split_keys >= 512 ? 2 : 1; TPI >= 1; --TPI) {
         // TMEM: 2 S buffers of a group and 2 O sets preferred, then fewer
         int NSB = 0, OB = 0;
         for (int ob = 2; ob >= 1 && !NSB; --ob)
@@ -1518,7 +1532,7 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
             NSB = 1;
             OB = 1;
         }
-        for (int pass = 0; pass < 2; ++pass)
+        for (int pass = 0; pass < 3; ++pass)
             for (int a = 0; a < 2; ++a)
                 for (int c = 0; c < 2; ++c) {
                     const int QB = qb_opts[a], NPB = TPI == 2 ? 2 : 3 - c;
@@ -1536,19 +1550,30 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
                     const int gsub = S_::NSUB * TPI;
                     int NK, NV, NR = 0;
                     if (!FP8) {
+                        if (pass == 2) continue;
                         int n = (int)(avail / S_::OP_STAGE);
                         n = n > 10 ? 10 : n;
                         NV = min(max(pass == 0 ? gsub : S_::NSUB, n - 2 * S_::NSUB), 2 * gsub);
                         NK = n - NV;
                         if (NK < (pass == 0 ? 2 * S_::NSUB : S_::NSUB) || NV < S_::NSUB) continue;
                     } else {
-                        NV = pass == 0 ? gsub : S_::NSUB;
-                        NR = pass == 0 ? 2 * S_::NSUB : S_::NSUB;
+                        // pass 0: converted-V stages for more than a group (the converters then
+                        // work on the next group while the P.V of this one is pending), at least
+                        // a group and one tile of K; pass 1: one group of V, two of K; pass 2:
+                        // one tile of each
+                        NR = pass < 2 ? 2 * S_::NSUB : S_::NSUB;
+                        const int nv_min = pass == 0 ? gsub + S_::NSUB : (pass == 1 ? gsub : S_::NSUB);
+                        const int nk_min = pass == 0 ? gsub + S_::NSUB : (pass == 1 ? 2 * gsub : S_::NSUB);
+                        NV = 0;
+                        for (int nv = pass == 0 ? 2 * gsub : nv_min; nv >= nv_min; --nv)
+                            if (avail >= nv * S_::OP_STAGE + NR * S_::F8_STAGE + nk_min * S_::F8_STAGE) {
+                                NV = nv;
+                                break;
+                            }
+                        if (!NV) continue;
                         const uint32_t used = NV * S_::OP_STAGE + NR * S_::F8_STAGE;
-                        if (avail < used) continue;
                         NK = (int)((avail - used) / S_::F8_STAGE);
                         NK = NK > 8 ? 8 : NK;
-                        if (NK < (pass == 0 ? 2 * gsub : S_::NSUB)) continue;
                     }
                     if (bar_map(NK, NV, NR, NSB, NPB).end > BAR_BYTES) return SPEC_ERR_UNSUPPORTED;
                     p.TPI = TPI;
@@ -1791,9 +1816,12 @@ SPEC_API size_t spec_verify_attn_workspace(const spec_kv_desc *kv, int B, int k,
     return spec::ws_layout(B, kv->n_kv_heads, n_splits, NQ, kv->head_dim, kv->kv_dtype == SPEC_KV_FP8_E4M3).total;
 }
 
-SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B, int k, int n_q_heads,
-                              const void *q, float scale, void *out, void *ws, size_t ws_bytes, int max_pos,
-                              int32_t *dev_err, spec_stream_t stream) {
+namespace spec {
+
+// The chain and tree entry points: the same kernels, the tree with per-row slot masks.
+static int attn_call(const spec_kv_desc *kvd, const int32_t *pos, int B, int k, int n_q_heads, const void *q,
+                     float scale, const int32_t *anc, void *out, void *ws, size_t ws_bytes, int max_pos,
+                     int32_t *dev_err, spec_stream_t stream) {
     int st = spec::check_kv_desc(kvd);
     if (st) return st;
     if (!pos || !q || !out) return SPEC_ERR_NULL;
@@ -1807,6 +1835,7 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
     st = spec::attn_setup(kvd, B, k, n_q_heads, max_pos, p);
     if (st) return st;
     p.pos = pos;
+    p.anc = anc;
     p.q = (const uint16_t *)q;
     p.out = (uint16_t *)out;
     p.scale_log2 = scale * spec::LOG2E;
@@ -1835,4 +1864,21 @@ SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B
         case 128: return spec::launch_combine<128>(p, s);
         default: return spec::launch_combine<256>(p, s);
     }
+}
+
+}  // namespace spec
+
+SPEC_API int spec_verify_attn(const spec_kv_desc *kvd, const int32_t *pos, int B, int k, int n_q_heads,
+                              const void *q, float scale, void *out, void *ws, size_t ws_bytes, int max_pos,
+                              int32_t *dev_err, spec_stream_t stream) {
+    return spec::attn_call(kvd, pos, B, k, n_q_heads, q, scale, nullptr, out, ws, ws_bytes, max_pos, dev_err,
+                           stream);
+}
+
+SPEC_API int spec_verify_attn_tree(const spec_kv_desc *kvd, const int32_t *pos, int B, int k, int n_q_heads,
+                                   const void *q, float scale, const int32_t *anc_mask, void *out, void *ws,
+                                   size_t ws_bytes, int max_pos, int32_t *dev_err, spec_stream_t stream) {
+    if (!anc_mask) return SPEC_ERR_NULL;
+    return spec::attn_call(kvd, pos, B, k, n_q_heads, q, scale, anc_mask, out, ws, ws_bytes, max_pos, dev_err,
+                           stream);
 }

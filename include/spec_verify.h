@@ -11,6 +11,8 @@
  *   spec_lmhead_argmax  logits = hidden . W^T with a fused per-row argmax
  *   spec_accept         greedy chain acceptance
  *   spec_accept_stop    greedy chain acceptance with stop tokens and a generation budget
+ *   spec_accept_sample  speculative sampling acceptance (random numbers as inputs)
+ *   spec_verify_attn_tree, spec_accept_tree, spec_kv_compact   tree / star verify
  *   spec_mtp_input      the draft head's input  fc([rmsnorm(E[tok]), rmsnorm(h)])
  *
  * The method follows the span-02 page `engine/crates/model/src/spec.rs`
@@ -77,6 +79,7 @@ typedef struct CUstream_st *spec_stream_t;
 #define SPEC_DEVERR_POS      16  /* pos[b] < 0, or pos[b]+k+1 > max_pos                 */
 #define SPEC_DEVERR_TIMEOUT  32  /* a bounded pipeline wait gave up (results invalid)   */
 #define SPEC_DEVERR_INTERNAL 64  /* an internal consistency check failed; the access was skipped */
+#define SPEC_DEVERR_TREE     128 /* a tree parent outside [0, row) or a path entry out of order */
 
 /* ---- limits ------------------------------------------------------------------------ */
 #define SPEC_KMAX            15  /* k <= 15: at most 16 verify rows per branch          */
@@ -188,6 +191,22 @@ int spec_verify_attn(const spec_kv_desc *kv, const int32_t *pos, int B, int k,
                      void *ws, size_t ws_bytes, int max_pos, int32_t *dev_err,
                      spec_stream_t stream);
 
+/* ---- f2: tree / star verify attention --------------------------------------------
+ * The verify rows of branch b own the slots pos_b .. pos_b+k (row j is written at slot
+ * pos_b + j by spec_kv_append); row j attends to every committed position (< pos_b) and to
+ * the slot pos_b + i exactly when bit i of anc_mask[b*(k+1)+j] is set (its ancestors in the
+ * draft tree and itself). A chain is the mask with bits 0..j (then the result is that of
+ * spec_verify_attn, bit for bit). Sources: DSSD-dev `_set_rows` / `_star_cycle` (a tree row
+ * reads the contiguous committed prefix and then the slots of its own path).
+ *   anc_mask  device int32 [B*(k+1)]; the other arguments, the workspace, the launch plan
+ *             and the errors are those of spec_verify_attn.
+ * Device errors: also SPEC_DEVERR_POS for a row that sees no key at all (empty mask and
+ * nothing committed); that row's output is left unwritten. */
+int spec_verify_attn_tree(const spec_kv_desc *kv, const int32_t *pos, int B, int k,
+                          int n_q_heads, const void *q, float scale, const int32_t *anc_mask,
+                          void *out, void *ws, size_t ws_bytes, int max_pos, int32_t *dev_err,
+                          spec_stream_t stream);
+
 /* ---- a3: LM head with fused argmax ------------------------------------------------
  *   logit[m][v] = sum_h hidden[m][h] * W[v][h]   (fp32 accumulation)
  *   ids[m]      = the lowest v attaining max_v logit[m][v]; with d2t, d2t[that v]
@@ -253,6 +272,10 @@ int spec_lmhead_argmax_static(const void *hidden, const void *W, int M, int V, i
  *   pos         device int32 [B]
  *   out_tokens  device int32 [B][k+1]: the n emitted tokens, then -1
  *   out_n, out_accepted, out_pos, out_next   device int32 [B] (out_next = bonus)
+ *   out_pos may be pos itself: the positions then advance in place, and a decode loop
+ *   captured in a CUDA graph keeps its step state (positions, next fed token in out_next,
+ *   the draft head's hidden row in h_out) on the device across replays. The same holds
+ *   for spec_accept_stop.
  *   hidden, H, h_out   optional (all three or none): h_out[b][:] =
  *       hidden[b*(k+1)+a][:], bf16 [B][H], the target hidden state of the row that
  *       produced the bonus token -- the next draft step's h (span-02 spec.rs,
@@ -288,6 +311,55 @@ int spec_accept_stop(const int32_t *drafts, const int32_t *ids, const int32_t *p
                      int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted,
                      int32_t *out_pos, int32_t *out_next, int32_t *out_done,
                      const void *hidden, int H, void *h_out, spec_stream_t stream);
+
+/* ---- f2: greedy tree walk and KV compaction --------------------------------------
+ * spec_accept_tree: per branch, rows 0..k form a tree (parent[b*(k+1)+j] < j for j >= 1;
+ * row 0 the root). From the root, repeatedly move to the first child c (in row order) with
+ * drafts[b][c-1] == ids[b*(k+1)+cur]; emitted = the drafts of the walked rows, then the
+ * target of the last row (the bonus); n = a+1 with a the rows walked; new pos = pos[b]+a+1;
+ * out_path[b][0] = 0, out_path[b][i] = the i-th walked row, then -1. With parent[j] = j-1 it
+ * is spec_accept. out_pos may be pos.
+ * spec_kv_compact: after the walk, row out_path[b][i] (written at slot pos_b + out_path[b][i])
+ * is moved to slot pos_b + i for i = 1..accepted[b] (pos = the position before the step),
+ * in ascending i; bf16 pools copy the bits, FP8 pools decode with the source page's scale
+ * and re-encode (round to nearest even, saturating) with the destination page's.
+ * Sources: DSSD-dev `_star_cycle` (walk the star / tree, copy the accepted child's K/V to
+ * slot pos0 + 1).
+ * Host errors: NULL, B < 1, k out of range, bad descriptor. Device errors: SPEC_DEVERR_TREE
+ * for a parent outside [0, j) (that row is never walked to) or a path entry out of order
+ * (that move is skipped); the page errors of spec_kv_append. */
+int spec_accept_tree(const int32_t *drafts, const int32_t *ids, const int32_t *pos,
+                     const int32_t *parent, int B, int k, int32_t *out_tokens, int32_t *out_n,
+                     int32_t *out_accepted, int32_t *out_pos, int32_t *out_next, int32_t *out_path,
+                     int32_t *dev_err, spec_stream_t stream);
+int spec_kv_compact(const spec_kv_desc *kv, const int32_t *pos, const int32_t *path,
+                    const int32_t *accepted, int B, int k, int32_t *dev_err, spec_stream_t stream);
+
+/* ---- f4: speculative sampling acceptance ------------------------------------------
+ * Per branch b, rows j = 0..k with p_j = softmax(logits[b*(k+1)+j] / temperature):
+ *   draft i (drafts[b][i], drawn by the draft model from q[b][i]) is kept when
+ *   p_i(d) >= q_i(d) or u_acc[b][i] < p_i(d) / q_i(d); the walk stops at the first draft
+ *   not kept (a = its index), whose replacement is drawn from max(0, p_a - q_a)
+ *   normalised (from p_a when that is all zero); after a full acceptance (a = k) the bonus
+ *   token is drawn from p_k. A draw from weights w takes the smallest index t whose running
+ *   sum (in index order) exceeds u_res[b] * sum(w).
+ *   emitted = drafts[b][0..a) followed by the drawn token; n = a+1; new pos = pos[b]+a+1.
+ * Sources: oxinfer `speculative_accept` (keep with probability min(1, p/q), else resample
+ * from the normalised positive part of p - q); DSSD-dev `_sample_verify` (stop at the first
+ * rejection; the bonus from the last row after a full acceptance). The random numbers are
+ * inputs, uniform in [0, 1).
+ *   drafts   device int32 [B][k];  logits  device fp32 [B*(k+1)][V];  q  device fp32 [B][k][V]
+ *            (probabilities);  u_acc  device fp32 [B][k];  u_res  device fp32 [B]
+ *   out_*    as spec_accept (out_pos may be pos);  temperature > 0
+ * Precision: probabilities in fp32 (exp2), sums in fp64 (compensated fp32 partial sums).
+ * A decision can differ from an all-fp64 evaluation only when its test value lies within
+ * that rounding of the boundary.
+ * Host errors: NULL, B < 1, k out of range, V < 1, temperature not positive and finite.
+ * Device errors: SPEC_DEVERR_TOKEN for a draft outside [0, V) (that draft is rejected). */
+int spec_accept_sample(const int32_t *drafts, const float *logits, const float *q, const int32_t *pos, int B,
+                       int k, int V, float temperature, const float *u_acc, const float *u_res,
+                       int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted, int32_t *out_pos,
+                       int32_t *out_next, int32_t *dev_err, spec_stream_t stream);
 
 /* ---- a5: MTP draft-head input -----------------------------------------------------
  *   c[m]  = [ rmsnorm(E[tok[m]]; g_emb) ; rmsnorm(h[m]; g_hid) ]  rounded to bf16
