@@ -21,8 +21,10 @@
 // Argmax: each (orderable fp32 logit, inverted vocab index) pair packs into 64 bits, so
 // the maximum key is the largest logit and, among equal logits, the lowest index. A warp
 // reduces its 32 vocab rows per column with one redux.sync + ballot; the four lane
-// quadrants and the CTA's tiles merge with 64-bit max; the last CTA to finish (atomic
-// counter) merges all CTAs' keys, applies d2t and writes the ids. Logits never reach HBM.
+// quadrants and the CTA's tiles merge with 64-bit max; each CTA folds its keys into one
+// global 64-bit maximum per row (atomicMax) and the last CTA to finish (atomic counter)
+// reads them back, zeroes them for the next call, applies d2t and writes the ids. Logits
+// never reach HBM.
 //
 // Every pipeline wait is bounded (1 s); on a timeout the kernel raises
 // SPEC_DEVERR_TIMEOUT, lets the loads and MMAs already issued land, frees TMEM and exits.
@@ -55,7 +57,7 @@ struct TcParams {
     uint32_t w_stage_bytes, a_stage_bytes, tmem_cols;
     float *logits;                  // TC_LOGITS: [M][V]
     float *partial;                 // TC_PARTIAL: [splits][M][V]
-    unsigned long long *keys;       // argmax: [gridDim.x][M]
+    unsigned long long *keys;       // argmax: [M] running maxima (zero between calls)
     unsigned int *counter;          // argmax: last-CTA detection (zero between calls)
     const int32_t *d2t;
     int d2t_limit;
@@ -282,9 +284,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             raise_error(p.err, SPEC_DEVERR_TIMEOUT);
         }
         if (EPI != TC_PARTIAL) {
+            // every CTA folds its keys into one 64-bit maximum per row in global memory as it
+            // finishes (order-independent, so the result is unique); the last CTA reads them
             for (int i = 0; i < 2; ++i) {
                 const int m = etid + 128 * i;
-                if (m < p.M) p.keys[(size_t)blockIdx.x * p.M + m] = running[i];
+                if (m < p.M) atomicMax(p.keys + m, running[i]);
             }
             __threadfence();
             epi_bar();
@@ -296,17 +300,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             epi_bar();
             if (*last_flag) {
                 __threadfence();
-                // merge every CTA's keys: coalesced reads spread over the 128 epilogue threads,
-                // 64-bit max in shared memory (order-independent, so the result is unique)
-                unsigned long long *red = cand;  // free now: [M]
-                for (int m = etid; m < p.M; m += 128) red[m] = 0ull;
-                epi_bar();
-                const int total = G * p.M;
-                for (int i = etid; i < total; i += 128)
-                    atomicMax(red + (i % p.M), __ldcg(p.keys + i));
-                epi_bar();
                 for (int m = etid; m < p.M; m += 128) {
-                    const unsigned long long b = red[m];
+                    const unsigned long long b = atomicExch(p.keys + m, 0ull);  // read, and zero for the next call
                     int id = (int)(0xFFFFFFFFu - (uint32_t)(b & 0xFFFFFFFFull));
                     if (p.max_logit) p.max_logit[m] = key_float((uint32_t)(b >> 32));
                     if (id < 0 || id >= p.V) {
