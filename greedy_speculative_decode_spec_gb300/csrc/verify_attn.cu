@@ -18,7 +18,8 @@
 // padding. FP8 pools feed their E4M3 K codes straight into kind::f8f6f4 MMAs: each query
 // is split into two E4M3 terms (q * sigma = hi + lo, sigma a power of two per query), exact
 // for every element within 2^10 of the query's largest one; V codes times their page
-// scale are rounded to bf16 for the P.V product. The K page scales are applied by the
+// scale are rounded to f16 for the P.V product (P in f16 too), or to bf16 (P in bf16) for a
+// unit with a V page scale outside [2^-14, 128]. The K page scales are applied by the
 // softmax to the scores.
 //
 // Softmax: a thread owns one key of the tile (its TMEM lane) and all query columns. One
@@ -76,6 +77,12 @@ constexpr int COMBINE_GROUP = 8;     // splits summed in order before the groups
 constexpr int MAX_NQ = 128;          // query vectors per (branch, kv head), padded to 16
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float RESCALE_TAU = 8.0f;  // P <= 2^8: exact range for bf16 and f16 alike
+// FP8 pools: the converted V and P are f16 when every V page scale of the unit lies in
+// [2^-14, 128] (the scale is an f16 normal, and |code * scale| <= 448 * 128 < 65504, so no
+// converted value overflows), bf16 otherwise; f16 keeps three more mantissa bits of both,
+// and the conversion is one f16 multiply
+constexpr float VF16_MIN_SCALE = 6.103515625e-05f;
+constexpr float VF16_MAX_SCALE = 128.0f;
 constexpr uint64_t ATT_WAIT_NS = 1000000000ull;
 constexpr int ATT_SMEM_LIMIT = 227 * 1024;
 constexpr int ATT_THREADS = 384;
@@ -96,6 +103,7 @@ struct alignas(16) UnitTable {
     float vsc[UT_ENTRIES];
     UnitInfo ui;
     int32_t bad;
+    int32_t vf16;          // FP8: the unit's P.V runs in f16 (every V page scale keeps code * scale in range)
     int32_t iter;          // the unit's index in the walk order, or -1: no more units
 };
 // the softmax scratch that follows the two tables is read with 16-byte vector loads
@@ -364,9 +372,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     // the A operand of the row-sum MMA: 8 rows x 128 bytes of ones (every 8-row group and
     // every K step of the MMA read this one atom)
     {
-        const uint32_t one2 = 0x3F803F80u;  // bf16 1.0, twice
+        // (then the same atom of f16 ones, for units whose P is f16)
         uint32_t *ones = reinterpret_cast<uint32_t *>(smem + p.off_ones);
-        for (int i = threadIdx.x; i < 256; i += ATT_THREADS) ones[i] = one2;
+        for (int i = threadIdx.x; i < 512; i += ATT_THREADS) ones[i] = i < 256 ? 0x3F803F80u : 0x3C003C00u;
         fence_proxy_async_smem();
     }
     if (warp == 8 && lane == 0) {
@@ -434,6 +442,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 break;
             }
             int badbits = 0;
+            bool v_big = false;  // some V page scale of the unit is too large for an f16 P.V
             if (!small_pages) {
                 const int nkeys = min(ui.kv_end - ui.s0, p.split_keys);
                 const int nent = (nkeys + p.kv.page_size - 1) >> log2P;
@@ -446,6 +455,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                         const size_t si = (size_t)pg * p.kv.n_kv_heads + ui.g;
                         ks = __ldg(p.kv.k_scale + si);
                         vs = __ldg(p.kv.v_scale + si);
+                        v_big |= !(vs >= VF16_MIN_SCALE && vs <= VF16_MAX_SCALE);
                     }
                     tab->page[e] = pg < 0 ? -1 : pg;
                     tab->ksc[e] = ks;
@@ -461,6 +471,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 }
             }
             badbits = __reduce_or_sync(0xFFFFFFFFu, badbits);
+            v_big = __any_sync(0xFFFFFFFFu, v_big);
             if (FP8) {  // the unit's query scales (1/sigma per column), read by the softmax
                 const float *qi = p.qinv_g + (size_t)(ui.b * p.kv.n_kv_heads + ui.g) * NQ;
                 for (int q = lane; q < NQ; q += 32) sx_qinv[ub * NQ + q] = __ldg(qi + q);
@@ -468,6 +479,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             if (lane == 0) {
                 tab->ui = ui;
                 tab->bad = badbits;
+                tab->vf16 = FP8 && !v_big ? 1 : 0;
                 tab->iter = it_u;
                 if (badbits) raise_error(p.err, badbits);
             }
@@ -617,8 +629,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         __syncwarp();
     } else if (warp == 10) {
         // ================= MMA issuer: O^T += V^T . P^T, L += 1 . P^T =================
-        const uint32_t idesc_pv = idesc_f16kind(128, NQ, false, true, true);
-        const uint32_t idesc_l = idesc_f16kind(128, NQ, false, false, true);
+        // bf16 operands, or f16 ones for FP8 units whose V and P are f16
+        const uint32_t idesc_pv_b = idesc_f16kind(128, NQ, false, true, true), idesc_l_b = idesc_f16kind(128, NQ, false, false, true);
+        const uint32_t idesc_pv_h = idesc_f16kind(128, NQ, true, true, true), idesc_l_h = idesc_f16kind(128, NQ, true, false, true);
         // V's MN-major descriptor: 64-column blocks 128 keys x 128 bytes apart; a 64-wide
         // head dimension repeats its one block on lanes 64..127 (never read)
         const uint32_t v_lbo = S_::SUB == 128 ? TILE_KEYS * 128 : 0;
@@ -631,8 +644,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             const int it_u = tables[ub].iter;
             if (it_u < 0) break;
             const UnitInfo ui = tables[ub].ui;
-            const int u = ui.u;
-            (void)u;
+            const bool vf16 = FP8 && tables[ub].vf16 != 0;
+            const uint32_t idesc_pv = vf16 ? idesc_pv_h : idesc_pv_b, idesc_l = vf16 ? idesc_l_h : idesc_l_b;
+            const uint32_t s_one = s_ones + (vf16 ? 1024u : 0u);
             __syncwarp();
             if (lane == 0) mbar_arrive(ufree + 8 * ub);
             const uint32_t ob = orr.s;
@@ -669,7 +683,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 }
                 if (!ok) break;
                 if (lane == 0) {
-                    const uint64_t one0 = desc_kmajor(s_ones, 128, 0);
+                    const uint64_t one0 = desc_kmajor(s_one, 128, 0);
 #pragma unroll 1
                     for (int i = 0; i < nt; ++i) {
                         const int t = t0 + i;
@@ -770,6 +784,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             const int u = ui.u;
             (void)u;
             const bool failed = tab->bad != 0;
+            const bool pf16 = FP8 && tab->vf16 != 0;  // this unit's P is f16 (its V is too)
             const uint32_t ob = orr.s, mb = ua & 1u;
             float *my_m = sx_m + (mb * 4 + qd) * NQ;
             // the E4M3 query scales of this unit: written by the producer before it published
@@ -983,7 +998,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 #pragma unroll
                             for (int j = 0; j < 16; j += 2) {
                                 ymax = fmaxf(ymax, fmaxf(y[j], y[j + 1]));
-                                pk[j >> 1] = pack2(ex2_approx(y[j]), ex2_approx(y[j + 1]), false);
+                                pk[j >> 1] = pack2(ex2_approx(y[j]), ex2_approx(y[j + 1]), pf16);
                             }
                             uint8_t *blk = prow + i * PTILE + c * (TILE_KEYS * 32);
                             *reinterpret_cast<uint4 *>(blk + (sw << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -1194,8 +1209,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
     } else {
         // ================= FP8 converters, warps 4-7 (one per SM sub-partition) =================
-        // Every raw V sub-tile, in ring order, becomes bf16(code * page scale) in the MMA's
-        // layout (the V ring), with the rows past the branch's last position written as
+        // Every raw V sub-tile, in ring order, becomes f16(code * page scale) (bf16 for a unit
+        // whose V scales leave the f16 range) in the MMA's layout (the V ring), with the rows past
+        // the branch's last position written as
         // zeros. Each warp fences its own share and arrives on the stage's barriers (count 4).
         // Their waits do not sleep: the converted V is on the P.V MMAs' critical path.
         const int ctid = (warp - 4) * 32 + lane;  // 0..127
@@ -1209,6 +1225,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             const int it_u = tab->iter;
             if (it_u < 0) break;
             const UnitInfo ui = tab->ui;
+            const bool vf16 = tab->vf16 != 0;
             ++ua;
             for (int t = 0; t < ui.T && ok; ++t) {
                 const int nvk = ui.kv_end - (ui.s0 + t * TILE_KEYS);  // valid keys of the tile (>= 1)
@@ -1245,12 +1262,24 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                             const bool live = row < nvk;  // rows past the last position: zeros, never code * 0
                             const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
                             uint32_t hv[8];
+                            if (vf16) {
+                                // f16(code * scale): the code is exact in f16, one f16 multiply
+                                const __half2 s2 = __float2half2_rn(vs[i]);
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const __half2_raw c2 = __nv_cvt_fp8x2_to_halfraw2(
-                                    (__nv_fp8x2_storage_t)((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu), __NV_E4M3);
-                                const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&c2));
-                                hv[e] = live ? pack2(f.x * vs[i], f.y * vs[i], false) : 0u;
+                                for (int e = 0; e < 8; ++e) {
+                                    const __half2_raw c2 = __nv_cvt_fp8x2_to_halfraw2(
+                                        (__nv_fp8x2_storage_t)((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu), __NV_E4M3);
+                                    const __half2 r2 = __hmul2(*reinterpret_cast<const __half2 *>(&c2), s2);
+                                    hv[e] = live ? *reinterpret_cast<const uint32_t *>(&r2) : 0u;
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const __half2_raw c2 = __nv_cvt_fp8x2_to_halfraw2(
+                                        (__nv_fp8x2_storage_t)((w[e >> 1] >> (16 * (e & 1))) & 0xFFFFu), __NV_E4M3);
+                                    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&c2));
+                                    hv[e] = live ? pack2(f.x * vs[i], f.y * vs[i], false) : 0u;
+                                }
                             }
                             *reinterpret_cast<uint4 *>(op + sw128_off(row, pc * 16, TILE_KEYS * 128)) =
                                 make_uint4(hv[0], hv[1], hv[2], hv[3]);
@@ -1540,7 +1569,7 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
                     const uint32_t q_bytes = FP8 ? 0 : QB * S_::NATOM_Q * NQ * 128;
                     const uint32_t q8_bytes = FP8 ? QB * 2 * S_::NQ8 * NQ * S_::Q8ROW : 0;
                     const uint32_t p_bytes = NPB * TPI * NQ * 256;
-                    const uint32_t fixed = align_up(q_bytes + q8_bytes + p_bytes, 1024) + 1024;  // + ones
+                    const uint32_t fixed = align_up(q_bytes + q8_bytes + p_bytes, 1024) + 2048;  // + bf16 and f16 ones
                     const uint32_t tail = ut_bytes + sx_bytes + bars + small + 32;  // + alignment slack
                     if (1024 + fixed + tail > ATT_SMEM_LIMIT) continue;
                     const uint32_t avail = ATT_SMEM_LIMIT - 1024 - fixed - tail;
@@ -1588,7 +1617,7 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
                     p.off_q8 = p.off_q + q_bytes;
                     p.off_p = p.off_q8 + q8_bytes;
                     p.off_ones = align_up(p.off_p + p_bytes, 1024);
-                    p.off_k = p.off_ones + 1024;
+                    p.off_k = p.off_ones + 2048;
                     p.off_v = p.off_k + NK * S_::K_STAGE;
                     p.off_raw = p.off_v + NV * S_::OP_STAGE;
                     p.off_ut = p.off_raw + NR * S_::F8_STAGE;

@@ -349,3 +349,14 @@ def test_accept_stop_host_errors():
     toks = torch.zeros((1, 2), **i32)
     with pytest.raises(bnd.SpecError):
         bnd.spec_accept_stop(t[:1], t[:2], t[:1], 1, 1, torch.zeros(33, **i32), None, toks, t[:1], t[:1], t[:1], t[:1])
+
+
+def test_fp8_large_v_scales_take_the_bf16_path():
+    """FP8 pools whose V page scales exceed the f16 range of the converted values: those
+    units multiply in bf16 (the same codes, every V value and scale times 2^16)."""
+    vi = verify_inputs(SMALL["long_fp8"])
+    big = 65536.0
+    vi.ctx_v = (vi.ctx_v.float() * big).to(torch.bfloat16)
+    vi.v_new = (vi.v_new.float() * big).to(torch.bfloat16)
+    vi.v_scale = vi.v_scale * big
+    _step_parity(vi, full_oracle=True)
