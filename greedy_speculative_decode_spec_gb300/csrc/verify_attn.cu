@@ -854,9 +854,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                         }
                     }
                 };
-                auto load2 = [&](int c, uint32_t (&r0)[16], uint32_t (&r1)[16]) {
+                auto issue2 = [&](int c, uint32_t (&r0)[16], uint32_t (&r1)[16]) {
                     tmem_ld16(sgrp + (uint32_t)(c * 16), r0);
                     if (nt > 1) tmem_ld16(sgrp + (uint32_t)(NQ + c * 16), r1);
+                };
+                auto load2 = [&](int c, uint32_t (&r0)[16], uint32_t (&r1)[16]) {
+                    issue2(c, r0, r1);
                     tmem_ld_wait();
                 };
                 // the flag (and, on the full path, maxima) exchange among the four warps
@@ -951,18 +954,22 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                             tmem_st_wait();
                         }
                     }
+                    // ---- P^T rows of this thread's keys: P = 2^y, y = s * slk (* 1/sigma) - m, the
+                    // product and the subtraction fused; ymax: whether some y exceeds RESCALE_TAU.
+                    // Each tile's scores of the next chunk start loading from TMEM into its
+                    // registers as soon as the tile is computed (the first chunk's while the P
+                    // buffer is awaited) ----
+                    uint32_t r0[16], r1[16];
+                    issue2(0, r0, r1);
                     if (!waited) {
                         ok = warp_wait(pfree + 8 * pb, pr.ph ^ 1u, abort_flag, wns);
                         if (!ok) break;
                         waited = true;
                     }
-                    // ---- P^T rows of this thread's keys: P = 2^y, y = s * slk (* 1/sigma) - m, the
-                    // product and the subtraction fused; ymax: whether some y exceeds RESCALE_TAU ----
+                    tmem_ld_wait();
                     float ymax = -INFINITY;
 #pragma unroll 1
                     for (int c = 0; c < nch; ++c) {
-                        uint32_t r0[16], r1[16];
-                        load2(c, r0, r1);
                         float m[16], qs[16];
 #pragma unroll
                         for (int j = 0; j < 16; j += 4) {
@@ -973,13 +980,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                                 qs[j] = b4.x; qs[j + 1] = b4.y; qs[j + 2] = b4.z; qs[j + 3] = b4.w;
                             }
                         }
-#pragma unroll 1
-                        for (int i = 0; i < nt; ++i) {
+                        // tile i's P from its registers r (never touched while a load into them is
+                        // in flight), then that tile's next chunk is requested into the same registers
+                        auto ptile = [&](int i, uint32_t (&r)[16]) {
                             const float slk = i ? slk1 : slk0;
                             float y[16];
 #pragma unroll
                             for (int j = 0; j < 16; ++j) {
-                                const float sj = __uint_as_float(i ? r1[j] : r0[j]);
+                                const float sj = __uint_as_float(r[j]);
                                 y[j] = FP8 ? fmaf(sj * slk, qs[j], -m[j]) : fmaf(sj, slk, -m[j]);
                             }
                             if (!(i ? vis1 : vis0)) {
@@ -1003,7 +1011,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                             uint8_t *blk = prow + i * PTILE + c * (TILE_KEYS * 32);
                             *reinterpret_cast<uint4 *>(blk + (sw << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                             *reinterpret_cast<uint4 *>(blk + ((sw ^ 1) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                        }
+                            if (c + 1 < nch) tmem_ld16(sgrp + (uint32_t)(i * NQ + (c + 1) * 16), r);
+                        };
+                        ptile(0, r0);
+                        if (nt > 1) ptile(1, r1);
+                        if (c + 1 < nch) tmem_ld_wait();
                     }
                     if (attempt == 0 && !full) {
                         // the one-pass try: keep it unless some warp saw a score above its maximum
