@@ -85,6 +85,7 @@ def lib():
         _lib.orc_kv_compact.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_int]
         _lib.orc_accept_sample.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int] * 3 + [ctypes.c_double]
                                            + [ctypes.c_void_p] * 7)
+        _lib.orc_accept_sample.restype = ctypes.c_int
         _lib.orc_accept_stop.argtypes = ([ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                           ctypes.c_int] + [ctypes.c_void_p] * 7)
         _lib.orc_mtp_input.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_double, ctypes.c_void_p, ctypes.c_int,
@@ -211,7 +212,8 @@ def accept_tree(drafts, ids, pos, parent, B: int, k: int):
 
 def accept_sample(drafts, logits, q, pos, B: int, k: int, temperature: float, u_acc, u_res):
     """Speculative sampling acceptance with the random numbers given: tokens, n, accepted,
-    new_pos, next. logits fp32 [B*(k+1)][V]; q fp32 [B][k][V]; u_acc [B][k]; u_res [B]."""
+    new_pos, next, error bits (a draft outside [0, V) or with q(d) = 0 is an error and is
+    rejected). logits fp32 [B*(k+1)][V]; q fp32 [B][k][V]; u_acc [B][k]; u_res [B]."""
     logits = _c(logits, np.float32)
     V = logits.shape[-1]
     drafts = _c(np.asarray(drafts).reshape(B, k) if k > 0 else np.zeros((B, 1)), np.int32)
@@ -220,9 +222,9 @@ def accept_sample(drafts, logits, q, pos, B: int, k: int, temperature: float, u_
     pos, u_res = _c(pos, np.int32), _c(u_res, np.float32)
     tokens = np.empty((B, k + 1), np.int32)
     n, a, npos, nxt = (np.empty(B, np.int32) for _ in range(4))
-    lib().orc_accept_sample(_p(drafts), _p(logits), _p(q), _p(pos), B, k, V, float(temperature), _p(u_acc), _p(u_res),
-                            _p(tokens), _p(n), _p(a), _p(npos), _p(nxt))
-    return tokens, n, a, npos, nxt
+    err = lib().orc_accept_sample(_p(drafts), _p(logits), _p(q), _p(pos), B, k, V, float(temperature), _p(u_acc),
+                                  _p(u_res), _p(tokens), _p(n), _p(a), _p(npos), _p(nxt))
+    return tokens, n, a, npos, nxt, int(err)
 
 
 def kv_compact(kv: KvPool, pos, path, accepted, B: int, k: int) -> int:

@@ -48,6 +48,7 @@
 #define ORC_ERR_TOKEN 4
 #define ORC_ERR_D2T 8
 #define ORC_ERR_POS 16
+#define ORC_ERR_TREE 32
 
 int orc_threads(void) {
 #ifdef _OPENMP
@@ -347,7 +348,12 @@ int orc_verify_attn_tree(const orc_kv *kv, const int32_t *pos, int B, int k, int
         double *s = (double *)malloc(sizeof(double) * (size_t)(maxp + 1));
         int32_t *keys = (int32_t *)malloc(sizeof(int32_t) * (size_t)(maxp + 1));
         double *o = out + ((size_t)r * Hq + h) * d;
+        /* row j of a branch is a tree node: it sees itself and only earlier rows (its
+         * ancestors), so bit j is set and no bit above j */
+        const int j = r % (k + 1);
+        const uint32_t m = (uint32_t)anc_mask[r];
         int e = pos[b] < 0 ? ORC_ERR_POS : 0, n = 0;
+        if (!((m >> j) & 1u) || ((m >> j) >> 1) != 0) e |= ORC_ERR_TREE;
         if (!e) {
             for (int t = 0; t < pos[b]; ++t) keys[n++] = t;
             for (int i = 0; i <= k; ++i)
@@ -556,7 +562,6 @@ void orc_accept_stop(const int32_t *drafts, const int32_t *ids, const int32_t *p
  * argmax (the bonus); path[b][0] = 0 and path[b][i] = the i-th accepted row, -1 after.
  * A parent array with parent[j] outside [0, j) gives an error bit and no walk past it.
  * With parent[j] = j-1 this is orc_accept. */
-#define ORC_ERR_TREE 32
 int orc_accept_tree(const int32_t *drafts, const int32_t *ids, const int32_t *pos, const int32_t *parent,
                     int B, int k, int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted,
                     int32_t *out_pos, int32_t *out_next, int32_t *out_path) {
@@ -658,11 +663,15 @@ static void softmax_t(const float *z, int V, double temperature, double *p) {
     for (int t = 0; t < V; ++t) p[t] /= den;
 }
 
-void orc_accept_sample(const int32_t *drafts, const float *logits, const float *q, const int32_t *pos, int B,
-                       int k, int V, double temperature, const float *u_acc, const float *u_res,
-                       int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted, int32_t *out_pos,
-                       int32_t *out_next) {
-#pragma omp parallel for schedule(dynamic, 16)
+/* A draft is a sample of q, so 0 <= d < V and q(d) > 0; a draft outside the vocabulary or
+ * one that q gives no probability cannot have been drawn: it is an input error
+ * (ORC_ERR_TOKEN) and is rejected (the replacement is drawn from the residual). */
+int orc_accept_sample(const int32_t *drafts, const float *logits, const float *q, const int32_t *pos, int B,
+                      int k, int V, double temperature, const float *u_acc, const float *u_res,
+                      int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted, int32_t *out_pos,
+                      int32_t *out_next) {
+    int err = 0;
+#pragma omp parallel for schedule(dynamic, 16) reduction(| : err)
     for (int b = 0; b < B; ++b) {
         double *p = (double *)malloc(sizeof(double) * (size_t)V);
         double *w = (double *)malloc(sizeof(double) * (size_t)V);
@@ -672,8 +681,10 @@ void orc_accept_sample(const int32_t *drafts, const float *logits, const float *
             softmax_t(logits + ((size_t)b * (k + 1) + i) * V, V, temperature, p);
             const int d = drafts[(size_t)b * k + i];
             const float *qi = q + ((size_t)b * k + i) * V;
-            const double pd = p[d], qd = (double)qi[d];
-            if (pd >= qd || (double)u_acc[(size_t)b * k + i] < pd / qd) {
+            const int valid = d >= 0 && d < V && (double)qi[d] > 0.0;
+            if (!valid) err |= ORC_ERR_TOKEN;
+            const double pd = valid ? p[d] : 0.0, qd = valid ? (double)qi[d] : 1.0;
+            if (valid && (pd >= qd || (double)u_acc[(size_t)b * k + i] < pd / qd)) {
                 emit[a++] = d;
                 continue;
             }
@@ -699,6 +710,7 @@ void orc_accept_sample(const int32_t *drafts, const float *logits, const float *
         free(p);
         free(w);
     }
+    return err;
 }
 
 /* ------------------------------------------------------------------------------------

@@ -66,6 +66,28 @@ def test_tree_attention_matches_sdpa_over_the_row_key_lists(orc, fp8):
             np.testing.assert_allclose(out[b * (k + 1) + j], ref[0, :, 0].numpy(), rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("bad", ["missing_self", "sees_a_later_row"])
+def test_tree_attention_rejects_masks_that_are_not_ancestor_sets(orc, bad):
+    """Row j of a tree sees itself and only earlier rows (DSSD-dev `_set_rows`: the row's
+    own path): a mask without bit j, or with a bit above j, is reported and its row is NaN;
+    the other rows are untouched."""
+    rng = np.random.default_rng(21)
+    B, k, Hq, Hkv, d, P = 2, 4, 4, 2, 8, 4
+    ctxs = [3, 6]
+    kv, q, _, _ = _attn_case(orc, rng, B, k, Hq, Hkv, d, P, ctxs)
+    masks = np.array([_ancestor_masks(_random_parents(rng, k)) for _ in range(B)], np.int32)
+    good, err = orc.verify_attn_tree(kv, ctxs, B, k, Hq, q, 0.3, masks)
+    assert err == 0
+    bb, j = 1, 2
+    masks[bb, j] = (masks[bb, j] & ~(1 << j)) if bad == "missing_self" else (masks[bb, j] | (1 << (j + 1)))
+    out, err = orc.verify_attn_tree(kv, ctxs, B, k, Hq, q, 0.3, masks)
+    assert err == orc.ERR_TREE
+    r = bb * (k + 1) + j
+    assert np.isnan(out[r]).all()
+    keep = np.arange(B * (k + 1)) != r
+    np.testing.assert_array_equal(out[keep], good[keep])
+
+
 def test_accept_tree_golden(orc):
     with open(os.path.join(GOLDEN, "accept_tree_example.json")) as f:
         fx = json.load(f)
