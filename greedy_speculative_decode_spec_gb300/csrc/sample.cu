@@ -193,11 +193,14 @@ __global__ void __launch_bounds__(SMP_THREADS) sample_accept_kernel(SampleArgs a
         row_stats(z, V, c, redf, red, mx, den);
         if (threadIdx.x == 0) {
             const int d = __ldg(a.drafts + (size_t)b * k + i);
+            // a draft is a sample of q: one outside [0, V) or with q(d) <= 0 (or NaN) is
+            // reported and rejected
+            const double qd = (d >= 0 && d < V) ? (double)__ldg(qi + d) : 0.0;
             int keep = 0;
-            if (d < 0 || d >= V) {
-                raise_error(a.err, SPEC_DEVERR_TOKEN);  // an invalid draft is rejected
+            if (!(qd > 0.0)) {
+                raise_error(a.err, SPEC_DEVERR_TOKEN);
             } else {
-                const double pd = (double)exp2f((__ldg(z + d) - mx) * c) / den, qd = (double)__ldg(qi + d);
+                const double pd = (double)exp2f((__ldg(z + d) - mx) * c) / den;
                 keep = (pd >= qd || (double)__ldg(a.u_acc + (size_t)b * k + i) < pd / qd) ? 1 : 0;
             }
             s_keep = keep;

@@ -1369,6 +1369,14 @@ __global__ void __launch_bounds__(512) attn_combine_kernel(AttnParams p, int W, 
         if (pos_b >= 0 && pos_b + p.k + 1 <= p.max_pos) {
             n_used = (pos_b + p.k + 1 + p.split_keys - 1) / p.split_keys;
         }
+        if (p.anc) {  // a tree row sees itself and only earlier rows: bit j set, none above
+            const int j = r % (p.k + 1);
+            const uint32_t m = (uint32_t)__ldg(p.anc + r);
+            if (!((m >> j) & 1u) || ((m >> j) >> 1) != 0) {
+                if (threadIdx.x % (W * 32) == 0) raise_error(p.err, SPEC_DEVERR_TREE);
+                n_used = 0;
+            }
+        }
         u0 = (size_t)(b * p.kv.n_kv_heads + g) * p.n_splits;
     }
     const int ng = (n_used + COMBINE_GROUP - 1) / COMBINE_GROUP;

@@ -200,8 +200,8 @@ int spec_verify_attn(const spec_kv_desc *kv, const int32_t *pos, int B, int k,
  * reads the contiguous committed prefix and then the slots of its own path).
  *   anc_mask  device int32 [B*(k+1)]; the other arguments, the workspace, the launch plan
  *             and the errors are those of spec_verify_attn.
- * Device errors: also SPEC_DEVERR_POS for a row that sees no key at all (empty mask and
- * nothing committed); that row's output is left unwritten. */
+ * Device errors: also SPEC_DEVERR_TREE for a row j whose mask lacks bit j or has a bit above
+ * j (a tree row sees itself and only earlier rows); that row's output is left unwritten. */
 int spec_verify_attn_tree(const spec_kv_desc *kv, const int32_t *pos, int B, int k,
                           int n_q_heads, const void *q, float scale, const int32_t *anc_mask,
                           void *out, void *ws, size_t ws_bytes, int max_pos, int32_t *dev_err,
@@ -355,7 +355,8 @@ int spec_kv_compact(const spec_kv_desc *kv, const int32_t *pos, const int32_t *p
  * A decision can differ from an all-fp64 evaluation only when its test value lies within
  * that rounding of the boundary.
  * Host errors: NULL, B < 1, k out of range, V < 1, temperature not positive and finite.
- * Device errors: SPEC_DEVERR_TOKEN for a draft outside [0, V) (that draft is rejected). */
+ * Device errors: SPEC_DEVERR_TOKEN for a draft outside [0, V) or with q_i(d) <= 0 (not a
+ * sample of q): that draft is treated as rejected. */
 int spec_accept_sample(const int32_t *drafts, const float *logits, const float *q, const int32_t *pos, int B,
                        int k, int V, float temperature, const float *u_acc, const float *u_res,
                        int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted, int32_t *out_pos,

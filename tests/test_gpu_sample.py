@@ -84,7 +84,8 @@ def test_sample_accept_matches_oracle(B, k, V, T):
     logits, q, drafts, u_acc, u_res, pos = _inputs(B, k, V, T, seed=V + k)
     g_toks, g_n, g_a, g_pos, g_next, err = _gpu(logits, q, drafts, u_acc, u_res, pos, B, k, T)
     assert err == 0
-    o_toks, o_n, o_a, o_pos, o_next = orc.accept_sample(drafts, logits, q, pos, B, k, T, u_acc, u_res)
+    o_toks, o_n, o_a, o_pos, o_next, o_err = orc.accept_sample(drafts, logits, q, pos, B, k, T, u_acc, u_res)
+    assert o_err == 0
     mismatches = [b for b in range(B) if not np.array_equal(g_toks[b], o_toks[b])]
     for b in mismatches:
         assert _near_tie(b, k, T, logits, q, drafts, u_acc, u_res, int(g_a[b]), int(o_a[b])), f"branch {b} differs"
@@ -122,3 +123,22 @@ def test_sample_accept_host_errors():
         bnd.spec_accept_sample(torch.zeros((1, 1), **i32), z, torch.zeros((1, 1, 8), device=DEV), torch.zeros(1, **i32),
                                1, 1, 0.0, torch.zeros((1, 1), device=DEV), torch.zeros(1, device=DEV),
                                torch.empty((1, 2), **i32), *o)
+
+
+@pytest.mark.parametrize("bad", ["below", "above", "q_zero"])
+def test_invalid_draft_is_rejected_and_reported(bad):
+    B, k, V, T = 4, 3, 3001, 1.0
+    logits, q, drafts, u_acc, u_res, pos = _inputs(B, k, V, T, seed=77)
+    bb, ii = 2, 1
+    if bad == "below":
+        drafts[bb, ii] = -5
+    elif bad == "above":
+        drafts[bb, ii] = V
+    else:
+        q[bb, ii, drafts[bb, ii]] = 0.0
+    g = _gpu(logits, q, drafts, u_acc, u_res, pos, B, k, T)
+    o = orc.accept_sample(drafts, logits, q, pos, B, k, T, u_acc, u_res)
+    assert g[5] == bnd.DEVERR_TOKEN and o[5] == orc.ERR_TOKEN
+    assert g[2][bb] <= ii
+    for gi, oi in zip(g[:5], o[:5]):
+        assert np.array_equal(gi, oi)

@@ -94,6 +94,33 @@ def test_tree_attention_with_chain_masks_is_the_chain_bit_for_bit(name):
     assert torch.equal(tree_out.view(torch.int16), chain_out.view(torch.int16))
 
 
+def test_tree_attention_reports_bad_masks():
+    """A row whose mask lacks its own bit, or has a later row's bit, is reported and left
+    unwritten; every other row matches the oracle."""
+    vi = verify_inputs(CASES["bf16"])
+    c = vi.cfg
+    gkv, okv = _appended(vi)
+    rng = np.random.default_rng(8)
+    masks = masks_from_parents(random_parents(c.B, c.k, rng))
+    masks[1, 3] &= ~(1 << 3)
+    masks[2, 1] |= 1 << 4
+    sentinel = torch.full((c.B * (c.k + 1), c.Hq, c.d), 7.0, dtype=torch.bfloat16, device=DEV)
+    out = sentinel.clone()
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    bnd.spec_verify_attn_tree(gkv.desc, vi.pos.cuda(), c.B, c.k, c.Hq, vi.q.cuda(), 1.0 / math.sqrt(c.d),
+                              torch.from_numpy(masks.reshape(-1)).to(DEV), out,
+                              attn_ws(gkv, c.B, c.k, c.Hq, vi.max_pos), vi.max_pos, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == bnd.DEVERR_TREE
+    ref, oe = orc.verify_attn_tree(okv, vi.pos.numpy(), c.B, c.k, c.Hq, bits(vi.q), 1.0 / math.sqrt(c.d), masks)
+    assert oe == orc.ERR_TREE
+    bad = [1 * (c.k + 1) + 3, 2 * (c.k + 1) + 1]
+    assert np.isnan(ref[bad]).all()
+    assert torch.equal(out[bad], sentinel[bad])
+    keep = [r for r in range(c.B * (c.k + 1)) if r not in bad]
+    assert_attn_close(out[keep], ref[keep], "tree attention, valid rows")
+
+
 def _walk_inputs(B, k, rng, V=50):
     par = random_parents(B, k, rng)
     ids = rng.integers(0, V, (B, k + 1)).astype(np.int32)

@@ -49,11 +49,21 @@ def test_static_scratch_matches_workspace_two_calls(V, H, M):
     want_ids, want_mx, e = _with_workspace(W, hidden)
     assert e == 0
     assert torch.equal(want_ids.long(), planted.long())
-    for _ in range(2):  # the second call finds the counter the first one left at zero
+    ids, mx, e = _static(W, hidden)  # the first call may set the scratch up
+    assert e == 0 and torch.equal(ids, want_ids)
+    torch.testing.assert_close(mx, want_mx, rtol=0, atol=0)
+    # the calls that follow allocate no device memory: neither through torch nor by the driver
+    torch.cuda.synchronize()
+    before_torch = torch.cuda.memory_allocated()
+    before_free = torch.cuda.mem_get_info()[0]
+    for _ in range(2):  # each call finds the counter the one before left at zero
         ids, mx, e = _static(W, hidden)
         assert e == 0
         assert torch.equal(ids, want_ids)
         torch.testing.assert_close(mx, want_mx, rtol=0, atol=0)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == before_torch
+    assert torch.cuda.mem_get_info()[0] == before_free
 
 
 @pytest.mark.gpu
