@@ -41,7 +41,11 @@ METRIC = "verified rows/s (B*(k+1) rows per verify step); us per verify step; HB
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the kernel as it
 # stands, from one ncu capture on that workload (profiles/); absent where none was taken.
-LMHEAD_TRAFFIC: dict = {}
+LMHEAD_TRAFFIC: dict = {
+    "long_context_fp8": 1_556_650_000 + 3_300_608,               # profiles/lmhead_argmax_long_context_fp8.md
+    "batched_branches_shared_pool": 1_248_504_000 + 3_307_776,   # profiles/lmhead_argmax_batched_branches_shared_pool.md
+    "single_stream_mtp_verify": 622_523_392 + 3_362_048,         # profiles/lmhead_argmax_single_stream_mtp_verify.md
+}
 ATTN_TRAFFIC: dict = {}
 
 

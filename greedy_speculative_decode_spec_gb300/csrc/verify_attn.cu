@@ -1257,7 +1257,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                     constexpr int RSTEP = 128 / CCH;         // rows between a thread's pieces
                     constexpr int NIT = TILE_KEYS / RSTEP;   // pieces per thread
                     constexpr int BATCH = NIT < 4 ? NIT : 4; // pieces loaded together
-                    const int pc = ctid % CCH, row0 = ctid / CCH;
+                    int pc = ctid % CCH, row0 = ctid / CCH;
+                    if (CCH == 8) {
+                        const int g = ctid >> 3, b2 = (ctid >> 2) & 1;
+                        pc = (ctid & 3) + 4 * b2;
+                        row0 = 2 * (g >> 1) + (b2 ^ (g & 1));
+                    }
 #pragma unroll 1
                     for (int i0 = 0; i0 < NIT; i0 += BATCH) {
                         uint4 v[BATCH];
