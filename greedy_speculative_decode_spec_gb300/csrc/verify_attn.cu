@@ -13,7 +13,8 @@
 // 128 keys of a tile sit on the TMEM lanes and the queries on the columns,
 //     S^T[key][q]  = K_tile[key][:] . Q[q][:]            (M = 128 keys, N = NQ >= n_q)
 //     O^T[d][q]   += V_tile^T[d][key] . P^T[key][q]      (M = 128 head-dim lanes)
-//     L[*][q]     += ones[*][key] . P^T[key][q]          (the row sums, on every lane)
+//     L[*][q]     += ones[*][key] . P^T[key][q]          (the row sums, on every lane; the
+//                                                         ones operand is held in TMEM)
 // so the tensor work per tile scales with the real query count, not with a 128-row
 // padding. FP8 pools feed their E4M3 K codes straight into kind::f8f6f4 MMAs: each query
 // is split into two E4M3 terms (q * sigma = hi + lo, sigma a power of two per query), exact
@@ -149,8 +150,9 @@ struct AttnParams {
     int32_t *err;
     uint64_t wait_ns;      // pipeline-wait limit
     int NK, NV, NR, NSB, NPB, QB, OB;  // K, bf16 V and (FP8) raw V ring stages; S, P, Q, O buffers
-    uint32_t off_q, off_q8, off_p, off_ones, off_k, off_v, off_raw, off_ut, off_sx, off_bar, off_small;
+    uint32_t off_q, off_q8, off_p, off_k, off_v, off_raw, off_ut, off_sx, off_bar, off_small;
     uint32_t t_o;          // first TMEM column of the O / L buffers
+    uint32_t t_one;        // first TMEM column of the ones operand (8 bf16 columns, then 8 f16)
 };
 
 // The CTA's mbarriers, as byte offsets from the barrier region (one definition for the
@@ -283,7 +285,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const uint32_t PTILE = (uint32_t)NQ * 256;                                  // a tile's P^T: [NQ/16][128 keys][32 B]
     const uint32_t PBUF = (uint32_t)p.TPI * PTILE;                              // a tile group's
     const uint32_t s_q = s_base + p.off_q, s_q8 = s_base + p.off_q8, s_p = s_base + p.off_p;
-    const uint32_t s_ones = s_base + p.off_ones, s_k = s_base + p.off_k, s_v = s_base + p.off_v;
+    const uint32_t s_k = s_base + p.off_k, s_v = s_base + p.off_v;
     const uint32_t s_raw = s_base + p.off_raw;
     UnitTable *tables = reinterpret_cast<UnitTable *>(smem + p.off_ut);  // [2]
     const BarMap bm = bar_map(p.NK, p.NV, p.NR, p.NSB, p.NPB);
@@ -368,14 +370,6 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             const int blk = i / per, r = i % per;
             *reinterpret_cast<uint4 *>(smem + p.off_q + blk * QATOM + n_q * 128 + r * 16) = make_uint4(0, 0, 0, 0);
         }
-    }
-    // the A operand of the row-sum MMA: 8 rows x 128 bytes of ones (every 8-row group and
-    // every K step of the MMA read this one atom)
-    {
-        // (then the same atom of f16 ones, for units whose P is f16)
-        uint32_t *ones = reinterpret_cast<uint32_t *>(smem + p.off_ones);
-        for (int i = threadIdx.x; i < 512; i += ATT_THREADS) ones[i] = i < 256 ? 0x3F803F80u : 0x3C003C00u;
-        fence_proxy_async_smem();
     }
     if (warp == 8 && lane == 0) {
         prefetch_tmap(&map_q);
@@ -646,7 +640,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             const UnitInfo ui = tables[ub].ui;
             const bool vf16 = FP8 && tables[ub].vf16 != 0;
             const uint32_t idesc_pv = vf16 ? idesc_pv_h : idesc_pv_b, idesc_l = vf16 ? idesc_l_h : idesc_l_b;
-            const uint32_t s_one = s_ones + (vf16 ? 1024u : 0u);
+            const uint32_t t_one = tmem + p.t_one + (vf16 ? 8u : 0u);  // the A operand of the row sums
             __syncwarp();
             if (lane == 0) mbar_arrive(ufree + 8 * ub);
             const uint32_t ob = orr.s;
@@ -683,15 +677,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 }
                 if (!ok) break;
                 if (lane == 0) {
-                    const uint64_t one0 = desc_kmajor(s_one, 128, 0);
 #pragma unroll 1
                     for (int i = 0; i < nt; ++i) {
                         const int t = t0 + i;
                         const uint64_t pa0 = desc_mnmajor_sw32(s_p + pb * PBUF + (uint32_t)i * PTILE, TILE_KEYS * 32);
 #pragma unroll
                         for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
-                            mma_bf16(d_o + S_::NSUB * NQ, desc_advance(one0, (ks & 3) * 32), desc_advance(pa0, ks * 512),
-                                     idesc_l, (t > 0 || ks > 0) ? 1u : 0u);
+                            mma_f16_ta(d_o + S_::NSUB * NQ, t_one, desc_advance(pa0, ks * 512), idesc_l,
+                                       (t > 0 || ks > 0) ? 1u : 0u);
                     }
                     mma_commit(pfree + 8 * pb);  // also: this group's O and L are complete
                 }
@@ -722,6 +715,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         int *my_msk = sx_msk + qd * NQ;
         const float sl = p.scale_log2;
         const int nch = NQ / 16;                 // 16-column chunks
+        {
+            // the A operand of the row-sum MMAs, all ones, in this warp's lane quadrant: 8 columns
+            // of bf16 pairs, then 8 of f16 pairs (ordered before the first row-sum MMA by this
+            // warp's first P hand-off)
+            uint32_t one[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) one[j] = j < 8 ? 0x3F803F80u : 0x3C003C00u;
+            tmem_st16(tmem + lane_base + p.t_one, one);
+            tmem_st_wait();
+        }
         uint32_t ua = 0;                  // units
         RingPos sr, pr, pr_last, orr;     // S buffers, P buffers (and the last group's), O buffers
         uint32_t nx = 0;                  // exchanges among the softmax warps (two barriers, alternating)
@@ -1555,9 +1558,10 @@ static bool make_kv_map(CUtensorMap *map, const void *pool, uint64_t rows, int d
 static uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 // Shared-memory and TMEM plan. In shared memory, in this order (swizzled blocks 1024-aligned):
-// bf16 Q buffers, E4M3 Q parts (FP8), P buffers, the ones atom, ring 0 (bf16 K/V or E4M3 K +
-// raw V), ring 1 (FP8: f16 V), 2 unit tables, softmax scratch, barriers, flags. In TMEM:
-// NSB S buffers of NQ columns, then OB sets of (NSUB O blocks + L) of NQ columns each.
+// bf16 Q buffers, E4M3 Q parts (FP8), P buffers, ring 0 (bf16 K/V or E4M3 K + raw V), ring 1
+// (FP8: f16 V), 2 unit tables, softmax scratch, barriers, flags. In TMEM: NSB S buffers of NQ
+// columns, then OB sets of (NSUB O blocks + L) of NQ columns each, then the 16 columns of the
+// row-sum MMAs' ones operand.
 template <int D, bool FP8>
 static int plan_attn(AttnParams &p, size_t *smem_bytes) {
     using S_ = AttnShape<D, FP8>;
@@ -1576,13 +1580,13 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
         int NSB = 0, OB = 0;
         for (int ob = 2; ob >= 1 && !NSB; --ob)
             for (int nsb = 4 / TPI; nsb >= 2; --nsb)
-                if (nsb * TPI * NQ + ob * (S_::NSUB + 1) * NQ <= 512) {
+                if (nsb * TPI * NQ + ob * (S_::NSUB + 1) * NQ + 16 <= 512) {
                     NSB = nsb;
                     OB = ob;
                     break;
                 }
         if (!NSB) {
-            if (TPI * NQ + (S_::NSUB + 1) * NQ > 512) continue;
+            if (TPI * NQ + (S_::NSUB + 1) * NQ + 16 > 512) continue;
             NSB = 1;
             OB = 1;
         }
@@ -1594,7 +1598,7 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
                     const uint32_t q_bytes = FP8 ? 0 : QB * S_::NATOM_Q * NQ * 128;
                     const uint32_t q8_bytes = FP8 ? QB * 2 * S_::NQ8 * NQ * S_::Q8ROW : 0;
                     const uint32_t p_bytes = NPB * TPI * NQ * 256;
-                    const uint32_t fixed = align_up(q_bytes + q8_bytes + p_bytes, 1024) + 2048;  // + bf16 and f16 ones
+                    const uint32_t fixed = align_up(q_bytes + q8_bytes + p_bytes, 1024);
                     const uint32_t tail = ut_bytes + sx_bytes + bars + small + 32;  // + alignment slack
                     if (1024 + fixed + tail > ATT_SMEM_LIMIT) continue;
                     const uint32_t avail = ATT_SMEM_LIMIT - 1024 - fixed - tail;
@@ -1641,8 +1645,7 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
                     p.off_q = 0;
                     p.off_q8 = p.off_q + q_bytes;
                     p.off_p = p.off_q8 + q8_bytes;
-                    p.off_ones = align_up(p.off_p + p_bytes, 1024);
-                    p.off_k = p.off_ones + 2048;
+                    p.off_k = align_up(p.off_p + p_bytes, 1024);
                     p.off_v = p.off_k + NK * S_::K_STAGE;
                     p.off_raw = p.off_v + NV * S_::OP_STAGE;
                     p.off_ut = p.off_raw + NR * S_::F8_STAGE;
@@ -1650,6 +1653,7 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
                     p.off_bar = align_up(p.off_sx + sx_bytes, 8);
                     p.off_small = p.off_bar + bars;
                     p.t_o = (uint32_t)(NSB * TPI * NQ);
+                    p.t_one = p.t_o + (uint32_t)(OB * (S_::NSUB + 1) * NQ);
                     *smem_bytes = 1024 + p.off_small + small;
                     return SPEC_OK;
                 }
@@ -1852,7 +1856,7 @@ SPEC_API int spec_verify_attn_plan(const spec_kv_desc *kvd, int B, int k, int n_
     if (st) return st;
     const int nsub = kvd->head_dim / (kvd->head_dim < 128 ? kvd->head_dim : 128);
     const int32_t v[SPEC_ATTN_PLAN_FIELDS] = {(int32_t)smem, p.NQ, p.NK, p.NV, p.NR, p.NSB, p.NPB, p.QB, p.OB,
-                                              (int32_t)(p.t_o + p.OB * (nsub + 1) * p.NQ), p.split_keys, p.n_splits,
+                                              (int32_t)(p.t_one + 16), p.split_keys, p.n_splits,
                                               p.n_units, p.TPI, p.tma_rows,
                                               (int32_t)spec::bar_map(p.NK, p.NV, p.NR, p.NSB, p.NPB).end,
                                               (int32_t)spec::BAR_BYTES};

@@ -31,8 +31,8 @@ def _check_plan(pl, P, d, Hkv, G, B, k, max_pos, fp8):
     assert pl["s_buffers"] >= 1 and pl["p_buffers"] in (2, 3) and pl["tile_group"] in (1, 2)
     assert pl["q_buffers"] in (1, 2) and pl["o_buffers"] in (1, 2)
     # TMEM: S buffers of a tile group's nq columns per tile, then per O buffer nsub blocks
-    # of O and one of row sums
-    assert pl["tmem_cols"] == pl["nq"] * (pl["s_buffers"] * pl["tile_group"] + pl["o_buffers"] * (nsub + 1)) <= 512
+    # of O and one of row sums, then 16 columns of the row-sum MMAs' ones operand
+    assert pl["tmem_cols"] == pl["nq"] * (pl["s_buffers"] * pl["tile_group"] + pl["o_buffers"] * (nsub + 1)) + 16 <= 512
     assert pl["barrier_bytes"] <= pl["barrier_bytes_reserved"]
     assert pl["split_keys"] == (256 if Hkv <= 2 else 512 if Hkv <= 4 else 1024)
     assert pl["n_splits"] == -(-max_pos // pl["split_keys"])
