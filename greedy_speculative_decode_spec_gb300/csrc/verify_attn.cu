@@ -257,6 +257,27 @@ __device__ __noinline__ void drain_ring(uint32_t bar0, RingPos r, int n, uint32_
 }
 constexpr uint32_t SLEEP_LOAD = 128;  // loaders, converters, producer
 constexpr uint32_t SLEEP_MMA = 32;    // MMA issuers
+// FP8 TMA lanes (polling probes): a failed probe sleeps, so that the polling warp leaves
+// the issue slots of its SM sub-partition to the softmax and converter warps there
+// (long-context FP8: 264 -> 246 us per call against busy polling)
+constexpr uint32_t SLEEP_POLL = 20;
+
+// The wait of the two FP8 TMA lanes, which share a warp but run their own loops: non-blocking
+// probes (a probe never holds the warp, so the other lane's path keeps being issued), a
+// sleep after each failed one, bounded like every other wait. Inline: an out-of-line call
+// made from the two divergent lanes serialises them, so that one lane's sleep stalls the
+// other.
+__device__ __forceinline__ bool lane_poll_wait(uint32_t bar, uint32_t parity, volatile int *abort, uint64_t timeout_ns) {
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(bar, parity)) return true;
+        __nanosleep(SLEEP_POLL);
+        if ((i & 7u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            if (globaltimer() - t0 > timeout_ns) return false;
+        }
+    }
+}
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, bool f16) {
     if (f16) {
@@ -1080,7 +1101,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             for (;;) {
                 const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
                 const UnitTable *tab = tables + ub;
-                if (!mbar_wait_poll(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
+                if (!lane_poll_wait(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
                 const int it_u = tab->iter;
                 if (it_u < 0) break;
                 const UnitInfo ui = tab->ui;
@@ -1091,7 +1112,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                     if (!is_v && t == max(0, ui.T - 3)) mbar_arrive(lfin + 8 * ub);
                     for (int h = 0; h < S_::NSUB; ++h, ++gi) {
                         const uint32_t s = rr.s;
-                        if (!mbar_wait_poll(empty0 + 8 * s, rr.ph ^ 1u, abort_flag, wns)) {
+                        if (!lane_poll_wait(empty0 + 8 * s, rr.ph ^ 1u, abort_flag, wns)) {
                             ok = false;
                             break;
                         }
