@@ -72,7 +72,7 @@ namespace spec {
 
 using namespace sm100;
 
-constexpr int SPLIT_KEYS = 1024;     // largest split; the split size is split_keys_for(Hkv)
+constexpr int SPLIT_KEYS = 2048;     // largest split; the split size is split_keys_for(Hkv)
 constexpr int TILE_KEYS = 128;
 constexpr int COMBINE_GROUP = 8;     // splits summed in order before the groups are
 constexpr int MAX_NQ = 128;          // query vectors per (branch, kv head), padded to 16
@@ -88,27 +88,42 @@ constexpr uint64_t ATT_WAIT_NS = 1000000000ull;
 constexpr int ATT_SMEM_LIMIT = 227 * 1024;
 constexpr int ATT_THREADS = 384;
 
-constexpr int UT_ENTRIES = SPLIT_KEYS / 8;
 struct UnitInfo {
     int b, g, split, rank, pos_b, kv_end, s0, T, n_used, u;  // u: the unit's workspace slot
     bool bad_pos;
 };
 
 // Per-unit table the producer warp fills: the unit itself (computed once, read by every
-// role), the page of each page-sized run of the split's keys (-1 if the table entry is
-// invalid), the page's FP8 K / V scales, and the error bits of any invalid entry. Pages are
-// listed for pages of >= 8 positions.
+// role), the error bits of any invalid page-table entry, and then, for pages of >= 8
+// positions, E = ceil(split_keys / page_size) entries each of: the page of each page-sized
+// run of the split's keys (-1 if the entry is invalid), and the page's FP8 K and V scales.
+// The plan sizes E; a table is the header followed by its three arrays.
 struct alignas(16) UnitTable {
-    int32_t page[UT_ENTRIES];
-    float ksc[UT_ENTRIES];
-    float vsc[UT_ENTRIES];
     UnitInfo ui;
     int32_t bad;
     int32_t vf16;          // FP8: the unit's P.V runs in f16 (every V page scale keeps code * scale in range)
     int32_t iter;          // the unit's index in the walk order, or -1: no more units
 };
-// the softmax scratch that follows the two tables is read with 16-byte vector loads
+// the arrays (and the softmax scratch that follows the two tables) are read with 16-byte
+// vector loads
 static_assert(sizeof(UnitTable) % 16 == 0, "unit table size must keep 16-byte alignment");
+struct UnitTabView {
+    UnitTable *h;
+    int32_t *page;
+    float *ksc, *vsc;
+};
+__host__ __device__ constexpr uint32_t unit_table_stride(int entries) {
+    return (uint32_t)((sizeof(UnitTable) + 12u * (uint32_t)entries + 15u) & ~15u);
+}
+__device__ __forceinline__ UnitTabView unit_tab(uint8_t *base, uint32_t ub, int entries) {
+    UnitTabView v;
+    uint8_t *t = base + ub * unit_table_stride(entries);
+    v.h = reinterpret_cast<UnitTable *>(t);
+    v.page = reinterpret_cast<int32_t *>(t + sizeof(UnitTable));
+    v.ksc = reinterpret_cast<float *>(v.page + entries);
+    v.vsc = v.ksc + entries;
+    return v;
+}
 
 // Split size in positions, a function of the model's KV-head count only (never of B, k or
 // the context length, so a row's split boundaries are the same in every batch): few KV
@@ -150,6 +165,7 @@ struct AttnParams {
     int32_t *err;
     uint64_t wait_ns;      // pipeline-wait limit
     int NK, NV, NR, NSB, NPB, QB, OB;  // K, bf16 V and (FP8) raw V ring stages; S, P, Q, O buffers
+    int ut_entries;        // page-table entries per unit table (0 for pages of < 8 positions)
     uint32_t off_q, off_q8, off_p, off_k, off_v, off_raw, off_ut, off_sx, off_bar, off_small;
     uint32_t t_o;          // first TMEM column of the O / L buffers
     uint32_t t_one;        // first TMEM column of the ones operand (8 bf16 columns, then 8 f16)
@@ -308,7 +324,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const uint32_t s_q = s_base + p.off_q, s_q8 = s_base + p.off_q8, s_p = s_base + p.off_p;
     const uint32_t s_k = s_base + p.off_k, s_v = s_base + p.off_v;
     const uint32_t s_raw = s_base + p.off_raw;
-    UnitTable *tables = reinterpret_cast<UnitTable *>(smem + p.off_ut);  // [2]
+    uint8_t *ut_base = smem + p.off_ut;  // [2] unit tables
+    const int UTE = p.ut_entries;
     const BarMap bm = bar_map(p.NK, p.NV, p.NR, p.NSB, p.NPB);
     const uint32_t bar0 = s_base + p.off_bar;
     const uint32_t kfull = bar0 + bm.kfull, kempty = bar0 + bm.kempty;
@@ -341,7 +358,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const uint64_t wns = p.wait_ns;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool small_pages = p.kv.page_size < 8;  // more than UT_ENTRIES pages per split
+    const bool small_pages = p.kv.page_size < 8;  // no page-table entries: per-row lookups
     const int log2P = p.kv.log2_page;
 
     if (threadIdx.x == 0) {
@@ -426,7 +443,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         bool ok = true;
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
-            UnitTable *tab = tables + ub;
+            const UnitTabView tv = unit_tab(ut_base, ub, UTE);
+            UnitTable *tab = tv.h;
             if (!warp_wait<SLEEP_LOAD>(ufree + 8 * ub, uph ^ 1u, abort_flag, wns)) { ok = false; break; }
             if (ua > 0 && !warp_wait<SLEEP_LOAD>(lfin + 8 * ((ua - 1) & 1u), ((ua - 1) >> 1) & 1u, abort_flag, wns)) {
                 ok = false;
@@ -472,9 +490,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                         vs = __ldg(p.kv.v_scale + si);
                         v_big |= !(vs >= VF16_MIN_SCALE && vs <= VF16_MAX_SCALE);
                     }
-                    tab->page[e] = pg < 0 ? -1 : pg;
-                    tab->ksc[e] = ks;
-                    tab->vsc[e] = vs;
+                    tv.page[e] = pg < 0 ? -1 : pg;
+                    tv.ksc[e] = ks;
+                    tv.vsc[e] = vs;
                 }
             } else {
                 // pages smaller than 8 positions: the loaders look each row up themselves;
@@ -552,11 +570,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
             if (!warp_wait<SLEEP_MMA>(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
-            const int it_u = tables[ub].iter;
+            const UnitTable *tab = unit_tab(ut_base, ub, UTE).h;
+            const int it_u = tab->iter;
             if (it_u < 0) break;
-            const UnitInfo ui = tables[ub].ui;
-            const int u = ui.u;
-            (void)u;
+            const UnitInfo ui = tab->ui;
             __syncwarp();
             if (lane == 0) mbar_arrive(ufree + 8 * ub);
             const uint32_t qs = qr.s;
@@ -656,10 +673,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
             if (!warp_wait<SLEEP_MMA>(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
-            const int it_u = tables[ub].iter;
+            const UnitTable *tab = unit_tab(ut_base, ub, UTE).h;
+            const int it_u = tab->iter;
             if (it_u < 0) break;
-            const UnitInfo ui = tables[ub].ui;
-            const bool vf16 = FP8 && tables[ub].vf16 != 0;
+            const UnitInfo ui = tab->ui;
+            const bool vf16 = FP8 && tab->vf16 != 0;
             const uint32_t idesc_pv = vf16 ? idesc_pv_h : idesc_pv_b, idesc_l = vf16 ? idesc_l_h : idesc_l_b;
             const uint32_t t_one = tmem + p.t_one + (vf16 ? 8u : 0u);  // the A operand of the row sums
             __syncwarp();
@@ -801,10 +819,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         while (ok) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
             if (!warp_wait(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
-            const UnitTable *tab = tables + ub;
+            const UnitTabView tv = unit_tab(ut_base, ub, UTE);
+            const UnitTable *tab = tv.h;
             const int it_u = tab->iter;
             if (it_u < 0) break;
-            const UnitInfo ui = tables[ub].ui;
+            const UnitInfo ui = tab->ui;
             const int u = ui.u;
             (void)u;
             const bool failed = tab->bad != 0;
@@ -851,8 +870,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 const uint32_t bit1 = (rel1 >= 0 && rel1 < 32) ? 1u << rel1 : 0u;
                 float slk0 = sl, slk1 = sl;
                 if (FP8) {
-                    slk0 = ui.s0 + koff0 < ui.kv_end ? sl * tab->ksc[koff0 >> log2P] : 0.f;
-                    slk1 = nt > 1 && ui.s0 + koff1 < ui.kv_end ? sl * tab->ksc[koff1 >> log2P] : 0.f;
+                    slk0 = ui.s0 + koff0 < ui.kv_end ? sl * tv.ksc[koff0 >> log2P] : 0.f;
+                    slk1 = nt > 1 && ui.s0 + koff1 < ui.kv_end ? sl * tv.ksc[koff1 >> log2P] : 0.f;
                 }
                 const bool vis0 = __all_sync(0xFFFFFFFFu, all0);
                 const bool vis1 = __all_sync(0xFFFFFFFFu, all1);
@@ -1100,7 +1119,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             const int BR = p.tma_rows, nruns = TILE_KEYS / BR;
             for (;;) {
                 const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
-                const UnitTable *tab = tables + ub;
+                const UnitTabView tv = unit_tab(ut_base, ub, UTE);
+                const UnitTable *tab = tv.h;
                 if (!lane_poll_wait(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
                 const int it_u = tab->iter;
                 if (it_u < 0) break;
@@ -1122,13 +1142,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                         for (int r = 0; r < nruns; ++r) {
                             const int kr = key0 + r * BR;
                             if (kr >= ui.kv_end) break;
-                            if (tab->page[(kr - ui.s0) >> log2P] >= 0) bytes += (uint32_t)(BR * S_::SUB);
+                            if (tv.page[(kr - ui.s0) >> log2P] >= 0) bytes += (uint32_t)(BR * S_::SUB);
                         }
                         mbar_arrive_expect_tx(full0 + 8 * s, bytes);
                         for (int r = 0; r < nruns; ++r) {
                             const int kr = key0 + r * BR;
                             if (kr >= ui.kv_end) break;
-                            const int pg = tab->page[(kr - ui.s0) >> log2P];
+                            const int pg = tv.page[(kr - ui.s0) >> log2P];
                             if (pg < 0) continue;
                             const int row = (pg * p.kv.n_kv_heads + ui.g) * p.kv.page_size + (kr & (p.kv.page_size - 1));
                             tma_load_2d(dst_base + (uint32_t)(r * BR) * S_::SUB, map, h * S_::SUB, row, full0 + 8 * s);
@@ -1170,7 +1190,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         bool ok = true;
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
-            const UnitTable *tab = tables + ub;
+            const UnitTabView tv = unit_tab(ut_base, ub, UTE);
+            const UnitTable *tab = tv.h;
             if (!warp_wait<SLEEP_LOAD>(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
             const int it_u = tab->iter;
             if (it_u < 0) break;
@@ -1201,7 +1222,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                         for (int k0 = 0; k0 < NPIECE; k0 += 8) {
                             int pg[8];
 #pragma unroll
-                            for (int k = 0; k < 8; ++k) pg[k] = tab->page[(t * TILE_KEYS + (k0 + k) * RPS + prow0) >> log2P];
+                            for (int k = 0; k < 8; ++k) pg[k] = tv.page[(t * TILE_KEYS + (k0 + k) * RPS + prow0) >> log2P];
 #pragma unroll
                             for (int k = 0; k < 8; ++k) {
                                 const int row = (k0 + k) * RPS + prow0, key = key0 + row;
@@ -1256,7 +1277,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         bool ok = true;
         for (;;) {
             const uint32_t ub = ua & 1u, uph = (ua >> 1) & 1u;
-            const UnitTable *tab = tables + ub;
+            const UnitTabView tv = unit_tab(ut_base, ub, UTE);
+            const UnitTable *tab = tv.h;
             if (!warp_wait<SLEEP_LOAD>(ufull + 8 * ub, uph, abort_flag, wns)) { ok = false; break; }
             const int it_u = tab->iter;
             if (it_u < 0) break;
@@ -1295,7 +1317,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                         for (int i = 0; i < BATCH; ++i) {
                             const int row = row0 + (i0 + i) * RSTEP;
                             v[i] = *reinterpret_cast<const uint4 *>(raw + row * S_::SUB + pc * 16);
-                            vs[i] = tab->vsc[(t * TILE_KEYS + (row < nvk ? row : 0)) >> log2P];
+                            vs[i] = tv.vsc[(t * TILE_KEYS + (row < nvk ? row : 0)) >> log2P];
                         }
 #pragma unroll
                         for (int i = 0; i < BATCH; ++i) {
@@ -1587,7 +1609,9 @@ template <int D, bool FP8>
 static int plan_attn(AttnParams &p, size_t *smem_bytes) {
     using S_ = AttnShape<D, FP8>;
     const int NQ = p.NQ;
-    const uint32_t ut_bytes = 2 * (uint32_t)sizeof(UnitTable);
+    // unit tables: one entry per page-sized run of a split (pages of >= 8 positions)
+    const int ut_entries = p.kv.page_size < 8 ? 0 : (p.split_keys + p.kv.page_size - 1) / p.kv.page_size;
+    const uint32_t ut_bytes = 2 * unit_table_stride(ut_entries);
     const uint32_t sx_bytes = (uint32_t)(8 + 8 + 4 + 4 + 2 + 2) * NQ * 4 + 32;
     const uint32_t bars = BAR_BYTES, small = 64;
     // Tile groups of 2 when the ring holds a whole group's K and V (the S of a group's last
@@ -1656,6 +1680,7 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
                     }
                     if (bar_map(NK, NV, NR, NSB, NPB).end > BAR_BYTES) return SPEC_ERR_UNSUPPORTED;
                     p.TPI = TPI;
+                    p.ut_entries = ut_entries;
                     p.NK = NK;
                     p.NV = NV;
                     p.NR = NR;
