@@ -271,6 +271,8 @@ __device__ __noinline__ void drain_ring(uint32_t bar0, RingPos r, int n, uint32_
         mbar_wait(bar0 + 8 * r.s, r.ph, nullptr, ATT_WAIT_NS);
     }
 }
+// tiles before a unit's end at which its K stream lets the producer take the next unit
+constexpr int NEXT_UNIT_LEAD = 6;
 constexpr uint32_t SLEEP_LOAD = 128;  // loaders, converters, producer
 constexpr uint32_t SLEEP_MMA = 32;    // MMA issuers
 // FP8 TMA lanes (polling probes): a failed probe sleeps, so that the polling warp leaves
@@ -434,10 +436,11 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         // Units are handed out dynamically: the producer takes the next index of the
         // rank-ordered walk from a global counter, skips empty units, and publishes the unit
         // in the shared table that every other role waits on (-1 ends their loops). It takes
-        // a unit only once a table is free and the K loads are issuing the last three tiles of
-        // the previous unit: late enough that a CTA holds little more than the work in its
-        // rings (the last units go to whichever CTAs run out of work first), early enough that
-        // the next unit's table and Q are ready when the loaders get to it.
+        // a unit only once a table is free and the K loads are issuing the last
+        // NEXT_UNIT_LEAD tiles of the previous unit: late enough that a CTA holds little more
+        // than the work in its rings (the last units go to whichever CTAs run out of work
+        // first), early enough that the next unit's table and Q are ready when the loaders
+        // get to it.
         uint32_t ua = 0;
         RingPos qr;  // Q buffers
         bool ok = true;
@@ -1129,7 +1132,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 for (int t = 0; t < ui.T && ok; ++t) {
                     const int key0 = ui.s0 + t * TILE_KEYS;
                     // the producer may prepare the next unit (see the bf16 loaders)
-                    if (!is_v && t == max(0, ui.T - 3)) mbar_arrive(lfin + 8 * ub);
+                    if (!is_v && t == max(0, ui.T - NEXT_UNIT_LEAD)) mbar_arrive(lfin + 8 * ub);
                     for (int h = 0; h < S_::NSUB; ++h, ++gi) {
                         const uint32_t s = rr.s;
                         if (!lane_poll_wait(empty0 + 8 * s, rr.ph ^ 1u, abort_flag, wns)) {
@@ -1199,10 +1202,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             ++ua;
             for (int t = 0; t < ui.T && ok; ++t) {
                 const int key0 = ui.s0 + t * TILE_KEYS;
-                // three tiles before the unit's end the K loaders let the producer prepare the next
-                // unit, so that its table and Q are there when this unit's last copies have been
-                // issued (the K stream runs ahead of the V stream)
-                if (!is_v && t == max(0, ui.T - 3)) {
+                // NEXT_UNIT_LEAD tiles before the unit's end the K loaders let the producer
+                // prepare the next unit, so that its table and Q are there when this unit's last
+                // copies have been issued (the K stream runs ahead of the V stream)
+                if (!is_v && t == max(0, ui.T - NEXT_UNIT_LEAD)) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(lfin + 8 * ub);
                 }
