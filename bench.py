@@ -46,7 +46,10 @@ LMHEAD_TRAFFIC: dict = {
     "batched_branches_shared_pool": 1_248_504_000 + 3_307_776,   # profiles/lmhead_argmax_batched_branches_shared_pool.md
     "single_stream_mtp_verify": 622_523_392 + 3_362_048,         # profiles/lmhead_argmax_single_stream_mtp_verify.md
 }
-ATTN_TRAFFIC: dict = {}
+ATTN_TRAFFIC: dict = {
+    "long_context_fp8": 673_155_328 + 19_923_456,    # profiles/verify_attn_long_context_fp8.md
+    "single_stream_mtp_verify": 8_535_552 + 0,       # profiles/verify_attn_single_stream_mtp_verify.md
+}
 
 
 def _peaks():

@@ -72,7 +72,7 @@ namespace spec {
 
 using namespace sm100;
 
-constexpr int SPLIT_KEYS = 2048;     // largest split; the split size is split_keys_for(Hkv)
+constexpr int SPLIT_KEYS = 2048;     // largest split; the split size is split_keys_for(Hkv, dtype)
 constexpr int TILE_KEYS = 128;
 constexpr int COMBINE_GROUP = 8;     // splits summed in order before the groups are
 constexpr int MAX_NQ = 128;          // query vectors per (branch, kv head), padded to 16
@@ -125,11 +125,14 @@ __device__ __forceinline__ UnitTabView unit_tab(uint8_t *base, uint32_t ub, int 
     return v;
 }
 
-// Split size in positions, a function of the model's KV-head count only (never of B, k or
-// the context length, so a row's split boundaries are the same in every batch): few KV
-// heads give few work units per branch, so their splits are shorter.
-__host__ __device__ constexpr int split_keys_for(int n_kv_heads) {
-    return n_kv_heads <= 2 ? 256 : (n_kv_heads <= 4 ? 512 : SPLIT_KEYS);
+// Split size in positions, a function of the KV pool's shape only (its KV-head count and
+// element type; never of B, k or the context length, so a row's split boundaries are the
+// same in every batch): few KV heads give few work units per branch, so their splits are
+// shorter; with more, a split holds about 512 KB of K and V at a head dimension of 128
+// (2048 E4M3 positions, 1024 bf16 ones), long enough that a unit's fixed costs are small
+// against its tiles, short enough that the units balance across the SMs.
+__host__ __device__ constexpr int split_keys_for(int n_kv_heads, bool fp8) {
+    return n_kv_heads <= 2 ? 256 : (n_kv_heads <= 4 ? 512 : (fp8 ? SPLIT_KEYS : SPLIT_KEYS / 2));
 }
 
 template <int D, bool FP8>
@@ -1864,7 +1867,7 @@ static int attn_setup(const spec_kv_desc *kvd, int B, int k, int n_q_heads, int 
     p.G = G;
     p.n_q = n_q;
     p.NQ = NQ;
-    p.split_keys = split_keys_for(kvd->n_kv_heads);
+    p.split_keys = split_keys_for(kvd->n_kv_heads, kvd->kv_dtype == SPEC_KV_FP8_E4M3);
     p.n_splits = (max_pos + p.split_keys - 1) / p.split_keys;
     p.max_pos = max_pos;
     p.n_units = B * kvd->n_kv_heads * p.n_splits;
@@ -1918,7 +1921,7 @@ SPEC_API size_t spec_verify_attn_workspace(const spec_kv_desc *kv, int B, int k,
     if (n_q_heads % kv->n_kv_heads) return 0;
     const int G = n_q_heads / kv->n_kv_heads;
     const int NQ = (((k + 1) * G + 15) / 16) * 16;
-    const int sk = spec::split_keys_for(kv->n_kv_heads);
+    const int sk = spec::split_keys_for(kv->n_kv_heads, kv->kv_dtype == SPEC_KV_FP8_E4M3);
     const int n_splits = (max_pos + sk - 1) / sk;
     return spec::ws_layout(B, kv->n_kv_heads, n_splits, NQ, kv->head_dim, kv->kv_dtype == SPEC_KV_FP8_E4M3).total;
 }

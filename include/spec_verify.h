@@ -161,7 +161,7 @@ int spec_verify_attn_plan(const spec_kv_desc *kv, int B, int k, int n_q_heads, i
  * ("query row r attends to keys [0..base_len+r+1)"); DSSD-dev fast.py,
  * `_attention` (per-row exact key path).
  * Split-KV: keys are cut into fixed splits of 256 positions (n_kv_heads <= 2),
- * 512 (n_kv_heads <= 4) or 2048 (otherwise): a function of the model's shape
+ * 512 (n_kv_heads <= 4), else 1024 (bf16) or 2048 (E4M3): a function of the pool's shape
  * only, independent of B, k and context, so a row's output is byte-identical
  * whatever batch it is verified in (memra-engine spec.rs, `MtpScratch`: fixed
  * split geometry). The splits are merged inside the same launch.

@@ -34,7 +34,7 @@ def _check_plan(pl, P, d, Hkv, G, B, k, max_pos, fp8):
     # of O and one of row sums, then 16 columns of the row-sum MMAs' ones operand
     assert pl["tmem_cols"] == pl["nq"] * (pl["s_buffers"] * pl["tile_group"] + pl["o_buffers"] * (nsub + 1)) + 16 <= 512
     assert pl["barrier_bytes"] <= pl["barrier_bytes_reserved"]
-    assert pl["split_keys"] == (256 if Hkv <= 2 else 512 if Hkv <= 4 else 2048)
+    assert pl["split_keys"] == (256 if Hkv <= 2 else 512 if Hkv <= 4 else (2048 if fp8 else 1024))
     assert pl["n_splits"] == -(-max_pos // pl["split_keys"])
     assert pl["n_units"] == B * Hkv * pl["n_splits"]
     assert pl["tma_rows"] == (min(P, 128) if fp8 else 0)
@@ -80,7 +80,7 @@ def test_plans_of_the_benchmark_workloads():
     """The plans the measured numbers were taken with (see the ncu summaries)."""
     want = {
         "single_stream_mtp_verify": dict(nq=48, split_keys=256, tma_rows=0),
-        "batched_branches_shared_pool": dict(nq=32, tile_group=2, s_buffers=2, o_buffers=2, split_keys=2048,
+        "batched_branches_shared_pool": dict(nq=32, tile_group=2, s_buffers=2, o_buffers=2, split_keys=1024,
                                              tma_rows=0),
         "long_context_fp8": dict(nq=32, tile_group=2, s_buffers=2, split_keys=2048, tma_rows=64),
     }
