@@ -49,6 +49,7 @@ LMHEAD_TRAFFIC: dict = {
 ATTN_TRAFFIC: dict = {
     "long_context_fp8": 673_155_328 + 19_923_456,    # profiles/verify_attn_long_context_fp8.md
     "single_stream_mtp_verify": 8_535_552 + 0,       # profiles/verify_attn_single_stream_mtp_verify.md
+    "batched_branches_shared_pool": 272_015_360 + 6_432_000,  # profiles/verify_attn_batched_branches_shared_pool.md
 }
 
 
