@@ -21,6 +21,7 @@ STATUS = {-1: "SPEC_ERR_NULL", -2: "SPEC_ERR_ARG", -3: "SPEC_ERR_UNSUPPORTED", -
           -5: "SPEC_ERR_CUDA", -6: "SPEC_ERR_ALIGN"}
 DEVERR_PAGE, DEVERR_COVER, DEVERR_TOKEN, DEVERR_D2T, DEVERR_POS, DEVERR_TIMEOUT, DEVERR_INTERNAL = 1, 2, 4, 8, 16, 32, 64
 DEVERR_TREE = 128
+DEVERR_SLOT = 256
 KMAX = 15
 KV_BF16, KV_FP8_E4M3 = 0, 1
 
@@ -37,7 +38,7 @@ EXPORTS = ("spec_strerror", "spec_version", "spec_kv_append", "spec_kv_write_row
            "spec_lmhead_argmax", "spec_lmhead_logits", "spec_accept", "spec_mtp_input_workspace",
            "spec_mtp_input", "spec_lmhead_argmax_static", "spec_accept_stop", "spec_verify_attn_plan",
            "spec_test_set_wait_limit", "spec_accept_sample", "spec_verify_attn_tree", "spec_accept_tree",
-           "spec_kv_compact")
+           "spec_kv_compact", "spec_h_gather", "spec_h_scatter")
 
 
 class SpecError(RuntimeError):
@@ -89,6 +90,8 @@ def lib() -> ctypes.CDLL:
         L.spec_verify_attn_tree.argtypes = [_KVP, _vp, _i32, _i32, _i32, _vp, _f32, _vp, _vp, _vp, _sz, _i32, _vp, _vp]
         L.spec_accept_tree.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         L.spec_kv_compact.argtypes = [_KVP, _vp, _vp, _vp, _i32, _i32, _vp, _vp]
+        L.spec_h_gather.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp]
+        L.spec_h_scatter.argtypes = [_vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp]
         L.spec_test_set_wait_limit.argtypes = [ctypes.c_uint64]
         L.spec_test_set_wait_limit.restype = None
         L.spec_mtp_input_workspace.restype = _sz
@@ -308,6 +311,22 @@ def spec_kv_compact(kv: spec_kv_desc, pos, path, accepted, B: int, k: int, dev_e
     _check("spec_kv_compact", lib().spec_kv_compact(
         ctypes.byref(kv), _ptr(pos, "pos", torch.int32), _ptr(path, "path", torch.int32),
         _ptr(accepted, "accepted", torch.int32), B, k, _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
+
+
+def spec_h_gather(h_out, hpool, hslot, dev_err=None, stream=None):
+    """h_out[b] = hpool[hslot[b]] (bf16 rows)."""
+    B, H = h_out.shape
+    _check("spec_h_gather", lib().spec_h_gather(
+        _ptr(h_out, "h_out", torch.bfloat16), _ptr(hpool, "hpool", torch.bfloat16), _ptr(hslot, "hslot", torch.int32),
+        B, H, int(hpool.shape[0]), _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
+
+
+def spec_h_scatter(hpool, h_in, hslot, dev_err=None, stream=None):
+    """hpool[hslot[b]] = h_in[b] (bf16 rows; distinct slots)."""
+    B, H = h_in.shape
+    _check("spec_h_scatter", lib().spec_h_scatter(
+        _ptr(hpool, "hpool", torch.bfloat16), _ptr(h_in, "h_in", torch.bfloat16), _ptr(hslot, "hslot", torch.int32),
+        B, H, int(hpool.shape[0]), _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
 
 
 def spec_test_set_wait_limit(ns: int) -> None:

@@ -103,3 +103,43 @@ class VerifyStep:
             bnd.spec_mtp_input(o.next_tok, m["E"], o.h_next, m["g_emb"], m["g_hid"], m["eps"], m["W_fc"], o.mtp_x,
                                self.mtp_ws, o.dev_err, stream)
         return o
+
+
+class StepGraphCache:
+    """CUDA graphs of a step, one per key, e.g. (k, B, splits) (span-02
+    engine/crates/model/src/spec.rs, `Spec::step_chunk`: a graph cache keyed by the step's
+    shape, eager execution when capture fails).
+
+    run(key, step) executes the step once per call: the first call for a key runs it
+    eagerly (which also warms the libraries up), the second captures it and replays the
+    graph, later calls replay it. The step must use the same device buffers on every call
+    (its state, such as positions advanced in place by spec_accept, lives in them); a key
+    whose capture raised runs eagerly from then on."""
+
+    def __init__(self):
+        self._graphs: dict = {}
+        self._seen: set = set()
+        self._eager: set = set()
+
+    def run(self, key, step) -> None:
+        g = self._graphs.get(key)
+        if g is not None:
+            g.replay()
+            return
+        if key in self._eager or key not in self._seen:
+            self._seen.add(key)
+            step()
+            return
+        g = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(g):
+                step()
+        except RuntimeError:
+            self._eager.add(key)
+            step()
+            return
+        self._graphs[key] = g
+        g.replay()
+
+    def captured(self, key) -> bool:
+        return key in self._graphs

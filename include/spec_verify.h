@@ -80,6 +80,7 @@ typedef struct CUstream_st *spec_stream_t;
 #define SPEC_DEVERR_TIMEOUT  32  /* a bounded pipeline wait gave up (results invalid)   */
 #define SPEC_DEVERR_INTERNAL 64  /* an internal consistency check failed; the access was skipped */
 #define SPEC_DEVERR_TREE     128 /* a tree parent outside [0, row) or a path entry out of order */
+#define SPEC_DEVERR_SLOT     256 /* a hidden-pool slot outside [0, n_slots)             */
 
 /* ---- limits ------------------------------------------------------------------------ */
 #define SPEC_KMAX            15  /* k <= 15: at most 16 verify rows per branch          */
@@ -361,6 +362,23 @@ int spec_accept_sample(const int32_t *drafts, const float *logits, const float *
                        int k, int V, float temperature, const float *u_acc, const float *u_res,
                        int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted, int32_t *out_pos,
                        int32_t *out_next, int32_t *dev_err, spec_stream_t stream);
+
+/* ---- f1: the draft head's remembered hidden rows ----------------------------------
+ * Each branch b owns slot hslot[b] of a pool of hidden rows. A step gathers the draft
+ * head's input rows h[b] = hpool[hslot[b]] before drafting, and scatters the rows the
+ * acceptance wrote (spec_accept's h_out) back, hpool[hslot[b]] = h[b], after it. Sources:
+ * span-02 engine/crates/model/src/spec.rs, `Spec::body_inner` (`spec_h_gather` at the start
+ * of a step, `spec_h_scatter` at its end).
+ *   hpool  device bf16 [n_slots][H];  hslot  device int32 [B];  h_out / h_in  device bf16
+ *          [B][H] (16-byte aligned rows with H % 8 == 0 copy by 16-byte vectors)
+ *   spec_h_scatter: slots must be distinct (with a repeated slot, which row lands there is
+ *   unspecified).
+ * Host errors: NULL, B < 1, H < 1, n_slots < 1.
+ * Device errors: SPEC_DEVERR_SLOT for a slot outside [0, n_slots); that row is skipped. */
+int spec_h_gather(void *h_out, const void *hpool, const int32_t *hslot, int B, int H, int n_slots,
+                  int32_t *dev_err, spec_stream_t stream);
+int spec_h_scatter(void *hpool, const void *h_in, const int32_t *hslot, int B, int H, int n_slots,
+                   int32_t *dev_err, spec_stream_t stream);
 
 /* ---- a5: MTP draft-head input -----------------------------------------------------
  *   c[m]  = [ rmsnorm(E[tok[m]]; g_emb) ; rmsnorm(h[m]; g_hid) ]  rounded to bf16

@@ -19,7 +19,7 @@ _HERE = Path(__file__).resolve().parent
 _SRC = _HERE / "oracle.c"
 _LIB = _HERE / "liboracle.so"
 
-ERR_PAGE, ERR_COVER, ERR_TOKEN, ERR_D2T, ERR_POS, ERR_TREE = 1, 2, 4, 8, 16, 32
+ERR_PAGE, ERR_COVER, ERR_TOKEN, ERR_D2T, ERR_POS, ERR_TREE, ERR_SLOT = 1, 2, 4, 8, 16, 32, 64
 
 
 def build(force: bool = False) -> Path:
@@ -86,6 +86,8 @@ def lib():
         _lib.orc_accept_sample.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int] * 3 + [ctypes.c_double]
                                            + [ctypes.c_void_p] * 7)
         _lib.orc_accept_sample.restype = ctypes.c_int
+        _lib.orc_h_gather.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3
+        _lib.orc_h_scatter.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 3
         _lib.orc_accept_stop.argtypes = ([ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                           ctypes.c_int] + [ctypes.c_void_p] * 7)
         _lib.orc_mtp_input.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_double, ctypes.c_void_p, ctypes.c_int,
@@ -225,6 +227,24 @@ def accept_sample(drafts, logits, q, pos, B: int, k: int, temperature: float, u_
     err = lib().orc_accept_sample(_p(drafts), _p(logits), _p(q), _p(pos), B, k, V, float(temperature), _p(u_acc),
                                   _p(u_res), _p(tokens), _p(n), _p(a), _p(npos), _p(nxt))
     return tokens, n, a, npos, nxt, int(err)
+
+
+def h_gather(hpool, hslot):
+    """(rows [B][H] uint16 with hpool[hslot[b]] (zero where the slot is invalid), error bits)."""
+    hpool = _c(hpool, np.uint16)
+    hslot = _c(hslot, np.int32)
+    n_slots, H = hpool.shape
+    out = np.zeros((len(hslot), H), np.uint16)
+    err = lib().orc_h_gather(_p(out), _p(hpool), _p(hslot), len(hslot), H, n_slots)
+    return out, int(err)
+
+
+def h_scatter(hpool, h_in, hslot) -> int:
+    """hpool[hslot[b]] = h_in[b] in place (uint16 arrays); returns the error bits."""
+    assert hpool.dtype == np.uint16 and hpool.flags.c_contiguous
+    h_in, hslot = _c(h_in, np.uint16), _c(hslot, np.int32)
+    n_slots, H = hpool.shape
+    return int(lib().orc_h_scatter(_p(hpool), _p(h_in), _p(hslot), len(hslot), H, n_slots))
 
 
 def kv_compact(kv: KvPool, pos, path, accepted, B: int, k: int) -> int:

@@ -49,6 +49,7 @@
 #define ORC_ERR_D2T 8
 #define ORC_ERR_POS 16
 #define ORC_ERR_TREE 32
+#define ORC_ERR_SLOT 64
 
 int orc_threads(void) {
 #ifdef _OPENMP
@@ -760,6 +761,38 @@ int orc_mtp_input(const int32_t *tok, const uint16_t *E, const uint16_t *h, cons
         double acc = 0.0;
         for (int i = 0; i < 2 * H; ++i) acc += orc_bf16_to_double(w[i]) * orc_bf16_to_double(c[i]);
         x_out[item] = acc;
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------------------------
+ * The draft head's remembered hidden rows (span-02 engine/crates/model/src/spec.rs,
+ * `Spec::body_inner`): a step gathers h[b] = hpool[hslot[b]] before drafting and scatters
+ * the acceptance's rows back, hpool[hslot[b]] = h[b], after it. Rows are bf16 bit patterns,
+ * copied as they are; a slot outside [0, n_slots) is an error bit and its row is skipped.
+ * ---------------------------------------------------------------------------------- */
+int orc_h_gather(uint16_t *h_out, const uint16_t *hpool, const int32_t *hslot, int B, int H, int n_slots) {
+    int err = 0;
+    for (int b = 0; b < B; ++b) {
+        const int s = hslot[b];
+        if (s < 0 || s >= n_slots) {
+            err |= ORC_ERR_SLOT;
+            continue;
+        }
+        for (int i = 0; i < H; ++i) h_out[(size_t)b * H + i] = hpool[(size_t)s * H + i];
+    }
+    return err;
+}
+
+int orc_h_scatter(uint16_t *hpool, const uint16_t *h_in, const int32_t *hslot, int B, int H, int n_slots) {
+    int err = 0;
+    for (int b = 0; b < B; ++b) {
+        const int s = hslot[b];
+        if (s < 0 || s >= n_slots) {
+            err |= ORC_ERR_SLOT;
+            continue;
+        }
+        for (int i = 0; i < H; ++i) hpool[(size_t)s * H + i] = h_in[(size_t)b * H + i];
     }
     return err;
 }

@@ -520,3 +520,35 @@ def test_spec_stream_equals_one_row_greedy(orc, k):
     assert got0 == got
     for a1, a0 in zip(side.attn_log, side0.attn_log):
         np.testing.assert_array_equal(a1, a0)
+
+
+def test_hidden_pool_gather_scatter_are_fancy_indexing(orc):
+    """h_gather is numpy's row indexing hpool[hslot]; h_scatter is hpool[hslot] = h (distinct
+    slots); an invalid slot is reported and its row skipped; scatter then gather returns the
+    scattered rows (span-02 `Spec::body_inner`: gather at a step's start, scatter at its end)."""
+    rng = np.random.default_rng(77)
+    S, H, B = 37, 33, 9
+    hpool = rng.integers(0, 1 << 16, (S, H)).astype(np.uint16)
+    hslot = rng.permutation(S)[:B].astype(np.int32)
+    got, err = orc.h_gather(hpool, hslot)
+    assert err == 0 and np.array_equal(got, hpool[hslot])
+    h_new = rng.integers(0, 1 << 16, (B, H)).astype(np.uint16)
+    pool2 = hpool.copy()
+    assert orc.h_scatter(pool2, h_new, hslot) == 0
+    want = hpool.copy()
+    want[hslot] = h_new
+    assert np.array_equal(pool2, want)
+    back, err = orc.h_gather(pool2, hslot)
+    assert err == 0 and np.array_equal(back, h_new)
+    bad = hslot.copy()
+    bad[2], bad[5] = -1, S
+    got, err = orc.h_gather(hpool, bad)
+    assert err == orc.ERR_SLOT
+    ok = np.ones(B, bool)
+    ok[[2, 5]] = False
+    assert np.array_equal(got[ok], hpool[bad[ok]]) and not got[~ok].any()
+    pool3 = hpool.copy()
+    assert orc.h_scatter(pool3, h_new, bad) == orc.ERR_SLOT
+    want = hpool.copy()
+    want[bad[ok]] = h_new[ok]
+    assert np.array_equal(pool3, want)
