@@ -1832,13 +1832,13 @@ static WsLayout ws_layout(int B, int Hkv, int n_splits, int NQ, int d, bool fp8)
     return w;
 }
 
-// The combine grid: W = warps per (row, head) item, ceil(splits / COMBINE_GROUP) rounded up
-// to a power of two (at most 16); 8 / W items per CTA when W < 8.
+// The combine grid: W = warps per (row, head) item, one per group of COMBINE_GROUP splits
+// (at most 16; a power of two would leave warps idle and, for long rows, need a second
+// wave of CTAs); 8 / W items per CTA when W < 8.
 template <int D>
 static int launch_combine(const AttnParams &p, cudaStream_t s) {
     const int ng_max = (p.n_splits + COMBINE_GROUP - 1) / COMBINE_GROUP;
-    int W = 1;
-    while (W < ng_max && W < 16) W <<= 1;
+    const int W = ng_max < 16 ? ng_max : 16;
     const int ipc = W >= 8 ? 1 : 8 / W;
     const int items = p.B * (p.k + 1) * p.Hq;
     const int grid = (items + ipc - 1) / ipc;
