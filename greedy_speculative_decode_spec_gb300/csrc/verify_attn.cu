@@ -1717,7 +1717,8 @@ static int plan_attn(AttnParams &p, size_t *smem_bytes) {
 // terms, q * sigma = hi + lo with sigma = 2^e chosen so that max|q * sigma| lies in [128, 256)
 // (clamped to 2^-126..2^126): exact for every element within 2^10 of the vector's largest.
 // Written as [pair][hi, lo][NQ][d] bytes (padding rows zero) with 1/sigma per column, for the
-// attention kernel to load by TMA. One CTA per (branch, kv head), a warp per query vector.
+// attention kernel to load by TMA. Grid (branch and kv head, NQ / 4): a warp per query
+// vector, so that every vector's load, maximum and conversion run at once.
 template <int D>
 __global__ void __launch_bounds__(128) attn_qsplit_kernel(const uint16_t *__restrict__ q, int B, int k, int Hq,
                                                           int G, int Hkv, int NQ, uint8_t *q8, float *qinv) {
@@ -1726,7 +1727,7 @@ __global__ void __launch_bounds__(128) attn_qsplit_kernel(const uint16_t *__rest
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_q = (k + 1) * G;
     constexpr int EL = D / 32;  // elements per lane
-    for (int r = warp; r < NQ; r += 4) {
+    for (int r = blockIdx.y * 4 + warp; r < NQ; r += 4 * gridDim.y) {
         float x[EL];
         if (r < n_q) {
             const uint16_t *src = q + ((size_t)(b * (k + 1) + r / G) * Hq + g * G + r % G) * D + lane * EL;
@@ -1789,7 +1790,7 @@ static int launch_attn(AttnParams &p, cudaStream_t s) {
     if (FP8) {
         // the queries' E4M3 split, written to the workspace by a kernel of its own
         const int pairs = p.B * p.kv.n_kv_heads;
-        const int st2 = launch_pdl(attn_qsplit_kernel<D>, dim3(pairs), dim3(128), 0, s, p.q, p.B, p.k, p.Hq, p.G,
+        const int st2 = launch_pdl(attn_qsplit_kernel<D>, dim3(pairs, p.NQ / 4), dim3(128), 0, s, p.q, p.B, p.k, p.Hq, p.G,
                                    p.kv.n_kv_heads, p.NQ, p.q8_g, const_cast<float *>(p.qinv_g));
         if (st2) return st2;
         if (!make_q8_map(&mq, p.q8_g, (uint64_t)pairs * 2 * p.NQ, D, p.NQ)) return SPEC_ERR_CUDA;

@@ -278,6 +278,17 @@ def test_attention_edge_shapes(P, d, k, B):
     _step_parity(vi, full_oracle=True)
 
 
+@pytest.mark.parametrize("P,d,k,B,G", [(8, 64, 3, 2, 2), (64, 256, 1, 2, 4), (16, 128, 15, 2, 2), (8, 128, 0, 1, 5)])
+def test_attention_edge_shapes_fp8(P, d, k, B, G):
+    """E4M3 pools at every head dimension (the queries' E4M3 split is written straight into
+    the 128- or 64-byte-swizzled operand layout), pages down to 8 positions, k = 0 and 15."""
+    cfg = scaled(WORKLOADS["tiny_verify"], B=B, k=k, P=P, d=d, Hq=2 * G, Hkv=2, ctx=tuple([3, 1030, 5][:B]),
+                 num_pages=0, permute_all_pages=False, accept_p=(0.7,) * k, V=64, H=256, kv_dtype="fp8",
+                 seed=70 + P + k + d)
+    vi = verify_inputs(cfg)
+    _step_parity(vi, full_oracle=True)
+
+
 def test_accept_random_patterns_max_k():
     rng = np.random.default_rng(9)
     for B, k in ((16, 15), (7, 1), (3, 0), (32, 6)):
