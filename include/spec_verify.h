@@ -13,6 +13,7 @@
  *   spec_accept_stop    greedy chain acceptance with stop tokens and a generation budget
  *   spec_accept_sample  speculative sampling acceptance (random numbers as inputs)
  *   spec_verify_attn_tree, spec_accept_tree, spec_kv_compact   tree / star verify
+ *   spec_h_gather, spec_h_scatter   the draft head's remembered hidden rows (slot pool)
  *   spec_mtp_input      the draft head's input  fc([rmsnorm(E[tok]), rmsnorm(h)])
  *
  * The method follows the span-02 page `engine/crates/model/src/spec.rs`
