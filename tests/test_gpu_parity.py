@@ -127,8 +127,9 @@ def test_step_parity_full_size(name):
 
 # ---- row invariance: a row's result does not depend on the batch it is verified in ---------
 
-def test_attention_rows_bytewise_equal_one_row_calls():
-    vi = verify_inputs(SMALL["branches"])
+@pytest.mark.parametrize("name", ["branches", "long_fp8"])
+def test_attention_rows_bytewise_equal_one_row_calls(name):
+    vi = verify_inputs(SMALL[name])
     c = vi.cfg
     gkv = gpu_pool(vi)
     pos_d = vi.pos.cuda()
@@ -137,7 +138,7 @@ def test_attention_rows_bytewise_equal_one_row_calls():
     out, e = gpu_attention(gkv, pos_d, c.B, c.k, c.Hq, q, vi.max_pos + 3000)
     assert e == 0
     for b in range(c.B):
-        desc1 = bnd.make_kv_desc(gkv.k, gkv.v, gkv.page_table[b:b + 1].contiguous(), c.P)
+        desc1 = bnd.make_kv_desc(gkv.k, gkv.v, gkv.page_table[b:b + 1].contiguous(), c.P, gkv.k_scale, gkv.v_scale)
         one = type(gkv).__new__(type(gkv))
         one.__dict__.update(gkv.__dict__)
         one.desc = desc1
