@@ -596,46 +596,45 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 }
 #pragma unroll 1
                 for (int i = 0; i < nt && ok; ++i) {
-                const int t = t0 + i;
 #pragma unroll
-                for (int h = 0; h < S_::NSUB; ++h) {
-                    const uint32_t st = kr.s;
-                    if (!warp_wait<SLEEP_MMA>(kfull + 8 * st, kr.ph, abort_flag, wns)) { ok = false; break; }
-                    kr.next(p.NK);
-                    ++gk;
-                    if (!FP8) fence_proxy_async_smem();  // cp.async data -> tensor core reads
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t kb = s_k + st * S_::K_STAGE;
-                        const uint32_t d_s = tmem + (sb * (uint32_t)p.TPI + (uint32_t)i) * (uint32_t)NQ;
-                        if (FP8) {
-                            // S = K . (hi + lo)^T: both E4M3 parts accumulate into one S
-                            const uint64_t ka0 = desc_kmajor(kb, S_::K8ROW, 8 * S_::K8ROW);
-                            const uint64_t qa0 = desc_kmajor(s_q8 + qs * 2 * Q8PART, S_::Q8ROW, 8 * S_::Q8ROW);
+                    for (int h = 0; h < S_::NSUB; ++h) {
+                        const uint32_t st = kr.s;
+                        if (!warp_wait<SLEEP_MMA>(kfull + 8 * st, kr.ph, abort_flag, wns)) { ok = false; break; }
+                        kr.next(p.NK);
+                        ++gk;
+                        if (!FP8) fence_proxy_async_smem();  // cp.async data -> tensor core reads
+                        tc_fence_after();
+                        if (lane == 0) {
+                            const uint32_t kb = s_k + st * S_::K_STAGE;
+                            const uint32_t d_s = tmem + (sb * (uint32_t)p.TPI + (uint32_t)i) * (uint32_t)NQ;
+                            if (FP8) {
+                                // S = K . (hi + lo)^T: both E4M3 parts accumulate into one S
+                                const uint64_t ka0 = desc_kmajor(kb, S_::K8ROW, 8 * S_::K8ROW);
+                                const uint64_t qa0 = desc_kmajor(s_q8 + qs * 2 * Q8PART, S_::Q8ROW, 8 * S_::Q8ROW);
 #pragma unroll
-                            for (int part = 0; part < 2; ++part) {
+                                for (int part = 0; part < 2; ++part) {
 #pragma unroll
-                                for (int kl = 0; kl < S_::SUB / 32; ++kl) {
-                                    const int ks = h * (S_::SUB / 32) + kl;  // 32-byte step over all of d
-                                    const uint32_t qoff = S_::Q8ROW == 128 ? (ks >> 2) * Q8ATOM + (ks & 3) * 32
-                                                                           : (uint32_t)ks * 32;
-                                    mma_f8(d_s, desc_advance(ka0, kl * 32), desc_advance(qa0, part * Q8PART + qoff), idesc,
-                                           (h > 0 || part > 0 || kl > 0) ? 1u : 0u);
+                                    for (int kl = 0; kl < S_::SUB / 32; ++kl) {
+                                        const int ks = h * (S_::SUB / 32) + kl;  // 32-byte step over all of d
+                                        const uint32_t qoff = S_::Q8ROW == 128 ? (ks >> 2) * Q8ATOM + (ks & 3) * 32
+                                                                               : (uint32_t)ks * 32;
+                                        mma_f8(d_s, desc_advance(ka0, kl * 32), desc_advance(qa0, part * Q8PART + qoff), idesc,
+                                               (h > 0 || part > 0 || kl > 0) ? 1u : 0u);
+                                    }
+                                }
+                            } else {
+                                const uint64_t ka0 = desc_kmajor(kb, 128, 1024), qb0 = desc_kmajor(s_q + qs * QBUF, 128, 1024);
+#pragma unroll
+                                for (int kl = 0; kl < S_::SUB / 16; ++kl) {
+                                    const int ks = h * (S_::SUB / 16) + kl;  // 16-element step over all of d
+                                    mma_bf16(d_s, desc_advance(ka0, (kl >> 2) * (TILE_KEYS * 128) + (kl & 3) * 32),
+                                             desc_advance(qb0, (ks >> 2) * QATOM + (ks & 3) * 32), idesc, ks > 0 ? 1u : 0u);
                                 }
                             }
-                        } else {
-                            const uint64_t ka0 = desc_kmajor(kb, 128, 1024), qb0 = desc_kmajor(s_q + qs * QBUF, 128, 1024);
-#pragma unroll
-                            for (int kl = 0; kl < S_::SUB / 16; ++kl) {
-                                const int ks = h * (S_::SUB / 16) + kl;  // 16-element step over all of d
-                                mma_bf16(d_s, desc_advance(ka0, (kl >> 2) * (TILE_KEYS * 128) + (kl & 3) * 32),
-                                         desc_advance(qb0, (ks >> 2) * QATOM + (ks & 3) * 32), idesc, ks > 0 ? 1u : 0u);
-                            }
+                            mma_commit(kempty + 8 * st);
                         }
-                        mma_commit(kempty + 8 * st);
+                        __syncwarp();
                     }
-                    __syncwarp();
-                }
                 }
                 if (!ok) break;
                 if (lane == 0) {
@@ -698,27 +697,27 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 if (!warp_wait<SLEEP_MMA>(pfull + 8 * pb, pr.ph, abort_flag, wns)) { ok = false; break; }
 #pragma unroll 1
                 for (int i = 0; i < nt && ok; ++i) {
-                const int t = t0 + i;
-                const uint32_t pa = s_p + pb * PBUF + (uint32_t)i * PTILE;
+                    const int t = t0 + i;
+                    const uint32_t pa = s_p + pb * PBUF + (uint32_t)i * PTILE;
 #pragma unroll
-                for (int h = 0; h < S_::NSUB; ++h) {
-                    const uint32_t st = vr.s;
-                    if (!warp_wait<SLEEP_MMA>(vfull + 8 * st, vr.ph, abort_flag, wns)) { ok = false; break; }
-                    if (!FP8) fence_proxy_async_smem();  // cp.async data -> tensor core reads
-                    const uint32_t vb = s_v + st * S_::OP_STAGE, rel = vempty + 8 * st;
-                    ++gv;
-                    vr.next(p.NV);
-                    tc_fence_after();
-                    if (lane == 0) {
-                        const uint64_t va0 = desc_mnmajor_sw128(vb, v_lbo), pa0 = desc_mnmajor_sw32(pa, TILE_KEYS * 32);
+                    for (int h = 0; h < S_::NSUB; ++h) {
+                        const uint32_t st = vr.s;
+                        if (!warp_wait<SLEEP_MMA>(vfull + 8 * st, vr.ph, abort_flag, wns)) { ok = false; break; }
+                        if (!FP8) fence_proxy_async_smem();  // cp.async data -> tensor core reads
+                        const uint32_t vb = s_v + st * S_::OP_STAGE, rel = vempty + 8 * st;
+                        ++gv;
+                        vr.next(p.NV);
+                        tc_fence_after();
+                        if (lane == 0) {
+                            const uint64_t va0 = desc_mnmajor_sw128(vb, v_lbo), pa0 = desc_mnmajor_sw32(pa, TILE_KEYS * 32);
 #pragma unroll
-                        for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
-                            mma_bf16(d_o + h * NQ, desc_advance(va0, ks * 2048), desc_advance(pa0, ks * 512), idesc_pv,
-                                     (t > 0 || ks > 0) ? 1u : 0u);
-                        mma_commit(rel);
+                            for (int ks = 0; ks < TILE_KEYS / 16; ++ks)
+                                mma_bf16(d_o + h * NQ, desc_advance(va0, ks * 2048), desc_advance(pa0, ks * 512), idesc_pv,
+                                         (t > 0 || ks > 0) ? 1u : 0u);
+                            mma_commit(rel);
+                        }
+                        __syncwarp();
                     }
-                    __syncwarp();
-                }
                 }
                 if (!ok) break;
                 if (lane == 0) {
@@ -1907,7 +1906,6 @@ SPEC_API int spec_verify_attn_plan(const spec_kv_desc *kvd, int B, int k, int n_
     size_t smem = 0;
     st = spec::plan_dispatch(p, &smem);
     if (st) return st;
-    const int nsub = kvd->head_dim / (kvd->head_dim < 128 ? kvd->head_dim : 128);
     const int32_t v[SPEC_ATTN_PLAN_FIELDS] = {(int32_t)smem, p.NQ, p.NK, p.NV, p.NR, p.NSB, p.NPB, p.QB, p.OB,
                                               (int32_t)(p.t_one + 16), p.split_keys, p.n_splits,
                                               p.n_units, p.TPI, p.tma_rows,
