@@ -15,6 +15,10 @@ the most bytes per step. The other workloads are reported under "all_configs".
 --only attn|lmhead runs just that call of the workload (W + K plain launches, no graph):
 the command the ncu summaries under profiles/ are taken with.
 
+--next times the calls beyond the chain step (hidden-row pool, graph replay against eager
+launches, tree verify, stop-aware and sampling acceptance) on the batched-branches workload
+and prints their own JSON line.
+
 --impl reference times the CPU oracle (the plain fp64 reference) on the same workload,
 one bounded sample per step, on this host's cores.
 Under torchrun (N > 1) every rank runs an independent replica (weak scaling; the path
@@ -431,6 +435,160 @@ def run_ours(args):
 
 # ---- the oracle on the host cores ------------------------------------------------------------
 
+def run_next(args):
+    """The calls beyond the chain step, on the batched-branches workload (B=16, k=6, 32/8
+    heads, d=128, bf16 pages of 16; V=151936, H=4096), each timed alone from a CUDA graph with
+    the L2 flushed before every replay: the hidden-row pool gather and scatter, eager launches
+    against one graph replay of the whole step (also on the single-stream workload), tree
+    attention over a binary tree of the 7 verify slots, the tree walk and the compaction of its
+    path, acceptance with stop ids and budgets, and speculative sampling acceptance. One JSON
+    line; bytes are the algorithmic bytes of each call."""
+    import torch
+    from greedy_speculative_decode_spec_gb300 import _binding as bnd
+    from greedy_speculative_decode_spec_gb300 import build as pkg_build
+
+    pkg_build.build()
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    hbm_peak, peak_kind = _peaks()
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def flush():
+        # as in the step timing: write 512 MiB, then read 256 MiB of it, so that the dirty
+        # lines are written back here and not inside the timed call
+        flush_buf.fill_(1)
+        flush_sink.copy_(flush_buf[: 256 << 20].view(torch.int64).sum())
+
+    def timed(fn, steps, reps=1):
+        def body():
+            for _ in range(reps):
+                fn()
+        g = _graph_of(body)
+        for _ in range(3):
+            g.replay()
+        ts = _time_region(g.replay, steps, flush, stream)
+        del g
+        return statistics.median(ts) * 1e3 / reps  # us per call
+
+    def small(e, fn):
+        # a latency-bound call: also its time per call in a graph of 20 back-to-back calls
+        e["us_each_of_20"] = round(timed(fn, steps, reps=20), 2)
+        return e
+
+    def entry(us, nbytes=None):
+        e = {"us": round(us, 2)}
+        if nbytes is not None:
+            gbs = nbytes / (us * 1e-6) / 1e9
+            e.update(bytes=int(nbytes), gbs=round(gbs, 1), frac=round(gbs / hbm_peak, 4))
+        return e
+
+    steps = args.steps
+    rows = {}
+    i32 = dict(dtype=torch.int32, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(2024)
+
+    # ---- f1: eager launches against one graph replay of the whole step ----
+    for cid in (1, 2):
+        w = _setup_workload(cid, dev)
+        step, inp = w["step"], w["inputs"]
+
+        def one():
+            step.run(inp["pos"], inp["q"], inp["k_new"], inp["v_new"], inp["hidden"], inp["drafts"], with_mtp=False)
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        eager = statistics.median(_time_region(one, steps, flush, stream)) * 1e3
+        rows[f"step_eager_{w['cfg'].name}"] = entry(eager)
+        rows[f"step_graph_{w['cfg'].name}"] = entry(timed(one, steps))
+        if cid == 2:
+            kept = w
+        else:
+            del w, step, inp
+            torch.cuda.empty_cache()
+    w = kept
+    c, step, inp, kv = w["cfg"], w["step"], w["inputs"], w["kv"]
+    B, k, H, V, R = c.B, c.k, c.H, c.V, c.B * (c.k + 1)
+    err = torch.zeros(1, **i32)
+
+    # ---- f1: hidden-row pool (64 slots of H bf16), gather then scatter of B rows ----
+    hpool = torch.randn((64, H), generator=g, device=dev).to(torch.bfloat16)
+    hslot = torch.randperm(64, generator=g, device=dev)[:B].to(torch.int32)
+    h = torch.empty((B, H), dtype=torch.bfloat16, device=dev)
+    row_bytes = 2 * B * H * 2  # each row read once and written once
+    gat = lambda: bnd.spec_h_gather(h, hpool, hslot, err)  # noqa: E731
+    sca = lambda: bnd.spec_h_scatter(hpool, h, hslot, err)  # noqa: E731
+    rows["h_gather"] = small(entry(timed(gat, steps), row_bytes), gat)
+    rows["h_scatter"] = small(entry(timed(sca, steps), row_bytes), sca)
+
+    # ---- f2: tree attention (binary tree over the 7 slots), tree walk, path compaction ----
+    parent = [-1, 0, 0, 1, 1, 2, 2][: k + 1]
+    masks = []
+    for j in range(k + 1):
+        m, x = 0, j
+        while x >= 0:
+            m |= 1 << x
+            x = parent[x]
+        masks.append(m)
+    anc = torch.tensor(masks * B, **i32)
+    out = torch.empty((R, c.Hq, c.d), dtype=torch.bfloat16, device=dev)
+
+    def tree_attn():
+        bnd.spec_verify_attn_tree(kv.desc, inp["pos"], B, k, c.Hq, inp["q"], step.scale, anc, out, step.attn_ws,
+                                  step.max_pos, err)
+    rows["verify_attn_tree"] = entry(timed(tree_attn, steps), w["kv_bytes"])
+    par = torch.tensor([max(p, 0) for p in parent] * B, **i32)
+    ids = torch.randint(0, V, (B, k + 1), generator=g, device=dev, dtype=torch.int32)
+    drafts = torch.randint(0, V, (B, k), generator=g, device=dev, dtype=torch.int32)
+    drafts[:, 0] = ids[:, 0]  # every walk takes its first step
+    drafts[:, 2] = ids[:, 1]
+    toks, path = torch.empty((B, k + 1), **i32), torch.empty((B, k + 1), **i32)
+    n, a, npos, nxt = (torch.empty(B, **i32) for _ in range(4))
+    walk = lambda: bnd.spec_accept_tree(drafts, ids, inp["pos"], par, B, k, toks, n, a, npos, nxt, path, err)  # noqa: E731
+    rows["accept_tree"] = small(entry(timed(walk, steps)), walk)
+    torch.cuda.synchronize()
+    moved = int(a.sum().item())  # rows moved by the compaction: K and V of every kv head
+    kv_row = 2 * c.Hkv * c.d * (2 if c.kv_dtype == "bf16" else 1)
+    comp = lambda: bnd.spec_kv_compact(kv.desc, inp["pos"], path, a, B, k, err)  # noqa: E731
+    rows["kv_compact"] = small(entry(timed(comp, steps), 2 * moved * kv_row), comp)
+
+    # ---- f3: acceptance with stop ids and per-branch budgets ----
+    stop = torch.tensor([151643, 151645, -1, -1], **i32)
+    budget = torch.randint(1, 2 * (k + 1), (B,), generator=g, device=dev, dtype=torch.int32)
+    stp = lambda: bnd.spec_accept_stop(inp["drafts"], step.out.ids, inp["pos"], B, k, stop, budget, toks, n, a,  # noqa: E731
+                                       npos, nxt)
+    rows["accept_stop"] = small(entry(timed(stp, steps)), stp)
+
+    # ---- f4: speculative sampling acceptance, fp32 logits [R][V] and draft probabilities [B][k][V] ----
+    del w, kept, step
+    torch.cuda.empty_cache()
+    logits = 3.0 * torch.randn((R, V), generator=g, device=dev)
+    qd = torch.softmax((logits.view(B, k + 1, V)[:, :k] + torch.randn((B, k, V), generator=g, device=dev)) / 1.3,
+                       dim=-1).contiguous()
+    sdrafts = torch.multinomial(qd.view(B * k, V), 1, generator=g).view(B, k).to(torch.int32)
+    u_acc = torch.rand((B, k), generator=g, device=dev)
+    u_res = torch.rand(B, generator=g, device=dev)
+    spos = torch.randint(0, 8000, (B,), generator=g, device=dev, dtype=torch.int32)
+    sws = torch.zeros(bnd.spec_accept_sample_workspace(B, k, V), dtype=torch.uint8, device=dev)
+    us = timed(lambda: bnd.spec_accept_sample(sdrafts, logits, qd, spos, B, k, 1.0, u_acc, u_res, toks, n, a, npos,
+                                              nxt, err, ws=sws), steps)
+    torch.cuda.synchronize()
+    # bytes: every verify row's logits once (all rows' softmax statistics are computed) and
+    # the q row of each rejected draft; "needed_bytes": only the rows up to the decisive one
+    acc = a.cpu().tolist()
+    nb = R * V * 4 + sum(V * 4 for x in acc if x < k)
+    rows["accept_sample"] = entry(us, nb)
+    rows["accept_sample"]["needed_bytes"] = sum((min(x, k) + 1) * V * 4 + (V * 4 if x < k else 0) for x in acc)
+    rows["accept_sample"]["accepted"] = acc
+    assert int(err.item()) == 0, "device error in the next-row calls"
+    line = {"mode": "next_rows", "workload": c.name, "steps": steps, "hbm_peak_gbs": hbm_peak, "peak": peak_kind,
+            "timing": "CUDA-event median of graph replays, L2 flushed before each; eager: plain launches",
+            "rows": rows}
+    print(json.dumps(line), flush=True)
+
+
 def _oracle_sample(cid: int):
     """A bounded sample of workload `cid` for the oracle: one verify row (b=0, j=k) through
     append, attention over all q heads, the full-vocabulary LM head and acceptance."""
@@ -519,9 +677,12 @@ def main():
     ap.add_argument("--no-all", dest="all", action="store_false")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--next", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    if args.impl == "reference":
+    if args.next:
+        run_next(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -37,7 +37,8 @@ EXPORTS = ("spec_strerror", "spec_version", "spec_kv_append", "spec_kv_write_row
            "spec_verify_attn_workspace", "spec_verify_attn", "spec_lmhead_workspace",
            "spec_lmhead_argmax", "spec_lmhead_logits", "spec_accept", "spec_mtp_input_workspace",
            "spec_mtp_input", "spec_lmhead_argmax_static", "spec_accept_stop", "spec_verify_attn_plan",
-           "spec_test_set_wait_limit", "spec_accept_sample", "spec_verify_attn_tree", "spec_accept_tree",
+           "spec_test_set_wait_limit", "spec_accept_sample", "spec_accept_sample_workspace",
+           "spec_verify_attn_tree", "spec_accept_tree",
            "spec_kv_compact", "spec_h_gather", "spec_h_scatter")
 
 
@@ -86,7 +87,9 @@ def lib() -> ctypes.CDLL:
         L.spec_accept_stop.argtypes = [_vp, _vp, _vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _vp, _i32, _vp, _vp]
         L.spec_accept_sample.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _f32, _vp, _vp, _vp, _vp, _vp, _vp,
-                                         _vp, _vp, _vp]
+                                         _vp, _vp, _sz, _vp, _vp]
+        L.spec_accept_sample_workspace.restype = _sz
+        L.spec_accept_sample_workspace.argtypes = [_i32, _i32, _i32]
         L.spec_verify_attn_tree.argtypes = [_KVP, _vp, _i32, _i32, _i32, _vp, _f32, _vp, _vp, _vp, _sz, _i32, _vp, _vp]
         L.spec_accept_tree.argtypes = [_vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         L.spec_kv_compact.argtypes = [_KVP, _vp, _vp, _vp, _i32, _i32, _vp, _vp]
@@ -274,17 +277,25 @@ def spec_accept_stop(drafts, ids, pos, B: int, k: int, stop_ids, budget, out_tok
         _ptr(h_out, "h_out", torch.bfloat16), _stream(stream)))
 
 
+def spec_accept_sample_workspace(B: int, k: int, V: int) -> int:
+    return int(lib().spec_accept_sample_workspace(B, k, V))
+
+
 def spec_accept_sample(drafts, logits, q, pos, B: int, k: int, temperature: float, u_acc, u_res, out_tokens, out_n,
-                       out_accepted, out_pos, out_next, dev_err=None, stream=None):
-    """Speculative sampling acceptance; logits fp32 [B*(k+1)][V], q fp32 [B][k][V]."""
+                       out_accepted, out_pos, out_next, dev_err=None, ws=None, stream=None):
+    """Speculative sampling acceptance; logits fp32 [B*(k+1)][V], q fp32 [B][k][V]; ws: a
+    zeroed device byte tensor of spec_accept_sample_workspace(B, k, V) bytes (made here if None)."""
     V = int(logits.shape[-1])
+    if ws is None:
+        ws = torch.zeros(max(1, spec_accept_sample_workspace(B, k, V)), dtype=torch.uint8, device=logits.device)
     _check("spec_accept_sample", lib().spec_accept_sample(
         _ptr(drafts, "drafts", torch.int32) if k > 0 else None, _ptr(logits, "logits", torch.float32),
         _ptr(q, "q", torch.float32) if k > 0 else None, _ptr(pos, "pos", torch.int32), B, k, V, float(temperature),
         _ptr(u_acc, "u_acc", torch.float32) if k > 0 else None, _ptr(u_res, "u_res", torch.float32),
         _ptr(out_tokens, "out_tokens", torch.int32), _ptr(out_n, "out_n", torch.int32),
         _ptr(out_accepted, "out_accepted", torch.int32), _ptr(out_pos, "out_pos", torch.int32),
-        _ptr(out_next, "out_next", torch.int32), _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
+        _ptr(out_next, "out_next", torch.int32), _ptr(ws, "ws"), ws.numel() * ws.element_size(),
+        _ptr(dev_err, "dev_err", torch.int32), _stream(stream)))
 
 
 def spec_verify_attn_tree(kv: spec_kv_desc, pos, B: int, k: int, n_q_heads: int, q, scale: float, anc_mask, out, ws,

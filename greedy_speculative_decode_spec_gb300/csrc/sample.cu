@@ -9,30 +9,45 @@
 // u < p / q) and u_res[b] is the one draw of the step: the smallest index t whose running
 // sum of the weights exceeds u * (their total), taken in index order.
 //
-// One CTA of 1024 threads per branch. Per verify row: the maximum of the logits (one pass,
-// warp max reductions), the softmax denominator (one pass; each thread sums exp2 of its
-// elements with a compensated fp32 sum, the 1024 partial sums are added in fp64), then the
-// draft's probability on one thread. A draw: each thread owns a contiguous chunk of the
-// vocabulary and sums its weights (compensated), the chunk sums are scanned in fp64, and the
-// thread whose chunk crosses u * total walks it in fp64. The decisions are taken in fp32
-// probabilities with fp64 sums; they can differ from an all-fp64 evaluation only where the
-// test value lies within the fp32 rounding of a boundary.
+// A verify row of a 151936-entry vocabulary is 600 KB of fp32 logits, so the work is spread
+// over the whole GPU, in chunks of SMP_CHUNK entries, in two launches:
+//  1. row statistics, one CTA per (verify row, chunk): the chunk's largest logit m_c and the
+//     fp64 sum of exp2((z - m_c) * c), c = log2(e) / T. Every verify row is read, all at
+//     once (rather than one after another up to the first rejection);
+//  2. the walk and the draw weights, one CTA per (branch, chunk): the branch's rows' maxima
+//     M (over chunks) and denominators S = sum_c s_c * 2^((m_c - M) c) (the factor in fp32,
+//     the sum in fp64, in chunk order), every draft's decision at once (the walk stops at the first draft not kept),
+//     then the chunk's sums of the draw weights of the decisive row (the residual and p);
+//  3. the draw, by the branch's last CTA of step 2 to finish: the chunk whose running sum
+//     crosses u * total (in chunk order), then the index inside it (each thread owns a
+//     contiguous run of SMP_PER entries; a scan of the runs' sums; the crossing run is
+//     walked entry by entry).
+// Probabilities are fp32 (exp2f); every sum is kept as a double-float (an unevaluated pair of
+// fp32 values, about 48 significant bits: Knuth's TwoSum and an fma-based TwoProduct give the
+// exact rounding error of each addition and product), from compensated fp32 partial sums, in
+// a fixed order: GB300's fp64 pipe is narrow, so per-thread fp64 would bound these kernels.
+// A decision can differ from an exact evaluation only where its test value lies within that
+// rounding (about 2^-24 relative, from the fp32 probabilities) of a boundary.
 #include <climits>
 #include <math.h>
 
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace spec {
 
-constexpr int SMP_THREADS = 1024;
-constexpr int SMP_WARPS = SMP_THREADS / 32;
+constexpr int SMP_T = 256;                  // threads per CTA
+constexpr int SMP_W = SMP_T / 32;
+constexpr int SMP_PER = 32;                 // entries per thread
+constexpr int SMP_CHUNK = SMP_T * SMP_PER;  // entries per CTA
 
 struct SampleArgs {
     const int32_t *drafts;  // [B][k]
     const float *logits;    // [B*(k+1)][V]
     const float *q;         // [B][k][V]
     const int32_t *pos;     // [B]
-    int B, k, V;
+    int B, k, V, NC;        // NC: chunks per row
+    bool vec;               // rows start on 16-byte boundaries (V % 4 == 0, aligned base)
     float inv_t_log2;       // log2(e) / temperature
     const float *u_acc;     // [B][k]
     const float *u_res;     // [B]
@@ -40,19 +55,83 @@ struct SampleArgs {
     int32_t *err;
 };
 
+// Workspace: per (row, chunk) the statistics; per (branch, chunk) the draw-weight sums and
+// the last index with a positive weight; per branch a count of its finished walk CTAs (zero
+// before a call; the branch's last CTA sets it back to zero).
+struct SampleWs {
+    float2 *s, *wq, *wp;  // double-floats (hi, lo)
+    float *m;
+    int32_t *lq, *lp;
+    uint32_t *cnt;  // per branch: the walk CTAs done (zero between calls)
+};
+__host__ __device__ inline size_t sample_ws_layout(int B, int k, int V, uint8_t *base, SampleWs *w) {
+    const size_t NC = (size_t)((V + SMP_CHUNK - 1) / SMP_CHUNK), R = (size_t)B * (k + 1);
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = (o + bytes + 255) & ~(size_t)255;
+        return base ? base + at : nullptr;
+    };
+    uint8_t *s = take(R * NC * 8), *wq = take((size_t)B * NC * 8), *wp = take((size_t)B * NC * 8);  // float2
+    uint8_t *m = take(R * NC * 4);
+    uint8_t *lq = take((size_t)B * NC * 4), *lp = take((size_t)B * NC * 4), *cnt = take((size_t)B * 4);
+    if (w) {
+        w->s = reinterpret_cast<float2 *>(s);
+        w->wq = reinterpret_cast<float2 *>(wq);
+        w->wp = reinterpret_cast<float2 *>(wp);
+        w->m = reinterpret_cast<float *>(m);
+        w->lq = reinterpret_cast<int32_t *>(lq);
+        w->lp = reinterpret_cast<int32_t *>(lp);
+        w->cnt = reinterpret_cast<uint32_t *>(cnt);
+    }
+    return o;
+}
+
 __device__ __forceinline__ float smp_warp_max(float v) {
     float r;
     asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
     return r;
 }
 
-__device__ __forceinline__ double smp_warp_sum(double v) {
+// Double-float arithmetic. A value is hi + lo with |lo| <= ulp(hi) / 2; every sum here is of
+// non-negative terms, so no addition cancels.
+struct DF {
+    float hi, lo;
+};
+__device__ __forceinline__ DF df_fast(float s, float e) {  // |s| >= |e|: the pair renormalised
+    const float h = s + e;
+    return {h, e - (h - s)};
+}
+// a + b: TwoSum gives the exact error of hi + hi (the same in either order); the low parts
+// are added as one commutative sum, so df_add(a, b) == df_add(b, a) bit for bit
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+    const float s = a.hi + b.hi;
+    const float bb = s - a.hi;
+    const float err = (a.hi - (s - bb)) + (b.hi - bb);
+    return df_fast(s, err + (a.lo + b.lo));
+}
+__device__ __forceinline__ DF df_addf(DF a, float b) { return df_add(a, DF{b, 0.f}); }
+// a * b (b fp32): the product's exact error by an fma
+__device__ __forceinline__ DF df_mulf(DF a, float b) {
+    const float p = a.hi * b;
+    return df_fast(p, fmaf(a.lo, b, fmaf(a.hi, b, -p)));
+}
+__device__ __forceinline__ bool df_less(DF a, DF b) { return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo); }
+__device__ __forceinline__ DF df_shfl_xor(DF v, int o) {
+    return {__shfl_xor_sync(0xFFFFFFFFu, v.hi, o), __shfl_xor_sync(0xFFFFFFFFu, v.lo, o)};
+}
+__device__ __forceinline__ DF df_shfl_up(DF v, int o) {
+    return {__shfl_up_sync(0xFFFFFFFFu, v.hi, o), __shfl_up_sync(0xFFFFFFFFu, v.lo, o)};
+}
+// xor butterfly: partners add the same two values (df_add commutes), so every lane ends
+// with the same sum
+__device__ __forceinline__ DF df_warp_sum(DF v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    for (int o = 16; o > 0; o >>= 1) v = df_add(v, df_shfl_xor(v, o));
     return v;
 }
 
-// compensated (Kahan) fp32 accumulation
+// compensated (Kahan) fp32 accumulation of one thread's terms
 struct KSum {
     float s = 0.f, c = 0.f;
     __device__ __forceinline__ void add(float x) {
@@ -61,188 +140,352 @@ struct KSum {
         c = (t - s) - y;
         s = t;
     }
-    __device__ __forceinline__ double value() const { return (double)s - (double)c; }
+    __device__ __forceinline__ DF value() const { return df_fast(s, -c); }
 };
 
-// block-wide maximum / fp64 sum through shared scratch (red: SMP_WARPS doubles)
+// block-wide maximum / double-float sum (every thread gets the result)
 __device__ float block_max(float v, float *redf) {
     v = smp_warp_max(v);
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     __syncthreads();
     if (l == 0) redf[w] = v;
     __syncthreads();
-    float r = l < SMP_WARPS ? redf[l] : -INFINITY;
-    return smp_warp_max(r);
+    return smp_warp_max(l < SMP_W ? redf[l] : -INFINITY);
 }
 
-__device__ double block_sum(double v, double *red) {
-    v = smp_warp_sum(v);
+__device__ DF block_sum(DF v, DF *red) {
+    v = df_warp_sum(v);
     const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
     __syncthreads();
     if (l == 0) red[w] = v;
     __syncthreads();
-    double r = l < SMP_WARPS ? red[l] : 0.0;
-    return smp_warp_sum(r);
+    return df_warp_sum(l < SMP_W ? red[l] : DF{0.f, 0.f});
 }
 
-// Softmax statistics of one row: the maximum logit and the fp64 sum of exp2((z - mx) * c).
-__device__ void row_stats(const float *z, int V, float c, float *redf, double *red, float &mx, double &den) {
-    float m = -INFINITY;
-    for (int t = threadIdx.x; t < V; t += SMP_THREADS) m = fmaxf(m, __ldg(z + t));
-    mx = block_max(m, redf);
-    KSum ks;
-    for (int t = threadIdx.x; t < V; t += SMP_THREADS) ks.add(exp2f((__ldg(z + t) - mx) * c));
-    den = block_sum(ks.value(), red);
-}
-
-// Inverse-CDF draw over the weights w_t = max(0, p_t - q_t) (q != nullptr, falling back to
-// p_t when they are all zero) or w_t = p_t, with p_t = exp2((z_t - mx) * c) / den: the
-// smallest t whose running sum exceeds u * sum(w) (the last t with w_t > 0 if rounding puts
-// the limit past the total). scan: SMP_THREADS + 1 doubles of shared scratch.
-__device__ int draw_index(const float *z, const float *q, int V, float mx, float c, double den, float u,
-                          float *redf, double *red, double *scan, int *s_found) {
-    const float inv = (float)(1.0 / den);
-    const int chunk = (V + SMP_THREADS - 1) / SMP_THREADS;
-    const int t0 = min(V, (int)threadIdx.x * chunk), t1 = min(V, t0 + chunk);
-    auto weight = [&](int t, bool use_q) -> float {
-        const float p = exp2f((__ldg(z + t) - mx) * c) * inv;
-        return use_q ? fmaxf(p - __ldg(q + t), 0.f) : p;
-    };
-    bool use_q = q != nullptr;
-    KSum ks;
-    for (int t = t0; t < t1; ++t) ks.add(weight(t, use_q));
-    double S = ks.value();
-    double total = block_sum(S, red);
-    if (use_q && !(total > 0.0)) {  // the residual is all zero: draw from p
-        use_q = false;
-        KSum kp;
-        for (int t = t0; t < t1; ++t) kp.add(weight(t, false));
-        S = kp.value();
-        total = block_sum(S, red);
-    }
-    // exclusive prefix of the chunk sums (fp64): warp scan, then the warp totals
-    const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-    double incl = S;
+// The SMP_PER entries of a row that thread `threadIdx.x` of a CTA owns in chunk ch:
+// contiguous (CONTIG: base + tid*SMP_PER + j, the order the draw walks) or spread for
+// coalesced loads (base + (j/4*SMP_T + tid)*4 + j%4); entries past V read as `fill`.
+template <bool CONTIG>
+__device__ __forceinline__ void load_run(const float *row, int ch, int V, bool vec, float fill, float (&x)[SMP_PER]) {
+    const int base = ch * SMP_CHUNK;
+    if (vec) {
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (l >= o) incl += y;
+        for (int j = 0; j < SMP_PER; j += 4) {
+            const int t = CONTIG ? base + threadIdx.x * SMP_PER + j : base + ((j / 4) * SMP_T + threadIdx.x) * 4;
+            float4 v = make_float4(fill, fill, fill, fill);
+            if (t < V) v = __ldg(reinterpret_cast<const float4 *>(row + t));  // V % 4 == 0: t + 3 < V
+            x[j] = v.x;
+            x[j + 1] = v.y;
+            x[j + 2] = v.z;
+            x[j + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < SMP_PER; ++j) {
+            const int t = CONTIG ? base + threadIdx.x * SMP_PER + j : base + j * SMP_T + threadIdx.x;
+            x[j] = t < V ? __ldg(row + t) : fill;
+        }
+    }
+}
+
+// p_t = exp2((z_t - M) * c) * inv (inv = 1/S rounded to fp32), the one definition the weight
+// sums and the draw's walk share
+__device__ __forceinline__ float prob(float z, float M, float c, float inv) { return exp2f((z - M) * c) * inv; }
+
+// ---- 1: per (row, chunk) maximum and sum of exp2((z - m_c) * c) ----
+__global__ void __launch_bounds__(SMP_T) sample_stats_kernel(SampleArgs a, SampleWs ws) {
+    __shared__ float redf[SMP_W];
+    __shared__ DF red[SMP_W];
+    const int ch = blockIdx.x, r = blockIdx.y;
+    float x[SMP_PER];
+    load_run<false>(a.logits + (size_t)r * a.V, ch, a.V, a.vec, -INFINITY, x);
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < SMP_PER; ++j) m = fmaxf(m, x[j]);
+    m = block_max(m, redf);
+    KSum ks;
+#pragma unroll
+    for (int j = 0; j < SMP_PER; ++j) ks.add(exp2f((x[j] - m) * a.inv_t_log2));  // padding adds 0
+    const DF s = block_sum(ks.value(), red);
+    if (threadIdx.x == 0) {
+        ws.m[(size_t)r * a.NC + ch] = m;
+        ws.s[(size_t)r * a.NC + ch] = make_float2(s.hi, s.lo);
+    }
+    sm100::grid_dep_launch();  // the walk kernel may be scheduled
+}
+
+// ---- 3: the draw and the outputs, by the branch's last walk CTA (the other CTAs' sums are
+// read from L2) ----
+__device__ void draw_branch(const SampleArgs &a, const SampleWs &ws, int b, int acc, float M, float inv, float *redf,
+                            DF *red) {
+    __shared__ float2 s_a[SMP_T], s_b[SMP_T];
+    __shared__ int s_l[SMP_T];
+    __shared__ int s_ch, s_use, s_found, s_last;
+    __shared__ DF s_base, s_lim;
+    const int k = a.k, V = a.V, NC = a.NC, tid = threadIdx.x;
+    const float c = a.inv_t_log2;
+    const float2 *wq = ws.wq + (size_t)b * NC, *wp = ws.wp + (size_t)b * NC;
+    // the chunks' sums in blocks of SMP_T staged in shared memory (loaded by all threads at
+    // once), each block then added on thread 0 in chunk order: first the totals
+    DF tq{0.f, 0.f}, tp{0.f, 0.f};
+    for (int j0 = 0; j0 < NC; j0 += SMP_T) {
+        const int n = min(SMP_T, NC - j0);
+        __syncthreads();
+        if (tid < n) {
+            s_a[tid] = __ldcg(wq + j0 + tid);
+            s_b[tid] = __ldcg(wp + j0 + tid);
+        }
+        __syncthreads();
+        if (tid == 0)
+            for (int j = 0; j < n; ++j) {
+                tq = df_add(tq, DF{s_a[j].x, s_a[j].y});
+                tp = df_add(tp, DF{s_b[j].x, s_b[j].y});
+            }
+    }
+    if (tid == 0) {
+        // the residual (after a rejection) unless it is all zero, else p
+        const bool use_q = acc < k && tq.hi > 0.f;
+        s_use = use_q ? 1 : 0;
+        s_lim = df_mulf(use_q ? tq : tp, __ldg(a.u_res + b));
     }
     __syncthreads();
-    if (l == 31) red[w] = incl;
-    if (threadIdx.x == 0) *s_found = INT_MAX;
+    const bool use_q = s_use != 0;
+    const float2 *w = use_q ? wq : wp;
+    const int32_t *lw = (use_q ? ws.lq : ws.lp) + (size_t)b * NC;
+    // then the chunk whose running sum crosses the limit: run <= lim < run + w
+    DF run{0.f, 0.f};
+    int pick = -1, last = -1;
+    for (int j0 = 0; j0 < NC; j0 += SMP_T) {
+        const int n = min(SMP_T, NC - j0);
+        __syncthreads();
+        if (tid < n) {
+            s_a[tid] = __ldcg(w + j0 + tid);
+            s_l[tid] = __ldcg(lw + j0 + tid);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            const DF lim = s_lim;
+            for (int j = 0; j < n; ++j) {
+                last = max(last, s_l[j]);
+                const DF nxt = df_add(run, DF{s_a[j].x, s_a[j].y});
+                if (pick < 0 && !df_less(lim, run) && df_less(lim, nxt)) {
+                    pick = j0 + j;
+                    s_base = run;
+                }
+                run = nxt;
+            }
+        }
+    }
+    if (tid == 0) {
+        s_ch = pick;
+        s_last = last < 0 ? 0 : last;  // the limit past the total: the last positive weight
+        s_found = INT_MAX;
+    }
     __syncthreads();
-    if (w == 0) {
-        double v = l < SMP_WARPS ? red[l] : 0.0, vi = v;
+    int tok = s_last;
+    const int ch = s_ch;
+    if (ch >= 0) {
+        const float *z = a.logits + ((size_t)b * (k + 1) + acc) * V;
+        float x[SMP_PER], y[SMP_PER];
+        load_run<true>(z, ch, V, a.vec, -INFINITY, x);
+        if (use_q) load_run<true>(a.q + ((size_t)b * k + acc) * V, ch, V, a.vec, 0.f, y);
+        float wt[SMP_PER];
+        KSum ks;
+#pragma unroll
+        for (int j = 0; j < SMP_PER; ++j) {
+            const float p = prob(x[j], M, c, inv);
+            wt[j] = use_q ? fmaxf(p - y[j], 0.f) : p;
+            ks.add(wt[j]);
+        }
+        // exclusive scan of the runs' sums: warp scan, then the warp totals in order
+        const DF St = ks.value();
+        const int wi = tid >> 5, l = tid & 31;
+        DF incl = St, excl{0.f, 0.f};
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const double y = __shfl_up_sync(0xFFFFFFFFu, vi, o);
-            if (l >= o) vi += y;
+            const DF v = df_shfl_up(incl, o);
+            if (l >= o) incl = df_add(v, incl);
         }
-        if (l < SMP_WARPS) red[l] = vi - v;  // exclusive prefix of the warps
-    }
-    __syncthreads();
-    const double excl = red[w] + (incl - S);
-    scan[threadIdx.x] = excl;
-    if (threadIdx.x == SMP_THREADS - 1) scan[SMP_THREADS] = excl + S;
-    __syncthreads();
-    const double lim = (double)u * total;
-    if (excl <= lim && lim < scan[threadIdx.x + 1]) {
-        double run = excl;
-        int pick = -1, last_pos = -1;
-        for (int t = t0; t < t1; ++t) {
-            const double wt = (double)weight(t, use_q);
-            if (wt > 0.0) last_pos = t;
-            run += wt;
-            if (run > lim) {
-                pick = t;
-                break;
-            }
+        {
+            const DF v = df_shfl_up(incl, 1);
+            if (l >= 1) excl = v;
         }
-        if (pick < 0) pick = last_pos;  // rounding: the chunk ended at the limit
-        if (pick >= 0) atomicMin(s_found, pick);
-    }
-    __syncthreads();
-    int found = *s_found;
-    if (found == INT_MAX) {
-        // the limit lies past the total: the last index with a positive weight
-        int last = -1;
-        for (int t = t0; t < t1; ++t)
-            if (weight(t, use_q) > 0.f) last = t;
-        found = (int)block_max((float)last, redf);
-        found = found < 0 ? 0 : found;
-    }
-    __syncthreads();
-    return found;
-}
-
-__global__ void __launch_bounds__(SMP_THREADS) sample_accept_kernel(SampleArgs a) {
-    __shared__ float redf[SMP_WARPS];
-    __shared__ double red[SMP_WARPS];
-    __shared__ double scan[SMP_THREADS + 1];
-    __shared__ int s_found, s_keep;
-    const int b = blockIdx.x;
-    const int k = a.k, V = a.V;
-    const float c = a.inv_t_log2;
-    int acc = k, last = -1;
-    for (int i = 0; i < k; ++i) {
-        const float *z = a.logits + ((size_t)b * (k + 1) + i) * V;
-        const float *qi = a.q + ((size_t)b * k + i) * V;
-        float mx;
-        double den;
-        row_stats(z, V, c, redf, red, mx, den);
-        if (threadIdx.x == 0) {
-            const int d = __ldg(a.drafts + (size_t)b * k + i);
-            // a draft is a sample of q: one outside [0, V) or with q(d) <= 0 (or NaN) is
-            // reported and rejected
-            const double qd = (d >= 0 && d < V) ? (double)__ldg(qi + d) : 0.0;
-            int keep = 0;
-            if (!(qd > 0.0)) {
-                raise_error(a.err, SPEC_DEVERR_TOKEN);
-            } else {
-                const double pd = (double)exp2f((__ldg(z + d) - mx) * c) / den;
-                keep = (pd >= qd || (double)__ldg(a.u_acc + (size_t)b * k + i) < pd / qd) ? 1 : 0;
-            }
-            s_keep = keep;
-        }
+        if (l == 31) red[wi] = incl;
         __syncthreads();
-        const int keep = s_keep;
-        __syncthreads();
-        if (!keep) {
-            acc = i;
-            last = draw_index(z, qi, V, mx, c, den, __ldg(a.u_res + b), redf, red, scan, &s_found);
-            break;
+        DF r = s_base;
+        for (int i = 0; i < wi; ++i) r = df_add(r, red[i]);
+        r = df_add(r, excl);
+        const DF lim = s_lim;
+        const int t0 = ch * SMP_CHUNK + tid * SMP_PER;
+        int lastpos = -1;
+        if (!df_less(lim, r) && df_less(lim, df_add(r, St))) {
+            int pk = -1;
+            for (int j = 0; j < SMP_PER; ++j) {
+                if (wt[j] > 0.f) lastpos = t0 + j;
+                r = df_addf(r, wt[j]);
+                if (df_less(lim, r)) {
+                    pk = t0 + j;
+                    break;
+                }
+            }
+            if (pk < 0) pk = lastpos;  // rounding: the run ended at the limit
+            if (pk >= 0) atomicMin(&s_found, pk);
         }
+        // the chunk's last positive weight, for a limit that the runs' own sums put past it
+#pragma unroll
+        for (int j = 0; j < SMP_PER; ++j)
+            if (wt[j] > 0.f) lastpos = t0 + j;
+        lastpos = (int)block_max((float)lastpos, redf);
+        const int found = s_found;
+        tok = found != INT_MAX ? found : (lastpos >= 0 ? lastpos : s_last);
     }
-    if (acc == k) {  // every draft kept: the bonus token from the last row's p
-        const float *z = a.logits + ((size_t)b * (k + 1) + k) * V;
-        float mx;
-        double den;
-        row_stats(z, V, c, redf, red, mx, den);
-        last = draw_index(z, nullptr, V, mx, c, den, __ldg(a.u_res + b), redf, red, scan, &s_found);
-    }
-    const int t = threadIdx.x;
+    const int t = tid;
     if (t <= k)
-        a.out_tokens[(size_t)b * (k + 1) + t] = t < acc ? __ldg(a.drafts + (size_t)b * k + t) : (t == acc ? last : -1);
+        a.out_tokens[(size_t)b * (k + 1) + t] = t < acc ? __ldg(a.drafts + (size_t)b * k + t) : (t == acc ? tok : -1);
     if (t == 0) {
         a.out_n[b] = acc + 1;
         a.out_accepted[b] = acc;
         a.out_pos[b] = a.pos[b] + acc + 1;  // out_pos may be pos
-        a.out_next[b] = last;
+        a.out_next[b] = tok;
     }
+}
+
+// ---- 2: the walk, then this chunk's draw-weight sums of the decisive row ----
+__global__ void __launch_bounds__(SMP_T) sample_walk_kernel(SampleArgs a, SampleWs ws) {
+    __shared__ float redf[SMP_W];
+    __shared__ DF red[SMP_W];
+    __shared__ float sM[SPEC_KMAX + 1];
+    __shared__ DF sS[SPEC_KMAX + 1];
+    __shared__ int s_acc;
+    __shared__ float s_inv;
+    const int ch = blockIdx.x, b = blockIdx.y, k = a.k, V = a.V, NC = a.NC;
+    const float c = a.inv_t_log2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the decisions' inputs first (their loads overlap the merge below): per draft its id, q(d)
+    // and logit z(d); a draft is a sample of q, so one outside [0, V) or with q(d) <= 0 (or NaN)
+    // is rejected, and reported if the walk reaches it
+    float qd = 0.f, ud = 0.f, zd = 0.f;
+    if (warp == 0 && lane < k) {
+        const int d = __ldg(a.drafts + (size_t)b * k + lane);
+        ud = __ldg(a.u_acc + (size_t)b * k + lane);
+        if (d >= 0 && d < V) {
+            qd = __ldg(a.q + ((size_t)b * k + lane) * V + d);
+            zd = __ldg(a.logits + ((size_t)b * (k + 1) + lane) * V + d);
+        }
+    }
+    sm100::grid_dep_wait();  // the row statistics
+    // each row's M and S from its chunks, one warp per row (lane-strided, then the
+    // butterfly: a fixed order)
+    for (int i = warp; i <= k; i += SMP_W) {
+        const size_t r0 = ((size_t)b * (k + 1) + i) * NC;
+        float m = -INFINITY;
+        for (int j = lane; j < NC; j += 32) m = fmaxf(m, ws.m[r0 + j]);
+        m = smp_warp_max(m);
+        DF sum{0.f, 0.f};
+        for (int j = lane; j < NC; j += 32) {
+            const float2 sc = ws.s[r0 + j];
+            sum = df_add(sum, df_mulf(DF{sc.x, sc.y}, exp2f((ws.m[r0 + j] - m) * c)));
+        }
+        sum = df_warp_sum(sum);
+        if (lane == 0) {
+            sM[i] = m;
+            sS[i] = sum;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // every draft's decision at once; the walk stops at the first one not kept
+        int keep = 1;
+        bool bad = false;
+        if (lane < k) {
+            if (!(qd > 0.f)) {
+                keep = 0;
+                bad = true;
+            } else {
+                // p(d) = e / S: kept when p(d) >= q(d) or u < p(d) / q(d), tested as e >= q(d) S
+                // or u q(d) S < e (q(d) > 0, S > 0)
+                const DF e{exp2f((zd - sM[lane]) * c), 0.f};
+                const DF qS = df_mulf(sS[lane], qd);
+                keep = (!df_less(e, qS) || df_less(df_mulf(qS, ud), e)) ? 1 : 0;
+            }
+        }
+        const unsigned rej = __ballot_sync(0xFFFFFFFFu, lane < k && !keep);
+        const int acc = rej ? __ffs(rej) - 1 : k;
+        if (ch == 0 && lane == acc && bad) raise_error(a.err, SPEC_DEVERR_TOKEN);
+        if (lane == 0) {
+            s_acc = acc;
+            s_inv = 1.f / (sS[acc].hi + sS[acc].lo);  // 1/S rounded to fp32
+        }
+    }
+    __syncthreads();
+    const int acc = s_acc;
+    const float M = sM[acc], inv = s_inv;
+    const float *z = a.logits + ((size_t)b * (k + 1) + acc) * V;
+    const float *qr = acc < k ? a.q + ((size_t)b * k + acc) * V : nullptr;
+    // this chunk's sums (spread entries for coalesced loads: a sum's order is free; the draw
+    // walks its chunk with sums of its own) and the last index with a positive weight
+    float x[SMP_PER], y[SMP_PER];
+    load_run<false>(z, ch, V, a.vec, -INFINITY, x);
+    if (qr) load_run<false>(qr, ch, V, a.vec, 0.f, y);
+    KSum kq, kp;
+    int lq = -1, lp = -1;
+#pragma unroll
+    for (int j = 0; j < SMP_PER; ++j) {
+        const int t = a.vec ? ch * SMP_CHUNK + ((j / 4) * SMP_T + threadIdx.x) * 4 + (j & 3)
+                            : ch * SMP_CHUNK + j * SMP_T + threadIdx.x;
+        const float p = prob(x[j], M, c, inv);  // 0 past V
+        kp.add(p);
+        if (p > 0.f) lp = max(lp, t);
+        if (qr) {
+            const float w = fmaxf(p - y[j], 0.f);
+            kq.add(w);
+            if (w > 0.f) lq = max(lq, t);
+        }
+    }
+    const DF sq = block_sum(kq.value(), red);
+    const DF sp = block_sum(kp.value(), red);
+    lq = (int)block_max((float)lq, redf);  // indices < 2^24: exact in fp32
+    lp = (int)block_max((float)lp, redf);
+    // publish this chunk's sums; the branch's last CTA to finish draws
+    __shared__ int s_lastcta;
+    if (threadIdx.x == 0) {
+        const size_t o = (size_t)b * NC + ch;
+        ws.wq[o] = make_float2(sq.hi, sq.lo);
+        ws.wp[o] = make_float2(sp.hi, sp.lo);
+        ws.lq[o] = lq;
+        ws.lp[o] = lp;
+        __threadfence();
+        const bool last = atomicAdd(ws.cnt + b, 1u) == (unsigned)NC - 1;
+        if (last) ws.cnt[b] = 0u;  // no other CTA of the branch touches it again in this call
+        s_lastcta = last ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_lastcta) return;
+    __threadfence();
+    draw_branch(a, ws, b, acc, M, inv, redf, red);
 }
 
 }  // namespace spec
 
+SPEC_API size_t spec_accept_sample_workspace(int B, int k, int V) {
+    if (B < 1 || k < 0 || k > SPEC_KMAX || V < 1) return 0;
+    return spec::sample_ws_layout(B, k, V, nullptr, nullptr);
+}
+
 SPEC_API int spec_accept_sample(const int32_t *drafts, const float *logits, const float *q, const int32_t *pos,
                                 int B, int k, int V, float temperature, const float *u_acc, const float *u_res,
                                 int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted, int32_t *out_pos,
-                                int32_t *out_next, int32_t *dev_err, spec_stream_t stream) {
+                                int32_t *out_next, void *workspace, size_t ws_bytes, int32_t *dev_err,
+                                spec_stream_t stream) {
     if (!logits || !pos || !u_res || !out_tokens || !out_n || !out_accepted || !out_pos || !out_next)
         return SPEC_ERR_NULL;
     if (k > 0 && (!drafts || !q || !u_acc)) return SPEC_ERR_NULL;
-    if (B < 1 || k < 0 || k > SPEC_KMAX || V < 1) return SPEC_ERR_ARG;
+    if (B < 1 || k < 0 || k > SPEC_KMAX || V < 1 || V >= (1 << 24)) return SPEC_ERR_ARG;
     if (!(temperature > 0.f) || !isfinite(temperature)) return SPEC_ERR_ARG;
+    spec::SampleWs ws;
+    const size_t need = spec::sample_ws_layout(B, k, V, reinterpret_cast<uint8_t *>(workspace), &ws);
+    if (!workspace || ws_bytes < need) return SPEC_ERR_WORKSPACE;
+    if (((uintptr_t)workspace % 16) != 0) return SPEC_ERR_ALIGN;
     spec::SampleArgs a;
     a.drafts = drafts;
     a.logits = logits;
@@ -251,6 +494,8 @@ SPEC_API int spec_accept_sample(const int32_t *drafts, const float *logits, cons
     a.B = B;
     a.k = k;
     a.V = V;
+    a.NC = (V + spec::SMP_CHUNK - 1) / spec::SMP_CHUNK;
+    a.vec = (V % 4) == 0 && ((uintptr_t)logits % 16) == 0 && (k == 0 || ((uintptr_t)q % 16) == 0);
     a.inv_t_log2 = (float)(1.4426950408889634 / (double)temperature);
     a.u_acc = u_acc;
     a.u_res = u_res;
@@ -260,6 +505,10 @@ SPEC_API int spec_accept_sample(const int32_t *drafts, const float *logits, cons
     a.out_pos = out_pos;
     a.out_next = out_next;
     a.err = dev_err;
-    spec::sample_accept_kernel<<<B, spec::SMP_THREADS, 0, (cudaStream_t)stream>>>(a);
-    return spec::launch_status();
+    const cudaStream_t s = (cudaStream_t)stream;
+    spec::sample_stats_kernel<<<dim3(a.NC, B * (k + 1)), spec::SMP_T, 0, s>>>(a, ws);
+    const int st = spec::launch_status();
+    if (st != SPEC_OK) return st;
+    // may start while the statistics finish (it waits for them before reading them)
+    return spec::launch_pdl(spec::sample_walk_kernel, dim3(a.NC, B), dim3(spec::SMP_T), 0, s, a, ws);
 }

@@ -353,16 +353,26 @@ int spec_kv_compact(const spec_kv_desc *kv, const int32_t *pos, const int32_t *p
  *   drafts   device int32 [B][k];  logits  device fp32 [B*(k+1)][V];  q  device fp32 [B][k][V]
  *            (probabilities);  u_acc  device fp32 [B][k];  u_res  device fp32 [B]
  *   out_*    as spec_accept (out_pos may be pos);  temperature > 0
- * Precision: probabilities in fp32 (exp2), sums in fp64 (compensated fp32 partial sums).
- * A decision can differ from an all-fp64 evaluation only when its test value lies within
- * that rounding of the boundary.
- * Host errors: NULL, B < 1, k out of range, V < 1, temperature not positive and finite.
+ *   workspace  device scratch of spec_accept_sample_workspace(B, k, V) bytes, 16-byte
+ *            aligned (per row and chunk of the vocabulary: the softmax statistics; per
+ *            branch: the draw weights' chunk sums and a counter). Zero it before its first
+ *            use; every call leaves it zeroed again. Calls sharing one must not overlap.
+ * Every verify row's softmax statistics are computed (all rows at once, spread over the
+ * GPU), then the walk and the draw; rows past the first rejection are read but unused.
+ * Precision: probabilities in fp32 (exp2); sums as double-floats (pairs of fp32 values,
+ * about 48 significant bits, from compensated fp32 partial sums), each in a fixed order, so
+ * results are deterministic. A decision can differ from an exact evaluation only when its
+ * test value lies within that rounding (about 2^-24 relative) of the boundary.
+ * Host errors: NULL, B < 1, k out of range, V < 1 or V >= 2^24, temperature not positive
+ * and finite, SPEC_ERR_WORKSPACE (NULL or too small), SPEC_ERR_ALIGN (workspace).
  * Device errors: SPEC_DEVERR_TOKEN for a draft outside [0, V) or with q_i(d) <= 0 (not a
- * sample of q): that draft is treated as rejected. */
+ * sample of q) that the walk reaches: that draft is treated as rejected. */
+size_t spec_accept_sample_workspace(int B, int k, int V); /* 0 for invalid sizes */
 int spec_accept_sample(const int32_t *drafts, const float *logits, const float *q, const int32_t *pos, int B,
                        int k, int V, float temperature, const float *u_acc, const float *u_res,
                        int32_t *out_tokens, int32_t *out_n, int32_t *out_accepted, int32_t *out_pos,
-                       int32_t *out_next, int32_t *dev_err, spec_stream_t stream);
+                       int32_t *out_next, void *workspace, size_t ws_bytes, int32_t *dev_err,
+                       spec_stream_t stream);
 
 /* ---- f1: the draft head's remembered hidden rows ----------------------------------
  * Each branch b owns slot hslot[b] of a pool of hidden rows. A step gathers the draft

@@ -119,6 +119,20 @@ def test_host_argument_errors(L):
     assert L.spec_mtp_input(p, p, p, p, p, ctypes.c_float(1e-6), p, 64, 256, 1000, p, p, mw - 1, None, s) == -4
     assert L.spec_mtp_input(p, p, p, p, p, ctypes.c_float(-1.0), p, 64, 256, 1000, p, p, mw, None, s) == -2
     assert L.spec_mtp_input(p, None, p, p, p, ctypes.c_float(1e-6), p, 64, 256, 1000, p, p, mw, None, s) == -1
+    # speculative sampling acceptance: workspace query, then the host checks (nothing launches)
+    f = ctypes.c_float
+    assert L.spec_accept_sample_workspace(0, 3, 1000) == 0
+    assert L.spec_accept_sample_workspace(1, 16, 1000) == 0
+    sw = L.spec_accept_sample_workspace(16, 6, 151936)
+    assert sw >= 12 * 16 * 7 * 19   # per (verify row, vocabulary chunk of 8192): fp32 max, fp64 sum
+    sa = L.spec_accept_sample
+    assert sa(p, p, p, p, 16, 6, 151936, f(1.0), p, p, p, p, p, p, p, p, sw - 1, None, s) == -4
+    assert sa(p, p, p, p, 16, 6, 151936, f(1.0), p, p, p, p, p, p, p, None, sw, None, s) == -4
+    assert sa(p, p, p, p, 16, 6, 151936, f(1.0), p, p, p, p, p, p, p, ctypes.c_void_p(FAKE + 8), sw, None, s) == -6
+    assert sa(p, p, p, p, 16, 6, 151936, f(0.0), p, p, p, p, p, p, p, p, sw, None, s) == -2
+    assert sa(p, p, p, p, 16, 16, 151936, f(1.0), p, p, p, p, p, p, p, p, sw, None, s) == -2
+    assert sa(p, p, p, p, 16, 6, 1 << 24, f(1.0), p, p, p, p, p, p, p, p, sw, None, s) == -2
+    assert sa(p, p, None, p, 16, 6, 151936, f(1.0), p, p, p, p, p, p, p, p, sw, None, s) == -1   # q missing
 
 
 def test_binding_refuses_cpu_tensors(L):
