@@ -490,8 +490,22 @@ def run_next(args):
     g = torch.Generator(device=dev)
     g.manual_seed(2024)
 
-    # ---- f1: eager launches against one graph replay of the whole step ----
-    for cid in (1, 2):
+    # ---- f1: eager launches against one graph replay of the whole step; back to back (no
+    # flush, events around 20 steps) the host's launch cost shows where the step is short ----
+    def b2b(fn, n=20):
+        import torch as _t
+        for _ in range(3):
+            fn()
+        _t.cuda.synchronize()
+        a_, b_ = _t.cuda.Event(enable_timing=True), _t.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        for _ in range(n):
+            fn()
+        b_.record(stream)
+        _t.cuda.synchronize()
+        return a_.elapsed_time(b_) * 1e3 / n
+
+    for cid in (0, 1, 2):
         w = _setup_workload(cid, dev)
         step, inp = w["step"], w["inputs"]
 
@@ -503,6 +517,10 @@ def run_next(args):
         eager = statistics.median(_time_region(one, steps, flush, stream)) * 1e3
         rows[f"step_eager_{w['cfg'].name}"] = entry(eager)
         rows[f"step_graph_{w['cfg'].name}"] = entry(timed(one, steps))
+        gstep = _graph_of(one)
+        rows[f"step_eager_{w['cfg'].name}"]["back_to_back_us"] = round(b2b(one), 2)
+        rows[f"step_graph_{w['cfg'].name}"]["back_to_back_us"] = round(b2b(gstep.replay), 2)
+        del gstep
         if cid == 2:
             kept = w
         else:

@@ -145,3 +145,27 @@ def test_invalid_draft_is_rejected_and_reported(bad):
     assert g[2][bb] <= ii
     for gi, oi in zip(g[:5], o[:5]):
         assert np.array_equal(gi, oi)
+
+
+def test_sample_accept_reuses_its_workspace():
+    """The workspace's per-branch counters are back at zero after a call: a second call on the
+    same workspace writes every output again, equal to the first."""
+    B, k, V, T = 5, 4, 20000, 0.9
+    logits, q, drafts, u_acc, u_res, pos = _inputs(B, k, V, T, seed=123)
+    args = [torch.from_numpy(x).to(DEV) for x in (drafts, logits, q, pos)]
+    ua, ur = torch.from_numpy(u_acc).to(DEV), torch.from_numpy(u_res).to(DEV)
+    ws = torch.zeros(bnd.spec_accept_sample_workspace(B, k, V), dtype=torch.uint8, device=DEV)
+    i32 = dict(dtype=torch.int32, device=DEV)
+    runs = []
+    for _ in range(3):
+        toks = torch.full((B, k + 1), -7, **i32)
+        outs = [torch.full((B,), -7, **i32) for _ in range(4)]
+        err = torch.zeros(1, **i32)
+        bnd.spec_accept_sample(*args, B, k, T, ua, ur, toks, *outs, dev_err=err, ws=ws)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        runs.append([toks.cpu()] + [o.cpu() for o in outs])
+    for r in runs[1:]:
+        for x, y in zip(runs[0], r):
+            assert torch.equal(x, y)
+    assert int(runs[0][1].min()) >= 1  # every branch's outputs were written
