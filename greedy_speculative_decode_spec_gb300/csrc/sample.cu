@@ -12,8 +12,9 @@
 // A verify row of a 151936-entry vocabulary is 600 KB of fp32 logits, so the work is spread
 // over the whole GPU, in chunks of SMP_CHUNK entries, in two launches:
 //  1. row statistics, one CTA per (verify row, chunk): the chunk's largest logit m_c and the
-//     fp64 sum of exp2((z - m_c) * c), c = log2(e) / T. Every verify row is read, all at
-//     once (rather than one after another up to the first rejection);
+//     sum of exp2(z c - m_c c), c = log2(e) / T (the hardware exp2, per-thread sums taken
+//     pairwise). Every verify row is read, all at once (rather than one after another up to
+//     the first rejection);
 //  2. the walk and the draw weights, one CTA per (branch, chunk): the branch's rows' maxima
 //     M (over chunks) and denominators S = sum_c s_c * 2^((m_c - M) c) (the factor in fp32,
 //     the sum in fp64, in chunk order), every draft's decision at once (the walk stops at the first draft not kept),
@@ -203,10 +204,17 @@ __global__ void __launch_bounds__(SMP_T) sample_stats_kernel(SampleArgs a, Sampl
 #pragma unroll
     for (int j = 0; j < SMP_PER; ++j) m = fmaxf(m, x[j]);
     m = block_max(m, redf);
-    KSum ks;
+    // the thread's terms exp2(z c - m c) (one fma and one exp2 each; padding gives 0), summed
+    // pairwise (31 additions in a fixed tree): this kernel streams every verify row, so it
+    // keeps its instruction count low
+    const float c = a.inv_t_log2, mc = m * c;
 #pragma unroll
-    for (int j = 0; j < SMP_PER; ++j) ks.add(exp2f((x[j] - m) * a.inv_t_log2));  // padding adds 0
-    const DF s = block_sum(ks.value(), red);
+    for (int j = 0; j < SMP_PER; ++j) x[j] = sm100::ex2_approx(fmaf(x[j], c, -mc));
+#pragma unroll
+    for (int w = SMP_PER / 2; w >= 1; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) x[j] += x[j + w];
+    const DF s = block_sum(DF{x[0], 0.f}, red);
     if (threadIdx.x == 0) {
         ws.m[(size_t)r * a.NC + ch] = m;
         ws.s[(size_t)r * a.NC + ch] = make_float2(s.hi, s.lo);
@@ -218,72 +226,80 @@ __global__ void __launch_bounds__(SMP_T) sample_stats_kernel(SampleArgs a, Sampl
 // read from L2) ----
 __device__ void draw_branch(const SampleArgs &a, const SampleWs &ws, int b, int acc, float M, float inv, float *redf,
                             DF *red) {
-    __shared__ float2 s_a[SMP_T], s_b[SMP_T];
-    __shared__ int s_l[SMP_T];
     __shared__ int s_ch, s_use, s_found, s_last;
     __shared__ DF s_base, s_lim;
     const int k = a.k, V = a.V, NC = a.NC, tid = threadIdx.x;
     const float c = a.inv_t_log2;
     const float2 *wq = ws.wq + (size_t)b * NC, *wp = ws.wp + (size_t)b * NC;
-    // the chunks' sums in blocks of SMP_T staged in shared memory (loaded by all threads at
-    // once), each block then added on thread 0 in chunk order: first the totals
-    DF tq{0.f, 0.f}, tp{0.f, 0.f};
-    for (int j0 = 0; j0 < NC; j0 += SMP_T) {
-        const int n = min(SMP_T, NC - j0);
-        __syncthreads();
-        if (tid < n) {
-            s_a[tid] = __ldcg(wq + j0 + tid);
-            s_b[tid] = __ldcg(wp + j0 + tid);
+    const int32_t *lq = ws.lq + (size_t)b * NC, *lp = ws.lp + (size_t)b * NC;
+    if (tid < 32) {
+        // warp 0 over the chunks' sums (read from L2: the other CTAs wrote them), 32 chunks at
+        // a time; the first 32 stay in registers
+        const int lane = tid;
+        const float2 z2 = make_float2(0.f, 0.f);
+        const float2 q0 = lane < NC ? __ldcg(wq + lane) : z2, p0 = lane < NC ? __ldcg(wp + lane) : z2;
+        const int lq0 = lane < NC ? __ldcg(lq + lane) : -1, lp0 = lane < NC ? __ldcg(lp + lane) : -1;
+        // the totals (lane-strided, then the butterfly: a fixed order)
+        DF tq{q0.x, q0.y}, tp{p0.x, p0.y};
+        for (int j = lane + 32; j < NC; j += 32) {
+            const float2 u = __ldcg(wq + j), v = __ldcg(wp + j);
+            tq = df_add(tq, DF{u.x, u.y});
+            tp = df_add(tp, DF{v.x, v.y});
         }
-        __syncthreads();
-        if (tid == 0)
-            for (int j = 0; j < n; ++j) {
-                tq = df_add(tq, DF{s_a[j].x, s_a[j].y});
-                tp = df_add(tp, DF{s_b[j].x, s_b[j].y});
-            }
-    }
-    if (tid == 0) {
+        tq = df_warp_sum(tq);
+        tp = df_warp_sum(tp);
         // the residual (after a rejection) unless it is all zero, else p
         const bool use_q = acc < k && tq.hi > 0.f;
-        s_use = use_q ? 1 : 0;
-        s_lim = df_mulf(use_q ? tq : tp, __ldg(a.u_res + b));
-    }
-    __syncthreads();
-    const bool use_q = s_use != 0;
-    const float2 *w = use_q ? wq : wp;
-    const int32_t *lw = (use_q ? ws.lq : ws.lp) + (size_t)b * NC;
-    // then the chunk whose running sum crosses the limit: run <= lim < run + w
-    DF run{0.f, 0.f};
-    int pick = -1, last = -1;
-    for (int j0 = 0; j0 < NC; j0 += SMP_T) {
-        const int n = min(SMP_T, NC - j0);
-        __syncthreads();
-        if (tid < n) {
-            s_a[tid] = __ldcg(w + j0 + tid);
-            s_l[tid] = __ldcg(lw + j0 + tid);
-        }
-        __syncthreads();
-        if (tid == 0) {
-            const DF lim = s_lim;
-            for (int j = 0; j < n; ++j) {
-                last = max(last, s_l[j]);
-                const DF nxt = df_add(run, DF{s_a[j].x, s_a[j].y});
-                if (pick < 0 && !df_less(lim, run) && df_less(lim, nxt)) {
-                    pick = j0 + j;
-                    s_base = run;
-                }
-                run = nxt;
+        const DF lim = df_mulf(use_q ? tq : tp, __ldg(a.u_res + b));
+        // the chunk whose running sum (in chunk order) crosses the limit, run <= lim < run + w:
+        // an inclusive warp scan per 32 chunks, carried over
+        DF run{0.f, 0.f};
+        int pick = -1, last = -1;
+        DF base{0.f, 0.f};
+        for (int j0 = 0; j0 < NC; j0 += 32) {
+            const int j = j0 + lane;
+            float2 wv;
+            int lv;
+            if (j0 == 0) {
+                wv = use_q ? q0 : p0;
+                lv = use_q ? lq0 : lp0;
+            } else {
+                wv = j < NC ? __ldcg((use_q ? wq : wp) + j) : z2;
+                lv = j < NC ? __ldcg((use_q ? lq : lp) + j) : -1;
             }
+            last = max(last, __reduce_max_sync(0xFFFFFFFFu, lv));
+            DF incl{wv.x, wv.y};
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const DF v = df_shfl_up(incl, o);
+                if (lane >= o) incl = df_add(v, incl);
+            }
+            DF excl = df_shfl_up(incl, 1);
+            if (lane == 0) excl = DF{0.f, 0.f};
+            const DF lo = df_add(run, excl), hi = df_add(run, incl);
+            const unsigned hit = __ballot_sync(0xFFFFFFFFu, j < NC && !df_less(lim, lo) && df_less(lim, hi));
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                pick = j0 + src;
+                base = DF{__shfl_sync(0xFFFFFFFFu, lo.hi, src), __shfl_sync(0xFFFFFFFFu, lo.lo, src)};
+                break;
+            }
+            const DF tot = DF{__shfl_sync(0xFFFFFFFFu, incl.hi, 31), __shfl_sync(0xFFFFFFFFu, incl.lo, 31)};
+            run = df_add(run, tot);
         }
-    }
-    if (tid == 0) {
-        s_ch = pick;
-        s_last = last < 0 ? 0 : last;  // the limit past the total: the last positive weight
-        s_found = INT_MAX;
+        if (lane == 0) {
+            s_use = use_q ? 1 : 0;
+            s_lim = lim;
+            s_ch = pick;
+            s_base = base;
+            s_last = last < 0 ? 0 : last;  // the limit past the total: the last positive weight
+            s_found = INT_MAX;
+        }
     }
     __syncthreads();
     int tok = s_last;
     const int ch = s_ch;
+    const bool use_q = s_use != 0;
     if (ch >= 0) {
         const float *z = a.logits + ((size_t)b * (k + 1) + acc) * V;
         float x[SMP_PER], y[SMP_PER];
