@@ -17,7 +17,8 @@ the command the ncu summaries under profiles/ are taken with.
 
 --next times the calls beyond the chain step (hidden-row pool, graph replay against eager
 launches, tree verify, stop-aware and sampling acceptance) on the batched-branches workload
-and prints their own JSON line.
+and prints their own JSON line; --next --only sample runs just the sampling call (W + K plain
+launches), the command its launch list is taken with.
 
 --impl reference times the CPU oracle (the plain fp64 reference) on the same workload,
 one bounded sample per step, on this host's cores.
@@ -435,6 +436,47 @@ def run_ours(args):
 
 # ---- the oracle on the host cores ------------------------------------------------------------
 
+def _sample_call(B, k, V, g, dev, toks, n, a, npos, nxt, err):
+    """Sampling acceptance inputs on the device (logits 3·N(0,1); q = softmax of the logits plus
+    N(0,1) noise at temperature 1.3; drafts drawn from q; uniform random numbers) and the call."""
+    import torch
+    from greedy_speculative_decode_spec_gb300 import _binding as bnd
+    logits = 3.0 * torch.randn((B * (k + 1), V), generator=g, device=dev)
+    qd = torch.softmax((logits.view(B, k + 1, V)[:, :k] + torch.randn((B, k, V), generator=g, device=dev)) / 1.3,
+                       dim=-1).contiguous()
+    sdrafts = torch.multinomial(qd.view(B * k, V), 1, generator=g).view(B, k).to(torch.int32)
+    u_acc = torch.rand((B, k), generator=g, device=dev)
+    u_res = torch.rand(B, generator=g, device=dev)
+    spos = torch.randint(0, 8000, (B,), generator=g, device=dev, dtype=torch.int32)
+    sws = torch.zeros(bnd.spec_accept_sample_workspace(B, k, V), dtype=torch.uint8, device=dev)
+    return lambda: bnd.spec_accept_sample(sdrafts, logits, qd, spos, B, k, 1.0, u_acc, u_res, toks, n, a, npos, nxt,
+                                          err, ws=sws)
+
+
+def run_next_sample_only(args):
+    """--next --only sample: W + K plain launches of the sampling call at the batched-branches
+    shape (B=16, k=6, V=151936), the command its launch list is taken with."""
+    import torch
+    from greedy_speculative_decode_spec_gb300 import build as pkg_build
+    pkg_build.build()
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(2024)
+    B, k, V = 16, 6, 151936
+    i32 = dict(dtype=torch.int32, device=dev)
+    toks = torch.empty((B, k + 1), **i32)
+    n, a, npos, nxt = (torch.empty(B, **i32) for _ in range(4))
+    err = torch.zeros(1, **i32)
+    call = _sample_call(B, k, V, g, dev, toks, n, a, npos, nxt, err)
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, "device error in the sampling call"
+    print(json.dumps({"mode": "next_rows", "only": "sample", "calls": args.warmup + args.steps,
+                      "accepted": a.cpu().tolist()}), flush=True)
+
+
 def run_next(args):
     """The calls beyond the chain step, on the batched-branches workload (B=16, k=6, 32/8
     heads, d=128, bf16 pages of 16; V=151936, H=4096), each timed alone from a CUDA graph with
@@ -582,16 +624,8 @@ def run_next(args):
     # ---- f4: speculative sampling acceptance, fp32 logits [R][V] and draft probabilities [B][k][V] ----
     del w, kept, step
     torch.cuda.empty_cache()
-    logits = 3.0 * torch.randn((R, V), generator=g, device=dev)
-    qd = torch.softmax((logits.view(B, k + 1, V)[:, :k] + torch.randn((B, k, V), generator=g, device=dev)) / 1.3,
-                       dim=-1).contiguous()
-    sdrafts = torch.multinomial(qd.view(B * k, V), 1, generator=g).view(B, k).to(torch.int32)
-    u_acc = torch.rand((B, k), generator=g, device=dev)
-    u_res = torch.rand(B, generator=g, device=dev)
-    spos = torch.randint(0, 8000, (B,), generator=g, device=dev, dtype=torch.int32)
-    sws = torch.zeros(bnd.spec_accept_sample_workspace(B, k, V), dtype=torch.uint8, device=dev)
-    us = timed(lambda: bnd.spec_accept_sample(sdrafts, logits, qd, spos, B, k, 1.0, u_acc, u_res, toks, n, a, npos,
-                                              nxt, err, ws=sws), steps)
+    call = _sample_call(B, k, V, g, dev, toks, n, a, npos, nxt, err)
+    us = timed(call, steps)
     torch.cuda.synchronize()
     # bytes: every verify row's logits once (all rows' softmax statistics are computed) and
     # the q row of each rejected draft; "needed_bytes": only the rows up to the decisive one
@@ -691,15 +725,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=3, choices=[0, 1, 2, 3, 4])
-    ap.add_argument("--only", choices=["attn", "lmhead"], default=None)
+    ap.add_argument("--only", choices=["attn", "lmhead", "sample"], default=None)
     ap.add_argument("--no-all", dest="all", action="store_false")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--next", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.only == "sample" and not args.next:
+        ap.error("--only sample goes with --next")
     if args.next:
-        run_next(args)
+        run_next_sample_only(args) if args.only == "sample" else run_next(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
