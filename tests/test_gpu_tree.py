@@ -213,3 +213,23 @@ def test_kv_compaction_matches_oracle(name):
     assert orc.kv_compact(okv, vi.pos.numpy(), path, acc, c.B, c.k) == 0
     assert_pools_equal(gkv, okv)
     assert acc.sum() > 0
+
+
+@pytest.mark.parametrize("name", ["batched_branches_shared_pool", "long_context_fp8"])
+def test_tree_attention_full_size(name):
+    """The full workloads with random trees over their verify slots, in the launch
+    configuration the benchmark times: every output against the oracle; chain masks give
+    the chain call bit for bit."""
+    vi = verify_inputs(WORKLOADS[name])
+    c = vi.cfg
+    gkv, okv = _appended(vi)
+    masks = masks_from_parents(random_parents(c.B, c.k, np.random.default_rng(c.seed)))
+    out, e = _tree_attention(gkv, vi, masks)
+    assert e == 0
+    ref, oe = orc.verify_attn_tree(okv, vi.pos.numpy(), c.B, c.k, c.Hq, bits(vi.q), 1.0 / math.sqrt(c.d), masks)
+    assert oe == 0
+    assert_attn_close(out, ref, "tree attention, full size")
+    tree_out, e1 = _tree_attention(gkv, vi, orc.chain_masks(c.B, c.k))
+    chain_out, e2 = gpu_attention(gkv, vi.pos.cuda(), c.B, c.k, c.Hq, vi.q.cuda(), vi.max_pos)
+    assert e1 == 0 and e2 == 0
+    assert torch.equal(tree_out.view(torch.int16), chain_out.view(torch.int16))
