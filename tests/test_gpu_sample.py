@@ -80,9 +80,9 @@ def _near_tie(b, k, T, logits, q, drafts, u_acc, u_res, a_gpu, a_orc):
 
 
 # vocabulary chunks of 8192: several with a ragged tail (16-byte vector loads when V % 4 == 0,
-# scalar otherwise), one, and the full 151936-entry vocabulary
+# scalar otherwise), one, and the full 151936-entry vocabulary (last: the benchmark's shape)
 @pytest.mark.parametrize("B,k,V,T", [(6, 4, 50021, 0.8), (5, 7, 4099, 1.3), (3, 0, 1000, 1.0), (2, 15, 300, 0.5),
-                                     (4, 3, 20000, 1.0), (2, 6, 151936, 1.0)])
+                                     (4, 3, 20000, 1.0), (2, 6, 151936, 1.0), (16, 6, 151936, 1.0)])
 def test_sample_accept_matches_oracle(B, k, V, T):
     logits, q, drafts, u_acc, u_res, pos = _inputs(B, k, V, T, seed=V + k)
     g_toks, g_n, g_a, g_pos, g_next, err = _gpu(logits, q, drafts, u_acc, u_res, pos, B, k, T)
