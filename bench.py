@@ -232,6 +232,36 @@ def _time_region(fn, steps, flush, stream):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def _time_in_graph(fn, steps, flush):
+    """Device time of one call of fn: CUDA events recorded inside its graph, on the launching
+    stream, right before and after the call's kernels (so the graph launch itself is not
+    counted); the L2 flushed before every replay. Falls back to events around the replay where
+    this PyTorch cannot record events as graph nodes."""
+    import torch
+    try:
+        a = torch.cuda.Event(enable_timing=True, external=True)
+        b = torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:
+        g = _graph_of(fn)
+        return _time_region(g.replay, steps, flush, torch.cuda.current_stream())
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush()
+        g.replay()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    del g
+    return ts
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -315,11 +345,10 @@ def run_ours(args):
             dist.barrier()
         del graph
         log(f"workload {cid}: per-kernel timing")
-        # per-call times of the two bandwidth calls (graph replays: same stream, same flush)
-        g_attn, g_head = _graph_of(attn), _graph_of(head)
-        t_attn = _time_region(g_attn.replay, steps, flush, stream)
-        t_head = _time_region(g_head.replay, steps, flush, stream)
-        del g_attn, g_head
+        # per-call times of the two bandwidth calls (events inside each call's graph, same
+        # stream, same flush)
+        t_attn = _time_in_graph(attn, steps, flush)
+        t_head = _time_in_graph(head, steps, flush)
         # the same step followed by the next draft step's MTP input
         g_mtp = _graph_of(lambda: one(with_mtp=True))
         for _ in range(warmup):
@@ -507,11 +536,9 @@ def run_next(args):
         def body():
             for _ in range(reps):
                 fn()
-        g = _graph_of(body)
         for _ in range(3):
-            g.replay()
-        ts = _time_region(g.replay, steps, flush, stream)
-        del g
+            body()
+        ts = _time_in_graph(body, steps, flush)
         return statistics.median(ts) * 1e3 / reps  # us per call
 
     def small(e, fn):
@@ -636,7 +663,8 @@ def run_next(args):
     rows["accept_sample"]["accepted"] = acc
     assert int(err.item()) == 0, "device error in the next-row calls"
     line = {"mode": "next_rows", "workload": c.name, "steps": steps, "hbm_peak_gbs": hbm_peak, "peak": peak_kind,
-            "timing": "CUDA-event median of graph replays, L2 flushed before each; eager: plain launches",
+            "timing": "CUDA-event median over graph replays (events recorded inside the graph around the call), "
+                      "L2 flushed before each; eager: plain launches, events around them",
             "rows": rows}
     print(json.dumps(line), flush=True)
 
