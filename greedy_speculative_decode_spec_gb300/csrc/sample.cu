@@ -17,16 +17,18 @@
 //     the first rejection);
 //  2. the walk and the draw weights, one CTA per (branch, chunk): the branch's rows' maxima
 //     M (over chunks) and denominators S = sum_c s_c * 2^((m_c - M) c) (the factor in fp32,
-//     the sum in fp64, in chunk order), every draft's decision at once (the walk stops at the first draft not kept),
-//     then the chunk's sums of the draw weights of the decisive row (the residual and p);
+//     the sum a double-float, in a fixed order), every draft's decision at once (the walk
+//     stops at the first draft not kept), then the chunk's sums of the draw weights of the
+//     decisive row (the residual and p);
 //  3. the draw, by the branch's last CTA of step 2 to finish: the chunk whose running sum
 //     crosses u * total (in chunk order), then the index inside it (each thread owns a
 //     contiguous run of SMP_PER entries; a scan of the runs' sums; the crossing run is
 //     walked entry by entry).
 // Probabilities are fp32 (exp2f); every sum is kept as a double-float (an unevaluated pair of
 // fp32 values, about 48 significant bits: Knuth's TwoSum and an fma-based TwoProduct give the
-// exact rounding error of each addition and product), from compensated fp32 partial sums, in
-// a fixed order: GB300's fp64 pipe is narrow, so per-thread fp64 would bound these kernels.
+// exact rounding error of each addition and product), from compensated or pairwise fp32
+// partial sums, in a fixed order: GB300's fp64 pipe is narrow, so per-thread fp64 would bound
+// these kernels.
 // A decision can differ from an exact evaluation only where its test value lies within that
 // rounding (about 2^-24 relative, from the fp32 probabilities) of a boundary.
 #include <climits>
